@@ -1,0 +1,128 @@
+"""Double-precision CPU oracle for stacked LSTM / GRU / tanh-RNN (fwd + BPTT + dW).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / reference leg may import this package.  The
+product library never loads it and shares no code with it.
+
+The arithmetic lives in ``rnn_ref.cpp`` (plain C++17 loops in double,
+OpenMP over batch rows / gate rows).  This module compiles it with the host
+compiler and wraps its two entry points with ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rnn_ref.cpp")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_OUT_DIR, "librnn_ref.so")
+_lib = None
+
+GATES = {0: 4, 1: 3, 2: 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/_build/librnn_ref.so (host compiler, -O2, OpenMP)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB) or
+             os.path.getmtime(_LIB) < max(os.path.getmtime(_SRC),
+                                          os.path.getmtime(os.path.join(_HERE, "rnn_ref.h"))))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-std=c++17", "-O2", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ci = ctypes.c_int
+        lib.rnn_ref_fwd.argtypes = [ci] * 6 + [dp] * 7
+        lib.rnn_ref_fwd.restype = ci
+        lib.rnn_ref_bwd.argtypes = [ci] * 6 + [dp] * 11
+        lib.rnn_ref_bwd.restype = ci
+        lib.rnn_ref_threads.restype = ci
+        _lib = lib
+    return _lib
+
+
+def threads() -> int:
+    return int(_load().rnn_ref_threads())
+
+
+def _p(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _c(a, shape=None):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    if shape is not None:
+        assert a.shape == tuple(shape), (a.shape, shape)
+    return a
+
+
+def weight_count(cell, L, I, H):
+    G = GATES[cell]
+    return sum(G * H * ((I if l == 0 else H) + H) + 2 * G * H for l in range(L))
+
+
+def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None):
+    """Forward pass. Returns (y[T][B][H], hT[L][B][H], cT[L][B][H] or None)."""
+    x = _c(x, (T, B, I))
+    w = _c(w, (weight_count(cell, L, I, H),))
+    h0 = _c(h0, (L, B, H))
+    c0 = _c(c0, (L, B, H)) if cell == 0 else None
+    y = np.zeros((T, B, H))
+    hT = np.zeros((L, B, H))
+    cT = np.zeros((L, B, H)) if cell == 0 else None
+    rc = _load().rnn_ref_fwd(cell, L, T, B, I, H, _p(x), _p(h0), _p(c0), _p(w), _p(y), _p(hT), _p(cT))
+    if rc != 0:
+        raise ValueError(f"rnn_ref_fwd rejected its arguments ({rc})")
+    return y, hT, cT
+
+
+def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None):
+    """Backward pass. Returns (dx[T][B][I], dh0[L][B][H], dc0 or None, dw like w)."""
+    x = _c(x, (T, B, I))
+    w = _c(w, (weight_count(cell, L, I, H),))
+    dy = _c(dy, (T, B, H))
+    h0 = _c(h0, (L, B, H))
+    c0 = _c(c0, (L, B, H)) if cell == 0 else None
+    dhT = _c(dhT, (L, B, H))
+    dcT = _c(dcT, (L, B, H)) if cell == 0 else None
+    dx = np.zeros((T, B, I))
+    dh0 = np.zeros((L, B, H))
+    dc0 = np.zeros((L, B, H)) if cell == 0 else None
+    dw = np.zeros_like(w)
+    rc = _load().rnn_ref_bwd(cell, L, T, B, I, H, _p(x), _p(h0), _p(c0), _p(w), _p(dy), _p(dhT),
+                             _p(dcT), _p(dx), _p(dh0), _p(dc0), _p(dw))
+    if rc != 0:
+        raise ValueError(f"rnn_ref_bwd rejected its arguments ({rc})")
+    return dx, dh0, dc0, dw
+
+
+def split_weights(cell, L, I, H, w):
+    """Views (W_x, W_h, b_x, b_h) per layer of a flat user-layout weight vector."""
+    G = GATES[cell]
+    out, o = [], 0
+    for l in range(L):
+        In = I if l == 0 else H
+        wx = w[o:o + G * H * In].reshape(G * H, In); o += G * H * In
+        wh = w[o:o + G * H * H].reshape(G * H, H); o += G * H * H
+        bx = w[o:o + G * H]; o += G * H
+        bh = w[o:o + G * H]; o += G * H
+        out.append((wx, wh, bx, bh))
+    return out

@@ -1,0 +1,47 @@
+/*
+ * rnn_ref.h -- double-precision CPU oracle for stacked LSTM / GRU / tanh-RNN
+ * forward and backward-through-time passes.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this code; only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no source with the CUDA path.
+ *
+ * What it computes follows the cells named by "Optimizing Performance of
+ * Recurrent Neural Networks on GPUs" (review page, section "제안 방법":
+ * LSTM with four gate matrices, GRU with three, simple RNN with one), written
+ * out as their textbook definitions because the pages print no equations.
+ *
+ * Layouts (all row-major, time-major, host memory, double):
+ *   x[T][B][I], y[T][B][H], h0/c0/hT/cT/dh0/dc0[L][B][H], dy[T][B][H]
+ *   w: per layer l (in order): W_x[G*H][I_l], W_h[G*H][H], b_x[G*H], b_h[G*H]
+ *      with I_0 = I, I_l = H for l >= 1, gate blocks LSTM (i,f,g,o),
+ *      GRU (r,z,n), RNN (single block).
+ *   dw: same layout as w.
+ * Nullable: h0, c0 (zero state), hT, cT (not written), dhT, dcT (zero),
+ *   dx, dh0, dc0 (not written).  c-arguments are ignored for GRU and RNN.
+ * Returns 0 on success, -1 on invalid arguments.
+ */
+#ifndef RNN_REF_H
+#define RNN_REF_H
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { RNN_REF_LSTM = 0, RNN_REF_GRU = 1, RNN_REF_TANH = 2 };
+
+int rnn_ref_fwd(int cell, int L, int T, int B, int I, int H,
+                const double* x, const double* h0, const double* c0, const double* w,
+                double* y, double* hT, double* cT);
+
+int rnn_ref_bwd(int cell, int L, int T, int B, int I, int H,
+                const double* x, const double* h0, const double* c0, const double* w,
+                const double* dy, const double* dhT, const double* dcT,
+                double* dx, double* dh0, double* dc0, double* dw);
+
+/* number of OpenMP threads the oracle runs on */
+int rnn_ref_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

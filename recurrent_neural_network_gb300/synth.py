@@ -1,0 +1,189 @@
+"""Seeded synthetic inputs for the stacked-RNN workloads.
+
+This module only draws numbers. It holds none of the recurrent arithmetic:
+both the CUDA path and the double-precision oracle receive the arrays it
+produces, so they see identical inputs.
+
+Generator: counter-based splitmix64.  Element ``i`` of tensor ``tid`` under
+seed ``s`` is the (i+1)-th output of a splitmix64 stream keyed by
+``mix(mix(s) ^ tid)``.  Any slice (a prefix of timesteps, one batch column)
+therefore regenerates identically without drawing the rest.  Uniforms are the
+top 53 bits scaled to [0, 1); normals use the Box-Muller transform on the
+uniforms of counters ``2i`` and ``2i+1``.
+
+Workload recipes follow the sizes and distributions stated for the five
+benchmark cases (one tiny fp32 LSTM, a 4-layer H=512 LSTM, a B=4 H=1024
+inference LSTM, a 4-layer H=4096 B=256 LSTM and an 8-layer H=1024 GRU).  The
+pages behind the method ("Optimizing Performance of Recurrent Neural Networks
+on GPUs", review page, section "주요 결과") measure only throughput on
+unnamed network sizes; these recipes stand in for those networks.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+CELL_LSTM, CELL_GRU, CELL_TANH = 0, 1, 2
+CELL_NAMES = {CELL_LSTM: "lstm", CELL_GRU: "gru", CELL_TANH: "tanh"}
+GATES = {CELL_LSTM: 4, CELL_GRU: 3, CELL_TANH: 1}
+MODE_FP32, MODE_BF16 = 0, 1
+
+# tensor ids of the counter streams
+TID_X, TID_H0, TID_C0, TID_DY, TID_DHT, TID_DCT = 1, 3, 4, 5, 6, 7
+
+
+def _mix(z):
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def _key(seed: int, tid: int) -> np.uint64:
+    with np.errstate(over="ignore"):
+        k = _mix(np.uint64(seed) + _GAMMA)
+        return _mix((k ^ np.uint64(tid)) + _GAMMA)
+
+
+def uniform01(seed: int, tid: int, start: int, count: int) -> np.ndarray:
+    """U[0,1) doubles for counters start .. start+count-1."""
+    key = _key(seed, tid)
+    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = _mix(key + idx * _GAMMA)
+    return (z >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+
+
+def uniform(seed, tid, shape, lo, hi, start=0):
+    n = int(np.prod(shape))
+    return (lo + (hi - lo) * uniform01(seed, tid, start, n)).reshape(shape)
+
+
+def normal(seed, tid, shape, std=1.0, start=0):
+    n = int(np.prod(shape))
+    u = uniform01(seed, tid, 2 * start, 2 * n)
+    u1, u2 = u[0::2], u[1::2]
+    r = np.sqrt(-2.0 * np.log1p(-u1))
+    return (std * r * np.cos(2.0 * math.pi * u2)).reshape(shape)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: shapes, storage mode and input distributions."""
+    name: str
+    cell: int
+    layers: int
+    T: int
+    B: int
+    input: int
+    hidden: int
+    mode: int
+    x_dist: str = "normal"        # "normal" N(0,1) or "uniform" U(-1,1)
+    forget_bias: float = 0.0      # added to b_x of the LSTM forget gate
+    state_std: float = 0.0        # h0 (and c0) ~ N(0, state_std^2); 0 means zeros
+    training: bool = True
+    seed: int = 0
+
+    @property
+    def G(self):
+        return GATES[self.cell]
+
+    def in_size(self, l):
+        return self.input if l == 0 else self.hidden
+
+    def layer_weight_count(self, l):
+        G, H = self.G, self.hidden
+        return G * H * self.in_size(l) + G * H * H + 2 * G * H
+
+    def weight_count(self):
+        return sum(self.layer_weight_count(l) for l in range(self.layers))
+
+    def replace(self, **kw):
+        return dataclasses.replace(self, **kw)
+
+    def gemm_flops(self):
+        """Algorithmic GEMM flops (2*M*N*K) of forward, backward-data and weight-gradient passes."""
+        G, H, T, B = self.G, self.hidden, self.T, self.B
+        fwd = sum(2.0 * T * B * G * H * (self.in_size(l) + H) for l in range(self.layers))
+        return {"fwd": fwd, "bwd_data": fwd, "bwd_weights": fwd}
+
+
+# The five benchmark workloads (index 0 .. 4).
+WORKLOADS = [
+    Workload("lstm_fp32_L1_T8_B4_H32", CELL_LSTM, 1, 8, 4, 32, 32, MODE_FP32,
+             x_dist="uniform", forget_bias=1.0),
+    Workload("lstm_bf16_L4_T100_B64_H512", CELL_LSTM, 4, 100, 64, 512, 512, MODE_BF16,
+             forget_bias=1.0, state_std=0.1),
+    Workload("lstm_bf16_L1_T1000_B4_H1024_infer", CELL_LSTM, 1, 1000, 4, 1024, 1024, MODE_BF16,
+             forget_bias=1.0, training=False),
+    Workload("lstm_bf16_L4_T50_B256_H4096", CELL_LSTM, 4, 50, 256, 4096, 4096, MODE_BF16,
+             forget_bias=1.0),
+    Workload("gru_bf16_L8_T200_B32_H1024", CELL_GRU, 8, 200, 32, 1024, 1024, MODE_BF16),
+]
+
+
+def layer_weights(wl: Workload, l: int, dtype=np.float64):
+    """User-layout weights of layer ``l``: (W_x[G*H][I_l], W_h[G*H][H], b_x[G*H], b_h[G*H]).
+
+    W_x and W_h ~ U(-1/sqrt(H), 1/sqrt(H)); biases are zero except the LSTM
+    forget gate (gate block 1 of b_x), which gets ``forget_bias``.
+    """
+    G, H, I = wl.G, wl.hidden, wl.in_size(l)
+    a = 1.0 / math.sqrt(H)
+    wx = uniform(wl.seed, 100 + 10 * l + 0, (G * H, I), -a, a).astype(dtype)
+    wh = uniform(wl.seed, 100 + 10 * l + 1, (G * H, H), -a, a).astype(dtype)
+    bx = np.zeros(G * H, dtype=dtype)
+    bh = np.zeros(G * H, dtype=dtype)
+    if wl.cell == CELL_LSTM and wl.forget_bias:
+        bx[H:2 * H] = wl.forget_bias
+    return wx, wh, bx, bh
+
+
+def flat_weights(wl: Workload, dtype=np.float64) -> np.ndarray:
+    """All layers' user-layout weights concatenated: per layer W_x, W_h, b_x, b_h."""
+    parts = []
+    for l in range(wl.layers):
+        parts.extend(p.ravel() for p in layer_weights(wl, l, dtype))
+    return np.concatenate(parts)
+
+
+def make_x(wl: Workload, T=None, dtype=np.float64):
+    T = wl.T if T is None else T
+    shape = (T, wl.B, wl.input)
+    if wl.x_dist == "uniform":
+        return uniform(wl.seed, TID_X, shape, -1.0, 1.0).astype(dtype)
+    return normal(wl.seed, TID_X, shape).astype(dtype)
+
+
+def make_state(wl: Workload, which: str, dtype=np.float64):
+    """h0 or c0, shape [L][B][H]."""
+    shape = (wl.layers, wl.B, wl.hidden)
+    if wl.state_std == 0.0:
+        return np.zeros(shape, dtype=dtype)
+    tid = TID_H0 if which == "h0" else TID_C0
+    return normal(wl.seed, tid, shape, std=wl.state_std).astype(dtype)
+
+
+def make_dy(wl: Workload, T=None, dtype=np.float64):
+    T = wl.T if T is None else T
+    return normal(wl.seed, TID_DY, (T, wl.B, wl.hidden)).astype(dtype)
+
+
+def make_dstate(wl: Workload, which: str, dtype=np.float64):
+    """dhT or dcT [L][B][H] ~ N(0,1); the benchmark workloads pass none (zero)."""
+    tid = TID_DHT if which == "dhT" else TID_DCT
+    return normal(wl.seed, tid, (wl.layers, wl.B, wl.hidden)).astype(dtype)
+
+
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round doubles to the nearest bfloat16 (ties to even), returned as float64."""
+    f = np.asarray(a, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    u = (u + np.uint64(0x7FFF) + lsb) & np.uint64(0xFFFF0000)
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
