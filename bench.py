@@ -1,0 +1,296 @@
+"""Benchmark of the stacked-RNN hot path on GB300.
+
+One step = one full pass of the path over one batch of seeded synthetic
+input: for a training workload the forward pass (input projection, fused
+recurrent steps, layer wavefront), the backward pass through time (fused
+reverse steps, data-gradient products) and the weight-gradient products; for
+an inference workload the forward pass.  Default workload: the 4-layer
+H=4096 B=256 T=50 bf16 LSTM training step.
+
+    python bench.py [--gpus N --steps K --warmup W] [--config IDX] [--impl reference]
+
+Prints one JSON line (rank 0).  Metric: algorithmic GEMM TFLOP/s of the step
+(2*M*N*K over the input, recurrent, data-gradient and weight-gradient
+products), with timesteps/s beside it.  With N > 1 (torchrun) every rank runs
+an independent replica of the workload (no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "LSTM fwd+bwd TFLOPS & timesteps/s on 1 GB300; % of bf16 tensor/SMEM roofline"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d.get("hbm_gbs", 6800.0), bf16_tflops=d.get("bf16_tflops", 1900.0),
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", 1700.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def step_flops(wl):
+    f = wl.gemm_flops()
+    return f["fwd"] + (f["bwd_data"] + f["bwd_weights"] if wl.training else 0.0)
+
+
+def class_flops(wl):
+    """Algorithmic flops per step of each kernel class (for the roofline of the dominant one)."""
+    G, H, T, B, L = wl.G, wl.hidden, wl.T, wl.B, wl.layers
+    inp = sum(2.0 * T * B * G * H * wl.in_size(l) for l in range(L))
+    rec = 2.0 * T * B * G * H * H * L
+    out = {"input_proj_gemm": inp, "fwd_step": rec}
+    if wl.training:
+        out.update({"bwd_step": rec, "dx_gemm": inp, "dw_gemm": inp + rec})
+    return out
+
+
+def time_oracle_sample(wl, budget_s=20.0):
+    """The double-precision oracle on a bounded sample of the workload (batch
+    columns and a prefix of timesteps), as TFLOP/s of that sample."""
+    import oracle
+    from recurrent_neural_network_gb300 import runner
+    B1 = min(wl.B, 2)
+    T1 = min(wl.T, 4 if wl.hidden >= 2048 else 16)
+    sw = wl.replace(B=B1, T=T1)
+    hi = runner.HostInputs(sw)
+    t0 = time.perf_counter()
+    if wl.training:
+        oracle.bwd(sw.cell, sw.layers, sw.T, sw.B, sw.input, sw.hidden, hi.x, hi.w, hi.dy, h0=hi.h0, c0=hi.c0)
+    else:
+        oracle.fwd(sw.cell, sw.layers, sw.T, sw.B, sw.input, sw.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0)
+    dt = time.perf_counter() - t0
+    fl = step_flops(sw)
+    return dict(value=fl / dt / 1e12, unit="TFLOP/s", cores=oracle.threads(), kind="oracle",
+                sample=f"B={B1} of {wl.B} columns, T={T1} of {wl.T} steps, all {wl.layers} layers "
+                       f"({'fwd+BPTT+dW' if wl.training else 'fwd'}), {dt:.2f} s"), dt
+
+
+def run_reference(args, wl, rank):
+    """--impl reference: the oracle timed on host cores, per step one bounded sample."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    times = []
+    res = None
+    for i in range(args.warmup + args.steps):
+        res, dt = time_oracle_sample(wl)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1e3 * statistics.mean(times)
+    line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "sample": res["sample"]},
+            "cpu_baseline": res, "e2e": {"value": res["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                          "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--chunk", type=int, default=0)
+    args = ap.parse_args()
+
+    from recurrent_neural_network_gb300 import synth
+    wl = synth.WORKLOADS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        return
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from recurrent_neural_network_gb300 import build, rnn, runner
+    build.build()
+    dev = torch.device("cuda", local)
+    flags = args.flags | rnn.FLAG_PROFILE
+    R = runner.Runner(wl, device=dev, flags=flags, chunk=args.chunk)
+    sdt = R.dt
+    R.x = synth.device_tensor(wl, "x", dev, sdt)
+    R.w_user = synth.device_tensor(wl, "w", dev, sdt)
+    R.h0 = synth.device_tensor(wl, "h0", dev, sdt)
+    R.c0 = synth.device_tensor(wl, "c0", dev, torch.float32) if wl.cell == synth.CELL_LSTM else None
+    R.dy = synth.device_tensor(wl, "dy", dev, sdt) if wl.training else None
+    R.pack()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        R.step()
+    assert R.status() == 0
+    R.r.profile(reset=True)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    barrier()
+    clocks.start()
+    n_launch0 = rnn.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        R.step()
+    ev1.record(stream)
+    barrier()
+    launches = rnn.launch_count() - n_launch0
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clk = clocks.stop()
+    prof = R.r.profile(reset=True)
+    st = R.status()
+    assert st == 0, f"device status {st}"
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    fl = step_flops(wl)
+    tflops = world * fl / (ms * 1e-3) / 1e12
+    pk = peaks()
+
+    # roofline of the dominant kernel class
+    cf = class_flops(wl)
+    dom = max(prof.items(), key=lambda kv: kv[1][1]) if prof else None
+    roof = None
+    if dom and dom[0] in cf:
+        name, (n, tot) = dom
+        per_launch_flops = cf[name] * args.steps / max(n, 1)
+        achieved = cf[name] * args.steps / (tot * 1e-3) / 1e12
+        roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
+                "launches": n // args.steps, "flops_per_launch": per_launch_flops,
+                "ms_per_launch": tot / max(n, 1), "peak_source": pk["source"] + " sustained"}
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    hx = torch.empty(R.x.shape, dtype=sdt, pin_memory=True)
+    hx.copy_(R.x)
+    hdy = None
+    if wl.training:
+        hdy = torch.empty(R.dy.shape, dtype=sdt, pin_memory=True)
+        hdy.copy_(R.dy)
+    hout = torch.empty(R.hT.shape, dtype=R.hT.dtype, pin_memory=True)
+    h2d = hx.numel() * hx.element_size() + (hdy.numel() * hdy.element_size() if hdy is not None else 0)
+    d2h = hout.numel() * hout.element_size()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        R.x.copy_(hx, non_blocking=True)
+        if hdy is not None:
+            R.dy.copy_(hdy, non_blocking=True)
+        R.step()
+        hout.copy_(R.hT, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    R.r.profile(reset=True)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if wl.mode == 1 else "f32", "data": "synthetic",
+        "timesteps_per_s": world * wl.T / (ms * 1e-3),
+        "config": {"workload": wl.name, "cell": synth.CELL_NAMES[wl.cell], "layers": wl.layers, "T": wl.T,
+                   "B": wl.B, "input": wl.input, "hidden": wl.hidden, "training": wl.training,
+                   "flops_per_step": fl, "plan": R.r.describe(),
+                   "l2": "inputs larger than L2 (weights, reserve and activations exceed 129 MB)"},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": {"value": world * fl / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "kernels": {k: {"launches": v[0] // args.steps, "ms_per_step": v[1] / args.steps} for k, v in prof.items()},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"], _ = time_oracle_sample(wl)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

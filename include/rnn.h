@@ -1,0 +1,188 @@
+/*
+ * rnn.h -- C-ABI of librnn: stacked LSTM / GRU / tanh-RNN forward and
+ * backward-through-time on one NVIDIA GB300 (sm_103a).
+ *
+ * The method follows "Optimizing Performance of Recurrent Neural Networks on
+ * GPUs" (Appleyard, Kocisky, Blunsom; review page, section "제안 방법"):
+ *   - the G gate matrices of a cell are stacked into one matrix so that each
+ *     product is one large GEMM (LSTM G=4, GRU G=3, simple RNN G=1);
+ *   - the input projection of all timesteps is independent of the recurrence
+ *     and runs as one GEMM ahead of it;
+ *   - forward and backward passes of consecutive layers overlap (a wavefront:
+ *     layer l+1 runs behind layer l);
+ *   - the weight update is one GEMM over all timesteps, the bias update a
+ *     cheap reduction.
+ * From "Persistent RNNs: Stashing Recurrent Weights On-Chip" (Diamos et al.,
+ * citing snippets on its page): a small-batch recurrence keeps its recurrent
+ * weights on-chip across timesteps and runs every timestep in one launch.
+ * The pages print no equations, layouts or API; the cells are the textbook
+ * ones (see each call) and the interface below is this library's own.
+ *
+ * Conventions for every call
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the
+ *     library never allocates device memory and keeps no pointer after a call
+ *     returns.  The handle is a host object holding the shape and the
+ *     library's launch plan.
+ *   - Calls are asynchronous on `stream`; they only enqueue work.  Errors that
+ *     the host can see (arguments, launch failures) are returned at once.
+ *     A bounded device-side wait that gave up is recorded in the workspace
+ *     and reported by rnn_sync_status().
+ *   - Element types: in RNN_MODE_BF16, x, y, h0, hT, dy, dhT, dx, dh0 and the
+ *     user weights are bfloat16; in RNN_MODE_FP32 they are float.  Cell
+ *     states c0, cT, dcT, dc0 and the weight gradient dw are always float.
+ *   - Layouts are row-major and time-major:
+ *       x[T][B][input], y/dy[T][B][hidden], dx[T][B][input],
+ *       h0/c0/hT/cT/dhT/dcT/dh0/dc0[layers][B][hidden].
+ *   - User weight layout (same element order as torch.nn.LSTM/GRU/RNN
+ *     parameters), per layer l in order:
+ *       W_x[G*hidden][I_l], W_h[G*hidden][hidden], b_x[G*hidden], b_h[G*hidden]
+ *     with I_0 = input, I_l = hidden for l >= 1, and gate blocks ordered
+ *     LSTM (i, f, g, o), GRU (r, z, n), RNN (one block).  dw has the same
+ *     layout in float.
+ *   - Pointers must be 16-byte aligned.  Shapes: in RNN_MODE_BF16 hidden must
+ *     be a multiple of 64 and input of 8; in RNN_MODE_FP32 hidden a multiple
+ *     of 32 and input of 4 (RNN_ERR_UNSUPPORTED otherwise).
+ *   - Return value: RNN_OK (0) or a negative RNN_ERR_* code; rnn_strerror()
+ *     names it.  No C++ exception crosses this interface.
+ */
+#ifndef RNN_H
+#define RNN_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define RNN_API __attribute__((visibility("default")))
+#else
+#define RNN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_TANH = 2 } rnn_cell_t;
+typedef enum { RNN_MODE_FP32 = 0, RNN_MODE_BF16 = 1 } rnn_mode_t;
+
+enum {
+  RNN_OK = 0,
+  RNN_ERR_INVALID_ARG = -1, /* null handle/pointer, bad size, misaligned buffer */
+  RNN_ERR_UNSUPPORTED = -2, /* shape or mode this build does not handle */
+  RNN_ERR_LAUNCH = -3,      /* kernel could not be launched (e.g. co-residency) */
+  RNN_ERR_CUDA = -4,        /* a CUDA runtime call failed */
+  RNN_ERR_TIMEOUT = -5,     /* a bounded device-side wait gave up */
+  RNN_ERR_NOMEM = -6        /* host allocation for the handle failed */
+};
+
+/* rnn_desc_t.flags */
+#define RNN_FLAG_NO_WAVEFRONT 0x1u      /* run layers one after another (no overlap) */
+#define RNN_FLAG_FORCE_STREAMING 0x2u   /* never use the persistent recurrence */
+#define RNN_FLAG_FORCE_PERSISTENT 0x4u  /* use the persistent recurrence or fail */
+#define RNN_FLAG_PROFILE 0x8u           /* record per-kernel CUDA-event timings */
+
+typedef struct {
+  int cell;             /* rnn_cell_t */
+  int layers;           /* L >= 1 */
+  int T;                /* timesteps >= 1 */
+  int B;                /* batch >= 1 */
+  int input;            /* input size of layer 0 */
+  int hidden;           /* hidden size H */
+  int mode;             /* rnn_mode_t */
+  unsigned flags;       /* RNN_FLAG_* */
+  long long timeout_ns; /* bound on every device-side wait; <= 0 selects 2 s */
+  int chunk;            /* wavefront chunk in timesteps; <= 0 selects automatically */
+} rnn_desc_t;
+
+typedef struct rnn_s* rnn_handle_t;
+
+/* Create a handle for one shape.  Validates the descriptor
+ * (RNN_ERR_INVALID_ARG / RNN_ERR_UNSUPPORTED) and chooses the launch plan
+ * (persistent vs streaming recurrence, wavefront chunk, GEMM tiles) for the
+ * current device.  *out receives the handle (host memory, freed by
+ * rnn_destroy). */
+RNN_API int rnn_create(const rnn_desc_t* desc, rnn_handle_t* out);
+RNN_API int rnn_destroy(rnn_handle_t h);
+
+/* Byte sizes of the caller-owned buffers: the user weight vector, the packed
+ * weight buffer, the reserve (training state kept from rnn_fwd for the
+ * backward calls) and the workspace (scratch for any call).  Any pointer may
+ * be NULL. */
+RNN_API int rnn_get_sizes(rnn_handle_t h, size_t* user_weight_bytes, size_t* packed_weight_bytes,
+                  size_t* reserve_bytes, size_t* workspace_bytes);
+
+/* Weight pack: converts user-layout weights into the packed layout every
+ * kernel reads (gate rows interleaved in blocks so that one output tile holds
+ * all gates of the same hidden units; biases folded and widened to float).
+ * Run once per weight update.  w_user: user layout in the mode's type. */
+RNN_API int rnn_pack_weights(rnn_handle_t h, const void* w_user, void* w_packed, cudaStream_t stream);
+
+/* Forward pass over all layers and timesteps.  Per layer l and step t:
+ *   LSTM: a = W_x in_t + b_x + W_h h_{t-1} + b_h; i,f,o = sigmoid, g = tanh;
+ *         c_t = f*c_{t-1} + i*g;  h_t = o*tanh(c_t)
+ *   GRU:  r,z = sigmoid(W_x in + b_x + W_h h + b_h) (their gate blocks);
+ *         n = tanh(W_xn in + b_xn + r*(W_hn h_{t-1} + b_hn));
+ *         h_t = (1-z)*n + z*h_{t-1}
+ *   RNN:  h_t = tanh(W_x in_t + b_x + W_h h_{t-1} + b_h)
+ * with in_t = x_t for layer 0 and h^{l-1}_t above it.  y_t = h^{L-1}_t.
+ * h0/c0 NULL mean zero state; hT/cT NULL are not written; c-arguments are
+ * ignored for GRU and RNN.  reserve == NULL runs inference; otherwise the
+ * reserve receives what rnn_bwd_data needs.  ws: workspace of
+ * rnn_get_sizes() bytes. */
+RNN_API int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, const void* w_packed,
+            void* y, void* hT, float* cT, void* reserve, void* ws, cudaStream_t stream);
+
+/* Backward pass through time for the data gradients: the exact gradient of
+ * sum(y*dy) + sum(hT*dhT) + sum(cT*dcT) with respect to x, h0 and c0,
+ * computed top layer first in reverse time.  It also leaves the gate
+ * gradients in the reserve for rnn_bwd_weights.  Must follow rnn_fwd with the
+ * same reserve.  dhT/dcT NULL count as zero; dx/dh0/dc0 NULL are not
+ * written. */
+RNN_API int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* dcT,
+                 const void* w_packed, const void* h0, const float* c0, void* dx, void* dh0,
+                 float* dc0, void* reserve, void* ws, cudaStream_t stream);
+
+/* Weight gradients, one GEMM per layer and weight matrix over all T*B rows:
+ *   dW_x = sum_t dGx_t^T in_t,  dW_h = sum_t dGh_t^T h_{t-1},
+ *   db_x = sum dGx, db_h = sum dGh
+ * written in the user layout as float.  accumulate != 0 adds to dw instead
+ * of overwriting it.  Must follow rnn_bwd_data with the same reserve. */
+RNN_API int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* reserve, float* dw,
+                    int accumulate, void* ws, cudaStream_t stream);
+
+/* Synchronizes `stream`, then reads and clears the device error word in the
+ * workspace: RNN_OK, or RNN_ERR_TIMEOUT if a bounded device wait gave up in
+ * any call since the last check. */
+RNN_API int rnn_sync_status(rnn_handle_t h, void* ws, cudaStream_t stream);
+
+RNN_API const char* rnn_strerror(int code);
+
+/* Plan introspection: writes a short text description of the chosen launch
+ * plan (recurrence kind, chunk, tiles) into buf (NUL-terminated). */
+RNN_API int rnn_describe(rnn_handle_t h, char* buf, size_t len);
+
+/* Number of kernels this library has launched since it was loaded. */
+RNN_API unsigned long long rnn_launch_count(void);
+
+/* With RNN_FLAG_PROFILE set, per-kernel-class CUDA-event timings of the calls
+ * made since the last reset.  Synchronizes the device.  For class index k
+ * (0 <= k < *n_classes) fills name (up to 32 chars), launches and total
+ * milliseconds; returns RNN_ERR_INVALID_ARG for k out of range.  reset != 0
+ * clears the records afterwards. */
+RNN_API int rnn_profile_query(rnn_handle_t h, int k, char* name, int* n_classes,
+                      unsigned long long* launches, double* total_ms, int reset);
+
+/* ------------------------------------------------------------------------
+ * Building block exposed for tests: the tcgen05 GEMM engine the input
+ * projection, the data-gradient and the weight-gradient products run on.
+ *   D[m][n] = sum_k A(m,k) * B(n,k)  (+ bias[n]) (+ D[m][n] if accumulate)
+ * A(m,k) = A[m*lda + k] when a_mn_major == 0, else A[k*lda + m]; B likewise.
+ * A, B bfloat16 on the device; D, bias float.  bias may be NULL.
+ * ---------------------------------------------------------------------- */
+RNN_API int rnn_gemm_bf16(int M, int N, int K, const void* A, long long lda, int a_mn_major,
+                  const void* B, long long ldb, int b_mn_major, float* D, long long ldd,
+                  const float* bias, int accumulate, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RNN_H */

@@ -1,0 +1,676 @@
+// api.cu -- the C-ABI of librnn: handle, buffer layouts, launch plan and the
+// layer-wavefront scheduler.
+//
+// Scheduling ("Optimizing Performance of Recurrent Neural Networks on GPUs",
+// review page, section "제안 방법": input and recurrent products are
+// independent; forward and backward passes of consecutive layers overlap):
+//   * layer 0's input projection for all T timesteps is one GEMM;
+//   * time is cut into chunks; layer l >= 1 projects its input chunk c as
+//     soon as layer l-1 has produced that chunk, then runs the chunk's
+//     recurrent steps.  Each layer owns a stream and (layer, chunk) events
+//     order the chunks, so layer l+1 works on chunk c while layer l works on
+//     chunk c+1 -- the wavefront.  The backward pass runs the same diagram
+//     top layer first in reverse time.
+//   * small-batch recurrences run all their timesteps in one persistent
+//     launch with the recurrent weights held on-chip (see persist.cu).
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/rnn.h"
+#include "launchers.h"
+
+namespace rnn {
+
+// ---------------------------------------------------------------- profiling
+struct Profiler {
+  struct Rec {
+    int cls;
+    cudaEvent_t a, b;
+  };
+  std::mutex mu;
+  std::vector<std::string> names;
+  std::vector<unsigned long long> launches;
+  std::vector<double> total_ms;
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> pool;
+  Rec open{};
+
+  int cls_of(const char* n) {
+    for (size_t i = 0; i < names.size(); ++i)
+      if (names[i] == n) return (int)i;
+    names.emplace_back(n);
+    launches.push_back(0);
+    total_ms.push_back(0.0);
+    return (int)names.size() - 1;
+  }
+  cudaEvent_t event() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  void settle() {  // requires the device to be idle
+    for (auto& r : pending) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+        total_ms[r.cls] += ms;
+        launches[r.cls] += 1;
+      }
+      pool.push_back(r.a);
+      pool.push_back(r.b);
+    }
+    pending.clear();
+  }
+  ~Profiler() {
+    for (auto& r : pending) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+    for (auto e : pool) cudaEventDestroy(e);
+  }
+};
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void launch_begin(const Launch& L) {
+  if (!L.prof) return;
+  Profiler& p = *L.prof;
+  std::lock_guard<std::mutex> g(p.mu);
+  p.open.cls = p.cls_of(L.name ? L.name : "kernel");
+  p.open.a = p.event();
+  p.open.b = p.event();
+  cudaEventRecord(p.open.a, L.stream);
+}
+
+void launch_end(const Launch& L, int n_kernels) {
+  g_launches += (unsigned long long)n_kernels;
+  if (!L.prof) return;
+  Profiler& p = *L.prof;
+  std::lock_guard<std::mutex> g(p.mu);
+  cudaEventRecord(p.open.b, L.stream);
+  p.pending.push_back(p.open);
+}
+
+}  // namespace rnn
+
+using namespace rnn;
+
+// ---------------------------------------------------------------- the handle
+struct rnn_s {
+  rnn_desc_t d{};
+  int G = 0, GH = 0, u = 0, elem = 0;
+  int num_sms = 152;
+  int have_device = 0;
+  // plan
+  int chunk = 1, nch = 1, wavefront = 0, bwd_bn = 128, bwd_splits = 1;
+  uint64_t limit_ns = 2000000000ull;
+  // sizes (bytes)
+  size_t user_w_bytes = 0, packed_bytes = 0, reserve_bytes = 0, ws_bytes = 0;
+  struct PL { size_t wx, wh, bias, bias_hn; };
+  struct RL { size_t gates, c, hn, hseq, dgx, dgh; };
+  struct WL { size_t P, hseq, c2, dyab, carry, part, ctr; };
+  struct UL { size_t wx, wh, bx, bh; };  // element offsets in the user weight vector
+  std::vector<PL> pl;
+  std::vector<RL> rl;
+  std::vector<WL> wl;
+  std::vector<UL> ul;
+  size_t ws_err = 0;
+  int ctr_count = 0;
+  // streams and events (created on first use)
+  std::vector<cudaStream_t> streams;
+  std::vector<cudaEvent_t> ev;  // [layer][chunk]
+  cudaEvent_t ev_fork = nullptr;
+  std::vector<cudaEvent_t> ev_join;
+  Profiler* prof = nullptr;
+
+  int In(int l) const { return l == 0 ? d.input : d.hidden; }
+};
+
+namespace {
+
+size_t take(size_t& cur, size_t bytes) {
+  const size_t at = (cur + 255) & ~size_t(255);
+  cur = at + bytes;
+  return at;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int plan_and_layout(rnn_s* h) {
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = d.hidden;
+  h->G = d.cell == RNN_LSTM ? 4 : d.cell == RNN_GRU ? 3 : 1;
+  h->GH = h->G * H;
+  h->elem = d.mode == RNN_MODE_BF16 ? 2 : 4;
+  const int GH = h->GH;
+  if (d.mode == RNN_MODE_BF16) {
+    if (H % 64 || d.input % 8) return RNN_ERR_UNSUPPORTED;
+    h->u = (d.cell == RNN_TANH && H % 128 == 0) ? 128 : 64;
+  } else {
+    if (H % 32 || d.input % 4) return RNN_ERR_UNSUPPORTED;
+    h->u = 32;
+  }
+  h->limit_ns = d.timeout_ns > 0 ? (uint64_t)d.timeout_ns : 2000000000ull;
+
+  // wavefront chunking
+  h->wavefront = (L > 1) && !(d.flags & RNN_FLAG_NO_WAVEFRONT);
+  if (!h->wavefront) h->chunk = T;
+  else if (d.chunk > 0) h->chunk = std::min(d.chunk, T);
+  else h->chunk = std::max(1, (T + 7) / 8);
+  h->nch = (T + h->chunk - 1) / h->chunk;
+
+  // backward step tiles: 128-row batch tiles x bn hidden units, split over K
+  // until the step covers the SMs (at most 8 ways, at least 4 K blocks each)
+  if (d.mode == RNN_MODE_BF16) {
+    h->bwd_bn = (H % 256 == 0) ? 256 : 128;
+    const int tiles = ((B + 127) / 128) * ((H + h->bwd_bn - 1) / h->bwd_bn);
+    const int kb = (GH + 63) / 64;
+    int s = std::max(1, h->num_sms / std::max(1, tiles));
+    s = std::min(s, 8);
+    s = std::min(s, std::max(1, kb / 4));
+    h->bwd_splits = s;
+    h->ctr_count = tiles;
+  } else {
+    h->bwd_bn = 32;
+    h->bwd_splits = 1;
+    h->ctr_count = 1;
+  }
+
+  const size_t e = h->elem;
+  const size_t BH = (size_t)B * H, BGH = (size_t)B * GH;
+  // user weights
+  h->ul.resize(L);
+  size_t off = 0;
+  for (int l = 0; l < L; ++l) {
+    h->ul[l].wx = off; off += (size_t)GH * h->In(l);
+    h->ul[l].wh = off; off += (size_t)GH * H;
+    h->ul[l].bx = off; off += GH;
+    h->ul[l].bh = off; off += GH;
+  }
+  h->user_w_bytes = off * e;
+  // packed weights
+  h->pl.resize(L);
+  size_t cur = 0;
+  for (int l = 0; l < L; ++l) {
+    h->pl[l].wx = take(cur, (size_t)GH * h->In(l) * e);
+    h->pl[l].wh = take(cur, (size_t)GH * H * e);
+    h->pl[l].bias = take(cur, (size_t)GH * 4);
+    h->pl[l].bias_hn = take(cur, (size_t)H * 4);
+  }
+  h->packed_bytes = (cur + 255) & ~size_t(255);
+  // reserve
+  h->rl.resize(L);
+  cur = 0;
+  for (int l = 0; l < L; ++l) {
+    h->rl[l].gates = take(cur, (size_t)T * BGH * 4);
+    h->rl[l].c = d.cell == RNN_LSTM ? take(cur, (size_t)T * BH * 4) : 0;
+    h->rl[l].hn = d.cell == RNN_GRU ? take(cur, (size_t)T * BH * 4) : 0;
+    h->rl[l].hseq = take(cur, (size_t)(T + 1) * BH * e);
+    h->rl[l].dgx = take(cur, (size_t)T * BGH * e);
+    h->rl[l].dgh = d.cell == RNN_GRU ? take(cur, (size_t)T * BGH * e) : h->rl[l].dgx;
+  }
+  h->reserve_bytes = (cur + 255) & ~size_t(255);
+  // workspace
+  h->wl.resize(L);
+  cur = 0;
+  h->ws_err = take(cur, 256);
+  for (int l = 0; l < L; ++l) {
+    h->wl[l].P = take(cur, (size_t)T * BGH * 4);
+    h->wl[l].hseq = take(cur, (size_t)(T + 1) * BH * e);
+    h->wl[l].c2 = take(cur, 2 * BH * 4);
+    h->wl[l].dyab = take(cur, (size_t)T * BH * 4);
+    h->wl[l].carry = take(cur, BH * 4);
+    h->wl[l].part = take(cur, (size_t)h->bwd_splits * BH * 4);
+    h->wl[l].ctr = take(cur, (size_t)h->ctr_count * 4);
+  }
+  h->ws_bytes = (cur + 255) & ~size_t(255);
+  return RNN_OK;
+}
+
+int ensure_runtime(rnn_s* h) {
+  if (!h->have_device) return RNN_ERR_CUDA;
+  if (!h->streams.empty() || h->d.layers == 0) return RNN_OK;
+  const int L = h->d.layers;
+  h->streams.resize(L);
+  for (int l = 0; l < L; ++l)
+    if (cudaStreamCreateWithFlags(&h->streams[l], cudaStreamNonBlocking) != cudaSuccess) return RNN_ERR_CUDA;
+  h->ev.resize((size_t)L * h->nch);
+  for (auto& e : h->ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return RNN_ERR_CUDA;
+  if (cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess) return RNN_ERR_CUDA;
+  h->ev_join.resize(L);
+  for (auto& e : h->ev_join)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return RNN_ERR_CUDA;
+  return RNN_OK;
+}
+
+// fork the layer streams off the caller's stream / join them back
+int fork_streams(rnn_s* h, cudaStream_t s) {
+  if (cudaEventRecord(h->ev_fork, s) != cudaSuccess) return RNN_ERR_CUDA;
+  for (auto st : h->streams)
+    if (cudaStreamWaitEvent(st, h->ev_fork, 0) != cudaSuccess) return RNN_ERR_CUDA;
+  return RNN_OK;
+}
+int join_streams(rnn_s* h, cudaStream_t s) {
+  for (size_t l = 0; l < h->streams.size(); ++l) {
+    if (cudaEventRecord(h->ev_join[l], h->streams[l]) != cudaSuccess) return RNN_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, h->ev_join[l], 0) != cudaSuccess) return RNN_ERR_CUDA;
+  }
+  return RNN_OK;
+}
+
+Launch mk(rnn_s* h, cudaStream_t s, void* ws, const char* name) {
+  Launch L;
+  L.stream = s;
+  L.err = ws ? reinterpret_cast<int*>(static_cast<char*>(ws) + h->ws_err) : nullptr;
+  L.limit_ns = h->limit_ns;
+  L.num_sms = h->num_sms;
+  L.prof = (h->d.flags & RNN_FLAG_PROFILE) ? h->prof : nullptr;
+  L.name = name;
+  return L;
+}
+
+#define RNN_TRY(x)              \
+  do {                          \
+    int rc__ = (x);             \
+    if (rc__ != RNN_OK) return rc__; \
+  } while (0)
+
+int cu(cudaError_t e) { return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA; }
+
+}  // namespace
+
+// ======================================================================= C ABI
+extern "C" {
+
+const char* rnn_strerror(int code) {
+  switch (code) {
+    case RNN_OK: return "ok";
+    case RNN_ERR_INVALID_ARG: return "invalid argument";
+    case RNN_ERR_UNSUPPORTED: return "unsupported shape or mode";
+    case RNN_ERR_LAUNCH: return "kernel launch failed (resources or co-residency)";
+    case RNN_ERR_CUDA: return "CUDA runtime error";
+    case RNN_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    case RNN_ERR_NOMEM: return "host allocation failed";
+    default: return "unknown error";
+  }
+}
+
+int rnn_create(const rnn_desc_t* desc, rnn_handle_t* out) {
+  if (!desc || !out) return RNN_ERR_INVALID_ARG;
+  *out = nullptr;
+  const rnn_desc_t& d = *desc;
+  if (d.cell < 0 || d.cell > 2 || d.mode < 0 || d.mode > 1 || d.layers < 1 || d.T < 1 || d.B < 1 ||
+      d.input < 1 || d.hidden < 1)
+    return RNN_ERR_INVALID_ARG;
+  if ((d.flags & RNN_FLAG_FORCE_STREAMING) && (d.flags & RNN_FLAG_FORCE_PERSISTENT)) return RNN_ERR_INVALID_ARG;
+  rnn_s* h = new (std::nothrow) rnn_s();
+  if (!h) return RNN_ERR_NOMEM;
+  h->d = d;
+  int dev = 0, n = 0;
+  if (cudaGetDeviceCount(&n) == cudaSuccess && n > 0 && cudaGetDevice(&dev) == cudaSuccess) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) {
+      h->num_sms = prop.multiProcessorCount;
+      h->have_device = 1;
+    }
+  } else {
+    cudaGetLastError();  // no device: host-side planning still works
+  }
+  int rc = plan_and_layout(h);
+  if (rc != RNN_OK) {
+    delete h;
+    return rc;
+  }
+  h->prof = new (std::nothrow) Profiler();
+  *out = h;
+  return RNN_OK;
+}
+
+int rnn_destroy(rnn_handle_t h) {
+  if (!h) return RNN_ERR_INVALID_ARG;
+  if (!h->streams.empty()) {
+    for (auto s : h->streams) cudaStreamSynchronize(s);
+    for (auto s : h->streams) cudaStreamDestroy(s);
+    for (auto e : h->ev) cudaEventDestroy(e);
+    for (auto e : h->ev_join) cudaEventDestroy(e);
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  }
+  delete h->prof;
+  delete h;
+  return RNN_OK;
+}
+
+int rnn_get_sizes(rnn_handle_t h, size_t* user_weight_bytes, size_t* packed_weight_bytes, size_t* reserve_bytes,
+                  size_t* workspace_bytes) {
+  if (!h) return RNN_ERR_INVALID_ARG;
+  if (user_weight_bytes) *user_weight_bytes = h->user_w_bytes;
+  if (packed_weight_bytes) *packed_weight_bytes = h->packed_bytes;
+  if (reserve_bytes) *reserve_bytes = h->reserve_bytes;
+  if (workspace_bytes) *workspace_bytes = h->ws_bytes;
+  return RNN_OK;
+}
+
+int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
+  if (!h || !buf || len == 0) return RNN_ERR_INVALID_ARG;
+  const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : "tanh";
+  snprintf(buf, len,
+           "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=streaming engine=%s wavefront=%d "
+           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d",
+           cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
+           h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->num_sms);
+  return RNN_OK;
+}
+
+unsigned long long rnn_launch_count(void) { return g_launches.load(); }
+
+int rnn_pack_weights(rnn_handle_t h, const void* w_user, void* w_packed, cudaStream_t stream) {
+  if (!h || !w_user || !w_packed) return RNN_ERR_INVALID_ARG;
+  if (!aligned16(w_user) || !aligned16(w_packed)) return RNN_ERR_INVALID_ARG;
+  RNN_TRY(ensure_runtime(h));
+  const char* U = static_cast<const char*>(w_user);
+  char* P = static_cast<char*>(w_packed);
+  const size_t e = h->elem;
+  for (int l = 0; l < h->d.layers; ++l) {
+    Launch L = mk(h, stream, nullptr, "pack");
+    RNN_TRY(pack_layer(L, h->d.mode, h->d.cell, h->d.hidden, h->In(l), h->u, U + h->ul[l].wx * e,
+                       U + h->ul[l].wh * e, U + h->ul[l].bx * e, U + h->ul[l].bh * e, P + h->pl[l].wx,
+                       P + h->pl[l].wh, reinterpret_cast<float*>(P + h->pl[l].bias),
+                       reinterpret_cast<float*>(P + h->pl[l].bias_hn)));
+  }
+  return RNN_OK;
+}
+
+int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, const void* w_packed, void* y,
+            void* hT, float* cT, void* reserve, void* ws, cudaStream_t stream) {
+  if (!h || !x || !w_packed || !y || !ws) return RNN_ERR_INVALID_ARG;
+  for (const void* p : {x, h0, (const void*)c0, w_packed, (const void*)y, (const void*)hT, (const void*)cT,
+                        (const void*)reserve, (const void*)ws})
+    if (!aligned16(p)) return RNN_ERR_INVALID_ARG;
+  RNN_TRY(ensure_runtime(h));
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, G = h->G, GH = h->GH, mode = d.mode;
+  const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
+  const bool train = reserve != nullptr;
+  const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+  char* R = static_cast<char*>(reserve);
+  char* W = static_cast<char*>(ws);
+  const char* PW = static_cast<const char*>(w_packed);
+  (void)G;
+
+  if (h->wavefront) RNN_TRY(fork_streams(h, stream));
+  const int nd = h->wavefront ? (L + h->nch - 1) : 1;
+  for (int dg = 0; dg < nd; ++dg) {
+    for (int l = 0; l < L; ++l) {
+      for (int c = 0; c < h->nch; ++c) {
+        if (h->wavefront && l + c != dg) continue;
+        cudaStream_t s = h->wavefront ? h->streams[l] : stream;
+        const int t0 = c * h->chunk, t1 = std::min(T, t0 + h->chunk);
+        char* hseq = train ? R + h->rl[l].hseq : W + h->wl[l].hseq;
+        float* P = reinterpret_cast<float*>(train ? R + h->rl[l].gates : W + h->wl[l].P);
+        if (c == 0) {
+          if (h0) RNN_TRY(cu(cudaMemcpyAsync(hseq, static_cast<const char*>(h0) + l * BH * e, BH * e,
+                                             cudaMemcpyDeviceToDevice, s)));
+          else RNN_TRY(cu(cudaMemsetAsync(hseq, 0, BH * e, s)));
+        }
+        if (h->wavefront && l > 0) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l - 1) * h->nch + c], 0)));
+        // input projection (layer 0: all T at once)
+        if (l > 0 || c == 0) {
+          const int r0 = l == 0 ? 0 : t0, r1 = l == 0 ? T : t1;
+          const int In = h->In(l);
+          Operand A;
+          A.ptr = l == 0 ? static_cast<const char*>(x) + (size_t)r0 * B * In * e
+                         : static_cast<const char*>(train ? R + h->rl[l - 1].hseq : W + h->wl[l - 1].hseq) +
+                               (size_t)(r0 + 1) * BH * e;
+          A.ld = In;
+          A.mn_major = 0;
+          A.mn_ext = (r1 - r0) * B;
+          A.k_ext = In;
+          Operand Bw{PW + h->pl[l].wx, In, 0, GH, In};
+          Remap none{0, 1, 1, 1};
+          Launch Lk = mk(h, s, ws, "input_proj_gemm");
+          RNN_TRY(gemm_f32(Lk, mode, A, Bw, (r1 - r0) * B, GH, In, P + (size_t)r0 * BGH, GH,
+                           reinterpret_cast<const float*>(PW + h->pl[l].bias), 0, none, 0));
+        }
+        // recurrent steps of the chunk
+        for (int t = t0; t < t1; ++t) {
+          FwdStepArgs a;
+          a.B = B;
+          a.H = H;
+          a.u = h->u;
+          a.P = P + (size_t)t * BGH;
+          a.write_gates = train ? 1 : 0;
+          a.bias_hn = reinterpret_cast<const float*>(PW + h->pl[l].bias_hn);
+          auto cbuf = [&](int tt) -> float* {
+            return train ? reinterpret_cast<float*>(R + h->rl[l].c) + (size_t)tt * BH
+                         : reinterpret_cast<float*>(W + h->wl[l].c2) + (size_t)(tt & 1) * BH;
+          };
+          a.c_prev = lstm ? (t == 0 ? (c0 ? c0 + l * BH : nullptr) : cbuf(t - 1)) : nullptr;
+          a.c_out = lstm ? cbuf(t) : nullptr;
+          a.h_prev = hseq + (size_t)t * BH * e;
+          a.h_out = hseq + (size_t)(t + 1) * BH * e;
+          a.y = l == L - 1 ? static_cast<char*>(y) + (size_t)t * BH * e : nullptr;
+          a.hT = (t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
+          a.cT = (t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
+          a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
+          Operand A{hseq + (size_t)t * BH * e, H, 0, B, H};
+          Operand Bw{PW + h->pl[l].wh, H, 0, GH, H};
+          Launch Lk = mk(h, s, ws, "fwd_step");
+          RNN_TRY(fwd_step(Lk, mode, d.cell, A, Bw, a));
+        }
+        if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + c], s)));
+      }
+    }
+  }
+  if (h->wavefront) RNN_TRY(join_streams(h, stream));
+  return RNN_OK;
+}
+
+int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* dcT, const void* w_packed,
+                 const void* h0, const float* c0, void* dx, void* dh0, float* dc0, void* reserve, void* ws,
+                 cudaStream_t stream) {
+  if (!h || !dy || !w_packed || !reserve || !ws) return RNN_ERR_INVALID_ARG;
+  for (const void* p : {dy, dhT, (const void*)dcT, w_packed, h0, (const void*)c0, (const void*)dx,
+                        (const void*)dh0, (const void*)dc0, (const void*)reserve, (const void*)ws})
+    if (!aligned16(p)) return RNN_ERR_INVALID_ARG;
+  (void)h0;
+  RNN_TRY(ensure_runtime(h));
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, GH = h->GH, mode = d.mode;
+  const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
+  const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+  char* R = static_cast<char*>(reserve);
+  char* W = static_cast<char*>(ws);
+  const char* PW = static_cast<const char*>(w_packed);
+
+  for (int l = 0; l < L; ++l)
+    RNN_TRY(cu(cudaMemsetAsync(W + h->wl[l].ctr, 0, (size_t)h->ctr_count * 4, stream)));
+  if (h->wavefront) RNN_TRY(fork_streams(h, stream));
+  const int nd = h->wavefront ? (L + h->nch - 1) : 1;
+  for (int dg = 0; dg < nd; ++dg) {
+    for (int li = 0; li < L; ++li) {
+      const int l = L - 1 - li;
+      for (int rc = 0; rc < h->nch; ++rc) {
+        if (h->wavefront && li + rc != dg) continue;
+        cudaStream_t s = h->wavefront ? h->streams[l] : stream;
+        const int t1 = T - rc * h->chunk, t0 = std::max(0, t1 - h->chunk);
+        if (h->wavefront && l < L - 1) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l + 1) * h->nch + rc], 0)));
+        const bool top = l == L - 1;
+        const char* dyl = top ? static_cast<const char*>(dy) : W + h->wl[l].dyab;
+        const size_t dy_es = top ? e : 4;
+        float* carry = reinterpret_cast<float*>(W + h->wl[l].carry);
+        char* hseq = R + h->rl[l].hseq;
+        const float* c0l = c0 ? c0 + l * BH : nullptr;
+        if (rc == 0 && (lstm || gru)) {
+          if (lstm && dcT) RNN_TRY(cu(cudaMemcpyAsync(carry, dcT + l * BH, BH * 4, cudaMemcpyDeviceToDevice, s)));
+          else RNN_TRY(cu(cudaMemsetAsync(carry, 0, BH * 4, s)));
+        }
+        auto args_for = [&](int st) {
+          BwdStepArgs a;
+          std::memset(&a, 0, sizeof(a));
+          a.B = B;
+          a.H = H;
+          a.u = h->u;
+          a.gates = reinterpret_cast<const float*>(R + h->rl[l].gates) + (size_t)st * BGH;
+          a.c_s = lstm ? reinterpret_cast<const float*>(R + h->rl[l].c) + (size_t)st * BH : nullptr;
+          a.c_sm1 = lstm ? (st > 0 ? reinterpret_cast<const float*>(R + h->rl[l].c) + (size_t)(st - 1) * BH : c0l)
+                         : nullptr;
+          a.hn_s = gru ? reinterpret_cast<const float*>(R + h->rl[l].hn) + (size_t)st * BH : nullptr;
+          a.h_sm1 = hseq + (size_t)st * BH * e;
+          a.dy = dyl + (size_t)st * BH * dy_es;
+          a.dy_f32 = top ? (mode == RNN_MODE_FP32) : 1;
+          a.carry = carry;
+          a.dGx = R + h->rl[l].dgx + (size_t)st * BGH * e;
+          a.dGh = R + h->rl[l].dgh + (size_t)st * BGH * e;
+          a.part = reinterpret_cast<float*>(W + h->wl[l].part);
+          a.counters = reinterpret_cast<int*>(W + h->wl[l].ctr);
+          return a;
+        };
+        Operand Bw{PW + h->pl[l].wh, H, 1, H, GH};
+        for (int st = t1 - 1; st >= t0; --st) {
+          BwdStepArgs a = args_for(st);
+          if (st == T - 1) {
+            Launch Lk = mk(h, s, ws, "bwd_point");
+            RNN_TRY(bwd_point(Lk, mode, d.cell, a, dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr));
+          } else {
+            Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
+            Launch Lk = mk(h, s, ws, "bwd_step");
+            RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+          }
+        }
+        if (t0 == 0 && (dh0 || (dc0 && lstm))) {
+          BwdStepArgs a = args_for(0);
+          a.final_ = 1;
+          a.dh0 = dh0 ? static_cast<char*>(dh0) + l * BH * e : nullptr;
+          a.dc0 = (dc0 && lstm) ? dc0 + l * BH : nullptr;
+          Operand A{R + h->rl[l].dgh, GH, 0, B, GH};
+          Launch Lk = mk(h, s, ws, "bwd_step");
+          RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+        }
+        // gradient of this chunk's layer inputs: dGx W_x
+        if (l > 0 || dx) {
+          const int In = h->In(l);
+          Operand A{R + h->rl[l].dgx + (size_t)t0 * BGH * e, GH, 0, (t1 - t0) * B, GH};
+          Operand Bx{PW + h->pl[l].wx, In, 1, In, GH};
+          Launch Lk = mk(h, s, ws, "dx_gemm");
+          if (l > 0) {
+            Remap none{0, 1, 1, 1};
+            RNN_TRY(gemm_f32(Lk, mode, A, Bx, (t1 - t0) * B, In, GH,
+                             reinterpret_cast<float*>(W + h->wl[l - 1].dyab) + (size_t)t0 * BH, In, nullptr, 0, none,
+                             0));
+          } else {
+            RNN_TRY(gemm_store(Lk, mode, A, Bx, (t1 - t0) * B, In, GH,
+                               static_cast<char*>(dx) + (size_t)t0 * B * In * e, In, 0));
+          }
+        }
+        if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + rc], s)));
+      }
+    }
+  }
+  if (h->wavefront) RNN_TRY(join_streams(h, stream));
+  return RNN_OK;
+}
+
+int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* reserve, float* dw, int accumulate,
+                    void* ws, cudaStream_t stream) {
+  if (!h || !x || !reserve || !dw || !ws) return RNN_ERR_INVALID_ARG;
+  for (const void* p : {x, h0, reserve, (const void*)dw, (const void*)ws})
+    if (!aligned16(p)) return RNN_ERR_INVALID_ARG;
+  (void)h0;  // h_{-1} = h0 was stored in the reserve by the forward pass
+  RNN_TRY(ensure_runtime(h));
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, G = h->G, GH = h->GH, mode = d.mode;
+  const size_t e = h->elem, BH = (size_t)B * H;
+  const char* R = static_cast<const char*>(reserve);
+  const int TB = T * B;
+  const bool multi = L > 1;
+  if (multi) RNN_TRY(fork_streams(h, stream));
+  for (int l = 0; l < L; ++l) {
+    cudaStream_t s = multi ? h->streams[l] : stream;
+    const int In = h->In(l);
+    Remap rm{1, G, h->u, H};
+    Operand dgx{R + h->rl[l].dgx, GH, 1, GH, TB};
+    Operand dgh{R + h->rl[l].dgh, GH, 1, GH, TB};
+    Operand X = l == 0 ? Operand{x, In, 1, In, TB} : Operand{R + h->rl[l - 1].hseq + BH * e, H, 1, H, TB};
+    Operand Hp{R + h->rl[l].hseq, H, 1, H, TB};
+    Launch Lk = mk(h, s, ws, "dw_gemm");
+    RNN_TRY(gemm_f32(Lk, mode, dgx, X, GH, In, TB, dw + h->ul[l].wx, In, nullptr, accumulate, rm, 0));
+    RNN_TRY(gemm_f32(Lk, mode, dgh, Hp, GH, H, TB, dw + h->ul[l].wh, H, nullptr, accumulate, rm, 0));
+    Launch Lb = mk(h, s, ws, "bias_grad");
+    RNN_TRY(bias_grad(Lb, mode, d.cell, H, h->u, TB, R + h->rl[l].dgx, R + h->rl[l].dgh, dw + h->ul[l].bx,
+                      dw + h->ul[l].bh, accumulate));
+  }
+  if (multi) RNN_TRY(join_streams(h, stream));
+  return RNN_OK;
+}
+
+int rnn_sync_status(rnn_handle_t h, void* ws, cudaStream_t stream) {
+  if (!h || !ws) return RNN_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return RNN_ERR_CUDA;
+  int word = 0;
+  char* p = static_cast<char*>(ws) + h->ws_err;
+  if (cudaMemcpy(&word, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return RNN_ERR_CUDA;
+  if (word != 0) {
+    if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return RNN_ERR_CUDA;
+    return RNN_ERR_TIMEOUT;
+  }
+  return RNN_OK;
+}
+
+int rnn_profile_query(rnn_handle_t h, int k, char* name, int* n_classes, unsigned long long* launches,
+                      double* total_ms, int reset) {
+  if (!h || !h->prof) return RNN_ERR_INVALID_ARG;
+  if (h->have_device && cudaDeviceSynchronize() != cudaSuccess) return RNN_ERR_CUDA;
+  Profiler& p = *h->prof;
+  std::lock_guard<std::mutex> g(p.mu);
+  p.settle();
+  if (n_classes) *n_classes = (int)p.names.size();
+  int rc = RNN_OK;
+  if (k >= 0 && k < (int)p.names.size()) {
+    if (name) {
+      std::strncpy(name, p.names[k].c_str(), 31);
+      name[31] = 0;
+    }
+    if (launches) *launches = p.launches[k];
+    if (total_ms) *total_ms = p.total_ms[k];
+  } else if (k >= 0) {
+    rc = RNN_ERR_INVALID_ARG;
+  }
+  if (reset) {
+    for (auto& v : p.launches) v = 0;
+    for (auto& v : p.total_ms) v = 0.0;
+  }
+  return rc;
+}
+
+int rnn_gemm_bf16(int M, int N, int K, const void* A, long long lda, int a_mn_major, const void* B, long long ldb,
+                  int b_mn_major, float* D, long long ldd, const float* bias, int accumulate, cudaStream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !D) return RNN_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || ((lda * 2) & 15) || ((ldb * 2) & 15)) return RNN_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return RNN_ERR_CUDA;
+  Operand a{A, lda, a_mn_major ? 1 : 0, M, K};
+  Operand b{B, ldb, b_mn_major ? 1 : 0, N, K};
+  Launch L;
+  L.stream = stream;
+  L.err = nullptr;
+  L.limit_ns = 2000000000ull;
+  L.num_sms = prop.multiProcessorCount;
+  L.prof = nullptr;
+  L.name = "gemm";
+  Remap none{0, 1, 1, 1};
+  return gemm_f32(L, RNN_MODE_BF16, a, b, M, N, K, D, ldd, bias, accumulate, none, 0);
+}
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// common.cuh -- types, conversions, error word and the cell arithmetic shared
+// by every kernel of librnn.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rnn {
+
+enum Cell { LSTM = 0, GRU = 1, TANH = 2 };
+
+template <int CELL>
+struct CellInfo;
+template <>
+struct CellInfo<LSTM> { static constexpr int G = 4; };
+template <>
+struct CellInfo<GRU> { static constexpr int G = 3; };
+template <>
+struct CellInfo<TANH> { static constexpr int G = 1; };
+
+// Device error word codes (written into the first word of the workspace).
+enum DevErr { DEV_OK = 0, DEV_TIMEOUT_PIPE = 1, DEV_TIMEOUT_STEP = 2 };
+
+// ---------------------------------------------------------------- storage types
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <class S>
+__device__ __forceinline__ S from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// 16 consecutive elements of storage type S, to/from float.
+template <class S>
+__device__ __forceinline__ void load16(const S* p, float* v) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = to_f32(p[i]);
+}
+template <>
+__device__ __forceinline__ void load16<float>(const float* p, float* v) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float4 f = q[i];
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+}
+template <>
+__device__ __forceinline__ void load16<__nv_bfloat16>(const __nv_bfloat16* p, float* v) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint4 u = q[i];
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[8 * i + 2 * k] = __uint_as_float(w[k] << 16);
+      v[8 * i + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+}
+// 16 floats through L2 only (data written by other CTAs of the same launch).
+__device__ __forceinline__ void load16_cg(const float* p, float* v) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float4 f = __ldcg(q + i);
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+}
+template <class S>
+__device__ __forceinline__ void store16(S* p, const float* v) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) p[i] = from_f32<S>(v[i]);
+}
+template <>
+__device__ __forceinline__ void store16<float>(float* p, const float* v) {
+  float4* q = reinterpret_cast<float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* p, const float* v) {
+  uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    q[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+  }
+}
+
+// ---------------------------------------------------------------- activations
+// Logistic sigmoid and tanh through CUDA's own expf / tanhf.
+__device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + expf(-a)); }
+__device__ __forceinline__ float tanh_(float a) { return tanhf(a); }
+
+// ---------------------------------------------------------------- time and errors
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void raise_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Packed gate-row index of (gate g, hidden unit j) with interleave block u:
+// rows are grouped [H/u][G][u] so that one block of G*u rows holds every gate
+// of u consecutive hidden units.
+__device__ __forceinline__ int packed_row(int g, int j, int G, int u) {
+  return (j / u) * (G * u) + g * u + (j % u);
+}
+
+}  // namespace rnn

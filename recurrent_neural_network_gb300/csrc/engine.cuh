@@ -1,0 +1,341 @@
+// engine.cuh -- the two GEMM mainloops every product of the recurrent path
+// runs on, both computing   D[m][n] = sum_k A(m,k) * B(n,k)   tile by tile and
+// handing each finished tile to an epilogue functor:
+//
+//  * tc_gemm_kernel: bf16 operands on the fifth-generation tensor cores.
+//    One warp issues TMA tile loads into a STAGES-deep shared-memory ring
+//    (128-byte swizzle), one thread issues tcgen05.mma into a double-buffered
+//    TMEM accumulator, four warps run the epilogue straight out of TMEM while
+//    the next tile's MMAs proceed.  Operands may be K-major or MN-major (the
+//    transposed products of the backward pass need the latter).  Tiles are
+//    128 x BN, K step 64; the grid is persistent over tiles and split-K ranges.
+//  * simt_gemm_kernel: fp32 FFMA (no TF32) for the fp32 storage mode.
+//
+// Epilogue functors implement
+//   template <class Acc> __device__ void operator()(const TileCoord&, int row, const Acc&) const
+// where `row` is the row inside the tile owned by the calling thread and
+// Acc::load16(col, v) returns 16 consecutive accumulator columns of that row.
+// All threads of a warp call load16 together (TMEM loads are warp-collective).
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace rnn {
+
+struct GemmGeom {
+  int M, N, K;
+  int m_tiles, n_tiles, splits;
+  int kb_total, kb_per_split;  // K blocks of 64 (tcgen05) or 16 (SIMT)
+  int num_tiles;               // m_tiles * n_tiles * splits
+  int a_mn, b_mn;              // operand majorness (1 = MN-major)
+  uint64_t limit_ns;           // bound on every pipeline wait
+  int* err;                    // device error word
+};
+
+struct TileCoord {
+  int m0, n0;       // first row / column of the tile
+  int mt, nt;       // tile indices
+  int split, splits;
+  int* scratch;     // 8 ints of shared memory for the epilogue warps (tcgen05 only)
+};
+
+struct TmemAcc {
+  uint32_t taddr;
+  __device__ __forceinline__ void load16(int col, float* v) const { tc::tmem_load16(taddr + col, v); }
+};
+
+struct SmemAcc {
+  const float* row;
+  __device__ __forceinline__ void load16(int col, float* v) const {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = row[col + i];
+  }
+};
+
+__device__ __forceinline__ void decode_tile(const GemmGeom& g, int tile, int& mt, int& nt, int& split) {
+  split = tile % g.splits;
+  const int mn = tile / g.splits;
+  mt = mn % g.m_tiles;
+  nt = mn / g.m_tiles;
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 engine
+// ---------------------------------------------------------------------------
+namespace tce {
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int A_BYTES = BM * BK * 2;
+template <int BN>
+__host__ __device__ constexpr int stage_bytes() { return A_BYTES + BN * BK * 2; }
+template <int BN>
+__host__ __device__ constexpr uint32_t tmem_cols() {
+  return (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+}
+template <int BN, int STAGES>
+__host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>() + 1024 + 256; }
+}  // namespace tce
+
+template <int BN, int STAGES, class Epi>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                   const GemmGeom g, const Epi epi) {
+  using namespace tce;
+  constexpr int STAGE = stage_bytes<BN>();
+  constexpr uint32_t TMEM_COLS = tmem_cols<BN>();
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* scratch = reinterpret_cast<int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(tfull + a, 1);
+      tc::mbar_init(tempty + a, 4);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&mapA);
+    tc::tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int last_par[STAGES];  // parity of the last load issued into each stage (-1: none)
+      for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < g.num_tiles && ok; tile += gridDim.x) {
+        int mt, nt, split;
+        decode_tile(g, tile, mt, nt, split);
+        const int kb0 = split * g.kb_per_split;
+        const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
+        const int m0 = mt * BM, n0 = nt * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, g.err, g.limit_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * STAGE;
+          uint8_t* sb = sa + A_BYTES;
+          tc::mbar_arrive_expect_tx(full + stage, STAGE);
+          last_par[stage] = static_cast<int>(phase);
+          const int k0 = kb * BK;
+          if (g.a_mn) {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tc::tma_load_2d(sa + j * 8192, &mapA, full + stage, m0 + 64 * j, k0);
+          } else {
+            tc::tma_load_2d(sa, &mapA, full + stage, k0, m0);
+          }
+          if (g.b_mn) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tc::tma_load_2d(sb + j * 8192, &mapB, full + stage, n0 + 64 * j, k0);
+          } else {
+            tc::tma_load_2d(sb, &mapB, full + stage, k0, n0);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // let copies already in flight land before the CTA's shared memory goes away
+        for (int s = 0; s < STAGES; ++s) {
+          if (last_par[s] < 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!tc::mbar_try_wait(full + s, static_cast<uint32_t>(last_par[s])) &&
+                 globaltimer_ns() - t0 < 1000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16(BM, BN, g.a_mn, g.b_mn);
+      uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < g.num_tiles && ok; tile += gridDim.x) {
+        int mt, nt, split;
+        decode_tile(g, tile, mt, nt, split);
+        const int kb0 = split * g.kb_per_split;
+        const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
+        if (!tc::mbar_wait(tempty + acc, aphase ^ 1, abort_flag, g.err, g.limit_ns)) break;
+        tc::fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!tc::mbar_wait(full + stage, phase, abort_flag, g.err, g.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t sa = tc::smem_addr(smem + stage * STAGE);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = g.a_mn ? tc::sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                       : tc::sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = g.b_mn ? tc::sdesc_sw128(sb + kk * 2048, 8192, 1024)
+                                       : tc::sdesc_sw128(sb + kk * 32, 16, 1024);
+            tc::mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(empty + stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(tfull + acc);
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;
+    uint32_t acc = 0, aphase = 0;
+    for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
+      int mt, nt, split;
+      decode_tile(g, tile, mt, nt, split);
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc::fence_after_sync();
+      TileCoord t;
+      t.m0 = mt * BM;
+      t.n0 = nt * BN;
+      t.mt = mt;
+      t.nt = nt;
+      t.split = split;
+      t.splits = g.splits;
+      t.scratch = scratch;
+      TmemAcc a{tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16)};
+      epi(t, row, a, BN);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tempty + acc);
+      acc ^= 1;
+      if (acc == 0) aphase ^= 1;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// fp32 SIMT engine (FFMA): 32 x BN tiles, 128 threads, K step 16.
+// ---------------------------------------------------------------------------
+namespace se {
+constexpr int BM = 32;
+constexpr int BK = 16;
+template <int BN>
+__host__ __device__ constexpr int smem_bytes() { return (BK * (BM + 1) + BK * (BN + 1) + BM * (BN + 1)) * 4; }
+}  // namespace se
+
+template <int BN, class Epi>
+__global__ void __launch_bounds__(128)
+    simt_gemm_kernel(const float* __restrict__ A, long long lda, const float* __restrict__ Bm, long long ldb,
+                     const GemmGeom g, const Epi epi) {
+  using namespace se;
+  static_assert(BN % 32 == 0, "SIMT tile width");
+  constexpr int NC = BN / 32;
+  extern __shared__ float sm[];
+  float* As = sm;                          // [BK][BM+1]
+  float* Bs = As + BK * (BM + 1);          // [BK][BN+1]
+  float* Cs = Bs + BK * (BN + 1);          // [BM][BN+1]
+  const int tid = threadIdx.x;
+  const int ty = tid >> 5, tx = tid & 31;
+  int mt, nt, split;
+  decode_tile(g, blockIdx.x, mt, nt, split);
+  const int m0 = mt * BM, n0 = nt * BN;
+  float acc[8][NC];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[r][c] = 0.f;
+
+  for (int k0 = 0; k0 < g.K; k0 += BK) {
+    for (int e = tid; e < BM * BK; e += 128) {
+      const int r = e / BK, kk = e % BK;
+      const int m = m0 + r, k = k0 + kk;
+      float v = 0.f;
+      if (m < g.M && k < g.K) v = g.a_mn ? A[(long long)k * lda + m] : A[(long long)m * lda + k];
+      As[kk * (BM + 1) + r] = v;
+    }
+    for (int e = tid; e < BN * BK; e += 128) {
+      const int c = e / BK, kk = e % BK;
+      const int n = n0 + c, k = k0 + kk;
+      float v = 0.f;
+      if (n < g.N && k < g.K) v = g.b_mn ? Bm[(long long)k * ldb + n] : Bm[(long long)n * ldb + k];
+      Bs[kk * (BN + 1) + c] = v;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[8], b[NC];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) a[r] = As[kk * (BM + 1) + ty * 8 + r];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) b[c] = Bs[kk * (BN + 1) + tx + 32 * c];
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int c = 0; c < NC; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int c = 0; c < NC; ++c) Cs[(ty * 8 + r) * (BN + 1) + tx + 32 * c] = acc[r][c];
+  __syncthreads();
+  if (tid < BM) {
+    TileCoord t;
+    t.m0 = m0;
+    t.n0 = n0;
+    t.mt = mt;
+    t.nt = nt;
+    t.split = 0;
+    t.splits = 1;
+    t.scratch = nullptr;
+    SmemAcc a{Cs + tid * (BN + 1)};
+    epi(t, tid, a, BN);
+  }
+}
+
+}  // namespace rnn

@@ -1,0 +1,138 @@
+// launch.cuh -- host templates that turn an (Operand, Operand, epilogue) triple
+// into a launch of one of the two GEMM engines.  Included by the kernel
+// translation units only.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "../../include/rnn.h"
+#include "engine.cuh"
+#include "launchers.h"
+
+namespace rnn {
+
+// cuTensorMapEncodeTiled, fetched once from the driver through the runtime.
+inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D bf16 tensor map over an operand with 128-byte swizzle.  K-major operands
+// use a box of 64 (k) x box_rows (mn); MN-major operands a box of 64 (mn) x 64 (k).
+inline int encode_operand(CUtensorMap* map, const Operand& op, int box_rows) {
+  auto enc = tmap_encoder();
+  if (!enc) return RNN_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(op.ptr) & 15) || ((op.ld * 2) & 15)) return RNN_ERR_INVALID_ARG;
+  cuuint64_t dims[2], strides[1];
+  cuuint32_t box[2], es[2] = {1, 1};
+  if (op.mn_major) {
+    dims[0] = (cuuint64_t)op.mn_ext;
+    dims[1] = (cuuint64_t)op.k_ext;
+    box[0] = 64;
+    box[1] = 64;
+  } else {
+    dims[0] = (cuuint64_t)op.k_ext;
+    dims[1] = (cuuint64_t)op.mn_ext;
+    box[0] = 64;
+    box[1] = (cuuint32_t)box_rows;
+  }
+  strides[0] = (cuuint64_t)op.ld * 2;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.ptr), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RNN_OK : RNN_ERR_INVALID_ARG;
+}
+
+inline int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return RNN_OK;
+  if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorLaunchOutOfResources) return RNN_ERR_LAUNCH;
+  return RNN_ERR_CUDA;
+}
+
+template <int BN, int STAGES, class Epi>
+int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, int splits, int max_ctas,
+              const Epi& epi) {
+  if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
+  if (B.mn_major && BN % 64) return RNN_ERR_UNSUPPORTED;
+  CUtensorMap ma, mb;
+  int rc = encode_operand(&ma, A, tce::BM);
+  if (rc) return rc;
+  rc = encode_operand(&mb, B, BN);
+  if (rc) return rc;
+  GemmGeom g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.m_tiles = (M + tce::BM - 1) / tce::BM;
+  g.n_tiles = (N + BN - 1) / BN;
+  g.kb_total = (K + tce::BK - 1) / tce::BK;
+  splits = std::max(1, std::min(splits, g.kb_total));
+  g.kb_per_split = (g.kb_total + splits - 1) / splits;
+  g.splits = (g.kb_total + g.kb_per_split - 1) / g.kb_per_split;
+  g.num_tiles = g.m_tiles * g.n_tiles * g.splits;
+  g.a_mn = A.mn_major;
+  g.b_mn = B.mn_major;
+  g.limit_ns = L.limit_ns;
+  g.err = L.err;
+  constexpr int smem = tce::smem_bytes<BN, STAGES>();
+  auto kern = tc_gemm_kernel<BN, STAGES, Epi>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    attr = true;
+  }
+  int cap = max_ctas > 0 ? max_ctas : L.num_sms;
+  int grid = std::min(g.num_tiles, cap);
+  launch_begin(L);
+  kern<<<grid, 192, smem, L.stream>>>(ma, mb, g, epi);
+  cudaError_t e = cudaGetLastError();
+  launch_end(L);
+  return cuda_status(e);
+}
+
+template <int BN, class Epi>
+int launch_simt(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, const Epi& epi) {
+  if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
+  GemmGeom g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.m_tiles = (M + se::BM - 1) / se::BM;
+  g.n_tiles = (N + BN - 1) / BN;
+  g.splits = 1;
+  g.kb_total = (K + se::BK - 1) / se::BK;
+  g.kb_per_split = g.kb_total;
+  g.num_tiles = g.m_tiles * g.n_tiles;
+  g.a_mn = A.mn_major;
+  g.b_mn = B.mn_major;
+  g.limit_ns = L.limit_ns;
+  g.err = L.err;
+  constexpr int smem = se::smem_bytes<BN>();
+  auto kern = simt_gemm_kernel<BN, Epi>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    attr = true;
+  }
+  launch_begin(L);
+  kern<<<g.num_tiles, 128, smem, L.stream>>>(static_cast<const float*>(A.ptr), A.ld,
+                                             static_cast<const float*>(B.ptr), B.ld, g, epi);
+  cudaError_t e = cudaGetLastError();
+  launch_end(L);
+  return cuda_status(e);
+}
+
+}  // namespace rnn

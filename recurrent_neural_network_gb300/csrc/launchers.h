@@ -1,0 +1,103 @@
+// launchers.h -- host-side entry points of the kernel translation units, used
+// by the C-ABI layer (api.cu).  Plain pointers and sizes only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rnn {
+
+// One GEMM operand: element (mn, k) sits at ptr[mn*ld + k] (K-major) or
+// ptr[k*ld + mn] (MN-major).  Elements outside [0,mn_ext) x [0,k_ext) are zero.
+struct Operand {
+  const void* ptr;
+  long long ld;
+  int mn_major;
+  int mn_ext, k_ext;
+};
+
+struct Profiler;  // defined in api.cu
+
+// Launch context: stream, device error word, wait bound, SM count, and the
+// profiling hook (null = off) with the kernel-class name to file timings under.
+struct Launch {
+  cudaStream_t stream;
+  int* err;
+  uint64_t limit_ns;
+  int num_sms;
+  Profiler* prof;
+  const char* name;
+};
+
+// profiling / counting hooks (api.cu)
+void launch_begin(const Launch& L);
+void launch_end(const Launch& L, int n_kernels = 1);
+
+// Packed -> user row mapping of the weight-gradient products.
+struct Remap {
+  int on, G, u, H;
+};
+
+// ---------------------------------------------------------------- gemm.cu
+// D[m][n] = sum_k A(m,k) B(n,k) (+ bias[n]) (+ D) with float output.
+// mode 1: bf16 operands on tcgen05; mode 0: fp32 operands on FFMA.
+int gemm_f32(const Launch& L, int mode, const Operand& A, const Operand& B, int M, int N, int K, float* D,
+             long long ldd, const float* bias, int accumulate, const Remap& remap, int max_ctas);
+// same with storage-type output (bf16 in mode 1, float in mode 0)
+int gemm_store(const Launch& L, int mode, const Operand& A, const Operand& B, int M, int N, int K, void* D,
+               long long ldd, int max_ctas);
+
+// user -> packed weights for one layer
+int pack_layer(const Launch& L, int mode, int cell, int H, int In, int u, const void* wx, const void* wh,
+               const void* bx, const void* bh, void* pwx, void* pwh, float* pbias, float* pbias_hn);
+
+// column sums over `rows` rows of the gate-gradient matrices into user-layout
+// bias gradients (gate blocks of H).  dgh may equal dgx.
+int bias_grad(const Launch& L, int mode, int cell, int H, int u, long long rows, const void* dgx, const void* dgh,
+              float* dbx, float* dbh, int accumulate);
+
+// ---------------------------------------------------------------- step_fwd.cu
+struct FwdStepArgs {
+  int B, H, u;
+  float* P;
+  int write_gates;
+  const float* bias_hn;
+  const float* c_prev;
+  float* c_out;
+  const void* h_prev;
+  void* h_out;
+  void* y;
+  void* hT;
+  float* cT;
+  float* hn_out;
+};
+// one forward timestep of one layer: A = h_{t-1} [B][H], B = packed W_h [G*H][H]
+int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, const FwdStepArgs& a);
+
+// ---------------------------------------------------------------- step_bwd.cu
+struct BwdStepArgs {
+  int B, H, u;
+  const float* gates;
+  const float* c_s;
+  const float* c_sm1;
+  const float* hn_s;
+  const void* h_sm1;
+  const void* dy;
+  int dy_f32;
+  float* carry;
+  void* dGx;
+  void* dGh;
+  int final_;
+  void* dh0;
+  float* dc0;
+  float* part;
+  int* counters;
+};
+// one backward timestep: A = dGh_{s+1} [B][G*H], Bw = packed W_h (MN-major view)
+int bwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, int bn, int splits,
+             const BwdStepArgs& a);
+// pointwise-only backward step (the last timestep): dh starts from dh_init
+// ([B][H], storage type, null = zero)
+int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const void* dh_init);
+
+}  // namespace rnn

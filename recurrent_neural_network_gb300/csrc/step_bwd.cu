@@ -1,0 +1,107 @@
+// step_bwd.cu -- one backward-through-time step of one layer: the product
+// dGh_{s+1} W_h (gate gradients times the packed recurrent weights, read
+// MN-major so that one packed copy serves both directions) with the pointwise
+// gate derivative of step s fused into its epilogue; plus the pointwise-only
+// first step of the reverse sweep.
+//
+// "Optimizing Performance of Recurrent Neural Networks on GPUs" (review page,
+// section "제안 방법"): backward passes overlap across layers the same way as
+// forward ones; the reverse sweep therefore has the same shape as the forward.
+#include "epilogues.cuh"
+#include "launch.cuh"
+
+namespace rnn {
+
+namespace {
+template <int CELL, class S>
+BwdPoint<CELL, S> make_point(const BwdStepArgs& a) {
+  BwdPoint<CELL, S> p;
+  p.B = a.B;
+  p.H = a.H;
+  p.u = a.u;
+  p.gates = a.gates;
+  p.c_s = a.c_s;
+  p.c_sm1 = a.c_sm1;
+  p.hn_s = a.hn_s;
+  p.h_sm1 = static_cast<const S*>(a.h_sm1);
+  p.dy = a.dy;
+  p.dy_f32 = a.dy_f32;
+  p.carry = a.carry;
+  p.dGx = static_cast<S*>(a.dGx);
+  p.dGh = static_cast<S*>(a.dGh);
+  return p;
+}
+
+template <int CELL, class S>
+EpiBwdStep<CELL, S> make_epi(const BwdStepArgs& a) {
+  EpiBwdStep<CELL, S> e;
+  e.pt = make_point<CELL, S>(a);
+  e.final_ = a.final_;
+  e.dh0 = static_cast<S*>(a.dh0);
+  e.dc0 = a.dc0;
+  e.part = a.part;
+  e.counters = a.counters;
+  return e;
+}
+
+template <int CELL>
+int bwd_step_cell(const Launch& L, int mode, const Operand& A, const Operand& Bw, int bn, int splits,
+                  const BwdStepArgs& a) {
+  const int G = CellInfo<CELL>::G;
+  const int M = a.B, N = a.H, K = G * a.H;
+  if (mode == 1) {
+    using S = __nv_bfloat16;
+    if (bn == 256) return launch_tc<256, 4>(L, A, Bw, M, N, K, splits, 0, make_epi<CELL, S>(a));
+    if (bn == 128) return launch_tc<128, 6>(L, A, Bw, M, N, K, splits, 0, make_epi<CELL, S>(a));
+    return RNN_ERR_UNSUPPORTED;
+  }
+  return launch_simt<32>(L, A, Bw, M, N, K, make_epi<CELL, float>(a));
+}
+
+template <int CELL, class S>
+__global__ void bwd_point_kernel(const BwdPoint<CELL, S> p, const S* __restrict__ dh_init) {
+  const int chunks = p.H / 16;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)p.B * chunks) return;
+  const int b = (int)(idx / chunks), j0 = (int)(idx % chunks) * 16;
+  float dh[16];
+  if (dh_init) load16(dh_init + (size_t)b * p.H + j0, dh);
+  else
+#pragma unroll
+    for (int i = 0; i < 16; ++i) dh[i] = 0.f;
+  p.run(b, j0, dh);
+}
+
+template <int CELL, class S>
+int point_launch(const Launch& L, const BwdStepArgs& a, const void* dh_init) {
+  const long long n = (long long)a.B * (a.H / 16);
+  const int threads = 128;
+  launch_begin(L);
+  bwd_point_kernel<CELL, S><<<(unsigned)((n + threads - 1) / threads), threads, 0, L.stream>>>(
+      make_point<CELL, S>(a), static_cast<const S*>(dh_init));
+  cudaError_t e = cudaGetLastError();
+  launch_end(L);
+  return cuda_status(e);
+}
+}  // namespace
+
+int bwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, int bn, int splits,
+             const BwdStepArgs& a) {
+  if (cell == LSTM) return bwd_step_cell<LSTM>(L, mode, A, Bw, bn, splits, a);
+  if (cell == GRU) return bwd_step_cell<GRU>(L, mode, A, Bw, bn, splits, a);
+  return bwd_step_cell<TANH>(L, mode, A, Bw, bn, splits, a);
+}
+
+int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const void* dh_init) {
+  if (mode == 1) {
+    using S = __nv_bfloat16;
+    if (cell == LSTM) return point_launch<LSTM, S>(L, a, dh_init);
+    if (cell == GRU) return point_launch<GRU, S>(L, a, dh_init);
+    return point_launch<TANH, S>(L, a, dh_init);
+  }
+  if (cell == LSTM) return point_launch<LSTM, float>(L, a, dh_init);
+  if (cell == GRU) return point_launch<GRU, float>(L, a, dh_init);
+  return point_launch<TANH, float>(L, a, dh_init);
+}
+
+}  // namespace rnn

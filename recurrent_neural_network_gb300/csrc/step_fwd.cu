@@ -1,0 +1,55 @@
+// step_fwd.cu -- one forward timestep of one layer: the recurrent product
+// h_{t-1} W_h^T on the tensor cores (bf16) or FFMA (fp32) with the gate
+// non-linearities and the cell/state update fused into its epilogue.
+//
+// "Optimizing Performance of Recurrent Neural Networks on GPUs" (review page,
+// section "제안 방법"): grouped gate matrices make each step one larger
+// product; "Persistent RNNs" (citing snippet "pointwise OPs are very cheap")
+// motivates keeping the pointwise work inside the product's epilogue.
+#include "epilogues.cuh"
+#include "launch.cuh"
+
+namespace rnn {
+
+namespace {
+template <int CELL, class S>
+EpiFwdStep<CELL, S> make_epi(const FwdStepArgs& a) {
+  EpiFwdStep<CELL, S> e;
+  e.B = a.B;
+  e.H = a.H;
+  e.u = a.u;
+  e.P = a.P;
+  e.write_gates = a.write_gates;
+  e.bias_hn = a.bias_hn;
+  e.c_prev = a.c_prev;
+  e.c_out = a.c_out;
+  e.h_prev = static_cast<const S*>(a.h_prev);
+  e.h_out = static_cast<S*>(a.h_out);
+  e.y = static_cast<S*>(a.y);
+  e.hT = static_cast<S*>(a.hT);
+  e.cT = a.cT;
+  e.hn_out = a.hn_out;
+  return e;
+}
+}  // namespace
+
+int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, const FwdStepArgs& a) {
+  const int G = cell == LSTM ? 4 : cell == GRU ? 3 : 1;
+  const int M = a.B, N = G * a.H, K = a.H;
+  if (mode == 1) {
+    using S = __nv_bfloat16;
+    // the tile width is one packed block of G*u gate rows
+    if (cell == LSTM && a.u == 64) return launch_tc<256, 4>(L, A, Bw, M, N, K, 1, 0, make_epi<LSTM, S>(a));
+    if (cell == GRU && a.u == 64) return launch_tc<192, 5>(L, A, Bw, M, N, K, 1, 0, make_epi<GRU, S>(a));
+    if (cell == TANH && a.u == 128) return launch_tc<128, 6>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a));
+    if (cell == TANH && a.u == 64) return launch_tc<64, 8>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a));
+    return RNN_ERR_UNSUPPORTED;
+  }
+  using S = float;
+  if (cell == LSTM && a.u == 32) return launch_simt<128>(L, A, Bw, M, N, K, make_epi<LSTM, S>(a));
+  if (cell == GRU && a.u == 32) return launch_simt<96>(L, A, Bw, M, N, K, make_epi<GRU, S>(a));
+  if (cell == TANH && a.u == 32) return launch_simt<32>(L, A, Bw, M, N, K, make_epi<TANH, S>(a));
+  return RNN_ERR_UNSUPPORTED;
+}
+
+}  // namespace rnn

@@ -24,10 +24,11 @@ import dataclasses
 import math
 
 import numpy as np
+import torch
 
-_GAMMA = np.uint64(0x9E3779B97F4A7C15)
-_M1 = np.uint64(0xBF58476D1CE4E5B9)
-_M2 = np.uint64(0x94D049BB133111EB)
+_GAMMA = 0x9E3779B97F4A7C15
+_M1 = 0xBF58476D1CE4E5B9
+_M2 = 0x94D049BB133111EB
 
 CELL_LSTM, CELL_GRU, CELL_TANH = 0, 1, 2
 CELL_NAMES = {CELL_LSTM: "lstm", CELL_GRU: "gru", CELL_TANH: "tanh"}
@@ -38,38 +39,68 @@ MODE_FP32, MODE_BF16 = 0, 1
 TID_X, TID_H0, TID_C0, TID_DY, TID_DHT, TID_DCT = 1, 3, 4, 5, 6, 7
 
 
-def _mix(z):
-    z = (z ^ (z >> np.uint64(30))) * _M1
-    z = (z ^ (z >> np.uint64(27))) * _M2
-    return z ^ (z >> np.uint64(31))
+def _s64(v: int) -> int:
+    """Two's-complement int64 with the same 64 bits as the unsigned value v."""
+    v &= (1 << 64) - 1
+    return v - (1 << 64) if v >= (1 << 63) else v
 
 
-def _key(seed: int, tid: int) -> np.uint64:
-    with np.errstate(over="ignore"):
-        k = _mix(np.uint64(seed) + _GAMMA)
-        return _mix((k ^ np.uint64(tid)) + _GAMMA)
+def _mix_int(z: int) -> int:
+    m = (1 << 64) - 1
+    z = ((z ^ (z >> 30)) * _M1) & m
+    z = ((z ^ (z >> 27)) * _M2) & m
+    return z ^ (z >> 31)
+
+
+def _key(seed: int, tid: int) -> int:
+    m = (1 << 64) - 1
+    k = _mix_int((seed + _GAMMA) & m)
+    return _mix_int(((k ^ tid) + _GAMMA) & m)
+
+
+def _srl(z, k):
+    """Logical right shift of int64 tensors holding uint64 bit patterns."""
+    return (z >> k) & ((1 << (64 - k)) - 1)
+
+
+def _uniform_bits(key: int, start: int, count: int, device):
+    # int64 arithmetic wraps modulo 2^64 exactly like uint64
+    idx = torch.arange(start + 1, start + count + 1, dtype=torch.int64, device=device)
+    z = idx * _s64(_GAMMA) + _s64(key)
+    z = (z ^ _srl(z, 30)) * _s64(_M1)
+    z = (z ^ _srl(z, 27)) * _s64(_M2)
+    z = z ^ _srl(z, 31)
+    return _srl(z, 11)  # top 53 bits
+
+
+def uniform01_t(seed: int, tid: int, start: int, count: int, device="cpu"):
+    """U[0,1) float64 tensor for counters start .. start+count-1."""
+    return _uniform_bits(_key(seed, tid), start, count, device).to(torch.float64) * (1.0 / 9007199254740992.0)
 
 
 def uniform01(seed: int, tid: int, start: int, count: int) -> np.ndarray:
-    """U[0,1) doubles for counters start .. start+count-1."""
-    key = _key(seed, tid)
-    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
-    with np.errstate(over="ignore"):
-        z = _mix(key + idx * _GAMMA)
-    return (z >> np.uint64(11)).astype(np.float64) * (1.0 / 9007199254740992.0)
+    return uniform01_t(seed, tid, start, count).numpy()
 
 
-def uniform(seed, tid, shape, lo, hi, start=0):
+def uniform_t(seed, tid, shape, lo, hi, device="cpu"):
     n = int(np.prod(shape))
-    return (lo + (hi - lo) * uniform01(seed, tid, start, n)).reshape(shape)
+    return (lo + (hi - lo) * uniform01_t(seed, tid, 0, n, device)).reshape(shape)
 
 
-def normal(seed, tid, shape, std=1.0, start=0):
+def normal_t(seed, tid, shape, std=1.0, device="cpu"):
     n = int(np.prod(shape))
-    u = uniform01(seed, tid, 2 * start, 2 * n)
+    u = uniform01_t(seed, tid, 0, 2 * n, device)
     u1, u2 = u[0::2], u[1::2]
-    r = np.sqrt(-2.0 * np.log1p(-u1))
-    return (std * r * np.cos(2.0 * math.pi * u2)).reshape(shape)
+    r = torch.sqrt(-2.0 * torch.log1p(-u1))
+    return (std * r * torch.cos(2.0 * math.pi * u2)).reshape(shape)
+
+
+def uniform(seed, tid, shape, lo, hi):
+    return uniform_t(seed, tid, shape, lo, hi).numpy()
+
+
+def normal(seed, tid, shape, std=1.0):
+    return normal_t(seed, tid, shape, std).numpy()
 
 
 @dataclasses.dataclass(frozen=True)
@@ -180,10 +211,43 @@ def make_dstate(wl: Workload, which: str, dtype=np.float64):
     return normal(wl.seed, tid, (wl.layers, wl.B, wl.hidden)).astype(dtype)
 
 
-def round_bf16(a: np.ndarray) -> np.ndarray:
-    """Round doubles to the nearest bfloat16 (ties to even), returned as float64."""
-    f = np.asarray(a, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    u = (u + np.uint64(0x7FFF) + lsb) & np.uint64(0xFFFF0000)
-    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+def round_bf16(a) -> np.ndarray:
+    """Round to the nearest bfloat16 (via float32, ties to even), returned as float64."""
+    t = torch.as_tensor(np.asarray(a)).to(torch.float32).to(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def device_tensor(wl: Workload, what: str, device, dtype):
+    """Draw one input directly on `device` (same counters as the host arrays;
+    transcendental rounding of the normal transform may differ in the last
+    ulp).  what: "x", "dy", "h0", "c0", "w"."""
+    if what == "x":
+        shape = (wl.T, wl.B, wl.input)
+        if wl.x_dist == "uniform":
+            t = uniform_t(wl.seed, TID_X, shape, -1.0, 1.0, device)
+        else:
+            t = normal_t(wl.seed, TID_X, shape, device=device)
+    elif what == "dy":
+        t = normal_t(wl.seed, TID_DY, (wl.T, wl.B, wl.hidden), device=device)
+    elif what in ("h0", "c0"):
+        shape = (wl.layers, wl.B, wl.hidden)
+        if wl.state_std == 0.0:
+            t = torch.zeros(shape, dtype=torch.float64, device=device)
+        else:
+            t = normal_t(wl.seed, TID_H0 if what == "h0" else TID_C0, shape, std=wl.state_std, device=device)
+    elif what == "w":
+        parts = []
+        for l in range(wl.layers):
+            G, H, I = wl.G, wl.hidden, wl.in_size(l)
+            a = 1.0 / math.sqrt(H)
+            parts.append(uniform_t(wl.seed, 100 + 10 * l, (G * H * I,), -a, a, device).to(torch.float32))
+            parts.append(uniform_t(wl.seed, 100 + 10 * l + 1, (G * H * H,), -a, a, device).to(torch.float32))
+            bx = torch.zeros(G * H, dtype=torch.float32, device=device)
+            if wl.cell == CELL_LSTM and wl.forget_bias:
+                bx[H:2 * H] = wl.forget_bias
+            parts.append(bx)
+            parts.append(torch.zeros(G * H, dtype=torch.float32, device=device))
+        t = torch.cat(parts)
+    else:
+        raise ValueError(what)
+    return t.to(torch.float32).to(dtype)

@@ -1,0 +1,96 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C-ABI
+and the oracle on the same seeded inputs, and compare them with the stated
+tolerances.
+
+Tolerances (fixed by the benchmark definition of this path):
+  fp32 storage mode: max relative error <= 1e-4 on every output, with the
+    relative error of element i taken as |g_i - o_i| / max(|o_i|, 1e-3 max_j |o_j|)
+    (a floor is needed where outputs pass through zero);
+  bf16 storage mode: max absolute error <= 3e-2 on y, hT and cT, and relative
+    L2 error ||g - o|| / ||o|| <= 2e-2 on dx, dh0, dc0 and each weight /
+    bias gradient block.
+"""
+import numpy as np
+
+import oracle
+from recurrent_neural_network_gb300 import runner, synth
+
+FP32_MAX_REL = 1e-4
+BF16_MAX_ABS = 3e-2
+BF16_REL_L2 = 2e-2
+
+
+def run_oracle(hi: runner.HostInputs, train=True):
+    w = hi.wl
+    y, hT, cT = oracle.fwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0)
+    out = dict(y=y, hT=hT, cT=cT)
+    if train:
+        dx, dh0, dc0, dw = oracle.bwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, hi.dy, h0=hi.h0,
+                                      c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT)
+        out.update(dx=dx, dh0=dh0, dc0=dc0, dw=dw)
+    return out
+
+
+def run_gpu(wl, hi, flags=0, chunk=0, train=None, timeout_ns=0, repeat=1):
+    r = runner.Runner(wl, flags=flags, chunk=chunk, timeout_ns=timeout_ns)
+    r.upload(hi)
+    train = wl.training if train is None else train
+    for _ in range(repeat):
+        if train:
+            r.forward(True)
+            r.backward()
+            r.weights()
+        else:
+            r.forward(False)
+    st = r.status()
+    assert st == 0, f"device status {st}"
+    return r.outputs()
+
+
+def max_rel(g, o):
+    g = np.asarray(g, np.float64).ravel()
+    o = np.asarray(o, np.float64).ravel()
+    floor = 1e-3 * max(np.abs(o).max(), 1e-30)
+    return float((np.abs(g - o) / np.maximum(np.abs(o), floor)).max())
+
+
+def rel_l2(g, o):
+    g = np.asarray(g, np.float64).ravel()
+    o = np.asarray(o, np.float64).ravel()
+    n = np.linalg.norm(o)
+    return float(np.linalg.norm(g - o) / n) if n > 0 else float(np.linalg.norm(g))
+
+
+def weight_blocks(wl, dw):
+    """(name, array) per layer and part of a user-layout gradient vector."""
+    out = []
+    for l, parts in enumerate(oracle.split_weights(wl.cell, wl.layers, wl.input, wl.hidden, dw)):
+        for nm, a in zip(("dWx", "dWh", "dbx", "dbh"), parts):
+            out.append((f"l{l}.{nm}", a))
+    return out
+
+
+def compare(wl, g, o, keys=None, report=None):
+    """Assert parity of every output both sides produced; returns the error table."""
+    errs = {}
+    keys = keys or [k for k in ("y", "hT", "cT", "dx", "dh0", "dc0") if o.get(k) is not None and g.get(k) is not None]
+    for k in keys:
+        if wl.mode == synth.MODE_FP32:
+            errs[k] = ("max_rel", max_rel(g[k], o[k]), FP32_MAX_REL)
+        elif k in ("y", "hT", "cT"):
+            errs[k] = ("max_abs", float(np.abs(g[k] - o[k]).max()), BF16_MAX_ABS)
+        else:
+            errs[k] = ("rel_l2", rel_l2(g[k], o[k]), BF16_REL_L2)
+    if g.get("dw") is not None and o.get("dw") is not None:
+        for (nm, ga), (_, oa) in zip(weight_blocks(wl, g["dw"]), weight_blocks(wl, o["dw"])):
+            if not np.any(oa) and not np.any(ga):
+                continue
+            if wl.mode == synth.MODE_FP32:
+                errs[nm] = ("max_rel", max_rel(ga, oa), FP32_MAX_REL)
+            else:
+                errs[nm] = ("rel_l2", rel_l2(ga, oa), BF16_REL_L2)
+    if report is not None:
+        report.update(errs)
+    bad = {k: v for k, v in errs.items() if not (v[1] <= v[2])}
+    assert not bad, f"parity failed: {bad}"
+    return errs

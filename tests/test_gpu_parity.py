@@ -1,0 +1,128 @@
+"""CUDA path vs the double-precision oracle, element by element, on the same
+seeded inputs: tiny shapes of every cell in both storage modes (several
+tiles, ragged edges, multi-chunk wavefront), the five benchmark workloads
+(in full where the oracle finishes in seconds, otherwise on sampled batch
+columns at full size), and the edge cases of the method."""
+import numpy as np
+import pytest
+
+from recurrent_neural_network_gb300 import rnn, runner, synth
+
+from parity import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+TINY = {
+    # mode: (L, T, B, I, H)
+    synth.MODE_FP32: (2, 5, 3, 40, 64),
+    synth.MODE_BF16: (2, 5, 3, 72, 128),
+}
+
+
+def tiny(cell, mode, **kw):
+    L, T, B, I, H = TINY[mode]
+    base = dict(name="tiny", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
+                forget_bias=1.0, state_std=0.3)
+    base.update(kw)
+    return synth.Workload(**base)
+
+
+@pytest.mark.parametrize("mode", [synth.MODE_FP32, synth.MODE_BF16], ids=["fp32", "bf16"])
+@pytest.mark.parametrize("cell", [0, 1, 2], ids=["lstm", "gru", "tanh"])
+@pytest.mark.parametrize("chunk", [0, 2], ids=["chunkauto", "chunk2"])
+def test_tiny_all_outputs(cell, mode, chunk):
+    wl = tiny(cell, mode)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    g = run_gpu(wl, hi, chunk=chunk)
+    o = run_oracle(hi)
+    compare(wl, g, o)
+
+
+@pytest.mark.parametrize("cell", [0, 1, 2], ids=["lstm", "gru", "tanh"])
+def test_layer_by_layer_equals_wavefront(cell):
+    wl = tiny(cell, synth.MODE_BF16, layers=3, T=7)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    a = run_gpu(wl, hi, chunk=2)
+    b = run_gpu(wl, hi, flags=rnn.FLAG_NO_WAVEFRONT)
+    for k in a:
+        if a[k] is not None:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+@pytest.mark.parametrize("cell", [0, 1], ids=["lstm", "gru"])
+def test_ragged_batch_and_input(cell):
+    """B = 130 spans two 128-row tiles with a ragged tail; I = 72 is not a multiple of 64."""
+    wl = synth.Workload("ragged", cell, 2, 3, 130, 72, 128, synth.MODE_BF16, forget_bias=1.0, state_std=0.2)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    compare(wl, run_gpu(wl, hi), run_oracle(hi))
+
+
+def test_single_step_and_single_row():
+    wl = synth.Workload("t1b1", 0, 1, 1, 1, 64, 64, synth.MODE_BF16, forget_bias=1.0, state_std=0.5)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    compare(wl, run_gpu(wl, hi), run_oracle(hi))
+
+
+def test_zero_input_zero_state_zero_bias_stays_exactly_zero():
+    wl = synth.Workload("zeros", 0, 2, 4, 8, 64, 64, synth.MODE_BF16)
+    hi = runner.HostInputs(wl)
+    hi.x[:] = 0
+    g = run_gpu(wl, hi)
+    assert not np.any(g["y"]) and not np.any(g["hT"]) and not np.any(g["cT"])
+
+
+def test_repeated_calls_are_deterministic():
+    wl = tiny(0, synth.MODE_BF16, B=9)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    a = run_gpu(wl, hi)
+    b = run_gpu(wl, hi, repeat=2)
+    for k in a:
+        if a[k] is not None:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
+# ---------------------------------------------------------------- benchmark workloads
+
+def test_workload_lstm_fp32_tiny():
+    wl = synth.WORKLOADS[0]
+    hi = runner.HostInputs(wl)
+    compare(wl, run_gpu(wl, hi), run_oracle(hi))
+
+
+def test_workload_lstm_h512_training():
+    wl = synth.WORKLOADS[1]
+    hi = runner.HostInputs(wl)
+    compare(wl, run_gpu(wl, hi), run_oracle(hi))
+
+
+def test_workload_lstm_b4_inference():
+    wl = synth.WORKLOADS[2]
+    hi = runner.HostInputs(wl)
+    compare(wl, run_gpu(wl, hi), run_oracle(hi, train=False))
+
+
+def masked_columns_check(wl, cols):
+    """Full-size run with dy zero outside `cols`; forward outputs, data
+    gradients and weight gradients of those columns against the oracle run on
+    them alone (sequences are independent; dW sums over columns)."""
+    hi = runner.HostInputs(wl)
+    mask = np.zeros(wl.B, bool)
+    mask[cols] = True
+    hi.dy[:, ~mask] = 0
+    g = run_gpu(wl, hi)
+    sub = hi.columns(cols)
+    o = run_oracle(sub)
+    gs = dict(y=g["y"][:, cols], hT=g["hT"][:, cols], cT=None if g["cT"] is None else g["cT"][:, cols],
+              dx=g["dx"][:, cols], dh0=g["dh0"][:, cols], dc0=None if g["dc0"] is None else g["dc0"][:, cols],
+              dw=g["dw"])
+    compare(sub.wl, gs, o)
+    # columns without upstream gradient get exactly zero data gradients
+    assert not np.any(g["dx"][:, ~mask])
+
+
+def test_workload_lstm_h4096_sampled_columns():
+    masked_columns_check(synth.WORKLOADS[3], [0, 201])
+
+
+def test_workload_gru_8layer_sampled_columns():
+    masked_columns_check(synth.WORKLOADS[4], [5, 31])

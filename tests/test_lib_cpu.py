@@ -1,0 +1,86 @@
+"""Host-side checks of librnn that need no GPU: it builds, loads, exports every
+symbol include/rnn.h declares, plans buffer sizes, and rejects bad arguments
+before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from recurrent_neural_network_gb300 import build, rnn, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return rnn.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "rnn.h")).read()
+    return sorted(set(re.findall(r"RNN_API\s+[\w\s\*]+?\b(rnn_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 13
+    assert set(names) == set(rnn.SYMBOLS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror(lib):
+    assert lib.rnn_strerror(0) == b"ok"
+    assert lib.rnn_strerror(-5).startswith(b"a bounded")
+
+
+def test_rejects_bad_descriptors(lib):
+    ok = dict(cell=0, layers=1, T=4, B=2, input=64, hidden=64, mode=1)
+    for bad in [dict(cell=3), dict(layers=0), dict(T=0), dict(B=0), dict(hidden=0), dict(mode=2)]:
+        d = dict(ok, **bad)
+        with pytest.raises(rnn.RnnError) as e:
+            rnn.RNN(**d)
+        assert e.value.code == -1
+    for unsup in [dict(hidden=96), dict(input=12), dict(mode=0, hidden=48)]:
+        with pytest.raises(rnn.RnnError) as e:
+            rnn.RNN(**dict(ok, **unsup))
+        assert e.value.code == -2
+    with pytest.raises(rnn.RnnError):
+        rnn.RNN(**ok, flags=rnn.FLAG_FORCE_PERSISTENT | rnn.FLAG_FORCE_STREAMING)
+
+
+@pytest.mark.parametrize("wl", synth.WORKLOADS, ids=lambda w: w.name)
+def test_buffer_sizes_cover_the_layouts(lib, wl):
+    r = rnn.RNN.for_workload(wl)
+    s = r.sizes()
+    e = 2 if wl.mode == 1 else 4
+    assert s["user_weights"] == wl.weight_count() * e
+    G, L, T, B, H = wl.G, wl.layers, wl.T, wl.B, wl.hidden
+    # reserve holds at least: gates (f32) + h sequence (T+1 slots) + gate gradients, per layer
+    floor = L * (T * B * G * H * 4 + (T + 1) * B * H * e + T * B * G * H * e)
+    assert s["reserve"] >= floor
+    mats = sum(G * H * (wl.in_size(l) + H) for l in range(L))
+    assert s["packed_weights"] >= mats * e + L * G * H * 4   # matrices in storage type + float biases
+    assert "wavefront=%d" % (1 if L > 1 else 0) in r.describe()
+
+
+def test_calls_validate_arguments_before_any_device_work(lib):
+    r = rnn.RNN(0, 1, 4, 2, 64, 64, 1)
+    H = r.h
+    assert lib.rnn_fwd(H, None, None, None, None, None, None, None, None, None, None) == -1
+    assert lib.rnn_bwd_data(H, *([None] * 12)) == -1
+    assert lib.rnn_bwd_weights(H, None, None, None, None, 0, None, None) == -1
+    # misaligned pointer
+    assert lib.rnn_fwd(H, ctypes.c_void_p(0x1001), None, None, ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000),
+                       None, None, None, ctypes.c_void_p(0x4000), None) == -1
+    assert lib.rnn_gemm_bf16(0, 1, 1, None, 8, 0, None, 8, 0, None, 1, None, 0, None) == -1
+    assert lib.rnn_get_sizes(None, None, None, None, None) == -1
+
+
+def test_wavefront_chunking_plan(lib):
+    r = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, chunk=5)
+    assert "chunk=5 nchunks=10" in r.describe()
+    r = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, flags=rnn.FLAG_NO_WAVEFRONT)
+    assert "wavefront=0 chunk=50 nchunks=1" in r.describe()
