@@ -151,14 +151,57 @@ def run_reference(args, wl, rank):
     print(json.dumps(line), flush=True)
 
 
+def e2e_run(R, wl, steps, sdt, stream, barrier):
+    """The same step through the public API with the inputs in pinned host
+    memory: host->device copies of x (and dy) and a device->host read of hT
+    inside the timed region."""
+    hx = torch.empty(R.x.shape, dtype=sdt, pin_memory=True)
+    hx.copy_(R.x)
+    hdy = None
+    if wl.training:
+        hdy = torch.empty(R.dy.shape, dtype=sdt, pin_memory=True)
+        hdy.copy_(R.dy)
+    hout = torch.empty(R.hT.shape, dtype=R.hT.dtype, pin_memory=True)
+    h2d = hx.numel() * hx.element_size() + (hdy.numel() * hdy.element_size() if hdy is not None else 0)
+    d2h = hout.numel() * hout.element_size()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        R.x.copy_(hx, non_blocking=True)
+        if hdy is not None:
+            R.dy.copy_(hdy, non_blocking=True)
+        R.step()
+        hout.copy_(R.hT, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def roofline(prof, wl, steps, pk):
+    """Roofline of the dominant kernel class: algorithmic flops per launch over
+    its average CUDA-event launch duration in the timed region."""
+    cf = class_flops(wl)
+    cand = [(k, v) for k, v in prof.items() if k in cf and v[0] > 0]
+    if not cand:
+        return None
+    name, (n, tot) = max(cand, key=lambda kv: kv[1][1])
+    achieved = cf[name] * steps / (tot * 1e-3) / 1e12
+    return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
+            "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
+            "launches_per_step": n // steps, "flops_per_launch": cf[name] * steps / n,
+            "ms_per_launch": tot / n, "peak_source": pk["source"] + " (sustained bf16, kernel timed inside the step)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--chunk", type=int, default=0)
     args = ap.parse_args()
@@ -181,8 +224,7 @@ def main():
     from recurrent_neural_network_gb300 import build, rnn, runner
     build.build()
     dev = torch.device("cuda", local)
-    flags = args.flags | rnn.FLAG_PROFILE
-    R = runner.Runner(wl, device=dev, flags=flags, chunk=args.chunk)
+    R = runner.Runner(wl, device=dev, flags=args.flags | rnn.FLAG_PROFILE, chunk=args.chunk)
     sdt = R.dt
     R.x = synth.device_tensor(wl, "x", dev, sdt)
     R.w_user = synth.device_tensor(wl, "w", dev, sdt)
@@ -206,15 +248,25 @@ def main():
     clocks = Clocks(local)
     barrier()
     clocks.start()
+    time.sleep(0.25)
     n_launch0 = rnn.launch_count()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        R.step()
-    ev1.record(stream)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        # phase boundaries on the caller's stream: forward | BPTT | weight gradients
+        ev[i][0].record(stream)
+        R.forward()
+        ev[i][1].record(stream)
+        if wl.training:
+            R.backward()
+        ev[i][2].record(stream)
+        if wl.training:
+            R.weights()
+        ev[i][3].record(stream)
     barrier()
     launches = rnn.launch_count() - n_launch0
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = ev[0][0].elapsed_time(ev[-1][3]) / args.steps
+    phases = {nm: statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev)
+              for k, nm in enumerate(["fwd", "bwd_data", "bwd_weights"])}
     clk = clocks.stop()
     prof = R.r.profile(reset=True)
     st = R.status()
@@ -227,42 +279,11 @@ def main():
     fl = step_flops(wl)
     tflops = world * fl / (ms * 1e-3) / 1e12
     pk = peaks()
-
-    # roofline of the dominant kernel class
-    cf = class_flops(wl)
-    dom = max(prof.items(), key=lambda kv: kv[1][1]) if prof else None
-    roof = None
-    if dom and dom[0] in cf:
-        name, (n, tot) = dom
-        per_launch_flops = cf[name] * args.steps / max(n, 1)
-        achieved = cf[name] * args.steps / (tot * 1e-3) / 1e12
-        roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
-                "launches": n // args.steps, "flops_per_launch": per_launch_flops,
-                "ms_per_launch": tot / max(n, 1), "peak_source": pk["source"] + " sustained"}
-
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
-    hx = torch.empty(R.x.shape, dtype=sdt, pin_memory=True)
-    hx.copy_(R.x)
-    hdy = None
-    if wl.training:
-        hdy = torch.empty(R.dy.shape, dtype=sdt, pin_memory=True)
-        hdy.copy_(R.dy)
-    hout = torch.empty(R.hT.shape, dtype=R.hT.dtype, pin_memory=True)
-    h2d = hx.numel() * hx.element_size() + (hdy.numel() * hdy.element_size() if hdy is not None else 0)
-    d2h = hout.numel() * hout.element_size()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        R.x.copy_(hx, non_blocking=True)
-        if hdy is not None:
-            R.dy.copy_(hdy, non_blocking=True)
-        R.step()
-        hout.copy_(R.hT, non_blocking=True)
-    e1.record(stream)
-    barrier()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
+    roof = roofline(prof, wl, args.steps, pk)
+    if args.no_e2e:
+        ms_e2e, h2d, d2h = float("nan"), 0, 0
+    else:
+        ms_e2e, h2d, d2h = e2e_run(R, wl, args.steps, sdt, stream, barrier)
     R.r.profile(reset=True)
 
     if rank != 0:
@@ -274,6 +295,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if wl.mode == 1 else "f32", "data": "synthetic",
         "timesteps_per_s": world * wl.T / (ms * 1e-3),
+        "tensor_peak_frac": {"of_measured_burst": tflops / world / pk["bf16_tflops"],
+                             "of_measured_sustained": tflops / world / pk["bf16_tflops_sustained"]},
         "config": {"workload": wl.name, "cell": synth.CELL_NAMES[wl.cell], "layers": wl.layers, "T": wl.T,
                    "B": wl.B, "input": wl.input, "hidden": wl.hidden, "training": wl.training,
                    "flops_per_step": fl, "plan": R.r.describe(),
@@ -283,6 +306,7 @@ def main():
         "clocks": clk,
         "e2e": {"value": world * fl / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "phases_ms": phases,
         "kernels": {k: {"launches": v[0] // args.steps, "ms_per_step": v[1] / args.steps} for k, v in prof.items()},
     }
     if world == 1 and not args.no_cpu_baseline:

@@ -119,6 +119,8 @@ struct rnn_s {
   struct PL { size_t wx, wh, bias, bias_hn; };
   struct RL { size_t gates, c, hn, hseq, dgx, dgh; };
   struct WL { size_t P, hseq, c2, dyab, carry, part, ctr; };
+  size_t ws_bias = 0;  // bias-gradient slices (shared by the layers, used one layer at a time)
+  int bias_slices = 1;
   struct UL { size_t wx, wh, bx, bh; };  // element offsets in the user weight vector
   std::vector<PL> pl;
   std::vector<RL> rl;
@@ -224,6 +226,8 @@ int plan_and_layout(rnn_s* h) {
   h->wl.resize(L);
   cur = 0;
   h->ws_err = take(cur, 256);
+  h->bias_slices = std::max(1, std::min(64, (T * B + 255) / 256));
+  h->ws_bias = take(cur, (size_t)h->bias_slices * GH * 4);
   for (int l = 0; l < L; ++l) {
     h->wl[l].P = take(cur, (size_t)T * BGH * 4);
     h->wl[l].hseq = take(cur, (size_t)(T + 1) * BH * e);
@@ -593,24 +597,24 @@ int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* r
   const size_t e = h->elem, BH = (size_t)B * H;
   const char* R = static_cast<const char*>(reserve);
   const int TB = T * B;
-  const bool multi = L > 1;
-  if (multi) RNN_TRY(fork_streams(h, stream));
+  // Each weight-gradient product has (G*H / 128) x (I_l / 256) tiles over
+  // K = T*B and fills the GPU by itself: the products run back to back on the
+  // caller's stream.
   for (int l = 0; l < L; ++l) {
-    cudaStream_t s = multi ? h->streams[l] : stream;
     const int In = h->In(l);
     Remap rm{1, G, h->u, H};
     Operand dgx{R + h->rl[l].dgx, GH, 1, GH, TB};
     Operand dgh{R + h->rl[l].dgh, GH, 1, GH, TB};
     Operand X = l == 0 ? Operand{x, In, 1, In, TB} : Operand{R + h->rl[l - 1].hseq + BH * e, H, 1, H, TB};
     Operand Hp{R + h->rl[l].hseq, H, 1, H, TB};
-    Launch Lk = mk(h, s, ws, "dw_gemm");
+    Launch Lk = mk(h, stream, ws, "dw_gemm");
     RNN_TRY(gemm_f32(Lk, mode, dgx, X, GH, In, TB, dw + h->ul[l].wx, In, nullptr, accumulate, rm, 0));
     RNN_TRY(gemm_f32(Lk, mode, dgh, Hp, GH, H, TB, dw + h->ul[l].wh, H, nullptr, accumulate, rm, 0));
-    Launch Lb = mk(h, s, ws, "bias_grad");
+    Launch Lb = mk(h, stream, ws, "bias_grad");
     RNN_TRY(bias_grad(Lb, mode, d.cell, H, h->u, TB, R + h->rl[l].dgx, R + h->rl[l].dgh, dw + h->ul[l].bx,
-                      dw + h->ul[l].bh, accumulate));
+                      dw + h->ul[l].bh, accumulate, reinterpret_cast<float*>(static_cast<char*>(ws) + h->ws_bias),
+                      h->bias_slices));
   }
-  if (multi) RNN_TRY(join_streams(h, stream));
   return RNN_OK;
 }
 

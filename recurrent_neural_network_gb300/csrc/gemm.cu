@@ -95,58 +95,84 @@ int pack_layer(const Launch& L, int mode, int cell, int H, int In, int u, const 
 }
 
 // ---------------------------------------------------------------- bias gradient
-// db[user col] = sum over rows of dG[row][packed col]; 32 packed columns per
-// block, 8 row groups reduced through shared memory.
+// db[user col] = sum over rows of dG[row][packed col].  Pass 1: each block
+// owns 256 packed columns (32 lanes x 8 columns, 16-byte loads) and one slice
+// of rows, its 8 warps stride the slice and reduce through shared memory into
+// a per-slice partial.  Pass 2 sums the slices in a fixed order, so the result
+// is deterministic.
 template <class S>
-__global__ void bias_grad_kernel(const S* __restrict__ dgx, const S* __restrict__ dgh, float* __restrict__ dbx,
-                                 float* __restrict__ dbh, long long rows, int G, int H, int u, int accumulate) {
-  __shared__ float sx[8][33], sh[8][33];
-  const int GH = G * H;
-  const int p = blockIdx.x * 32 + threadIdx.x;
-  float ax = 0.f, ah = 0.f;
-  if (p < GH) {
-    for (long long r = threadIdx.y; r < rows; r += 8) {
-      ax += to_f32(dgx[r * GH + p]);
-      ah += to_f32(dgh[r * GH + p]);
+__global__ void bias_part_kernel(const S* __restrict__ dg, float* __restrict__ part, long long rows, int GH,
+                                 long long rows_per_slice) {
+  __shared__ float red[8][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 256 + lane * 8;
+  const long long r0 = (long long)blockIdx.y * rows_per_slice;
+  const long long r1 = min(rows, r0 + rows_per_slice);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (c0 < GH) {
+    for (long long r = r0 + warp; r < r1; r += 8) {
+      const S* p = dg + r * GH + c0;
+      if (sizeof(S) == 2) {
+        uint4 u = *reinterpret_cast<const uint4*>(p);
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[2 * k] += __uint_as_float(w[k] << 16);
+          acc[2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += to_f32(p[i]);
+      }
     }
   }
-  sx[threadIdx.y][threadIdx.x] = ax;
-  sh[threadIdx.y][threadIdx.x] = ah;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = acc[i];
   __syncthreads();
-  if (threadIdx.y == 0 && p < GH) {
-    float tx = 0.f, th = 0.f;
-    for (int i = 0; i < 8; ++i) {
-      tx += sx[i][threadIdx.x];
-      th += sh[i][threadIdx.x];
-    }
-    const int blk = p / (G * u), r = p % (G * u);
-    const int ur = (r / u) * H + blk * u + (r % u);
-    if (accumulate) {
-      dbx[ur] += tx;
-      dbh[ur] += th;
-    } else {
-      dbx[ur] = tx;
-      dbh[ur] = th;
-    }
-  }
+  const int c = threadIdx.x;  // 256 threads: one column each
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t += red[w][c];
+  const int col = blockIdx.x * 256 + c;
+  if (col < GH) part[(size_t)blockIdx.y * GH + col] = t;
+}
+
+__global__ void bias_final_kernel(const float* __restrict__ part, int slices, int G, int H, int u,
+                                  float* __restrict__ db, int accumulate) {
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  const int GH = G * H;
+  if (p >= GH) return;
+  float t = 0.f;
+  for (int s = 0; s < slices; ++s) t += part[(size_t)s * GH + p];
+  const int blk = p / (G * u), r = p % (G * u);
+  const int ur = (r / u) * H + blk * u + (r % u);
+  db[ur] = accumulate ? db[ur] + t : t;
 }
 
 int bias_grad(const Launch& L, int mode, int cell, int H, int u, long long rows, const void* dgx, const void* dgh,
-              float* dbx, float* dbh, int accumulate) {
+              float* dbx, float* dbh, int accumulate, float* part, int slices) {
   const int G = cell == LSTM ? 4 : cell == GRU ? 3 : 1;
-  dim3 grid((G * H + 31) / 32), block(32, 8);
+  const int GH = G * H;
+  if (GH % 8 || slices < 1) return RNN_ERR_INVALID_ARG;
+  const long long per = (rows + slices - 1) / slices;
+  dim3 grid((GH + 255) / 256, slices);
   launch_begin(L);
-  if (mode == 1) {
-    using S = __nv_bfloat16;
-    bias_grad_kernel<S><<<grid, block, 0, L.stream>>>(static_cast<const S*>(dgx), static_cast<const S*>(dgh), dbx,
-                                                      dbh, rows, G, H, u, accumulate);
-  } else {
-    using S = float;
-    bias_grad_kernel<S><<<grid, block, 0, L.stream>>>(static_cast<const S*>(dgx), static_cast<const S*>(dgh), dbx,
-                                                      dbh, rows, G, H, u, accumulate);
+  int n = 0;
+  for (int which = 0; which < 2; ++which) {
+    const void* dg = which == 0 ? dgx : dgh;
+    float* db = which == 0 ? dbx : dbh;
+    if (mode == 1)
+      bias_part_kernel<__nv_bfloat16><<<grid, 256, 0, L.stream>>>(static_cast<const __nv_bfloat16*>(dg), part, rows,
+                                                                  GH, per);
+    else
+      bias_part_kernel<float><<<grid, 256, 0, L.stream>>>(static_cast<const float*>(dg), part, rows, GH, per);
+    bias_final_kernel<<<(GH + 255) / 256, 256, 0, L.stream>>>(part, slices, G, H, u, db, accumulate);
+    n += 2;
   }
   cudaError_t e = cudaGetLastError();
-  launch_end(L);
+  launch_end(L, n);
   return cuda_status(e);
 }
 

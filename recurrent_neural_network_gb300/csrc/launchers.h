@@ -52,9 +52,10 @@ int pack_layer(const Launch& L, int mode, int cell, int H, int In, int u, const 
                const void* bx, const void* bh, void* pwx, void* pwh, float* pbias, float* pbias_hn);
 
 // column sums over `rows` rows of the gate-gradient matrices into user-layout
-// bias gradients (gate blocks of H).  dgh may equal dgx.
+// bias gradients (gate blocks of H).  dgh may equal dgx.  part: scratch of
+// slices * G*H floats.
 int bias_grad(const Launch& L, int mode, int cell, int H, int u, long long rows, const void* dgx, const void* dgh,
-              float* dbx, float* dbh, int accumulate);
+              float* dbx, float* dbh, int accumulate, float* part, int slices);
 
 // ---------------------------------------------------------------- step_fwd.cu
 struct FwdStepArgs {
