@@ -182,6 +182,31 @@ RNN_API int rnn_gemm_bf16(int M, int N, int K, const void* A, long long lda, int
                   const void* B, long long ldb, int b_mn_major, float* D, long long ldd,
                   const float* bias, int accumulate, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Bias gradients with no workspace and no allocation.  The paper has no
+ * counterpart; this exists for callers that cannot allocate device memory
+ * when they need the result: for example a host framework that hands a
+ * plugin fixed input/output buffers only and forbids cudaMalloc after
+ * start-up (it synchronizes the device and can fail under memory pressure),
+ * so there is no room for the workspace rnn_bwd_weights takes.
+ *
+ * Computes db_x and db_h of every layer from the gate gradients that
+ * rnn_bwd_data left in `reserve`, and writes them into `dw` (user layout,
+ * float) at the same places rnn_bwd_weights does; dW_x and dW_h in `dw` are
+ * not touched.  accumulate != 0 adds instead of overwriting.
+ *
+ * Scratch: a fixed array of RNN_BIAS_STATIC_FLOATS floats (4 MiB) inside
+ * the library, held by every GPU that loads it until the process exits.
+ * G*hidden must not exceed RNN_BIAS_STATIC_FLOATS (RNN_ERR_UNSUPPORTED).
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the one array: calls that overlap on the GPU (other streams, other
+ * handles) race and must be ordered by the caller.
+ * ---------------------------------------------------------------------- */
+#define RNN_BIAS_STATIC_FLOATS (1 << 20)
+RNN_API int rnn_bias_grad_static(rnn_handle_t h, const void* reserve, float* dw, int accumulate,
+                                 cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

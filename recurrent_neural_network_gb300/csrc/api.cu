@@ -678,3 +678,52 @@ int rnn_gemm_bf16(int M, int N, int K, const void* A, long long lda, int a_mn_ma
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- bias gradients without allocation
+// The per-slice partial sums of the bias-gradient reduction live in this fixed
+// device array instead of the caller's workspace.  Host code may not pass the
+// symbol itself to a kernel (on the host it is only a stand-in); the device
+// address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) float g_bias_static[RNN_BIAS_STATIC_FLOATS];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+float* g_static_ptr[kMaxDevices] = {};
+
+int static_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RNN_ERR_CUDA;
+  std::lock_guard<std::mutex> g(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bias_static) != cudaSuccess || !p) return RNN_ERR_CUDA;
+    g_static_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return RNN_OK;
+}
+}  // namespace
+
+extern "C" int rnn_bias_grad_static(rnn_handle_t h, const void* reserve, float* dw, int accumulate,
+                                    cudaStream_t stream) {
+  if (!h || !reserve || !dw || !aligned16(reserve) || !aligned16(dw)) return RNN_ERR_INVALID_ARG;
+  const rnn_desc_t& d = h->d;
+  const int GH = h->GH;
+  if ((long long)GH > (long long)RNN_BIAS_STATIC_FLOATS) return RNN_ERR_UNSUPPORTED;
+  if (!h->have_device) return RNN_ERR_CUDA;
+  float* part = nullptr;
+  RNN_TRY(static_scratch(&part));
+  // every slice entry is written before it is read: nothing needs clearing
+  const long long TB = (long long)d.T * d.B;
+  int slices = (int)std::min<long long>(64, (TB + 255) / 256);
+  slices = std::max(1, std::min(slices, RNN_BIAS_STATIC_FLOATS / GH));
+  const char* R = static_cast<const char*>(reserve);
+  for (int l = 0; l < d.layers; ++l) {
+    Launch Lb = mk(h, stream, nullptr, "bias_grad_static");
+    Lb.prof = nullptr;
+    RNN_TRY(bias_grad(Lb, d.mode, d.cell, d.hidden, h->u, TB, R + h->rl[l].dgx, R + h->rl[l].dgh,
+                      dw + h->ul[l].bx, dw + h->ul[l].bh, accumulate, part, slices));
+  }
+  return RNN_OK;
+}

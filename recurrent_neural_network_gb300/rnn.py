@@ -26,7 +26,8 @@ FLAG_PROFILE = 0x8
 # every symbol include/rnn.h declares
 SYMBOLS = ["rnn_create", "rnn_destroy", "rnn_get_sizes", "rnn_pack_weights", "rnn_fwd", "rnn_bwd_data",
            "rnn_bwd_weights", "rnn_sync_status", "rnn_strerror", "rnn_describe", "rnn_launch_count",
-           "rnn_profile_query", "rnn_gemm_bf16"]
+           "rnn_profile_query", "rnn_gemm_bf16", "rnn_bias_grad_static"]
+BIAS_STATIC_FLOATS = 1 << 20
 
 
 class RnnError(RuntimeError):
@@ -71,6 +72,7 @@ def load(path: str = LIB_PATH):
                                       ctypes.POINTER(ctypes.c_double), ci]
     lib.rnn_gemm_bf16.argtypes = [ci, ci, ci, vp, ctypes.c_longlong, ci, vp, ctypes.c_longlong, ci, vp,
                                   ctypes.c_longlong, vp, ci, vp]
+    lib.rnn_bias_grad_static.argtypes = [H, vp, vp, ci, vp]
     for name in SYMBOLS:
         if name != "rnn_strerror" and name != "rnn_launch_count":
             getattr(lib, name).restype = ci
@@ -161,6 +163,11 @@ class RNN:
     def bwd_weights(self, x, reserve, dw, ws, h0=None, accumulate=False, stream=None):
         check(self.lib.rnn_bwd_weights(self.h, _ptr(x), _ptr(h0), _ptr(reserve), _ptr(dw), int(accumulate), _ptr(ws),
                                        _stream(stream)), "rnn_bwd_weights")
+
+    def bias_grad_static(self, reserve, dw, accumulate=False, stream=None):
+        """Bias gradients into dw using the library's fixed scratch array (no workspace)."""
+        check(self.lib.rnn_bias_grad_static(self.h, _ptr(reserve), _ptr(dw), int(accumulate), _stream(stream)),
+              "rnn_bias_grad_static")
 
     def sync_status(self, ws, stream=None) -> int:
         return int(self.lib.rnn_sync_status(self.h, _ptr(ws), _stream(stream)))
