@@ -113,6 +113,7 @@ struct rnn_s {
   int have_device = 0;
   // plan
   int chunk = 1, nch = 1, wavefront = 0, bwd_bn = 128, bwd_splits = 1;
+  int persist = 0, persist_ctas = 0;  // forward recurrence kind: 1 = persistent (one launch per layer)
   uint64_t limit_ns = 2000000000ull;
   // sizes (bytes)
   size_t user_w_bytes = 0, packed_bytes = 0, reserve_bytes = 0, ws_bytes = 0;
@@ -164,8 +165,20 @@ int plan_and_layout(rnn_s* h) {
   }
   h->limit_ns = d.timeout_ns > 0 ? (uint64_t)d.timeout_ns : 2000000000ull;
 
+  // persistent recurrence for small batches (weights on-chip, one launch per
+  // layer); it runs layer after layer, so it replaces the wavefront.
+  if (d.mode == RNN_MODE_BF16 && !(d.flags & RNN_FLAG_FORCE_STREAMING)) {
+    int ctas = 0;
+    const bool fits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &ctas) == RNN_OK
+                                     : (B <= 8 && H % 128 == 0 && H <= (d.cell == RNN_GRU ? 512 : d.cell == RNN_LSTM ? 1024 : 2048));
+    if (fits) {
+      h->persist = 1;
+      h->persist_ctas = ctas;
+    }
+  }
+  if ((d.flags & RNN_FLAG_FORCE_PERSISTENT) && !h->persist) return RNN_ERR_UNSUPPORTED;
   // wavefront chunking
-  h->wavefront = (L > 1) && !(d.flags & RNN_FLAG_NO_WAVEFRONT);
+  h->wavefront = (L > 1) && !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !h->persist;
   if (!h->wavefront) h->chunk = T;
   else if (d.chunk > 0) h->chunk = std::min(d.chunk, T);
   else h->chunk = std::max(1, (T + 7) / 8);
@@ -369,10 +382,10 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   if (!h || !buf || len == 0) return RNN_ERR_INVALID_ARG;
   const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : "tanh";
   snprintf(buf, len,
-           "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=streaming engine=%s wavefront=%d "
+           "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
            "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
-           h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->num_sms);
+           h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->num_sms);
   return RNN_OK;
 }
 
@@ -445,6 +458,33 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
           Launch Lk = mk(h, s, ws, "input_proj_gemm");
           RNN_TRY(gemm_f32(Lk, mode, A, Bw, (r1 - r0) * B, GH, In, P + (size_t)r0 * BGH, GH,
                            reinterpret_cast<const float*>(PW + h->pl[l].bias), 0, none, 0));
+        }
+        // persistent recurrence: all T steps of the layer in one launch
+        if (h->persist) {
+          const size_t bytes = (size_t)T * BH * e;
+          RNN_TRY(cu(cudaMemsetAsync(hseq + BH * e, 0xFF, bytes, s)));
+          PersistArgs pa{};
+          pa.T = T;
+          pa.B = B;
+          pa.H = H;
+          pa.u_pack = h->u;
+          pa.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
+          pa.P = P;
+          pa.gates_out = train ? P : nullptr;
+          pa.bias_hn = reinterpret_cast<const float*>(PW + h->pl[l].bias_hn);
+          pa.c0 = (lstm && c0) ? c0 + l * BH : nullptr;
+          pa.c_out = (train && lstm) ? reinterpret_cast<float*>(R + h->rl[l].c) : nullptr;
+          pa.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) : nullptr;
+          pa.hseq = reinterpret_cast<__nv_bfloat16*>(hseq);
+          pa.y = l == L - 1 ? static_cast<__nv_bfloat16*>(y) : nullptr;
+          pa.hT = hT ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(hT) + (size_t)l * BH * e) : nullptr;
+          pa.cT = (cT && lstm) ? cT + (size_t)l * BH : nullptr;
+          pa.err = reinterpret_cast<int*>(W + h->ws_err);
+          pa.limit_ns = h->limit_ns;
+          pa.test_skip_publish = (d.flags & RNN_FLAG_TEST_SKIP_PUBLISH) ? 1 : 0;
+          Launch Lk = mk(h, s, ws, "persist_fwd");
+          RNN_TRY(persist_fwd(Lk, d.cell, pa));
+          continue;
         }
         // recurrent steps of the chunk
         for (int t = t0; t < t1; ++t) {

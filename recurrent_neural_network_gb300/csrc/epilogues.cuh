@@ -110,7 +110,7 @@ struct EpiFwdStep {
       const int j0 = jblk + c;
       float* prow = P + (size_t)b * GH + t.n0 + c;
       float hnew[16];
-      if (CELL == LSTM) {
+      if constexpr (CELL == LSTM) {
         float cp[16];
         if (c_prev) load16(c_prev + (size_t)b * H + j0, cp);
         else
@@ -133,7 +133,7 @@ struct EpiFwdStep {
         }
         store16(c_out + (size_t)b * H + j0, cn);
         if (cT) store16(cT + (size_t)b * H + j0, cn);
-      } else if (CELL == GRU) {
+      } else if constexpr (CELL == GRU) {
         float hp[16], p[16], bn[16], hn[16];
         if (h_prev) load16(h_prev + (size_t)b * H + j0, hp);
         else
@@ -208,7 +208,7 @@ struct BwdPoint {
     const int p0 = (j0 / u) * (G * u) + (j0 % u);  // packed column of gate 0
     const float* grow = gates + (size_t)b * GH + p0;
     S* gx = dGx + (size_t)b * GH + p0;
-    if (CELL == LSTM) {
+    if constexpr (CELL == LSTM) {
       float ig[16], fg[16], gg[16], og[16], cs[16], cp[16], dc[16];
       load16(grow, ig);
       load16(grow + u, fg);
@@ -237,7 +237,7 @@ struct BwdPoint {
       store16(gx + 2 * u, d2);
       store16(gx + 3 * u, d3);
       store16(carry + bj, dc);
-    } else if (CELL == GRU) {
+    } else if constexpr (CELL == GRU) {
       float r[16], z[16], n[16], hn[16], hp[16], cz[16];
       load16(grow, r);
       load16(grow + u, z);

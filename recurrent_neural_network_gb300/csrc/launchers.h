@@ -2,6 +2,7 @@
 // by the C-ABI layer (api.cu).  Plain pointers and sizes only.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -100,5 +101,29 @@ int bwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
 // pointwise-only backward step (the last timestep): dh starts from dh_init
 // ([B][H], storage type, null = zero)
 int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const void* dh_init);
+
+// ---------------------------------------------------------------- persist.cu
+struct PersistArgs {
+  int T, B, H, u_pack, uc;
+  const __nv_bfloat16* Wh;  // packed [G*H][H]
+  const float* P;           // [T][B][G*H] input projection incl. bias
+  float* gates_out;         // training: activated gates [T][B][G*H] (may alias P), else null
+  const float* bias_hn;     // GRU [H]
+  const float* c0;          // LSTM [B][H] or null
+  float* c_out;             // LSTM training [T][B][H] or null
+  float* hn_out;            // GRU training [T][B][H] or null
+  __nv_bfloat16* hseq;      // [T+1][B][H]; slot 0 = h0, slots 1..T filled with 0xFFFF before the launch
+  __nv_bfloat16* y;         // [T][B][H] or null
+  __nv_bfloat16* hT;        // [B][H] or null
+  float* cT;                // [B][H] or null
+  int* err;
+  uint64_t limit_ns;
+  int test_skip_publish;    // test hook: CTA 0 never publishes h_0
+};
+// RNN_OK if the persistent recurrence supports (cell, H, B) and all its CTAs
+// fit on the device at once; *ctas receives the grid size.
+int persist_check(int cell, int H, int B, int num_sms, int* ctas);
+// all T timesteps of one layer in one cooperative launch (bf16 storage only)
+int persist_fwd(const Launch& L, int cell, const PersistArgs& a);
 
 }  // namespace rnn

@@ -1,0 +1,261 @@
+// persist.cu -- persistent forward recurrence for small batches.
+//
+// "Persistent RNNs: Stashing Recurrent Weights On-Chip" (citing snippets on
+// its page): cache the recurrent weights on-chip across timesteps and run all
+// timesteps in one kernel launch; small-batch RNNs are matrix-vector work.
+// Each CTA owns uc hidden units (all G gates of them) and keeps their rows of
+// the packed W_h in registers as mma.sync A fragments for the whole sequence.
+// Per timestep it reads h_{t-1} (all B x H values) from global memory, forms
+// its G*uc x B slice of h_{t-1} W_h^T on the tensor cores (split over K
+// across 8 warps, reduced through shared memory), applies the cell update to
+// its units and publishes its part of h_t.
+//
+// Step hand-off without a grid barrier: before the launch the h-sequence
+// slots 1..T are filled with the 16-bit pattern 0xFFFF, which the cell never
+// produces (a NaN with that exact pattern is replaced by 0x7FFF).  A reader
+// polls the 32-bit words it needs with volatile loads until neither half is
+// 0xFFFF; each half is written once, by one thread, with one 16-bit store, so
+// a non-sentinel half is final.  Every wait is bounded (globaltimer); on
+// timeout the CTA records DEV_TIMEOUT_STEP in the error word and leaves.
+// Co-residency of all CTAs is guaranteed by a cooperative launch.
+#include <cuda_bf16.h>
+
+#include "../../include/rnn.h"
+#include "common.cuh"
+#include "launchers.h"
+
+namespace rnn {
+
+namespace {
+
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ bool has_sentinel(uint32_t w) {
+  return (w & 0xFFFFu) == 0xFFFFu || (w >> 16) == 0xFFFFu;
+}
+
+__device__ __forceinline__ unsigned short bf16_bits(float v) {
+  unsigned short s = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return s == 0xFFFFu ? (unsigned short)0x7FFFu : s;
+}
+
+template <int CELL, int MT, int KT>
+__global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a) {
+  constexpr int G = CellInfo<CELL>::G;
+  constexpr int ROWS = MT * 16;  // = G * uc
+  __shared__ float part[8][ROWS][8];
+  __shared__ float sums[ROWS][8];
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int uc = ROWS / G;
+  const int H = a.H, B = a.B, GH = G * H;
+  const int jbase = blockIdx.x * uc;
+  if (threadIdx.x == 0) abort_flag = 0;
+
+  // ---- this CTA's rows of W_h as A fragments (row r = g*uc + local unit)
+  uint32_t wf[MT][KT][4];
+  {
+    const int kw = warp * KT * 16;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int r0 = mt * 16 + (lane >> 2), r1 = r0 + 8;
+      const int p0 = packed_row(r0 / uc, jbase + r0 % uc, G, a.u_pack);
+      const int p1 = packed_row(r1 / uc, jbase + r1 % uc, G, a.u_pack);
+      const uint32_t* w0 = reinterpret_cast<const uint32_t*>(a.Wh + (size_t)p0 * H);
+      const uint32_t* w1 = reinterpret_cast<const uint32_t*>(a.Wh + (size_t)p1 * H);
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt) {
+        const int k = kw + kt * 16 + (lane & 3) * 2;
+        wf[mt][kt][0] = w0[k >> 1];
+        wf[mt][kt][1] = w1[k >> 1];
+        wf[mt][kt][2] = w0[(k + 8) >> 1];
+        wf[mt][kt][3] = w1[(k + 8) >> 1];
+      }
+    }
+  }
+
+  // ---- cell-update threads: one (unit, batch row) pair each
+  const int q = threadIdx.x;
+  const int jl = q % uc, bq = q / uc;
+  const bool pair = bq < B && q < uc * 8;
+  const int j = jbase + jl;
+  float c_state = 0.f, h_prev = 0.f;
+  int pcol[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) pcol[g] = packed_row(g, j, G, a.u_pack);
+  if (pair) {
+    if (CELL == LSTM && a.c0) c_state = a.c0[(size_t)bq * H + j];
+    if (CELL == GRU) h_prev = __bfloat162float(a.hseq[(size_t)bq * H + j]);
+  }
+  const float bhn = (CELL == GRU && pair) ? a.bias_hn[j] : 0.f;
+  __syncthreads();
+
+  const int nb = lane >> 2;  // batch column of this lane's B fragment
+  const int kw = warp * KT * 16 + (lane & 3) * 2;
+  for (int t = 0; t < a.T; ++t) {
+    // input projection of this step for the pair (independent of the recurrence)
+    float pv[G];
+    if (pair) {
+      const float* prow = a.P + ((size_t)t * B + bq) * GH;
+#pragma unroll
+      for (int g = 0; g < G; ++g) pv[g] = prow[pcol[g]];
+    }
+    // ---- wait for h_{t-1} (slot t) and load this warp's B fragments
+    uint32_t bf[KT][2];
+    const volatile uint32_t* hs =
+        reinterpret_cast<const volatile uint32_t*>(a.hseq + ((size_t)t * B + nb) * H + kw);
+    bool ok = true;
+    if (nb < B) {
+      uint64_t t0 = 0;
+      for (int spin = 0;; ++spin) {
+        bool ready = true;
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+          bf[kt][0] = hs[(kt * 16) >> 1];
+          bf[kt][1] = hs[(kt * 16 + 8) >> 1];
+          ready = ready && !has_sentinel(bf[kt][0]) && !has_sentinel(bf[kt][1]);
+        }
+        if (ready) break;
+        if (spin == 0) t0 = globaltimer_ns();
+        else if ((spin & 15) == 0 &&
+                   (*reinterpret_cast<volatile int*>(&abort_flag) || globaltimer_ns() - t0 > a.limit_ns)) {
+          ok = false;
+          break;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt) bf[kt][0] = bf[kt][1] = 0u;
+    }
+    if (!ok) {
+      abort_flag = 1;
+      raise_error(a.err, DEV_TIMEOUT_STEP);
+    }
+    // ---- partial products over this warp's K range
+    float acc[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[mt], wf[mt][kt], bf[kt]);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int r = mt * 16 + (lane >> 2), c = (lane & 3) * 2;
+      part[warp][r][c] = acc[mt][0];
+      part[warp][r][c + 1] = acc[mt][1];
+      part[warp][r + 8][c] = acc[mt][2];
+      part[warp][r + 8][c + 1] = acc[mt][3];
+    }
+    __syncthreads();
+    if (abort_flag) break;
+    for (int idx = threadIdx.x; idx < ROWS * 8; idx += 256) {
+      const int r = idx >> 3, c = idx & 7;
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) s += part[w][r][c];
+      sums[r][c] = s;
+    }
+    __syncthreads();
+    // ---- cell update of this CTA's units
+    if (pair) {
+      float av[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) av[g] = sums[g * uc + jl][bq];
+      float hnew, gv[G];
+      if constexpr (CELL == LSTM) {
+        const float ig = sigm(av[0] + pv[0]), fg = sigm(av[1] + pv[1]);
+        const float gg = tanh_(av[2] + pv[2]), og = sigm(av[3] + pv[3]);
+        c_state = fg * c_state + ig * gg;
+        hnew = og * tanh_(c_state);
+        gv[0] = ig; gv[1] = fg; gv[2] = gg; gv[G - 1] = og;
+      } else if constexpr (CELL == GRU) {
+        const float r = sigm(av[0] + pv[0]), z = sigm(av[1] + pv[1]);
+        const float hn = av[2] + bhn;
+        const float n = tanh_(pv[2] + r * hn);
+        hnew = (1.f - z) * n + z * h_prev;
+        h_prev = hnew;
+        gv[0] = r; gv[1] = z; gv[G - 1] = n;
+        if (a.hn_out) a.hn_out[((size_t)t * B + bq) * H + j] = hn;
+      } else {
+        hnew = tanh_(av[0] + pv[0]);
+        gv[0] = hnew;
+      }
+      const size_t bj = (size_t)bq * H + j;
+      const unsigned short hb = bf16_bits(hnew);
+      if (a.gates_out) {
+        float* grow = a.gates_out + ((size_t)t * B + bq) * GH;
+#pragma unroll
+        for (int g = 0; g < G; ++g) grow[pcol[g]] = gv[g];
+      }
+      if (CELL == LSTM && a.c_out) a.c_out[(size_t)t * B * H + bj] = c_state;
+      if (a.y) reinterpret_cast<unsigned short*>(a.y)[(size_t)t * B * H + bj] = hb;
+      if (t == a.T - 1) {
+        if (a.hT) reinterpret_cast<unsigned short*>(a.hT)[bj] = hb;
+        if (CELL == LSTM && a.cT) a.cT[bj] = c_state;
+      }
+      // publish h_t last: readers of slot t+1 may proceed as soon as they see it
+      if (!(a.test_skip_publish && blockIdx.x == 0 && t == 0))
+        *reinterpret_cast<volatile unsigned short*>(a.hseq + (size_t)(t + 1) * B * H + bj) = hb;
+    }
+  }
+}
+
+template <int CELL, int MT, int KT>
+int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only, int num_sms) {
+  auto kern = persist_fwd_kernel<CELL, MT, KT>;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess) return RNN_ERR_CUDA;
+  if (per_sm * num_sms < ctas) return RNN_ERR_LAUNCH;
+  if (query_only) return RNN_OK;
+  PersistArgs args = a;
+  void* params[] = {&args};
+  launch_begin(L);
+  cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(ctas), dim3(256), params, 0,
+                                              L.stream);
+  launch_end(L);
+  if (e == cudaErrorCooperativeLaunchTooLarge) return RNN_ERR_LAUNCH;
+  return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA;
+}
+
+// (cell, H) -> kernel instance; MT*16 = G*uc rows per CTA, KT*16*8 = H.
+int dispatch(const Launch& L, int cell, const PersistArgs& a, bool query_only, int num_sms, int* ctas_out) {
+  const int H = a.H;
+  if (H % 128 || a.B < 1 || a.B > 8) return RNN_ERR_UNSUPPORTED;
+  const int KT = H / 128;
+  int uc = cell == LSTM ? 8 : 16;
+  const int ctas = H / uc;
+  if (ctas_out) *ctas_out = ctas;
+  PersistArgs b = a;
+  b.uc = uc;
+#define RNN_P(C, MT_, KT_) \
+  if (cell == C && KT == KT_) return launch_one<C, MT_, KT_>(L, b, ctas, query_only, num_sms);
+  RNN_P(LSTM, 2, 1) RNN_P(LSTM, 2, 2) RNN_P(LSTM, 2, 4) RNN_P(LSTM, 2, 8)
+  RNN_P(GRU, 3, 1) RNN_P(GRU, 3, 2) RNN_P(GRU, 3, 4)
+  RNN_P(TANH, 1, 1) RNN_P(TANH, 1, 2) RNN_P(TANH, 1, 4) RNN_P(TANH, 1, 8) RNN_P(TANH, 1, 16)
+#undef RNN_P
+  return RNN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+int persist_check(int cell, int H, int B, int num_sms, int* ctas) {
+  Launch L{};
+  PersistArgs a{};
+  a.H = H;
+  a.B = B;
+  return dispatch(L, cell, a, true, num_sms, ctas);
+}
+
+int persist_fwd(const Launch& L, int cell, const PersistArgs& a) {
+  int ctas = 0;
+  return dispatch(L, cell, a, false, L.num_sms, &ctas);
+}
+
+}  // namespace rnn

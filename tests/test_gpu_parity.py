@@ -126,3 +126,49 @@ def test_workload_lstm_h4096_sampled_columns():
 
 def test_workload_gru_8layer_sampled_columns():
     masked_columns_check(synth.WORKLOADS[4], [5, 31])
+
+
+# ---------------------------------------------------------------- persistent recurrence
+
+PERSIST_CASES = [
+    # cell, layers, T, B, I, H
+    (0, 1, 7, 1, 64, 128),
+    (0, 2, 6, 3, 72, 1024),
+    (0, 1, 5, 8, 128, 256),
+    (1, 2, 6, 4, 64, 256),
+    (1, 1, 5, 8, 64, 128),
+    (2, 2, 6, 5, 64, 2048),
+]
+
+
+@pytest.mark.parametrize("case", PERSIST_CASES, ids=lambda c: "c%d_L%d_T%d_B%d_I%d_H%d" % c)
+def test_persistent_recurrence_training(case):
+    cell, L, T, B, I, H = case
+    wl = synth.Workload("persist", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    r = runner.Runner(wl, flags=rnn.FLAG_FORCE_PERSISTENT)
+    assert "recurrence=persistent" in r.r.describe()
+    compare(wl, run_gpu(wl, hi, flags=rnn.FLAG_FORCE_PERSISTENT), run_oracle(hi))
+
+
+def test_persistent_equals_streaming_within_tolerance():
+    wl = synth.Workload("pvs", 0, 2, 9, 4, 128, 512, synth.MODE_BF16, forget_bias=1.0, state_std=0.3)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    p = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_PERSISTENT)
+    s = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_STREAMING)
+    for k in ("y", "hT", "cT"):
+        assert float(np.abs(p[k] - s[k]).max()) <= 3e-2, k
+
+
+def test_persistent_bounded_wait_reports_timeout():
+    """One CTA never publishes its first step: the others' waits give up after
+    the handle's bound and the error word says so; the context stays usable."""
+    wl = synth.Workload("skip", 0, 1, 4, 2, 64, 256, synth.MODE_BF16, training=False)
+    hi = runner.HostInputs(wl)
+    r = runner.Runner(wl, flags=rnn.FLAG_FORCE_PERSISTENT | rnn.FLAG_TEST_SKIP_PUBLISH, timeout_ns=20_000_000)
+    r.upload(hi)
+    r.forward(False)
+    assert r.status() == -5  # RNN_ERR_TIMEOUT
+    assert r.status() == 0   # the word was cleared
+    g = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_PERSISTENT)
+    compare(wl, g, run_oracle(hi, train=False))

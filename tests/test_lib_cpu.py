@@ -79,6 +79,18 @@ def test_calls_validate_arguments_before_any_device_work(lib):
     assert lib.rnn_get_sizes(None, None, None, None, None) == -1
 
 
+def test_persistent_plan_selection(lib):
+    # small batch, supported width: persistent, no wavefront
+    assert "recurrence=persistent" in rnn.RNN(0, 2, 10, 4, 64, 1024, 1).describe()
+    assert "recurrence=streaming" in rnn.RNN(0, 2, 10, 4, 64, 1024, 1, flags=rnn.FLAG_FORCE_STREAMING).describe()
+    assert "recurrence=streaming" in rnn.RNN(0, 2, 10, 64, 64, 1024, 1).describe()
+    with pytest.raises(rnn.RnnError) as e:
+        rnn.RNN(0, 1, 10, 64, 64, 1024, 1, flags=rnn.FLAG_FORCE_PERSISTENT)
+    assert e.value.code == -2
+    with pytest.raises(rnn.RnnError):
+        rnn.RNN(0, 1, 10, 4, 64, 1024, 0, flags=rnn.FLAG_FORCE_PERSISTENT)  # fp32 mode has no persistent path
+
+
 def test_wavefront_chunking_plan(lib):
     r = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, chunk=5)
     assert "chunk=5 nchunks=10" in r.describe()
