@@ -128,6 +128,7 @@ struct rnn_s {
   std::vector<WL> wl;
   std::vector<UL> ul;
   size_t ws_err = 0;
+  size_t ws_arrive = 0;  // persistent recurrence: per-timestep arrival counters
   int ctr_count = 0;
   // streams and events (created on first use)
   std::vector<cudaStream_t> streams;
@@ -239,6 +240,7 @@ int plan_and_layout(rnn_s* h) {
   h->wl.resize(L);
   cur = 0;
   h->ws_err = take(cur, 256);
+  h->ws_arrive = take(cur, (size_t)T * 4);
   h->bias_slices = std::max(1, std::min(64, (T * B + 255) / 256));
   h->ws_bias = take(cur, (size_t)h->bias_slices * GH * 4);
   for (int l = 0; l < L; ++l) {
@@ -461,9 +463,10 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
         }
         // persistent recurrence: all T steps of the layer in one launch
         if (h->persist) {
-          const size_t bytes = (size_t)T * BH * e;
-          RNN_TRY(cu(cudaMemsetAsync(hseq + BH * e, 0xFF, bytes, s)));
+          unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
+          RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
           PersistArgs pa{};
+          pa.arrive = arrive;
           pa.T = T;
           pa.B = B;
           pa.H = H;

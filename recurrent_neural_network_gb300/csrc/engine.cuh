@@ -226,6 +226,18 @@ __global__ void __launch_bounds__(192, 1)
     for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
       int mt, nt, split;
       decode_tile(g, tile, mt, nt, split);
+      {
+        // let the epilogue's own global inputs travel to L2 while the MMAs run
+        TileCoord tp;
+        tp.m0 = mt * BM;
+        tp.n0 = nt * BN;
+        tp.mt = mt;
+        tp.nt = nt;
+        tp.split = split;
+        tp.splits = g.splits;
+        tp.scratch = scratch;
+        epi.prefetch(tp, row, BN);
+      }
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);

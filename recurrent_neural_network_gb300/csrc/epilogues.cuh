@@ -24,6 +24,7 @@
 
 #include "common.cuh"
 #include "engine.cuh"
+#include "tc.cuh"
 
 namespace rnn {
 
@@ -38,6 +39,8 @@ struct EpiStore {
   // packed -> user row remap (weight gradients): row p of the product is
   // gate row g of hidden unit j, stored at user row g*H + j.
   int remap, G, u, H;
+
+  __device__ __forceinline__ void prefetch(const TileCoord&, int, int) const {}
 
   __device__ __forceinline__ long long out_row(int m) const {
     if (!remap) return m;
@@ -95,6 +98,16 @@ struct EpiFwdStep {
   S* hT;                 // [B][H] or null
   float* cT;             // [B][H] or null
   float* hn_out;         // GRU [B][H] or null
+
+  __device__ __forceinline__ void prefetch(const TileCoord& t, int row, int /*bn*/) const {
+    constexpr int G = CellInfo<CELL>::G;
+    const int b = t.m0 + row;
+    if (b >= B) return;
+    const int jblk = (t.n0 / (G * u)) * u;
+    tc::prefetch_l2(P + (size_t)b * G * H + t.n0, G * u * 4);
+    if (CELL == LSTM && c_prev) tc::prefetch_l2(c_prev + (size_t)b * H + jblk, u * 4);
+    if (CELL == GRU && h_prev) tc::prefetch_l2(h_prev + (size_t)b * H + jblk, u * sizeof(S));
+  }
 
   template <class Acc>
   __device__ __forceinline__ void operator()(const TileCoord& t, int row, const Acc& acc, int /*bn*/) const {
@@ -311,6 +324,30 @@ struct EpiBwdStep {
       load16(pt.carry + bj, dc);
       store16(dc0 + bj, dc);
     }
+  }
+
+  // Rows are shared out over the split-K CTAs of the tile: whichever of them
+  // arrives last finds its inputs in L2.
+  __device__ __forceinline__ void prefetch(const TileCoord& t, int row, int bn) const {
+    constexpr int G = CellInfo<CELL>::G;
+    const int b = t.m0 + row;
+    const int B = pt.B, H = pt.H;
+    if (b >= B || final_ || (row % t.splits) != t.split) return;
+    const int nu = min(bn, H - t.n0);  // units of this tile (a multiple of u)
+    const size_t bj = (size_t)b * H + t.n0;
+    const int p0 = (t.n0 / pt.u) * (G * pt.u);
+    tc::prefetch_l2(pt.gates + (size_t)b * G * H + p0, nu * G * 4);
+    if (CELL == LSTM) {
+      tc::prefetch_l2(pt.c_s + bj, nu * 4);
+      if (pt.c_sm1) tc::prefetch_l2(pt.c_sm1 + bj, nu * 4);
+    }
+    if (CELL == GRU) {
+      tc::prefetch_l2(pt.hn_s + bj, nu * 4);
+      if (pt.h_sm1) tc::prefetch_l2(pt.h_sm1 + bj, nu * sizeof(S));
+    }
+    if (CELL != TANH) tc::prefetch_l2(pt.carry + bj, nu * 4);
+    if (pt.dy) tc::prefetch_l2(static_cast<const char*>(pt.dy) + bj * (pt.dy_f32 ? 4 : sizeof(S)),
+                               nu * (pt.dy_f32 ? 4 : (int)sizeof(S)));
   }
 
   template <class Acc>

@@ -112,7 +112,8 @@ struct PersistArgs {
   const float* c0;          // LSTM [B][H] or null
   float* c_out;             // LSTM training [T][B][H] or null
   float* hn_out;            // GRU training [T][B][H] or null
-  __nv_bfloat16* hseq;      // [T+1][B][H]; slot 0 = h0, slots 1..T filled with 0xFFFF before the launch
+  __nv_bfloat16* hseq;      // [T+1][B][H]; slot 0 = h0
+  unsigned int* arrive;     // [T] arrival counters, zero before the launch
   __nv_bfloat16* y;         // [T][B][H] or null
   __nv_bfloat16* hT;        // [B][H] or null
   float* cT;                // [B][H] or null

@@ -10,14 +10,14 @@
 // across 8 warps, reduced through shared memory), applies the cell update to
 // its units and publishes its part of h_t.
 //
-// Step hand-off without a grid barrier: before the launch the h-sequence
-// slots 1..T are filled with the 16-bit pattern 0xFFFF, which the cell never
-// produces (a NaN with that exact pattern is replaced by 0x7FFF).  A reader
-// polls the 32-bit words it needs with volatile loads until neither half is
-// 0xFFFF; each half is written once, by one thread, with one 16-bit store, so
-// a non-sentinel half is final.  Every wait is bounded (globaltimer); on
-// timeout the CTA records DEV_TIMEOUT_STEP in the error word and leaves.
-// Co-residency of all CTAs is guaranteed by a cooperative launch.
+// Step hand-off: after its h_t stores a CTA makes one fenced arrival on the
+// step's counter (one counter per timestep, zeroed before the launch); one
+// thread per CTA polls the counter of the previous step until every CTA has
+// arrived, then the CTA reads h_{t-1} once through L2.  Only 1 thread per CTA
+// spins, on one word, so the polling does not crowd the L2 slices that serve
+// the h data to every SM.  Every wait is bounded (globaltimer); on timeout the
+// CTA records DEV_TIMEOUT_STEP in the error word and leaves.  Co-residency of
+// all CTAs is guaranteed by a cooperative launch.
 #include <cuda_bf16.h>
 
 #include "../../include/rnn.h"
@@ -36,13 +36,8 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, cons
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-__device__ __forceinline__ bool has_sentinel(uint32_t w) {
-  return (w & 0xFFFFu) == 0xFFFFu || (w >> 16) == 0xFFFFu;
-}
-
 __device__ __forceinline__ unsigned short bf16_bits(float v) {
-  unsigned short s = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  return s == 0xFFFFu ? (unsigned short)0x7FFFu : s;
+  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
 template <int CELL, int MT, int KT>
@@ -106,36 +101,38 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
 #pragma unroll
       for (int g = 0; g < G; ++g) pv[g] = prow[pcol[g]];
     }
-    // ---- wait for h_{t-1} (slot t) and load this warp's B fragments
+    // ---- wait until every CTA has published h_{t-1} (slot t), then load this
+    // warp's B fragments of it through L2
+    if (t > 0) {
+      if (threadIdx.x == 0) {
+        const volatile unsigned int* cnt = a.arrive + (t - 1);
+        const unsigned int want = gridDim.x;
+        if (*cnt < want) {
+          const uint64_t t0 = globaltimer_ns();
+          while (*cnt < want) {
+            if (globaltimer_ns() - t0 > a.limit_ns) {
+              abort_flag = 1;
+              raise_error(a.err, DEV_TIMEOUT_STEP);
+              break;
+            }
+          }
+        }
+        __threadfence();
+      }
+      __syncthreads();
+      if (abort_flag) break;
+    }
     uint32_t bf[KT][2];
-    const volatile uint32_t* hs =
-        reinterpret_cast<const volatile uint32_t*>(a.hseq + ((size_t)t * B + nb) * H + kw);
-    bool ok = true;
     if (nb < B) {
-      uint64_t t0 = 0;
-      for (int spin = 0;; ++spin) {
-        bool ready = true;
+      const uint32_t* hs = reinterpret_cast<const uint32_t*>(a.hseq + ((size_t)t * B + nb) * H + kw);
 #pragma unroll
-        for (int kt = 0; kt < KT; ++kt) {
-          bf[kt][0] = hs[(kt * 16) >> 1];
-          bf[kt][1] = hs[(kt * 16 + 8) >> 1];
-          ready = ready && !has_sentinel(bf[kt][0]) && !has_sentinel(bf[kt][1]);
-        }
-        if (ready) break;
-        if (spin == 0) t0 = globaltimer_ns();
-        else if ((spin & 15) == 0 &&
-                   (*reinterpret_cast<volatile int*>(&abort_flag) || globaltimer_ns() - t0 > a.limit_ns)) {
-          ok = false;
-          break;
-        }
+      for (int kt = 0; kt < KT; ++kt) {
+        bf[kt][0] = __ldcg(hs + ((kt * 16) >> 1));
+        bf[kt][1] = __ldcg(hs + ((kt * 16 + 8) >> 1));
       }
     } else {
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) bf[kt][0] = bf[kt][1] = 0u;
-    }
-    if (!ok) {
-      abort_flag = 1;
-      raise_error(a.err, DEV_TIMEOUT_STEP);
     }
     // ---- partial products over this warp's K range
     float acc[MT][4];
@@ -154,7 +151,6 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       part[warp][r + 8][c + 1] = acc[mt][3];
     }
     __syncthreads();
-    if (abort_flag) break;
     for (int idx = threadIdx.x; idx < ROWS * 8; idx += 256) {
       const int r = idx >> 3, c = idx & 7;
       float s = 0.f;
@@ -200,9 +196,14 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
         if (a.hT) reinterpret_cast<unsigned short*>(a.hT)[bj] = hb;
         if (CELL == LSTM && a.cT) a.cT[bj] = c_state;
       }
-      // publish h_t last: readers of slot t+1 may proceed as soon as they see it
-      if (!(a.test_skip_publish && blockIdx.x == 0 && t == 0))
-        *reinterpret_cast<volatile unsigned short*>(a.hseq + (size_t)(t + 1) * B * H + bj) = hb;
+      reinterpret_cast<unsigned short*>(a.hseq)[(size_t)(t + 1) * B * H + bj] = hb;
+    }
+    // ---- publish: once all of this CTA's h_t stores are done, one fenced
+    // arrival on the step's counter
+    __syncthreads();
+    if (threadIdx.x == 0 && !(a.test_skip_publish && blockIdx.x == 0 && t == 0)) {
+      __threadfence();
+      atomicAdd(a.arrive + t, 1u);
     }
   }
 }
