@@ -189,11 +189,17 @@ int plan_and_layout(rnn_s* h) {
   // until the step covers the SMs (at most 8 ways, at least 4 K blocks each)
   if (d.mode == RNN_MODE_BF16) {
     h->bwd_bn = (H % 256 == 0) ? 256 : 128;
+    // narrower tiles when even 8-way splits of 256-wide tiles leave most SMs idle
+    if (h->bwd_bn == 256 && ((B + 127) / 128) * (H / 256) * 8 < h->num_sms / 2) h->bwd_bn = 128;
     const int tiles = ((B + 127) / 128) * ((H + h->bwd_bn - 1) / h->bwd_bn);
     const int kb = (GH + 63) / 64;
-    int s = std::max(1, h->num_sms / std::max(1, tiles));
-    s = std::min(s, 8);
-    s = std::min(s, std::max(1, kb / 4));
+    int want = std::max(1, h->num_sms / std::max(1, tiles));
+    want = std::min(want, 8);
+    want = std::min(want, std::max(1, kb / 4));
+    // a power of two that the K blocks fill exactly, so that every split has
+    // work and the cluster reduction cuts the tile into 16-column slices
+    int s = 1;
+    while (s * 2 <= want && (s * 2 - 1) * ((kb + s * 2 - 1) / (s * 2)) < kb) s *= 2;
     h->bwd_splits = s;
     h->ctr_count = tiles;
   } else {
@@ -581,6 +587,7 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
           a.dGh = R + h->rl[l].dgh + (size_t)st * BGH * e;
           a.part = reinterpret_cast<float*>(W + h->wl[l].part);
           a.counters = reinterpret_cast<int*>(W + h->wl[l].ctr);
+          a.cluster_splitk = 1;
           return a;
         };
         Operand Bw{PW + h->pl[l].wh, H, 1, H, GH};

@@ -33,6 +33,7 @@ struct GemmGeom {
   int a_mn, b_mn;              // operand majorness (1 = MN-major)
   uint64_t limit_ns;           // bound on every pipeline wait
   int* err;                    // device error word
+  int cluster;                 // > 1: the split-K CTAs of a tile form one thread-block cluster
 };
 
 struct TileCoord {
@@ -40,6 +41,12 @@ struct TileCoord {
   int mt, nt;       // tile indices
   int split, splits;
   int* scratch;     // 8 ints of shared memory for the epilogue warps (tcgen05 only)
+  // cluster split-K (tcgen05, cluster > 1): the CTA's stage buffers reused as a
+  // float tile for the reduction, and two cluster-wide barriers
+  int cluster;
+  float* red;
+  uint64_t* red_full;
+  uint64_t* red_done;
 };
 
 struct TmemAcc {
@@ -94,7 +101,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* red_full = tempty + 2;
+  uint64_t* red_done = red_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* scratch = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -110,6 +119,8 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_init(tfull + a, 1);
       tc::mbar_init(tempty + a, 4);
     }
+    tc::mbar_init(red_full, 4 * g.cluster);
+    tc::mbar_init(red_done, 4 * g.cluster);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&mapA);
@@ -122,6 +133,7 @@ __global__ void __launch_bounds__(192, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (g.cluster > 1) tc::cluster_sync_all();  // peers' barriers are initialised before any remote arrive
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
@@ -236,6 +248,10 @@ __global__ void __launch_bounds__(192, 1)
         tp.split = split;
         tp.splits = g.splits;
         tp.scratch = scratch;
+        tp.cluster = g.cluster;
+        tp.red = reinterpret_cast<float*>(smem);
+        tp.red_full = red_full;
+        tp.red_done = red_done;
         epi.prefetch(tp, row, BN);
       }
       int ok = 1;
@@ -251,6 +267,10 @@ __global__ void __launch_bounds__(192, 1)
       t.split = split;
       t.splits = g.splits;
       t.scratch = scratch;
+      t.cluster = g.cluster;
+      t.red = reinterpret_cast<float*>(smem);
+      t.red_full = red_full;
+      t.red_done = red_done;
       TmemAcc a{tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16)};
       epi(t, row, a, BN);
       tc::fence_before_sync();
@@ -267,6 +287,7 @@ __global__ void __launch_bounds__(192, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  if (g.cluster > 1) tc::cluster_sync_all();  // no peer touches this CTA's shared memory after it exits
 }
 
 // ---------------------------------------------------------------------------
@@ -345,6 +366,9 @@ __global__ void __launch_bounds__(128)
     t.split = 0;
     t.splits = 1;
     t.scratch = nullptr;
+    t.cluster = 1;
+    t.red = nullptr;
+    t.red_full = t.red_done = nullptr;
     SmemAcc a{Cs + tid * (BN + 1)};
     epi(t, tid, a, BN);
   }

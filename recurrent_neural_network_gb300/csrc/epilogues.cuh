@@ -302,8 +302,10 @@ struct EpiBwdStep {
   int final_;
   S* dh0;        // [B][H] (final)
   float* dc0;    // [B][H] (final, LSTM)
-  float* part;   // split-K partials [splits][B][H]
+  float* part;   // split-K partials [splits][B][H] (global-memory reduction)
   int* counters; // one per (m-tile, n-tile), zero before the first use
+  int* err;      // device error word (cluster reduction waits)
+  uint64_t limit_ns;
 
   __device__ __forceinline__ void finish(int b, int j0, float* dh) const {
     const int H = pt.H;
@@ -354,6 +356,58 @@ struct EpiBwdStep {
   __device__ __forceinline__ void operator()(const TileCoord& t, int row, const Acc& acc, int bn) const {
     const int b = t.m0 + row;
     const int B = pt.B, H = pt.H;
+    if (t.splits > 1 && t.cluster > 1) {
+      // Split-K partials reduced across the cluster: every CTA parks its
+      // partial tile in its own shared memory, then CTA `split` sums columns
+      // [split*cw, (split+1)*cw) over all CTAs through distributed shared
+      // memory and runs the pointwise step for those hidden units.
+      const int RS = bn + 4;
+      const int lane = threadIdx.x & 31;
+      float* mine = t.red + (size_t)row * RS;
+      for (int c = 0; c < bn; c += 16) {
+        float v[16];
+        acc.load16(c, v);
+        float4* d = reinterpret_cast<float4*>(mine + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+      tc::fence_acq_rel_cluster();
+      __syncwarp();
+      const uint32_t full_local = tc::smem_addr(t.red_full), done_local = tc::smem_addr(t.red_done);
+      if (lane == 0)
+        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(full_local, p));
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait_cluster(t.red_full, 0, err, limit_ns) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok && b < B) {
+        const int cw = bn / t.cluster;
+        const uint32_t mine_addr = tc::smem_addr(mine);
+        for (int c = t.split * cw; c < (t.split + 1) * cw; c += 16) {
+          const int j0 = t.n0 + c;
+          if (j0 >= H) break;
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int p = 0; p < t.cluster; ++p) {
+            const uint32_t ra = tc::mapa(mine_addr, p) + c * 4;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float w[4];
+              tc::ld_dsmem4(ra + 16 * q, w);
+              v[4 * q] += w[0]; v[4 * q + 1] += w[1]; v[4 * q + 2] += w[2]; v[4 * q + 3] += w[3];
+            }
+          }
+          finish(b, j0, v);
+        }
+      }
+      tc::fence_acq_rel_cluster();
+      __syncwarp();
+      if (lane == 0)
+        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(done_local, p));
+      if (lane == 0) tc::mbar_wait_cluster(t.red_done, 0, err, limit_ns);
+      __syncwarp();
+      return;
+    }
     if (t.splits > 1) {
       // write this split's partial, then the last CTA of the tile reduces
       for (int c = 0; c < bn; c += 16) {

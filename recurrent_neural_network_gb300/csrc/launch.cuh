@@ -60,9 +60,12 @@ inline int cuda_status(cudaError_t e) {
   return RNN_ERR_CUDA;
 }
 
+// cluster_splitk: with more than one K split, the splits of each output tile
+// run as one thread-block cluster and reduce through distributed shared
+// memory (the epilogue must support it); one tile per CTA.
 template <int BN, int STAGES, class Epi>
 int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, int splits, int max_ctas,
-              const Epi& epi) {
+              const Epi& epi, bool cluster_splitk = false) {
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
   if (B.mn_major && BN % 64) return RNN_ERR_UNSUPPORTED;
   CUtensorMap ma, mb;
@@ -85,6 +88,11 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   g.b_mn = B.mn_major;
   g.limit_ns = L.limit_ns;
   g.err = L.err;
+  // The cluster reduction gives each CTA BN/splits columns, read as 16-byte
+  // vectors and processed 16 hidden units at a time: it needs BN to be a
+  // multiple of 16*splits and at most 8 CTAs per cluster.  Otherwise the
+  // partials go through global memory.
+  g.cluster = (cluster_splitk && g.splits > 1 && g.splits <= 8 && BN % (16 * g.splits) == 0) ? g.splits : 1;
   constexpr int smem = tce::smem_bytes<BN, STAGES>();
   auto kern = tc_gemm_kernel<BN, STAGES, Epi>;
   static bool attr = false;
@@ -95,9 +103,26 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   }
   int cap = max_ctas > 0 ? max_ctas : L.num_sms;
   int grid = std::min(g.num_tiles, cap);
+  cudaError_t e;
   launch_begin(L);
-  kern<<<grid, 192, smem, L.stream>>>(ma, mb, g, epi);
-  cudaError_t e = cudaGetLastError();
+  if (g.cluster > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g.num_tiles);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = g.cluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, g, epi);
+  } else {
+    kern<<<grid, 192, smem, L.stream>>>(ma, mb, g, epi);
+    e = cudaGetLastError();
+  }
   launch_end(L);
   return cuda_status(e);
 }
@@ -115,6 +140,7 @@ int launch_simt(const Launch& L, const Operand& A, const Operand& B, int M, int 
   g.kb_total = (K + se::BK - 1) / se::BK;
   g.kb_per_split = g.kb_total;
   g.num_tiles = g.m_tiles * g.n_tiles;
+  g.cluster = 1;
   g.a_mn = A.mn_major;
   g.b_mn = B.mn_major;
   g.limit_ns = L.limit_ns;

@@ -94,6 +94,7 @@ struct BwdStepArgs {
   float* dc0;
   float* part;
   int* counters;
+  int cluster_splitk;  // reduce split-K partials inside a thread-block cluster instead of through global memory
 };
 // one backward timestep: A = dGh_{s+1} [B][G*H], Bw = packed W_h (MN-major view)
 int bwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, int bn, int splits,

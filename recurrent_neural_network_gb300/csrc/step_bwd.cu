@@ -41,6 +41,8 @@ EpiBwdStep<CELL, S> make_epi(const BwdStepArgs& a) {
   e.dc0 = a.dc0;
   e.part = a.part;
   e.counters = a.counters;
+  e.err = nullptr;
+  e.limit_ns = 0;
   return e;
 }
 
@@ -51,8 +53,11 @@ int bwd_step_cell(const Launch& L, int mode, const Operand& A, const Operand& Bw
   const int M = a.B, N = a.H, K = G * a.H;
   if (mode == 1) {
     using S = __nv_bfloat16;
-    if (bn == 256) return launch_tc<256, 4>(L, A, Bw, M, N, K, splits, 0, make_epi<CELL, S>(a));
-    if (bn == 128) return launch_tc<128, 6>(L, A, Bw, M, N, K, splits, 0, make_epi<CELL, S>(a));
+    auto e = make_epi<CELL, S>(a);
+    e.err = L.err;
+    e.limit_ns = L.limit_ns;
+    if (bn == 256) return launch_tc<256, 4>(L, A, Bw, M, N, K, splits, 0, e, a.cluster_splitk != 0);
+    if (bn == 128) return launch_tc<128, 6>(L, A, Bw, M, N, K, splits, 0, e, a.cluster_splitk != 0);
     return RNN_ERR_UNSUPPORTED;
   }
   return launch_simt<32>(L, A, Bw, M, N, K, make_epi<CELL, float>(a));

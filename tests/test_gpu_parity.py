@@ -57,6 +57,16 @@ def test_ragged_batch_and_input(cell):
     compare(wl, run_gpu(wl, hi), run_oracle(hi))
 
 
+@pytest.mark.parametrize("cell,B,H", [(1, 4, 192), (0, 70, 320), (2, 9, 64), (1, 33, 256)],
+                         ids=["gru_B4_H192", "lstm_B70_H320", "tanh_B9_H64", "gru_B33_H256"])
+def test_backward_split_shapes(cell, B, H):
+    """Widths whose gate-gradient K blocks are not a power of two (3*192/64 = 9,
+    4*320/64 = 20 ...): the backward step's split-K plan and its cluster reduction."""
+    wl = synth.Workload("splits", cell, 2, 4, B, 64, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.2)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    compare(wl, run_gpu(wl, hi, flags=rnn.FLAG_FORCE_STREAMING), run_oracle(hi))
+
+
 def test_single_step_and_single_row():
     wl = synth.Workload("t1b1", 0, 1, 1, 1, 64, 64, synth.MODE_BF16, forget_bias=1.0, state_std=0.5)
     hi = runner.HostInputs(wl, with_state_grads=True)

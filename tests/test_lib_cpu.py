@@ -96,3 +96,19 @@ def test_wavefront_chunking_plan(lib):
     assert "chunk=5 nchunks=10" in r.describe()
     r = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, flags=rnn.FLAG_NO_WAVEFRONT)
     assert "wavefront=0 chunk=50 nchunks=1" in r.describe()
+
+
+def test_backward_split_plan_invariants(lib):
+    """Backward-step K splits: a power of two that the K blocks fill exactly
+    (every split has work) and that cuts a tile into 16-column slices."""
+    import re
+    for cell in (0, 1, 2):
+        G = {0: 4, 1: 3, 2: 1}[cell]
+        for H in (64, 128, 192, 256, 320, 512, 768, 1024, 2048, 4096):
+            for B in (1, 4, 32, 64, 130, 256):
+                d = rnn.RNN(cell, 1, 3, B, 64, H, 1, flags=rnn.FLAG_FORCE_STREAMING).describe()
+                bn = int(re.search(r"bwd_bn=(\d+)", d).group(1))
+                sp = int(re.search(r"bwd_splits=(\d+)", d).group(1))
+                kb = (G * H + 63) // 64
+                per = -(-kb // sp)
+                assert sp & (sp - 1) == 0 and -(-kb // per) == sp and bn % (16 * sp) == 0, (cell, H, B, bn, sp)
