@@ -114,6 +114,7 @@ struct rnn_s {
   // plan
   int chunk = 1, nch = 1, wavefront = 0, bwd_bn = 128, bwd_splits = 1;
   int persist = 0, persist_ctas = 0;  // forward recurrence kind: 1 = persistent (one launch per layer)
+  int fwd_mcast = 4;  // forward-step clusters along N sharing h_{t-1} by TMA multicast
   uint64_t limit_ns = 2000000000ull;
   // sizes (bytes)
   size_t user_w_bytes = 0, packed_bytes = 0, reserve_bytes = 0, ws_bytes = 0;
@@ -178,6 +179,7 @@ int plan_and_layout(rnn_s* h) {
     }
   }
   if ((d.flags & RNN_FLAG_FORCE_PERSISTENT) && !h->persist) return RNN_ERR_UNSUPPORTED;
+  h->fwd_mcast = (d.flags & RNN_FLAG_NO_MULTICAST) ? 1 : 4;
   // wavefront chunking
   h->wavefront = (L > 1) && !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !h->persist;
   if (!h->wavefront) h->chunk = T;
@@ -391,9 +393,9 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : "tanh";
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
-           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d",
+           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
-           h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->num_sms);
+           h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms);
   return RNN_OK;
 }
 
@@ -516,6 +518,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
           a.hT = (t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
           a.cT = (t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
           a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
+          a.mcast = h->fwd_mcast;
           Operand A{hseq + (size_t)t * BH * e, H, 0, B, H};
           Operand Bw{PW + h->pl[l].wh, H, 0, GH, H};
           Launch Lk = mk(h, s, ws, "fwd_step");

@@ -34,6 +34,8 @@ struct GemmGeom {
   uint64_t limit_ns;           // bound on every pipeline wait
   int* err;                    // device error word
   int cluster;                 // > 1: the split-K CTAs of a tile form one thread-block cluster
+  int mcast;                   // > 1: clusters of `mcast` CTAs along N share (multicast) their A tile
+  int nfast;                   // tile order: n-tiles fastest (needed by multicast clusters)
 };
 
 struct TileCoord {
@@ -65,8 +67,13 @@ struct SmemAcc {
 __device__ __forceinline__ void decode_tile(const GemmGeom& g, int tile, int& mt, int& nt, int& split) {
   split = tile % g.splits;
   const int mn = tile / g.splits;
-  mt = mn % g.m_tiles;
-  nt = mn / g.m_tiles;
+  if (g.nfast) {
+    nt = mn % g.n_tiles;
+    mt = mn / g.n_tiles;
+  } else {
+    mt = mn % g.m_tiles;
+    nt = mn / g.m_tiles;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -113,7 +120,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, 1);
+      tc::mbar_init(empty + s, g.mcast);  // every CTA of a multicast cluster frees the stage
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull + a, 1);
@@ -133,12 +140,14 @@ __global__ void __launch_bounds__(192, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (g.cluster > 1) tc::cluster_sync_all();  // peers' barriers are initialised before any remote arrive
+  if (g.cluster > 1 || g.mcast > 1) tc::cluster_sync_all();  // peers' barriers exist before any remote traffic
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const int crank = g.mcast > 1 ? (int)tc::cluster_ctarank() : 0;
+      const uint16_t mc_mask = (uint16_t)((1u << g.mcast) - 1u);
       uint32_t stage = 0, phase = 0;
       int last_par[STAGES];  // parity of the last load issued into each stage (-1: none)
       for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
@@ -159,7 +168,11 @@ __global__ void __launch_bounds__(192, 1)
           tc::mbar_arrive_expect_tx(full + stage, STAGE);
           last_par[stage] = static_cast<int>(phase);
           const int k0 = kb * BK;
-          if (g.a_mn) {
+          if (g.mcast > 1) {
+            // this CTA's 1/mcast of the A rows, into every peer's stage
+            const int rows = BM / g.mcast;
+            tc::tma_load_2d_mc(sa + crank * rows * 128, &mapA, full + stage, k0, m0 + crank * rows, mc_mask);
+          } else if (g.a_mn) {
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j) tc::tma_load_2d(sa + j * 8192, &mapA, full + stage, m0 + 64 * j, k0);
           } else {
@@ -218,7 +231,8 @@ __global__ void __launch_bounds__(192, 1)
                                        : tc::sdesc_sw128(sb + kk * 32, 16, 1024);
             tc::mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          tc::mma_commit(empty + stage);
+          if (g.mcast > 1) tc::mma_commit_mc(empty + stage, (uint16_t)((1u << g.mcast) - 1u));
+          else tc::mma_commit(empty + stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -287,7 +301,7 @@ __global__ void __launch_bounds__(192, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem_base, TMEM_COLS);
   }
-  if (g.cluster > 1) tc::cluster_sync_all();  // no peer touches this CTA's shared memory after it exits
+  if (g.cluster > 1 || g.mcast > 1) tc::cluster_sync_all();  // no peer touches this CTA's shared memory after it exits
 }
 
 // ---------------------------------------------------------------------------

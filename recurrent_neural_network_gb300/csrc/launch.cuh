@@ -63,13 +63,18 @@ inline int cuda_status(cudaError_t e) {
 // cluster_splitk: with more than one K split, the splits of each output tile
 // run as one thread-block cluster and reduce through distributed shared
 // memory (the epilogue must support it); one tile per CTA.
+// mcast > 1: CTAs that share an m-tile run as clusters of `mcast` along N and
+// multicast their A tile (each loads BM/mcast rows); used when the shape
+// allows it (K-major A, no split, n-tiles a multiple of mcast), else ignored.
 template <int BN, int STAGES, class Epi>
 int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, int splits, int max_ctas,
-              const Epi& epi, bool cluster_splitk = false) {
+              const Epi& epi, bool cluster_splitk = false, int mcast = 1) {
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
   if (B.mn_major && BN % 64) return RNN_ERR_UNSUPPORTED;
+  const int n_tiles = (N + BN - 1) / BN;
+  if (!(mcast == 2 || mcast == 4 || mcast == 8) || A.mn_major || splits > 1 || n_tiles % mcast) mcast = 1;
   CUtensorMap ma, mb;
-  int rc = encode_operand(&ma, A, tce::BM);
+  int rc = encode_operand(&ma, A, tce::BM / mcast);
   if (rc) return rc;
   rc = encode_operand(&mb, B, BN);
   if (rc) return rc;
@@ -93,6 +98,8 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   // multiple of 16*splits and at most 8 CTAs per cluster.  Otherwise the
   // partials go through global memory.
   g.cluster = (cluster_splitk && g.splits > 1 && g.splits <= 8 && BN % (16 * g.splits) == 0) ? g.splits : 1;
+  g.mcast = g.cluster > 1 ? 1 : mcast;
+  g.nfast = g.mcast > 1 ? 1 : 0;
   constexpr int smem = tce::smem_bytes<BN, STAGES>();
   auto kern = tc_gemm_kernel<BN, STAGES, Epi>;
   static bool attr = false;
@@ -103,17 +110,19 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   }
   int cap = max_ctas > 0 ? max_ctas : L.num_sms;
   int grid = std::min(g.num_tiles, cap);
+  if (g.mcast > 1) grid = std::max(g.mcast, grid / g.mcast * g.mcast);
+  const int cl = g.cluster > 1 ? g.cluster : g.mcast;
   cudaError_t e;
   launch_begin(L);
-  if (g.cluster > 1) {
+  if (cl > 1) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(g.num_tiles);
+    cfg.gridDim = dim3(g.cluster > 1 ? g.num_tiles : grid);
     cfg.blockDim = dim3(192);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = g.cluster;
+    at[0].val.clusterDim.x = cl;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
@@ -141,6 +150,8 @@ int launch_simt(const Launch& L, const Operand& A, const Operand& B, int M, int 
   g.kb_per_split = g.kb_total;
   g.num_tiles = g.m_tiles * g.n_tiles;
   g.cluster = 1;
+  g.mcast = 1;
+  g.nfast = 0;
   g.a_mn = A.mn_major;
   g.b_mn = B.mn_major;
   g.limit_ns = L.limit_ns;

@@ -39,10 +39,12 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
   if (mode == 1) {
     using S = __nv_bfloat16;
     // the tile width is one packed block of G*u gate rows
-    if (cell == LSTM && a.u == 64) return launch_tc<256, 4>(L, A, Bw, M, N, K, 1, 0, make_epi<LSTM, S>(a));
-    if (cell == GRU && a.u == 64) return launch_tc<192, 5>(L, A, Bw, M, N, K, 1, 0, make_epi<GRU, S>(a));
-    if (cell == TANH && a.u == 128) return launch_tc<128, 6>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a));
-    if (cell == TANH && a.u == 64) return launch_tc<64, 8>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a));
+    // the batch rows h_{t-1} are shared by every n-tile: multicast them within clusters along N
+    const int mc = a.mcast;
+    if (cell == LSTM && a.u == 64) return launch_tc<256, 4>(L, A, Bw, M, N, K, 1, 0, make_epi<LSTM, S>(a), false, mc);
+    if (cell == GRU && a.u == 64) return launch_tc<192, 5>(L, A, Bw, M, N, K, 1, 0, make_epi<GRU, S>(a), false, mc);
+    if (cell == TANH && a.u == 128) return launch_tc<128, 6>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a), false, mc);
+    if (cell == TANH && a.u == 64) return launch_tc<64, 8>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a), false, mc);
     return RNN_ERR_UNSUPPORTED;
   }
   using S = float;

@@ -22,6 +22,7 @@ FLAG_NO_WAVEFRONT = 0x1
 FLAG_FORCE_STREAMING = 0x2
 FLAG_FORCE_PERSISTENT = 0x4
 FLAG_PROFILE = 0x8
+FLAG_NO_MULTICAST = 0x10
 FLAG_TEST_SKIP_PUBLISH = 0x100
 
 # every symbol include/rnn.h declares
