@@ -304,6 +304,7 @@ Launch mk(rnn_s* h, cudaStream_t s, void* ws, const char* name) {
   L.num_sms = h->num_sms;
   L.prof = (h->d.flags & RNN_FLAG_PROFILE) ? h->prof : nullptr;
   L.name = name;
+  L.pair = (h->d.flags & RNN_FLAG_NO_PAIR) ? 0 : 1;
   return L;
 }
 

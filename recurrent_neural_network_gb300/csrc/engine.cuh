@@ -305,6 +305,217 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ---------------------------------------------------------------------------
+// tcgen05 engine on CTA pairs (cta_group::2): a cluster of 2 CTAs computes a
+// 256 x BN tile.  Each CTA loads its 128 rows of A and its BN/2 rows of B
+// (so the pair reads every byte of a tile once), the even CTA issues the
+// M=256 MMAs for both, each CTA's TMEM receives its 128 rows of the result
+// and each CTA runs the epilogue on them.  Per SM this needs 32 KB of operand
+// traffic per 64-deep K block instead of 48 KB for the same MMA work, which
+// is what keeps the tensor pipe fed when the loads come from HBM.
+//   full[s]    even CTA only: both CTAs' TMA bytes of stage s
+//   empty[s]   both CTAs: the pair's MMAs have read stage s
+//   tfull[a]   both CTAs: accumulator a is complete
+//   tempty[a]  even CTA only: both CTAs' epilogues have read accumulator a
+// ---------------------------------------------------------------------------
+namespace tce2 {
+constexpr int BM = 256;  // pair tile rows; 128 per CTA
+constexpr int BK = 64;
+constexpr int A_BYTES = 128 * BK * 2;
+template <int BN>
+__host__ __device__ constexpr int stage_bytes() { return A_BYTES + (BN / 2) * BK * 2; }
+template <int BN, int STAGES>
+__host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>() + 1024 + 256; }
+}  // namespace tce2
+
+template <int BN, int STAGES, class Epi>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                    const GemmGeom g, const Epi epi) {
+  using namespace tce2;
+  constexpr int STAGE = stage_bytes<BN>();
+  constexpr uint32_t TMEM_COLS = tce::tmem_cols<BN>();
+  constexpr int HB = BN / 2;  // B rows per CTA
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=256");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* scratch = reinterpret_cast<int*>(tmem_slot + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = tc::cluster_ctarank();  // 0 = the CTA that issues the MMAs
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(tfull + a, 1);
+      tc::mbar_init(tempty + a, 8);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::tma_prefetch_desc(&mapA);
+    tc::tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish_pair();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  tc::cluster_sync_all();  // both CTAs' barriers and TMEM exist before any pair traffic
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int last_par[STAGES];
+      for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
+      bool ok = true;
+      for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
+        int mt, nt, split;
+        decode_tile(g, tile, mt, nt, split);
+        const int kb0 = split * g.kb_per_split;
+        const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
+        const int m0 = mt * BM + (int)rank * 128, n0 = nt * BN + (int)rank * HB;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, g.err, g.limit_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * STAGE;
+          uint8_t* sb = sa + A_BYTES;
+          const uint32_t fb = tc::mapa(tc::smem_addr(full + stage), 0);
+          if (rank == 0) tc::mbar_arrive_expect_tx(full + stage, 2 * STAGE);
+          last_par[stage] = static_cast<int>(phase);
+          const int k0 = kb * BK;
+          if (g.a_mn) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tc::tma_load_2d_pair(sa + j * 8192, &mapA, fb, m0 + 64 * j, k0);
+          } else {
+            tc::tma_load_2d_pair(sa, &mapA, fb, k0, m0);
+          }
+          if (g.b_mn) {
+#pragma unroll
+            for (int j = 0; j < HB / 64; ++j) tc::tma_load_2d_pair(sb + j * 8192, &mapB, fb, n0 + 64 * j, k0);
+          } else {
+            tc::tma_load_2d_pair(sb, &mapB, fb, k0, n0);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok && rank == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+          if (last_par[s] < 0) continue;
+          const uint64_t t0 = globaltimer_ns();
+          while (!tc::mbar_try_wait(full + s, static_cast<uint32_t>(last_par[s])) &&
+                 globaltimer_ns() - t0 < 1000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = tc::idesc_bf16(BM, BN, g.a_mn, g.b_mn);
+      uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
+      bool ok = true;
+      for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
+        int mt, nt, split;
+        decode_tile(g, tile, mt, nt, split);
+        const int kb0 = split * g.kb_per_split;
+        const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
+        if (!tc::mbar_wait(tempty + acc, aphase ^ 1, abort_flag, g.err, g.limit_ns)) break;
+        tc::fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!tc::mbar_wait(full + stage, phase, abort_flag, g.err, g.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t sa = tc::smem_addr(smem + stage * STAGE);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = g.a_mn ? tc::sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                       : tc::sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = g.b_mn ? tc::sdesc_sw128(sb + kk * 2048, 8192, 1024)
+                                       : tc::sdesc_sw128(sb + kk * 32, 16, 1024);
+            tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit_pair(empty + stage, 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit_pair(tfull + acc, 0x3);
+        acc ^= 1;
+        if (acc == 0) aphase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps (both CTAs)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const uint32_t te_base = tc::mapa(tc::smem_addr(tempty), 0);
+    uint32_t acc = 0, aphase = 0;
+    for (int tile = pair; tile < g.num_tiles; tile += npairs) {
+      int mt, nt, split;
+      decode_tile(g, tile, mt, nt, split);
+      TileCoord t;
+      t.m0 = mt * BM + (int)rank * 128;
+      t.n0 = nt * BN;
+      t.mt = mt * 2 + (int)rank;
+      t.nt = nt;
+      t.split = split;
+      t.splits = g.splits;
+      t.scratch = scratch;
+      t.cluster = 1;
+      t.red = nullptr;
+      t.red_full = t.red_done = nullptr;
+      epi.prefetch(t, row, BN);
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc::fence_after_sync();
+      TmemAcc a{tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16)};
+      epi(t, row, a, BN);
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_remote(te_base + acc * 8);
+      acc ^= 1;
+      if (acc == 0) aphase ^= 1;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::cluster_sync_all();  // the pair's MMAs and remote arrivals are done before TMEM and smem go away
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // fp32 SIMT engine (FFMA): 32 x BN tiles, 128 threads, K step 16.
 // ---------------------------------------------------------------------------
 namespace se {

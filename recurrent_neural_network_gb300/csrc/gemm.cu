@@ -17,6 +17,7 @@ template <class OutT>
 int run_store(const Launch& L, int mode, const Operand& A, const Operand& B, int M, int N, int K,
               const EpiStore<OutT>& epi, int max_ctas) {
   if (mode == 1) {
+    if (N > 128 && M > 128 && L.pair) return launch_tc2<256, 6>(L, A, B, M, N, K, max_ctas, epi);
     if (N > 128) return launch_tc<256, 4>(L, A, B, M, N, K, 1, max_ctas, epi);
     return launch_tc<128, 6>(L, A, B, M, N, K, 1, max_ctas, epi);
   }

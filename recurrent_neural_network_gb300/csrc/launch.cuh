@@ -136,6 +136,62 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   return cuda_status(e);
 }
 
+// CTA-pair engine: 256 x BN tiles over clusters of 2 CTAs (no split-K).
+template <int BN, int STAGES, class Epi>
+int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, int max_ctas,
+               const Epi& epi) {
+  if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
+  if (B.mn_major && (BN / 2) % 64) return RNN_ERR_UNSUPPORTED;
+  CUtensorMap ma, mb;
+  int rc = encode_operand(&ma, A, 128);
+  if (rc) return rc;
+  rc = encode_operand(&mb, B, BN / 2);
+  if (rc) return rc;
+  GemmGeom g;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.m_tiles = (M + tce2::BM - 1) / tce2::BM;
+  g.n_tiles = (N + BN - 1) / BN;
+  g.kb_total = (K + tce2::BK - 1) / tce2::BK;
+  g.splits = 1;
+  g.kb_per_split = g.kb_total;
+  g.num_tiles = g.m_tiles * g.n_tiles;
+  g.a_mn = A.mn_major;
+  g.b_mn = B.mn_major;
+  g.limit_ns = L.limit_ns;
+  g.err = L.err;
+  g.cluster = 1;
+  g.mcast = 1;
+  g.nfast = 0;
+  constexpr int smem = tce2::smem_bytes<BN, STAGES>();
+  auto kern = tc_gemm2_kernel<BN, STAGES, Epi>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_status(e);
+    attr = true;
+  }
+  const int cap = (max_ctas > 0 ? max_ctas : L.num_sms) / 2;
+  const int pairs = std::max(1, std::min(g.num_tiles, cap));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  launch_begin(L);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, g, epi);
+  launch_end(L);
+  return cuda_status(e);
+}
+
 template <int BN, class Epi>
 int launch_simt(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, const Epi& epi) {
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;

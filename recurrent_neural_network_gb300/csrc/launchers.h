@@ -28,6 +28,7 @@ struct Launch {
   int num_sms;
   Profiler* prof;
   const char* name;
+  int pair = 1;  // products with more than 128 rows may run on CTA pairs (256-row tiles)
 };
 
 // profiling / counting hooks (api.cu)

@@ -41,6 +41,12 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
     // the tile width is one packed block of G*u gate rows
     // the batch rows h_{t-1} are shared by every n-tile: multicast them within clusters along N
     const int mc = a.mcast;
+    // more than 128 batch rows: 256-row tiles on CTA pairs
+    if (M > 128 && L.pair) {
+      if (cell == LSTM && a.u == 64) return launch_tc2<256, 6>(L, A, Bw, M, N, K, 0, make_epi<LSTM, S>(a));
+      if (cell == GRU && a.u == 64) return launch_tc2<192, 7>(L, A, Bw, M, N, K, 0, make_epi<GRU, S>(a));
+      if (cell == TANH && a.u == 128) return launch_tc2<128, 8>(L, A, Bw, M, N, K, 0, make_epi<TANH, S>(a));
+    }
     if (cell == LSTM && a.u == 64) return launch_tc<256, 4>(L, A, Bw, M, N, K, 1, 0, make_epi<LSTM, S>(a), false, mc);
     if (cell == GRU && a.u == 64) return launch_tc<192, 5>(L, A, Bw, M, N, K, 1, 0, make_epi<GRU, S>(a), false, mc);
     if (cell == TANH && a.u == 128) return launch_tc<128, 6>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a), false, mc);
