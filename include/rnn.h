@@ -81,6 +81,8 @@ enum {
 #define RNN_FLAG_PROFILE 0x8u           /* record per-kernel CUDA-event timings */
 #define RNN_FLAG_NO_MULTICAST 0x10u     /* forward steps load h_{t-1} per CTA (no cluster multicast) */
 #define RNN_FLAG_NO_PAIR 0x20u          /* keep every product on single-CTA 128-row tiles */
+#define RNN_FLAG_NO_GRAPH 0x40u         /* enqueue kernels directly; by default a call whose pointers were
+                                           seen before replays a cached CUDA graph of its launches */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */

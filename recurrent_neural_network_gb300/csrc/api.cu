@@ -32,7 +32,10 @@ struct Profiler {
   struct Rec {
     int cls;
     cudaEvent_t a, b;
+    bool graph = false;  // recorded by a captured graph: its events belong to that graph
   };
+  bool capturing = false;
+  std::vector<Rec> captured;
   std::mutex mu;
   std::vector<std::string> names;
   std::vector<unsigned long long> launches;
@@ -66,8 +69,10 @@ struct Profiler {
         total_ms[r.cls] += ms;
         launches[r.cls] += 1;
       }
-      pool.push_back(r.a);
-      pool.push_back(r.b);
+      if (!r.graph) {
+        pool.push_back(r.a);
+        pool.push_back(r.b);
+      }
     }
     pending.clear();
   }
@@ -87,8 +92,14 @@ void launch_begin(const Launch& L) {
   Profiler& p = *L.prof;
   std::lock_guard<std::mutex> g(p.mu);
   p.open.cls = p.cls_of(L.name ? L.name : "kernel");
-  p.open.a = p.event();
-  p.open.b = p.event();
+  p.open.graph = p.capturing;
+  if (p.capturing) {  // events owned by the graph being captured
+    cudaEventCreate(&p.open.a);
+    cudaEventCreate(&p.open.b);
+  } else {
+    p.open.a = p.event();
+    p.open.b = p.event();
+  }
   cudaEventRecord(p.open.a, L.stream);
 }
 
@@ -98,7 +109,8 @@ void launch_end(const Launch& L, int n_kernels) {
   Profiler& p = *L.prof;
   std::lock_guard<std::mutex> g(p.mu);
   cudaEventRecord(p.open.b, L.stream);
-  p.pending.push_back(p.open);
+  if (p.capturing) p.captured.push_back(p.open);
+  else p.pending.push_back(p.open);
 }
 
 }  // namespace rnn
@@ -137,6 +149,16 @@ struct rnn_s {
   cudaEvent_t ev_fork = nullptr;
   std::vector<cudaEvent_t> ev_join;
   Profiler* prof = nullptr;
+  // launch sequences captured as CUDA graphs, keyed by call kind and pointers
+  struct GraphEntry {
+    std::vector<uintptr_t> key;
+    cudaGraphExec_t exec = nullptr;
+    std::vector<Profiler::Rec> prof;
+    unsigned long long kernels = 0;
+  };
+  std::vector<GraphEntry> graphs;
+  std::vector<std::vector<uintptr_t>> seen, no_graph;
+  cudaStream_t cap = nullptr;
 
   int In(int l) const { return l == 0 ? d.input : d.hidden; }
 };
@@ -308,6 +330,96 @@ Launch mk(rnn_s* h, cudaStream_t s, void* ws, const char* name) {
   return L;
 }
 
+// Runs `issue` (which enqueues a whole call on the stream it is given) through
+// a cached CUDA graph: the first call with a given key runs directly, the
+// second is captured (on an internal stream, with the layer streams forked
+// from it) and every later one replays the graph on the caller's stream, so a
+// call costs one graph launch instead of hundreds of kernel launches.  A
+// capture that fails leaves the key on the direct path.
+template <class F>
+int run_graphed(rnn_s* h, cudaStream_t user, const std::vector<uintptr_t>& key, F&& issue) {
+  if (h->d.flags & RNN_FLAG_NO_GRAPH) return issue(user);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(user, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return issue(user);
+  for (auto& g : h->graphs) {
+    if (g.key != key) continue;
+    if (cudaGraphLaunch(g.exec, user) != cudaSuccess) return RNN_ERR_CUDA;
+    g_launches += g.kernels;
+    if (h->prof && (h->d.flags & RNN_FLAG_PROFILE)) {
+      std::lock_guard<std::mutex> lk(h->prof->mu);
+      for (auto& r : g.prof) {
+        h->prof->pending.push_back(r);
+      }
+    }
+    return RNN_OK;
+  }
+  auto in = [&](const std::vector<std::vector<uintptr_t>>& v) { return std::find(v.begin(), v.end(), key) != v.end(); };
+  if (in(h->no_graph)) return issue(user);
+  if (!in(h->seen)) {
+    if (h->seen.size() >= 64) h->seen.erase(h->seen.begin());
+    h->seen.push_back(key);
+    return issue(user);
+  }
+  if (!h->cap && cudaStreamCreateWithFlags(&h->cap, cudaStreamNonBlocking) != cudaSuccess) return issue(user);
+  const unsigned long long before = g_launches.load();
+  if (cudaStreamBeginCapture(h->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    h->no_graph.push_back(key);
+    return issue(user);
+  }
+  if (h->prof) {
+    std::lock_guard<std::mutex> lk(h->prof->mu);
+    h->prof->capturing = true;
+    h->prof->captured.clear();
+  }
+  const int rc = issue(h->cap);
+  cudaGraph_t gr = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(h->cap, &gr);
+  std::vector<Profiler::Rec> recs;
+  if (h->prof) {
+    std::lock_guard<std::mutex> lk(h->prof->mu);
+    h->prof->capturing = false;
+    recs.swap(h->prof->captured);
+  }
+  const unsigned long long kernels = g_launches.load() - before;
+  g_launches -= kernels;  // captured, not run
+  cudaGraphExec_t ex = nullptr;
+  const bool ok = rc == RNN_OK && e == cudaSuccess && gr && cudaGraphInstantiate(&ex, gr, 0) == cudaSuccess;
+  if (gr) cudaGraphDestroy(gr);
+  if (!ok) {
+    cudaGetLastError();
+    for (auto& r : recs) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+    h->no_graph.push_back(key);
+    return issue(user);
+  }
+  if (h->graphs.size() >= 8) {  // evict the oldest (let it finish first)
+    cudaDeviceSynchronize();
+    cudaGraphExecDestroy(h->graphs.front().exec);
+    for (auto& r : h->graphs.front().prof) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+    h->graphs.erase(h->graphs.begin());
+  }
+  rnn_s::GraphEntry ge;
+  ge.key = key;
+  ge.exec = ex;
+  ge.prof = std::move(recs);
+  ge.kernels = kernels;
+  h->graphs.push_back(std::move(ge));
+  auto& g = h->graphs.back();
+  if (cudaGraphLaunch(g.exec, user) != cudaSuccess) return RNN_ERR_CUDA;
+  g_launches += g.kernels;
+  if (h->prof && (h->d.flags & RNN_FLAG_PROFILE)) {
+    std::lock_guard<std::mutex> lk(h->prof->mu);
+    for (auto& r : g.prof) h->prof->pending.push_back(r);
+  }
+  return RNN_OK;
+}
+
 #define RNN_TRY(x)              \
   do {                          \
     int rc__ = (x);             \
@@ -374,6 +486,15 @@ int rnn_destroy(rnn_handle_t h) {
     for (auto e : h->ev_join) cudaEventDestroy(e);
     if (h->ev_fork) cudaEventDestroy(h->ev_fork);
   }
+  if (!h->graphs.empty()) cudaDeviceSynchronize();
+  for (auto& g : h->graphs) {
+    cudaGraphExecDestroy(g.exec);
+    for (auto& r : g.prof) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+  }
+  if (h->cap) cudaStreamDestroy(h->cap);
   delete h->prof;
   delete h;
   return RNN_OK;
@@ -426,111 +547,115 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
                         (const void*)reserve, (const void*)ws})
     if (!aligned16(p)) return RNN_ERR_INVALID_ARG;
   RNN_TRY(ensure_runtime(h));
-  const rnn_desc_t& d = h->d;
-  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, G = h->G, GH = h->GH, mode = d.mode;
-  const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
-  const bool train = reserve != nullptr;
-  const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
-  char* R = static_cast<char*>(reserve);
-  char* W = static_cast<char*>(ws);
-  const char* PW = static_cast<const char*>(w_packed);
-  (void)G;
+  const std::vector<uintptr_t> key = {1, (uintptr_t)x, (uintptr_t)h0, (uintptr_t)c0, (uintptr_t)w_packed, (uintptr_t)y, (uintptr_t)hT, (uintptr_t)cT, (uintptr_t)reserve, (uintptr_t)ws};
+  auto issue = [&](cudaStream_t stream) -> int {
+    const rnn_desc_t& d = h->d;
+    const int L = d.layers, T = d.T, B = d.B, H = d.hidden, G = h->G, GH = h->GH, mode = d.mode;
+    const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
+    const bool train = reserve != nullptr;
+    const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+    char* R = static_cast<char*>(reserve);
+    char* W = static_cast<char*>(ws);
+    const char* PW = static_cast<const char*>(w_packed);
+    (void)G;
 
-  if (h->wavefront) RNN_TRY(fork_streams(h, stream));
-  const int nd = h->wavefront ? (L + h->nch - 1) : 1;
-  for (int dg = 0; dg < nd; ++dg) {
-    for (int l = 0; l < L; ++l) {
-      for (int c = 0; c < h->nch; ++c) {
-        if (h->wavefront && l + c != dg) continue;
-        cudaStream_t s = h->wavefront ? h->streams[l] : stream;
-        const int t0 = c * h->chunk, t1 = std::min(T, t0 + h->chunk);
-        char* hseq = train ? R + h->rl[l].hseq : W + h->wl[l].hseq;
-        float* P = reinterpret_cast<float*>(train ? R + h->rl[l].gates : W + h->wl[l].P);
-        if (c == 0) {
-          if (h0) RNN_TRY(cu(cudaMemcpyAsync(hseq, static_cast<const char*>(h0) + l * BH * e, BH * e,
-                                             cudaMemcpyDeviceToDevice, s)));
-          else RNN_TRY(cu(cudaMemsetAsync(hseq, 0, BH * e, s)));
+    if (h->wavefront) RNN_TRY(fork_streams(h, stream));
+    const int nd = h->wavefront ? (L + h->nch - 1) : 1;
+    for (int dg = 0; dg < nd; ++dg) {
+      for (int l = 0; l < L; ++l) {
+        for (int c = 0; c < h->nch; ++c) {
+          if (h->wavefront && l + c != dg) continue;
+          cudaStream_t s = h->wavefront ? h->streams[l] : stream;
+          const int t0 = c * h->chunk, t1 = std::min(T, t0 + h->chunk);
+          char* hseq = train ? R + h->rl[l].hseq : W + h->wl[l].hseq;
+          float* P = reinterpret_cast<float*>(train ? R + h->rl[l].gates : W + h->wl[l].P);
+          if (c == 0) {
+            if (h0) RNN_TRY(cu(cudaMemcpyAsync(hseq, static_cast<const char*>(h0) + l * BH * e, BH * e,
+                                               cudaMemcpyDeviceToDevice, s)));
+            else RNN_TRY(cu(cudaMemsetAsync(hseq, 0, BH * e, s)));
+          }
+          if (h->wavefront && l > 0) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l - 1) * h->nch + c], 0)));
+          // input projection (layer 0: all T at once)
+          if (l > 0 || c == 0) {
+            const int r0 = l == 0 ? 0 : t0, r1 = l == 0 ? T : t1;
+            const int In = h->In(l);
+            Operand A;
+            A.ptr = l == 0 ? static_cast<const char*>(x) + (size_t)r0 * B * In * e
+                           : static_cast<const char*>(train ? R + h->rl[l - 1].hseq : W + h->wl[l - 1].hseq) +
+                                 (size_t)(r0 + 1) * BH * e;
+            A.ld = In;
+            A.mn_major = 0;
+            A.mn_ext = (r1 - r0) * B;
+            A.k_ext = In;
+            Operand Bw{PW + h->pl[l].wx, In, 0, GH, In};
+            Remap none{0, 1, 1, 1};
+            Launch Lk = mk(h, s, ws, "input_proj_gemm");
+            RNN_TRY(gemm_f32(Lk, mode, A, Bw, (r1 - r0) * B, GH, In, P + (size_t)r0 * BGH, GH,
+                             reinterpret_cast<const float*>(PW + h->pl[l].bias), 0, none, 0));
+          }
+          // persistent recurrence: all T steps of the layer in one launch
+          if (h->persist) {
+            unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
+            RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
+            PersistArgs pa{};
+            pa.arrive = arrive;
+            pa.T = T;
+            pa.B = B;
+            pa.H = H;
+            pa.u_pack = h->u;
+            pa.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
+            pa.P = P;
+            pa.gates_out = train ? P : nullptr;
+            pa.bias_hn = reinterpret_cast<const float*>(PW + h->pl[l].bias_hn);
+            pa.c0 = (lstm && c0) ? c0 + l * BH : nullptr;
+            pa.c_out = (train && lstm) ? reinterpret_cast<float*>(R + h->rl[l].c) : nullptr;
+            pa.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) : nullptr;
+            pa.hseq = reinterpret_cast<__nv_bfloat16*>(hseq);
+            pa.y = l == L - 1 ? static_cast<__nv_bfloat16*>(y) : nullptr;
+            pa.hT = hT ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(hT) + (size_t)l * BH * e) : nullptr;
+            pa.cT = (cT && lstm) ? cT + (size_t)l * BH : nullptr;
+            pa.err = reinterpret_cast<int*>(W + h->ws_err);
+            pa.limit_ns = h->limit_ns;
+            pa.test_skip_publish = (d.flags & RNN_FLAG_TEST_SKIP_PUBLISH) ? 1 : 0;
+            Launch Lk = mk(h, s, ws, "persist_fwd");
+            RNN_TRY(persist_fwd(Lk, d.cell, pa));
+            continue;
+          }
+          // recurrent steps of the chunk
+          for (int t = t0; t < t1; ++t) {
+            FwdStepArgs a;
+            a.B = B;
+            a.H = H;
+            a.u = h->u;
+            a.P = P + (size_t)t * BGH;
+            a.write_gates = train ? 1 : 0;
+            a.bias_hn = reinterpret_cast<const float*>(PW + h->pl[l].bias_hn);
+            auto cbuf = [&](int tt) -> float* {
+              return train ? reinterpret_cast<float*>(R + h->rl[l].c) + (size_t)tt * BH
+                           : reinterpret_cast<float*>(W + h->wl[l].c2) + (size_t)(tt & 1) * BH;
+            };
+            a.c_prev = lstm ? (t == 0 ? (c0 ? c0 + l * BH : nullptr) : cbuf(t - 1)) : nullptr;
+            a.c_out = lstm ? cbuf(t) : nullptr;
+            a.h_prev = hseq + (size_t)t * BH * e;
+            a.h_out = hseq + (size_t)(t + 1) * BH * e;
+            a.y = l == L - 1 ? static_cast<char*>(y) + (size_t)t * BH * e : nullptr;
+            a.hT = (t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
+            a.cT = (t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
+            a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
+            a.mcast = h->fwd_mcast;
+            Operand A{hseq + (size_t)t * BH * e, H, 0, B, H};
+            Operand Bw{PW + h->pl[l].wh, H, 0, GH, H};
+            Launch Lk = mk(h, s, ws, "fwd_step");
+            RNN_TRY(fwd_step(Lk, mode, d.cell, A, Bw, a));
+          }
+          if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + c], s)));
         }
-        if (h->wavefront && l > 0) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l - 1) * h->nch + c], 0)));
-        // input projection (layer 0: all T at once)
-        if (l > 0 || c == 0) {
-          const int r0 = l == 0 ? 0 : t0, r1 = l == 0 ? T : t1;
-          const int In = h->In(l);
-          Operand A;
-          A.ptr = l == 0 ? static_cast<const char*>(x) + (size_t)r0 * B * In * e
-                         : static_cast<const char*>(train ? R + h->rl[l - 1].hseq : W + h->wl[l - 1].hseq) +
-                               (size_t)(r0 + 1) * BH * e;
-          A.ld = In;
-          A.mn_major = 0;
-          A.mn_ext = (r1 - r0) * B;
-          A.k_ext = In;
-          Operand Bw{PW + h->pl[l].wx, In, 0, GH, In};
-          Remap none{0, 1, 1, 1};
-          Launch Lk = mk(h, s, ws, "input_proj_gemm");
-          RNN_TRY(gemm_f32(Lk, mode, A, Bw, (r1 - r0) * B, GH, In, P + (size_t)r0 * BGH, GH,
-                           reinterpret_cast<const float*>(PW + h->pl[l].bias), 0, none, 0));
-        }
-        // persistent recurrence: all T steps of the layer in one launch
-        if (h->persist) {
-          unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
-          RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
-          PersistArgs pa{};
-          pa.arrive = arrive;
-          pa.T = T;
-          pa.B = B;
-          pa.H = H;
-          pa.u_pack = h->u;
-          pa.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
-          pa.P = P;
-          pa.gates_out = train ? P : nullptr;
-          pa.bias_hn = reinterpret_cast<const float*>(PW + h->pl[l].bias_hn);
-          pa.c0 = (lstm && c0) ? c0 + l * BH : nullptr;
-          pa.c_out = (train && lstm) ? reinterpret_cast<float*>(R + h->rl[l].c) : nullptr;
-          pa.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) : nullptr;
-          pa.hseq = reinterpret_cast<__nv_bfloat16*>(hseq);
-          pa.y = l == L - 1 ? static_cast<__nv_bfloat16*>(y) : nullptr;
-          pa.hT = hT ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(hT) + (size_t)l * BH * e) : nullptr;
-          pa.cT = (cT && lstm) ? cT + (size_t)l * BH : nullptr;
-          pa.err = reinterpret_cast<int*>(W + h->ws_err);
-          pa.limit_ns = h->limit_ns;
-          pa.test_skip_publish = (d.flags & RNN_FLAG_TEST_SKIP_PUBLISH) ? 1 : 0;
-          Launch Lk = mk(h, s, ws, "persist_fwd");
-          RNN_TRY(persist_fwd(Lk, d.cell, pa));
-          continue;
-        }
-        // recurrent steps of the chunk
-        for (int t = t0; t < t1; ++t) {
-          FwdStepArgs a;
-          a.B = B;
-          a.H = H;
-          a.u = h->u;
-          a.P = P + (size_t)t * BGH;
-          a.write_gates = train ? 1 : 0;
-          a.bias_hn = reinterpret_cast<const float*>(PW + h->pl[l].bias_hn);
-          auto cbuf = [&](int tt) -> float* {
-            return train ? reinterpret_cast<float*>(R + h->rl[l].c) + (size_t)tt * BH
-                         : reinterpret_cast<float*>(W + h->wl[l].c2) + (size_t)(tt & 1) * BH;
-          };
-          a.c_prev = lstm ? (t == 0 ? (c0 ? c0 + l * BH : nullptr) : cbuf(t - 1)) : nullptr;
-          a.c_out = lstm ? cbuf(t) : nullptr;
-          a.h_prev = hseq + (size_t)t * BH * e;
-          a.h_out = hseq + (size_t)(t + 1) * BH * e;
-          a.y = l == L - 1 ? static_cast<char*>(y) + (size_t)t * BH * e : nullptr;
-          a.hT = (t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
-          a.cT = (t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
-          a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
-          a.mcast = h->fwd_mcast;
-          Operand A{hseq + (size_t)t * BH * e, H, 0, B, H};
-          Operand Bw{PW + h->pl[l].wh, H, 0, GH, H};
-          Launch Lk = mk(h, s, ws, "fwd_step");
-          RNN_TRY(fwd_step(Lk, mode, d.cell, A, Bw, a));
-        }
-        if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + c], s)));
       }
     }
-  }
-  if (h->wavefront) RNN_TRY(join_streams(h, stream));
-  return RNN_OK;
+    if (h->wavefront) RNN_TRY(join_streams(h, stream));
+    return RNN_OK;
+  };
+  return run_graphed(h, stream, key, issue);
 }
 
 int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* dcT, const void* w_packed,
@@ -542,101 +667,105 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
     if (!aligned16(p)) return RNN_ERR_INVALID_ARG;
   (void)h0;
   RNN_TRY(ensure_runtime(h));
-  const rnn_desc_t& d = h->d;
-  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, GH = h->GH, mode = d.mode;
-  const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
-  const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
-  char* R = static_cast<char*>(reserve);
-  char* W = static_cast<char*>(ws);
-  const char* PW = static_cast<const char*>(w_packed);
+  const std::vector<uintptr_t> key = {2, (uintptr_t)dy, (uintptr_t)dhT, (uintptr_t)dcT, (uintptr_t)w_packed, (uintptr_t)h0, (uintptr_t)c0, (uintptr_t)dx, (uintptr_t)dh0, (uintptr_t)dc0, (uintptr_t)reserve, (uintptr_t)ws};
+  auto issue = [&](cudaStream_t stream) -> int {
+    const rnn_desc_t& d = h->d;
+    const int L = d.layers, T = d.T, B = d.B, H = d.hidden, GH = h->GH, mode = d.mode;
+    const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
+    const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+    char* R = static_cast<char*>(reserve);
+    char* W = static_cast<char*>(ws);
+    const char* PW = static_cast<const char*>(w_packed);
 
-  for (int l = 0; l < L; ++l)
-    RNN_TRY(cu(cudaMemsetAsync(W + h->wl[l].ctr, 0, (size_t)h->ctr_count * 4, stream)));
-  if (h->wavefront) RNN_TRY(fork_streams(h, stream));
-  const int nd = h->wavefront ? (L + h->nch - 1) : 1;
-  for (int dg = 0; dg < nd; ++dg) {
-    for (int li = 0; li < L; ++li) {
-      const int l = L - 1 - li;
-      for (int rc = 0; rc < h->nch; ++rc) {
-        if (h->wavefront && li + rc != dg) continue;
-        cudaStream_t s = h->wavefront ? h->streams[l] : stream;
-        const int t1 = T - rc * h->chunk, t0 = std::max(0, t1 - h->chunk);
-        if (h->wavefront && l < L - 1) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l + 1) * h->nch + rc], 0)));
-        const bool top = l == L - 1;
-        const char* dyl = top ? static_cast<const char*>(dy) : W + h->wl[l].dyab;
-        const size_t dy_es = top ? e : 4;
-        float* carry = reinterpret_cast<float*>(W + h->wl[l].carry);
-        char* hseq = R + h->rl[l].hseq;
-        const float* c0l = c0 ? c0 + l * BH : nullptr;
-        if (rc == 0 && (lstm || gru)) {
-          if (lstm && dcT) RNN_TRY(cu(cudaMemcpyAsync(carry, dcT + l * BH, BH * 4, cudaMemcpyDeviceToDevice, s)));
-          else RNN_TRY(cu(cudaMemsetAsync(carry, 0, BH * 4, s)));
-        }
-        auto args_for = [&](int st) {
-          BwdStepArgs a;
-          std::memset(&a, 0, sizeof(a));
-          a.B = B;
-          a.H = H;
-          a.u = h->u;
-          a.gates = reinterpret_cast<const float*>(R + h->rl[l].gates) + (size_t)st * BGH;
-          a.c_s = lstm ? reinterpret_cast<const float*>(R + h->rl[l].c) + (size_t)st * BH : nullptr;
-          a.c_sm1 = lstm ? (st > 0 ? reinterpret_cast<const float*>(R + h->rl[l].c) + (size_t)(st - 1) * BH : c0l)
-                         : nullptr;
-          a.hn_s = gru ? reinterpret_cast<const float*>(R + h->rl[l].hn) + (size_t)st * BH : nullptr;
-          a.h_sm1 = hseq + (size_t)st * BH * e;
-          a.dy = dyl + (size_t)st * BH * dy_es;
-          a.dy_f32 = top ? (mode == RNN_MODE_FP32) : 1;
-          a.carry = carry;
-          a.dGx = R + h->rl[l].dgx + (size_t)st * BGH * e;
-          a.dGh = R + h->rl[l].dgh + (size_t)st * BGH * e;
-          a.part = reinterpret_cast<float*>(W + h->wl[l].part);
-          a.counters = reinterpret_cast<int*>(W + h->wl[l].ctr);
-          a.cluster_splitk = 1;
-          return a;
-        };
-        Operand Bw{PW + h->pl[l].wh, H, 1, H, GH};
-        for (int st = t1 - 1; st >= t0; --st) {
-          BwdStepArgs a = args_for(st);
-          if (st == T - 1) {
-            Launch Lk = mk(h, s, ws, "bwd_point");
-            RNN_TRY(bwd_point(Lk, mode, d.cell, a, dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr));
-          } else {
-            Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
+    for (int l = 0; l < L; ++l)
+      RNN_TRY(cu(cudaMemsetAsync(W + h->wl[l].ctr, 0, (size_t)h->ctr_count * 4, stream)));
+    if (h->wavefront) RNN_TRY(fork_streams(h, stream));
+    const int nd = h->wavefront ? (L + h->nch - 1) : 1;
+    for (int dg = 0; dg < nd; ++dg) {
+      for (int li = 0; li < L; ++li) {
+        const int l = L - 1 - li;
+        for (int rc = 0; rc < h->nch; ++rc) {
+          if (h->wavefront && li + rc != dg) continue;
+          cudaStream_t s = h->wavefront ? h->streams[l] : stream;
+          const int t1 = T - rc * h->chunk, t0 = std::max(0, t1 - h->chunk);
+          if (h->wavefront && l < L - 1) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l + 1) * h->nch + rc], 0)));
+          const bool top = l == L - 1;
+          const char* dyl = top ? static_cast<const char*>(dy) : W + h->wl[l].dyab;
+          const size_t dy_es = top ? e : 4;
+          float* carry = reinterpret_cast<float*>(W + h->wl[l].carry);
+          char* hseq = R + h->rl[l].hseq;
+          const float* c0l = c0 ? c0 + l * BH : nullptr;
+          if (rc == 0 && (lstm || gru)) {
+            if (lstm && dcT) RNN_TRY(cu(cudaMemcpyAsync(carry, dcT + l * BH, BH * 4, cudaMemcpyDeviceToDevice, s)));
+            else RNN_TRY(cu(cudaMemsetAsync(carry, 0, BH * 4, s)));
+          }
+          auto args_for = [&](int st) {
+            BwdStepArgs a;
+            std::memset(&a, 0, sizeof(a));
+            a.B = B;
+            a.H = H;
+            a.u = h->u;
+            a.gates = reinterpret_cast<const float*>(R + h->rl[l].gates) + (size_t)st * BGH;
+            a.c_s = lstm ? reinterpret_cast<const float*>(R + h->rl[l].c) + (size_t)st * BH : nullptr;
+            a.c_sm1 = lstm ? (st > 0 ? reinterpret_cast<const float*>(R + h->rl[l].c) + (size_t)(st - 1) * BH : c0l)
+                           : nullptr;
+            a.hn_s = gru ? reinterpret_cast<const float*>(R + h->rl[l].hn) + (size_t)st * BH : nullptr;
+            a.h_sm1 = hseq + (size_t)st * BH * e;
+            a.dy = dyl + (size_t)st * BH * dy_es;
+            a.dy_f32 = top ? (mode == RNN_MODE_FP32) : 1;
+            a.carry = carry;
+            a.dGx = R + h->rl[l].dgx + (size_t)st * BGH * e;
+            a.dGh = R + h->rl[l].dgh + (size_t)st * BGH * e;
+            a.part = reinterpret_cast<float*>(W + h->wl[l].part);
+            a.counters = reinterpret_cast<int*>(W + h->wl[l].ctr);
+            a.cluster_splitk = 1;
+            return a;
+          };
+          Operand Bw{PW + h->pl[l].wh, H, 1, H, GH};
+          for (int st = t1 - 1; st >= t0; --st) {
+            BwdStepArgs a = args_for(st);
+            if (st == T - 1) {
+              Launch Lk = mk(h, s, ws, "bwd_point");
+              RNN_TRY(bwd_point(Lk, mode, d.cell, a, dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr));
+            } else {
+              Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
+              Launch Lk = mk(h, s, ws, "bwd_step");
+              RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+            }
+          }
+          if (t0 == 0 && (dh0 || (dc0 && lstm))) {
+            BwdStepArgs a = args_for(0);
+            a.final_ = 1;
+            a.dh0 = dh0 ? static_cast<char*>(dh0) + l * BH * e : nullptr;
+            a.dc0 = (dc0 && lstm) ? dc0 + l * BH : nullptr;
+            Operand A{R + h->rl[l].dgh, GH, 0, B, GH};
             Launch Lk = mk(h, s, ws, "bwd_step");
             RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
           }
-        }
-        if (t0 == 0 && (dh0 || (dc0 && lstm))) {
-          BwdStepArgs a = args_for(0);
-          a.final_ = 1;
-          a.dh0 = dh0 ? static_cast<char*>(dh0) + l * BH * e : nullptr;
-          a.dc0 = (dc0 && lstm) ? dc0 + l * BH : nullptr;
-          Operand A{R + h->rl[l].dgh, GH, 0, B, GH};
-          Launch Lk = mk(h, s, ws, "bwd_step");
-          RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
-        }
-        // gradient of this chunk's layer inputs: dGx W_x
-        if (l > 0 || dx) {
-          const int In = h->In(l);
-          Operand A{R + h->rl[l].dgx + (size_t)t0 * BGH * e, GH, 0, (t1 - t0) * B, GH};
-          Operand Bx{PW + h->pl[l].wx, In, 1, In, GH};
-          Launch Lk = mk(h, s, ws, "dx_gemm");
-          if (l > 0) {
-            Remap none{0, 1, 1, 1};
-            RNN_TRY(gemm_f32(Lk, mode, A, Bx, (t1 - t0) * B, In, GH,
-                             reinterpret_cast<float*>(W + h->wl[l - 1].dyab) + (size_t)t0 * BH, In, nullptr, 0, none,
-                             0));
-          } else {
-            RNN_TRY(gemm_store(Lk, mode, A, Bx, (t1 - t0) * B, In, GH,
-                               static_cast<char*>(dx) + (size_t)t0 * B * In * e, In, 0));
+          // gradient of this chunk's layer inputs: dGx W_x
+          if (l > 0 || dx) {
+            const int In = h->In(l);
+            Operand A{R + h->rl[l].dgx + (size_t)t0 * BGH * e, GH, 0, (t1 - t0) * B, GH};
+            Operand Bx{PW + h->pl[l].wx, In, 1, In, GH};
+            Launch Lk = mk(h, s, ws, "dx_gemm");
+            if (l > 0) {
+              Remap none{0, 1, 1, 1};
+              RNN_TRY(gemm_f32(Lk, mode, A, Bx, (t1 - t0) * B, In, GH,
+                               reinterpret_cast<float*>(W + h->wl[l - 1].dyab) + (size_t)t0 * BH, In, nullptr, 0, none,
+                               0));
+            } else {
+              RNN_TRY(gemm_store(Lk, mode, A, Bx, (t1 - t0) * B, In, GH,
+                                 static_cast<char*>(dx) + (size_t)t0 * B * In * e, In, 0));
+            }
           }
+          if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + rc], s)));
         }
-        if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + rc], s)));
       }
     }
-  }
-  if (h->wavefront) RNN_TRY(join_streams(h, stream));
-  return RNN_OK;
+    if (h->wavefront) RNN_TRY(join_streams(h, stream));
+    return RNN_OK;
+  };
+  return run_graphed(h, stream, key, issue);
 }
 
 int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* reserve, float* dw, int accumulate,
@@ -646,30 +775,34 @@ int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* r
     if (!aligned16(p)) return RNN_ERR_INVALID_ARG;
   (void)h0;  // h_{-1} = h0 was stored in the reserve by the forward pass
   RNN_TRY(ensure_runtime(h));
-  const rnn_desc_t& d = h->d;
-  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, G = h->G, GH = h->GH, mode = d.mode;
-  const size_t e = h->elem, BH = (size_t)B * H;
-  const char* R = static_cast<const char*>(reserve);
-  const int TB = T * B;
-  // Each weight-gradient product has (G*H / 128) x (I_l / 256) tiles over
-  // K = T*B and fills the GPU by itself: the products run back to back on the
-  // caller's stream.
-  for (int l = 0; l < L; ++l) {
-    const int In = h->In(l);
-    Remap rm{1, G, h->u, H};
-    Operand dgx{R + h->rl[l].dgx, GH, 1, GH, TB};
-    Operand dgh{R + h->rl[l].dgh, GH, 1, GH, TB};
-    Operand X = l == 0 ? Operand{x, In, 1, In, TB} : Operand{R + h->rl[l - 1].hseq + BH * e, H, 1, H, TB};
-    Operand Hp{R + h->rl[l].hseq, H, 1, H, TB};
-    Launch Lk = mk(h, stream, ws, "dw_gemm");
-    RNN_TRY(gemm_f32(Lk, mode, dgx, X, GH, In, TB, dw + h->ul[l].wx, In, nullptr, accumulate, rm, 0));
-    RNN_TRY(gemm_f32(Lk, mode, dgh, Hp, GH, H, TB, dw + h->ul[l].wh, H, nullptr, accumulate, rm, 0));
-    Launch Lb = mk(h, stream, ws, "bias_grad");
-    RNN_TRY(bias_grad(Lb, mode, d.cell, H, h->u, TB, R + h->rl[l].dgx, R + h->rl[l].dgh, dw + h->ul[l].bx,
-                      dw + h->ul[l].bh, accumulate, reinterpret_cast<float*>(static_cast<char*>(ws) + h->ws_bias),
-                      h->bias_slices));
-  }
-  return RNN_OK;
+  const std::vector<uintptr_t> key = {3, (uintptr_t)x, (uintptr_t)h0, (uintptr_t)reserve, (uintptr_t)dw, (uintptr_t)accumulate, (uintptr_t)ws};
+  auto issue = [&](cudaStream_t stream) -> int {
+    const rnn_desc_t& d = h->d;
+    const int L = d.layers, T = d.T, B = d.B, H = d.hidden, G = h->G, GH = h->GH, mode = d.mode;
+    const size_t e = h->elem, BH = (size_t)B * H;
+    const char* R = static_cast<const char*>(reserve);
+    const int TB = T * B;
+    // Each weight-gradient product has (G*H / 128) x (I_l / 256) tiles over
+    // K = T*B and fills the GPU by itself: the products run back to back on the
+    // caller's stream.
+    for (int l = 0; l < L; ++l) {
+      const int In = h->In(l);
+      Remap rm{1, G, h->u, H};
+      Operand dgx{R + h->rl[l].dgx, GH, 1, GH, TB};
+      Operand dgh{R + h->rl[l].dgh, GH, 1, GH, TB};
+      Operand X = l == 0 ? Operand{x, In, 1, In, TB} : Operand{R + h->rl[l - 1].hseq + BH * e, H, 1, H, TB};
+      Operand Hp{R + h->rl[l].hseq, H, 1, H, TB};
+      Launch Lk = mk(h, stream, ws, "dw_gemm");
+      RNN_TRY(gemm_f32(Lk, mode, dgx, X, GH, In, TB, dw + h->ul[l].wx, In, nullptr, accumulate, rm, 0));
+      RNN_TRY(gemm_f32(Lk, mode, dgh, Hp, GH, H, TB, dw + h->ul[l].wh, H, nullptr, accumulate, rm, 0));
+      Launch Lb = mk(h, stream, ws, "bias_grad");
+      RNN_TRY(bias_grad(Lb, mode, d.cell, H, h->u, TB, R + h->rl[l].dgx, R + h->rl[l].dgh, dw + h->ul[l].bx,
+                        dw + h->ul[l].bh, accumulate, reinterpret_cast<float*>(static_cast<char*>(ws) + h->ws_bias),
+                        h->bias_slices));
+    }
+    return RNN_OK;
+  };
+  return run_graphed(h, stream, key, issue);
 }
 
 int rnn_sync_status(rnn_handle_t h, void* ws, cudaStream_t stream) {

@@ -24,6 +24,7 @@ FLAG_FORCE_PERSISTENT = 0x4
 FLAG_PROFILE = 0x8
 FLAG_NO_MULTICAST = 0x10
 FLAG_NO_PAIR = 0x20
+FLAG_NO_GRAPH = 0x40
 FLAG_TEST_SKIP_PUBLISH = 0x100
 
 # every symbol include/rnn.h declares

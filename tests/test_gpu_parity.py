@@ -182,3 +182,28 @@ def test_persistent_bounded_wait_reports_timeout():
     assert r.status() == 0   # the word was cleared
     g = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_PERSISTENT)
     compare(wl, g, run_oracle(hi, train=False))
+
+
+# ---------------------------------------------------------------- graph replay
+
+@pytest.mark.parametrize("flags,kw", [(0, dict(layers=3, T=7, B=9)), (rnn.FLAG_FORCE_PERSISTENT, dict(layers=2, T=6, B=4)),
+                                      (0, dict(layers=2, T=5, B=200))], ids=["wavefront", "persistent", "pairs"])
+def test_graph_capture_and_replay_match_direct_calls(flags, kw):
+    """Call 1 runs directly, call 2 is captured into a CUDA graph and launched,
+    call 3 replays it: all three give identical results, equal to a handle that
+    never uses graphs."""
+    wl = tiny(0, synth.MODE_BF16, **kw)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    r = runner.Runner(wl, flags=flags, chunk=2)
+    r.upload(hi)
+    outs = []
+    for _ in range(3):
+        r.step()
+        assert r.status() == 0
+        outs.append(r.outputs())
+    ref = run_gpu(wl, hi, flags=flags | rnn.FLAG_NO_GRAPH, chunk=2)
+    for o in outs:
+        for k in ref:
+            if ref[k] is not None:
+                np.testing.assert_array_equal(o[k], ref[k], err_msg=k)
+    compare(wl, outs[-1], run_oracle(hi))
