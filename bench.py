@@ -314,6 +314,7 @@ def main():
         ms_e2e, h2d, d2h = float("nan"), 0, 0
     else:
         ms_e2e, h2d, d2h = e2e_run(R, wl, args.steps, sdt, stream, barrier)
+    plan = R.r.describe()
     del R
     torch.cuda.empty_cache()
     prof, psteps = kernel_profile(wl, dev, args, sdt)
@@ -332,7 +333,7 @@ def main():
                              "of_measured_sustained": tflops / world / pk["bf16_tflops_sustained"]},
         "config": {"workload": wl.name, "cell": synth.CELL_NAMES[wl.cell], "layers": wl.layers, "T": wl.T,
                    "B": wl.B, "input": wl.input, "hidden": wl.hidden, "training": wl.training,
-                   "flops_per_step": fl, "plan": R.r.describe(),
+                   "flops_per_step": fl, "plan": plan,
                    "l2": "inputs larger than L2 (weights, reserve and activations exceed 129 MB)"},
         "gpu_launches": launches,
         "roofline": roof,

@@ -45,7 +45,9 @@ struct TileCoord {
   int* scratch;     // 8 ints of shared memory for the epilogue warps (tcgen05 only)
   // cluster split-K (tcgen05, cluster > 1): the CTA's stage buffers reused as a
   // float tile for the reduction, and two cluster-wide barriers
-  int cluster;
+  int cluster;     // number of CTAs that reduce together (the K splits)
+  int peer_base;   // cluster rank of split 0 of this CTA's reduction group
+  int peer_stride; // rank distance between consecutive splits of the group
   float* red;
   uint64_t* red_full;
   uint64_t* red_done;
@@ -263,6 +265,8 @@ __global__ void __launch_bounds__(192, 1)
         tp.splits = g.splits;
         tp.scratch = scratch;
         tp.cluster = g.cluster;
+        tp.peer_base = 0;
+        tp.peer_stride = 1;
         tp.red = reinterpret_cast<float*>(smem);
         tp.red_full = red_full;
         tp.red_done = red_done;
@@ -282,6 +286,8 @@ __global__ void __launch_bounds__(192, 1)
       t.splits = g.splits;
       t.scratch = scratch;
       t.cluster = g.cluster;
+      t.peer_base = 0;
+      t.peer_stride = 1;
       t.red = reinterpret_cast<float*>(smem);
       t.red_full = red_full;
       t.red_done = red_done;
@@ -343,13 +349,21 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* red_full = tempty + 2;
+  uint64_t* red_done = red_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* scratch = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = tc::cluster_ctarank();  // 0 = the CTA that issues the MMAs
+  // The two CTAs of a pair have cluster ranks 2i and 2i+1; the even one
+  // issues the MMAs.  With split-K the cluster holds `g.cluster` such pairs.
+  const uint32_t rank = tc::cluster_ctarank();
+  const uint32_t leader = rank & ~1u;
+  const bool is_leader = (rank & 1u) == 0;
+  const uint16_t pair_mask = (uint16_t)(0x3u << leader);
+  const int pr = (int)(rank & 1u);
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
@@ -361,6 +375,8 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_init(tfull + a, 1);
       tc::mbar_init(tempty + a, 8);
     }
+    tc::mbar_init(red_full, 4 * g.cluster);
+    tc::mbar_init(red_done, 4 * g.cluster);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&mapA);
@@ -388,7 +404,7 @@ __global__ void __launch_bounds__(192, 1)
         decode_tile(g, tile, mt, nt, split);
         const int kb0 = split * g.kb_per_split;
         const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
-        const int m0 = mt * BM + (int)rank * 128, n0 = nt * BN + (int)rank * HB;
+        const int m0 = mt * BM + pr * 128, n0 = nt * BN + pr * HB;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, g.err, g.limit_ns)) {
             ok = false;
@@ -396,8 +412,8 @@ __global__ void __launch_bounds__(192, 1)
           }
           uint8_t* sa = smem + stage * STAGE;
           uint8_t* sb = sa + A_BYTES;
-          const uint32_t fb = tc::mapa(tc::smem_addr(full + stage), 0);
-          if (rank == 0) tc::mbar_arrive_expect_tx(full + stage, 2 * STAGE);
+          const uint32_t fb = tc::mapa(tc::smem_addr(full + stage), leader);
+          if (is_leader) tc::mbar_arrive_expect_tx(full + stage, 2 * STAGE);
           last_par[stage] = static_cast<int>(phase);
           const int k0 = kb * BK;
           if (g.a_mn) {
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      if (!ok && rank == 0) {
+      if (!ok && is_leader) {
         for (int s = 0; s < STAGES; ++s) {
           if (last_par[s] < 0) continue;
           const uint64_t t0 = globaltimer_ns();
@@ -430,7 +446,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
-    if (lane == 0 && rank == 0) {
+    if (lane == 0 && is_leader) {
       const uint32_t idesc = tc::idesc_bf16(BM, BN, g.a_mn, g.b_mn);
       uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
       bool ok = true;
@@ -458,14 +474,14 @@ __global__ void __launch_bounds__(192, 1)
                                        : tc::sdesc_sw128(sb + kk * 32, 16, 1024);
             tc::mma_bf16_pair(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          tc::mma_commit_pair(empty + stage, 0x3);
+          tc::mma_commit_pair(empty + stage, pair_mask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        tc::mma_commit_pair(tfull + acc, 0x3);
+        tc::mma_commit_pair(tfull + acc, pair_mask);
         acc ^= 1;
         if (acc == 0) aphase ^= 1;
       }
@@ -474,22 +490,25 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ epilogue warps (both CTAs)
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const uint32_t te_base = tc::mapa(tc::smem_addr(tempty), 0);
+    const uint32_t te_base = tc::mapa(tc::smem_addr(tempty), leader);
     uint32_t acc = 0, aphase = 0;
     for (int tile = pair; tile < g.num_tiles; tile += npairs) {
       int mt, nt, split;
       decode_tile(g, tile, mt, nt, split);
       TileCoord t;
-      t.m0 = mt * BM + (int)rank * 128;
+      t.m0 = mt * BM + pr * 128;
       t.n0 = nt * BN;
-      t.mt = mt * 2 + (int)rank;
+      t.mt = mt * 2 + pr;
       t.nt = nt;
       t.split = split;
       t.splits = g.splits;
       t.scratch = scratch;
-      t.cluster = 1;
-      t.red = nullptr;
-      t.red_full = t.red_done = nullptr;
+      t.cluster = g.cluster;  // > 1: the splits reduce through the cluster, pairs interleaved
+      t.peer_base = pr;
+      t.peer_stride = 2;
+      t.red = reinterpret_cast<float*>(smem);
+      t.red_full = red_full;
+      t.red_done = red_done;
       epi.prefetch(t, row, BN);
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
@@ -592,6 +611,8 @@ __global__ void __launch_bounds__(128)
     t.splits = 1;
     t.scratch = nullptr;
     t.cluster = 1;
+    t.peer_base = 0;
+    t.peer_stride = 1;
     t.red = nullptr;
     t.red_full = t.red_done = nullptr;
     SmemAcc a{Cs + tid * (BN + 1)};

@@ -375,7 +375,7 @@ struct EpiBwdStep {
       __syncwarp();
       const uint32_t full_local = tc::smem_addr(t.red_full), done_local = tc::smem_addr(t.red_done);
       if (lane == 0)
-        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(full_local, p));
+        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(full_local, t.peer_base + p * t.peer_stride));
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait_cluster(t.red_full, 0, err, limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -389,7 +389,7 @@ struct EpiBwdStep {
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = 0.f;
           for (int p = 0; p < t.cluster; ++p) {
-            const uint32_t ra = tc::mapa(mine_addr, p) + c * 4;
+            const uint32_t ra = tc::mapa(mine_addr, t.peer_base + p * t.peer_stride) + c * 4;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               float w[4];
@@ -403,7 +403,7 @@ struct EpiBwdStep {
       tc::fence_acq_rel_cluster();
       __syncwarp();
       if (lane == 0)
-        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(done_local, p));
+        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(done_local, t.peer_base + p * t.peer_stride));
       if (lane == 0) tc::mbar_wait_cluster(t.red_done, 0, err, limit_ns);
       __syncwarp();
       return;

@@ -141,7 +141,7 @@ __global__ void bias_part_kernel(const S* __restrict__ dg, float* __restrict__ p
 }
 
 __global__ void bias_final_kernel(const float* __restrict__ part, int slices, int G, int H, int u,
-                                  float* __restrict__ db, int accumulate) {
+                                  float* __restrict__ db, float* __restrict__ db2, int accumulate) {
   const int p = blockIdx.x * blockDim.x + threadIdx.x;
   const int GH = G * H;
   if (p >= GH) return;
@@ -150,6 +150,7 @@ __global__ void bias_final_kernel(const float* __restrict__ part, int slices, in
   const int blk = p / (G * u), r = p % (G * u);
   const int ur = (r / u) * H + blk * u + (r % u);
   db[ur] = accumulate ? db[ur] + t : t;
+  if (db2) db2[ur] = accumulate ? db2[ur] + t : t;  // same column sums, second destination
 }
 
 int bias_grad(const Launch& L, int mode, int cell, int H, int u, long long rows, const void* dgx, const void* dgh,
@@ -159,21 +160,23 @@ int bias_grad(const Launch& L, int mode, int cell, int H, int u, long long rows,
   if (GH % 8 || slices < 1) return RNN_ERR_INVALID_ARG;
   const long long per = (rows + slices - 1) / slices;
   dim3 grid((GH + 255) / 256, slices);
+  // LSTM and RNN share one gate-gradient matrix between the input and the
+  // recurrent side: reduce it once and write both bias gradients
+  const int passes = dgx == dgh ? 1 : 2;
   launch_begin(L);
-  int n = 0;
-  for (int which = 0; which < 2; ++which) {
+  for (int which = 0; which < passes; ++which) {
     const void* dg = which == 0 ? dgx : dgh;
     float* db = which == 0 ? dbx : dbh;
+    float* db2 = passes == 1 ? dbh : nullptr;
     if (mode == 1)
       bias_part_kernel<__nv_bfloat16><<<grid, 256, 0, L.stream>>>(static_cast<const __nv_bfloat16*>(dg), part, rows,
                                                                   GH, per);
     else
       bias_part_kernel<float><<<grid, 256, 0, L.stream>>>(static_cast<const float*>(dg), part, rows, GH, per);
-    bias_final_kernel<<<(GH + 255) / 256, 256, 0, L.stream>>>(part, slices, G, H, u, db, accumulate);
-    n += 2;
+    bias_final_kernel<<<(GH + 255) / 256, 256, 0, L.stream>>>(part, slices, G, H, u, db, db2, accumulate);
   }
   cudaError_t e = cudaGetLastError();
-  launch_end(L, n);
+  launch_end(L, 2 * passes);
   return cuda_status(e);
 }
 

@@ -136,10 +136,13 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   return cuda_status(e);
 }
 
-// CTA-pair engine: 256 x BN tiles over clusters of 2 CTAs (no split-K).
+// CTA-pair engine: 256 x BN tiles over clusters of 2 CTAs.  With splits > 1
+// the K splits of a tile run as one cluster of 2*splits CTAs (pairs at ranks
+// 2i, 2i+1) and reduce through distributed shared memory (the epilogue must
+// support it); RNN_ERR_UNSUPPORTED when the split cannot be laid out so.
 template <int BN, int STAGES, class Epi>
 int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, int max_ctas,
-               const Epi& epi) {
+               const Epi& epi, int splits = 1) {
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
   if (B.mn_major && (BN / 2) % 64) return RNN_ERR_UNSUPPORTED;
   CUtensorMap ma, mb;
@@ -154,14 +157,16 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   g.m_tiles = (M + tce2::BM - 1) / tce2::BM;
   g.n_tiles = (N + BN - 1) / BN;
   g.kb_total = (K + tce2::BK - 1) / tce2::BK;
-  g.splits = 1;
-  g.kb_per_split = g.kb_total;
-  g.num_tiles = g.m_tiles * g.n_tiles;
+  splits = std::max(1, std::min(splits, g.kb_total));
+  g.kb_per_split = (g.kb_total + splits - 1) / splits;
+  g.splits = (g.kb_total + g.kb_per_split - 1) / g.kb_per_split;
+  if (g.splits > 1 && (g.splits > 4 || BN % (16 * g.splits))) return RNN_ERR_UNSUPPORTED;
+  g.num_tiles = g.m_tiles * g.n_tiles * g.splits;
   g.a_mn = A.mn_major;
   g.b_mn = B.mn_major;
   g.limit_ns = L.limit_ns;
   g.err = L.err;
-  g.cluster = 1;
+  g.cluster = g.splits;
   g.mcast = 1;
   g.nfast = 0;
   constexpr int smem = tce2::smem_bytes<BN, STAGES>();
@@ -173,7 +178,8 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
     attr = true;
   }
   const int cap = (max_ctas > 0 ? max_ctas : L.num_sms) / 2;
-  const int pairs = std::max(1, std::min(g.num_tiles, cap));
+  // split-K: one tile per pair so that the cluster reduction can reuse the stages
+  const int pairs = g.cluster > 1 ? g.num_tiles : std::max(1, std::min(g.num_tiles, cap));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(192);
@@ -181,7 +187,7 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   cfg.stream = L.stream;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.x = 2 * g.cluster;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
