@@ -108,6 +108,30 @@ def class_flops(wl):
     return out
 
 
+def class_bytes(wl):
+    """Algorithmic HBM bytes per step of the recurrent-step classes: every
+    timestep reads W_h once plus the state it updates (bf16 storage, f32 gates,
+    cell state and gate pre-activations)."""
+    G, H, T, B, L = wl.G, wl.hidden, wl.T, wl.B, wl.layers
+    e = 2 if wl.mode == 1 else 4
+    wh = G * H * H * e
+    # forward: h_{t-1} + P (read) ; gates (write) ; c_{t-1}/c_t ; h_t, y
+    fwd = wh + B * H * e + B * G * H * 4 * 2 + B * H * 4 * 2 + B * H * e * 2
+    # backward: dG_{t+1} + gates + c_t, c_{t-1} + dy + carry (read) ; dG_t + carry (write)
+    bwd = wh + B * G * H * e + B * G * H * 4 + B * H * 4 * 2 + B * H * 4 * 2 + B * G * H * e + B * H * 4
+    out = {"fwd_step": fwd * T * L}
+    if wl.training:
+        out["bwd_step"] = bwd * T * L
+    return out
+
+
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
+# ncu capture of the same kernel build on a one-layer T=2 case with the same
+# per-step shape; summarised in profiles/ncu_step_kernels_lstm_B256_H4096.md.
+NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 206.72e6,
+               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 179.34e6}
+
+
 def time_oracle_sample(wl, budget_s=20.0):
     """The double-precision oracle on a bounded sample of the workload (batch
     columns and a prefix of timesteps), as TFLOP/s of that sample."""
@@ -179,19 +203,32 @@ def e2e_run(R, wl, steps, sdt, stream, barrier):
 
 
 def roofline(prof, wl, steps, pk):
-    """Roofline of the dominant kernel class: algorithmic flops per launch over
-    its average CUDA-event launch duration in the timed region."""
-    cf = class_flops(wl)
+    """Roofline of the dominant kernel class (largest device time): its
+    algorithmic flops and bytes per launch over its average CUDA-event launch
+    duration, against the tensor or the HBM peak, whichever its arithmetic
+    intensity makes binding."""
+    cf, cb = class_flops(wl), class_bytes(wl)
     cand = [(k, v) for k, v in prof.items() if k in cf and v[0] > 0]
     if not cand:
         return None
     name, (n, tot) = max(cand, key=lambda kv: kv[1][1])
-    achieved = cf[name] * steps / (tot * 1e-3) / 1e12
-    return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
-            "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
-            "launches_per_step": n // steps, "flops_per_launch": cf[name] * steps / n,
-            "ms_per_launch": tot / n, "peak_source": pk["source"] + " (sustained bf16, kernel timed inside the step)",
-            "measured_in": "serialised profiling pass (see kernels_note)"}
+    sec = tot * 1e-3 / n
+    flops = cf[name] * steps / n
+    t_tensor = flops / (pk["bf16_tflops_sustained"] * 1e12)
+    nbytes = cb[name] * steps / n if name in cb else 0.0
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9) if nbytes else 0.0
+    common = {"kernel": name, "launches_per_step": n // steps, "flops_per_launch": flops, "bytes_per_launch": nbytes,
+              "ms_per_launch": 1e3 * sec, "measured_in": "serialised profiling pass (see kernels_note)",
+              "traffic": NCU_TRAFFIC.get((wl.name, name))}
+    if t_hbm > t_tensor:
+        ach = nbytes / sec / 1e9
+        return dict(common, bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s", frac=ach / pk["hbm_gbs"],
+                    tensor_frac=flops / sec / 1e12 / pk["bf16_tflops_sustained"],
+                    peak_source=pk["source"] + " (copy bandwidth)")
+    ach = flops / sec / 1e12
+    return dict(common, bound="tensor", achieved=ach, peak=pk["bf16_tflops_sustained"], unit="TFLOP/s",
+                frac=ach / pk["bf16_tflops_sustained"],
+                peak_source=pk["source"] + " (sustained bf16, kernel timed inside the step)")
 
 
 def kernel_profile(wl, dev, args, sdt):
