@@ -10,7 +10,7 @@
 // across 8 warps, reduced through shared memory), applies the cell update to
 // its units and publishes its part of h_t.
 //
-// Step hand-off: after its h_t stores a CTA makes one fenced arrival on the
+// Step hand-off: after its h_t stores a CTA makes one release arrival on the
 // step's counter (one counter per timestep, zeroed before the launch); one
 // thread per CTA polls the counter of the previous step until every CTA has
 // arrived, then the CTA reads h_{t-1} once through L2.  Only 1 thread per CTA
@@ -34,6 +34,17 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, cons
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Release-ordered add: this thread's earlier writes, and those it has
+// synchronised with through a barrier, are visible before the count changes.
+__device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned short bf16_bits(float v) {
@@ -105,11 +116,11 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
     // warp's B fragments of it through L2
     if (t > 0) {
       if (threadIdx.x == 0) {
-        const volatile unsigned int* cnt = a.arrive + (t - 1);
+        const unsigned int* cnt = a.arrive + (t - 1);
         const unsigned int want = gridDim.x;
-        if (*cnt < want) {
+        if (ld_acquire(cnt) < want) {
           const uint64_t t0 = globaltimer_ns();
-          while (*cnt < want) {
+          while (ld_acquire(cnt) < want) {
             if (globaltimer_ns() - t0 > a.limit_ns) {
               abort_flag = 1;
               raise_error(a.err, DEV_TIMEOUT_STEP);
@@ -117,7 +128,6 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
             }
           }
         }
-        __threadfence();
       }
       __syncthreads();
       if (abort_flag) break;
@@ -198,12 +208,17 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       }
       reinterpret_cast<unsigned short*>(a.hseq)[(size_t)(t + 1) * B * H + bj] = hb;
     }
-    // ---- publish: once all of this CTA's h_t stores are done, one fenced
-    // arrival on the step's counter
-    __syncthreads();
-    if (threadIdx.x == 0 && !(a.test_skip_publish && blockIdx.x == 0 && t == 0)) {
-      __threadfence();
-      atomicAdd(a.arrive + t, 1u);
+    // ---- publish: once all of this CTA's h_t stores are done, one release
+    // arrival on the step's counter.  When every cell-update thread is in warp
+    // 0 a warp barrier orders their stores before lane 0's release.
+    if (uc * B <= 32) {
+      if (warp == 0) {
+        __syncwarp();
+        if (lane == 0 && !(a.test_skip_publish && blockIdx.x == 0 && t == 0)) red_release_add(a.arrive + t, 1u);
+      }
+    } else {
+      __syncthreads();
+      if (threadIdx.x == 0 && !(a.test_skip_publish && blockIdx.x == 0 && t == 0)) red_release_add(a.arrive + t, 1u);
     }
   }
 }
