@@ -92,6 +92,20 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
+def replica_aggregate(ms_local, flops_per_step, dist=None, device="cpu"):
+    """Whole-job throughput of N independent replicas: every rank processed
+    one workload per step; the step time is the maximum over ranks.  Returns
+    (max ms per step, aggregate TFLOP/s, world size)."""
+    world = 1
+    ms = float(ms_local)
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * flops_per_step / (ms * 1e-3) / 1e12, world
+
+
 def step_flops(wl):
     f = wl.gemm_flops()
     return f["fwd"] + (f["bwd_data"] + f["bwd_weights"] if wl.training else 0.0)
@@ -258,6 +272,45 @@ def kernel_profile(wl, dev, args, sdt):
     return prof, steps
 
 
+def persistent_probe(dev, steps=10, warmup=3):
+    """Second target of the path: the persistent small-batch recurrence
+    (1-layer LSTM, B=4, H=1024, T=1000 inference).  Per step it reads the
+    8 MiB W_h from on-chip storage; its roofline is that read at the
+    aggregate shared-memory bandwidth of the GPU, derived from the unit
+    counts (152 SMs x 128 B/clk x max SM clock)."""
+    from recurrent_neural_network_gb300 import rnn, runner, synth
+    wl = synth.WORKLOADS[2]
+    R = runner.Runner(wl, device=dev, flags=rnn.FLAG_FORCE_PERSISTENT)
+    R.x = synth_tensor(wl, "x", dev, R.dt)
+    R.w_user = synth_tensor(wl, "w", dev, R.dt)
+    R.h0 = synth_tensor(wl, "h0", dev, R.dt)
+    R.c0 = synth_tensor(wl, "c0", dev, torch.float32)
+    R.pack()
+    for _ in range(warmup):
+        R.forward(False)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        R.forward(False)
+    e1.record()
+    torch.cuda.synchronize()
+    assert R.status() == 0
+    ms = e0.elapsed_time(e1) / steps
+    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    mhz = pk.get("sm_max_mhz", 2070.0)
+    smem_gbs = 152 * 128 * mhz * 1e6 / 1e9
+    wh_bytes = 4 * wl.hidden * wl.hidden * 2
+    us_step = 1e3 * ms / wl.T
+    roof_us = wh_bytes / (smem_gbs * 1e9) * 1e6
+    return {"workload": wl.name, "ms_per_call": ms, "us_per_timestep": us_step, "timesteps_per_s": wl.T / (ms * 1e-3),
+            "tflops": step_flops(wl) / (ms * 1e-3) / 1e12, "plan": R.r.describe(),
+            "roofline": {"bound": "smem", "bytes_per_timestep": wh_bytes, "peak": smem_gbs, "unit": "GB/s",
+                         "peak_source": "derived: 152 SMs x 128 B/clk x %.0f MHz" % mhz,
+                         "roofline_us_per_timestep": roof_us, "achieved": wh_bytes / (us_step * 1e-6) / 1e9,
+                         "frac": roof_us / us_step}}
+
+
 def synth_tensor(wl, what, dev, dtype):
     from recurrent_neural_network_gb300 import synth
     return synth.device_tensor(wl, what, dev, dtype)
@@ -272,6 +325,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-persistent", action="store_true")
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--chunk", type=int, default=0)
     args = ap.parse_args()
@@ -339,13 +393,8 @@ def main():
     clk = clocks.stop()
     st = R.status()
     assert st == 0, f"device status {st}"
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-
     fl = step_flops(wl)
-    tflops = world * fl / (ms * 1e-3) / 1e12
+    ms, tflops, world = replica_aggregate(ms, fl, dist, dev)
     pk = peaks()
     if args.no_e2e:
         ms_e2e, h2d, d2h = float("nan"), 0, 0
@@ -356,6 +405,7 @@ def main():
     torch.cuda.empty_cache()
     prof, psteps = kernel_profile(wl, dev, args, sdt)
     roof = roofline(prof, wl, psteps, pk)
+    persistent = persistent_probe(dev) if (world == 1 and args.config != 2 and not args.no_persistent) else None
 
     if rank != 0:
         if dist is not None:
@@ -378,6 +428,7 @@ def main():
         "e2e": {"value": world * fl / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "phases_ms": phases,
+        "persistent_recurrence": persistent,
         "kernels": {k: {"launches": v[0] // psteps, "ms_per_step": v[1] / psteps, "us_per_launch": 1e3 * v[1] / v[0]}
                     for k, v in prof.items() if v[0]},
         "kernels_note": "per-kernel CUDA-event times from a separate pass of the same workload with launches "
