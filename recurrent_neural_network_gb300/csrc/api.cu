@@ -183,6 +183,10 @@ int plan_and_layout(rnn_s* h) {
   if (d.mode == RNN_MODE_BF16) {
     if (H % 64 || d.input % 8) return RNN_ERR_UNSUPPORTED;
     h->u = (d.cell == RNN_TANH && H % 128 == 0) ? 128 : 64;
+    // a forward step has ceil(B/128) x H/u tiles: narrow the packing unit
+    // (down to 16 units, 32 for tanh) until a step covers at least 64 CTAs
+    const int mtl = (B + 127) / 128, umin = d.cell == RNN_TANH ? 32 : 16;
+    while (h->u > umin && mtl * (H / h->u) < 64) h->u /= 2;
   } else {
     if (H % 32 || d.input % 4) return RNN_ERR_UNSUPPORTED;
     h->u = 32;

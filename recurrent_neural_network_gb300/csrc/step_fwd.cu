@@ -47,10 +47,12 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
       if (cell == GRU && a.u == 64) return launch_tc2<192, 7>(L, A, Bw, M, N, K, 0, make_epi<GRU, S>(a));
       if (cell == TANH && a.u == 128) return launch_tc2<128, 8>(L, A, Bw, M, N, K, 0, make_epi<TANH, S>(a));
     }
-    if (cell == LSTM && a.u == 64) return launch_tc<256, 4>(L, A, Bw, M, N, K, 1, 0, make_epi<LSTM, S>(a), false, mc);
-    if (cell == GRU && a.u == 64) return launch_tc<192, 5>(L, A, Bw, M, N, K, 1, 0, make_epi<GRU, S>(a), false, mc);
-    if (cell == TANH && a.u == 128) return launch_tc<128, 6>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a), false, mc);
-    if (cell == TANH && a.u == 64) return launch_tc<64, 8>(L, A, Bw, M, N, K, 1, 0, make_epi<TANH, S>(a), false, mc);
+#define RNN_STEP(C, U, BN_, ST)     \
+  if (cell == C && a.u == U) return launch_tc<BN_, ST>(L, A, Bw, M, N, K, 1, 0, make_epi<C, S>(a), false, mc);
+    RNN_STEP(LSTM, 64, 256, 4) RNN_STEP(LSTM, 32, 128, 6) RNN_STEP(LSTM, 16, 64, 8)
+    RNN_STEP(GRU, 64, 192, 5) RNN_STEP(GRU, 32, 96, 7) RNN_STEP(GRU, 16, 48, 8)
+    RNN_STEP(TANH, 128, 128, 6) RNN_STEP(TANH, 64, 64, 8) RNN_STEP(TANH, 32, 32, 8)
+#undef RNN_STEP
     return RNN_ERR_UNSUPPORTED;
   }
   using S = float;
