@@ -96,9 +96,30 @@ __device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* p, const f
 }
 
 // ---------------------------------------------------------------- activations
-// Logistic sigmoid and tanh through CUDA's own expf / tanhf.
+// Logistic sigmoid and tanh through CUDA's own expf / tanhf (fp32 storage mode).
 __device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + expf(-a)); }
 __device__ __forceinline__ float tanh_(float a) { return tanhf(a); }
+// bf16 storage mode: the hardware tanh approximation (tanh.approx.f32, one
+// special-function op, relative error about 2^-11) and the identity
+// sigmoid(a) = (1 + tanh(a/2)) / 2.  The cell outputs are stored in bf16
+// (relative step 2^-8), so the approximation stays below the storage rounding.
+__device__ __forceinline__ float tanh_hw(float a) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(a));
+  return y;
+}
+__device__ __forceinline__ float sigm_hw(float a) { return fmaf(0.5f, tanh_hw(0.5f * a), 0.5f); }
+// activation pair for storage type S
+template <class S>
+struct Act {
+  __device__ __forceinline__ static float sig(float a) { return sigm(a); }
+  __device__ __forceinline__ static float th(float a) { return tanh_(a); }
+};
+template <>
+struct Act<__nv_bfloat16> {
+  __device__ __forceinline__ static float sig(float a) { return sigm_hw(a); }
+  __device__ __forceinline__ static float th(float a) { return tanh_hw(a); }
+};
 
 // ---------------------------------------------------------------- time and errors
 __device__ __forceinline__ uint64_t globaltimer_ns() {

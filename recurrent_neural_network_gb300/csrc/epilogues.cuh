@@ -138,10 +138,10 @@ struct EpiFwdStep {
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float ig = sigm(a[0][i]), fg = sigm(a[1][i]), gg = tanh_(a[2][i]), og = sigm(a[3][i]);
+          const float ig = Act<S>::sig(a[0][i]), fg = Act<S>::sig(a[1][i]), gg = Act<S>::th(a[2][i]), og = Act<S>::sig(a[3][i]);
           const float cc = fg * cp[i] + ig * gg;
           cn[i] = cc;
-          hnew[i] = og * tanh_(cc);
+          hnew[i] = og * Act<S>::th(cc);
           a[0][i] = ig; a[1][i] = fg; a[2][i] = gg; a[3][i] = og;
         }
         store16(c_out + (size_t)b * H + j0, cn);
@@ -162,9 +162,9 @@ struct EpiFwdStep {
         load16(prow + 2 * u, p);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float r = sigm(a[0][i]), z = sigm(a[1][i]);
+          const float r = Act<S>::sig(a[0][i]), z = Act<S>::sig(a[1][i]);
           hn[i] = a[2][i] + bn[i];
-          const float n = tanh_(p[i] + r * hn[i]);
+          const float n = Act<S>::th(p[i] + r * hn[i]);
           hnew[i] = (1.f - z) * n + z * hp[i];
           a[0][i] = r; a[1][i] = z; a[2][i] = n;
         }
@@ -174,7 +174,7 @@ struct EpiFwdStep {
         load16(prow, p);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          hnew[i] = tanh_(a[0][i] + p[i]);
+          hnew[i] = Act<S>::th(a[0][i] + p[i]);
           a[0][i] = hnew[i];
         }
       }
@@ -236,7 +236,7 @@ struct BwdPoint {
       float d0[16], d1[16], d2[16], d3[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float tau = tanh_(cs[i]);
+        const float tau = Act<S>::th(cs[i]);
         const float dov = dh[i] * tau;
         const float dcv = dc[i] + dh[i] * og[i] * (1.f - tau * tau);
         d0[i] = dcv * gg[i] * ig[i] * (1.f - ig[i]);

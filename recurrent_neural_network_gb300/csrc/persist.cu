@@ -176,21 +176,21 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       for (int g = 0; g < G; ++g) av[g] = sums[g * uc + jl][bq];
       float hnew, gv[G];
       if constexpr (CELL == LSTM) {
-        const float ig = sigm(av[0] + pv[0]), fg = sigm(av[1] + pv[1]);
-        const float gg = tanh_(av[2] + pv[2]), og = sigm(av[3] + pv[3]);
+        const float ig = sigm_hw(av[0] + pv[0]), fg = sigm_hw(av[1] + pv[1]);
+        const float gg = tanh_hw(av[2] + pv[2]), og = sigm_hw(av[3] + pv[3]);
         c_state = fg * c_state + ig * gg;
-        hnew = og * tanh_(c_state);
+        hnew = og * tanh_hw(c_state);
         gv[0] = ig; gv[1] = fg; gv[2] = gg; gv[G - 1] = og;
       } else if constexpr (CELL == GRU) {
-        const float r = sigm(av[0] + pv[0]), z = sigm(av[1] + pv[1]);
+        const float r = sigm_hw(av[0] + pv[0]), z = sigm_hw(av[1] + pv[1]);
         const float hn = av[2] + bhn;
-        const float n = tanh_(pv[2] + r * hn);
+        const float n = tanh_hw(pv[2] + r * hn);
         hnew = (1.f - z) * n + z * h_prev;
         h_prev = hnew;
         gv[0] = r; gv[1] = z; gv[G - 1] = n;
         if (a.hn_out) a.hn_out[((size_t)t * B + bq) * H + j] = hn;
       } else {
-        hnew = tanh_(av[0] + pv[0]);
+        hnew = tanh_hw(av[0] + pv[0]);
         gv[0] = hnew;
       }
       const size_t bj = (size_t)bq * H + j;

@@ -44,7 +44,10 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
     // more than 128 batch rows: 256-row tiles on CTA pairs
     if (M > 128 && L.pair) {
       if (cell == LSTM && a.u == 64) return launch_tc2<256, 6>(L, A, Bw, M, N, K, 0, make_epi<LSTM, S>(a));
+      if (cell == LSTM && a.u == 32) return launch_tc2<128, 8>(L, A, Bw, M, N, K, 0, make_epi<LSTM, S>(a));
+      if (cell == LSTM && a.u == 16) return launch_tc2<64, 10>(L, A, Bw, M, N, K, 0, make_epi<LSTM, S>(a));
       if (cell == GRU && a.u == 64) return launch_tc2<192, 7>(L, A, Bw, M, N, K, 0, make_epi<GRU, S>(a));
+      if (cell == GRU && a.u == 32) return launch_tc2<96, 9>(L, A, Bw, M, N, K, 0, make_epi<GRU, S>(a));
       if (cell == TANH && a.u == 128) return launch_tc2<128, 8>(L, A, Bw, M, N, K, 0, make_epi<TANH, S>(a));
     }
 #define RNN_STEP(C, U, BN_, ST)     \
