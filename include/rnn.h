@@ -83,6 +83,14 @@ enum {
 #define RNN_FLAG_NO_PAIR 0x20u          /* keep every product on single-CTA 128-row tiles */
 #define RNN_FLAG_NO_GRAPH 0x40u         /* enqueue kernels directly; by default a call whose pointers were
                                            seen before replays a cached CUDA graph of its launches */
+#define RNN_FLAG_NO_PDL 0x80u          /* launch every kernel after the previous one on its stream has
+                                           finished; by default the tensor-core kernels of a call start
+                                           while their predecessor drains (programmatic dependent launch)
+                                           and load the packed weights before they wait on it */
+#define RNN_FLAG_NO_TRANSPOSED 0x200u   /* keep the recurrent steps in the h W_h^T orientation */
+#define RNN_FLAG_FORCE_TRANSPOSED 0x400u /* take the recurrent steps as W_h h^T (bf16 LSTM / tanh RNN,
+                                            B <= 256, H % 32 == 0) or fail; by default chosen when
+                                            G*H >= 12288 */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */

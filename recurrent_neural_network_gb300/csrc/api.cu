@@ -127,6 +127,7 @@ struct rnn_s {
   int chunk = 1, nch = 1, wavefront = 0, bwd_bn = 128, bwd_splits = 1;
   int persist = 0, persist_ctas = 0;  // forward recurrence kind: 1 = persistent (one launch per layer)
   int fwd_mcast = 4;  // forward-step clusters along N sharing h_{t-1} by TMA multicast
+  int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
   uint64_t limit_ns = 2000000000ull;
   // sizes (bytes)
   size_t user_w_bytes = 0, packed_bytes = 0, reserve_bytes = 0, ws_bytes = 0;
@@ -213,9 +214,30 @@ int plan_and_layout(rnn_s* h) {
   else h->chunk = std::max(1, (T + 7) / 8);
   h->nch = (T + h->chunk - 1) / h->chunk;
 
-  // backward step tiles: 128-row batch tiles x bn hidden units, split over K
-  // until the step covers the SMs (at most 8 ways, at least 4 K blocks each)
-  if (d.mode == RNN_MODE_BF16) {
+  // Transposed recurrent steps: with many gate rows (a step of 256-row pair
+  // tiles covers most SMs) and at most 256 batch entries, W_h h^T puts the
+  // batch on the tile columns and keeps the epilogue's accesses contiguous.
+  if (d.mode == RNN_MODE_BF16 && !h->persist && (d.cell == RNN_LSTM || d.cell == RNN_TANH) && B <= 256 &&
+      H % 32 == 0 && !(d.flags & RNN_FLAG_NO_TRANSPOSED)) {
+    if (GH >= 12288 || (d.flags & RNN_FLAG_FORCE_TRANSPOSED)) h->tstep = 1;
+  }
+  if ((d.flags & RNN_FLAG_FORCE_TRANSPOSED) && !h->tstep) return RNN_ERR_UNSUPPORTED;
+  if (h->tstep) {
+    h->u = 1;
+    // backward: 128-unit x bn-batch tiles, K split in clusters of a power of
+    // two that the K blocks fill exactly, until the step covers the SMs
+    h->bwd_bn = B > 128 ? 256 : B > 64 ? 128 : 64;
+    const int tiles = (H + 127) / 128;
+    const int kb = (GH + 63) / 64;
+    int s = 1;
+    while (s * 2 <= 8 && tiles * s * 2 <= h->num_sms && h->bwd_bn % (16 * s * 2) == 0 && kb / (s * 2) >= 4 &&
+           (s * 2 - 1) * ((kb + s * 2 - 1) / (s * 2)) < kb)
+      s *= 2;
+    h->bwd_splits = s;
+    h->ctr_count = tiles;
+  } else if (d.mode == RNN_MODE_BF16) {
+    // backward step tiles: 128-row batch tiles x bn hidden units, split over K
+    // until the step covers the SMs (at most 8 ways, at least 4 K blocks each)
     h->bwd_bn = (H % 256 == 0) ? 256 : 128;
     // narrower tiles when even 8-way splits of 256-wide tiles leave most SMs idle
     if (h->bwd_bn == 256 && ((B + 127) / 128) * (H / 256) * 8 < h->num_sms / 2) h->bwd_bn = 128;
@@ -331,6 +353,8 @@ Launch mk(rnn_s* h, cudaStream_t s, void* ws, const char* name) {
   L.prof = (h->d.flags & RNN_FLAG_PROFILE) ? h->prof : nullptr;
   L.name = name;
   L.pair = (h->d.flags & RNN_FLAG_NO_PAIR) ? 0 : 1;
+  // per-kernel event timing needs each kernel to start after the previous one
+  L.pdl = (h->d.flags & (RNN_FLAG_NO_PDL | RNN_FLAG_PROFILE)) ? 0 : 1;
   return L;
 }
 
@@ -519,9 +543,10 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : "tanh";
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
-           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d",
+           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d transposed=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
-           h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms);
+           h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch,
+           h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms, h->tstep);
   return RNN_OK;
 }
 
@@ -591,7 +616,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
             A.mn_major = 0;
             A.mn_ext = (r1 - r0) * B;
             A.k_ext = In;
-            Operand Bw{PW + h->pl[l].wx, In, 0, GH, In};
+            Operand Bw{PW + h->pl[l].wx, In, 0, GH, In, 1};
             Remap none{0, 1, 1, 1};
             Launch Lk = mk(h, s, ws, "input_proj_gemm");
             RNN_TRY(gemm_f32(Lk, mode, A, Bw, (r1 - r0) * B, GH, In, P + (size_t)r0 * BGH, GH,
@@ -648,9 +673,10 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
             a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
             a.mcast = h->fwd_mcast;
             Operand A{hseq + (size_t)t * BH * e, H, 0, B, H};
-            Operand Bw{PW + h->pl[l].wh, H, 0, GH, H};
+            Operand Bw{PW + h->pl[l].wh, H, 0, GH, H, 1};
             Launch Lk = mk(h, s, ws, "fwd_step");
-            RNN_TRY(fwd_step(Lk, mode, d.cell, A, Bw, a));
+            if (h->tstep) RNN_TRY(fwd_step_t(Lk, d.cell, Bw, A, a));
+            else RNN_TRY(fwd_step(Lk, mode, d.cell, A, Bw, a));
           }
           if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + c], s)));
         }
@@ -725,9 +751,35 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
             a.cluster_splitk = 1;
             return a;
           };
-          Operand Bw{PW + h->pl[l].wh, H, 1, H, GH};
+          Operand Bw{PW + h->pl[l].wh, H, 1, H, GH, 1};
           for (int st = t1 - 1; st >= t0; --st) {
             BwdStepArgs a = args_for(st);
+            if (h->tstep) {
+              // transposed: the product writes dh_s, a pointwise kernel follows
+              PointVArgs pv{};
+              pv.B = B;
+              pv.H = H;
+              pv.dy = a.dy;
+              pv.dy_f32 = a.dy_f32;
+              pv.gates = a.gates;
+              pv.c_s = a.c_s;
+              pv.c_sm1 = a.c_sm1;
+              pv.carry = a.carry;
+              pv.dc0 = (st == 0 && dc0 && lstm) ? dc0 + l * BH : nullptr;
+              pv.dGx = a.dGx;
+              if (st == T - 1) {
+                pv.dh_init = dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr;
+              } else {
+                float* dhb = reinterpret_cast<float*>(W + h->wl[l].part);
+                Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
+                Launch Lk = mk(h, s, ws, "bwd_step");
+                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_splits, dhb, nullptr, 0));
+                pv.dh = dhb;
+              }
+              Launch Lp = mk(h, s, ws, "bwd_point");
+              RNN_TRY(bwd_point_v(Lp, d.cell, pv));
+              continue;
+            }
             if (st == T - 1) {
               Launch Lk = mk(h, s, ws, "bwd_point");
               RNN_TRY(bwd_point(Lk, mode, d.cell, a, dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr));
@@ -744,13 +796,18 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
             a.dc0 = (dc0 && lstm) ? dc0 + l * BH : nullptr;
             Operand A{R + h->rl[l].dgh, GH, 0, B, GH};
             Launch Lk = mk(h, s, ws, "bwd_step");
-            RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+            if (h->tstep) {
+              // dc0 came out of step 0's pointwise kernel
+              if (dh0) RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_splits, nullptr, a.dh0, 1));
+            } else {
+              RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+            }
           }
           // gradient of this chunk's layer inputs: dGx W_x
           if (l > 0 || dx) {
             const int In = h->In(l);
             Operand A{R + h->rl[l].dgx + (size_t)t0 * BGH * e, GH, 0, (t1 - t0) * B, GH};
-            Operand Bx{PW + h->pl[l].wx, In, 1, In, GH};
+            Operand Bx{PW + h->pl[l].wx, In, 1, In, GH, 1};
             Launch Lk = mk(h, s, ws, "dx_gemm");
             if (l > 0) {
               Remap none{0, 1, 1, 1};

@@ -18,6 +18,8 @@
 // All threads of a warp call load16 together (TMEM loads are warp-collective).
 #pragma once
 
+#include <type_traits>
+
 #include <cuda.h>
 
 #include "common.cuh"
@@ -36,6 +38,9 @@ struct GemmGeom {
   int cluster;                 // > 1: the split-K CTAs of a tile form one thread-block cluster
   int mcast;                   // > 1: clusters of `mcast` CTAs along N share (multicast) their A tile
   int nfast;                   // tile order: n-tiles fastest (needed by multicast clusters)
+  int pdl;                     // launched as a programmatic dependent: wait before touching produced data
+  int static_op;               // operand no earlier kernel writes (0 none, 1 A, 2 B): its first STAGES
+                               // blocks of the first tile are loaded before that wait
 };
 
 struct TileCoord {
@@ -51,6 +56,22 @@ struct TileCoord {
   float* red;
   uint64_t* red_full;
   uint64_t* red_done;
+};
+
+// Epilogues that declare a Stash type can stage their global inputs while the
+// MMAs run: stage() copies them into the CTA's idle second TMEM accumulator
+// (and into registers held in the Stash) before the accumulator is complete,
+// run_staged() then reads them from there.  The engine uses it when a CTA has
+// exactly one tile, so that the second accumulator stays unused.
+template <class E, class = void>
+struct EpiStaged {
+  static constexpr bool value = false;
+  using Stash = int;
+};
+template <class E>
+struct EpiStaged<E, std::void_t<typename E::Stash>> {
+  static constexpr bool value = true;
+  using Stash = typename E::Stash;
 };
 
 struct TmemAcc {
@@ -144,6 +165,7 @@ __global__ void __launch_bounds__(192, 1)
   tc::fence_after_sync();
   if (g.cluster > 1 || g.mcast > 1) tc::cluster_sync_all();  // peers' barriers exist before any remote traffic
   const uint32_t tmem_base = *tmem_slot;
+  tc::pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -154,6 +176,46 @@ __global__ void __launch_bounds__(192, 1)
       int last_par[STAGES];  // parity of the last load issued into each stage (-1: none)
       for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
       bool ok = true;
+      auto load_a = [&](uint8_t* sa, uint64_t* bar, int m0, int kb) {
+        const int k0 = kb * BK;
+        if (g.mcast > 1) {
+          // this CTA's 1/mcast of the A rows, into every peer's stage
+          const int rows = BM / g.mcast;
+          tc::tma_load_2d_mc(sa + crank * rows * 128, &mapA, bar, k0, m0 + crank * rows, mc_mask);
+        } else if (g.a_mn) {
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j) tc::tma_load_2d(sa + j * 8192, &mapA, bar, m0 + 64 * j, k0);
+        } else {
+          tc::tma_load_2d(sa, &mapA, bar, k0, m0);
+        }
+      };
+      auto load_b = [&](uint8_t* sb, uint64_t* bar, int n0, int kb) {
+        const int k0 = kb * BK;
+        if (g.b_mn) {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) tc::tma_load_2d(sb + j * 8192, &mapB, bar, n0 + 64 * j, k0);
+        } else {
+          tc::tma_load_2d(sb, &mapB, bar, k0, n0);
+        }
+      };
+      // programmatic dependent launch: the packed weights (the static operand)
+      // of the first stages can stream in before the kernels this one depends
+      // on finish
+      int pre = 0;
+      if (g.pdl) {
+        if (g.static_op && g.mcast == 1 && (int)blockIdx.x < g.num_tiles) {
+          int mt, nt, split;
+          decode_tile(g, blockIdx.x, mt, nt, split);
+          const int kb0 = split * g.kb_per_split;
+          pre = min(STAGES, min(g.kb_total, kb0 + g.kb_per_split) - kb0);
+          for (int i = 0; i < pre; ++i) {
+            tc::mbar_arrive_expect_tx(full + i, STAGE);
+            if (g.static_op == 1) load_a(smem + i * STAGE, full + i, mt * BM, kb0 + i);
+            else load_b(smem + i * STAGE + A_BYTES, full + i, nt * BN, kb0 + i);
+          }
+        }
+        tc::pdl_wait();
+      }
       for (int tile = blockIdx.x; tile < g.num_tiles && ok; tile += gridDim.x) {
         int mt, nt, split;
         decode_tile(g, tile, mt, nt, split);
@@ -161,31 +223,17 @@ __global__ void __launch_bounds__(192, 1)
         const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
         const int m0 = mt * BM, n0 = nt * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, g.err, g.limit_ns)) {
+          const bool prefilled = tile == (int)blockIdx.x && kb - kb0 < pre;  // static operand in flight, stage armed
+          if (!prefilled && !tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, g.err, g.limit_ns)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + stage * STAGE;
           uint8_t* sb = sa + A_BYTES;
-          tc::mbar_arrive_expect_tx(full + stage, STAGE);
+          if (!prefilled) tc::mbar_arrive_expect_tx(full + stage, STAGE);
           last_par[stage] = static_cast<int>(phase);
-          const int k0 = kb * BK;
-          if (g.mcast > 1) {
-            // this CTA's 1/mcast of the A rows, into every peer's stage
-            const int rows = BM / g.mcast;
-            tc::tma_load_2d_mc(sa + crank * rows * 128, &mapA, full + stage, k0, m0 + crank * rows, mc_mask);
-          } else if (g.a_mn) {
-#pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tc::tma_load_2d(sa + j * 8192, &mapA, full + stage, m0 + 64 * j, k0);
-          } else {
-            tc::tma_load_2d(sa, &mapA, full + stage, k0, m0);
-          }
-          if (g.b_mn) {
-#pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tc::tma_load_2d(sb + j * 8192, &mapB, full + stage, n0 + 64 * j, k0);
-          } else {
-            tc::tma_load_2d(sb, &mapB, full + stage, k0, n0);
-          }
+          if (!prefilled || g.static_op != 1) load_a(sa, full + stage, m0, kb);
+          if (!prefilled || g.static_op != 2) load_b(sb, full + stage, n0, kb);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -207,6 +255,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16(BM, BN, g.a_mn, g.b_mn);
+      if (g.pdl) tc::pdl_wait();  // the pipeline waits below are bounded from here on
       uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < g.num_tiles && ok; tile += gridDim.x) {
@@ -250,12 +299,16 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = q * 32 + lane;
+    if (g.pdl) tc::pdl_wait();  // the epilogue reads and writes data of earlier kernels
     uint32_t acc = 0, aphase = 0;
+    const uint32_t lane_q = static_cast<uint32_t>(q * 32) << 16;
     for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
       int mt, nt, split;
       decode_tile(g, tile, mt, nt, split);
+      const bool solo = tile == (int)blockIdx.x && tile + (int)gridDim.x >= g.num_tiles;
+      typename EpiStaged<Epi>::Stash stash;
       {
-        // let the epilogue's own global inputs travel to L2 while the MMAs run
+        // let the epilogue's own global inputs travel to L2 (or on-chip) while the MMAs run
         TileCoord tp;
         tp.m0 = mt * BM;
         tp.n0 = nt * BN;
@@ -271,6 +324,9 @@ __global__ void __launch_bounds__(192, 1)
         tp.red_full = red_full;
         tp.red_done = red_done;
         epi.prefetch(tp, row, BN);
+        if constexpr (EpiStaged<Epi>::value) {
+          if (solo) epi.stage(tp, row, tmem_base + BN + lane_q, BN, stash);
+        }
       }
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
@@ -291,8 +347,13 @@ __global__ void __launch_bounds__(192, 1)
       t.red = reinterpret_cast<float*>(smem);
       t.red_full = red_full;
       t.red_done = red_done;
-      TmemAcc a{tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16)};
-      epi(t, row, a, BN);
+      TmemAcc a{tmem_base + acc * BN + lane_q};
+      if constexpr (EpiStaged<Epi>::value) {
+        if (solo) epi.run_staged(t, row, a, TmemAcc{tmem_base + BN + lane_q}, BN, stash);
+        else epi(t, row, a, BN);
+      } else {
+        epi(t, row, a, BN);
+      }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(tempty + acc);
@@ -391,6 +452,7 @@ __global__ void __launch_bounds__(192, 1)
   tc::fence_after_sync();
   tc::cluster_sync_all();  // both CTAs' barriers and TMEM exist before any pair traffic
   const uint32_t tmem_base = *tmem_slot;
+  tc::pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -399,6 +461,43 @@ __global__ void __launch_bounds__(192, 1)
       int last_par[STAGES];
       for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
       bool ok = true;
+      auto load_a = [&](uint8_t* sa, uint32_t fb, int m0, int kb) {
+        const int k0 = kb * BK;
+        if (g.a_mn) {
+#pragma unroll
+          for (int j = 0; j < 2; ++j) tc::tma_load_2d_pair(sa + j * 8192, &mapA, fb, m0 + 64 * j, k0);
+        } else {
+          tc::tma_load_2d_pair(sa, &mapA, fb, k0, m0);
+        }
+      };
+      auto load_b = [&](uint8_t* sb, uint32_t fb, int n0, int kb) {
+        const int k0 = kb * BK;
+        if (g.b_mn) {
+#pragma unroll
+          for (int j = 0; j < HB / 64; ++j) tc::tma_load_2d_pair(sb + j * 8192, &mapB, fb, n0 + 64 * j, k0);
+        } else {
+          tc::tma_load_2d_pair(sb, &mapB, fb, k0, n0);
+        }
+      };
+      // programmatic dependent launch: the packed weights (the static operand)
+      // of the first stages can stream in before the kernels this one depends
+      // on finish
+      int pre = 0;
+      if (g.pdl) {
+        if (g.static_op && pair < g.num_tiles) {
+          int mt, nt, split;
+          decode_tile(g, pair, mt, nt, split);
+          const int kb0 = split * g.kb_per_split;
+          pre = min(STAGES, min(g.kb_total, kb0 + g.kb_per_split) - kb0);
+          for (int i = 0; i < pre; ++i) {
+            const uint32_t fb = tc::mapa(tc::smem_addr(full + i), leader);
+            if (is_leader) tc::mbar_arrive_expect_tx(full + i, 2 * STAGE);
+            if (g.static_op == 1) load_a(smem + i * STAGE, fb, mt * BM + pr * 128, kb0 + i);
+            else load_b(smem + i * STAGE + A_BYTES, fb, nt * BN + pr * HB, kb0 + i);
+          }
+        }
+        tc::pdl_wait();
+      }
       for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
         int mt, nt, split;
         decode_tile(g, tile, mt, nt, split);
@@ -406,28 +505,18 @@ __global__ void __launch_bounds__(192, 1)
         const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
         const int m0 = mt * BM + pr * 128, n0 = nt * BN + pr * HB;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, g.err, g.limit_ns)) {
+          const bool prefilled = tile == pair && kb - kb0 < pre;  // static operand in flight, stage armed
+          if (!prefilled && !tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, g.err, g.limit_ns)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + stage * STAGE;
           uint8_t* sb = sa + A_BYTES;
           const uint32_t fb = tc::mapa(tc::smem_addr(full + stage), leader);
-          if (is_leader) tc::mbar_arrive_expect_tx(full + stage, 2 * STAGE);
+          if (is_leader && !prefilled) tc::mbar_arrive_expect_tx(full + stage, 2 * STAGE);
           last_par[stage] = static_cast<int>(phase);
-          const int k0 = kb * BK;
-          if (g.a_mn) {
-#pragma unroll
-            for (int j = 0; j < 2; ++j) tc::tma_load_2d_pair(sa + j * 8192, &mapA, fb, m0 + 64 * j, k0);
-          } else {
-            tc::tma_load_2d_pair(sa, &mapA, fb, k0, m0);
-          }
-          if (g.b_mn) {
-#pragma unroll
-            for (int j = 0; j < HB / 64; ++j) tc::tma_load_2d_pair(sb + j * 8192, &mapB, fb, n0 + 64 * j, k0);
-          } else {
-            tc::tma_load_2d_pair(sb, &mapB, fb, k0, n0);
-          }
+          if (!prefilled || g.static_op != 1) load_a(sa, fb, m0, kb);
+          if (!prefilled || g.static_op != 2) load_b(sb, fb, n0, kb);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -448,6 +537,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ MMA issuer (even CTA)
     if (lane == 0 && is_leader) {
       const uint32_t idesc = tc::idesc_bf16(BM, BN, g.a_mn, g.b_mn);
+      if (g.pdl) tc::pdl_wait();  // the pipeline waits below are bounded from here on
       uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
       bool ok = true;
       for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
@@ -491,10 +581,14 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     const uint32_t te_base = tc::mapa(tc::smem_addr(tempty), leader);
+    if (g.pdl) tc::pdl_wait();  // the epilogue reads and writes data of earlier kernels
     uint32_t acc = 0, aphase = 0;
+    const uint32_t lane_q = static_cast<uint32_t>(q * 32) << 16;
     for (int tile = pair; tile < g.num_tiles; tile += npairs) {
       int mt, nt, split;
       decode_tile(g, tile, mt, nt, split);
+      const bool solo = tile == pair && tile + npairs >= g.num_tiles;
+      typename EpiStaged<Epi>::Stash stash;
       TileCoord t;
       t.m0 = mt * BM + pr * 128;
       t.n0 = nt * BN;
@@ -510,13 +604,21 @@ __global__ void __launch_bounds__(192, 1)
       t.red_full = red_full;
       t.red_done = red_done;
       epi.prefetch(t, row, BN);
+      if constexpr (EpiStaged<Epi>::value) {
+        if (solo) epi.stage(t, row, tmem_base + BN + lane_q, BN, stash);
+      }
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc::fence_after_sync();
-      TmemAcc a{tmem_base + acc * BN + (static_cast<uint32_t>(q * 32) << 16)};
-      epi(t, row, a, BN);
+      TmemAcc a{tmem_base + acc * BN + lane_q};
+      if constexpr (EpiStaged<Epi>::value) {
+        if (solo) epi.run_staged(t, row, a, TmemAcc{tmem_base + BN + lane_q}, BN, stash);
+        else epi(t, row, a, BN);
+      } else {
+        epi(t, row, a, BN);
+      }
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_remote(te_base + acc * 8);

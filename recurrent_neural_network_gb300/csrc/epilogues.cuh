@@ -453,4 +453,384 @@ struct EpiBwdStep {
   }
 };
 
+// ---------------------------------------------------------------------------
+// Transposed recurrent steps.  With many gate rows and at most a few hundred
+// batch rows the step product is taken as W_h h^T instead of h W_h^T: tile
+// rows are packed gate rows (forward) or hidden units (backward) and tile
+// columns are batch entries.  A warp's 32 TMEM lanes are then 32 consecutive
+// rows, so each of its global accesses in the epilogue is one contiguous run
+// (the batch-row-per-thread layout above touches 32 separate lines per
+// access).  These epilogues use the packing unit u = 1: packed row G*j + g is
+// gate g of hidden unit j, so the four LSTM gates of a unit sit in four
+// neighbouring lanes of one warp.
+
+// a[s] for a lane-dependent s in 0..3 without local-memory indexing
+__device__ __forceinline__ float pick4(float a0, float a1, float a2, float a3, int s) {
+  const float lo = (s & 1) ? a1 : a0, hi = (s & 1) ? a3 : a2;
+  return (s & 2) ? hi : lo;
+}
+
+// Forward step, tile = 128 packed gate rows (one CTA of a pair) x bn batch
+// entries.  acc[p][b] = (W_h h_{t-1}^T)[p][b].  When the CTA owns a single
+// tile, stage() moves this tile's slice of P into the idle second TMEM
+// accumulator (and the LSTM c_{t-1} values into registers) while the MMAs
+// run, so the epilogue proper only reads TMEM and stores.
+template <int CELL>
+struct EpiFwdStepT {
+  using S = __nv_bfloat16;
+  static constexpr int kAhead = 4;  // chunks of c_{t-1} loaded ahead of their use
+  struct Stash {
+    float cp[kAhead][4];  // LSTM c_{t-1} of the next kAhead chunks
+  };
+  int B, H;
+  float* P;          // [B][G*H] this step: input projection incl. bias; activated gates written back if write_gates
+  int write_gates;
+  const float* c_prev;  // LSTM [B][H], null = zero
+  float* c_out;         // LSTM [B][H]
+  S* h_out;             // [B][H]
+  S* y;                 // [B][H] or null
+  S* hT;                // [B][H] or null
+  float* cT;            // [B][H] or null
+
+  __device__ __forceinline__ void prefetch(const TileCoord& t, int row, int bn) const {
+    constexpr int G = CellInfo<CELL>::G;
+    const int GH = G * H;
+    if (t.m0 >= GH) return;
+    const int rows = min(128, GH - t.m0);
+    for (int i = row; i < bn; i += 128) {
+      const int b = t.n0 + i;
+      if (b >= B) break;
+      tc::prefetch_l2(P + (size_t)b * GH + t.m0, rows * 4);
+      if (CELL == LSTM && c_prev) tc::prefetch_l2(c_prev + (size_t)b * H + t.m0 / 4, rows);
+    }
+  }
+
+  // c_{t-1} for the (unit p/4, batch entry c + 4k + p%4) pairs of chunk c
+  __device__ __forceinline__ void load_cp(int n0, int p, bool live, int c, int nmax, float* cp) const {
+    const int g = p & 3, j = p >> 2;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int bi = c + 4 * k + g;
+      cp[k] = (live && c_prev && bi < nmax) ? c_prev[(size_t)(n0 + bi) * H + j] : 0.f;
+    }
+  }
+
+  // v: pre-activations (P included) of gate row p for batch entries c..c+15
+  __device__ __forceinline__ void finish(int n0, int p, bool live, int c, int nb, float* v, const float* cp) const {
+    constexpr int G = CellInfo<CELL>::G;
+    const int GH = G * H;
+    float* pc = P + (size_t)(n0 + c) * GH + p;
+    if constexpr (CELL == LSTM) {
+      // g = p % 4: input, forget, cell candidate (tanh), output gate
+      const int g = p & 3;
+      const float sc = g == 2 ? 1.f : 0.5f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float th = tanh_hw(sc * v[i]);
+        v[i] = g == 2 ? th : fmaf(0.5f, th, 0.5f);
+      }
+      if (write_gates && live) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < nb) pc[(size_t)i * GH] = v[i];
+      }
+      // 4 x 4 transposes within each group of four lanes: afterwards lane g
+      // of unit j holds all four gates of j for batch entry c + 4k + g
+      const int j = p >> 2;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float q0 = v[4 * k], q1 = v[4 * k + 1], q2 = v[4 * k + 2], q3 = v[4 * k + 3];
+        float gt[4];
+        gt[0] = gt[1] = gt[2] = gt[3] = pick4(q0, q1, q2, q3, g);
+#pragma unroll
+        for (int r = 1; r < 4; ++r) {
+          const float got = __shfl_xor_sync(0xffffffffu, pick4(q0, q1, q2, q3, g ^ r), r);
+          const int src = g ^ r;  // the lane holding gate src sent its value for batch entry c + 4k + g
+          gt[0] = src == 0 ? got : gt[0];
+          gt[1] = src == 1 ? got : gt[1];
+          gt[2] = src == 2 ? got : gt[2];
+          gt[3] = src == 3 ? got : gt[3];
+        }
+        const int bi = 4 * k + g;
+        if (!live || bi >= nb) continue;
+        const size_t bj = (size_t)(n0 + c + bi) * H + j;
+        const float cn = gt[1] * cp[k] + gt[0] * gt[2];
+        const float hn = gt[3] * tanh_hw(cn);
+        c_out[bj] = cn;
+        if (cT) cT[bj] = cn;
+        const S hb = __float2bfloat16_rn(hn);
+        h_out[bj] = hb;
+        if (y) y[bj] = hb;
+        if (hT) hT[bj] = hb;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = tanh_hw(v[i]);
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (i >= nb) continue;
+          if (write_gates) pc[(size_t)i * GH] = v[i];
+          const size_t bj = (size_t)(n0 + c + i) * H + p;
+          const S hb = __float2bfloat16_rn(v[i]);
+          h_out[bj] = hb;
+          if (y) y[bj] = hb;
+          if (hT) hT[bj] = hb;
+        }
+      }
+    }
+  }
+
+  template <class Acc>
+  __device__ __forceinline__ void operator()(const TileCoord& t, int row, const Acc& acc, int bn) const {
+    constexpr int G = CellInfo<CELL>::G;
+    const int GH = G * H;
+    const int p = t.m0 + row;  // packed gate row of this lane
+    const bool live = p < GH;
+    const int nmax = min(bn, B - t.n0);
+#pragma unroll 1
+    for (int c = 0; c < nmax; c += 16) {
+      float v[16], pv[16], cp[4];
+      const int nb = min(16, nmax - c);
+      const float* pc = P + (size_t)(t.n0 + c) * GH + p;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pv[i] = (live && i < nb) ? pc[(size_t)i * GH] : 0.f;
+      if (CELL == LSTM) load_cp(t.n0, p, live, c, nmax, cp);
+      acc.load16(c, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] += pv[i];
+      finish(t.n0, p, live, c, nb, v, cp);
+    }
+  }
+
+  __device__ __forceinline__ void stage(const TileCoord& t, int row, uint32_t taddr, int bn, Stash& st) const {
+    constexpr int G = CellInfo<CELL>::G;
+    const int GH = G * H;
+    const int p = t.m0 + row;
+    const bool live = p < GH;
+    const int nmax = min(bn, B - t.n0);
+    if constexpr (CELL == LSTM) {
+#pragma unroll
+      for (int a = 0; a < kAhead; ++a) load_cp(t.n0, p, live, 16 * a, nmax, st.cp[a]);
+    }
+    // P, two chunks (32 loads per lane) in flight at a time
+#pragma unroll 1
+    for (int c = 0; c < nmax; c += 32) {
+      float v0[16], v1[16];
+      const float* pc = P + (size_t)(t.n0 + c) * GH + p;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        v0[i] = (live && c + i < nmax) ? pc[(size_t)i * GH] : 0.f;
+        v1[i] = (live && c + 16 + i < nmax) ? pc[(size_t)(16 + i) * GH] : 0.f;
+      }
+      tc::tmem_store16(taddr + c, v0);
+      if (c + 16 < nmax) tc::tmem_store16(taddr + c + 16, v1);
+    }
+    tc::tmem_store_wait();
+  }
+
+  template <class Acc>
+  __device__ __forceinline__ void run_staged(const TileCoord& t, int row, const Acc& acc, const Acc& staged, int bn,
+                                             Stash& st) const {
+    constexpr int G = CellInfo<CELL>::G;
+    const int p = t.m0 + row;
+    const bool live = p < G * H;
+    const int nmax = min(bn, B - t.n0);
+#pragma unroll 1
+    for (int c = 0; c < nmax; c += 16) {
+      float v[16], pv[16], cp[4];
+      acc.load16(c, v);
+      staged.load16(c, pv);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] += pv[i];
+      if constexpr (CELL == LSTM) {
+        // rotate the look-ahead ring and start the loads of chunk c + kAhead
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cp[k] = st.cp[0][k];
+#pragma unroll
+        for (int a = 0; a + 1 < kAhead; ++a)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) st.cp[a][k] = st.cp[a + 1][k];
+        load_cp(t.n0, p, live, c + 16 * kAhead, nmax, st.cp[kAhead - 1]);
+      }
+      finish(t.n0, p, live, c, min(16, nmax - c), v, cp);
+    }
+  }
+};
+
+// Backward step product, tile = 128 hidden units x bn batch entries:
+// acc[j][b] = (W_h^T dG_{s+1}^T)[j][b] = dh_s[b][j] before the gradient from
+// above is added.  The epilogue only stores dh (fp32 [B][H]; bf16 dh0 for
+// the final product); the pointwise step runs as its own full-occupancy
+// kernel (bwd_point_v), whose wide loads keep far more bytes in flight than
+// the 128 epilogue threads of a CTA can.  K splits reduce through the
+// cluster's shared memory, each CTA storing bn / splits batch columns.
+struct EpiBwdDhT {
+  using S = __nv_bfloat16;
+  int B, H;
+  float* dh;   // [B][H] (not final)
+  S* dh0;      // [B][H] (final)
+  int final_;
+  int* err;
+  uint64_t limit_ns;
+
+  __device__ __forceinline__ void prefetch(const TileCoord&, int, int) const {}
+
+  __device__ __forceinline__ void put(int j, int b, float v) const {
+    const size_t bj = (size_t)b * H + j;
+    if (final_) dh0[bj] = __float2bfloat16_rn(v);
+    else dh[bj] = v;
+  }
+
+  template <class Acc>
+  __device__ __forceinline__ void operator()(const TileCoord& t, int row, const Acc& acc, int bn) const {
+    const int j = t.m0 + row;
+    const bool live = j < H && (!final_ || dh0);
+    if (t.cluster > 1) {
+      const int RS = bn + 4;
+      const int lane = threadIdx.x & 31;
+      float* mine = t.red + (size_t)row * RS;
+      for (int c = 0; c < bn; c += 16) {
+        float v[16];
+        acc.load16(c, v);
+        float4* d = reinterpret_cast<float4*>(mine + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+      tc::fence_acq_rel_cluster();
+      __syncwarp();
+      const uint32_t full_local = tc::smem_addr(t.red_full), done_local = tc::smem_addr(t.red_done);
+      if (lane == 0)
+        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(full_local, t.peer_base + p * t.peer_stride));
+      int ok = 1;
+      if (lane == 0) ok = tc::mbar_wait_cluster(t.red_full, 0, err, limit_ns) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok && live) {
+        const int cw = bn / t.cluster;
+        const uint32_t mine_addr = tc::smem_addr(mine);
+#pragma unroll 1
+        for (int c = t.split * cw; c < (t.split + 1) * cw; c += 16) {
+          if (t.n0 + c >= B) break;
+          float v[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+          for (int p = 0; p < t.cluster; ++p) {
+            const uint32_t ra = tc::mapa(mine_addr, t.peer_base + p * t.peer_stride) + c * 4;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float w[4];
+              tc::ld_dsmem4(ra + 16 * q, w);
+              v[4 * q] += w[0]; v[4 * q + 1] += w[1]; v[4 * q + 2] += w[2]; v[4 * q + 3] += w[3];
+            }
+          }
+          const int nb = min(16, B - (t.n0 + c));
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < nb) put(j, t.n0 + c + i, v[i]);
+        }
+      }
+      tc::fence_acq_rel_cluster();
+      __syncwarp();
+      if (lane == 0)
+        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(done_local, t.peer_base + p * t.peer_stride));
+      if (lane == 0) tc::mbar_wait_cluster(t.red_done, 0, err, limit_ns);
+      __syncwarp();
+      return;
+    }
+    const int nmax = min(bn, B - t.n0);
+    for (int c = 0; c < nmax; c += 16) {
+      float v[16];
+      acc.load16(c, v);
+      const int nb = min(16, nmax - c);
+      if (live) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < nb) put(j, t.n0 + c + i, v[i]);
+      }
+    }
+  }
+};
+
+// Pointwise backward step s for the packing unit 1, four hidden units of one
+// batch entry per thread (16-byte loads and stores throughout):
+//   dh = dh_s (+ dy_s);  LSTM: tau = tanh(c_s), dc = carry + dh o (1 - tau^2),
+//   d(i, f, g, o) = (dc g i(1-i), dc c_{s-1} f(1-f), dc i (1-g^2), dh tau o(1-o)),
+//   carry <- dc f;   tanh RNN: d = dh (1 - h_s^2).
+template <int CELL>
+struct BwdPointV {
+  using S = __nv_bfloat16;
+  int B, H;
+  const float* dh;      // [B][H] product part of dh_s, or null
+  const S* dh_init;     // [B][H] used when dh is null (gradient into the last step), or null = zero
+  const void* dy;       // [B][H] (float if dy_f32 else S), or null
+  int dy_f32;
+  const float* gates;   // [B][G*H] activated gates of step s (tanh RNN: h_s)
+  const float* c_s;     // LSTM [B][H]
+  const float* c_sm1;   // LSTM [B][H], null = zero
+  float* carry;         // LSTM [B][H]: dc into step s (in) / into s-1 (out)
+  float* dc0;           // LSTM [B][H]: also receives the outgoing carry (s = 0), or null
+  S* dGx;               // [B][G*H]
+
+  __device__ __forceinline__ void run(long long q) const {
+    // q indexes groups of four hidden units: b = q / (H/4), j0 = 4 (q % (H/4))
+    const int hq = H / 4;
+    const int b = (int)(q / hq), j0 = 4 * (int)(q % hq);
+    const size_t bj = (size_t)b * H + j0;
+    float4 d = dh ? *reinterpret_cast<const float4*>(dh + bj) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!dh && dh_init) {
+      const uint2 w = *reinterpret_cast<const uint2*>(dh_init + bj);
+      d = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                      __uint_as_float(w.y & 0xFFFF0000u));
+    }
+    if (dy) {
+      if (dy_f32) {
+        const float4 e = *reinterpret_cast<const float4*>(static_cast<const float*>(dy) + bj);
+        d.x += e.x; d.y += e.y; d.z += e.z; d.w += e.w;
+      } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const S*>(dy) + bj);
+        d.x += __uint_as_float(w.x << 16); d.y += __uint_as_float(w.x & 0xFFFF0000u);
+        d.z += __uint_as_float(w.y << 16); d.w += __uint_as_float(w.y & 0xFFFF0000u);
+      }
+    }
+    const float dhv[4] = {d.x, d.y, d.z, d.w};
+    if constexpr (CELL == LSTM) {
+      const float4* gp = reinterpret_cast<const float4*>(gates + (size_t)b * 4 * H + 4 * (size_t)j0);
+      const float4 g4[4] = {gp[0], gp[1], gp[2], gp[3]};
+      const float4 cs = *reinterpret_cast<const float4*>(c_s + bj);
+      const float4 cp = c_sm1 ? *reinterpret_cast<const float4*>(c_sm1 + bj) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 dc = *reinterpret_cast<const float4*>(carry + bj);
+      const float csv[4] = {cs.x, cs.y, cs.z, cs.w}, cpv[4] = {cp.x, cp.y, cp.z, cp.w}, dcv_in[4] = {dc.x, dc.y, dc.z, dc.w};
+      float dco[4];
+      uint32_t packed[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 gt = g4[k];
+        const float tau = tanh_hw(csv[k]);
+        const float dov = dhv[k] * tau;
+        const float dcv = dcv_in[k] + dhv[k] * gt.w * (1.f - tau * tau);
+        const float d0 = dcv * gt.z * gt.x * (1.f - gt.x);
+        const float d1 = dcv * cpv[k] * gt.y * (1.f - gt.y);
+        const float d2 = dcv * gt.x * (1.f - gt.z * gt.z);
+        const float d3 = dov * gt.w * (1.f - gt.w);
+        dco[k] = dcv * gt.y;
+        packed[2 * k] = pack_bf16x2(d0, d1);
+        packed[2 * k + 1] = pack_bf16x2(d2, d3);
+      }
+      const float4 co = make_float4(dco[0], dco[1], dco[2], dco[3]);
+      *reinterpret_cast<float4*>(carry + bj) = co;
+      if (dc0) *reinterpret_cast<float4*>(dc0 + bj) = co;
+      uint4* gx = reinterpret_cast<uint4*>(dGx + (size_t)b * 4 * H + 4 * (size_t)j0);
+      gx[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      gx[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    } else {
+      const float4 hv = *reinterpret_cast<const float4*>(gates + bj);
+      const float hvv[4] = {hv.x, hv.y, hv.z, hv.w};
+      float o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = dhv[k] * (1.f - hvv[k] * hvv[k]);
+      *reinterpret_cast<uint2*>(dGx + bj) = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+    }
+  }
+};
+
 }  // namespace rnn

@@ -60,6 +60,27 @@ inline int cuda_status(cudaError_t e) {
   return RNN_ERR_CUDA;
 }
 
+// Launch attributes of a tcgen05 engine launch: a cluster shape when the
+// cluster has more than one CTA, and programmatic stream serialization when
+// the kernel may start while the previous kernel on the stream is finishing
+// (the engine waits on the grid dependency before it touches produced data).
+inline unsigned launch_attrs(cudaLaunchAttribute* at, int cluster, int pdl) {
+  unsigned n = 0;
+  if (cluster > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  return n;
+}
+
 // cluster_splitk: with more than one K split, the splits of each output tile
 // run as one thread-block cluster and reduce through distributed shared
 // memory (the epilogue must support it); one tile per CTA.
@@ -112,26 +133,18 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   int grid = std::min(g.num_tiles, cap);
   if (g.mcast > 1) grid = std::max(g.mcast, grid / g.mcast * g.mcast);
   const int cl = g.cluster > 1 ? g.cluster : g.mcast;
-  cudaError_t e;
+  g.pdl = L.pdl;
+  g.static_op = A.is_static ? 1 : B.is_static ? 2 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g.cluster > 1 ? g.num_tiles : grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute at[2];
+  cfg.attrs = at;
+  cfg.numAttrs = launch_attrs(at, cl, L.pdl);
   launch_begin(L);
-  if (cl > 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(g.cluster > 1 ? g.num_tiles : grid);
-    cfg.blockDim = dim3(192);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = L.stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = cl;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, g, epi);
-  } else {
-    kern<<<grid, 192, smem, L.stream>>>(ma, mb, g, epi);
-    e = cudaGetLastError();
-  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, g, epi);
   launch_end(L);
   return cuda_status(e);
 }
@@ -180,18 +193,16 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   const int cap = (max_ctas > 0 ? max_ctas : L.num_sms) / 2;
   // split-K: one tile per pair so that the cluster reduction can reuse the stages
   const int pairs = g.cluster > 1 ? g.num_tiles : std::max(1, std::min(g.num_tiles, cap));
+  g.pdl = L.pdl;
+  g.static_op = A.is_static ? 1 : B.is_static ? 2 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2 * g.cluster;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute at[2];
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_attrs(at, 2 * g.cluster, L.pdl);
   launch_begin(L);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, g, epi);
   launch_end(L);
@@ -214,6 +225,8 @@ int launch_simt(const Launch& L, const Operand& A, const Operand& B, int M, int 
   g.cluster = 1;
   g.mcast = 1;
   g.nfast = 0;
+  g.pdl = 0;
+  g.static_op = 0;
   g.a_mn = A.mn_major;
   g.b_mn = B.mn_major;
   g.limit_ns = L.limit_ns;

@@ -15,6 +15,9 @@ struct Operand {
   long long ld;
   int mn_major;
   int mn_ext, k_ext;
+  // 1: no kernel that may still be running writes this operand (packed
+  // weights), so a dependent launch may start loading it before it waits
+  int is_static = 0;
 };
 
 struct Profiler;  // defined in api.cu
@@ -29,6 +32,7 @@ struct Launch {
   Profiler* prof;
   const char* name;
   int pair = 1;  // products with more than 128 rows may run on CTA pairs (256-row tiles)
+  int pdl = 0;   // launch as a programmatic dependent of the previous kernel on the stream
 };
 
 // profiling / counting hooks (api.cu)
@@ -77,6 +81,9 @@ struct FwdStepArgs {
 };
 // one forward timestep of one layer: A = h_{t-1} [B][H], B = packed W_h [G*H][H]
 int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, const FwdStepArgs& a);
+// the same step transposed (bf16, LSTM / tanh RNN, packing unit 1):
+// A = packed W_h [G*H][H], B = h_{t-1} [B][H]; tiles of 256 gate rows x the batch
+int fwd_step_t(const Launch& L, int cell, const Operand& Wh, const Operand& Hp, const FwdStepArgs& a);
 
 // ---------------------------------------------------------------- step_bwd.cu
 struct BwdStepArgs {
@@ -104,6 +111,27 @@ int bwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
 // pointwise-only backward step (the last timestep): dh starts from dh_init
 // ([B][H], storage type, null = zero)
 int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const void* dh_init);
+// Transposed backward product (bf16, packing unit 1): A = packed W_h read
+// MN-major ([H] x [G*H]), B = dG_{s+1} [B][G*H]; tiles of 128 hidden units x
+// the batch, K split `splits` ways inside clusters.  Writes dh (fp32 [B][H]),
+// or dh0 (bf16 [B][H]) when final_ (dh0 null: nothing to write).
+int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int splits, float* dh,
+             void* dh0, int final_);
+// the pointwise backward step that follows it (packing unit 1, H % 4 == 0)
+struct PointVArgs {
+  int B, H;
+  const float* dh;      // product part of dh_s, or null
+  const void* dh_init;  // bf16 [B][H] used when dh is null, or null = zero
+  const void* dy;       // [B][H] gradient from above, float if dy_f32 else bf16, or null
+  int dy_f32;
+  const float* gates;   // [B][G*H]
+  const float* c_s;     // LSTM
+  const float* c_sm1;   // LSTM, null = zero
+  float* carry;         // LSTM
+  float* dc0;           // LSTM, step 0 only: copy of the outgoing carry, or null
+  void* dGx;            // bf16 [B][G*H]
+};
+int bwd_point_v(const Launch& L, int cell, const PointVArgs& a);
 
 // ---------------------------------------------------------------- persist.cu
 struct PersistArgs {

@@ -111,4 +111,67 @@ int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const v
   return point_launch<TANH, float>(L, a, dh_init);
 }
 
+namespace {
+template <int CELL>
+__global__ void __launch_bounds__(256) bwd_point_v_kernel(const BwdPointV<CELL> p) {
+  const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q < (long long)p.B * (p.H / 4)) p.run(q);
+}
+}  // namespace
+
+int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int splits, float* dh,
+             void* dh0, int final_) {
+  const int M = H, N = B, K = G * H;
+  EpiBwdDhT e;
+  e.B = B;
+  e.H = H;
+  e.dh = dh;
+  e.dh0 = static_cast<__nv_bfloat16*>(dh0);
+  e.final_ = final_;
+  e.err = L.err;
+  e.limit_ns = L.limit_ns;
+  // the K splits of a tile reduce inside a cluster (the only split-K path of
+  // this epilogue): bn / splits must be a multiple of 16, at most 8 splits
+  const int bn = N > 128 ? 256 : N > 64 ? 128 : 64;
+  const int kb = (K + 63) / 64, sp = std::max(1, std::min(splits, kb));
+  const int eff = (kb + (kb + sp - 1) / sp - 1) / ((kb + sp - 1) / sp);
+  if (eff > 1 && (eff > 8 || bn % (16 * eff))) return RNN_ERR_UNSUPPORTED;
+  if (N > 128) return launch_tc<256, 4>(L, WhT, dG, M, N, K, splits, 0, e, true);
+  if (N > 64) return launch_tc<128, 6>(L, WhT, dG, M, N, K, splits, 0, e, true);
+  return launch_tc<64, 8>(L, WhT, dG, M, N, K, splits, 0, e, true);
+}
+
+int bwd_point_v(const Launch& L, int cell, const PointVArgs& a) {
+  if (a.H % 4 || (cell != LSTM && cell != TANH)) return RNN_ERR_UNSUPPORTED;
+  const long long n = (long long)a.B * (a.H / 4);
+  const int grid = (int)((n + 255) / 256);
+  auto fill = [&](auto& p) {
+    p.B = a.B;
+    p.H = a.H;
+    p.dh = a.dh;
+    p.dh_init = static_cast<const __nv_bfloat16*>(a.dh_init);
+    p.dy = a.dy;
+    p.dy_f32 = a.dy_f32;
+    p.gates = a.gates;
+    p.c_s = a.c_s;
+    p.c_sm1 = a.c_sm1;
+    p.carry = a.carry;
+    p.dc0 = a.dc0;
+    p.dGx = static_cast<__nv_bfloat16*>(a.dGx);
+  };
+  launch_begin(L);
+  if (cell == LSTM) {
+    BwdPointV<LSTM> p;
+    fill(p);
+    bwd_point_v_kernel<LSTM><<<grid, 256, 0, L.stream>>>(p);
+  } else {
+    BwdPointV<TANH> p;
+    fill(p);
+    bwd_point_v_kernel<TANH><<<grid, 256, 0, L.stream>>>(p);
+  }
+  const cudaError_t e = cudaGetLastError();
+  launch_end(L);
+  return cuda_status(e);
+}
+
 }  // namespace rnn

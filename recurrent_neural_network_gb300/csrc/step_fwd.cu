@@ -65,4 +65,40 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
   return RNN_ERR_UNSUPPORTED;
 }
 
+namespace {
+template <int CELL>
+EpiFwdStepT<CELL> make_epi_t(const FwdStepArgs& a) {
+  using S = __nv_bfloat16;
+  EpiFwdStepT<CELL> e;
+  e.B = a.B;
+  e.H = a.H;
+  e.P = a.P;
+  e.write_gates = a.write_gates;
+  e.c_prev = a.c_prev;
+  e.c_out = a.c_out;
+  e.h_out = static_cast<S*>(a.h_out);
+  e.y = static_cast<S*>(a.y);
+  e.hT = static_cast<S*>(a.hT);
+  e.cT = a.cT;
+  return e;
+}
+}  // namespace
+
+int fwd_step_t(const Launch& L, int cell, const Operand& Wh, const Operand& Hp, const FwdStepArgs& a) {
+  const int G = cell == LSTM ? 4 : cell == TANH ? 1 : 0;
+  if (!G || a.u != 1) return RNN_ERR_UNSUPPORTED;
+  const int M = G * a.H, N = a.B, K = a.H;
+  // one n-tile holds the whole batch (up to 256 entries): W_h streams once per step
+  if (N > 128) {
+    if (cell == LSTM) return launch_tc2<256, 6>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a));
+    return launch_tc2<256, 6>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a));
+  }
+  if (N > 64) {
+    if (cell == LSTM) return launch_tc2<128, 8>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a));
+    return launch_tc2<128, 8>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a));
+  }
+  if (cell == LSTM) return launch_tc2<64, 10>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a));
+  return launch_tc2<64, 10>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a));
+}
+
 }  // namespace rnn

@@ -25,7 +25,10 @@ FLAG_PROFILE = 0x8
 FLAG_NO_MULTICAST = 0x10
 FLAG_NO_PAIR = 0x20
 FLAG_NO_GRAPH = 0x40
+FLAG_NO_PDL = 0x80
 FLAG_TEST_SKIP_PUBLISH = 0x100
+FLAG_NO_TRANSPOSED = 0x200
+FLAG_FORCE_TRANSPOSED = 0x400
 
 # every symbol include/rnn.h declares
 SYMBOLS = ["rnn_create", "rnn_destroy", "rnn_get_sizes", "rnn_pack_weights", "rnn_fwd", "rnn_bwd_data",

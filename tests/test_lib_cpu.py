@@ -112,3 +112,31 @@ def test_backward_split_plan_invariants(lib):
                 kb = (G * H + 63) // 64
                 per = -(-kb // sp)
                 assert sp & (sp - 1) == 0 and -(-kb // per) == sp and bn % (16 * sp) == 0, (cell, H, B, bn, sp)
+
+
+def test_transposed_step_plan(lib):
+    """Recurrent steps taken as W_h h^T: chosen for many gate rows and at most
+    256 batch entries (bf16 LSTM / tanh RNN), with packing unit 1; forced or
+    refused by flags; every split count keeps the backward invariants."""
+    import re
+    d = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1).describe()
+    assert "transposed=1" in d and " u=1 " in d and "bwd_bn=256 bwd_splits=4" in d
+    d = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, flags=rnn.FLAG_NO_TRANSPOSED).describe()
+    assert "transposed=0" in d and " u=64 " in d
+    assert "transposed=0" in rnn.RNN(0, 4, 50, 257, 4096, 4096, 1).describe()   # batch wider than one tile
+    assert "transposed=0" in rnn.RNN(1, 4, 50, 256, 4096, 4096, 1).describe()   # GRU keeps h W_h^T
+    assert "transposed=0" in rnn.RNN(0, 2, 10, 64, 512, 512, 1).describe()      # too few gate rows
+    for bad in [dict(cell=1, B=9, H=256, mode=1), dict(cell=0, B=300, H=256, mode=1), dict(cell=0, B=9, H=256, mode=0)]:
+        with pytest.raises(rnn.RnnError):
+            rnn.RNN(bad["cell"], 1, 3, bad["B"], 64, bad["H"], bad["mode"], flags=rnn.FLAG_FORCE_TRANSPOSED)
+    for cell, G in ((0, 4), (2, 1)):
+        for H in (64, 128, 192, 256, 512, 1024, 4096):
+            for B in (1, 9, 64, 65, 129, 256):
+                d = rnn.RNN(cell, 1, 3, B, 64, H, 1, flags=rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING).describe()
+                assert "transposed=1" in d and " u=1 " in d
+                bn = int(re.search(r"bwd_bn=(\d+)", d).group(1))
+                sp = int(re.search(r"bwd_splits=(\d+)", d).group(1))
+                kb = (G * H + 63) // 64
+                per = -(-kb // sp)
+                assert bn >= min(256, B) and sp & (sp - 1) == 0 and -(-kb // per) == sp and bn % (16 * sp) == 0 \
+                    and sp <= 8, (cell, H, B, bn, sp)
