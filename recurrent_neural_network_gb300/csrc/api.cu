@@ -773,7 +773,8 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
                 float* dhb = reinterpret_cast<float*>(W + h->wl[l].part);
                 Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
                 Launch Lk = mk(h, s, ws, "bwd_step");
-                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_splits, dhb, nullptr, 0));
+                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, dhb, nullptr, 0, a.gates, a.c_s,
+                                 a.c_sm1));
                 pv.dh = dhb;
               }
               Launch Lp = mk(h, s, ws, "bwd_point");
@@ -798,7 +799,8 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
             Launch Lk = mk(h, s, ws, "bwd_step");
             if (h->tstep) {
               // dc0 came out of step 0's pointwise kernel
-              if (dh0) RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_splits, nullptr, a.dh0, 1));
+              if (dh0)
+                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, nullptr, a.dh0, 1));
             } else {
               RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
             }

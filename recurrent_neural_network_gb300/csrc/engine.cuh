@@ -47,6 +47,7 @@ struct TileCoord {
   int m0, n0;       // first row / column of the tile
   int mt, nt;       // tile indices
   int split, splits;
+  int part, parts;  // this thread's share of the tile's columns (epilogues with 8 warps: 2 parts)
   int* scratch;     // 8 ints of shared memory for the epilogue warps (tcgen05 only)
   // cluster split-K (tcgen05, cluster > 1): the CTA's stage buffers reused as a
   // float tile for the reduction, and two cluster-wide barriers
@@ -74,9 +75,40 @@ struct EpiStaged<E, std::void_t<typename E::Stash>> {
   using Stash = typename E::Stash;
 };
 
+// Number of epilogue warps: 4 (one per TMEM lane quadrant) unless the
+// epilogue declares kWarps = 8, in which case two warps share each quadrant
+// and split the tile's columns (TileCoord::part of TileCoord::parts).  More
+// warps hide the latency of the epilogue's dependent arithmetic and stores.
+template <class E, class = void>
+struct EpiWarps {
+  static constexpr int value = 4;
+};
+template <class E>
+struct EpiWarps<E, std::void_t<decltype(E::kWarps)>> {
+  static constexpr int value = E::kWarps;
+};
+
+// Epilogues with a tail_prefetch(const TileCoord&, int bn) member get it
+// called by the TMA producer thread of the single-CTA engine once it has
+// issued the last loads of the CTA's last tile: a few pipeline stages before
+// the MMAs finish, late enough that what it pulls into L2 is not evicted by
+// the operand stream (e.g. the inputs of the kernel that follows).
+template <class E, class = void>
+struct EpiTail {
+  static constexpr bool value = false;
+};
+template <class E>
+struct EpiTail<E, std::void_t<decltype(&E::tail_prefetch)>> {
+  static constexpr bool value = true;
+};
+
 struct TmemAcc {
   uint32_t taddr;
   __device__ __forceinline__ void load16(int col, float* v) const { tc::tmem_load16(taddr + col, v); }
+  // 32 columns of this accumulator and of `other` with a single wait
+  __device__ __forceinline__ void load32_with(const TmemAcc& other, int col, float* v, float* w) const {
+    tc::tmem_load32x2(taddr + col, other.taddr + col, v, w);
+  }
 };
 
 struct SmemAcc {
@@ -117,7 +149,7 @@ __host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>
 }  // namespace tce
 
 template <int BN, int STAGES, class Epi>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                    const GemmGeom g, const Epi epi) {
   using namespace tce;
@@ -147,10 +179,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull + a, 1);
-      tc::mbar_init(tempty + a, 4);
+      tc::mbar_init(tempty + a, EpiWarps<Epi>::value);
     }
-    tc::mbar_init(red_full, 4 * g.cluster);
-    tc::mbar_init(red_done, 4 * g.cluster);
+    tc::mbar_init(red_full, EpiWarps<Epi>::value * g.cluster);
+    tc::mbar_init(red_done, EpiWarps<Epi>::value * g.cluster);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&mapA);
@@ -239,6 +271,20 @@ __global__ void __launch_bounds__(192, 1)
             phase ^= 1;
           }
         }
+        if constexpr (EpiTail<Epi>::value) {
+          if (ok && tile + (int)gridDim.x >= g.num_tiles) {
+            TileCoord tt{};
+            tt.m0 = m0;
+            tt.n0 = n0;
+            tt.mt = mt;
+            tt.nt = nt;
+            tt.split = split;
+            tt.splits = g.splits;
+            tt.cluster = g.cluster;
+            tt.parts = 1;
+            epi.tail_prefetch(tt, BN);
+          }
+        }
       }
       if (!ok) {
         // let copies already in flight land before the CTA's shared memory goes away
@@ -299,6 +345,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int row = q * 32 + lane;
+    const int part = (warp - 2) >> 2, parts = EpiWarps<Epi>::value / 4;
     if (g.pdl) tc::pdl_wait();  // the epilogue reads and writes data of earlier kernels
     uint32_t acc = 0, aphase = 0;
     const uint32_t lane_q = static_cast<uint32_t>(q * 32) << 16;
@@ -316,6 +363,8 @@ __global__ void __launch_bounds__(192, 1)
         tp.nt = nt;
         tp.split = split;
         tp.splits = g.splits;
+        tp.part = part;
+        tp.parts = parts;
         tp.scratch = scratch;
         tp.cluster = g.cluster;
         tp.peer_base = 0;
@@ -340,6 +389,8 @@ __global__ void __launch_bounds__(192, 1)
       t.nt = nt;
       t.split = split;
       t.splits = g.splits;
+      t.part = part;
+      t.parts = parts;
       t.scratch = scratch;
       t.cluster = g.cluster;
       t.peer_base = 0;
@@ -395,7 +446,7 @@ __host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>
 }  // namespace tce2
 
 template <int BN, int STAGES, class Epi>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     tc_gemm2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const GemmGeom g, const Epi epi) {
   using namespace tce2;
@@ -434,10 +485,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull + a, 1);
-      tc::mbar_init(tempty + a, 8);
+      tc::mbar_init(tempty + a, 2 * EpiWarps<Epi>::value);
     }
-    tc::mbar_init(red_full, 4 * g.cluster);
-    tc::mbar_init(red_done, 4 * g.cluster);
+    tc::mbar_init(red_full, EpiWarps<Epi>::value * g.cluster);
+    tc::mbar_init(red_done, EpiWarps<Epi>::value * g.cluster);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&mapA);
@@ -580,6 +631,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ epilogue warps (both CTAs)
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    const int part = (warp - 2) >> 2, parts = EpiWarps<Epi>::value / 4;
     const uint32_t te_base = tc::mapa(tc::smem_addr(tempty), leader);
     if (g.pdl) tc::pdl_wait();  // the epilogue reads and writes data of earlier kernels
     uint32_t acc = 0, aphase = 0;
@@ -596,6 +648,8 @@ __global__ void __launch_bounds__(192, 1)
       t.nt = nt;
       t.split = split;
       t.splits = g.splits;
+      t.part = part;
+      t.parts = parts;
       t.scratch = scratch;
       t.cluster = g.cluster;  // > 1: the splits reduce through the cluster, pairs interleaved
       t.peer_base = pr;

@@ -477,6 +477,7 @@ __device__ __forceinline__ float pick4(float a0, float a1, float a2, float a3, i
 // run, so the epilogue proper only reads TMEM and stores.
 template <int CELL>
 struct EpiFwdStepT {
+  static constexpr int kWarps = 8;  // two warps per TMEM lane quadrant, each half of the columns
   using S = __nv_bfloat16;
   static constexpr int kAhead = 4;  // chunks of c_{t-1} loaded ahead of their use
   struct Stash {
@@ -587,9 +588,10 @@ struct EpiFwdStepT {
     const int GH = G * H;
     const int p = t.m0 + row;  // packed gate row of this lane
     const bool live = p < GH;
-    const int nmax = min(bn, B - t.n0);
+    const int cw = bn / t.parts, cb = t.part * cw;
+    const int nmax = min(cb + cw, B - t.n0);
 #pragma unroll 1
-    for (int c = 0; c < nmax; c += 16) {
+    for (int c = cb; c < nmax; c += 16) {
       float v[16], pv[16], cp[4];
       const int nb = min(16, nmax - c);
       const float* pc = P + (size_t)(t.n0 + c) * GH + p;
@@ -608,14 +610,15 @@ struct EpiFwdStepT {
     const int GH = G * H;
     const int p = t.m0 + row;
     const bool live = p < GH;
-    const int nmax = min(bn, B - t.n0);
+    const int cw = bn / t.parts, cb = t.part * cw;
+    const int nmax = min(cb + cw, B - t.n0);
     if constexpr (CELL == LSTM) {
 #pragma unroll
-      for (int a = 0; a < kAhead; ++a) load_cp(t.n0, p, live, 16 * a, nmax, st.cp[a]);
+      for (int a = 0; a < kAhead; ++a) load_cp(t.n0, p, live, cb + 16 * a, nmax, st.cp[a]);
     }
     // P, two chunks (32 loads per lane) in flight at a time
 #pragma unroll 1
-    for (int c = 0; c < nmax; c += 32) {
+    for (int c = cb; c < nmax; c += 32) {
       float v0[16], v1[16];
       const float* pc = P + (size_t)(t.n0 + c) * GH + p;
 #pragma unroll
@@ -635,25 +638,32 @@ struct EpiFwdStepT {
     constexpr int G = CellInfo<CELL>::G;
     const int p = t.m0 + row;
     const bool live = p < G * H;
-    const int nmax = min(bn, B - t.n0);
+    const int cw = bn / t.parts, cb = t.part * cw;
+    const int nmax = min(cb + cw, B - t.n0);
+    // 32 columns (two chunks) per TMEM round trip; each part is a multiple of 32 wide
 #pragma unroll 1
-    for (int c = 0; c < nmax; c += 16) {
-      float v[16], pv[16], cp[4];
-      acc.load16(c, v);
-      staged.load16(c, pv);
+    for (int c2 = cb; c2 < nmax; c2 += 32) {
+      float v2[32], pv2[32];
+      acc.load32_with(staged, c2, v2, pv2);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] += pv[i];
-      if constexpr (CELL == LSTM) {
-        // rotate the look-ahead ring and start the loads of chunk c + kAhead
+      for (int i = 0; i < 32; ++i) v2[i] += pv2[i];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cp[k] = st.cp[0][k];
+      for (int h = 0; h < 2; ++h) {
+        const int c = c2 + 16 * h;
+        if (c >= nmax) break;
+        float cp[4];
+        if constexpr (CELL == LSTM) {
+          // rotate the look-ahead ring and start the loads of chunk c + kAhead
 #pragma unroll
-        for (int a = 0; a + 1 < kAhead; ++a)
+          for (int k = 0; k < 4; ++k) cp[k] = st.cp[0][k];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) st.cp[a][k] = st.cp[a + 1][k];
-        load_cp(t.n0, p, live, c + 16 * kAhead, nmax, st.cp[kAhead - 1]);
+          for (int a = 0; a + 1 < kAhead; ++a)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) st.cp[a][k] = st.cp[a + 1][k];
+          load_cp(t.n0, p, live, c + 16 * kAhead, nmax, st.cp[kAhead - 1]);
+        }
+        finish(t.n0, p, live, c, min(16, nmax - c), v2 + 16 * h, cp);
       }
-      finish(t.n0, p, live, c, min(16, nmax - c), v, cp);
     }
   }
 };
@@ -666,6 +676,7 @@ struct EpiFwdStepT {
 // the 128 epilogue threads of a CTA can.  K splits reduce through the
 // cluster's shared memory, each CTA storing bn / splits batch columns.
 struct EpiBwdDhT {
+  static constexpr int kWarps = 8;  // two warps per TMEM lane quadrant, each half of the columns
   using S = __nv_bfloat16;
   int B, H;
   float* dh;   // [B][H] (not final)
@@ -673,8 +684,29 @@ struct EpiBwdDhT {
   int final_;
   int* err;
   uint64_t limit_ns;
+  // inputs of the pointwise kernel that follows, pulled into L2 near the end
+  // of the mainloop (null: none)
+  const float* pf_gates;  // [B][G*H]
+  const float* pf_c_s;    // [B][H]
+  const float* pf_c_sm1;  // [B][H]
+  int G;
 
   __device__ __forceinline__ void prefetch(const TileCoord&, int, int) const {}
+
+  // this CTA's (unit, batch entry) block of the pointwise inputs
+  __device__ __forceinline__ void tail_prefetch(const TileCoord& t, int bn) const {
+    if (!pf_gates || t.m0 >= H) return;
+    const int cw = t.cluster > 1 ? bn / t.cluster : bn;
+    const int b0 = t.n0 + (t.cluster > 1 ? t.split * cw : 0);
+    const int units = min(128, H - t.m0);
+    for (int i = 0; i < cw; ++i) {
+      const int b = b0 + i;
+      if (b >= B) break;
+      tc::prefetch_l2(pf_gates + (size_t)b * G * H + (size_t)G * t.m0, units * G * 4);
+      if (pf_c_s) tc::prefetch_l2(pf_c_s + (size_t)b * H + t.m0, units * 4);
+      if (pf_c_sm1) tc::prefetch_l2(pf_c_sm1 + (size_t)b * H + t.m0, units * 4);
+    }
+  }
 
   __device__ __forceinline__ void put(int j, int b, float v) const {
     const size_t bj = (size_t)b * H + j;
@@ -690,7 +722,7 @@ struct EpiBwdDhT {
       const int RS = bn + 4;
       const int lane = threadIdx.x & 31;
       float* mine = t.red + (size_t)row * RS;
-      for (int c = 0; c < bn; c += 16) {
+      for (int c = t.part * (bn / t.parts); c < (t.part + 1) * (bn / t.parts); c += 16) {
         float v[16];
         acc.load16(c, v);
         float4* d = reinterpret_cast<float4*>(mine + c);
@@ -708,24 +740,34 @@ struct EpiBwdDhT {
       if (ok && live) {
         const int cw = bn / t.cluster;
         const uint32_t mine_addr = tc::smem_addr(mine);
+        // 8 columns at a time with the loads from every peer (up to 8) in
+        // flight together
+        uint32_t peer[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) peer[p] = tc::mapa(mine_addr, t.peer_base + min(p, t.cluster - 1) * t.peer_stride);
 #pragma unroll 1
-        for (int c = t.split * cw; c < (t.split + 1) * cw; c += 16) {
+        const int pw = cw / t.parts;
+        for (int c = t.split * cw + t.part * pw; c < t.split * cw + (t.part + 1) * pw; c += 8) {
           if (t.n0 + c >= B) break;
-          float v[16];
+          float w[8][8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = 0.f;
-          for (int p = 0; p < t.cluster; ++p) {
-            const uint32_t ra = tc::mapa(mine_addr, t.peer_base + p * t.peer_stride) + c * 4;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float w[4];
-              tc::ld_dsmem4(ra + 16 * q, w);
-              v[4 * q] += w[0]; v[4 * q + 1] += w[1]; v[4 * q + 2] += w[2]; v[4 * q + 3] += w[3];
+          for (int p = 0; p < 8; ++p) {
+            if (p < t.cluster) {
+              tc::ld_dsmem4(peer[p] + c * 4, w[p]);
+              tc::ld_dsmem4(peer[p] + c * 4 + 16, w[p] + 4);
             }
           }
-          const int nb = min(16, B - (t.n0 + c));
+          float v[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
+          for (int i = 0; i < 8; ++i) {
+            v[i] = 0.f;
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+              if (p < t.cluster) v[i] += w[p][i];
+          }
+          const int nb = min(8, B - (t.n0 + c));
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
             if (i < nb) put(j, t.n0 + c + i, v[i]);
         }
       }
@@ -737,8 +779,9 @@ struct EpiBwdDhT {
       __syncwarp();
       return;
     }
-    const int nmax = min(bn, B - t.n0);
-    for (int c = 0; c < nmax; c += 16) {
+    const int pw = bn / t.parts;
+    const int nmax = min((t.part + 1) * pw, B - t.n0);
+    for (int c = t.part * pw; c < nmax; c += 16) {
       float v[16];
       acc.load16(c, v);
       const int nb = min(16, nmax - c);

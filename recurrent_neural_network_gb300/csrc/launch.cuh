@@ -137,7 +137,7 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   g.static_op = A.is_static ? 1 : B.is_static ? 2 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.cluster > 1 ? g.num_tiles : grid);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(64 + 32 * EpiWarps<Epi>::value);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
   cudaLaunchAttribute at[2];
@@ -197,7 +197,7 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   g.static_op = A.is_static ? 1 : B.is_static ? 2 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(64 + 32 * EpiWarps<Epi>::value);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
   cudaLaunchAttribute at[2];

@@ -115,8 +115,12 @@ int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const v
 // MN-major ([H] x [G*H]), B = dG_{s+1} [B][G*H]; tiles of 128 hidden units x
 // the batch, K split `splits` ways inside clusters.  Writes dh (fp32 [B][H]),
 // or dh0 (bf16 [B][H]) when final_ (dh0 null: nothing to write).
-int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int splits, float* dh,
-             void* dh0, int final_);
+// pf_*: inputs of the pointwise step that follows, pulled into L2 near the
+// end of the product's mainloop (null: none)
+// Tiles are 128 units x bn (64, 128 or 256) batch entries.
+int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int bn, int splits,
+             float* dh, void* dh0, int final_, const float* pf_gates = nullptr, const float* pf_c_s = nullptr,
+             const float* pf_c_sm1 = nullptr);
 // the pointwise backward step that follows it (packing unit 1, H % 4 == 0)
 struct PointVArgs {
   int B, H;

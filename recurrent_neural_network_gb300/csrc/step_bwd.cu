@@ -119,8 +119,8 @@ __global__ void __launch_bounds__(256) bwd_point_v_kernel(const BwdPointV<CELL> 
 }
 }  // namespace
 
-int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int splits, float* dh,
-             void* dh0, int final_) {
+int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int bn, int splits,
+             float* dh, void* dh0, int final_, const float* pf_gates, const float* pf_c_s, const float* pf_c_sm1) {
   const int M = H, N = B, K = G * H;
   EpiBwdDhT e;
   e.B = B;
@@ -130,15 +130,19 @@ int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int 
   e.final_ = final_;
   e.err = L.err;
   e.limit_ns = L.limit_ns;
+  e.pf_gates = pf_gates;
+  e.pf_c_s = pf_c_s;
+  e.pf_c_sm1 = pf_c_sm1;
+  e.G = G;
   // the K splits of a tile reduce inside a cluster (the only split-K path of
   // this epilogue): bn / splits must be a multiple of 16, at most 8 splits
-  const int bn = N > 128 ? 256 : N > 64 ? 128 : 64;
   const int kb = (K + 63) / 64, sp = std::max(1, std::min(splits, kb));
   const int eff = (kb + (kb + sp - 1) / sp - 1) / ((kb + sp - 1) / sp);
   if (eff > 1 && (eff > 8 || bn % (16 * eff))) return RNN_ERR_UNSUPPORTED;
-  if (N > 128) return launch_tc<256, 4>(L, WhT, dG, M, N, K, splits, 0, e, true);
-  if (N > 64) return launch_tc<128, 6>(L, WhT, dG, M, N, K, splits, 0, e, true);
-  return launch_tc<64, 8>(L, WhT, dG, M, N, K, splits, 0, e, true);
+  if (bn == 256) return launch_tc<256, 4>(L, WhT, dG, M, N, K, splits, 0, e, true);
+  if (bn == 128) return launch_tc<128, 6>(L, WhT, dG, M, N, K, splits, 0, e, true);
+  if (bn == 64) return launch_tc<64, 8>(L, WhT, dG, M, N, K, splits, 0, e, true);
+  return RNN_ERR_UNSUPPORTED;
 }
 
 int bwd_point_v(const Launch& L, int cell, const PointVArgs& a) {
