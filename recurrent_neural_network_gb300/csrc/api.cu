@@ -133,7 +133,7 @@ struct rnn_s {
   size_t user_w_bytes = 0, packed_bytes = 0, reserve_bytes = 0, ws_bytes = 0;
   struct PL { size_t wx, wh, bias, bias_hn; };
   struct RL { size_t gates, c, hn, hseq, dgx, dgh; };
-  struct WL { size_t P, hseq, c2, dyab, carry, part, ctr; };
+  struct WL { size_t P, hseq, c2, dyab, carry, part, ctr, dh; };
   size_t ws_bias = 0;  // bias-gradient slices (shared by the layers, used one layer at a time)
   int bias_slices = 1;
   struct UL { size_t wx, wh, bx, bh; };  // element offsets in the user weight vector
@@ -305,7 +305,10 @@ int plan_and_layout(rnn_s* h) {
     h->wl[l].c2 = take(cur, 2 * BH * 4);
     h->wl[l].dyab = take(cur, (size_t)T * BH * 4);
     h->wl[l].carry = take(cur, BH * 4);
-    h->wl[l].part = take(cur, (size_t)h->bwd_splits * BH * 4);
+    // split-K partials; the transposed product pads each split's batch rows to whole tiles
+    const size_t bp = h->tstep ? (size_t)((B + h->bwd_bn - 1) / h->bwd_bn * h->bwd_bn) : (size_t)B;
+    h->wl[l].part = take(cur, (size_t)h->bwd_splits * bp * H * 4);
+    h->wl[l].dh = h->tstep ? take(cur, BH * 4) : 0;
     h->wl[l].ctr = take(cur, (size_t)h->ctr_count * 4);
   }
   h->ws_bytes = (cur + 255) & ~size_t(255);
@@ -770,11 +773,11 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
               if (st == T - 1) {
                 pv.dh_init = dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr;
               } else {
-                float* dhb = reinterpret_cast<float*>(W + h->wl[l].part);
+                float* dhb = reinterpret_cast<float*>(W + h->wl[l].dh);
                 Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
                 Launch Lk = mk(h, s, ws, "bwd_step");
-                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, dhb, nullptr, 0, a.gates, a.c_s,
-                                 a.c_sm1));
+                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, dhb, nullptr, 0,
+                                 reinterpret_cast<float*>(W + h->wl[l].part), a.gates, a.c_s, a.c_sm1));
                 pv.dh = dhb;
               }
               Launch Lp = mk(h, s, ws, "bwd_point");
@@ -800,7 +803,8 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
             if (h->tstep) {
               // dc0 came out of step 0's pointwise kernel
               if (dh0)
-                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, nullptr, a.dh0, 1));
+                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, nullptr, a.dh0, 1,
+                                 reinterpret_cast<float*>(W + h->wl[l].part)));
             } else {
               RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
             }

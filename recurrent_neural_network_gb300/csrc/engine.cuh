@@ -57,6 +57,7 @@ struct TileCoord {
   float* red;
   uint64_t* red_full;
   uint64_t* red_done;
+  uint64_t* aux;
 };
 
 // Epilogues that declare a Stash type can stage their global inputs while the
@@ -145,13 +146,13 @@ __host__ __device__ constexpr uint32_t tmem_cols() {
   return (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
 }
 template <int BN, int STAGES>
-__host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>() + 1024 + 256; }
+__host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>() + 1024 + 512; }
 }  // namespace tce
 
 template <int BN, int STAGES, class Epi>
 __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                   const GemmGeom g, const Epi epi) {
+                   const GemmGeom g, const __grid_constant__ Epi epi) {
   using namespace tce;
   constexpr int STAGE = stage_bytes<BN>();
   constexpr uint32_t TMEM_COLS = tmem_cols<BN>();
@@ -165,7 +166,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* red_full = tempty + 2;
   uint64_t* red_done = red_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_done + 1);
+  uint64_t* aux = red_done + 1;  // one-arrival barrier the epilogue may use for its own bulk copies
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* scratch = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     }
     tc::mbar_init(red_full, EpiWarps<Epi>::value * g.cluster);
     tc::mbar_init(red_done, EpiWarps<Epi>::value * g.cluster);
+    tc::mbar_init(aux, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&mapA);
@@ -372,6 +375,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
         tp.red = reinterpret_cast<float*>(smem);
         tp.red_full = red_full;
         tp.red_done = red_done;
+        tp.aux = aux;
         epi.prefetch(tp, row, BN);
         if constexpr (EpiStaged<Epi>::value) {
           if (solo) epi.stage(tp, row, tmem_base + BN + lane_q, BN, stash);
@@ -398,6 +402,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       t.red = reinterpret_cast<float*>(smem);
       t.red_full = red_full;
       t.red_done = red_done;
+      t.aux = aux;
       TmemAcc a{tmem_base + acc * BN + lane_q};
       if constexpr (EpiStaged<Epi>::value) {
         if (solo) epi.run_staged(t, row, a, TmemAcc{tmem_base + BN + lane_q}, BN, stash);
@@ -442,13 +447,13 @@ constexpr int A_BYTES = 128 * BK * 2;
 template <int BN>
 __host__ __device__ constexpr int stage_bytes() { return A_BYTES + (BN / 2) * BK * 2; }
 template <int BN, int STAGES>
-__host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>() + 1024 + 256; }
+__host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>() + 1024 + 512; }
 }  // namespace tce2
 
 template <int BN, int STAGES, class Epi>
 __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     tc_gemm2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                    const GemmGeom g, const Epi epi) {
+                    const GemmGeom g, const __grid_constant__ Epi epi) {
   using namespace tce2;
   constexpr int STAGE = stage_bytes<BN>();
   constexpr uint32_t TMEM_COLS = tce::tmem_cols<BN>();
@@ -463,7 +468,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* red_full = tempty + 2;
   uint64_t* red_done = red_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_done + 1);
+  uint64_t* aux = red_done + 1;  // one-arrival barrier the epilogue may use for its own bulk copies
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* scratch = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -489,6 +495,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     }
     tc::mbar_init(red_full, EpiWarps<Epi>::value * g.cluster);
     tc::mbar_init(red_done, EpiWarps<Epi>::value * g.cluster);
+    tc::mbar_init(aux, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&mapA);
@@ -657,6 +664,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       t.red = reinterpret_cast<float*>(smem);
       t.red_full = red_full;
       t.red_done = red_done;
+      t.aux = aux;
       epi.prefetch(t, row, BN);
       if constexpr (EpiStaged<Epi>::value) {
         if (solo) epi.stage(t, row, tmem_base + BN + lane_q, BN, stash);

@@ -673,12 +673,20 @@ struct EpiFwdStepT {
 // above is added.  The epilogue only stores dh (fp32 [B][H]; bf16 dh0 for
 // the final product); the pointwise step runs as its own full-occupancy
 // kernel (bwd_point_v), whose wide loads keep far more bytes in flight than
-// the 128 epilogue threads of a CTA can.  K splits reduce through the
-// cluster's shared memory, each CTA storing bn / splits batch columns.
+// the epilogue threads of a CTA can.
+//
+// K splits run as one cluster per tile.  Their partial tiles meet through L2
+// with bulk tensor copies: each CTA writes its partial, transposed to
+// [batch][unit], into its (now idle) pipeline buffers, stores the slices
+// other CTAs own to the partial-sum buffer, and after a cluster barrier loads
+// the peers' partials of its own slice into the rows it just vacated, sums
+// them in a fixed order and stores its slice of dh with one more bulk copy.
 struct EpiBwdDhT {
   static constexpr int kWarps = 8;  // two warps per TMEM lane quadrant, each half of the columns
   using S = __nv_bfloat16;
-  int B, H;
+  CUtensorMap map_part;  // partials [splits * Bp][H] fp32, box 128 units x (bn / splits) rows
+  CUtensorMap map_dh;    // dh [B][H] fp32, same box
+  int B, H, Bp;          // Bp: batch rows per split in the partial buffer (a multiple of bn)
   float* dh;   // [B][H] (not final)
   S* dh0;      // [B][H] (final)
   int final_;
@@ -718,65 +726,93 @@ struct EpiBwdDhT {
   __device__ __forceinline__ void operator()(const TileCoord& t, int row, const Acc& acc, int bn) const {
     const int j = t.m0 + row;
     const bool live = j < H && (!final_ || dh0);
+    const int lane = threadIdx.x & 31;
     if (t.cluster > 1) {
-      const int RS = bn + 4;
-      const int lane = threadIdx.x & 31;
-      float* mine = t.red + (size_t)row * RS;
+      constexpr int EWT = kWarps * 32;
+      const bool leader = threadIdx.x == 64;  // first epilogue thread
+      const int cw = bn / t.cluster;
+      float* tile = t.red;  // [bn][128]: tile[b * 128 + row]
+      // 1. partial tile -> shared memory as [batch][unit]
       for (int c = t.part * (bn / t.parts); c < (t.part + 1) * (bn / t.parts); c += 16) {
         float v[16];
         acc.load16(c, v);
-        float4* d = reinterpret_cast<float4*>(mine + c);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int i = 0; i < 16; ++i) tile[(c + i) * 128 + row] = v[i];
       }
-      tc::fence_acq_rel_cluster();
+      tc::fence_proxy_async_smem();
+      tc::named_bar(1, EWT);
+      // 2. the slices other CTAs own go to the partial buffer (rows split*Bp + batch)
+      if (leader) {
+        for (int o = 0; o < t.cluster; ++o)
+          if (o != t.split) tc::tma_store_2d(&map_part, tile + (size_t)o * cw * 128, t.m0, t.split * Bp + t.n0 + o * cw);
+        tc::bulk_commit();
+        tc::bulk_wait_all();
+        tc::fence_proxy_async_global();
+      }
+      tc::named_bar(1, EWT);
+      const uint32_t full_local = tc::smem_addr(t.red_full);
       __syncwarp();
-      const uint32_t full_local = tc::smem_addr(t.red_full), done_local = tc::smem_addr(t.red_done);
       if (lane == 0)
         for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(full_local, t.peer_base + p * t.peer_stride));
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait_cluster(t.red_full, 0, err, limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok && live) {
-        const int cw = bn / t.cluster;
-        const uint32_t mine_addr = tc::smem_addr(mine);
-        // 8 columns at a time with the loads from every peer (up to 8) in
-        // flight together
-        uint32_t peer[8];
-#pragma unroll
-        for (int p = 0; p < 8; ++p) peer[p] = tc::mapa(mine_addr, t.peer_base + min(p, t.cluster - 1) * t.peer_stride);
+      // 3. the peers' partials of this CTA's slice, into the rows they vacated
+      if (leader && ok) {
+        tc::fence_proxy_async_global();
+        tc::mbar_arrive_expect_tx(t.aux, (uint32_t)((t.cluster - 1) * cw * 128 * 4));
+        for (int sp = 0; sp < t.cluster; ++sp)
+          if (sp != t.split)
+            tc::tma_load_2d(tile + (size_t)sp * cw * 128, &map_part, t.aux, t.m0, sp * Bp + t.n0 + t.split * cw);
+      }
+      if (lane == 0 && ok) ok = tc::mbar_wait_cluster(t.aux, 0, err, limit_ns) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // 4. own slice = own partial + peers' partials in split order; dh by one bulk store
+      if (ok) {
+        // 8 rows at a time, every partial's loads issued before the adds
+        const int pw = cw / t.parts;  // a multiple of 8
+        const int r0 = t.split * cw + t.part * pw;
 #pragma unroll 1
-        const int pw = cw / t.parts;
-        for (int c = t.split * cw + t.part * pw; c < t.split * cw + (t.part + 1) * pw; c += 8) {
-          if (t.n0 + c >= B) break;
-          float w[8][8];
-#pragma unroll
-          for (int p = 0; p < 8; ++p) {
-            if (p < t.cluster) {
-              tc::ld_dsmem4(peer[p] + c * 4, w[p]);
-              tc::ld_dsmem4(peer[p] + c * 4 + 16, w[p] + 4);
-            }
-          }
+        for (int r = r0; r < r0 + pw; r += 8) {
           float v[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            v[i] = 0.f;
+          for (int i = 0; i < 8; ++i) v[i] = 0.f;
 #pragma unroll
-            for (int p = 0; p < 8; ++p)
-              if (p < t.cluster) v[i] += w[p][i];
+          for (int sp = 0; sp < 8; ++sp) {
+            if (sp < t.cluster) {
+              const float* src = tile + (size_t)(sp == t.split ? r : sp * cw + (r - t.split * cw)) * 128 + row;
+              float w[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w[i] = src[i * 128];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] += w[i];
+            }
           }
-          const int nb = min(8, B - (t.n0 + c));
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i < nb) put(j, t.n0 + c + i, v[i]);
+          for (int i = 0; i < 8; ++i) {
+            if (final_) {
+              if (live && t.n0 + r + i < B) put(j, t.n0 + r + i, v[i]);
+            } else {
+              tile[(size_t)(r + i) * 128 + row] = v[i];
+            }
+          }
         }
       }
-      tc::fence_acq_rel_cluster();
-      __syncwarp();
-      if (lane == 0)
-        for (int p = 0; p < t.cluster; ++p) tc::mbar_arrive_remote(tc::mapa(done_local, t.peer_base + p * t.peer_stride));
-      if (lane == 0) tc::mbar_wait_cluster(t.red_done, 0, err, limit_ns);
-      __syncwarp();
+      if (!final_) {
+        tc::fence_proxy_async_smem();
+        tc::named_bar(1, EWT);
+        if (leader && ok) {
+          tc::tma_store_2d(&map_dh, tile + (size_t)t.split * cw * 128, t.m0, t.n0 + t.split * cw);
+          tc::bulk_commit();
+          tc::bulk_wait_read_all();
+        }
+      }
+      if (!ok && leader) {
+        // a load may still be landing in this CTA's buffers: let it (bounded)
+        const uint64_t t0 = globaltimer_ns();
+        while (!tc::mbar_try_wait(t.aux, 0) && globaltimer_ns() - t0 < 1000000ull) {
+        }
+      }
       return;
     }
     const int pw = bn / t.parts;

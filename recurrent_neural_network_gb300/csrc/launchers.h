@@ -117,10 +117,11 @@ int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const v
 // or dh0 (bf16 [B][H]) when final_ (dh0 null: nothing to write).
 // pf_*: inputs of the pointwise step that follows, pulled into L2 near the
 // end of the product's mainloop (null: none)
-// Tiles are 128 units x bn (64, 128 or 256) batch entries.
+// Tiles are 128 units x bn (64, 128 or 256) batch entries; with splits > 1
+// the partial sums pass through `part` (fp32, splits * ceil(B/bn)*bn * H).
 int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int bn, int splits,
-             float* dh, void* dh0, int final_, const float* pf_gates = nullptr, const float* pf_c_s = nullptr,
-             const float* pf_c_sm1 = nullptr);
+             float* dh, void* dh0, int final_, float* part, const float* pf_gates = nullptr,
+             const float* pf_c_s = nullptr, const float* pf_c_sm1 = nullptr);
 // the pointwise backward step that follows it (packing unit 1, H % 4 == 0)
 struct PointVArgs {
   int B, H;
