@@ -483,6 +483,13 @@ struct EpiFwdStepT {
   struct Stash {
     float cp[kAhead][4];  // LSTM c_{t-1} of the next kAhead chunks
   };
+  static constexpr int kUnits = 128 / CellInfo<CELL>::G;  // hidden units of a 128-row tile
+  // Bulk-store maps of the single-tile path (tma_out): the epilogue writes
+  // gates, c and h as [batch][row] tiles into its idle pipeline buffers and
+  // stores each with one bulk tensor copy (boxes of 128 gate rows or kUnits
+  // units x bn batch entries).
+  CUtensorMap map_p, map_c, map_h, map_y, map_hT, map_cT;
+  int tma_out;
   int B, H;
   float* P;          // [B][G*H] this step: input projection incl. bias; activated gates written back if write_gates
   int write_gates;
@@ -516,8 +523,12 @@ struct EpiFwdStepT {
     }
   }
 
-  // v: pre-activations (P included) of gate row p for batch entries c..c+15
-  __device__ __forceinline__ void finish(int n0, int p, bool live, int c, int nb, float* v, const float* cp) const {
+  // v: pre-activations (P included) of gate row p for batch entries c..c+15.
+  // With sm_g non-null the outputs go to the shared-memory tiles sm_g
+  // ([bn][128] gates), sm_c / sm_h ([bn][kUnits]) at tile row `row`.
+  __device__ __forceinline__ void finish(int n0, int p, bool live, int c, int nb, float* v, const float* cp,
+                                         int row = 0, float* sm_g = nullptr, float* sm_c = nullptr,
+                                         S* sm_h = nullptr) const {
     constexpr int G = CellInfo<CELL>::G;
     const int GH = G * H;
     float* pc = P + (size_t)(n0 + c) * GH + p;
@@ -530,7 +541,10 @@ struct EpiFwdStepT {
         const float th = tanh_hw(sc * v[i]);
         v[i] = g == 2 ? th : fmaf(0.5f, th, 0.5f);
       }
-      if (write_gates && live) {
+      if (sm_g) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sm_g[(c + i) * 128 + row] = v[i];
+      } else if (write_gates && live) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           if (i < nb) pc[(size_t)i * GH] = v[i];
@@ -553,13 +567,18 @@ struct EpiFwdStepT {
           gt[3] = src == 3 ? got : gt[3];
         }
         const int bi = 4 * k + g;
-        if (!live || bi >= nb) continue;
-        const size_t bj = (size_t)(n0 + c + bi) * H + j;
         const float cn = gt[1] * cp[k] + gt[0] * gt[2];
         const float hn = gt[3] * tanh_hw(cn);
+        const S hb = __float2bfloat16_rn(hn);
+        if (sm_c) {
+          sm_c[(c + bi) * kUnits + (row >> 2)] = cn;
+          sm_h[(c + bi) * kUnits + (row >> 2)] = hb;
+          continue;
+        }
+        if (!live || bi >= nb) continue;
+        const size_t bj = (size_t)(n0 + c + bi) * H + j;
         c_out[bj] = cn;
         if (cT) cT[bj] = cn;
-        const S hb = __float2bfloat16_rn(hn);
         h_out[bj] = hb;
         if (y) y[bj] = hb;
         if (hT) hT[bj] = hb;
@@ -567,7 +586,13 @@ struct EpiFwdStepT {
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = tanh_hw(v[i]);
-      if (live) {
+      if (sm_g) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          sm_g[(c + i) * 128 + row] = v[i];
+          sm_h[(c + i) * kUnits + row] = __float2bfloat16_rn(v[i]);
+        }
+      } else if (live) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (i >= nb) continue;
@@ -640,6 +665,10 @@ struct EpiFwdStepT {
     const bool live = p < G * H;
     const int cw = bn / t.parts, cb = t.part * cw;
     const int nmax = min(cb + cw, B - t.n0);
+    // output tiles in the pipeline buffers (free once the tile's MMAs are done)
+    float* sm_g = t.red;
+    float* sm_c = sm_g + (size_t)bn * 128;
+    S* sm_h = reinterpret_cast<S*>(sm_c + (CELL == LSTM ? (size_t)bn * kUnits : 0));
     // 32 columns (two chunks) per TMEM round trip; each part is a multiple of 32 wide
 #pragma unroll 1
     for (int c2 = cb; c2 < nmax; c2 += 32) {
@@ -662,7 +691,28 @@ struct EpiFwdStepT {
             for (int k = 0; k < 4; ++k) st.cp[a][k] = st.cp[a + 1][k];
           load_cp(t.n0, p, live, c + 16 * kAhead, nmax, st.cp[kAhead - 1]);
         }
-        finish(t.n0, p, live, c, min(16, nmax - c), v2 + 16 * h, cp);
+        if (tma_out)
+          finish(t.n0, p, live, c, min(16, nmax - c), v2 + 16 * h, cp, row, sm_g, sm_c, sm_h);
+        else
+          finish(t.n0, p, live, c, min(16, nmax - c), v2 + 16 * h, cp);
+      }
+    }
+    if (tma_out) {
+      // every epilogue thread's tile writes, then one thread's bulk stores
+      tc::fence_proxy_async_smem();
+      tc::named_bar(1, kWarps * 32);
+      if (threadIdx.x == 64) {
+        const int cx = CELL == LSTM ? t.m0 / 4 : t.m0;
+        if (write_gates) tc::tma_store_2d(&map_p, sm_g, t.m0, t.n0);
+        if (CELL == LSTM) {
+          tc::tma_store_2d(&map_c, sm_c, cx, t.n0);
+          if (cT) tc::tma_store_2d(&map_cT, sm_c, cx, t.n0);
+        }
+        tc::tma_store_2d(&map_h, sm_h, cx, t.n0);
+        if (y) tc::tma_store_2d(&map_y, sm_h, cx, t.n0);
+        if (hT) tc::tma_store_2d(&map_hT, sm_h, cx, t.n0);
+        tc::bulk_commit();
+        tc::bulk_wait_read_all();
       }
     }
   }

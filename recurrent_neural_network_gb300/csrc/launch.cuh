@@ -54,6 +54,23 @@ inline int encode_operand(CUtensorMap* map, const Operand& op, int box_rows) {
   return r == CUDA_SUCCESS ? RNN_OK : RNN_ERR_INVALID_ARG;
 }
 
+// 2-D tensor map without swizzle over a row-major rows x cols array of
+// fp32 (elem 4) or bf16 (elem 2) with row pitch ld elements; box box_cols x
+// box_rows.  Used for the bulk stores and loads of epilogues.
+inline int encode_plain(CUtensorMap* map, const void* ptr, int elem, long long rows, long long cols, long long ld,
+                        int box_cols, int box_rows) {
+  auto enc = tmap_encoder();
+  if (!enc) return RNN_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || ((ld * elem) & 15) || ((box_cols * elem) & 15))
+    return RNN_ERR_INVALID_ARG;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows}, strides[1] = {(cuuint64_t)(ld * elem)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows}, es[2] = {1, 1};
+  CUresult r = enc(map, elem == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RNN_OK : RNN_ERR_INVALID_ARG;
+}
+
 inline int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return RNN_OK;
   if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorLaunchOutOfResources) return RNN_ERR_LAUNCH;

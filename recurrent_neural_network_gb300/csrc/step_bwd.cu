@@ -121,21 +121,6 @@ __global__ void __launch_bounds__(256) bwd_point_v_kernel(const BwdPointV<CELL> 
 }
 }  // namespace
 
-namespace {
-// 2-D fp32 tensor map without swizzle: rows x cols, row pitch ld floats, box box_cols x box_rows
-int encode_f32(CUtensorMap* map, const float* ptr, long long rows, long long cols, long long ld, int box_cols,
-               int box_rows) {
-  auto enc = tmap_encoder();
-  if (!enc) return RNN_ERR_CUDA;
-  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || ((ld * 4) & 15)) return RNN_ERR_INVALID_ARG;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows}, strides[1] = {(cuuint64_t)ld * 4};
-  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows}, es[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? RNN_OK : RNN_ERR_INVALID_ARG;
-}
-}  // namespace
 
 int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int bn, int splits,
              float* dh, void* dh0, int final_, float* part, const float* pf_gates, const float* pf_c_s,
@@ -164,10 +149,10 @@ int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int 
   e.Bp = (B + bn - 1) / bn * bn;
   if (eff > 1) {
     if (!part) return RNN_ERR_INVALID_ARG;
-    int rc = encode_f32(&e.map_part, part, (long long)eff * e.Bp, H, H, 128, bn / eff);
+    int rc = encode_plain(&e.map_part, part, 4, (long long)eff * e.Bp, H, H, 128, bn / eff);
     if (rc) return rc;
     if (!final_) {
-      rc = encode_f32(&e.map_dh, dh, B, H, H, 128, bn / eff);
+      rc = encode_plain(&e.map_dh, dh, 4, B, H, H, 128, bn / eff);
       if (rc) return rc;
     }
   }

@@ -6,6 +6,8 @@
 // section "제안 방법"): grouped gate matrices make each step one larger
 // product; "Persistent RNNs" (citing snippet "pointwise OPs are very cheap")
 // motivates keeping the pointwise work inside the product's epilogue.
+#include <cstring>
+
 #include "epilogues.cuh"
 #include "launch.cuh"
 
@@ -67,9 +69,10 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
 
 namespace {
 template <int CELL>
-EpiFwdStepT<CELL> make_epi_t(const FwdStepArgs& a) {
+EpiFwdStepT<CELL> make_epi_t(const FwdStepArgs& a, int bn) {
   using S = __nv_bfloat16;
   EpiFwdStepT<CELL> e;
+  std::memset(&e, 0, sizeof(e));
   e.B = a.B;
   e.H = a.H;
   e.P = a.P;
@@ -80,6 +83,15 @@ EpiFwdStepT<CELL> make_epi_t(const FwdStepArgs& a) {
   e.y = static_cast<S*>(a.y);
   e.hT = static_cast<S*>(a.hT);
   e.cT = a.cT;
+  // bulk-store maps for the single-tile path; any failure keeps plain stores
+  const int G = CellInfo<CELL>::G, ku = EpiFwdStepT<CELL>::kUnits;
+  int rc = encode_plain(&e.map_p, a.P, 4, a.B, (long long)G * a.H, (long long)G * a.H, 128, bn);
+  if (!rc && CELL == LSTM) rc = encode_plain(&e.map_c, a.c_out, 4, a.B, a.H, a.H, ku, bn);
+  if (!rc && CELL == LSTM && a.cT) rc = encode_plain(&e.map_cT, a.cT, 4, a.B, a.H, a.H, ku, bn);
+  if (!rc) rc = encode_plain(&e.map_h, a.h_out, 2, a.B, a.H, a.H, ku, bn);
+  if (!rc && a.y) rc = encode_plain(&e.map_y, a.y, 2, a.B, a.H, a.H, ku, bn);
+  if (!rc && a.hT) rc = encode_plain(&e.map_hT, a.hT, 2, a.B, a.H, a.H, ku, bn);
+  e.tma_out = rc == RNN_OK ? 1 : 0;
   return e;
 }
 }  // namespace
@@ -90,15 +102,15 @@ int fwd_step_t(const Launch& L, int cell, const Operand& Wh, const Operand& Hp, 
   const int M = G * a.H, N = a.B, K = a.H;
   // one n-tile holds the whole batch (up to 256 entries): W_h streams once per step
   if (N > 128) {
-    if (cell == LSTM) return launch_tc2<256, 6>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a));
-    return launch_tc2<256, 6>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a));
+    if (cell == LSTM) return launch_tc2<256, 6>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, 256));
+    return launch_tc2<256, 6>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a, 256));
   }
   if (N > 64) {
-    if (cell == LSTM) return launch_tc2<128, 8>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a));
-    return launch_tc2<128, 8>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a));
+    if (cell == LSTM) return launch_tc2<128, 8>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, 128));
+    return launch_tc2<128, 8>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a, 128));
   }
-  if (cell == LSTM) return launch_tc2<64, 10>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a));
-  return launch_tc2<64, 10>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a));
+  if (cell == LSTM) return launch_tc2<64, 10>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, 64));
+  return launch_tc2<64, 10>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a, 64));
 }
 
 }  // namespace rnn
