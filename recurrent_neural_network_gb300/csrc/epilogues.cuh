@@ -486,8 +486,8 @@ struct EpiFwdStepT {
   static constexpr int kUnits = 128 / CellInfo<CELL>::G;  // hidden units of a 128-row tile
   // Bulk-store maps of the single-tile path (tma_out): the epilogue writes
   // gates, c and h as [batch][row] tiles into its idle pipeline buffers and
-  // stores each with one bulk tensor copy (boxes of 128 gate rows or kUnits
-  // units x bn batch entries).
+  // stores every 32 finished batch rows with bulk tensor copies (boxes of 128
+  // gate rows or kUnits units x 32 batch entries) while it computes the next.
   CUtensorMap map_p, map_c, map_h, map_y, map_hT, map_cT;
   int tma_out;
   int B, H;
@@ -696,25 +696,27 @@ struct EpiFwdStepT {
         else
           finish(t.n0, p, live, c, min(16, nmax - c), v2 + 16 * h, cp);
       }
-    }
-    if (tma_out) {
-      // every epilogue thread's tile writes, then one thread's bulk stores
-      tc::fence_proxy_async_smem();
-      tc::named_bar(1, kWarps * 32);
-      if (threadIdx.x == 64) {
-        const int cx = CELL == LSTM ? t.m0 / 4 : t.m0;
-        if (write_gates) tc::tma_store_2d(&map_p, sm_g, t.m0, t.n0);
-        if (CELL == LSTM) {
-          tc::tma_store_2d(&map_c, sm_c, cx, t.n0);
-          if (cT) tc::tma_store_2d(&map_cT, sm_c, cx, t.n0);
+      if (tma_out) {
+        // this part's 32 batch rows are complete: its first thread stores
+        // them while the part goes on with the next rows
+        tc::fence_proxy_async_smem();
+        tc::named_bar(2 + t.part, 128);
+        if (threadIdx.x == 64 + 128 * t.part) {
+          const int cx = CELL == LSTM ? t.m0 / 4 : t.m0, y0 = t.n0 + c2;
+          if (write_gates) tc::tma_store_2d(&map_p, sm_g + (size_t)c2 * 128, t.m0, y0);
+          if (CELL == LSTM) {
+            tc::tma_store_2d(&map_c, sm_c + (size_t)c2 * kUnits, cx, y0);
+            if (cT) tc::tma_store_2d(&map_cT, sm_c + (size_t)c2 * kUnits, cx, y0);
+          }
+          tc::tma_store_2d(&map_h, sm_h + (size_t)c2 * kUnits, cx, y0);
+          if (y) tc::tma_store_2d(&map_y, sm_h + (size_t)c2 * kUnits, cx, y0);
+          if (hT) tc::tma_store_2d(&map_hT, sm_h + (size_t)c2 * kUnits, cx, y0);
+          tc::bulk_commit();
         }
-        tc::tma_store_2d(&map_h, sm_h, cx, t.n0);
-        if (y) tc::tma_store_2d(&map_y, sm_h, cx, t.n0);
-        if (hT) tc::tma_store_2d(&map_hT, sm_h, cx, t.n0);
-        tc::bulk_commit();
-        tc::bulk_wait_read_all();
       }
     }
+    // the shared-memory tiles must outlive the stores' reads
+    if (tma_out && threadIdx.x == 64 + 128 * t.part) tc::bulk_wait_read_all();
   }
 };
 

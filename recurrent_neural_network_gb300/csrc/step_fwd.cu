@@ -85,12 +85,14 @@ EpiFwdStepT<CELL> make_epi_t(const FwdStepArgs& a, int bn) {
   e.cT = a.cT;
   // bulk-store maps for the single-tile path; any failure keeps plain stores
   const int G = CellInfo<CELL>::G, ku = EpiFwdStepT<CELL>::kUnits;
-  int rc = encode_plain(&e.map_p, a.P, 4, a.B, (long long)G * a.H, (long long)G * a.H, 128, bn);
-  if (!rc && CELL == LSTM) rc = encode_plain(&e.map_c, a.c_out, 4, a.B, a.H, a.H, ku, bn);
-  if (!rc && CELL == LSTM && a.cT) rc = encode_plain(&e.map_cT, a.cT, 4, a.B, a.H, a.H, ku, bn);
-  if (!rc) rc = encode_plain(&e.map_h, a.h_out, 2, a.B, a.H, a.H, ku, bn);
-  if (!rc && a.y) rc = encode_plain(&e.map_y, a.y, 2, a.B, a.H, a.H, ku, bn);
-  if (!rc && a.hT) rc = encode_plain(&e.map_hT, a.hT, 2, a.B, a.H, a.H, ku, bn);
+  constexpr int rows = 32;  // batch rows per bulk store
+  (void)bn;
+  int rc = encode_plain(&e.map_p, a.P, 4, a.B, (long long)G * a.H, (long long)G * a.H, 128, rows);
+  if (!rc && CELL == LSTM) rc = encode_plain(&e.map_c, a.c_out, 4, a.B, a.H, a.H, ku, rows);
+  if (!rc && CELL == LSTM && a.cT) rc = encode_plain(&e.map_cT, a.cT, 4, a.B, a.H, a.H, ku, rows);
+  if (!rc) rc = encode_plain(&e.map_h, a.h_out, 2, a.B, a.H, a.H, ku, rows);
+  if (!rc && a.y) rc = encode_plain(&e.map_y, a.y, 2, a.B, a.H, a.H, ku, rows);
+  if (!rc && a.hT) rc = encode_plain(&e.map_hT, a.hT, 2, a.B, a.H, a.H, ku, rows);
   e.tma_out = rc == RNN_OK ? 1 : 0;
   return e;
 }
