@@ -122,28 +122,39 @@ def class_flops(wl):
     return out
 
 
-def class_bytes(wl):
+def class_bytes(wl, transposed):
     """Algorithmic HBM bytes per step of the recurrent-step classes: every
     timestep reads W_h once plus the state it updates (bf16 storage, f32 gates,
-    cell state and gate pre-activations)."""
+    cell state and gate pre-activations).  With transposed steps the BPTT
+    product only writes dh and a pointwise kernel (bwd_point) does the rest."""
     G, H, T, B, L = wl.G, wl.hidden, wl.T, wl.B, wl.layers
     e = 2 if wl.mode == 1 else 4
     wh = G * H * H * e
     # forward: h_{t-1} + P (read) ; gates (write) ; c_{t-1}/c_t ; h_t, y
     fwd = wh + B * H * e + B * G * H * 4 * 2 + B * H * 4 * 2 + B * H * e * 2
-    # backward: dG_{t+1} + gates + c_t, c_{t-1} + dy + carry (read) ; dG_t + carry (write)
-    bwd = wh + B * G * H * e + B * G * H * 4 + B * H * 4 * 2 + B * H * 4 * 2 + B * G * H * e + B * H * 4
     out = {"fwd_step": fwd * T * L}
-    if wl.training:
-        out["bwd_step"] = bwd * T * L
+    if not wl.training:
+        return out
+    if transposed:
+        # product: W_h + dG_{s+1} (read) ; dh (write)
+        out["bwd_step"] = (wh + B * G * H * e + B * H * 4) * T * L
+        # pointwise: dh, dy, gates, c_s, c_{s-1}, carry (read) ; dG_s, carry (write)
+        out["bwd_point"] = (B * H * 4 + B * H * 4 + B * G * H * 4 + B * H * 4 * 2 + B * H * 4 * 2 + B * G * H * e) * T * L
+    else:
+        # fused: dG_{t+1} + gates + c_t, c_{t-1} + dy + carry (read) ; dG_t + carry (write)
+        out["bwd_step"] = (wh + B * G * H * e + B * G * H * 4 + B * H * 4 * 2 + B * H * 4 * 2 + B * G * H * e
+                           + B * H * 4) * T * L
     return out
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the same kernel build on a one-layer T=2 case with the same
-# per-step shape; summarised in profiles/ncu_step_kernels_lstm_B256_H4096.md.
-NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 206.72e6,
-               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 179.34e6}
+# per-step shape (transposed steps); summarised in
+# profiles/ncu_step_kernels_lstm_B256_H4096.md.  The BPTT product's figure
+# includes the pointwise inputs it pulls into L2 for the kernel after it.
+NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 171.03e6,
+               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.90e6,
+               ("lstm_bf16_L4_T50_B256_H4096", "bwd_point"): 35.68e6}
 
 
 def time_oracle_sample(wl, budget_s=20.0):
@@ -216,12 +227,12 @@ def e2e_run(R, wl, steps, sdt, stream, barrier):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
-def roofline(prof, wl, steps, pk):
+def roofline(prof, wl, steps, pk, transposed):
     """Roofline of the dominant kernel class (largest device time): its
     algorithmic flops and bytes per launch over its average CUDA-event launch
     duration, against the tensor or the HBM peak, whichever its arithmetic
     intensity makes binding."""
-    cf, cb = class_flops(wl), class_bytes(wl)
+    cf, cb = class_flops(wl), class_bytes(wl, transposed)
     cand = [(k, v) for k, v in prof.items() if k in cf and v[0] > 0]
     if not cand:
         return None
@@ -404,7 +415,7 @@ def main():
     del R
     torch.cuda.empty_cache()
     prof, psteps = kernel_profile(wl, dev, args, sdt)
-    roof = roofline(prof, wl, psteps, pk)
+    roof = roofline(prof, wl, psteps, pk, "transposed=1" in plan)
     persistent = persistent_probe(dev) if (world == 1 and args.config != 2 and not args.no_persistent) else None
 
     if rank != 0:
