@@ -91,6 +91,8 @@ enum {
 #define RNN_FLAG_FORCE_TRANSPOSED 0x400u /* take the recurrent steps as W_h h^T (bf16 LSTM / tanh RNN,
                                             B <= 256, H % 32 == 0) or fail; by default chosen when
                                             G*H >= 12288 */
+#define RNN_FLAG_NO_FUSED_POINT 0x800u  /* transposed LSTM steps: run the pointwise BPTT step as its own
+                                           kernel after each product instead of inside its epilogue */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */

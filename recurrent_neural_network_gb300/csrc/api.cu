@@ -128,6 +128,7 @@ struct rnn_s {
   int persist = 0, persist_ctas = 0;  // forward recurrence kind: 1 = persistent (one launch per layer)
   int fwd_mcast = 4;  // forward-step clusters along N sharing h_{t-1} by TMA multicast
   int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
+  int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
   uint64_t limit_ns = 2000000000ull;
   // sizes (bytes)
   size_t user_w_bytes = 0, packed_bytes = 0, reserve_bytes = 0, ws_bytes = 0;
@@ -235,6 +236,7 @@ int plan_and_layout(rnn_s* h) {
       s *= 2;
     h->bwd_splits = s;
     h->ctr_count = tiles;
+    h->bwd_fuse = (d.cell == RNN_LSTM && h->bwd_bn == 256 && s == 4 && !(d.flags & RNN_FLAG_NO_FUSED_POINT)) ? 1 : 0;
   } else if (d.mode == RNN_MODE_BF16) {
     // backward step tiles: 128-row batch tiles x bn hidden units, split over K
     // until the step covers the SMs (at most 8 ways, at least 4 K blocks each)
@@ -546,10 +548,10 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : "tanh";
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
-           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d transposed=%d",
+           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d transposed=%d fused_point=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
            h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch,
-           h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms, h->tstep);
+           h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms, h->tstep, h->bwd_fuse);
   return RNN_OK;
 }
 
@@ -777,7 +779,9 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
                 Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
                 Launch Lk = mk(h, s, ws, "bwd_step");
                 RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, dhb, nullptr, 0,
-                                 reinterpret_cast<float*>(W + h->wl[l].part), a.gates, a.c_s, a.c_sm1));
+                                 reinterpret_cast<float*>(W + h->wl[l].part), a.gates, a.c_s, a.c_sm1,
+                                 h->bwd_fuse ? &pv : nullptr));
+                if (h->bwd_fuse) continue;  // the product ran the pointwise step too
                 pv.dh = dhb;
               }
               Launch Lp = mk(h, s, ws, "bwd_point");

@@ -57,7 +57,7 @@ struct TileCoord {
   float* red;
   uint64_t* red_full;
   uint64_t* red_done;
-  uint64_t* aux;
+  uint64_t* aux;  // [3]
 };
 
 // Epilogues that declare a Stash type can stage their global inputs while the
@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* red_full = tempty + 2;
   uint64_t* red_done = red_full + 1;
-  uint64_t* aux = red_done + 1;  // one-arrival barrier the epilogue may use for its own bulk copies
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 1);
+  uint64_t* aux = red_done + 1;  // three one-arrival barriers the epilogue may use for its own bulk copies
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* scratch = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     }
     tc::mbar_init(red_full, EpiWarps<Epi>::value * g.cluster);
     tc::mbar_init(red_done, EpiWarps<Epi>::value * g.cluster);
-    tc::mbar_init(aux, 1);
+    for (int a = 0; a < 3; ++a) tc::mbar_init(aux + a, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&mapA);
@@ -468,8 +468,8 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* red_full = tempty + 2;
   uint64_t* red_done = red_full + 1;
-  uint64_t* aux = red_done + 1;  // one-arrival barrier the epilogue may use for its own bulk copies
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 1);
+  uint64_t* aux = red_done + 1;  // three one-arrival barriers the epilogue may use for its own bulk copies
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* scratch = reinterpret_cast<int*>(tmem_slot + 2);
 
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     }
     tc::mbar_init(red_full, EpiWarps<Epi>::value * g.cluster);
     tc::mbar_init(red_done, EpiWarps<Epi>::value * g.cluster);
-    tc::mbar_init(aux, 1);
+    for (int a = 0; a < 3; ++a) tc::mbar_init(aux + a, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::tma_prefetch_desc(&mapA);

@@ -738,6 +738,18 @@ struct EpiBwdDhT {
   using S = __nv_bfloat16;
   CUtensorMap map_part;  // partials [splits * Bp][H] fp32, box 128 units x (bn / splits) rows
   CUtensorMap map_dh;    // dh [B][H] fp32, same box
+  // Fused LSTM pointwise step (fuse = 1; bn = 256 in clusters of 4): each CTA
+  // runs it on its own 64-entry slice of dh while that is still in shared
+  // memory, its inputs arriving by bulk loads of 16 batch rows at a time.
+  CUtensorMap map_g;     // gates [B][4H] fp32, box 256 x 16 (64 units' four gates)
+  CUtensorMap map_cs;    // c_s [B][H] fp32, box 128 x 16
+  CUtensorMap map_cp;    // c_{s-1}, same (has_cp)
+  CUtensorMap map_dc;    // carry, same
+  CUtensorMap map_dy;    // dy [B][H] fp32 or bf16, box 128 x 16 (has_dy)
+  int fuse, has_cp, has_dy, dy_f32;
+  float* carry;          // [B][H] dc into step s (in) / into s-1 (out)
+  float* dc0;            // [B][H] copy of the outgoing carry (s = 0), or null
+  S* dGx;                // [B][4H]
   int B, H, Bp;          // Bp: batch rows per split in the partial buffer (a multiple of bn)
   float* dh;   // [B][H] (not final)
   S* dh0;      // [B][H] (final)
@@ -768,6 +780,54 @@ struct EpiBwdDhT {
     }
   }
 
+  // Shared-memory home of one 16-row quarter of the pointwise inputs.
+  struct Quarter {
+    float* g;   // [2][16][256]: gates of units 0-63, then 64-127 (the two bulk boxes)
+    float* cs;  // [16][128]
+    float* cp;
+    float* dc;
+    void* dy;   // [16][128] fp32 or bf16
+  };
+  __device__ __forceinline__ uint32_t quarter_bytes() const {
+    return 32768u + 8192u * (2u + (has_cp ? 1u : 0u)) + (has_dy ? (dy_f32 ? 8192u : 4096u) : 0u);
+  }
+  __device__ __forceinline__ void load_quarter(const Quarter& qd, uint64_t* bar, int m0, int b) const {
+    tc::mbar_arrive_expect_tx(bar, quarter_bytes());
+    tc::tma_load_2d(qd.g, &map_g, bar, 4 * m0, b);
+    tc::tma_load_2d(qd.g + 16 * 256, &map_g, bar, 4 * m0 + 256, b);
+    tc::tma_load_2d(qd.cs, &map_cs, bar, m0, b);
+    if (has_cp) tc::tma_load_2d(qd.cp, &map_cp, bar, m0, b);
+    tc::tma_load_2d(qd.dc, &map_dc, bar, m0, b);
+    if (has_dy) tc::tma_load_2d(qd.dy, &map_dy, bar, m0, b);
+  }
+  // the pointwise step for rows [r0, r0 + 8) of a quarter starting at batch entry b0
+  __device__ __forceinline__ void run_quarter(const Quarter& qd, const float* dh_rows, int row, int j, bool live,
+                                              int b0, int r0) const {
+    const float4* g4 = reinterpret_cast<const float4*>(qd.g + (row >> 6) * 16 * 256) + (row & 63);
+#pragma unroll 4
+    for (int r = r0; r < r0 + 8; ++r) {
+      const int b = b0 + r;
+      if (!live || b >= B) continue;
+      float dh = dh_rows[r * 128 + row];
+      if (has_dy)
+        dh += dy_f32 ? static_cast<const float*>(qd.dy)[r * 128 + row]
+                     : __bfloat162float(static_cast<const S*>(qd.dy)[r * 128 + row]);
+      const float4 gt = g4[r * 64];
+      const float cs = qd.cs[r * 128 + row], cp = has_cp ? qd.cp[r * 128 + row] : 0.f, dc = qd.dc[r * 128 + row];
+      const float tau = tanh_hw(cs);
+      const float dov = dh * tau;
+      const float dcv = dc + dh * gt.w * (1.f - tau * tau);
+      const float d0 = dcv * gt.z * gt.x * (1.f - gt.x);
+      const float d1 = dcv * cp * gt.y * (1.f - gt.y);
+      const float d2 = dcv * gt.x * (1.f - gt.z * gt.z);
+      const float d3 = dov * gt.w * (1.f - gt.w);
+      const size_t bj = (size_t)b * H + j;
+      carry[bj] = dcv * gt.y;
+      if (dc0) dc0[bj] = dcv * gt.y;
+      *reinterpret_cast<uint2*>(dGx + (size_t)b * 4 * H + 4 * (size_t)j) = make_uint2(pack_bf16x2(d0, d1), pack_bf16x2(d2, d3));
+    }
+  }
+
   __device__ __forceinline__ void put(int j, int b, float v) const {
     const size_t bj = (size_t)b * H + j;
     if (final_) dh0[bj] = __float2bfloat16_rn(v);
@@ -784,6 +844,20 @@ struct EpiBwdDhT {
       const bool leader = threadIdx.x == 64;  // first epilogue thread
       const int cw = bn / t.cluster;
       float* tile = t.red;  // [bn][128]: tile[b * 128 + row]
+      // fused pointwise: quarters 0 and 2 go to the pipeline buffers past the
+      // tile (region A), quarters 1 and 3 to two slices other CTAs own (region B)
+      const bool fz = fuse && !final_ && bn == 256 && t.cluster == 4;
+      const int b_own = t.n0 + t.split * cw;
+      Quarter qa, qb;
+      {
+        float* ra = tile + (size_t)bn * 128;
+        qa = Quarter{ra, ra + 8192, ra + 10240, ra + 12288, ra + 14336};
+        const int o1 = t.split == 0 ? 1 : 0, o2 = t.split <= 1 ? 2 : 1;
+        float* s1 = tile + (size_t)o1 * cw * 128;
+        float* s2 = tile + (size_t)o2 * cw * 128;
+        qb = Quarter{s1, s2, s2 + 2048, s2 + 4096, s2 + 6144};
+      }
+      if (fz && leader) load_quarter(qa, t.aux + 1, t.m0, b_own);
       // 1. partial tile -> shared memory as [batch][unit]
       for (int c = t.part * (bn / t.parts); c < (t.part + 1) * (bn / t.parts); c += 16) {
         float v[16];
@@ -850,7 +924,27 @@ struct EpiBwdDhT {
           }
         }
       }
-      if (!final_) {
+      if (fz) {
+        // 5. the pointwise step on the own slice, 16 batch rows per bulk load
+        const float* dh_rows = tile + (size_t)t.split * cw * 128;
+        const int r0 = t.part * 8;
+        tc::fence_proxy_async_smem();
+        tc::named_bar(1, EWT);  // the peers' partials in region B have been read
+        if (leader && ok) load_quarter(qb, t.aux + 2, t.m0, b_own + 16);
+        for (int q = 0; q < 4; ++q) {
+          const Quarter& qd = (q & 1) ? qb : qa;
+          uint64_t* bar = t.aux + 1 + (q & 1);
+          if (lane == 0 && ok) ok = tc::mbar_wait_cluster(bar, (uint32_t)(q >> 1), err, limit_ns) ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (ok) run_quarter(qd, dh_rows + (size_t)16 * q * 128, row, j, live, b_own + 16 * q, r0);
+          if (q < 2) {
+            // reload this region with quarter q + 2 once every thread is done with it
+            tc::fence_proxy_async_smem();
+            tc::named_bar(1, EWT);
+            if (leader && ok) load_quarter(qd, bar, t.m0, b_own + 16 * (q + 2));
+          }
+        }
+      } else if (!final_) {
         tc::fence_proxy_async_smem();
         tc::named_bar(1, EWT);
         if (leader && ok) {
@@ -860,10 +954,15 @@ struct EpiBwdDhT {
         }
       }
       if (!ok && leader) {
-        // a load may still be landing in this CTA's buffers: let it (bounded)
+        // loads may still be landing in this CTA's buffers: let them (bounded)
         const uint64_t t0 = globaltimer_ns();
         while (!tc::mbar_try_wait(t.aux, 0) && globaltimer_ns() - t0 < 1000000ull) {
         }
+        if (fz)
+          for (int a = 1; a < 3; ++a)
+            for (int ph = 0; ph < 2; ++ph)
+              while (!tc::mbar_try_wait(t.aux + a, ph) && globaltimer_ns() - t0 < 2000000ull) {
+              }
       }
       return;
     }

@@ -119,9 +119,12 @@ int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const v
 // end of the product's mainloop (null: none)
 // Tiles are 128 units x bn (64, 128 or 256) batch entries; with splits > 1
 // the partial sums pass through `part` (fp32, splits * ceil(B/bn)*bn * H).
+// fuse non-null (LSTM, bn = 256, 4 splits): the pointwise step runs inside
+// the product's epilogue with these arguments (dh is then not written).
+struct PointVArgs;
 int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int bn, int splits,
              float* dh, void* dh0, int final_, float* part, const float* pf_gates = nullptr,
-             const float* pf_c_s = nullptr, const float* pf_c_sm1 = nullptr);
+             const float* pf_c_s = nullptr, const float* pf_c_sm1 = nullptr, const PointVArgs* fuse = nullptr);
 // the pointwise backward step that follows it (packing unit 1, H % 4 == 0)
 struct PointVArgs {
   int B, H;

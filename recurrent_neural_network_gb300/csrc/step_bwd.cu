@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(256) bwd_point_v_kernel(const BwdPointV<CELL> 
 
 int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int H, int G, int bn, int splits,
              float* dh, void* dh0, int final_, float* part, const float* pf_gates, const float* pf_c_s,
-             const float* pf_c_sm1) {
+             const float* pf_c_sm1, const PointVArgs* fuse) {
   const int M = H, N = B, K = G * H;
   EpiBwdDhT e;
   std::memset(&e, 0, sizeof(e));
@@ -151,10 +151,27 @@ int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int 
     if (!part) return RNN_ERR_INVALID_ARG;
     int rc = encode_plain(&e.map_part, part, 4, (long long)eff * e.Bp, H, H, 128, bn / eff);
     if (rc) return rc;
-    if (!final_) {
+    if (!final_ && !fuse) {
       rc = encode_plain(&e.map_dh, dh, 4, B, H, H, 128, bn / eff);
       if (rc) return rc;
     }
+  }
+  if (fuse) {
+    if (final_ || G != 4 || bn != 256 || eff != 4) return RNN_ERR_UNSUPPORTED;
+    const PointVArgs& a = *fuse;
+    int rc = encode_plain(&e.map_g, a.gates, 4, B, 4LL * H, 4LL * H, 256, 16);
+    if (!rc) rc = encode_plain(&e.map_cs, a.c_s, 4, B, H, H, 128, 16);
+    if (!rc && a.c_sm1) rc = encode_plain(&e.map_cp, a.c_sm1, 4, B, H, H, 128, 16);
+    if (!rc) rc = encode_plain(&e.map_dc, a.carry, 4, B, H, H, 128, 16);
+    if (!rc && a.dy) rc = encode_plain(&e.map_dy, a.dy, a.dy_f32 ? 4 : 2, B, H, H, 128, 16);
+    if (rc) return rc;
+    e.fuse = 1;
+    e.has_cp = a.c_sm1 ? 1 : 0;
+    e.has_dy = a.dy ? 1 : 0;
+    e.dy_f32 = a.dy_f32;
+    e.carry = a.carry;
+    e.dc0 = a.dc0;
+    e.dGx = static_cast<__nv_bfloat16*>(a.dGx);
   }
   if (bn == 256) return launch_tc<256, 4>(L, WhT, dG, M, N, K, splits, 0, e, true);
   if (bn == 128) return launch_tc<128, 6>(L, WhT, dG, M, N, K, splits, 0, e, true);

@@ -237,6 +237,8 @@ TRANSPOSED = [
     (0, 2, 4, 129, 72, 320),
     (2, 2, 5, 9, 72, 256),
     (2, 2, 4, 130, 64, 384),
+    (0, 2, 5, 200, 64, 256),   # 256-wide batch tiles, 4 splits: pointwise BPTT fused into the product
+    (0, 2, 4, 256, 64, 256),
 ]
 
 
@@ -273,3 +275,21 @@ def test_transposed_equals_row_major_steps_within_tolerance():
         for k in outs[0]:
             if outs[0][k] is not None:
                 np.testing.assert_array_equal(o[k], outs[0][k], err_msg=k)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B", [200, 256])
+def test_fused_pointwise_equals_separate_kernel(B):
+    """The transposed LSTM BPTT runs its pointwise step inside the product's
+    epilogue (inputs staged by bulk loads) or as its own kernel: same
+    arithmetic in the same order, bit-identical results."""
+    wl = tiny(0, synth.MODE_BF16, layers=2, T=5, B=B, hidden=256)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    r = runner.Runner(wl, flags=rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING)
+    assert "fused_point=1" in r.r.describe()
+    a = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING)
+    b = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_FUSED_POINT)
+    for k in b:
+        if b[k] is not None:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    compare(wl, a, run_oracle(hi))

@@ -120,7 +120,9 @@ def test_transposed_step_plan(lib):
     refused by flags; every split count keeps the backward invariants."""
     import re
     d = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1).describe()
-    assert "transposed=1" in d and " u=1 " in d and "bwd_bn=256 bwd_splits=4" in d
+    assert "transposed=1" in d and " u=1 " in d and "bwd_bn=256 bwd_splits=4" in d and "fused_point=1" in d
+    assert "fused_point=0" in rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, flags=rnn.FLAG_NO_FUSED_POINT).describe()
+    assert "fused_point=0" in rnn.RNN(2, 1, 10, 256, 4096, 16384, 1).describe()  # tanh: separate kernel
     d = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, flags=rnn.FLAG_NO_TRANSPOSED).describe()
     assert "transposed=0" in d and " u=64 " in d
     assert "transposed=0" in rnn.RNN(0, 4, 50, 257, 4096, 4096, 1).describe()   # batch wider than one tile
