@@ -122,7 +122,7 @@ def class_flops(wl):
     return out
 
 
-def class_bytes(wl, transposed):
+def class_bytes(wl, transposed, fused_point=False):
     """Algorithmic HBM bytes per step of the recurrent-step classes: every
     timestep reads W_h once plus the state it updates (bf16 storage, f32 gates,
     cell state and gate pre-activations).  With transposed steps the BPTT
@@ -136,10 +136,16 @@ def class_bytes(wl, transposed):
     if not wl.training:
         return out
     if transposed:
-        # product: W_h + dG_{s+1} (read) ; dh (write)
-        out["bwd_step"] = (wh + B * G * H * e + B * H * 4) * T * L
-        # pointwise: dh, dy, gates, c_s, c_{s-1}, carry (read) ; dG_s, carry (write)
-        out["bwd_point"] = (B * H * 4 + B * H * 4 + B * G * H * 4 + B * H * 4 * 2 + B * H * 4 * 2 + B * G * H * e) * T * L
+        # pointwise: dy, gates, c_s, c_{s-1}, carry (read) ; dG_s, carry (write)
+        point = B * H * 4 + B * G * H * 4 + B * H * 4 * 2 + B * H * 4 * 2 + B * G * H * e
+        if fused_point:
+            # product with the pointwise step in its epilogue: W_h + dG_{s+1} + pointwise inputs and outputs
+            out["bwd_step"] = (wh + B * G * H * e + point) * T * L
+            out["bwd_point"] = (B * H * 4 + point) * L  # only the last timestep runs it alone
+        else:
+            # product: W_h + dG_{s+1} (read) ; dh (write).  pointwise: dh (read) + the rest
+            out["bwd_step"] = (wh + B * G * H * e + B * H * 4) * T * L
+            out["bwd_point"] = (B * H * 4 + point) * T * L
     else:
         # fused: dG_{t+1} + gates + c_t, c_{t-1} + dy + carry (read) ; dG_t + carry (write)
         out["bwd_step"] = (wh + B * G * H * e + B * G * H * 4 + B * H * 4 * 2 + B * H * 4 * 2 + B * G * H * e
@@ -149,10 +155,9 @@ def class_bytes(wl, transposed):
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the same kernel build on a one-layer T=2 case with the same
-# per-step shape (transposed steps); summarised in
-# profiles/ncu_step_kernels_lstm_B256_H4096.md.  The BPTT product's figure
-# includes the pointwise inputs it pulls into L2 for the kernel after it.
-NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 171.03e6,
+# per-step shape (transposed steps, BPTT pointwise fused into the product);
+# summarised in profiles/ncu_step_kernels_lstm_B256_H4096.md.
+NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.30e6,
                ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.90e6,
                ("lstm_bf16_L4_T50_B256_H4096", "bwd_point"): 35.68e6}
 
@@ -227,12 +232,12 @@ def e2e_run(R, wl, steps, sdt, stream, barrier):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
-def roofline(prof, wl, steps, pk, transposed):
+def roofline(prof, wl, steps, pk, transposed, fused_point=False):
     """Roofline of the dominant kernel class (largest device time): its
     algorithmic flops and bytes per launch over its average CUDA-event launch
     duration, against the tensor or the HBM peak, whichever its arithmetic
     intensity makes binding."""
-    cf, cb = class_flops(wl), class_bytes(wl, transposed)
+    cf, cb = class_flops(wl), class_bytes(wl, transposed, fused_point)
     cand = [(k, v) for k, v in prof.items() if k in cf and v[0] > 0]
     if not cand:
         return None
@@ -415,7 +420,7 @@ def main():
     del R
     torch.cuda.empty_cache()
     prof, psteps = kernel_profile(wl, dev, args, sdt)
-    roof = roofline(prof, wl, psteps, pk, "transposed=1" in plan)
+    roof = roofline(prof, wl, psteps, pk, "transposed=1" in plan, "fused_point=1" in plan)
     persistent = persistent_probe(dev) if (world == 1 and args.config != 2 and not args.no_persistent) else None
 
     if rank != 0:
