@@ -1,0 +1,75 @@
+"""Data-parallel training over batch shards, simulated with world-size-2
+gloo ranks on CPU: each rank runs the double-precision oracle on its half
+of the batch, the weight gradients are summed with one all-reduce, and the
+result must equal the full-batch weight gradient (sequences are independent,
+so dW is a sum over batch entries), while each rank's dx, dh0, dc0 are the
+full-batch values of its own columns.  This is the one exchange step a
+data-parallel training step adds to the path; no GPU is involved."""
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _inputs(cell):
+    from recurrent_neural_network_gb300 import runner, synth
+    wl = synth.Workload(name="dp", cell=cell, layers=2, T=4, B=6, input=5, hidden=4, mode=synth.MODE_FP32,
+                        forget_bias=1.0, state_std=0.3)
+    return wl, runner.HostInputs(wl, with_state_grads=True)
+
+
+def _bwd(hi):
+    import oracle
+    w = hi.wl
+    return oracle.bwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, hi.dy, h0=hi.h0, c0=hi.c0,
+                      dhT=hi.dhT, dcT=hi.dcT)
+
+
+def _rank(rank, world, port, cell, out):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    wl, hi = _inputs(cell)
+    cols = list(range(rank * wl.B // world, (rank + 1) * wl.B // world))
+    dx, dh0, dc0, dw = _bwd(hi.columns(cols))
+    t = torch.from_numpy(np.ascontiguousarray(dw))
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    out[rank] = (cols, dx, dh0, dc0, t.numpy().copy())
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("cell", [0, 1, 2], ids=["lstm", "gru", "tanh"])
+def test_batch_shards_plus_allreduce_equal_full_batch(cell):
+    sys.path.insert(0, ROOT)
+    import oracle
+    oracle.build()
+    world = 2
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_rank, args=(world, port, cell, out), nprocs=world, join=True)
+        res = dict(out)
+    wl, hi = _inputs(cell)
+    dx, dh0, dc0, dw = _bwd(hi)
+    for r in range(world):
+        cols, rdx, rdh0, rdc0, rdw = res[r]
+        np.testing.assert_allclose(rdw, dw, rtol=1e-12, atol=1e-14 * np.abs(dw).max())
+        np.testing.assert_allclose(rdx, dx[:, cols], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(rdh0, dh0[:, cols], rtol=1e-12, atol=1e-15)
+        if dc0 is not None:
+            np.testing.assert_allclose(rdc0, dc0[:, cols], rtol=1e-12, atol=1e-15)
