@@ -327,6 +327,51 @@ def persistent_probe(dev, steps=10, warmup=3):
                          "frac": roof_us / us_step}}
 
 
+def sweep(dev, steps=5, warmup=2):
+    """Selector sweep: one-layer bf16 LSTM and tanh-RNN training steps (T=16)
+    over a grid of batch sizes and widths, timed with the library's own plan
+    and with each recurrent-step orientation forced, one JSON line per shape.
+    Used to place the planner's switch between the two orientations."""
+    from recurrent_neural_network_gb300 import rnn, runner, synth
+    variants = [("default", 0), ("transposed", rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING),
+                ("row_major", rnn.FLAG_NO_TRANSPOSED | rnn.FLAG_FORCE_STREAMING)]
+    for cell, H, B in [(c, h, b) for c in (0, 2) for h in (512, 1024, 2048, 4096) for b in (16, 32, 64, 128, 256)]:
+        if True:
+            wl = synth.Workload(name=f"sweep_c{cell}_B{B}_H{H}", cell=cell, layers=1, T=16, B=B, input=H, hidden=H,
+                                mode=synth.MODE_BF16, forget_bias=1.0, state_std=0.1)
+            res, plan = {}, None
+            for name, fl in variants:
+                try:
+                    R = runner.Runner(wl, device=dev, flags=fl)
+                except rnn.RnnError:
+                    continue
+                if name == "default":
+                    plan = R.r.describe()
+                R.x = synth_tensor(wl, "x", dev, R.dt)
+                R.w_user = synth_tensor(wl, "w", dev, R.dt)
+                R.h0 = synth_tensor(wl, "h0", dev, R.dt)
+                R.c0 = synth_tensor(wl, "c0", dev, torch.float32) if cell == 0 else None
+                R.dy = synth_tensor(wl, "dy", dev, R.dt)
+                R.pack()
+                for _ in range(warmup):
+                    R.step()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(steps):
+                    R.step()
+                e1.record()
+                torch.cuda.synchronize()
+                assert R.status() == 0
+                res[name] = e0.elapsed_time(e1) / steps
+                del R
+                torch.cuda.empty_cache()
+            fl = step_flops(wl)
+            print(json.dumps({"sweep": {"cell": ["lstm", "gru", "tanh"][cell], "L": 1, "T": 16, "B": B, "H": H},
+                              "ms": {k: round(v, 4) for k, v in res.items()},
+                              "tflops": {k: round(fl / (v * 1e-3) / 1e12, 1) for k, v in res.items()},
+                              "plan": plan}), flush=True)
+
+
 def synth_tensor(wl, what, dev, dtype):
     from recurrent_neural_network_gb300 import synth
     return synth.device_tensor(wl, what, dev, dtype)
@@ -344,7 +389,14 @@ def main():
     ap.add_argument("--no-persistent", action="store_true")
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="selector sweep over batch sizes and widths instead of the benchmark line")
     args = ap.parse_args()
+    if args.sweep:
+        from recurrent_neural_network_gb300 import build
+        build.build()
+        sweep(torch.device("cuda", 0))
+        return
 
     from recurrent_neural_network_gb300 import synth
     wl = synth.WORKLOADS[args.config]

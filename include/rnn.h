@@ -89,8 +89,9 @@ enum {
                                            and load the packed weights before they wait on it */
 #define RNN_FLAG_NO_TRANSPOSED 0x200u   /* keep the recurrent steps in the h W_h^T orientation */
 #define RNN_FLAG_FORCE_TRANSPOSED 0x400u /* take the recurrent steps as W_h h^T (bf16 LSTM / tanh RNN,
-                                            B <= 256, H % 32 == 0) or fail; by default chosen when
-                                            G*H >= 12288 */
+                                            B <= 256, H % 32 == 0) or fail; by default chosen where it
+                                            measured faster (LSTM: H >= 2048, or H >= 1024 and B >= 64,
+                                            or H >= 512 and 64 <= B <= 128; tanh: H >= 2048) */
 #define RNN_FLAG_NO_FUSED_POINT 0x800u  /* transposed LSTM steps: run the pointwise BPTT step as its own
                                            kernel after each product instead of inside its epilogue */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never

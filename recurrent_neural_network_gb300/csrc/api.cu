@@ -215,12 +215,17 @@ int plan_and_layout(rnn_s* h) {
   else h->chunk = std::max(1, (T + 7) / 8);
   h->nch = (T + h->chunk - 1) / h->chunk;
 
-  // Transposed recurrent steps: with many gate rows (a step of 256-row pair
-  // tiles covers most SMs) and at most 256 batch entries, W_h h^T puts the
-  // batch on the tile columns and keeps the epilogue's accesses contiguous.
+  // Transposed recurrent steps: with at most 256 batch entries, W_h h^T puts
+  // the batch on the tile columns and keeps the epilogue's accesses
+  // contiguous.  Where it wins was measured over batch and width (one-layer
+  // training steps): LSTM from H = 2048 at every batch size, from H = 1024 at
+  // B >= 64 and at H = 512 for 64 <= B <= 128; tanh RNN from H = 2048.
   if (d.mode == RNN_MODE_BF16 && !h->persist && (d.cell == RNN_LSTM || d.cell == RNN_TANH) && B <= 256 &&
       H % 32 == 0 && !(d.flags & RNN_FLAG_NO_TRANSPOSED)) {
-    if (GH >= 12288 || (d.flags & RNN_FLAG_FORCE_TRANSPOSED)) h->tstep = 1;
+    const bool lstm_wins = d.cell == RNN_LSTM && (H >= 2048 || (H >= 1024 && B >= 64) ||
+                                                   (H >= 512 && B >= 64 && B <= 128));
+    const bool tanh_wins = d.cell == RNN_TANH && H >= 2048;
+    if (lstm_wins || tanh_wins || (d.flags & RNN_FLAG_FORCE_TRANSPOSED)) h->tstep = 1;
   }
   if ((d.flags & RNN_FLAG_FORCE_TRANSPOSED) && !h->tstep) return RNN_ERR_UNSUPPORTED;
   if (h->tstep) {

@@ -127,7 +127,12 @@ def test_transposed_step_plan(lib):
     assert "transposed=0" in d and " u=64 " in d
     assert "transposed=0" in rnn.RNN(0, 4, 50, 257, 4096, 4096, 1).describe()   # batch wider than one tile
     assert "transposed=0" in rnn.RNN(1, 4, 50, 256, 4096, 4096, 1).describe()   # GRU keeps h W_h^T
-    assert "transposed=0" in rnn.RNN(0, 2, 10, 64, 512, 512, 1).describe()      # too few gate rows
+    assert "transposed=1" in rnn.RNN(0, 2, 10, 64, 512, 512, 1).describe()      # measured faster there
+    assert "transposed=0" in rnn.RNN(0, 2, 10, 256, 512, 512, 1).describe()     # ... but not at B=256
+    assert "transposed=0" in rnn.RNN(0, 2, 10, 32, 1024, 1024, 1).describe()    # nor at H=1024, B<64
+    assert "transposed=1" in rnn.RNN(0, 2, 10, 32, 2048, 2048, 1).describe()
+    assert "transposed=1" in rnn.RNN(2, 2, 10, 16, 2048, 2048, 1).describe()    # tanh from H=2048
+    assert "transposed=0" in rnn.RNN(2, 2, 10, 256, 1024, 1024, 1).describe()
     for bad in [dict(cell=1, B=9, H=256, mode=1), dict(cell=0, B=300, H=256, mode=1), dict(cell=0, B=9, H=256, mode=0)]:
         with pytest.raises(rnn.RnnError):
             rnn.RNN(bad["cell"], 1, 3, bad["B"], 64, bad["H"], bad["mode"], flags=rnn.FLAG_FORCE_TRANSPOSED)
