@@ -22,7 +22,7 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_OUT_DIR, "librnn_ref.so")
 _lib = None
 
-GATES = {0: 4, 1: 3, 2: 1}
+GATES = {0: 4, 1: 3, 2: 1, 3: 1}
 
 
 def build(force: bool = False) -> str:

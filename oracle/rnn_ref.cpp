@@ -1,4 +1,4 @@
-// rnn_ref.cpp -- plain double-precision oracle for stacked LSTM / GRU / tanh-RNN.
+// rnn_ref.cpp -- plain double-precision oracle for stacked LSTM / GRU / simple RNN.
 //
 // TEST INFRASTRUCTURE ONLY: used by the tests, the smoke check and the
 // benchmark's CPU-baseline leg; never by the product library.
@@ -13,12 +13,14 @@
 //   GRU (gates r,z,n):     r=s(x_r+h_r) z=s(x_z+h_z) n=tanh(x_n + r*h_n)
 //        with x_* = W_x in + b_x, h_* = W_h h + b_h;  h' = (1-z) n + z h
 //   RNN:                   h' = tanh(W_x in + b_x + W_h h + b_h)
+//   ReLU RNN:              h' = max(0, W_x in + b_x + W_h h + b_h)
 // The backward pass is the exact gradient of
 //   L = sum(y*dy) + sum(hT*dhT) + sum(cT*dcT)
 // taken in reverse time, top layer first, one step and one layer at a time
 // (no reordering beyond the definition).
 #include "rnn_ref.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -68,7 +70,7 @@ struct Record {
 };
 
 bool bad_args(int cell, int L, int T, int B, int I, int H, const double* x, const double* w) {
-  return cell < 0 || cell > 2 || L < 1 || T < 0 || B < 0 || I < 1 || H < 1 || (!x && T * B > 0) || !w;
+  return cell < 0 || cell > 3 || L < 1 || T < 0 || B < 0 || I < 1 || H < 1 || (!x && T * B > 0) || !w;
 }
 
 // Forward over all layers; fills one Record per layer.
@@ -130,6 +132,9 @@ void forward(int cell, int L, int T, int B, int I, int H, const double* x, const
             hnew = (1.0 - z) * n + z * hprev;
             R.n(t, b)[j] = hn;
             gt[j] = r; gt[H + j] = z; gt[2 * H + j] = n;
+          } else if (cell == RNN_REF_RELU) {
+            hnew = std::max(0.0, sx[j] + sh[j]);
+            gt[j] = hnew;
           } else {
             hnew = std::tanh(sx[j] + sh[j]);
             gt[j] = hnew;
@@ -245,6 +250,11 @@ extern "C" int rnn_ref_bwd(int cell, int L, int T, int B, int I, int H, const do
             gh[H + j] = gx[H + j];
             gh[2 * H + j] = dhn;
             dh_new[(size_t)b * H + j] = dh * z;  // direct path h' = ... + z h
+          } else if (cell == RNN_REF_RELU) {
+            // d max(0, a)/da = 1 where a > 0 (h > 0), else 0
+            gx[j] = gt[j] > 0.0 ? dh : 0.0;
+            gh[j] = gx[j];
+            dh_new[(size_t)b * H + j] = 0.0;
           } else {
             double h = gt[j];
             gx[j] = dh * (1.0 - h * h);

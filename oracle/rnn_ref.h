@@ -1,6 +1,6 @@
 /*
- * rnn_ref.h -- double-precision CPU oracle for stacked LSTM / GRU / tanh-RNN
- * forward and backward-through-time passes.
+ * rnn_ref.h -- double-precision CPU oracle for stacked LSTM / GRU / simple-RNN
+ * (tanh or ReLU) forward and backward-through-time passes.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
  * calls this code; only the test suite, the smoke check and the CPU-baseline
@@ -15,7 +15,7 @@
  *   x[T][B][I], y[T][B][H], h0/c0/hT/cT/dh0/dc0[L][B][H], dy[T][B][H]
  *   w: per layer l (in order): W_x[G*H][I_l], W_h[G*H][H], b_x[G*H], b_h[G*H]
  *      with I_0 = I, I_l = H for l >= 1, gate blocks LSTM (i,f,g,o),
- *      GRU (r,z,n), RNN (single block).
+ *      GRU (r,z,n), RNN tanh / ReLU (single block).
  *   dw: same layout as w.
  * Nullable: h0, c0 (zero state), hT, cT (not written), dhT, dcT (zero),
  *   dx, dh0, dc0 (not written).  c-arguments are ignored for GRU and RNN.
@@ -27,7 +27,7 @@
 extern "C" {
 #endif
 
-enum { RNN_REF_LSTM = 0, RNN_REF_GRU = 1, RNN_REF_TANH = 2 };
+enum { RNN_REF_LSTM = 0, RNN_REF_GRU = 1, RNN_REF_TANH = 2, RNN_REF_RELU = 3 };
 
 int rnn_ref_fwd(int cell, int L, int T, int B, int I, int H,
                 const double* x, const double* h0, const double* c0, const double* w,

@@ -17,8 +17,8 @@ import torch
 import oracle
 from recurrent_neural_network_gb300 import synth
 
-CELLS = [0, 1, 2]
-G = {0: 4, 1: 3, 2: 1}
+CELLS = [0, 1, 2, 3]
+G = {0: 4, 1: 3, 2: 1, 3: 1}
 
 
 def rand_case(cell, L, T, B, I, H, seed):
@@ -40,7 +40,7 @@ def torch_model(cell, L, I, H, w):
     elif cell == 1:
         m = torch.nn.GRU(I, H, L, dtype=torch.float64)
     else:
-        m = torch.nn.RNN(I, H, L, nonlinearity="tanh", dtype=torch.float64)
+        m = torch.nn.RNN(I, H, L, nonlinearity="tanh" if cell == 2 else "relu", dtype=torch.float64)
     for l, (wx, wh, bx, bh) in enumerate(oracle.split_weights(cell, L, I, H, w)):
         getattr(m, f"weight_ih_l{l}").data.copy_(torch.from_numpy(wx))
         getattr(m, f"weight_hh_l{l}").data.copy_(torch.from_numpy(wh))
@@ -159,6 +159,36 @@ def test_rnn_closed_form_zero_weights():
     np.testing.assert_allclose(hT[0], math.tanh(0.25 - 0.1), rtol=1e-14)
 
 
+def test_relu_rnn_closed_form_zero_weights():
+    """Zero weights: every step of every layer is max(0, b_x + b_h) (0 where
+    that sum is negative), whatever x and h0 are."""
+    L, T, B, I, H = 2, 4, 2, 3, 4
+    w = np.zeros(oracle.weight_count(3, L, I, H))
+    for l, (_, _, bx, bh) in enumerate(oracle.split_weights(3, L, I, H, w)):
+        bx[:] = [0.3, -0.2, 0.05 * (l + 1), -1.0]
+        bh[:] = 0.1
+    x = np.random.default_rng(4).normal(size=(T, B, I))
+    y, hT, _ = oracle.fwd(3, L, T, B, I, H, x, w, h0=np.ones((L, B, H)))
+    want = np.maximum(0.0, np.array([0.4, -0.1, 0.2, -0.9]))
+    np.testing.assert_allclose(y, np.broadcast_to(want, y.shape), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(hT[0], np.broadcast_to(np.maximum(0.0, [0.4, -0.1, 0.15, -0.9]), hT[0].shape),
+                               rtol=1e-14, atol=0)
+
+
+def test_relu_rnn_gradient_is_masked_by_the_activation():
+    """One step, one unit: dL/da = dy where a > 0 and exactly 0 where a < 0,
+    so dx = dy * w_x on active entries and 0 elsewhere."""
+    L, T, B, I, H = 1, 1, 2, 1, 1
+    w = np.array([2.0, 0.0, -0.5, 0.0])  # W_x, W_h, b_x, b_h
+    x = np.array([[[1.0], [-1.0]]])       # a = 2x - 0.5: 1.5 (active), -2.5 (inactive)
+    dy = np.array([[[3.0], [7.0]]])
+    y, _, _ = oracle.fwd(3, L, T, B, I, H, x, w)
+    np.testing.assert_array_equal(y.reshape(-1), [1.5, 0.0])
+    dx, dh0, _, dw = oracle.bwd(3, L, T, B, I, H, x, w, dy)
+    np.testing.assert_array_equal(dx.reshape(-1), [6.0, 0.0])
+    np.testing.assert_array_equal(dw, [3.0, 0.0, 3.0, 3.0])  # dW_x = 3*1, dW_h = 3*h0 = 0, db = 3
+
+
 def test_lstm_t1_single_unit_by_hand():
     """One step of a 1x1 LSTM written out scalar by scalar."""
     # w layout: Wx[4][1], Wh[4][1], bx[4], bh[4]
@@ -208,7 +238,10 @@ def test_zero_input_zero_state_zero_bias_stays_zero(cell):
     dx, dh0, dc0, dw = oracle.bwd(cell, L, T, B, I, H, x, w, dy)
     for (dwx, dwh, dbx, dbh) in oracle.split_weights(cell, L, I, H, dw):
         assert not dwx.any() and not dwh.any()   # every product has a zero operand
-        assert dbx.any()                          # the bias gradient does not vanish
+        if cell == 3:
+            assert not dbx.any()  # every pre-activation is exactly 0, where ReLU's slope is taken as 0
+        else:
+            assert dbx.any()      # the bias gradient does not vanish
 
 
 # ---------------------------------------------------------------- finite differences
