@@ -1,5 +1,5 @@
 /*
- * rnn.h -- C-ABI of librnn: stacked LSTM / GRU / tanh-RNN forward and
+ * rnn.h -- C-ABI of librnn: stacked LSTM / GRU / simple-RNN (tanh or ReLU) forward and
  * backward-through-time on one NVIDIA GB300 (sm_103a).
  *
  * The method follows "Optimizing Performance of Recurrent Neural Networks on
@@ -61,7 +61,7 @@
 extern "C" {
 #endif
 
-typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_TANH = 2 } rnn_cell_t;
+typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_TANH = 2, RNN_RELU = 3 } rnn_cell_t;
 typedef enum { RNN_MODE_FP32 = 0, RNN_MODE_BF16 = 1 } rnn_mode_t;
 
 enum {
@@ -88,10 +88,10 @@ enum {
                                            while their predecessor drains (programmatic dependent launch)
                                            and load the packed weights before they wait on it */
 #define RNN_FLAG_NO_TRANSPOSED 0x200u   /* keep the recurrent steps in the h W_h^T orientation */
-#define RNN_FLAG_FORCE_TRANSPOSED 0x400u /* take the recurrent steps as W_h h^T (bf16 LSTM / tanh RNN,
+#define RNN_FLAG_FORCE_TRANSPOSED 0x400u /* take the recurrent steps as W_h h^T (bf16 LSTM / simple RNN,
                                             B <= 256, H % 32 == 0) or fail; by default chosen where it
                                             measured faster (LSTM: H >= 2048, or H >= 1024 and B >= 64,
-                                            or H >= 512 and 64 <= B <= 128; tanh: H >= 2048) */
+                                            or H >= 512 and 64 <= B <= 128; simple RNN: H >= 2048) */
 #define RNN_FLAG_NO_FUSED_POINT 0x800u  /* transposed LSTM steps: run the pointwise BPTT step as its own
                                            kernel after each product instead of inside its epilogue */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never
@@ -141,6 +141,9 @@ RNN_API int rnn_pack_weights(rnn_handle_t h, const void* w_user, void* w_packed,
  *         n = tanh(W_xn in + b_xn + r*(W_hn h_{t-1} + b_hn));
  *         h_t = (1-z)*n + z*h_{t-1}
  *   RNN:  h_t = tanh(W_x in_t + b_x + W_h h_{t-1} + b_h)
+ *   ReLU RNN: h_t = max(0, W_x in_t + b_x + W_h h_{t-1} + b_h) (slope 0 at the kink).
+ *         The pages name the simple RNN without its activation; tanh is the
+ *         named target, ReLU the other common choice for the cell.
  * with in_t = x_t for layer 0 and h^{l-1}_t above it.  y_t = h^{L-1}_t.
  * h0/c0 NULL mean zero state; hT/cT NULL are not written; c-arguments are
  * ignored for GRU and RNN.  reserve == NULL runs inference; otherwise the

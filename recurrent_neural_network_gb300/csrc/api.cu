@@ -184,10 +184,11 @@ int plan_and_layout(rnn_s* h) {
   const int GH = h->GH;
   if (d.mode == RNN_MODE_BF16) {
     if (H % 64 || d.input % 8) return RNN_ERR_UNSUPPORTED;
-    h->u = (d.cell == RNN_TANH && H % 128 == 0) ? 128 : 64;
+    const bool simple = d.cell == RNN_TANH || d.cell == RNN_RELU;
+    h->u = (simple && H % 128 == 0) ? 128 : 64;
     // a forward step has ceil(B/128) x H/u tiles: narrow the packing unit
     // (down to 16 units, 32 for tanh) until a step covers at least 64 CTAs
-    const int mtl = (B + 127) / 128, umin = d.cell == RNN_TANH ? 32 : 16;
+    const int mtl = (B + 127) / 128, umin = simple ? 32 : 16;
     while (h->u > umin && mtl * (H / h->u) < 64) h->u /= 2;
   } else {
     if (H % 32 || d.input % 4) return RNN_ERR_UNSUPPORTED;
@@ -220,11 +221,11 @@ int plan_and_layout(rnn_s* h) {
   // contiguous.  Where it wins was measured over batch and width (one-layer
   // training steps): LSTM from H = 2048 at every batch size, from H = 1024 at
   // B >= 64 and at H = 512 for 64 <= B <= 128; tanh RNN from H = 2048.
-  if (d.mode == RNN_MODE_BF16 && !h->persist && (d.cell == RNN_LSTM || d.cell == RNN_TANH) && B <= 256 &&
+  if (d.mode == RNN_MODE_BF16 && !h->persist && d.cell != RNN_GRU && B <= 256 &&
       H % 32 == 0 && !(d.flags & RNN_FLAG_NO_TRANSPOSED)) {
     const bool lstm_wins = d.cell == RNN_LSTM && (H >= 2048 || (H >= 1024 && B >= 64) ||
                                                    (H >= 512 && B >= 64 && B <= 128));
-    const bool tanh_wins = d.cell == RNN_TANH && H >= 2048;
+    const bool tanh_wins = (d.cell == RNN_TANH || d.cell == RNN_RELU) && H >= 2048;
     if (lstm_wins || tanh_wins || (d.flags & RNN_FLAG_FORCE_TRANSPOSED)) h->tstep = 1;
   }
   if ((d.flags & RNN_FLAG_FORCE_TRANSPOSED) && !h->tstep) return RNN_ERR_UNSUPPORTED;
@@ -488,7 +489,7 @@ int rnn_create(const rnn_desc_t* desc, rnn_handle_t* out) {
   if (!desc || !out) return RNN_ERR_INVALID_ARG;
   *out = nullptr;
   const rnn_desc_t& d = *desc;
-  if (d.cell < 0 || d.cell > 2 || d.mode < 0 || d.mode > 1 || d.layers < 1 || d.T < 1 || d.B < 1 ||
+  if (d.cell < 0 || d.cell > 3 || d.mode < 0 || d.mode > 1 || d.layers < 1 || d.T < 1 || d.B < 1 ||
       d.input < 1 || d.hidden < 1)
     return RNN_ERR_INVALID_ARG;
   if ((d.flags & RNN_FLAG_FORCE_STREAMING) && (d.flags & RNN_FLAG_FORCE_PERSISTENT)) return RNN_ERR_INVALID_ARG;

@@ -8,7 +8,7 @@
 
 namespace rnn {
 
-enum Cell { LSTM = 0, GRU = 1, TANH = 2 };
+enum Cell { LSTM = 0, GRU = 1, TANH = 2, RELU = 3 };
 
 template <int CELL>
 struct CellInfo;
@@ -18,6 +18,8 @@ template <>
 struct CellInfo<GRU> { static constexpr int G = 3; };
 template <>
 struct CellInfo<TANH> { static constexpr int G = 1; };
+template <>
+struct CellInfo<RELU> { static constexpr int G = 1; };
 
 // Device error word codes (written into the first word of the workspace).
 enum DevErr { DEV_OK = 0, DEV_TIMEOUT_PIPE = 1, DEV_TIMEOUT_STEP = 2 };
@@ -120,6 +122,20 @@ struct Act<__nv_bfloat16> {
   __device__ __forceinline__ static float sig(float a) { return sigm_hw(a); }
   __device__ __forceinline__ static float th(float a) { return tanh_hw(a); }
 };
+
+// Simple-RNN cells (one gate block): activation h = act(a) and its slope
+// written in terms of h (tanh: 1 - h^2; ReLU: 1 where h > 0, taken as 0 at
+// the kink).
+template <int CELL, class S>
+__device__ __forceinline__ float simple_act(float a) {
+  if constexpr (CELL == RELU) return fmaxf(a, 0.f);
+  else return Act<S>::th(a);
+}
+template <int CELL>
+__device__ __forceinline__ float simple_slope(float h) {
+  if constexpr (CELL == RELU) return h > 0.f ? 1.f : 0.f;
+  else return 1.f - h * h;
+}
 
 // ---------------------------------------------------------------- time and errors
 __device__ __forceinline__ uint64_t globaltimer_ns() {

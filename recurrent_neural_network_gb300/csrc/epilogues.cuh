@@ -174,7 +174,7 @@ struct EpiFwdStep {
         load16(prow, p);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          hnew[i] = Act<S>::th(a[0][i] + p[i]);
+          hnew[i] = simple_act<CELL, S>(a[0][i] + p[i]);
           a[0][i] = hnew[i];
         }
       }
@@ -286,7 +286,7 @@ struct BwdPoint {
       float hv[16], da[16];
       load16(grow, hv);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) da[i] = dh[i] * (1.f - hv[i] * hv[i]);
+      for (int i = 0; i < 16; ++i) da[i] = dh[i] * simple_slope<CELL>(hv[i]);
       store16(gx, da);
     }
   }
@@ -347,7 +347,7 @@ struct EpiBwdStep {
       tc::prefetch_l2(pt.hn_s + bj, nu * 4);
       if (pt.h_sm1) tc::prefetch_l2(pt.h_sm1 + bj, nu * sizeof(S));
     }
-    if (CELL != TANH) tc::prefetch_l2(pt.carry + bj, nu * 4);
+    if (CELL == LSTM || CELL == GRU) tc::prefetch_l2(pt.carry + bj, nu * 4);
     if (pt.dy) tc::prefetch_l2(static_cast<const char*>(pt.dy) + bj * (pt.dy_f32 ? 4 : sizeof(S)),
                                nu * (pt.dy_f32 ? 4 : (int)sizeof(S)));
   }
@@ -585,7 +585,7 @@ struct EpiFwdStepT {
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = tanh_hw(v[i]);
+      for (int i = 0; i < 16; ++i) v[i] = simple_act<CELL, S>(v[i]);
       if (sm_g) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -1057,7 +1057,7 @@ struct BwdPointV {
       const float hvv[4] = {hv.x, hv.y, hv.z, hv.w};
       float o[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) o[k] = dhv[k] * (1.f - hvv[k] * hvv[k]);
+      for (int k = 0; k < 4; ++k) o[k] = dhv[k] * simple_slope<CELL>(hvv[k]);
       *reinterpret_cast<uint2*>(dGx + bj) = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
     }
   }

@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
         gv[0] = r; gv[1] = z; gv[G - 1] = n;
         if (a.hn_out) a.hn_out[((size_t)t * B + bq) * H + j] = hn;
       } else {
-        hnew = tanh_hw(av[0] + pv[0]);
+        hnew = simple_act<CELL, __nv_bfloat16>(av[0] + pv[0]);
         gv[0] = hnew;
       }
       const size_t bj = (size_t)bq * H + j;
@@ -255,6 +255,7 @@ int dispatch(const Launch& L, int cell, const PersistArgs& a, bool query_only, i
   RNN_P(LSTM, 2, 1) RNN_P(LSTM, 2, 2) RNN_P(LSTM, 2, 4) RNN_P(LSTM, 2, 8)
   RNN_P(GRU, 3, 1) RNN_P(GRU, 3, 2) RNN_P(GRU, 3, 4)
   RNN_P(TANH, 1, 1) RNN_P(TANH, 1, 2) RNN_P(TANH, 1, 4) RNN_P(TANH, 1, 8) RNN_P(TANH, 1, 16)
+  RNN_P(RELU, 1, 1) RNN_P(RELU, 1, 2) RNN_P(RELU, 1, 4) RNN_P(RELU, 1, 8) RNN_P(RELU, 1, 16)
 #undef RNN_P
   return RNN_ERR_UNSUPPORTED;
 }

@@ -98,6 +98,7 @@ int bwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
              const BwdStepArgs& a) {
   if (cell == LSTM) return bwd_step_cell<LSTM>(L, mode, A, Bw, bn, splits, a);
   if (cell == GRU) return bwd_step_cell<GRU>(L, mode, A, Bw, bn, splits, a);
+  if (cell == RELU) return bwd_step_cell<RELU>(L, mode, A, Bw, bn, splits, a);
   return bwd_step_cell<TANH>(L, mode, A, Bw, bn, splits, a);
 }
 
@@ -106,10 +107,12 @@ int bwd_point(const Launch& L, int mode, int cell, const BwdStepArgs& a, const v
     using S = __nv_bfloat16;
     if (cell == LSTM) return point_launch<LSTM, S>(L, a, dh_init);
     if (cell == GRU) return point_launch<GRU, S>(L, a, dh_init);
+    if (cell == RELU) return point_launch<RELU, S>(L, a, dh_init);
     return point_launch<TANH, S>(L, a, dh_init);
   }
   if (cell == LSTM) return point_launch<LSTM, float>(L, a, dh_init);
   if (cell == GRU) return point_launch<GRU, float>(L, a, dh_init);
+  if (cell == RELU) return point_launch<RELU, float>(L, a, dh_init);
   return point_launch<TANH, float>(L, a, dh_init);
 }
 
@@ -180,7 +183,7 @@ int bwd_dh_t(const Launch& L, const Operand& WhT, const Operand& dG, int B, int 
 }
 
 int bwd_point_v(const Launch& L, int cell, const PointVArgs& a) {
-  if (a.H % 4 || (cell != LSTM && cell != TANH)) return RNN_ERR_UNSUPPORTED;
+  if (a.H % 4 || (cell != LSTM && cell != TANH && cell != RELU)) return RNN_ERR_UNSUPPORTED;
   const long long n = (long long)a.B * (a.H / 4);
   const int grid = (int)((n + 255) / 256);
   auto fill = [&](auto& p) {
@@ -203,9 +206,15 @@ int bwd_point_v(const Launch& L, int cell, const PointVArgs& a) {
     fill(p);
     bwd_point_v_kernel<LSTM><<<grid, 256, 0, L.stream>>>(p);
   } else {
-    BwdPointV<TANH> p;
-    fill(p);
-    bwd_point_v_kernel<TANH><<<grid, 256, 0, L.stream>>>(p);
+    if (cell == RELU) {
+      BwdPointV<RELU> p;
+      fill(p);
+      bwd_point_v_kernel<RELU><<<grid, 256, 0, L.stream>>>(p);
+    } else {
+      BwdPointV<TANH> p;
+      fill(p);
+      bwd_point_v_kernel<TANH><<<grid, 256, 0, L.stream>>>(p);
+    }
   }
   const cudaError_t e = cudaGetLastError();
   launch_end(L);

@@ -51,12 +51,14 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
       if (cell == GRU && a.u == 64) return launch_tc2<192, 7>(L, A, Bw, M, N, K, 0, make_epi<GRU, S>(a));
       if (cell == GRU && a.u == 32) return launch_tc2<96, 9>(L, A, Bw, M, N, K, 0, make_epi<GRU, S>(a));
       if (cell == TANH && a.u == 128) return launch_tc2<128, 8>(L, A, Bw, M, N, K, 0, make_epi<TANH, S>(a));
+      if (cell == RELU && a.u == 128) return launch_tc2<128, 8>(L, A, Bw, M, N, K, 0, make_epi<RELU, S>(a));
     }
 #define RNN_STEP(C, U, BN_, ST)     \
   if (cell == C && a.u == U) return launch_tc<BN_, ST>(L, A, Bw, M, N, K, 1, 0, make_epi<C, S>(a), false, mc);
     RNN_STEP(LSTM, 64, 256, 4) RNN_STEP(LSTM, 32, 128, 6) RNN_STEP(LSTM, 16, 64, 8)
     RNN_STEP(GRU, 64, 192, 5) RNN_STEP(GRU, 32, 96, 7) RNN_STEP(GRU, 16, 48, 8)
     RNN_STEP(TANH, 128, 128, 6) RNN_STEP(TANH, 64, 64, 8) RNN_STEP(TANH, 32, 32, 8)
+    RNN_STEP(RELU, 128, 128, 6) RNN_STEP(RELU, 64, 64, 8) RNN_STEP(RELU, 32, 32, 8)
 #undef RNN_STEP
     return RNN_ERR_UNSUPPORTED;
   }
@@ -64,6 +66,7 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
   if (cell == LSTM && a.u == 32) return launch_simt<128>(L, A, Bw, M, N, K, make_epi<LSTM, S>(a));
   if (cell == GRU && a.u == 32) return launch_simt<96>(L, A, Bw, M, N, K, make_epi<GRU, S>(a));
   if (cell == TANH && a.u == 32) return launch_simt<32>(L, A, Bw, M, N, K, make_epi<TANH, S>(a));
+  if (cell == RELU && a.u == 32) return launch_simt<32>(L, A, Bw, M, N, K, make_epi<RELU, S>(a));
   return RNN_ERR_UNSUPPORTED;
 }
 
@@ -99,20 +102,22 @@ EpiFwdStepT<CELL> make_epi_t(const FwdStepArgs& a, int bn) {
 }  // namespace
 
 int fwd_step_t(const Launch& L, int cell, const Operand& Wh, const Operand& Hp, const FwdStepArgs& a) {
-  const int G = cell == LSTM ? 4 : cell == TANH ? 1 : 0;
+  const int G = cell == LSTM ? 4 : (cell == TANH || cell == RELU) ? 1 : 0;
   if (!G || a.u != 1) return RNN_ERR_UNSUPPORTED;
   const int M = G * a.H, N = a.B, K = a.H;
   // one n-tile holds the whole batch (up to 256 entries): W_h streams once per step
+#define RNN_STEP_T(BN_, ST)                                                                          \
+  if (cell == LSTM) return launch_tc2<BN_, ST>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, BN_));      \
+  if (cell == RELU) return launch_tc2<BN_, ST>(L, Wh, Hp, M, N, K, 0, make_epi_t<RELU>(a, BN_));      \
+  return launch_tc2<BN_, ST>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a, BN_));
   if (N > 128) {
-    if (cell == LSTM) return launch_tc2<256, 6>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, 256));
-    return launch_tc2<256, 6>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a, 256));
+    RNN_STEP_T(256, 6)
   }
   if (N > 64) {
-    if (cell == LSTM) return launch_tc2<128, 8>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, 128));
-    return launch_tc2<128, 8>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a, 128));
+    RNN_STEP_T(128, 8)
   }
-  if (cell == LSTM) return launch_tc2<64, 10>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, 64));
-  return launch_tc2<64, 10>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a, 64));
+  RNN_STEP_T(64, 10)
+#undef RNN_STEP_T
 }
 
 }  // namespace rnn

@@ -30,9 +30,9 @@ _GAMMA = 0x9E3779B97F4A7C15
 _M1 = 0xBF58476D1CE4E5B9
 _M2 = 0x94D049BB133111EB
 
-CELL_LSTM, CELL_GRU, CELL_TANH = 0, 1, 2
-CELL_NAMES = {CELL_LSTM: "lstm", CELL_GRU: "gru", CELL_TANH: "tanh"}
-GATES = {CELL_LSTM: 4, CELL_GRU: 3, CELL_TANH: 1}
+CELL_LSTM, CELL_GRU, CELL_TANH, CELL_RELU = 0, 1, 2, 3
+CELL_NAMES = {CELL_LSTM: "lstm", CELL_GRU: "gru", CELL_TANH: "tanh", CELL_RELU: "relu"}
+GATES = {CELL_LSTM: 4, CELL_GRU: 3, CELL_TANH: 1, CELL_RELU: 1}
 MODE_FP32, MODE_BF16 = 0, 1
 
 # tensor ids of the counter streams
@@ -119,6 +119,10 @@ class Workload:
     state_std: float = 0.0        # h0 (and c0) ~ N(0, state_std^2); 0 means zeros
     training: bool = True
     seed: int = 0
+    # > 0: weights shrunk 20x and b_x = +kink_margin / -kink_margin on even /
+    # odd units, so that every pre-activation of a ReLU RNN stays well away
+    # from 0 and the activation's on/off decision is the same at any precision
+    kink_margin: float = 0.0
 
     @property
     def G(self):
@@ -144,7 +148,7 @@ class Workload:
         return {"fwd": fwd, "bwd_data": fwd, "bwd_weights": fwd}
 
 
-# The five benchmark workloads (index 0 .. 4).
+# The benchmark workloads (index 0 .. 4) and one cell-variant workload (5).
 WORKLOADS = [
     Workload("lstm_fp32_L1_T8_B4_H32", CELL_LSTM, 1, 8, 4, 32, 32, MODE_FP32,
              x_dist="uniform", forget_bias=1.0),
@@ -155,6 +159,8 @@ WORKLOADS = [
     Workload("lstm_bf16_L4_T50_B256_H4096", CELL_LSTM, 4, 50, 256, 4096, 4096, MODE_BF16,
              forget_bias=1.0),
     Workload("gru_bf16_L8_T200_B32_H1024", CELL_GRU, 8, 200, 32, 1024, 1024, MODE_BF16),
+    # cell variant beyond the five: a 4-layer ReLU simple RNN, wide enough for the transposed steps
+    Workload("relu_bf16_L4_T100_B256_H2048", CELL_RELU, 4, 100, 256, 2048, 2048, MODE_BF16, kink_margin=0.75),
 ]
 
 
@@ -165,13 +171,16 @@ def layer_weights(wl: Workload, l: int, dtype=np.float64):
     forget gate (gate block 1 of b_x), which gets ``forget_bias``.
     """
     G, H, I = wl.G, wl.hidden, wl.in_size(l)
-    a = 1.0 / math.sqrt(H)
+    a = (0.05 if wl.kink_margin else 1.0) / math.sqrt(H)
     wx = uniform(wl.seed, 100 + 10 * l + 0, (G * H, I), -a, a).astype(dtype)
     wh = uniform(wl.seed, 100 + 10 * l + 1, (G * H, H), -a, a).astype(dtype)
     bx = np.zeros(G * H, dtype=dtype)
     bh = np.zeros(G * H, dtype=dtype)
     if wl.cell == CELL_LSTM and wl.forget_bias:
         bx[H:2 * H] = wl.forget_bias
+    if wl.kink_margin:
+        bx[0::2] = wl.kink_margin
+        bx[1::2] = -wl.kink_margin
     return wx, wh, bx, bh
 
 
@@ -239,12 +248,15 @@ def device_tensor(wl: Workload, what: str, device, dtype):
         parts = []
         for l in range(wl.layers):
             G, H, I = wl.G, wl.hidden, wl.in_size(l)
-            a = 1.0 / math.sqrt(H)
+            a = (0.05 if wl.kink_margin else 1.0) / math.sqrt(H)
             parts.append(uniform_t(wl.seed, 100 + 10 * l, (G * H * I,), -a, a, device).to(torch.float32))
             parts.append(uniform_t(wl.seed, 100 + 10 * l + 1, (G * H * H,), -a, a, device).to(torch.float32))
             bx = torch.zeros(G * H, dtype=torch.float32, device=device)
             if wl.cell == CELL_LSTM and wl.forget_bias:
                 bx[H:2 * H] = wl.forget_bias
+            if wl.kink_margin:
+                bx[0::2] = wl.kink_margin
+                bx[1::2] = -wl.kink_margin
             parts.append(bx)
             parts.append(torch.zeros(G * H, dtype=torch.float32, device=device))
         t = torch.cat(parts)

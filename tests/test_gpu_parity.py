@@ -22,13 +22,13 @@ TINY = {
 def tiny(cell, mode, **kw):
     L, T, B, I, H = TINY[mode]
     base = dict(name="tiny", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
-                forget_bias=1.0, state_std=0.3)
+                forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0)
     base.update(kw)
     return synth.Workload(**base)
 
 
 @pytest.mark.parametrize("mode", [synth.MODE_FP32, synth.MODE_BF16], ids=["fp32", "bf16"])
-@pytest.mark.parametrize("cell", [0, 1, 2], ids=["lstm", "gru", "tanh"])
+@pytest.mark.parametrize("cell", [0, 1, 2, 3], ids=["lstm", "gru", "tanh", "relu"])
 @pytest.mark.parametrize("chunk", [0, 2], ids=["chunkauto", "chunk2"])
 def test_tiny_all_outputs(cell, mode, chunk):
     wl = tiny(cell, mode)
@@ -138,6 +138,10 @@ def test_workload_gru_8layer_sampled_columns():
     masked_columns_check(synth.WORKLOADS[4], [5, 31])
 
 
+def test_workload_relu_4layer_sampled_columns():
+    masked_columns_check(synth.WORKLOADS[5], [3, 250])
+
+
 # ---------------------------------------------------------------- persistent recurrence
 
 PERSIST_CASES = [
@@ -148,13 +152,15 @@ PERSIST_CASES = [
     (1, 2, 6, 4, 64, 256),
     (1, 1, 5, 8, 64, 128),
     (2, 2, 6, 5, 64, 2048),
+    (3, 2, 6, 4, 64, 512),
 ]
 
 
 @pytest.mark.parametrize("case", PERSIST_CASES, ids=lambda c: "c%d_L%d_T%d_B%d_I%d_H%d" % c)
 def test_persistent_recurrence_training(case):
     cell, L, T, B, I, H = case
-    wl = synth.Workload("persist", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3)
+    wl = synth.Workload("persist", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3,
+                        kink_margin=0.75 if cell == 3 else 0.0)
     hi = runner.HostInputs(wl, with_state_grads=True)
     r = runner.Runner(wl, flags=rnn.FLAG_FORCE_PERSISTENT)
     assert "recurrence=persistent" in r.r.describe()
@@ -237,6 +243,8 @@ TRANSPOSED = [
     (0, 2, 4, 129, 72, 320),
     (2, 2, 5, 9, 72, 256),
     (2, 2, 4, 130, 64, 384),
+    (3, 2, 5, 9, 72, 256),
+    (3, 2, 4, 200, 64, 320),
     (0, 2, 5, 200, 64, 256),   # 256-wide batch tiles, 4 splits: pointwise BPTT fused into the product
     (0, 2, 4, 256, 64, 256),
 ]
@@ -249,7 +257,7 @@ def test_transposed_steps(case):
     columns) against the oracle, every output and gradient."""
     cell, L, T, B, I, H = case
     wl = synth.Workload(name="transposed", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=synth.MODE_BF16,
-                        forget_bias=1.0, state_std=0.3)
+                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0)
     hi = runner.HostInputs(wl, with_state_grads=True)
     g = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING, chunk=2)
     compare(wl, g, run_oracle(hi))
@@ -293,3 +301,18 @@ def test_fused_pointwise_equals_separate_kernel(B):
         if b[k] is not None:
             np.testing.assert_array_equal(a[k], b[k], err_msg=k)
     compare(wl, a, run_oracle(hi))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("flags", [rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_TRANSPOSED, rnn.FLAG_FORCE_TRANSPOSED],
+                         ids=["row_major", "transposed"])
+def test_relu_forward_with_unshaped_weights(flags):
+    """ReLU RNN with the ordinary weight distribution (pre-activations
+    crossing 0 everywhere): the forward outputs still agree within the bf16
+    bound; gradients are compared only on margin-shaped inputs, where the
+    on/off decision cannot flip between precisions."""
+    wl = synth.Workload(name="relu", cell=3, layers=2, T=6, B=33, input=72, hidden=256, mode=synth.MODE_BF16,
+                        state_std=0.3)
+    hi = runner.HostInputs(wl)
+    g = run_gpu(wl, hi, flags=flags, train=False)
+    compare(wl, g, run_oracle(hi, train=False))

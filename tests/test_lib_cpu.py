@@ -38,7 +38,7 @@ def test_strerror(lib):
 
 def test_rejects_bad_descriptors(lib):
     ok = dict(cell=0, layers=1, T=4, B=2, input=64, hidden=64, mode=1)
-    for bad in [dict(cell=3), dict(layers=0), dict(T=0), dict(B=0), dict(hidden=0), dict(mode=2)]:
+    for bad in [dict(cell=4), dict(cell=-1), dict(layers=0), dict(T=0), dict(B=0), dict(hidden=0), dict(mode=2)]:
         d = dict(ok, **bad)
         with pytest.raises(rnn.RnnError) as e:
             rnn.RNN(**d)
@@ -133,6 +133,8 @@ def test_transposed_step_plan(lib):
     assert "transposed=1" in rnn.RNN(0, 2, 10, 32, 2048, 2048, 1).describe()
     assert "transposed=1" in rnn.RNN(2, 2, 10, 16, 2048, 2048, 1).describe()    # tanh from H=2048
     assert "transposed=0" in rnn.RNN(2, 2, 10, 256, 1024, 1024, 1).describe()
+    assert "transposed=1" in rnn.RNN(3, 2, 10, 64, 2048, 2048, 1).describe()    # ReLU RNN like tanh
+    assert "recurrence=persistent" in rnn.RNN(3, 1, 10, 4, 64, 1024, 1).describe()
     for bad in [dict(cell=1, B=9, H=256, mode=1), dict(cell=0, B=300, H=256, mode=1), dict(cell=0, B=9, H=256, mode=0)]:
         with pytest.raises(rnn.RnnError):
             rnn.RNN(bad["cell"], 1, 3, bad["B"], 64, bad["H"], bad["mode"], flags=rnn.FLAG_FORCE_TRANSPOSED)
