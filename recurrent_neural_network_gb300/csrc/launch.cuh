@@ -137,7 +137,10 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   // partials go through global memory.
   g.cluster = (cluster_splitk && g.splits > 1 && g.splits <= 8 && BN % (16 * g.splits) == 0) ? g.splits : 1;
   g.mcast = g.cluster > 1 ? 1 : mcast;
-  g.nfast = g.mcast > 1 ? 1 : 0;
+  // tile order: run along the dimension with fewer tiles first, so that the
+  // CTAs in flight at any time share operand slabs of the other dimension
+  // (for the deep-K products this keeps the slabs they stream in L2)
+  g.nfast = (g.mcast > 1 || g.n_tiles < g.m_tiles) ? 1 : 0;
   constexpr int smem = tce::smem_bytes<BN, STAGES>();
   auto kern = tc_gemm_kernel<BN, STAGES, Epi>;
   static bool attr = false;
@@ -198,7 +201,7 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   g.err = L.err;
   g.cluster = g.splits;
   g.mcast = 1;
-  g.nfast = 0;
+  g.nfast = g.n_tiles < g.m_tiles ? 1 : 0;  // as in launch_tc
   constexpr int smem = tce2::smem_bytes<BN, STAGES>();
   auto kern = tc_gemm2_kernel<BN, STAGES, Epi>;
   static bool attr = false;
