@@ -50,6 +50,11 @@ def _load():
         lib.rnn_ref_fwd.restype = ci
         lib.rnn_ref_bwd.argtypes = [ci] * 6 + [dp] * 11
         lib.rnn_ref_bwd.restype = ci
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.rnn_ref_fwd_len.argtypes = [ci] * 6 + [ip] + [dp] * 7
+        lib.rnn_ref_fwd_len.restype = ci
+        lib.rnn_ref_bwd_len.argtypes = [ci] * 6 + [ip] + [dp] * 11
+        lib.rnn_ref_bwd_len.restype = ci
         lib.rnn_ref_threads.restype = ci
         _lib = lib
     return _lib
@@ -79,8 +84,23 @@ def weight_count(cell, L, I, H):
     return sum(G * H * ((I if l == 0 else H) + H) + 2 * G * H for l in range(L))
 
 
-def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None):
-    """Forward pass. Returns (y[T][B][H], hT[L][B][H], cT[L][B][H] or None)."""
+def _lens(lens, T, B):
+    if lens is None:
+        return None
+    a = np.ascontiguousarray(lens, dtype=np.int32)
+    assert a.shape == (B,)
+    return a
+
+
+def _ip(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None, lens=None):
+    """Forward pass. Returns (y[T][B][H], hT[L][B][H], cT[L][B][H] or None).
+    lens[B] (optional): per-sequence lengths; later outputs are 0 and hT / cT
+    are each sequence's state after its own last step."""
+    lens = _lens(lens, T, B)
     x = _c(x, (T, B, I))
     w = _c(w, (weight_count(cell, L, I, H),))
     h0 = _c(h0, (L, B, H))
@@ -88,14 +108,16 @@ def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None):
     y = np.zeros((T, B, H))
     hT = np.zeros((L, B, H))
     cT = np.zeros((L, B, H)) if cell == 0 else None
-    rc = _load().rnn_ref_fwd(cell, L, T, B, I, H, _p(x), _p(h0), _p(c0), _p(w), _p(y), _p(hT), _p(cT))
+    rc = _load().rnn_ref_fwd_len(cell, L, T, B, I, H, _ip(lens), _p(x), _p(h0), _p(c0), _p(w), _p(y), _p(hT),
+                                 _p(cT))
     if rc != 0:
         raise ValueError(f"rnn_ref_fwd rejected its arguments ({rc})")
     return y, hT, cT
 
 
-def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None):
+def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None, lens=None):
     """Backward pass. Returns (dx[T][B][I], dh0[L][B][H], dc0 or None, dw like w)."""
+    lens = _lens(lens, T, B)
     x = _c(x, (T, B, I))
     w = _c(w, (weight_count(cell, L, I, H),))
     dy = _c(dy, (T, B, H))
@@ -107,8 +129,8 @@ def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None):
     dh0 = np.zeros((L, B, H))
     dc0 = np.zeros((L, B, H)) if cell == 0 else None
     dw = np.zeros_like(w)
-    rc = _load().rnn_ref_bwd(cell, L, T, B, I, H, _p(x), _p(h0), _p(c0), _p(w), _p(dy), _p(dhT),
-                             _p(dcT), _p(dx), _p(dh0), _p(dc0), _p(dw))
+    rc = _load().rnn_ref_bwd_len(cell, L, T, B, I, H, _ip(lens), _p(x), _p(h0), _p(c0), _p(w), _p(dy), _p(dhT),
+                                 _p(dcT), _p(dx), _p(dh0), _p(dc0), _p(dw))
     if rc != 0:
         raise ValueError(f"rnn_ref_bwd rejected its arguments ({rc})")
     return dx, dh0, dc0, dw

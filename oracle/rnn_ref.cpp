@@ -14,6 +14,9 @@
 //        with x_* = W_x in + b_x, h_* = W_h h + b_h;  h' = (1-z) n + z h
 //   RNN:                   h' = tanh(W_x in + b_x + W_h h + b_h)
 //   ReLU RNN:              h' = max(0, W_x in + b_x + W_h h + b_h)
+// Variable lengths (the *_len entry points): sequence b runs steps
+// 0 .. lens[b]-1; afterwards its outputs are 0 and its state is carried, so
+// hT / cT are its state after its own last step.
 // The backward pass is the exact gradient of
 //   L = sum(y*dy) + sum(hT*dhT) + sum(cT*dcT)
 // taken in reverse time, top layer first, one step and one layer at a time
@@ -74,8 +77,11 @@ bool bad_args(int cell, int L, int T, int B, int I, int H, const double* x, cons
 }
 
 // Forward over all layers; fills one Record per layer.
+// lens (nullable = all T): sequence b runs steps 0 .. lens[b]-1; at later
+// steps its state is carried unchanged (so slot T holds its final state) and
+// its outputs are zero.
 void forward(int cell, int L, int T, int B, int I, int H, const double* x, const double* h0,
-             const double* c0, const std::vector<LayerW>& W, std::vector<Record>& rec) {
+             const double* c0, const std::vector<LayerW>& W, std::vector<Record>& rec, const int* lens) {
   const int G = gates_of(cell);
   const int GH = G * H;
   rec.assign(L, Record());
@@ -115,6 +121,12 @@ void forward(int cell, int L, int T, int B, int I, int H, const double* x, const
           double* gt = R.g(t, b);
           double hprev = R.h(t, b)[j];
           double hnew;
+          if (lens && t >= lens[b]) {
+            // finished sequence: state carried, no gate values
+            R.h(t + 1, b)[j] = hprev;
+            if (cell == RNN_REF_LSTM) R.c(t + 1, b)[j] = R.c(t, b)[j];
+            continue;
+          }
           if (cell == RNN_REF_LSTM) {
             double i = sigm(sx[j] + sh[j]);
             double f = sigm(sx[H + j] + sh[H + j]);
@@ -146,6 +158,13 @@ void forward(int cell, int L, int T, int B, int I, int H, const double* x, const
   }
 }
 
+bool bad_lens(int T, int B, const int* lens) {
+  if (!lens) return false;
+  for (int b = 0; b < B; ++b)
+    if (lens[b] < 0 || lens[b] > T) return true;
+  return false;
+}
+
 }  // namespace
 
 extern "C" int rnn_ref_threads(void) {
@@ -156,15 +175,21 @@ extern "C" int rnn_ref_threads(void) {
 #endif
 }
 
-extern "C" int rnn_ref_fwd(int cell, int L, int T, int B, int I, int H, const double* x,
-                           const double* h0, const double* c0, const double* w, double* y,
-                           double* hT, double* cT) {
-  if (bad_args(cell, L, T, B, I, H, x, w)) return -1;
+extern "C" int rnn_ref_fwd_len(int cell, int L, int T, int B, int I, int H, const int* lens, const double* x,
+                               const double* h0, const double* c0, const double* w, double* y,
+                               double* hT, double* cT) {
+  if (bad_args(cell, L, T, B, I, H, x, w) || bad_lens(T, B, lens)) return -1;
   const int G = gates_of(cell);
   std::vector<LayerW> W = split_weights(w, G, L, I, H);
   std::vector<Record> rec;
-  forward(cell, L, T, B, I, H, x, h0, c0, W, rec);
-  if (y && T > 0) std::memcpy(y, rec[L - 1].h(1, 0), sizeof(double) * (size_t)T * B * H);
+  forward(cell, L, T, B, I, H, x, h0, c0, W, rec, lens);
+  if (y && T > 0) {
+    std::memcpy(y, rec[L - 1].h(1, 0), sizeof(double) * (size_t)T * B * H);
+    if (lens)
+      for (int t = 0; t < T; ++t)
+        for (int b = 0; b < B; ++b)
+          if (t >= lens[b]) std::memset(y + ((size_t)t * B + b) * H, 0, sizeof(double) * H);
+  }
   for (int l = 0; l < L; ++l) {
     if (hT) std::memcpy(hT + (size_t)l * B * H, rec[l].h(T, 0), sizeof(double) * B * H);
     if (cT && cell == RNN_REF_LSTM)
@@ -173,16 +198,22 @@ extern "C" int rnn_ref_fwd(int cell, int L, int T, int B, int I, int H, const do
   return 0;
 }
 
-extern "C" int rnn_ref_bwd(int cell, int L, int T, int B, int I, int H, const double* x,
-                           const double* h0, const double* c0, const double* w,
-                           const double* dy, const double* dhT, const double* dcT, double* dx,
-                           double* dh0, double* dc0, double* dw) {
-  if (bad_args(cell, L, T, B, I, H, x, w) || (!dy && T * B > 0)) return -1;
+extern "C" int rnn_ref_fwd(int cell, int L, int T, int B, int I, int H, const double* x,
+                           const double* h0, const double* c0, const double* w, double* y,
+                           double* hT, double* cT) {
+  return rnn_ref_fwd_len(cell, L, T, B, I, H, nullptr, x, h0, c0, w, y, hT, cT);
+}
+
+extern "C" int rnn_ref_bwd_len(int cell, int L, int T, int B, int I, int H, const int* lens, const double* x,
+                               const double* h0, const double* c0, const double* w,
+                               const double* dy, const double* dhT, const double* dcT, double* dx,
+                               double* dh0, double* dc0, double* dw) {
+  if (bad_args(cell, L, T, B, I, H, x, w) || (!dy && T * B > 0) || bad_lens(T, B, lens)) return -1;
   const int G = gates_of(cell);
   const int GH = G * H;
   std::vector<LayerW> W = split_weights(w, G, L, I, H);
   std::vector<Record> rec;
-  forward(cell, L, T, B, I, H, x, h0, c0, W, rec);
+  forward(cell, L, T, B, I, H, x, h0, c0, W, rec, lens);
 
   // gradient arriving at each layer's outputs h_t from above (dy for the top layer)
   std::vector<double> dabove(dy, dy + (size_t)T * B * H);
@@ -217,9 +248,17 @@ extern "C" int rnn_ref_bwd(int cell, int L, int T, int B, int I, int H, const do
       for (int b = 0; b < B; ++b) {
         for (int j = 0; j < H; ++j) {
           const double* gt = R.g(t, b);
-          double dh = dabove[((size_t)t * B + b) * H + j] + dh_rec[(size_t)b * H + j];
           double* gx = &dGx[(size_t)b * GH];
           double* gh = &dGh[(size_t)b * GH];
+          if (lens && t >= lens[b]) {
+            // finished sequence: the step is the identity on the state and its
+            // output is the constant 0, so the state gradient passes through
+            for (int q = 0; q < G; ++q) gx[q * H + j] = gh[q * H + j] = 0.0;
+            dh_new[(size_t)b * H + j] = dh_rec[(size_t)b * H + j];
+            if (cell == RNN_REF_LSTM) dc_new[(size_t)b * H + j] = dc_rec[(size_t)b * H + j];
+            continue;
+          }
+          double dh = dabove[((size_t)t * B + b) * H + j] + dh_rec[(size_t)b * H + j];
           if (cell == RNN_REF_LSTM) {
             double i = gt[j], f = gt[H + j], g = gt[2 * H + j], o = gt[3 * H + j];
             double c = R.c(t + 1, b)[j], cp = R.c(t, b)[j];
@@ -308,4 +347,11 @@ extern "C" int rnn_ref_bwd(int cell, int L, int T, int B, int I, int H, const do
     }
   }
   return 0;
+}
+
+extern "C" int rnn_ref_bwd(int cell, int L, int T, int B, int I, int H, const double* x,
+                           const double* h0, const double* c0, const double* w,
+                           const double* dy, const double* dhT, const double* dcT, double* dx,
+                           double* dh0, double* dc0, double* dw) {
+  return rnn_ref_bwd_len(cell, L, T, B, I, H, nullptr, x, h0, c0, w, dy, dhT, dcT, dx, dh0, dc0, dw);
 }

@@ -41,6 +41,17 @@ int rnn_ref_bwd(int cell, int L, int T, int B, int I, int H,
 /* number of OpenMP threads the oracle runs on */
 int rnn_ref_threads(void);
 
+/* The same with per-sequence lengths lens[B] (0 <= lens[b] <= T; null = all T):
+ * sequence b runs steps 0 .. lens[b]-1, its later outputs are 0 and its state
+ * is carried unchanged, so hT / cT are its state after its own last step. */
+int rnn_ref_fwd_len(int cell, int L, int T, int B, int I, int H, const int* lens,
+                    const double* x, const double* h0, const double* c0, const double* w,
+                    double* y, double* hT, double* cT);
+int rnn_ref_bwd_len(int cell, int L, int T, int B, int I, int H, const int* lens,
+                    const double* x, const double* h0, const double* c0, const double* w,
+                    const double* dy, const double* dhT, const double* dcT,
+                    double* dx, double* dh0, double* dc0, double* dw);
+
 #ifdef __cplusplus
 }
 #endif

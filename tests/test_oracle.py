@@ -353,3 +353,73 @@ def test_oracle_matches_stored_fixture(name):
     now = make_golden.compute(sh["cell"], sh["L"], sh["T"], sh["B"], sh["I"], sh["H"])
     for k, v in rec["values"].items():
         np.testing.assert_allclose(now[k], v, rtol=1e-12, atol=1e-14, err_msg=k)
+
+
+# ---------------------------------------------------------------- variable lengths
+
+LENS_CASES = [(0, [3, 1, 4, 2]), (1, [4, 4, 2, 1]), (2, [1, 3, 2, 4]), (3, [2, 4, 1, 3])]
+
+
+@pytest.mark.parametrize("cell,lens", LENS_CASES, ids=["lstm", "gru", "tanh", "relu"])
+def test_variable_lengths_equal_separate_truncated_runs(cell, lens):
+    """A batch of sequences of different lengths equals running each sequence
+    alone for its own number of steps: outputs (zero past the end), final
+    states, data gradients, and weight gradients summed over the sequences."""
+    L, T, B, I, H = 2, 4, 4, 3, 5
+    w, x, h0, c0, dy, dhT, dcT = rand_case(cell, L, T, B, I, H, seed=41 + cell)
+    y, hT, cT = oracle.fwd(cell, L, T, B, I, H, x, w, h0=h0, c0=c0, lens=lens)
+    dx, dh0, dc0, dw = oracle.bwd(cell, L, T, B, I, H, x, w, dy, h0=h0, c0=c0, dhT=dhT, dcT=dcT, lens=lens)
+    dw_sum = np.zeros_like(dw)
+    for b, n in enumerate(lens):
+        s = slice(b, b + 1)
+        cb = c0[:, s] if cell == 0 else None
+        yb, hb, cTb = oracle.fwd(cell, L, n, 1, I, H, x[:n, s], w, h0=h0[:, s], c0=cb)
+        np.testing.assert_allclose(y[:n, s], yb, rtol=1e-13, atol=1e-15)
+        assert not y[n:, b].any()
+        np.testing.assert_allclose(hT[:, s], hb, rtol=1e-13, atol=1e-15)
+        if cell == 0:
+            np.testing.assert_allclose(cT[:, s], cTb, rtol=1e-13, atol=1e-15)
+        dxb, dh0b, dc0b, dwb = oracle.bwd(cell, L, n, 1, I, H, x[:n, s], w, dy[:n, s], h0=h0[:, s], c0=cb,
+                                          dhT=dhT[:, s], dcT=dcT[:, s] if cell == 0 else None)
+        np.testing.assert_allclose(dx[:n, s], dxb, rtol=1e-12, atol=1e-14)
+        assert not dx[n:, b].any()
+        np.testing.assert_allclose(dh0[:, s], dh0b, rtol=1e-12, atol=1e-14)
+        if cell == 0:
+            np.testing.assert_allclose(dc0[:, s], dc0b, rtol=1e-12, atol=1e-14)
+        dw_sum += dwb
+    np.testing.assert_allclose(dw, dw_sum, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("cell,lens", LENS_CASES, ids=["lstm", "gru", "tanh", "relu"])
+def test_variable_lengths_match_torch_packed_sequences(cell, lens):
+    """PyTorch float64 on a packed batch (pack_padded_sequence) with autograd."""
+    L, T, B, I, H = 2, 4, 4, 3, 5
+    w, x, h0, c0, dy, dhT, dcT = rand_case(cell, L, T, B, I, H, seed=51 + cell)
+    y, hT, cT = oracle.fwd(cell, L, T, B, I, H, x, w, h0=h0, c0=c0, lens=lens)
+    dx, dh0, dc0, dw = oracle.bwd(cell, L, T, B, I, H, x, w, dy, h0=h0, c0=c0, dhT=dhT, dcT=dcT, lens=lens)
+    m = torch_model(cell, L, I, H, w)
+    xt = torch.tensor(x, requires_grad=True)
+    h0t = torch.tensor(h0, requires_grad=True)
+    c0t = torch.tensor(c0, requires_grad=True)
+    packed = torch.nn.utils.rnn.pack_padded_sequence(xt, torch.tensor(lens), enforce_sorted=False)
+    if cell == 0:
+        out, (hTt, cTt) = m(packed, (h0t, c0t))
+    else:
+        out, hTt = m(packed, h0t)
+    yt, _ = torch.nn.utils.rnn.pad_packed_sequence(out, total_length=T)
+    loss = (yt * torch.tensor(dy)).sum() + (hTt * torch.tensor(dhT)).sum()
+    if cell == 0:
+        loss = loss + (cTt * torch.tensor(dcT)).sum()
+    loss.backward()
+    np.testing.assert_allclose(y, yt.detach().numpy(), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(hT, hTt.detach().numpy(), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dh0, h0t.grad.numpy(), rtol=1e-10, atol=1e-12)
+    if cell == 0:
+        np.testing.assert_allclose(cT, cTt.detach().numpy(), rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(dc0, c0t.grad.numpy(), rtol=1e-10, atol=1e-12)
+    tw = []
+    for l in range(L):
+        for nm in ("weight_ih", "weight_hh", "bias_ih", "bias_hh"):
+            tw.append(getattr(m, f"{nm}_l{l}").grad.numpy().ravel())
+    np.testing.assert_allclose(dw, np.concatenate(tw), rtol=1e-10, atol=1e-12)
