@@ -134,6 +134,20 @@ RNN_API int rnn_get_sizes(rnn_handle_t h, size_t* user_weight_bytes, size_t* pac
  * Run once per weight update.  w_user: user layout in the mode's type. */
 RNN_API int rnn_pack_weights(rnn_handle_t h, const void* w_user, void* w_packed, cudaStream_t stream);
 
+/* Variable-length sequences (packed-sequence semantics) for later calls on
+ * this handle: lens[B] on the host, non-increasing (the batch sorted longest
+ * first), 1 <= lens[b] <= T; NULL = every sequence runs all T steps.
+ * Sequence b runs steps 0 .. lens[b]-1: y is 0 at its later steps, hT / cT
+ * receive its state after its own last step, its dy at later steps is
+ * ignored, dhT / dcT enter at its last step, and dx is 0 at later steps.
+ * Padding in x past a sequence's end must be finite (it meets zero gate
+ * gradients in the weight-gradient product).  At each step only the
+ * sequences still running are computed.  A handle that had planned the
+ * persistent recurrence switches to per-step launches; cached launch graphs
+ * are dropped.  Returns RNN_ERR_INVALID_ARG for unsorted or out-of-range
+ * lengths (nothing changes then). */
+RNN_API int rnn_set_lengths(rnn_handle_t h, const int* lens);
+
 /* Forward pass over all layers and timesteps.  Per layer l and step t:
  *   LSTM: a = W_x in_t + b_x + W_h h_{t-1} + b_h; i,f,o = sigmoid, g = tanh;
  *         c_t = f*c_{t-1} + i*g;  h_t = o*tanh(c_t)

@@ -126,9 +126,15 @@ struct rnn_s {
   // plan
   int chunk = 1, nch = 1, wavefront = 0, bwd_bn = 128, bwd_splits = 1;
   int persist = 0, persist_ctas = 0;  // forward recurrence kind: 1 = persistent (one launch per layer)
+  int persist_plan = 0;               // the kind the plan chose (variable lengths turn it off)
   int fwd_mcast = 4;  // forward-step clusters along N sharing h_{t-1} by TMA multicast
   int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
   int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
+  // variable lengths (rnn_set_lengths): Bt[t] = number of sequences still
+  // running at step t (the batch is sorted by non-increasing length, so the
+  // running ones are rows 0 .. Bt[t]-1); Bt[T] = 0
+  int varlen = 0;
+  std::vector<int> Bt;
   uint64_t limit_ns = 2000000000ull;
   // sizes (bytes)
   size_t user_w_bytes = 0, packed_bytes = 0, reserve_bytes = 0, ws_bytes = 0;
@@ -204,6 +210,7 @@ int plan_and_layout(rnn_s* h) {
                                      : (B <= 8 && H % 128 == 0 && H <= (d.cell == RNN_GRU ? 512 : d.cell == RNN_LSTM ? 1024 : 2048));
     if (fits) {
       h->persist = 1;
+      h->persist_plan = 1;
       h->persist_ctas = ctas;
     }
   }
@@ -539,6 +546,44 @@ int rnn_destroy(rnn_handle_t h) {
   return RNN_OK;
 }
 
+namespace {
+// drop every cached launch graph (the launch sequence changed)
+void clear_graphs(rnn_s* h) {
+  if (!h->graphs.empty()) cudaDeviceSynchronize();
+  for (auto& g : h->graphs) {
+    cudaGraphExecDestroy(g.exec);
+    for (auto& r : g.prof) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+  }
+  h->graphs.clear();
+  h->seen.clear();
+  h->no_graph.clear();
+}
+}  // namespace
+
+int rnn_set_lengths(rnn_handle_t h, const int* lens) {
+  if (!h) return RNN_ERR_INVALID_ARG;
+  const int T = h->d.T, B = h->d.B;
+  if (lens) {
+    for (int b = 0; b < B; ++b)
+      if (lens[b] < 1 || lens[b] > T || (b > 0 && lens[b] > lens[b - 1])) return RNN_ERR_INVALID_ARG;
+  }
+  clear_graphs(h);
+  h->varlen = (lens && lens[B - 1] < T) ? 1 : 0;
+  h->Bt.assign(T + 1, 0);
+  for (int t = 0; t < T; ++t) {
+    int n = 0;
+    while (n < B && (!lens || lens[n] > t)) ++n;
+    h->Bt[t] = n;
+  }
+  // the persistent recurrence runs all T steps of every sequence: step
+  // launches take over (the packing unit it was planned with serves them)
+  h->persist = h->varlen ? 0 : h->persist_plan;
+  return RNN_OK;
+}
+
 int rnn_get_sizes(rnn_handle_t h, size_t* user_weight_bytes, size_t* packed_weight_bytes, size_t* reserve_bytes,
                   size_t* workspace_bytes) {
   if (!h) return RNN_ERR_INVALID_ARG;
@@ -599,6 +644,15 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
     const char* PW = static_cast<const char*>(w_packed);
     (void)G;
 
+    if (h->varlen) {
+      // rows past a sequence's end are never written by the steps: y reads 0
+      // there, and the h sequences the weight gradients and the next layer
+      // read hold zeros instead of stale memory
+      RNN_TRY(cu(cudaMemsetAsync(y, 0, (size_t)T * BH * e, stream)));
+      for (int l = 0; l < L; ++l)
+        RNN_TRY(cu(cudaMemsetAsync(train ? R + h->rl[l].hseq : W + h->wl[l].hseq, 0, (size_t)(T + 1) * BH * e,
+                                   stream)));
+    }
     if (h->wavefront) RNN_TRY(fork_streams(h, stream));
     const int nd = h->wavefront ? (L + h->nch - 1) : 1;
     for (int dg = 0; dg < nd; ++dg) {
@@ -661,10 +715,13 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
             RNN_TRY(persist_fwd(Lk, d.cell, pa));
             continue;
           }
-          // recurrent steps of the chunk
+          // recurrent steps of the chunk (with variable lengths only the
+          // Bt[t] sequences still running, rows 0 .. Bt[t]-1)
           for (int t = t0; t < t1; ++t) {
+            const int Bs = h->varlen ? h->Bt[t] : B;
+            if (Bs == 0) continue;
             FwdStepArgs a;
-            a.B = B;
+            a.B = Bs;
             a.H = H;
             a.u = h->u;
             a.P = P + (size_t)t * BGH;
@@ -679,15 +736,26 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
             a.h_prev = hseq + (size_t)t * BH * e;
             a.h_out = hseq + (size_t)(t + 1) * BH * e;
             a.y = l == L - 1 ? static_cast<char*>(y) + (size_t)t * BH * e : nullptr;
-            a.hT = (t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
-            a.cT = (t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
+            a.hT = (!h->varlen && t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
+            a.cT = (!h->varlen && t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
             a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
             a.mcast = h->fwd_mcast;
-            Operand A{hseq + (size_t)t * BH * e, H, 0, B, H};
+            Operand A{hseq + (size_t)t * BH * e, H, 0, Bs, H};
             Operand Bw{PW + h->pl[l].wh, H, 0, GH, H, 1};
             Launch Lk = mk(h, s, ws, "fwd_step");
             if (h->tstep) RNN_TRY(fwd_step_t(Lk, d.cell, Bw, A, a));
             else RNN_TRY(fwd_step(Lk, mode, d.cell, A, Bw, a));
+            if (h->varlen) {
+              // sequences ending at step t (rows Bt[t+1] .. Bt[t]-1): final states
+              const int r0 = h->Bt[t + 1], nr = Bs - r0;
+              if (nr > 0 && hT)
+                RNN_TRY(cu(cudaMemcpyAsync(static_cast<char*>(hT) + ((size_t)l * BH + (size_t)r0 * H) * e,
+                                           static_cast<const char*>(a.h_out) + (size_t)r0 * H * e, (size_t)nr * H * e,
+                                           cudaMemcpyDeviceToDevice, s)));
+              if (nr > 0 && cT && lstm)
+                RNN_TRY(cu(cudaMemcpyAsync(cT + (size_t)l * BH + (size_t)r0 * H, a.c_out + (size_t)r0 * H,
+                                           (size_t)nr * H * 4, cudaMemcpyDeviceToDevice, s)));
+            }
           }
           if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + c], s)));
         }
@@ -720,6 +788,15 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
 
     for (int l = 0; l < L; ++l)
       RNN_TRY(cu(cudaMemsetAsync(W + h->wl[l].ctr, 0, (size_t)h->ctr_count * 4, stream)));
+    if (h->varlen) {
+      // gate gradients of finished sequences are never written: zero, so that
+      // the products that read every row (dx, dW, the next step) see zeros
+      for (int l = 0; l < L; ++l) {
+        RNN_TRY(cu(cudaMemsetAsync(R + h->rl[l].dgx, 0, (size_t)T * BGH * e, stream)));
+        if (h->rl[l].dgh != h->rl[l].dgx)
+          RNN_TRY(cu(cudaMemsetAsync(R + h->rl[l].dgh, 0, (size_t)T * BGH * e, stream)));
+      }
+    }
     if (h->wavefront) RNN_TRY(fork_streams(h, stream));
     const int nd = h->wavefront ? (L + h->nch - 1) : 1;
     for (int dg = 0; dg < nd; ++dg) {
@@ -763,44 +840,77 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
             return a;
           };
           Operand Bw{PW + h->pl[l].wh, H, 1, H, GH, 1};
+          // the arguments of args_for moved down by r0 batch rows
+          auto offset_rows = [&](BwdStepArgs x, int r0) {
+            x.gates += (size_t)r0 * GH;
+            if (x.c_s) x.c_s += (size_t)r0 * H;
+            if (x.c_sm1) x.c_sm1 += (size_t)r0 * H;
+            if (x.hn_s) x.hn_s += (size_t)r0 * H;
+            if (x.h_sm1) x.h_sm1 = static_cast<const char*>(x.h_sm1) + (size_t)r0 * H * e;
+            x.dy = static_cast<const char*>(x.dy) + (size_t)r0 * H * dy_es;
+            x.carry += (size_t)r0 * H;
+            x.dGx = static_cast<char*>(x.dGx) + (size_t)r0 * GH * e;
+            x.dGh = static_cast<char*>(x.dGh) + (size_t)r0 * GH * e;
+            return x;
+          };
+          auto point_args = [&](const BwdStepArgs& x, int st, int r0, int rows) {
+            PointVArgs pv{};
+            pv.B = rows;
+            pv.H = H;
+            pv.dy = x.dy;
+            pv.dy_f32 = x.dy_f32;
+            pv.gates = x.gates;
+            pv.c_s = x.c_s;
+            pv.c_sm1 = x.c_sm1;
+            pv.carry = x.carry;
+            pv.dc0 = (st == 0 && dc0 && lstm) ? dc0 + l * BH + (size_t)r0 * H : nullptr;
+            pv.dGx = x.dGx;
+            return pv;
+          };
           for (int st = t1 - 1; st >= t0; --st) {
+            // rows 0 .. Bn-1 were running at st+1 (their dh has a recurrent
+            // part); rows Bn .. Bs-1 end at st (their dh starts from dhT)
+            const int Bs = h->varlen ? h->Bt[st] : B;
+            const int Bn = st == T - 1 ? 0 : (h->varlen ? h->Bt[st + 1] : B);
+            const char* dhTl = dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr;
             BwdStepArgs a = args_for(st);
-            if (h->tstep) {
-              // transposed: the product writes dh_s, a pointwise kernel follows
-              PointVArgs pv{};
-              pv.B = B;
-              pv.H = H;
-              pv.dy = a.dy;
-              pv.dy_f32 = a.dy_f32;
-              pv.gates = a.gates;
-              pv.c_s = a.c_s;
-              pv.c_sm1 = a.c_sm1;
-              pv.carry = a.carry;
-              pv.dc0 = (st == 0 && dc0 && lstm) ? dc0 + l * BH : nullptr;
-              pv.dGx = a.dGx;
-              if (st == T - 1) {
-                pv.dh_init = dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr;
-              } else {
-                float* dhb = reinterpret_cast<float*>(W + h->wl[l].dh);
-                Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
-                Launch Lk = mk(h, s, ws, "bwd_step");
-                RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, dhb, nullptr, 0,
-                                 reinterpret_cast<float*>(W + h->wl[l].part), a.gates, a.c_s, a.c_sm1,
-                                 h->bwd_fuse ? &pv : nullptr));
-                if (h->bwd_fuse) continue;  // the product ran the pointwise step too
-                pv.dh = dhb;
-              }
-              Launch Lp = mk(h, s, ws, "bwd_point");
-              RNN_TRY(bwd_point_v(Lp, d.cell, pv));
-              continue;
-            }
-            if (st == T - 1) {
-              Launch Lk = mk(h, s, ws, "bwd_point");
-              RNN_TRY(bwd_point(Lk, mode, d.cell, a, dhT ? static_cast<const char*>(dhT) + l * BH * e : nullptr));
-            } else {
-              Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, B, GH};
+            if (Bn > 0) {
+              a.B = Bn;
+              Operand A{R + h->rl[l].dgh + (size_t)(st + 1) * BGH * e, GH, 0, Bn, GH};
               Launch Lk = mk(h, s, ws, "bwd_step");
-              RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+              if (h->tstep) {
+                // transposed: the product writes dh_s (or runs the pointwise
+                // step in its epilogue), else a pointwise kernel follows
+                PointVArgs pv = point_args(a, st, 0, Bn);
+                const int bnn = Bn > 128 ? 256 : Bn > 64 ? 128 : 64;
+                int sp = h->bwd_splits;
+                while (sp > 1 && bnn % (16 * sp)) sp /= 2;
+                const bool fuse = h->bwd_fuse && bnn == 256 && sp == 4;
+                float* dhb = reinterpret_cast<float*>(W + h->wl[l].dh);
+                RNN_TRY(bwd_dh_t(Lk, Bw, A, Bn, H, h->G, bnn, sp, dhb, nullptr, 0,
+                                 reinterpret_cast<float*>(W + h->wl[l].part), a.gates, a.c_s, a.c_sm1,
+                                 fuse ? &pv : nullptr));
+                if (!fuse) {
+                  pv.dh = dhb;
+                  Launch Lp = mk(h, s, ws, "bwd_point");
+                  RNN_TRY(bwd_point_v(Lp, d.cell, pv));
+                }
+              } else {
+                RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+              }
+            }
+            if (Bs > Bn) {
+              BwdStepArgs ar = offset_rows(args_for(st), Bn);
+              ar.B = Bs - Bn;
+              const char* dh_init = dhTl ? dhTl + (size_t)Bn * H * e : nullptr;
+              Launch Lp = mk(h, s, ws, "bwd_point");
+              if (h->tstep) {
+                PointVArgs pv = point_args(ar, st, Bn, Bs - Bn);
+                pv.dh_init = dh_init;
+                RNN_TRY(bwd_point_v(Lp, d.cell, pv));
+              } else {
+                RNN_TRY(bwd_point(Lp, mode, d.cell, ar, dh_init));
+              }
             }
           }
           if (t0 == 0 && (dh0 || (dc0 && lstm))) {

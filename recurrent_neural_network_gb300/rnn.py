@@ -34,7 +34,7 @@ FLAG_NO_FUSED_POINT = 0x800
 # every symbol include/rnn.h declares
 SYMBOLS = ["rnn_create", "rnn_destroy", "rnn_get_sizes", "rnn_pack_weights", "rnn_fwd", "rnn_bwd_data",
            "rnn_bwd_weights", "rnn_sync_status", "rnn_strerror", "rnn_describe", "rnn_launch_count",
-           "rnn_profile_query", "rnn_gemm_bf16", "rnn_bias_grad_static"]
+           "rnn_profile_query", "rnn_gemm_bf16", "rnn_bias_grad_static", "rnn_set_lengths"]
 BIAS_STATIC_FLOATS = 1 << 20
 
 
@@ -81,6 +81,7 @@ def load(path: str = LIB_PATH):
     lib.rnn_gemm_bf16.argtypes = [ci, ci, ci, vp, ctypes.c_longlong, ci, vp, ctypes.c_longlong, ci, vp,
                                   ctypes.c_longlong, vp, ci, vp]
     lib.rnn_bias_grad_static.argtypes = [H, vp, vp, ci, vp]
+    lib.rnn_set_lengths.argtypes = [H, ctypes.POINTER(ci)]
     for name in SYMBOLS:
         if name != "rnn_strerror" and name != "rnn_launch_count":
             getattr(lib, name).restype = ci
@@ -171,6 +172,17 @@ class RNN:
     def bwd_weights(self, x, reserve, dw, ws, h0=None, accumulate=False, stream=None):
         check(self.lib.rnn_bwd_weights(self.h, _ptr(x), _ptr(h0), _ptr(reserve), _ptr(dw), int(accumulate), _ptr(ws),
                                        _stream(stream)), "rnn_bwd_weights")
+
+    def set_lengths(self, lens=None):
+        """Per-sequence lengths (non-increasing, 1..T) for later calls; None = all T."""
+        if lens is None:
+            check(self.lib.rnn_set_lengths(self.h, None), "rnn_set_lengths")
+            return
+        lens = [int(v) for v in lens]
+        if len(lens) != self.B:
+            raise ValueError(f"set_lengths: {len(lens)} lengths for a batch of {self.B}")
+        arr = (ctypes.c_int * len(lens))(*lens)
+        check(self.lib.rnn_set_lengths(self.h, arr), "rnn_set_lengths")
 
     def bias_grad_static(self, reserve, dw, accumulate=False, stream=None):
         """Bias gradients into dw using the library's fixed scratch array (no workspace)."""

@@ -23,19 +23,21 @@ BF16_MAX_ABS = 3e-2
 BF16_REL_L2 = 2e-2
 
 
-def run_oracle(hi: runner.HostInputs, train=True):
+def run_oracle(hi: runner.HostInputs, train=True, lens=None):
     w = hi.wl
-    y, hT, cT = oracle.fwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0)
+    y, hT, cT = oracle.fwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0, lens=lens)
     out = dict(y=y, hT=hT, cT=cT)
     if train:
         dx, dh0, dc0, dw = oracle.bwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, hi.dy, h0=hi.h0,
-                                      c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT)
+                                      c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT, lens=lens)
         out.update(dx=dx, dh0=dh0, dc0=dc0, dw=dw)
     return out
 
 
-def run_gpu(wl, hi, flags=0, chunk=0, train=None, timeout_ns=0, repeat=1):
+def run_gpu(wl, hi, flags=0, chunk=0, train=None, timeout_ns=0, repeat=1, lens=None):
     r = runner.Runner(wl, flags=flags, chunk=chunk, timeout_ns=timeout_ns)
+    if lens is not None:
+        r.r.set_lengths(lens)
     r.upload(hi)
     train = wl.training if train is None else train
     for _ in range(repeat):

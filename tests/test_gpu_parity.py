@@ -316,3 +316,47 @@ def test_relu_forward_with_unshaped_weights(flags):
     hi = runner.HostInputs(wl)
     g = run_gpu(wl, hi, flags=flags, train=False)
     compare(wl, g, run_oracle(hi, train=False))
+
+
+
+# ---------------------------------------------------------------- variable lengths
+
+VARLEN = [
+    # cell, mode, flags, (L, T, B, I, H)
+    (0, synth.MODE_BF16, 0, (2, 7, 9, 72, 128)),
+    (0, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING, (2, 7, 9, 72, 256)),
+    (0, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING, (2, 6, 200, 64, 256)),
+    (1, synth.MODE_BF16, 0, (2, 7, 9, 72, 128)),
+    (2, synth.MODE_BF16, 0, (2, 7, 9, 72, 128)),
+    (3, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING, (2, 7, 9, 72, 256)),
+    (0, synth.MODE_FP32, 0, (2, 7, 5, 40, 64)),
+    (1, synth.MODE_FP32, 0, (2, 7, 5, 40, 64)),
+    (0, synth.MODE_BF16, 0, (1, 9, 4, 64, 256)),   # planned persistent: switches to step launches
+]
+
+
+def _lengths(T, B, seed):
+    rng = np.random.default_rng(seed)
+    lens = np.sort(rng.integers(1, T + 1, size=B))[::-1].copy()
+    lens[0] = T
+    return [int(v) for v in lens]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", VARLEN, ids=lambda c: "c%d_m%d_f%x_L%d_T%d_B%d_I%d_H%d" % (c[0], c[1], c[2], *c[3]))
+def test_variable_lengths(case):
+    """Sequences of different lengths (sorted longest first) against the
+    oracle with the same lengths: outputs zero past each end, final states
+    after each sequence's own last step, every gradient; twice through the
+    same handle (direct call, then the captured graph)."""
+    cell, mode, flags, (L, T, B, I, H) = case
+    wl = synth.Workload(name="varlen", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
+                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    lens = _lengths(T, B, seed=B + T + cell)
+    g = run_gpu(wl, hi, flags=flags, chunk=2, lens=lens, repeat=2)
+    o = run_oracle(hi, lens=lens)
+    compare(wl, g, o)
+    for b, n in enumerate(lens):
+        assert not np.any(g["y"][n:, b]), b
+        assert not np.any(g["dx"][n:, b]), b

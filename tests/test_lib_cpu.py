@@ -149,3 +149,23 @@ def test_transposed_step_plan(lib):
                 per = -(-kb // sp)
                 assert bn >= min(256, B) and sp & (sp - 1) == 0 and -(-kb // per) == sp and bn % (16 * sp) == 0 \
                     and sp <= 8, (cell, H, B, bn, sp)
+
+
+def test_set_lengths_validation_and_plan(lib):
+    """Lengths must be 1..T and non-increasing; a handle planned with the
+    persistent recurrence switches to step launches once lengths differ."""
+    r = rnn.RNN(0, 1, 10, 4, 64, 1024, 1)
+    assert "recurrence=persistent" in r.describe()
+    with pytest.raises(ValueError):
+        r.set_lengths([10, 9, 8])
+    for bad in ([10, 11, 3, 1], [0, 0, 0, 0], [3, 5, 5, 1]):
+        with pytest.raises(rnn.RnnError) as e:
+            r.set_lengths(bad)
+        assert e.value.code == -1
+    assert "recurrence=persistent" in r.describe()
+    r.set_lengths([10, 10, 10, 10])            # all full: nothing changes
+    assert "recurrence=persistent" in r.describe()
+    r.set_lengths([10, 7, 7, 2])
+    assert "recurrence=streaming" in r.describe()
+    r.set_lengths(None)
+    assert "recurrence=persistent" in r.describe()
