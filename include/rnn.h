@@ -94,6 +94,9 @@ enum {
                                             or H >= 512 and 64 <= B <= 128; simple RNN: H >= 2048) */
 #define RNN_FLAG_NO_FUSED_POINT 0x800u  /* transposed LSTM steps: run the pointwise BPTT step as its own
                                            kernel after each product instead of inside its epilogue */
+#define RNN_FLAG_NO_PERSIST_CLUSTER 0x1000u /* persistent recurrence: hand h_t over through per-step
+                                               arrival counters and L2 reads instead of tagged words
+                                               gathered per thread-block cluster */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */

@@ -127,6 +127,7 @@ struct rnn_s {
   int chunk = 1, nch = 1, wavefront = 0, bwd_bn = 128, bwd_splits = 1;
   int persist = 0, persist_ctas = 0;  // forward recurrence kind: 1 = persistent (one launch per layer)
   int persist_plan = 0;               // the kind the plan chose (variable lengths turn it off)
+  int persist_cl = 0;                 // persistent hand-off: cluster size of the tagged-word exchange, 0 = counters
   int fwd_mcast = 4;  // forward-step clusters along N sharing h_{t-1} by TMA multicast
   int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
   int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
@@ -150,6 +151,7 @@ struct rnn_s {
   std::vector<UL> ul;
   size_t ws_err = 0;
   size_t ws_arrive = 0;  // persistent recurrence: per-timestep arrival counters
+  size_t ws_hx = 0;      // persistent recurrence, cluster exchange: tagged h words [2][B*H/2]
   int ctr_count = 0;
   // streams and events (created on first use)
   std::vector<cudaStream_t> streams;
@@ -206,12 +208,14 @@ int plan_and_layout(rnn_s* h) {
   // layer); it runs layer after layer, so it replaces the wavefront.
   if (d.mode == RNN_MODE_BF16 && !(d.flags & RNN_FLAG_FORCE_STREAMING)) {
     int ctas = 0;
-    const bool fits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &ctas) == RNN_OK
+    int cl = 8;  // without a device: as measured on the target (clusters of 8 co-reside)
+    const bool fits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &ctas, &cl) == RNN_OK
                                      : (B <= 8 && H % 128 == 0 && H <= (d.cell == RNN_GRU ? 512 : d.cell == RNN_LSTM ? 1024 : 2048));
     if (fits) {
       h->persist = 1;
       h->persist_plan = 1;
       h->persist_ctas = ctas;
+      h->persist_cl = (d.flags & RNN_FLAG_NO_PERSIST_CLUSTER) ? 0 : cl;
     }
   }
   if ((d.flags & RNN_FLAG_FORCE_PERSISTENT) && !h->persist) return RNN_ERR_UNSUPPORTED;
@@ -312,6 +316,7 @@ int plan_and_layout(rnn_s* h) {
   cur = 0;
   h->ws_err = take(cur, 256);
   h->ws_arrive = take(cur, (size_t)T * 4);
+  h->ws_hx = h->persist_plan ? take(cur, (size_t)8 * B * H) : 0;
   h->bias_slices = std::max(1, std::min(64, (T * B + 255) / 256));
   h->ws_bias = take(cur, (size_t)h->bias_slices * GH * 4);
   for (int l = 0; l < L; ++l) {
@@ -596,13 +601,14 @@ int rnn_get_sizes(rnn_handle_t h, size_t* user_weight_bytes, size_t* packed_weig
 
 int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   if (!h || !buf || len == 0) return RNN_ERR_INVALID_ARG;
-  const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : "tanh";
+  const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : h->d.cell == RNN_RELU ? "relu" : "tanh";
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
-           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d transposed=%d fused_point=%d",
+           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d transposed=%d fused_point=%d "
+           "persist_cluster=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
            h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch,
-           h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms, h->tstep, h->bwd_fuse);
+           h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms, h->tstep, h->bwd_fuse, h->persist ? h->persist_cl : 0);
   return RNN_OK;
 }
 
@@ -690,9 +696,12 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
           // persistent recurrence: all T steps of the layer in one launch
           if (h->persist) {
             unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
-            RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
+            if (h->persist_cl) RNN_TRY(cu(cudaMemsetAsync(W + h->ws_hx, 0, (size_t)8 * B * H, s)));
+            else RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
             PersistArgs pa{};
             pa.arrive = arrive;
+            pa.cluster = h->persist_cl;
+            pa.hx = reinterpret_cast<uint64_t*>(W + h->ws_hx);
             pa.T = T;
             pa.B = B;
             pa.H = H;

@@ -153,6 +153,8 @@ struct PersistArgs {
   float* hn_out;            // GRU training [T][B][H] or null
   __nv_bfloat16* hseq;      // [T+1][B][H]; slot 0 = h0
   unsigned int* arrive;     // [T] arrival counters, zero before the launch
+  int cluster;              // > 0: cluster-exchange hand-off with clusters of this size
+  uint64_t* hx;             // cluster exchange: [2][B*H/2] tagged words, zero before the launch
   __nv_bfloat16* y;         // [T][B][H] or null
   __nv_bfloat16* hT;        // [B][H] or null
   float* cT;                // [B][H] or null
@@ -161,8 +163,10 @@ struct PersistArgs {
   int test_skip_publish;    // test hook: CTA 0 never publishes h_0
 };
 // RNN_OK if the persistent recurrence supports (cell, H, B) and all its CTAs
-// fit on the device at once; *ctas receives the grid size.
-int persist_check(int cell, int H, int B, int num_sms, int* ctas);
+// fit on the device at once; *ctas receives the grid size and *cluster (if
+// not null) the largest cluster size (8, 4 or 2) whose clusters all fit at
+// once for the cluster-exchange hand-off, 0 if none.
+int persist_check(int cell, int H, int B, int num_sms, int* ctas, int* cluster = nullptr);
 // all T timesteps of one layer in one cooperative launch (bf16 storage only)
 int persist_fwd(const Launch& L, int cell, const PersistArgs& a);
 

@@ -10,19 +10,33 @@
 // across 8 warps, reduced through shared memory), applies the cell update to
 // its units and publishes its part of h_t.
 //
-// Step hand-off: after its h_t stores a CTA makes one release arrival on the
-// step's counter (one counter per timestep, zeroed before the launch); one
-// thread per CTA polls the counter of the previous step until every CTA has
-// arrived, then the CTA reads h_{t-1} once through L2.  Only 1 thread per CTA
-// spins, on one word, so the polling does not crowd the L2 slices that serve
-// the h data to every SM.  Every wait is bounded (globaltimer); on timeout the
-// CTA records DEV_TIMEOUT_STEP in the error word and leaves.  Co-residency of
-// all CTAs is guaranteed by a cooperative launch.
+// Step hand-off, two variants.
+//
+// Cluster exchange (default where clusters of 2-8 CTAs co-reside): each CTA
+// writes its slice of h_t as tagged 8-byte words (two bf16 values and the
+// step number + 1) into a global ping-pong buffer; a word carries its own
+// validity, so the producer needs no release fence.  The CTAs of a cluster
+// split the words of h_{t-1} among them: each polls its share until the tags
+// match, scatters the values into the h_{t-1} buffer in the shared memory of
+// every CTA of the cluster, and one cluster barrier later every CTA holds
+// all of h_{t-1} on chip.  Each word is polled by one CTA per cluster, not by
+// every CTA, which keeps the polling off the L2 slices' critical path.
+//
+// Counter (fallback): after its h_t stores a CTA makes one release arrival on
+// the step's counter (one counter per timestep, zeroed before the launch);
+// one thread per CTA polls the counter of the previous step until every CTA
+// has arrived, then the CTA reads h_{t-1} once through L2.
+//
+// Every wait is bounded (globaltimer); on timeout the CTA records
+// DEV_TIMEOUT_STEP in the error word and leaves (in the cluster variant the
+// whole cluster leaves together, after the step's cluster barrier).
+// Co-residency of all CTAs is guaranteed by a cooperative launch.
 #include <cuda_bf16.h>
 
 #include "../../include/rnn.h"
 #include "common.cuh"
 #include "launchers.h"
+#include "tc.cuh"
 
 namespace rnn {
 
@@ -47,17 +61,41 @@ __device__ __forceinline__ void red_release_add(unsigned int* p, unsigned int v)
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// every thread of every CTA of the cluster (threads may arrive diverged)
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ unsigned short bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-template <int CELL, int MT, int KT>
+// most tagged words one thread polls per step (the cluster size is chosen so
+// that B*H/2 words over the cluster's CTAs of 256 threads stay within it)
+constexpr int kMaxWords = 4;
+
+template <int CELL, int MT, int KT, bool XCL>
 __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a) {
   constexpr int G = CellInfo<CELL>::G;
   constexpr int ROWS = MT * 16;  // = G * uc
   __shared__ float part[8][ROWS][8];
   __shared__ float sums[ROWS][8];
   __shared__ int abort_flag;
+  __shared__ int abort_x[2];  // cluster exchange: set in every CTA of the cluster by one that gave up
+  // cluster exchange: h_{t-1} ping-pong [2][B][H + 8] bf16 (rows padded so
+  // that the eight batch rows of a fragment load fall in distinct banks)
+  extern __shared__ __align__(16) unsigned char hbuf[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int uc = ROWS / G;
   const int H = a.H, B = a.B, GH = G * H;
@@ -100,6 +138,38 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
     if (CELL == GRU) h_prev = __bfloat162float(a.hseq[(size_t)bq * H + j]);
   }
   const float bhn = (CELL == GRU && pair) ? a.bias_hn[j] : 0.f;
+  const int HP2 = H / 2 + 4;            // words per padded h row
+  const int NW = (H / 2) * B;           // tagged words of h per step
+  const int WS = (uc * B) / 2;          // of which this CTA produces
+  uint32_t crank = 0, csize = 1;
+  // this thread's share of the tagged words of a step: w0 + 256 i, i < nmine,
+  // and where word i lands in an h buffer (word w of CTA c holds units jj,
+  // jj+1 of batch row bq)
+  int w0 = 0, nmine = 0;
+  uint32_t offw[kMaxWords];
+  if constexpr (XCL) {
+    crank = tc::cluster_ctarank();
+    csize = (uint32_t)a.cluster;
+    const int per = NW / (int)csize;
+    w0 = (int)crank * per + threadIdx.x;
+    nmine = per > (int)threadIdx.x ? min(kMaxWords, (per - (int)threadIdx.x + 255) / 256) : 0;
+#pragma unroll
+    for (int i = 0; i < kMaxWords; ++i) {
+      const int w = w0 + i * 256;
+      const int c = w / WS, q0 = 2 * (w - c * WS);
+      const int bq = q0 / uc, jj = c * uc + (q0 - bq * uc);
+      offw[i] = (uint32_t)(bq * HP2 * 4 + jj * 2);
+    }
+    const uint32_t* h0w = reinterpret_cast<const uint32_t*>(a.hseq);
+    uint32_t* hw = reinterpret_cast<uint32_t*>(hbuf);
+    for (int i = threadIdx.x; i < NW; i += 256) {
+      const int b = i / (H / 2);
+      hw[b * HP2 + (i - b * (H / 2))] = h0w[i];
+    }
+    if (threadIdx.x < 2) abort_x[threadIdx.x] = 0;
+    // peers write into this CTA's buffers and flags only after this point
+    cluster_barrier();
+  }
   __syncthreads();
 
   const int nb = lane >> 2;  // batch column of this lane's B fragment
@@ -112,9 +182,49 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
 #pragma unroll
       for (int g = 0; g < G; ++g) pv[g] = prow[pcol[g]];
     }
-    // ---- wait until every CTA has published h_{t-1} (slot t), then load this
-    // warp's B fragments of it through L2
-    if (t > 0) {
+    // ---- wait until every CTA has published h_{t-1}, then load this warp's
+    // B fragments of it
+    if (XCL && t > 0) {
+      // this CTA's share of the tagged words of h_{t-1}, scattered into
+      // buffer t&1 of every CTA of the cluster
+      const uint64_t* src = a.hx + (size_t)((t - 1) & 1) * NW;
+      const uint32_t want = (uint32_t)t;
+      const uint32_t hbase = tc::smem_addr(hbuf) + (uint32_t)((t & 1) * B * HP2 * 4);
+      // every round loads all of this thread's missing words at once, so a
+      // word that is already there costs no extra round trip
+      uint32_t pending = (1u << nmine) - 1u;
+      bool bad = false;
+      uint64_t t0 = 0;
+      while (pending) {
+        uint64_t v[kMaxWords];
+#pragma unroll
+        for (int i = 0; i < kMaxWords; ++i)
+          if ((pending >> i) & 1u) v[i] = ld_relaxed_u64(src + w0 + i * 256);
+#pragma unroll
+        for (int i = 0; i < kMaxWords; ++i) {
+          if (((pending >> i) & 1u) && (uint32_t)(v[i] >> 32) == want) {
+            pending &= ~(1u << i);
+            const uint32_t off = hbase + offw[i];
+            for (uint32_t r = 0; r < csize; ++r) st_dsmem_u32(tc::mapa(off, r), (uint32_t)v[i]);
+          }
+        }
+        if (!pending) break;
+        if (t0 == 0) {
+          t0 = globaltimer_ns();
+        } else if (globaltimer_ns() - t0 > a.limit_ns) {
+          bad = true;
+          break;
+        }
+      }
+      if (bad) {
+        raise_error(a.err, DEV_TIMEOUT_STEP);
+        const uint32_t fo = tc::smem_addr(&abort_x[t & 1]);
+        for (uint32_t r = 0; r < csize; ++r) st_dsmem_u32(tc::mapa(fo, r), 1u);
+      }
+      cluster_barrier();
+      if (*reinterpret_cast<volatile int*>(&abort_x[t & 1])) break;
+    }
+    if (!XCL && t > 0) {
       if (threadIdx.x == 0) {
         const unsigned int* cnt = a.arrive + (t - 1);
         const unsigned int want = gridDim.x;
@@ -133,7 +243,14 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       if (abort_flag) break;
     }
     uint32_t bf[KT][2];
-    if (nb < B) {
+    if (XCL && nb < B) {
+      const uint32_t* hs = reinterpret_cast<const uint32_t*>(hbuf) + ((t & 1) * B + nb) * HP2 + (kw >> 1);
+#pragma unroll
+      for (int kt = 0; kt < KT; ++kt) {
+        bf[kt][0] = hs[kt * 8];
+        bf[kt][1] = hs[kt * 8 + 4];
+      }
+    } else if (nb < B) {
       const uint32_t* hs = reinterpret_cast<const uint32_t*>(a.hseq + ((size_t)t * B + nb) * H + kw);
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
@@ -170,6 +287,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
     }
     __syncthreads();
     // ---- cell update of this CTA's units
+    uint32_t hv = 0;
     if (pair) {
       float av[G];
 #pragma unroll
@@ -195,6 +313,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       }
       const size_t bj = (size_t)bq * H + j;
       const unsigned short hb = bf16_bits(hnew);
+      hv = hb;
       if (a.gates_out) {
         float* grow = a.gates_out + ((size_t)t * B + bq) * GH;
 #pragma unroll
@@ -208,9 +327,22 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       }
       reinterpret_cast<unsigned short*>(a.hseq)[(size_t)(t + 1) * B * H + bj] = hb;
     }
-    // ---- publish: once all of this CTA's h_t stores are done, one release
-    // arrival on the step's counter.  When every cell-update thread is in warp
-    // 0 a warp barrier orders their stores before lane 0's release.
+    // ---- publish
+    if constexpr (XCL) {
+      // even cell-update threads pair their value with the next unit's and
+      // store one tagged word (the warps holding cell-update threads are
+      // whole warps here, so the shuffle's mask is every lane)
+      if (warp * 32 < uc * B) {
+        const uint32_t nbr = __shfl_down_sync(0xffffffffu, hv, 1);
+        if (pair && !(q & 1) && !(a.test_skip_publish && blockIdx.x == 0 && t == 0))
+          st_relaxed_u64(a.hx + (size_t)(t & 1) * NW + (size_t)blockIdx.x * WS + (q >> 1),
+                         ((uint64_t)(t + 1) << 32) | (uint64_t)(hv | (nbr << 16)));
+      }
+      continue;
+    }
+    // counter variant: once all of this CTA's h_t stores are done, one
+    // release arrival on the step's counter.  When every cell-update thread is
+    // in warp 0 a warp barrier orders their stores before lane 0's release.
     if (uc * B <= 32) {
       if (warp == 0) {
         __syncwarp();
@@ -224,24 +356,78 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
 }
 
 template <int CELL, int MT, int KT>
-int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only, int num_sms) {
-  auto kern = persist_fwd_kernel<CELL, MT, KT>;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess) return RNN_ERR_CUDA;
-  if (per_sm * num_sms < ctas) return RNN_ERR_LAUNCH;
-  if (query_only) return RNN_OK;
+int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only, int num_sms, int* cl_out) {
+  auto kc = persist_fwd_kernel<CELL, MT, KT, false>;
+  auto kx = persist_fwd_kernel<CELL, MT, KT, true>;
+  const size_t dyn = (size_t)2 * a.B * (a.H + 8) * 2;  // h_{t-1} ping-pong of the cluster variant
+  if (query_only) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, 256, 0) != cudaSuccess) return RNN_ERR_CUDA;
+    if (per_sm * num_sms < ctas) return RNN_ERR_LAUNCH;
+    if (cl_out) {
+      // the largest cluster size whose clusters all co-reside (0: none)
+      *cl_out = 0;
+      if (cudaFuncSetAttribute(kx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return RNN_OK;
+      }
+      for (int c = 8; c >= 2; c /= 2) {
+        if (ctas % c || (a.H / 2) * a.B / c > 256 * kMaxWords) continue;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(ctas);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = dyn;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = c;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, kx, &cfg) == cudaSuccess && nc * c >= ctas) {
+          *cl_out = c;
+          break;
+        }
+        (void)cudaGetLastError();
+      }
+    }
+    return RNN_OK;
+  }
   PersistArgs args = a;
-  void* params[] = {&args};
+  cudaError_t e;
   launch_begin(L);
-  cudaError_t e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(ctas), dim3(256), params, 0,
-                                              L.stream);
+  if (a.cluster > 0) {
+    e = cudaFuncSetAttribute(kx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(ctas);
+      cfg.blockDim = dim3(256);
+      cfg.dynamicSmemBytes = dyn;
+      cfg.stream = L.stream;
+      cudaLaunchAttribute at[2];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = a.cluster;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      at[1].id = cudaLaunchAttributeCooperative;
+      at[1].val.cooperative = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 2;
+      e = cudaLaunchKernelEx(&cfg, kx, args);
+    }
+  } else {
+    void* params[] = {&args};
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kc), dim3(ctas), dim3(256), params, 0, L.stream);
+  }
   launch_end(L);
   if (e == cudaErrorCooperativeLaunchTooLarge) return RNN_ERR_LAUNCH;
   return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA;
 }
 
 // (cell, H) -> kernel instance; MT*16 = G*uc rows per CTA, KT*16*8 = H.
-int dispatch(const Launch& L, int cell, const PersistArgs& a, bool query_only, int num_sms, int* ctas_out) {
+int dispatch(const Launch& L, int cell, const PersistArgs& a, bool query_only, int num_sms, int* ctas_out,
+             int* cl_out) {
   const int H = a.H;
   if (H % 128 || a.B < 1 || a.B > 8) return RNN_ERR_UNSUPPORTED;
   const int KT = H / 128;
@@ -251,7 +437,7 @@ int dispatch(const Launch& L, int cell, const PersistArgs& a, bool query_only, i
   PersistArgs b = a;
   b.uc = uc;
 #define RNN_P(C, MT_, KT_) \
-  if (cell == C && KT == KT_) return launch_one<C, MT_, KT_>(L, b, ctas, query_only, num_sms);
+  if (cell == C && KT == KT_) return launch_one<C, MT_, KT_>(L, b, ctas, query_only, num_sms, cl_out);
   RNN_P(LSTM, 2, 1) RNN_P(LSTM, 2, 2) RNN_P(LSTM, 2, 4) RNN_P(LSTM, 2, 8)
   RNN_P(GRU, 3, 1) RNN_P(GRU, 3, 2) RNN_P(GRU, 3, 4)
   RNN_P(TANH, 1, 1) RNN_P(TANH, 1, 2) RNN_P(TANH, 1, 4) RNN_P(TANH, 1, 8) RNN_P(TANH, 1, 16)
@@ -262,17 +448,17 @@ int dispatch(const Launch& L, int cell, const PersistArgs& a, bool query_only, i
 
 }  // namespace
 
-int persist_check(int cell, int H, int B, int num_sms, int* ctas) {
+int persist_check(int cell, int H, int B, int num_sms, int* ctas, int* cluster) {
   Launch L{};
   PersistArgs a{};
   a.H = H;
   a.B = B;
-  return dispatch(L, cell, a, true, num_sms, ctas);
+  return dispatch(L, cell, a, true, num_sms, ctas, cluster);
 }
 
 int persist_fwd(const Launch& L, int cell, const PersistArgs& a) {
   int ctas = 0;
-  return dispatch(L, cell, a, false, L.num_sms, &ctas);
+  return dispatch(L, cell, a, false, L.num_sms, &ctas, nullptr);
 }
 
 }  // namespace rnn

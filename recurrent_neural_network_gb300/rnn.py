@@ -30,6 +30,7 @@ FLAG_TEST_SKIP_PUBLISH = 0x100
 FLAG_NO_TRANSPOSED = 0x200
 FLAG_FORCE_TRANSPOSED = 0x400
 FLAG_NO_FUSED_POINT = 0x800
+FLAG_NO_PERSIST_CLUSTER = 0x1000
 
 # every symbol include/rnn.h declares
 SYMBOLS = ["rnn_create", "rnn_destroy", "rnn_get_sizes", "rnn_pack_weights", "rnn_fwd", "rnn_bwd_data",
