@@ -893,9 +893,32 @@ struct EpiBwdDhT {
       }
       if (lane == 0 && ok) ok = tc::mbar_wait_cluster(t.aux, 0, err, limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      // 4. own slice = own partial + peers' partials in split order; dh by one bulk store
-      if (ok) {
-        // 8 rows at a time, every partial's loads issued before the adds
+      // 4. own slice = own partial + peers' partials in split order; dh by one bulk store.
+      // Partial sp of this slice's batch row r sits at tile row sp * cw + r for
+      // every sp (the own partial included), so the sum runs over contiguous
+      // 16-byte vectors, with no tie to the TMEM lane a thread was given.
+      if (ok && !final_) {
+        const int et = threadIdx.x - 64;  // epilogue threads are 64 .. 64 + EWT - 1
+        const float4* t4 = reinterpret_cast<const float4*>(tile);
+        float4* o4 = reinterpret_cast<float4*>(tile) + (size_t)t.split * cw * 32;
+#pragma unroll 2
+        for (int f = et; f < cw * 32; f += EWT) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int sp = 0; sp < 8; ++sp) {
+            if (sp < t.cluster) {
+              const float4 w = t4[(size_t)sp * cw * 32 + f];
+              v.x += w.x;
+              v.y += w.y;
+              v.z += w.z;
+              v.w += w.w;
+            }
+          }
+          o4[f] = v;
+        }
+      } else if (ok) {
+        // final product (dh0 in the storage type): 8 rows at a time, every
+        // partial's loads issued before the adds
         const int pw = cw / t.parts;  // a multiple of 8
         const int r0 = t.split * cw + t.part * pw;
 #pragma unroll 1
