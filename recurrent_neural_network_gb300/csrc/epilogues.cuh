@@ -513,9 +513,19 @@ struct EpiFwdStepT {
     }
   }
 
-  // c_{t-1} for the (unit p/4, batch entry c + 4k + p%4) pairs of chunk c
-  __device__ __forceinline__ void load_cp(int n0, int p, bool live, int c, int nmax, float* cp) const {
-    const int g = p & 3, j = p >> 2;
+  // c_{t-1} for the (unit p/4, batch entry c + 4k + p%4) pairs of chunk c;
+  // in the cell update from the shared-memory gate tile (smem_map) a lane
+  // takes instead unit (first unit of its warp) + lane % 8, batch entry
+  // c + 4k + lane / 8
+  __device__ __forceinline__ void load_cp(int n0, int p, bool live, int c, int nmax, float* cp,
+                                          bool smem_map = false) const {
+    int g = p & 3, j = p >> 2;
+    if (smem_map) {
+      const int lane = threadIdx.x & 31;
+      g = lane >> 3;
+      j = ((p & ~31) >> 2) + (lane & 7);
+      live = j < H;
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int bi = c + 4 * k + g;
@@ -544,7 +554,25 @@ struct EpiFwdStepT {
       if (sm_g) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) sm_g[(c + i) * 128 + row] = v[i];
-      } else if (write_gates && live) {
+        // the warp's 32 gate rows (8 units) of these 16 batch entries are in
+        // the tile: lane (u, e) = (lane & 7, lane >> 3) reads the four gates of
+        // unit u for batch entry c + 4k + e as one 16-byte vector (each 8-lane
+        // phase reads 128 contiguous bytes)
+        __syncwarp();
+        const int lane = threadIdx.x & 31, rw = row & ~31;
+        const int ul = rw / 4 + (lane & 7), e = lane >> 3;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int bi = 4 * k + e;
+          const float4 gt = *reinterpret_cast<const float4*>(sm_g + (c + bi) * 128 + rw + 4 * (lane & 7));
+          const float cn = gt.y * cp[k] + gt.x * gt.z;
+          const float hn = gt.w * tanh_hw(cn);
+          sm_c[(c + bi) * kUnits + ul] = cn;
+          sm_h[(c + bi) * kUnits + ul] = __float2bfloat16_rn(hn);
+        }
+        return;
+      }
+      if (write_gates && live) {
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           if (i < nb) pc[(size_t)i * GH] = v[i];
@@ -570,11 +598,6 @@ struct EpiFwdStepT {
         const float cn = gt[1] * cp[k] + gt[0] * gt[2];
         const float hn = gt[3] * tanh_hw(cn);
         const S hb = __float2bfloat16_rn(hn);
-        if (sm_c) {
-          sm_c[(c + bi) * kUnits + (row >> 2)] = cn;
-          sm_h[(c + bi) * kUnits + (row >> 2)] = hb;
-          continue;
-        }
         if (!live || bi >= nb) continue;
         const size_t bj = (size_t)(n0 + c + bi) * H + j;
         c_out[bj] = cn;
@@ -639,7 +662,7 @@ struct EpiFwdStepT {
     const int nmax = min(cb + cw, B - t.n0);
     if constexpr (CELL == LSTM) {
 #pragma unroll
-      for (int a = 0; a < kAhead; ++a) load_cp(t.n0, p, live, cb + 16 * a, nmax, st.cp[a]);
+      for (int a = 0; a < kAhead; ++a) load_cp(t.n0, p, live, cb + 16 * a, nmax, st.cp[a], tma_out);
     }
     // P, two chunks (32 loads per lane) in flight at a time
 #pragma unroll 1
@@ -689,7 +712,7 @@ struct EpiFwdStepT {
           for (int a = 0; a + 1 < kAhead; ++a)
 #pragma unroll
             for (int k = 0; k < 4; ++k) st.cp[a][k] = st.cp[a + 1][k];
-          load_cp(t.n0, p, live, c + 16 * kAhead, nmax, st.cp[kAhead - 1]);
+          load_cp(t.n0, p, live, c + 16 * kAhead, nmax, st.cp[kAhead - 1], tma_out);
         }
         if (tma_out)
           finish(t.n0, p, live, c, min(16, nmax - c), v2 + 16 * h, cp, row, sm_g, sm_c, sm_h);
