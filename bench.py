@@ -154,12 +154,11 @@ def class_bytes(wl, transposed, fused_point=False):
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
-# ncu capture of the same kernel build on a one-layer T=2 case with the same
-# per-step shape (transposed steps, BPTT pointwise fused into the product);
-# summarised in profiles/ncu_step_kernels_lstm_B256_H4096.md.
-NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.30e6,
-               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.90e6,
-               ("lstm_bf16_L4_T50_B256_H4096", "bwd_point"): 35.68e6}
+# ncu capture of the same kernel build on `bench.py --ncu-steps` (one layer,
+# T=2, the same per-step shape; transposed steps, BPTT pointwise fused into the
+# product); summarised in profiles/ncu_step_kernels_lstm_B256_H4096.md.
+NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.36e6,
+               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.64e6}
 
 
 def time_oracle_sample(wl, budget_s=20.0):
@@ -377,6 +376,28 @@ def synth_tensor(wl, what, dev, dtype):
     return synth.device_tensor(wl, what, dev, dtype)
 
 
+def ncu_steps(args):
+    """A short program for ncu: two timesteps of one layer of the configured
+    workload (forward, BPTT, weight gradients), run twice, no timing."""
+    from recurrent_neural_network_gb300 import build, runner, synth
+    build.build()
+    dev = torch.device("cuda", 0)
+    wl = synth.WORKLOADS[args.config].replace(layers=1, T=2)
+    R = runner.Runner(wl, device=dev, flags=args.flags, chunk=args.chunk)
+    R.x = synth_tensor(wl, "x", dev, R.dt)
+    R.w_user = synth_tensor(wl, "w", dev, R.dt)
+    R.h0 = synth_tensor(wl, "h0", dev, R.dt)
+    if wl.cell == synth.CELL_LSTM:
+        R.c0 = synth_tensor(wl, "c0", dev, torch.float32)
+    R.dy = synth_tensor(wl, "dy", dev, R.dt)
+    R.pack()
+    for _ in range(2):
+        R.step()
+    torch.cuda.synchronize()
+    assert R.status() == 0
+    print(json.dumps({"ncu_steps": wl.name, "plan": R.r.describe()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -391,11 +412,17 @@ def main():
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--sweep", action="store_true",
                     help="selector sweep over batch sizes and widths instead of the benchmark line")
+    ap.add_argument("--ncu-steps", action="store_true",
+                    help="one training pass (forward, BPTT, weight gradients) of a one-layer T=2 copy of the "
+                         "workload, for profiler captures: every recurrent-step launch has the full per-step shape")
     args = ap.parse_args()
     if args.sweep:
         from recurrent_neural_network_gb300 import build
         build.build()
         sweep(torch.device("cuda", 0))
+        return
+    if args.ncu_steps:
+        ncu_steps(args)
         return
 
     from recurrent_neural_network_gb300 import synth
