@@ -55,6 +55,10 @@ def _load():
         lib.rnn_ref_fwd_len.restype = ci
         lib.rnn_ref_bwd_len.argtypes = [ci] * 6 + [ip] + [dp] * 11
         lib.rnn_ref_bwd_len.restype = ci
+        lib.rnn_ref_fwd_dir.argtypes = [ci] * 7 + [ip] + [dp] * 7
+        lib.rnn_ref_fwd_dir.restype = ci
+        lib.rnn_ref_bwd_dir.argtypes = [ci] * 7 + [ip] + [dp] * 11
+        lib.rnn_ref_bwd_dir.restype = ci
         lib.rnn_ref_threads.restype = ci
         _lib = lib
     return _lib
@@ -79,9 +83,10 @@ def _c(a, shape=None):
     return a
 
 
-def weight_count(cell, L, I, H):
+def weight_count(cell, L, I, H, D=1):
+    """Length of the flat weight vector: per (layer, direction) W_x, W_h, b_x, b_h."""
     G = GATES[cell]
-    return sum(G * H * ((I if l == 0 else H) + H) + 2 * G * H for l in range(L))
+    return sum(D * (G * H * ((I if l == 0 else D * H) + H) + 2 * G * H) for l in range(L))
 
 
 def _lens(lens, T, B):
@@ -96,55 +101,58 @@ def _ip(a):
     return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
 
 
-def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None, lens=None):
-    """Forward pass. Returns (y[T][B][H], hT[L][B][H], cT[L][B][H] or None).
+def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None, lens=None, D=1):
+    """Forward pass. Returns (y[T][B][D*H], hT[L*D][B][H], cT[L*D][B][H] or None).
     lens[B] (optional): per-sequence lengths; later outputs are 0 and hT / cT
-    are each sequence's state after its own last step."""
+    are each sequence's state after its own last step.  D = 2: bidirectional
+    layers (direction 1 runs time backwards; states indexed layer * 2 + direction)."""
     lens = _lens(lens, T, B)
     x = _c(x, (T, B, I))
-    w = _c(w, (weight_count(cell, L, I, H),))
-    h0 = _c(h0, (L, B, H))
-    c0 = _c(c0, (L, B, H)) if cell == 0 else None
-    y = np.zeros((T, B, H))
-    hT = np.zeros((L, B, H))
-    cT = np.zeros((L, B, H)) if cell == 0 else None
-    rc = _load().rnn_ref_fwd_len(cell, L, T, B, I, H, _ip(lens), _p(x), _p(h0), _p(c0), _p(w), _p(y), _p(hT),
+    w = _c(w, (weight_count(cell, L, I, H, D),))
+    h0 = _c(h0, (L * D, B, H))
+    c0 = _c(c0, (L * D, B, H)) if cell == 0 else None
+    y = np.zeros((T, B, D * H))
+    hT = np.zeros((L * D, B, H))
+    cT = np.zeros((L * D, B, H)) if cell == 0 else None
+    rc = _load().rnn_ref_fwd_dir(cell, L, D, T, B, I, H, _ip(lens), _p(x), _p(h0), _p(c0), _p(w), _p(y), _p(hT),
                                  _p(cT))
     if rc != 0:
         raise ValueError(f"rnn_ref_fwd rejected its arguments ({rc})")
     return y, hT, cT
 
 
-def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None, lens=None):
-    """Backward pass. Returns (dx[T][B][I], dh0[L][B][H], dc0 or None, dw like w)."""
+def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None, lens=None, D=1):
+    """Backward pass. Returns (dx[T][B][I], dh0[L*D][B][H], dc0 or None, dw like w)."""
     lens = _lens(lens, T, B)
     x = _c(x, (T, B, I))
-    w = _c(w, (weight_count(cell, L, I, H),))
-    dy = _c(dy, (T, B, H))
-    h0 = _c(h0, (L, B, H))
-    c0 = _c(c0, (L, B, H)) if cell == 0 else None
-    dhT = _c(dhT, (L, B, H))
-    dcT = _c(dcT, (L, B, H)) if cell == 0 else None
+    w = _c(w, (weight_count(cell, L, I, H, D),))
+    dy = _c(dy, (T, B, D * H))
+    h0 = _c(h0, (L * D, B, H))
+    c0 = _c(c0, (L * D, B, H)) if cell == 0 else None
+    dhT = _c(dhT, (L * D, B, H))
+    dcT = _c(dcT, (L * D, B, H)) if cell == 0 else None
     dx = np.zeros((T, B, I))
-    dh0 = np.zeros((L, B, H))
-    dc0 = np.zeros((L, B, H)) if cell == 0 else None
+    dh0 = np.zeros((L * D, B, H))
+    dc0 = np.zeros((L * D, B, H)) if cell == 0 else None
     dw = np.zeros_like(w)
-    rc = _load().rnn_ref_bwd_len(cell, L, T, B, I, H, _ip(lens), _p(x), _p(h0), _p(c0), _p(w), _p(dy), _p(dhT),
+    rc = _load().rnn_ref_bwd_dir(cell, L, D, T, B, I, H, _ip(lens), _p(x), _p(h0), _p(c0), _p(w), _p(dy), _p(dhT),
                                  _p(dcT), _p(dx), _p(dh0), _p(dc0), _p(dw))
     if rc != 0:
         raise ValueError(f"rnn_ref_bwd rejected its arguments ({rc})")
     return dx, dh0, dc0, dw
 
 
-def split_weights(cell, L, I, H, w):
-    """Views (W_x, W_h, b_x, b_h) per layer of a flat user-layout weight vector."""
+def split_weights(cell, L, I, H, w, D=1):
+    """Views (W_x, W_h, b_x, b_h) per (layer, direction) l * D + d of a flat
+    user-layout weight vector."""
     G = GATES[cell]
     out, o = [], 0
     for l in range(L):
-        In = I if l == 0 else H
-        wx = w[o:o + G * H * In].reshape(G * H, In); o += G * H * In
-        wh = w[o:o + G * H * H].reshape(G * H, H); o += G * H * H
-        bx = w[o:o + G * H]; o += G * H
-        bh = w[o:o + G * H]; o += G * H
-        out.append((wx, wh, bx, bh))
+        for _ in range(D):
+            In = I if l == 0 else D * H
+            wx = w[o:o + G * H * In].reshape(G * H, In); o += G * H * In
+            wh = w[o:o + G * H * H].reshape(G * H, H); o += G * H * H
+            bx = w[o:o + G * H]; o += G * H
+            bh = w[o:o + G * H]; o += G * H
+            out.append((wx, wh, bx, bh))
     return out

@@ -52,6 +52,21 @@ int rnn_ref_bwd_len(int cell, int L, int T, int B, int I, int H, const int* lens
                     const double* dy, const double* dhT, const double* dcT,
                     double* dx, double* dh0, double* dc0, double* dw);
 
+/* Bidirectional stacks (D = 2; D = 1 is the unidirectional case above).  Each
+ * layer l has D sets of weights, v = l*D + d, in that order in w and dw:
+ * W_x[G*H][I_l], W_h[G*H][H], b_x[G*H], b_h[G*H] with I_0 = I, I_l = D*H.
+ * Direction 1 runs time backwards (from lens[b]-1, or T-1, down to 0, from its
+ * own h0).  y[T][B][D*H] holds [h_dir0(t), h_dir1(t)]; h0, c0, hT, cT, dh0,
+ * dc0, dhT, dcT are [L*D][B][H] (index v); dy is [T][B][D*H].  hT of
+ * direction 1 is its state after time 0. */
+int rnn_ref_fwd_dir(int cell, int L, int D, int T, int B, int I, int H, const int* lens,
+                    const double* x, const double* h0, const double* c0, const double* w,
+                    double* y, double* hT, double* cT);
+int rnn_ref_bwd_dir(int cell, int L, int D, int T, int B, int I, int H, const int* lens,
+                    const double* x, const double* h0, const double* c0, const double* w,
+                    const double* dy, const double* dhT, const double* dcT,
+                    double* dx, double* dh0, double* dc0, double* dw);
+
 #ifdef __cplusplus
 }
 #endif

@@ -423,3 +423,161 @@ def test_variable_lengths_match_torch_packed_sequences(cell, lens):
         for nm in ("weight_ih", "weight_hh", "bias_ih", "bias_hh"):
             tw.append(getattr(m, f"{nm}_l{l}").grad.numpy().ravel())
     np.testing.assert_allclose(dw, np.concatenate(tw), rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- bidirectional layers
+
+def rand_case_bidir(cell, L, T, B, I, H, seed):
+    rng = np.random.default_rng(seed)
+    n = oracle.weight_count(cell, L, I, H, D=2)
+    w = rng.uniform(-0.6, 0.6, n)
+    x = rng.normal(size=(T, B, I))
+    h0 = rng.normal(scale=0.5, size=(2 * L, B, H))
+    c0 = rng.normal(scale=0.5, size=(2 * L, B, H))
+    dy = rng.normal(size=(T, B, 2 * H))
+    dhT = rng.normal(size=(2 * L, B, H))
+    dcT = rng.normal(size=(2 * L, B, H))
+    return w, x, h0, c0, dy, dhT, dcT
+
+
+def torch_bidir(cell, L, I, H, w):
+    kw = dict(bidirectional=True, dtype=torch.float64)
+    if cell == 0:
+        m = torch.nn.LSTM(I, H, L, **kw)
+    elif cell == 1:
+        m = torch.nn.GRU(I, H, L, **kw)
+    else:
+        m = torch.nn.RNN(I, H, L, nonlinearity="tanh" if cell == 2 else "relu", **kw)
+    views = oracle.split_weights(cell, L, I, H, w, D=2)
+    for l in range(L):
+        for d, sfx in enumerate(("", "_reverse")):
+            wx, wh, bx, bh = views[2 * l + d]
+            getattr(m, f"weight_ih_l{l}{sfx}").data.copy_(torch.from_numpy(wx))
+            getattr(m, f"weight_hh_l{l}{sfx}").data.copy_(torch.from_numpy(wh))
+            getattr(m, f"bias_ih_l{l}{sfx}").data.copy_(torch.from_numpy(bx))
+            getattr(m, f"bias_hh_l{l}{sfx}").data.copy_(torch.from_numpy(bh))
+    return m
+
+
+def torch_bidir_run(cell, L, T, B, I, H, w, x, h0, c0, dy, dhT, dcT, lens=None):
+    m = torch_bidir(cell, L, I, H, w)
+    xt = torch.tensor(x, requires_grad=True)
+    h0t = torch.tensor(h0, requires_grad=True)
+    c0t = torch.tensor(c0, requires_grad=True)
+    inp = xt if lens is None else torch.nn.utils.rnn.pack_padded_sequence(xt, torch.tensor(lens), enforce_sorted=False)
+    if cell == 0:
+        out, (hT, cT) = m(inp, (h0t, c0t))
+    else:
+        out, hT = m(inp, h0t)
+        cT = None
+    y = out if lens is None else torch.nn.utils.rnn.pad_packed_sequence(out, total_length=T)[0]
+    loss = (y * torch.tensor(dy)).sum() + (hT * torch.tensor(dhT)).sum()
+    if cell == 0:
+        loss = loss + (cT * torch.tensor(dcT)).sum()
+    loss.backward()
+    dw = []
+    for l in range(L):
+        for sfx in ("", "_reverse"):
+            for nm in ("weight_ih", "weight_hh", "bias_ih", "bias_hh"):
+                dw.append(getattr(m, f"{nm}_l{l}{sfx}").grad.numpy().ravel())
+    return dict(y=y.detach().numpy(), hT=hT.detach().numpy(),
+                cT=None if cT is None else cT.detach().numpy(),
+                dx=xt.grad.numpy(), dh0=h0t.grad.numpy(),
+                dc0=c0t.grad.numpy() if cell == 0 else None, dw=np.concatenate(dw))
+
+
+def oracle_bidir_run(cell, L, T, B, I, H, w, x, h0, c0, dy, dhT, dcT, lens=None):
+    y, hT, cT = oracle.fwd(cell, L, T, B, I, H, x, w, h0=h0, c0=c0, lens=lens, D=2)
+    dx, dh0, dc0, dw = oracle.bwd(cell, L, T, B, I, H, x, w, dy, h0=h0, c0=c0, dhT=dhT, dcT=dcT, lens=lens, D=2)
+    return dict(y=y, hT=hT, cT=cT, dx=dx, dh0=dh0, dc0=dc0, dw=dw)
+
+
+@pytest.mark.parametrize("cell", CELLS)
+@pytest.mark.parametrize("shape", [(2, 3, 2, 3, 2), (3, 5, 3, 7, 6)])
+def test_bidirectional_matches_torch_float64(cell, shape):
+    """PyTorch float64 bidirectional nn.LSTM / GRU / RNN with autograd: outputs
+    [forward, reverse] per timestep, final states per (layer, direction), and
+    every gradient."""
+    L, T, B, I, H = shape
+    args = rand_case_bidir(cell, L, T, B, I, H, seed=71 + cell)
+    o = oracle_bidir_run(cell, L, T, B, I, H, *args)
+    r = torch_bidir_run(cell, L, T, B, I, H, *args)
+    for k in o:
+        if o[k] is None:
+            continue
+        np.testing.assert_allclose(o[k], r[k], rtol=1e-10, atol=1e-12, err_msg=k)
+
+
+@pytest.mark.parametrize("cell,lens", LENS_CASES, ids=["lstm", "gru", "tanh", "relu"])
+def test_bidirectional_variable_lengths_match_torch_packed(cell, lens):
+    """Packed bidirectional batch: the reverse direction of each sequence starts
+    at its own last step."""
+    L, T, B, I, H = 2, 4, 4, 3, 5
+    args = rand_case_bidir(cell, L, T, B, I, H, seed=81 + cell)
+    o = oracle_bidir_run(cell, L, T, B, I, H, *args, lens=lens)
+    r = torch_bidir_run(cell, L, T, B, I, H, *args, lens=lens)
+    for k in o:
+        if o[k] is None:
+            continue
+        np.testing.assert_allclose(o[k], r[k], rtol=1e-10, atol=1e-12, err_msg=k)
+
+
+@pytest.mark.parametrize("cell", CELLS)
+def test_bidirectional_single_layer_is_two_unidirectional_runs(cell):
+    """One bidirectional layer = the forward-direction weights run on x, and the
+    reverse-direction weights run on x reversed in time with the output
+    reversed back (both by the unidirectional oracle)."""
+    T, B, I, H = 5, 3, 4, 6
+    w, x, h0, c0, dy, dhT, dcT = rand_case_bidir(cell, 1, T, B, I, H, seed=91 + cell)
+    y, hT, cT = oracle.fwd(cell, 1, T, B, I, H, x, w, h0=h0, c0=c0, D=2)
+    n1 = oracle.weight_count(cell, 1, I, H)
+    c0f = c0[0:1] if cell == 0 else None
+    c0r = c0[1:2] if cell == 0 else None
+    yf, hf, cf = oracle.fwd(cell, 1, T, B, I, H, x, w[:n1], h0=h0[0:1], c0=c0f)
+    yr, hr, cr = oracle.fwd(cell, 1, T, B, I, H, x[::-1], w[n1:], h0=h0[1:2], c0=c0r)
+    np.testing.assert_allclose(y[:, :, :H], yf, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(y[:, :, H:], yr[::-1], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(hT[0], hf[0], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(hT[1], hr[0], rtol=1e-13, atol=1e-15)
+    dx, dh0, dc0, dw = oracle.bwd(cell, 1, T, B, I, H, x, w, dy, h0=h0, c0=c0, dhT=dhT, dcT=dcT, D=2)
+    dxf, dh0f, dc0f, dwf = oracle.bwd(cell, 1, T, B, I, H, x, w[:n1], dy[:, :, :H], h0=h0[0:1], c0=c0f,
+                                      dhT=dhT[0:1], dcT=dcT[0:1] if cell == 0 else None)
+    dxr, dh0r, dc0r, dwr = oracle.bwd(cell, 1, T, B, I, H, x[::-1], w[n1:], dy[::-1, :, H:], h0=h0[1:2], c0=c0r,
+                                      dhT=dhT[1:2], dcT=dcT[1:2] if cell == 0 else None)
+    np.testing.assert_allclose(dx, dxf + dxr[::-1], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dh0, np.concatenate([dh0f, dh0r]), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dw, np.concatenate([dwf, dwr]), rtol=1e-12, atol=1e-14)
+    if cell == 0:
+        np.testing.assert_allclose(cT, np.concatenate([cf, cr]), rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(dc0, np.concatenate([dc0f, dc0r]), rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("cell", CELLS)
+def test_bidirectional_central_finite_differences(cell):
+    L, T, B, I, H = 2, 3, 2, 3, 2
+    w, x, h0, c0, dy, dhT, dcT = rand_case_bidir(cell, L, T, B, I, H, seed=101 + cell)
+    dx, dh0, dc0, dw = oracle.bwd(cell, L, T, B, I, H, x, w, dy, h0=h0, c0=c0, dhT=dhT, dcT=dcT, D=2)
+
+    def loss():
+        y, hT, cT = oracle.fwd(cell, L, T, B, I, H, x, w, h0=h0, c0=c0, D=2)
+        v = float((y * dy).sum() + (hT * dhT).sum())
+        return v + (float((cT * dcT).sum()) if cell == 0 else 0.0)
+
+    eps = 1e-6
+    targets = [("w", w, dw), ("x", x, dx), ("h0", h0, dh0)]
+    if cell == 0:
+        targets.append(("c0", c0, dc0))
+    for name, arr, grad in targets:
+        flat = arr.reshape(-1)
+        num = np.zeros(flat.size)
+        for k in range(flat.size):
+            save = flat[k]
+            flat[k] = save + eps
+            lp = loss()
+            flat[k] = save - eps
+            lm = loss()
+            flat[k] = save
+            num[k] = (lp - lm) / (2 * eps)
+        scale = max(np.abs(num).max(), 1e-3)
+        err = np.abs(num - grad.reshape(-1)).max() / scale
+        assert err < 1e-7, (name, err)
