@@ -39,6 +39,15 @@
  *     with I_0 = input, I_l = hidden for l >= 1, and gate blocks ordered
  *     LSTM (i, f, g, o), GRU (r, z, n), RNN (one block).  dw has the same
  *     layout in float.
+ *   - Bidirectional stacks (RNN_FLAG_BIDIRECTIONAL; D = 2, else D = 1): each
+ *     layer has a forward and a reverse direction, the reverse one running
+ *     from t = T-1 down to 0 from its own initial state.  Weights come per
+ *     (layer, direction) v = l*D + d in that order (torch's "_reverse"
+ *     parameters after each layer's own), with I_l = D*hidden for l >= 1;
+ *     y/dy are [T][B][D*hidden] with y[t] = [h_forward(t), h_reverse(t)];
+ *     the state arrays are [layers*D][B][hidden] indexed by v, and hT of the
+ *     reverse direction is its state after t = 0.  Not combined with
+ *     rnn_set_lengths() nor the persistent recurrence.
  *   - Pointers must be 16-byte aligned.  Shapes: in RNN_MODE_BF16 hidden must
  *     be a multiple of 64 and input of 8; in RNN_MODE_FP32 hidden a multiple
  *     of 32 and input of 4 (RNN_ERR_UNSUPPORTED otherwise).
@@ -97,6 +106,8 @@ enum {
 #define RNN_FLAG_NO_PERSIST_CLUSTER 0x1000u /* persistent recurrence: hand h_t over through per-step
                                                arrival counters and L2 reads instead of tagged words
                                                gathered per thread-block cluster */
+#define RNN_FLAG_BIDIRECTIONAL 0x2000u /* every layer gets a second direction that runs time backwards
+                                          with its own weights (see the layouts below) */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */

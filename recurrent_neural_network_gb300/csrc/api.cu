@@ -121,6 +121,7 @@ using namespace rnn;
 struct rnn_s {
   rnn_desc_t d{};
   int G = 0, GH = 0, u = 0, elem = 0;
+  int D = 1;  // directions per layer (2: bidirectional); per-(layer, direction) arrays are indexed v = l*D + d
   int num_sms = 152;
   int have_device = 0;
   // plan
@@ -152,6 +153,8 @@ struct rnn_s {
   size_t ws_err = 0;
   size_t ws_arrive = 0;  // persistent recurrence: per-timestep arrival counters
   size_t ws_hx = 0;      // persistent recurrence, cluster exchange: tagged h words [2][B*H/2]
+  size_t ws_dtop = 0;    // bidirectional: the two halves of dy, [2][T][B][H] storage type
+  size_t ws_dxacc = 0;   // bidirectional bf16: dx of both directions summed in f32, [T][B][I]
   int ctr_count = 0;
   // streams and events (created on first use)
   std::vector<cudaStream_t> streams;
@@ -170,7 +173,8 @@ struct rnn_s {
   std::vector<std::vector<uintptr_t>> seen, no_graph;
   cudaStream_t cap = nullptr;
 
-  int In(int l) const { return l == 0 ? d.input : d.hidden; }
+  int In(int l) const { return l == 0 ? d.input : D * d.hidden; }
+  int V() const { return d.layers * D; }
 };
 
 namespace {
@@ -188,6 +192,7 @@ int plan_and_layout(rnn_s* h) {
   const int L = d.layers, T = d.T, B = d.B, H = d.hidden;
   h->G = d.cell == RNN_LSTM ? 4 : d.cell == RNN_GRU ? 3 : 1;
   h->GH = h->G * H;
+  h->D = (d.flags & RNN_FLAG_BIDIRECTIONAL) ? 2 : 1;
   h->elem = d.mode == RNN_MODE_BF16 ? 2 : 4;
   const int GH = h->GH;
   if (d.mode == RNN_MODE_BF16) {
@@ -206,9 +211,10 @@ int plan_and_layout(rnn_s* h) {
 
   // persistent recurrence for small batches (weights on-chip, one launch per
   // layer); it runs layer after layer, so it replaces the wavefront.
-  if (d.mode == RNN_MODE_BF16 && !(d.flags & RNN_FLAG_FORCE_STREAMING)) {
+  // (not for bidirectional stacks: its hand-off runs time forwards only)
+  if (d.mode == RNN_MODE_BF16 && !(d.flags & RNN_FLAG_FORCE_STREAMING) && h->D == 1) {
     int ctas = 0;
-    int cl = 8;  // without a device: as measured on the target (clusters of 8 co-reside)
+    int cl = 4;  // without a device: the size that co-resides on GB300 for 128 CTAs
     const bool fits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &ctas, &cl) == RNN_OK
                                      : (B <= 8 && H % 128 == 0 && H <= (d.cell == RNN_GRU ? 512 : d.cell == RNN_LSTM ? 1024 : 2048));
     if (fits) {
@@ -221,7 +227,8 @@ int plan_and_layout(rnn_s* h) {
   if ((d.flags & RNN_FLAG_FORCE_PERSISTENT) && !h->persist) return RNN_ERR_UNSUPPORTED;
   h->fwd_mcast = (d.flags & RNN_FLAG_NO_MULTICAST) ? 1 : 4;
   // wavefront chunking
-  h->wavefront = (L > 1) && !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !h->persist;
+  // (a bidirectional layer needs all of the layer below: no wavefront)
+  h->wavefront = (L > 1) && !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !h->persist && h->D == 1;
   if (!h->wavefront) h->chunk = T;
   else if (d.chunk > 0) h->chunk = std::min(d.chunk, T);
   else h->chunk = std::max(1, (T + 7) / 8);
@@ -279,30 +286,32 @@ int plan_and_layout(rnn_s* h) {
 
   const size_t e = h->elem;
   const size_t BH = (size_t)B * H, BGH = (size_t)B * GH;
+  // per (layer, direction) v = l * D + d; In of layer l = v / D
+  const int V = h->V(), Dn = h->D;
   // user weights
-  h->ul.resize(L);
+  h->ul.resize(V);
   size_t off = 0;
-  for (int l = 0; l < L; ++l) {
-    h->ul[l].wx = off; off += (size_t)GH * h->In(l);
+  for (int l = 0; l < V; ++l) {
+    h->ul[l].wx = off; off += (size_t)GH * h->In(l / Dn);
     h->ul[l].wh = off; off += (size_t)GH * H;
     h->ul[l].bx = off; off += GH;
     h->ul[l].bh = off; off += GH;
   }
   h->user_w_bytes = off * e;
   // packed weights
-  h->pl.resize(L);
+  h->pl.resize(V);
   size_t cur = 0;
-  for (int l = 0; l < L; ++l) {
-    h->pl[l].wx = take(cur, (size_t)GH * h->In(l) * e);
+  for (int l = 0; l < V; ++l) {
+    h->pl[l].wx = take(cur, (size_t)GH * h->In(l / Dn) * e);
     h->pl[l].wh = take(cur, (size_t)GH * H * e);
     h->pl[l].bias = take(cur, (size_t)GH * 4);
     h->pl[l].bias_hn = take(cur, (size_t)H * 4);
   }
   h->packed_bytes = (cur + 255) & ~size_t(255);
   // reserve
-  h->rl.resize(L);
+  h->rl.resize(V);
   cur = 0;
-  for (int l = 0; l < L; ++l) {
+  for (int l = 0; l < V; ++l) {
     h->rl[l].gates = take(cur, (size_t)T * BGH * 4);
     h->rl[l].c = d.cell == RNN_LSTM ? take(cur, (size_t)T * BH * 4) : 0;
     h->rl[l].hn = d.cell == RNN_GRU ? take(cur, (size_t)T * BH * 4) : 0;
@@ -312,14 +321,16 @@ int plan_and_layout(rnn_s* h) {
   }
   h->reserve_bytes = (cur + 255) & ~size_t(255);
   // workspace
-  h->wl.resize(L);
+  h->wl.resize(V);
   cur = 0;
   h->ws_err = take(cur, 256);
   h->ws_arrive = take(cur, (size_t)T * 4);
   h->ws_hx = h->persist_plan ? take(cur, (size_t)8 * B * H) : 0;
   h->bias_slices = std::max(1, std::min(64, (T * B + 255) / 256));
   h->ws_bias = take(cur, (size_t)h->bias_slices * GH * 4);
-  for (int l = 0; l < L; ++l) {
+  h->ws_dtop = Dn == 2 ? take(cur, (size_t)2 * T * BH * e) : 0;
+  h->ws_dxacc = (Dn == 2 && d.mode == RNN_MODE_BF16) ? take(cur, (size_t)T * B * d.input * 4) : 0;
+  for (int l = 0; l < V; ++l) {
     h->wl[l].P = take(cur, (size_t)T * BGH * 4);
     h->wl[l].hseq = take(cur, (size_t)(T + 1) * BH * e);
     h->wl[l].c2 = take(cur, 2 * BH * 4);
@@ -479,6 +490,273 @@ int run_graphed(rnn_s* h, cudaStream_t user, const std::vector<uintptr_t>& key, 
 
 int cu(cudaError_t e) { return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA; }
 
+// ---------------------------------------------------------------- bidirectional stacks
+// Every layer has a forward (d = 0) and a reverse (d = 1) direction with their
+// own weights, v = 2 l + d.  Both keep their h sequence in time order: the
+// forward one at slots 1..T (slot 0 = its h0), the reverse one at slots
+// 0..T-1 (slot T = its h0), so the next layer's input, dW_x and dW_h read
+// plain strided operands.  A layer's input of width 2H enters its products as
+// two halves of K (the second product accumulating).  Layers run one after
+// another (layer l + 1 needs all of layer l's reverse direction), directions
+// one after the other, all on the caller's stream.
+
+// slot of h at time t in direction d (t = -1 forward, t = T reverse: the initial state)
+size_t hslot(int d, int t) { return (size_t)(t + 1 - d); }
+
+int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const char* PW, void* y, void* hT,
+              float* cT, char* R, char* W, void* ws, cudaStream_t s) {
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, GH = h->GH, mode = d.mode;
+  const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
+  const bool train = R != nullptr;
+  const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+  const Remap none{0, 1, 1, 1};
+  auto hseq_of = [&](int v) -> char* { return train ? R + h->rl[v].hseq : W + h->wl[v].hseq; };
+  for (int l = 0; l < L; ++l) {
+    for (int dd = 0; dd < 2; ++dd) {
+      const int v = 2 * l + dd;
+      char* hseq = hseq_of(v);
+      float* P = reinterpret_cast<float*>(train ? R + h->rl[v].gates : W + h->wl[v].P);
+      char* hinit = hseq + hslot(dd, dd == 0 ? -1 : T) * BH * e;
+      if (h0)
+        RNN_TRY(cu(cudaMemcpyAsync(hinit, static_cast<const char*>(h0) + v * BH * e, BH * e, cudaMemcpyDeviceToDevice,
+                                   s)));
+      else
+        RNN_TRY(cu(cudaMemsetAsync(hinit, 0, BH * e, s)));
+      // input projection over all T (layer >= 1: one product per half of the input)
+      const float* bias = reinterpret_cast<const float*>(PW + h->pl[v].bias);
+      if (l == 0) {
+        const int In = d.input;
+        Operand A{x, In, 0, T * B, In};
+        Operand Bw{PW + h->pl[v].wx, In, 0, GH, In, 1};
+        Launch Lk = mk(h, s, ws, "input_proj_gemm");
+        RNN_TRY(gemm_f32(Lk, mode, A, Bw, T * B, GH, In, P, GH, bias, 0, none, 0));
+      } else {
+        for (int q = 0; q < 2; ++q) {
+          Operand A{hseq_of(2 * (l - 1) + q) + hslot(q, 0) * BH * e, H, 0, T * B, H};
+          Operand Bw{PW + h->pl[v].wx + (size_t)q * H * e, 2 * H, 0, GH, H, 1};
+          Launch Lk = mk(h, s, ws, "input_proj_gemm");
+          RNN_TRY(gemm_f32(Lk, mode, A, Bw, T * B, GH, H, P, GH, q == 0 ? bias : nullptr, q, none, 0));
+        }
+      }
+      auto cbuf = [&](int tt) -> float* {
+        return train ? reinterpret_cast<float*>(R + h->rl[v].c) + (size_t)tt * BH
+                     : reinterpret_cast<float*>(W + h->wl[v].c2) + (size_t)(tt & 1) * BH;
+      };
+      // the recurrence: step k at time t, after the step at time tp
+      for (int k = 0; k < T; ++k) {
+        const int t = dd == 0 ? k : T - 1 - k, tp = dd == 0 ? t - 1 : t + 1;
+        FwdStepArgs a;
+        a.B = B;
+        a.H = H;
+        a.u = h->u;
+        a.P = P + (size_t)t * BGH;
+        a.write_gates = train ? 1 : 0;
+        a.bias_hn = reinterpret_cast<const float*>(PW + h->pl[v].bias_hn);
+        a.c_prev = lstm ? (k == 0 ? (c0 ? c0 + v * BH : nullptr) : cbuf(tp)) : nullptr;
+        a.c_out = lstm ? cbuf(t) : nullptr;
+        a.h_prev = hseq + hslot(dd, tp) * BH * e;
+        a.h_out = hseq + hslot(dd, t) * BH * e;
+        a.y = nullptr;
+        a.hT = (k == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)v * BH * e : nullptr;
+        a.cT = (k == T - 1 && cT && lstm) ? cT + (size_t)v * BH : nullptr;
+        a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[v].hn) + (size_t)t * BH : nullptr;
+        a.mcast = h->fwd_mcast;
+        Operand A{a.h_prev, H, 0, B, H};
+        Operand Bw{PW + h->pl[v].wh, H, 0, GH, H, 1};
+        Launch Lk = mk(h, s, ws, "fwd_step");
+        if (h->tstep) RNN_TRY(fwd_step_t(Lk, d.cell, Bw, A, a));
+        else RNN_TRY(fwd_step(Lk, mode, d.cell, A, Bw, a));
+      }
+      // the top layer's output y[T][B][2H] = [h_forward(t), h_reverse(t)]
+      if (l == L - 1)
+        RNN_TRY(cu(cudaMemcpy2DAsync(static_cast<char*>(y) + (size_t)dd * H * e, 2 * H * e, hseq + hslot(dd, 0) * BH * e,
+                                     H * e, H * e, (size_t)T * B, cudaMemcpyDeviceToDevice, s)));
+    }
+  }
+  return RNN_OK;
+}
+
+int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const char* PW, const float* c0, void* dx,
+              void* dh0, float* dc0, char* R, char* W, void* ws, cudaStream_t s) {
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, GH = h->GH, mode = d.mode;
+  const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
+  const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+  const Remap none{0, 1, 1, 1};
+  for (int v = 0; v < 2 * L; ++v)
+    RNN_TRY(cu(cudaMemsetAsync(W + h->wl[v].ctr, 0, (size_t)h->ctr_count * 4, s)));
+  // the two halves of dy, each [T][B][H]
+  for (int dd = 0; dd < 2; ++dd)
+    RNN_TRY(cu(cudaMemcpy2DAsync(W + h->ws_dtop + (size_t)dd * T * BH * e, H * e,
+                                 static_cast<const char*>(dy) + (size_t)dd * H * e, 2 * H * e, H * e, (size_t)T * B,
+                                 cudaMemcpyDeviceToDevice, s)));
+  for (int l = L - 1; l >= 0; --l) {
+    for (int dd = 0; dd < 2; ++dd) {
+      const int v = 2 * l + dd;
+      const bool top = l == L - 1;
+      const char* dyl = top ? W + h->ws_dtop + (size_t)dd * T * BH * e : W + h->wl[v].dyab;
+      const size_t dy_es = top ? e : 4;
+      float* carry = reinterpret_cast<float*>(W + h->wl[v].carry);
+      char* hseq = R + h->rl[v].hseq;
+      const float* c0v = c0 ? c0 + v * BH : nullptr;
+      if (lstm || gru) {
+        if (lstm && dcT) RNN_TRY(cu(cudaMemcpyAsync(carry, dcT + v * BH, BH * 4, cudaMemcpyDeviceToDevice, s)));
+        else RNN_TRY(cu(cudaMemsetAsync(carry, 0, BH * 4, s)));
+      }
+      // time of the k-th step of this direction's forward pass
+      auto time_at = [&](int k) { return dd == 0 ? k : T - 1 - k; };
+      auto args_for = [&](int k) {
+        const int t = time_at(k), tp = dd == 0 ? t - 1 : t + 1;
+        BwdStepArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.B = B;
+        a.H = H;
+        a.u = h->u;
+        a.gates = reinterpret_cast<const float*>(R + h->rl[v].gates) + (size_t)t * BGH;
+        a.c_s = lstm ? reinterpret_cast<const float*>(R + h->rl[v].c) + (size_t)t * BH : nullptr;
+        a.c_sm1 = lstm ? (k > 0 ? reinterpret_cast<const float*>(R + h->rl[v].c) + (size_t)tp * BH : c0v) : nullptr;
+        a.hn_s = gru ? reinterpret_cast<const float*>(R + h->rl[v].hn) + (size_t)t * BH : nullptr;
+        a.h_sm1 = hseq + hslot(dd, tp) * BH * e;
+        a.dy = dyl + (size_t)t * BH * dy_es;
+        a.dy_f32 = top ? (mode == RNN_MODE_FP32) : 1;
+        a.carry = carry;
+        a.dGx = R + h->rl[v].dgx + (size_t)t * BGH * e;
+        a.dGh = R + h->rl[v].dgh + (size_t)t * BGH * e;
+        a.part = reinterpret_cast<float*>(W + h->wl[v].part);
+        a.counters = reinterpret_cast<int*>(W + h->wl[v].ctr);
+        a.cluster_splitk = 1;
+        return a;
+      };
+      auto point_args = [&](const BwdStepArgs& x, int k) {
+        PointVArgs pv{};
+        pv.B = B;
+        pv.H = H;
+        pv.dy = x.dy;
+        pv.dy_f32 = x.dy_f32;
+        pv.gates = x.gates;
+        pv.c_s = x.c_s;
+        pv.c_sm1 = x.c_sm1;
+        pv.carry = x.carry;
+        pv.dc0 = (k == 0 && dc0 && lstm) ? dc0 + v * BH : nullptr;
+        pv.dGx = x.dGx;
+        return pv;
+      };
+      Operand Bw{PW + h->pl[v].wh, H, 1, H, GH, 1};
+      // the forward steps in reverse order; the product of step k reads the
+      // gate gradients of step k + 1
+      for (int k = T - 1; k >= 0; --k) {
+        BwdStepArgs a = args_for(k);
+        if (k < T - 1) {
+          Operand A{R + h->rl[v].dgh + (size_t)time_at(k + 1) * BGH * e, GH, 0, B, GH};
+          Launch Lk = mk(h, s, ws, "bwd_step");
+          if (h->tstep) {
+            PointVArgs pv = point_args(a, k);
+            float* dhb = reinterpret_cast<float*>(W + h->wl[v].dh);
+            RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, dhb, nullptr, 0,
+                             reinterpret_cast<float*>(W + h->wl[v].part), a.gates, a.c_s, a.c_sm1,
+                             h->bwd_fuse ? &pv : nullptr));
+            if (!h->bwd_fuse) {
+              pv.dh = dhb;
+              Launch Lp = mk(h, s, ws, "bwd_point");
+              RNN_TRY(bwd_point_v(Lp, d.cell, pv));
+            }
+          } else {
+            RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+          }
+        } else {
+          // the direction's last step: dh starts from dhT
+          const char* dh_init = dhT ? static_cast<const char*>(dhT) + v * BH * e : nullptr;
+          Launch Lp = mk(h, s, ws, "bwd_point");
+          if (h->tstep) {
+            PointVArgs pv = point_args(a, k);
+            pv.dh_init = dh_init;
+            RNN_TRY(bwd_point_v(Lp, d.cell, pv));
+          } else {
+            RNN_TRY(bwd_point(Lp, mode, d.cell, a, dh_init));
+          }
+        }
+      }
+      if (dh0 || (dc0 && lstm)) {
+        BwdStepArgs a = args_for(0);
+        a.final_ = 1;
+        a.dh0 = dh0 ? static_cast<char*>(dh0) + v * BH * e : nullptr;
+        a.dc0 = (dc0 && lstm) ? dc0 + v * BH : nullptr;
+        Operand A{R + h->rl[v].dgh + (size_t)time_at(0) * BGH * e, GH, 0, B, GH};
+        Launch Lk = mk(h, s, ws, "bwd_step");
+        if (h->tstep) {
+          // dc0 came out of the first step's pointwise kernel
+          if (dh0)
+            RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, nullptr, a.dh0, 1,
+                             reinterpret_cast<float*>(W + h->wl[v].part)));
+        } else {
+          RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+        }
+      }
+      // gradient of the layer input: dGx W_x, both directions summed
+      Operand A{R + h->rl[v].dgx, GH, 0, T * B, GH};
+      if (l > 0) {
+        // into the gradients from above of the two directions of layer l - 1
+        for (int q = 0; q < 2; ++q) {
+          Operand Bx{PW + h->pl[v].wx + (size_t)q * H * e, 2 * H, 1, H, GH, 1};
+          Launch Lk = mk(h, s, ws, "dx_gemm");
+          RNN_TRY(gemm_f32(Lk, mode, A, Bx, T * B, H, GH, reinterpret_cast<float*>(W + h->wl[2 * (l - 1) + q].dyab), H,
+                           nullptr, dd, none, 0));
+        }
+      } else if (dx) {
+        const int In = d.input;
+        Operand Bx{PW + h->pl[v].wx, In, 1, In, GH, 1};
+        Launch Lk = mk(h, s, ws, "dx_gemm");
+        if (mode == RNN_MODE_FP32) {
+          RNN_TRY(gemm_f32(Lk, mode, A, Bx, T * B, In, GH, static_cast<float*>(dx), In, nullptr, dd, none, 0));
+        } else {
+          float* acc = reinterpret_cast<float*>(W + h->ws_dxacc);
+          RNN_TRY(gemm_f32(Lk, mode, A, Bx, T * B, In, GH, acc, In, nullptr, dd, none, 0));
+          if (dd == 1) {
+            Launch Lc = mk(h, s, ws, "cast");
+            RNN_TRY(cast_bf16(Lc, acc, dx, (size_t)T * B * In));
+          }
+        }
+      }
+    }
+  }
+  return RNN_OK;
+}
+
+int wgrad_bidir(rnn_s* h, const void* x, const char* R, float* dw, int accumulate, void* ws, cudaStream_t s) {
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, G = h->G, GH = h->GH, mode = d.mode;
+  const size_t e = h->elem, BH = (size_t)B * H;
+  const int TB = T * B;
+  const Remap rm{1, G, h->u, H};
+  for (int v = 0; v < 2 * L; ++v) {
+    const int l = v / 2, dd = v % 2;
+    Operand dgx{R + h->rl[v].dgx, GH, 1, GH, TB};
+    Operand dgh{R + h->rl[v].dgh, GH, 1, GH, TB};
+    Launch Lk = mk(h, s, ws, "dw_gemm");
+    if (l == 0) {
+      const int In = d.input;
+      Operand X{x, In, 1, In, TB};
+      RNN_TRY(gemm_f32(Lk, mode, dgx, X, GH, In, TB, dw + h->ul[v].wx, In, nullptr, accumulate, rm, 0));
+    } else {
+      // the two halves of dW_x: inputs from the two directions of layer l - 1
+      for (int q = 0; q < 2; ++q) {
+        Operand X{R + h->rl[2 * (l - 1) + q].hseq + hslot(q, 0) * BH * e, H, 1, H, TB};
+        RNN_TRY(gemm_f32(Lk, mode, dgx, X, GH, H, TB, dw + h->ul[v].wx + (size_t)q * H, 2 * H, nullptr, accumulate, rm,
+                         0));
+      }
+    }
+    // h before the step at time t: slot t (forward) or t + 1 (reverse)
+    Operand Hp{R + h->rl[v].hseq + (size_t)dd * BH * e, H, 1, H, TB};
+    RNN_TRY(gemm_f32(Lk, mode, dgh, Hp, GH, H, TB, dw + h->ul[v].wh, H, nullptr, accumulate, rm, 0));
+    Launch Lb = mk(h, s, ws, "bias_grad");
+    RNN_TRY(bias_grad(Lb, mode, d.cell, H, h->u, TB, R + h->rl[v].dgx, R + h->rl[v].dgh, dw + h->ul[v].bx,
+                      dw + h->ul[v].bh, accumulate, reinterpret_cast<float*>(static_cast<char*>(ws) + h->ws_bias),
+                      h->bias_slices));
+  }
+  return RNN_OK;
+}
+
 }  // namespace
 
 // ======================================================================= C ABI
@@ -575,6 +853,8 @@ int rnn_set_lengths(rnn_handle_t h, const int* lens) {
     for (int b = 0; b < B; ++b)
       if (lens[b] < 1 || lens[b] > T || (b > 0 && lens[b] > lens[b - 1])) return RNN_ERR_INVALID_ARG;
   }
+  // bidirectional stacks run every sequence over all T (lengths not supported)
+  if (h->D == 2 && lens && lens[B - 1] < T) return RNN_ERR_UNSUPPORTED;
   clear_graphs(h);
   h->varlen = (lens && lens[B - 1] < T) ? 1 : 0;
   h->Bt.assign(T + 1, 0);
@@ -605,10 +885,10 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
            "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d transposed=%d fused_point=%d "
-           "persist_cluster=%d",
+           "persist_cluster=%d directions=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
            h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch,
-           h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms, h->tstep, h->bwd_fuse, h->persist ? h->persist_cl : 0);
+           h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms, h->tstep, h->bwd_fuse, h->persist ? h->persist_cl : 0, h->D);
   return RNN_OK;
 }
 
@@ -621,9 +901,9 @@ int rnn_pack_weights(rnn_handle_t h, const void* w_user, void* w_packed, cudaStr
   const char* U = static_cast<const char*>(w_user);
   char* P = static_cast<char*>(w_packed);
   const size_t e = h->elem;
-  for (int l = 0; l < h->d.layers; ++l) {
+  for (int l = 0; l < h->V(); ++l) {
     Launch L = mk(h, stream, nullptr, "pack");
-    RNN_TRY(pack_layer(L, h->d.mode, h->d.cell, h->d.hidden, h->In(l), h->u, U + h->ul[l].wx * e,
+    RNN_TRY(pack_layer(L, h->d.mode, h->d.cell, h->d.hidden, h->In(l / h->D), h->u, U + h->ul[l].wx * e,
                        U + h->ul[l].wh * e, U + h->ul[l].bx * e, U + h->ul[l].bh * e, P + h->pl[l].wx,
                        P + h->pl[l].wh, reinterpret_cast<float*>(P + h->pl[l].bias),
                        reinterpret_cast<float*>(P + h->pl[l].bias_hn)));
@@ -649,6 +929,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
     char* W = static_cast<char*>(ws);
     const char* PW = static_cast<const char*>(w_packed);
     (void)G;
+    if (h->D == 2) return fwd_bidir(h, x, h0, c0, PW, y, hT, cT, R, W, ws, stream);
 
     if (h->varlen) {
       // rows past a sequence's end are never written by the steps: y reads 0
@@ -794,6 +1075,7 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
     char* R = static_cast<char*>(reserve);
     char* W = static_cast<char*>(ws);
     const char* PW = static_cast<const char*>(w_packed);
+    if (h->D == 2) return bwd_bidir(h, dy, dhT, dcT, PW, c0, dx, dh0, dc0, R, W, ws, stream);
 
     for (int l = 0; l < L; ++l)
       RNN_TRY(cu(cudaMemsetAsync(W + h->wl[l].ctr, 0, (size_t)h->ctr_count * 4, stream)));
@@ -978,6 +1260,7 @@ int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* r
     const size_t e = h->elem, BH = (size_t)B * H;
     const char* R = static_cast<const char*>(reserve);
     const int TB = T * B;
+    if (h->D == 2) return wgrad_bidir(h, x, R, dw, accumulate, ws, stream);
     // Each weight-gradient product has (G*H / 128) x (I_l / 256) tiles over
     // K = T*B and fills the GPU by itself: the products run back to back on the
     // caller's stream.

@@ -6,6 +6,8 @@
 // section "제안 방법"): the gate matrices are grouped into one larger product,
 // the input product is independent of the recurrence, and the weight update
 // is a single large product over all timesteps with a cheap bias update.
+#include <algorithm>
+
 #include "epilogues.cuh"
 #include "launch.cuh"
 
@@ -92,6 +94,28 @@ int pack_layer(const Launch& L, int mode, int cell, int H, int In, int u, const 
   }
   cudaError_t e = cudaGetLastError();
   launch_end(L, 3);
+  return cuda_status(e);
+}
+
+// ---------------------------------------------------------------- f32 -> bf16 copy
+__global__ void cast_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const float4 v = src[i];
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    dst[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  }
+}
+
+int cast_bf16(const Launch& L, const float* src, void* dst, size_t n) {
+  if (n % 4 || (reinterpret_cast<uintptr_t>(src) & 15) || (reinterpret_cast<uintptr_t>(dst) & 15))
+    return RNN_ERR_INVALID_ARG;
+  const size_t n4 = n / 4;
+  if (n4 == 0) return RNN_OK;
+  const int blocks = (int)std::min<size_t>((n4 + 255) / 256, (size_t)L.num_sms * 8);
+  launch_begin(L);
+  cast_bf16_kernel<<<blocks, 256, 0, L.stream>>>(reinterpret_cast<const float4*>(src), static_cast<uint2*>(dst), n4);
+  cudaError_t e = cudaGetLastError();
+  launch_end(L);
   return cuda_status(e);
 }
 

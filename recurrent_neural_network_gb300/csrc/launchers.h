@@ -62,6 +62,8 @@ int pack_layer(const Launch& L, int mode, int cell, int H, int In, int u, const 
 // slices * G*H floats.
 int bias_grad(const Launch& L, int mode, int cell, int H, int u, long long rows, const void* dgx, const void* dgh,
               float* dbx, float* dbh, int accumulate, float* part, int slices);
+// dst[i] = src[i] rounded to bf16 (n a multiple of 4; both 16-byte aligned)
+int cast_bf16(const Launch& L, const float* src, void* dst, size_t n);
 
 // ---------------------------------------------------------------- step_fwd.cu
 struct FwdStepArgs {

@@ -31,6 +31,7 @@ FLAG_NO_TRANSPOSED = 0x200
 FLAG_FORCE_TRANSPOSED = 0x400
 FLAG_NO_FUSED_POINT = 0x800
 FLAG_NO_PERSIST_CLUSTER = 0x1000
+FLAG_BIDIRECTIONAL = 0x2000
 
 # every symbol include/rnn.h declares
 SYMBOLS = ["rnn_create", "rnn_destroy", "rnn_get_sizes", "rnn_pack_weights", "rnn_fwd", "rnn_bwd_data",
@@ -131,9 +132,12 @@ class RNN:
         self.h = h
         self.cell, self.layers, self.T, self.B, self.input, self.hidden, self.mode = \
             cell, layers, T, B, input, hidden, mode
+        self.D = 2 if flags & FLAG_BIDIRECTIONAL else 1
 
     @classmethod
     def for_workload(cls, wl: synth.Workload, **kw):
+        if wl.directions == 2:
+            kw["flags"] = kw.get("flags", 0) | FLAG_BIDIRECTIONAL
         return cls(wl.cell, wl.layers, wl.T, wl.B, wl.input, wl.hidden, wl.mode, **kw)
 
     def close(self):

@@ -31,8 +31,8 @@ class HostInputs:
         m = wl.mode
         self.wl = wl
         self.x = as_storage(synth.make_x(wl), m)
-        self.w = np.concatenate([as_storage(synth.layer_weights(wl, l)[k].ravel(), m)
-                                 for l in range(wl.layers) for k in range(4)])
+        self.w = np.concatenate([as_storage(synth.layer_weights(wl, l, d=d)[k].ravel(), m)
+                                 for l in range(wl.layers) for d in range(wl.directions) for k in range(4)])
         self.h0 = as_storage(synth.make_state(wl, "h0"), m)
         self.c0 = as_f32(synth.make_state(wl, "c0")) if wl.cell == synth.CELL_LSTM else None
         self.dy = as_storage(synth.make_dy(wl), m)
@@ -75,13 +75,14 @@ class Runner:
         self.reserve = torch.empty(self.sz["reserve"], **u8) if wl.training else None
         L, T, B, I, H = wl.layers, wl.T, wl.B, wl.input, wl.hidden
         f = dict(dtype=self.dt, device=self.device)
-        self.y = torch.empty(T, B, H, **f)
-        self.hT = torch.empty(L, B, H, **f)
-        self.cT = torch.empty(L, B, H, dtype=torch.float32, device=self.device) if wl.cell == 0 else None
+        S, D = wl.states, wl.directions
+        self.y = torch.empty(T, B, D * H, **f)
+        self.hT = torch.empty(S, B, H, **f)
+        self.cT = torch.empty(S, B, H, dtype=torch.float32, device=self.device) if wl.cell == 0 else None
         if wl.training:
             self.dx = torch.empty(T, B, I, **f)
-            self.dh0 = torch.empty(L, B, H, **f)
-            self.dc0 = torch.empty(L, B, H, dtype=torch.float32, device=self.device) if wl.cell == 0 else None
+            self.dh0 = torch.empty(S, B, H, **f)
+            self.dc0 = torch.empty(S, B, H, dtype=torch.float32, device=self.device) if wl.cell == 0 else None
             self.dw = torch.empty(self.sz["user_weights"] // (2 if wl.mode == 1 else 4), dtype=torch.float32,
                                   device=self.device)
         self.x = self.h0 = self.c0 = self.dy = self.dhT = self.dcT = self.w_user = None

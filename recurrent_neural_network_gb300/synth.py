@@ -123,20 +123,29 @@ class Workload:
     # odd units, so that every pre-activation of a ReLU RNN stays well away
     # from 0 and the activation's on/off decision is the same at any precision
     kink_margin: float = 0.0
+    # 2: bidirectional layers (a second set of weights per layer runs time
+    # backwards; outputs and the next layer's input are 2*hidden wide)
+    directions: int = 1
 
     @property
     def G(self):
         return GATES[self.cell]
 
     def in_size(self, l):
-        return self.input if l == 0 else self.hidden
+        return self.input if l == 0 else self.directions * self.hidden
 
     def layer_weight_count(self, l):
+        """Weights of one direction of layer l."""
         G, H = self.G, self.hidden
         return G * H * self.in_size(l) + G * H * H + 2 * G * H
 
     def weight_count(self):
-        return sum(self.layer_weight_count(l) for l in range(self.layers))
+        return sum(self.directions * self.layer_weight_count(l) for l in range(self.layers))
+
+    @property
+    def states(self):
+        """Rows of the state arrays: one per (layer, direction)."""
+        return self.layers * self.directions
 
     def replace(self, **kw):
         return dataclasses.replace(self, **kw)
@@ -144,7 +153,7 @@ class Workload:
     def gemm_flops(self):
         """Algorithmic GEMM flops (2*M*N*K) of forward, backward-data and weight-gradient passes."""
         G, H, T, B = self.G, self.hidden, self.T, self.B
-        fwd = sum(2.0 * T * B * G * H * (self.in_size(l) + H) for l in range(self.layers))
+        fwd = sum(2.0 * self.directions * T * B * G * H * (self.in_size(l) + H) for l in range(self.layers))
         return {"fwd": fwd, "bwd_data": fwd, "bwd_weights": fwd}
 
 
@@ -164,16 +173,17 @@ WORKLOADS = [
 ]
 
 
-def layer_weights(wl: Workload, l: int, dtype=np.float64):
-    """User-layout weights of layer ``l``: (W_x[G*H][I_l], W_h[G*H][H], b_x[G*H], b_h[G*H]).
+def layer_weights(wl: Workload, l: int, dtype=np.float64, d: int = 0):
+    """User-layout weights of direction ``d`` of layer ``l``:
+    (W_x[G*H][I_l], W_h[G*H][H], b_x[G*H], b_h[G*H]).
 
     W_x and W_h ~ U(-1/sqrt(H), 1/sqrt(H)); biases are zero except the LSTM
     forget gate (gate block 1 of b_x), which gets ``forget_bias``.
     """
     G, H, I = wl.G, wl.hidden, wl.in_size(l)
     a = (0.05 if wl.kink_margin else 1.0) / math.sqrt(H)
-    wx = uniform(wl.seed, 100 + 10 * l + 0, (G * H, I), -a, a).astype(dtype)
-    wh = uniform(wl.seed, 100 + 10 * l + 1, (G * H, H), -a, a).astype(dtype)
+    wx = uniform(wl.seed, 100 + 10 * l + 2 * d, (G * H, I), -a, a).astype(dtype)
+    wh = uniform(wl.seed, 100 + 10 * l + 2 * d + 1, (G * H, H), -a, a).astype(dtype)
     bx = np.zeros(G * H, dtype=dtype)
     bh = np.zeros(G * H, dtype=dtype)
     if wl.cell == CELL_LSTM and wl.forget_bias:
@@ -185,10 +195,11 @@ def layer_weights(wl: Workload, l: int, dtype=np.float64):
 
 
 def flat_weights(wl: Workload, dtype=np.float64) -> np.ndarray:
-    """All layers' user-layout weights concatenated: per layer W_x, W_h, b_x, b_h."""
+    """All layers' user-layout weights concatenated: per (layer, direction) W_x, W_h, b_x, b_h."""
     parts = []
     for l in range(wl.layers):
-        parts.extend(p.ravel() for p in layer_weights(wl, l, dtype))
+        for d in range(wl.directions):
+            parts.extend(p.ravel() for p in layer_weights(wl, l, dtype, d))
     return np.concatenate(parts)
 
 
@@ -201,8 +212,8 @@ def make_x(wl: Workload, T=None, dtype=np.float64):
 
 
 def make_state(wl: Workload, which: str, dtype=np.float64):
-    """h0 or c0, shape [L][B][H]."""
-    shape = (wl.layers, wl.B, wl.hidden)
+    """h0 or c0, shape [L*D][B][H]."""
+    shape = (wl.states, wl.B, wl.hidden)
     if wl.state_std == 0.0:
         return np.zeros(shape, dtype=dtype)
     tid = TID_H0 if which == "h0" else TID_C0
@@ -211,13 +222,13 @@ def make_state(wl: Workload, which: str, dtype=np.float64):
 
 def make_dy(wl: Workload, T=None, dtype=np.float64):
     T = wl.T if T is None else T
-    return normal(wl.seed, TID_DY, (T, wl.B, wl.hidden)).astype(dtype)
+    return normal(wl.seed, TID_DY, (T, wl.B, wl.directions * wl.hidden)).astype(dtype)
 
 
 def make_dstate(wl: Workload, which: str, dtype=np.float64):
-    """dhT or dcT [L][B][H] ~ N(0,1); the benchmark workloads pass none (zero)."""
+    """dhT or dcT [L*D][B][H] ~ N(0,1); the benchmark workloads pass none (zero)."""
     tid = TID_DHT if which == "dhT" else TID_DCT
-    return normal(wl.seed, tid, (wl.layers, wl.B, wl.hidden)).astype(dtype)
+    return normal(wl.seed, tid, (wl.states, wl.B, wl.hidden)).astype(dtype)
 
 
 def round_bf16(a) -> np.ndarray:
@@ -237,20 +248,20 @@ def device_tensor(wl: Workload, what: str, device, dtype):
         else:
             t = normal_t(wl.seed, TID_X, shape, device=device)
     elif what == "dy":
-        t = normal_t(wl.seed, TID_DY, (wl.T, wl.B, wl.hidden), device=device)
+        t = normal_t(wl.seed, TID_DY, (wl.T, wl.B, wl.directions * wl.hidden), device=device)
     elif what in ("h0", "c0"):
-        shape = (wl.layers, wl.B, wl.hidden)
+        shape = (wl.states, wl.B, wl.hidden)
         if wl.state_std == 0.0:
             t = torch.zeros(shape, dtype=torch.float64, device=device)
         else:
             t = normal_t(wl.seed, TID_H0 if what == "h0" else TID_C0, shape, std=wl.state_std, device=device)
     elif what == "w":
         parts = []
-        for l in range(wl.layers):
+        for l, d in ((l, d) for l in range(wl.layers) for d in range(wl.directions)):
             G, H, I = wl.G, wl.hidden, wl.in_size(l)
             a = (0.05 if wl.kink_margin else 1.0) / math.sqrt(H)
-            parts.append(uniform_t(wl.seed, 100 + 10 * l, (G * H * I,), -a, a, device).to(torch.float32))
-            parts.append(uniform_t(wl.seed, 100 + 10 * l + 1, (G * H * H,), -a, a, device).to(torch.float32))
+            parts.append(uniform_t(wl.seed, 100 + 10 * l + 2 * d, (G * H * I,), -a, a, device).to(torch.float32))
+            parts.append(uniform_t(wl.seed, 100 + 10 * l + 2 * d + 1, (G * H * H,), -a, a, device).to(torch.float32))
             bx = torch.zeros(G * H, dtype=torch.float32, device=device)
             if wl.cell == CELL_LSTM and wl.forget_bias:
                 bx[H:2 * H] = wl.forget_bias

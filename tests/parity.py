@@ -25,11 +25,12 @@ BF16_REL_L2 = 2e-2
 
 def run_oracle(hi: runner.HostInputs, train=True, lens=None):
     w = hi.wl
-    y, hT, cT = oracle.fwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0, lens=lens)
+    y, hT, cT = oracle.fwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0, lens=lens,
+                           D=w.directions)
     out = dict(y=y, hT=hT, cT=cT)
     if train:
         dx, dh0, dc0, dw = oracle.bwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, hi.dy, h0=hi.h0,
-                                      c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT, lens=lens)
+                                      c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT, lens=lens, D=w.directions)
         out.update(dx=dx, dh0=dh0, dc0=dc0, dw=dw)
     return out
 
@@ -69,7 +70,7 @@ def rel_l2(g, o):
 def weight_blocks(wl, dw):
     """(name, array) per layer and part of a user-layout gradient vector."""
     out = []
-    for l, parts in enumerate(oracle.split_weights(wl.cell, wl.layers, wl.input, wl.hidden, dw)):
+    for l, parts in enumerate(oracle.split_weights(wl.cell, wl.layers, wl.input, wl.hidden, dw, D=wl.directions)):
         for nm, a in zip(("dWx", "dWh", "dbx", "dbh"), parts):
             out.append((f"l{l}.{nm}", a))
     return out

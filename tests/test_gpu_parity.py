@@ -388,3 +388,45 @@ def test_variable_lengths(case):
     for b, n in enumerate(lens):
         assert not np.any(g["y"][n:, b]), b
         assert not np.any(g["dx"][n:, b]), b
+
+
+# ---------------------------------------------------------------- bidirectional layers
+
+BIDIR = [
+    # cell, mode, flags, (L, T, B, I, H)
+    (0, synth.MODE_BF16, 0, (2, 7, 9, 72, 128)),                              # row-major steps
+    (0, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED, (2, 6, 9, 72, 256)),      # transposed, separate pointwise
+    (0, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED, (2, 5, 200, 64, 256)),    # transposed, fused pointwise
+    (1, synth.MODE_BF16, 0, (2, 6, 9, 72, 128)),
+    (2, synth.MODE_BF16, 0, (3, 5, 9, 72, 128)),
+    (3, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED, (2, 6, 9, 72, 256)),
+    (0, synth.MODE_FP32, 0, (2, 5, 5, 40, 64)),
+    (1, synth.MODE_FP32, 0, (2, 5, 5, 40, 64)),
+    (2, synth.MODE_FP32, 0, (1, 4, 3, 36, 32)),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", BIDIR, ids=lambda c: "c%d_m%d_f%x_L%d_T%d_B%d_I%d_H%d" % (c[0], c[1], c[2], *c[3]))
+def test_bidirectional(case):
+    """Bidirectional stacks against the oracle: y = [forward, reverse] per
+    timestep, final states and their gradients per (layer, direction), dx and
+    every weight block; twice through the same handle (direct call, then the
+    captured graph)."""
+    cell, mode, flags, (L, T, B, I, H) = case
+    wl = synth.Workload(name="bidir", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
+                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0, directions=2)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    g = run_gpu(wl, hi, flags=flags, repeat=2)
+    compare(wl, g, run_oracle(hi))
+
+
+@pytest.mark.gpu
+def test_bidirectional_inference_matches_training_forward():
+    wl = synth.Workload(name="bidir", cell=0, layers=2, T=6, B=9, input=72, hidden=128, mode=synth.MODE_BF16,
+                        forget_bias=1.0, state_std=0.3, directions=2)
+    hi = runner.HostInputs(wl)
+    a = run_gpu(wl.replace(training=False), hi)
+    b = run_gpu(wl, hi, train=True)
+    for k in ("y", "hT", "cT"):
+        assert np.array_equal(a[k], b[k]), k
