@@ -172,9 +172,11 @@ def time_oracle_sample(wl, budget_s=20.0):
     hi = runner.HostInputs(sw)
     t0 = time.perf_counter()
     if wl.training:
-        oracle.bwd(sw.cell, sw.layers, sw.T, sw.B, sw.input, sw.hidden, hi.x, hi.w, hi.dy, h0=hi.h0, c0=hi.c0)
+        oracle.bwd(sw.cell, sw.layers, sw.T, sw.B, sw.input, sw.hidden, hi.x, hi.w, hi.dy, h0=hi.h0, c0=hi.c0,
+                   D=sw.directions)
     else:
-        oracle.fwd(sw.cell, sw.layers, sw.T, sw.B, sw.input, sw.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0)
+        oracle.fwd(sw.cell, sw.layers, sw.T, sw.B, sw.input, sw.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0,
+                   D=sw.directions)
     dt = time.perf_counter() - t0
     fl = step_flops(sw)
     return dict(value=fl / dt / 1e12, unit="TFLOP/s", cores=oracle.threads(), kind="oracle",

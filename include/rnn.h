@@ -84,7 +84,8 @@ enum {
 };
 
 /* rnn_desc_t.flags */
-#define RNN_FLAG_NO_WAVEFRONT 0x1u      /* run layers one after another (no overlap) */
+#define RNN_FLAG_NO_WAVEFRONT 0x1u      /* run layers (and the two directions of a bidirectional layer)
+                                           one after another (no overlap) */
 #define RNN_FLAG_FORCE_STREAMING 0x2u   /* never use the persistent recurrence */
 #define RNN_FLAG_FORCE_PERSISTENT 0x4u  /* use the persistent recurrence or fail */
 #define RNN_FLAG_PROFILE 0x8u           /* record per-kernel CUDA-event timings */

@@ -350,14 +350,15 @@ int ensure_runtime(rnn_s* h) {
   if (!h->have_device) return RNN_ERR_CUDA;
   if (!h->streams.empty() || h->d.layers == 0) return RNN_OK;
   const int L = h->d.layers;
-  h->streams.resize(L);
-  for (int l = 0; l < L; ++l)
+  const int NS = std::max(L, h->D);  // one stream per layer (wavefront) or per direction
+  h->streams.resize(NS);
+  for (int l = 0; l < NS; ++l)
     if (cudaStreamCreateWithFlags(&h->streams[l], cudaStreamNonBlocking) != cudaSuccess) return RNN_ERR_CUDA;
   h->ev.resize((size_t)L * h->nch);
   for (auto& e : h->ev)
     if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return RNN_ERR_CUDA;
   if (cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess) return RNN_ERR_CUDA;
-  h->ev_join.resize(L);
+  h->ev_join.resize(NS);
   for (auto& e : h->ev_join)
     if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return RNN_ERR_CUDA;
   return RNN_OK;
@@ -497,8 +498,9 @@ int cu(cudaError_t e) { return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA; }
 // 0..T-1 (slot T = its h0), so the next layer's input, dW_x and dW_h read
 // plain strided operands.  A layer's input of width 2H enters its products as
 // two halves of K (the second product accumulating).  Layers run one after
-// another (layer l + 1 needs all of layer l's reverse direction), directions
-// one after the other, all on the caller's stream.
+// another (layer l + 1 needs all of layer l's reverse direction); the two
+// directions of a layer run side by side on two streams, forked from and
+// joined back into the caller's stream around each layer.
 
 // slot of h at time t in direction d (t = -1 forward, t = T reverse: the initial state)
 size_t hslot(int d, int t) { return (size_t)(t + 1 - d); }
@@ -512,9 +514,13 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
   const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
   const Remap none{0, 1, 1, 1};
   auto hseq_of = [&](int v) -> char* { return train ? R + h->rl[v].hseq : W + h->wl[v].hseq; };
+  cudaStream_t caller = s;
+  const bool side = !(d.flags & RNN_FLAG_NO_WAVEFRONT);  // directions side by side
   for (int l = 0; l < L; ++l) {
+    if (side) RNN_TRY(fork_streams(h, caller));
     for (int dd = 0; dd < 2; ++dd) {
       const int v = 2 * l + dd;
+      s = side ? h->streams[dd] : caller;
       char* hseq = hseq_of(v);
       float* P = reinterpret_cast<float*>(train ? R + h->rl[v].gates : W + h->wl[v].P);
       char* hinit = hseq + hslot(dd, dd == 0 ? -1 : T) * BH * e;
@@ -573,6 +579,7 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
         RNN_TRY(cu(cudaMemcpy2DAsync(static_cast<char*>(y) + (size_t)dd * H * e, 2 * H * e, hseq + hslot(dd, 0) * BH * e,
                                      H * e, H * e, (size_t)T * B, cudaMemcpyDeviceToDevice, s)));
     }
+    if (side) RNN_TRY(join_streams(h, caller));
   }
   return RNN_OK;
 }
@@ -591,9 +598,13 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
     RNN_TRY(cu(cudaMemcpy2DAsync(W + h->ws_dtop + (size_t)dd * T * BH * e, H * e,
                                  static_cast<const char*>(dy) + (size_t)dd * H * e, 2 * H * e, H * e, (size_t)T * B,
                                  cudaMemcpyDeviceToDevice, s)));
+  cudaStream_t caller = s;
+  const bool side = !(d.flags & RNN_FLAG_NO_WAVEFRONT);  // directions side by side
   for (int l = L - 1; l >= 0; --l) {
+    if (side) RNN_TRY(fork_streams(h, caller));
     for (int dd = 0; dd < 2; ++dd) {
       const int v = 2 * l + dd;
+      s = side ? h->streams[dd] : caller;
       const bool top = l == L - 1;
       const char* dyl = top ? W + h->ws_dtop + (size_t)dd * T * BH * e : W + h->wl[v].dyab;
       const size_t dy_es = top ? e : 4;
@@ -693,7 +704,13 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
           RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
         }
       }
-      // gradient of the layer input: dGx W_x, both directions summed
+    }
+    if (side) RNN_TRY(join_streams(h, caller));
+    // gradient of the layer input: dGx W_x, both directions summed (on the
+    // caller's stream, one product after the other)
+    s = caller;
+    for (int dd = 0; dd < 2; ++dd) {
+      const int v = 2 * l + dd;
       Operand A{R + h->rl[v].dgx, GH, 0, T * B, GH};
       if (l > 0) {
         // into the gradients from above of the two directions of layer l - 1

@@ -157,7 +157,7 @@ class Workload:
         return {"fwd": fwd, "bwd_data": fwd, "bwd_weights": fwd}
 
 
-# The benchmark workloads (index 0 .. 4) and one cell-variant workload (5).
+# The benchmark workloads (index 0 .. 4), a cell-variant workload (5) and a bidirectional stack (6).
 WORKLOADS = [
     Workload("lstm_fp32_L1_T8_B4_H32", CELL_LSTM, 1, 8, 4, 32, 32, MODE_FP32,
              x_dist="uniform", forget_bias=1.0),
@@ -170,6 +170,9 @@ WORKLOADS = [
     Workload("gru_bf16_L8_T200_B32_H1024", CELL_GRU, 8, 200, 32, 1024, 1024, MODE_BF16),
     # cell variant beyond the five: a 4-layer ReLU simple RNN, wide enough for the transposed steps
     Workload("relu_bf16_L4_T100_B256_H2048", CELL_RELU, 4, 100, 256, 2048, 2048, MODE_BF16, kink_margin=0.75),
+    # bidirectional stack (beyond the five): 2 layers x 2 directions of a bf16 LSTM
+    Workload("lstm_bf16_L2_T100_B128_H2048_bidir", CELL_LSTM, 2, 100, 128, 2048, 2048, MODE_BF16,
+             forget_bias=1.0, directions=2),
 ]
 
 

@@ -142,6 +142,10 @@ def test_workload_relu_4layer_sampled_columns():
     masked_columns_check(synth.WORKLOADS[5], [3, 250])
 
 
+def test_workload_bidirectional_lstm_sampled_columns():
+    masked_columns_check(synth.WORKLOADS[6], [77])
+
+
 # ---------------------------------------------------------------- persistent recurrence
 
 PERSIST_CASES = [
@@ -403,6 +407,7 @@ BIDIR = [
     (0, synth.MODE_FP32, 0, (2, 5, 5, 40, 64)),
     (1, synth.MODE_FP32, 0, (2, 5, 5, 40, 64)),
     (2, synth.MODE_FP32, 0, (1, 4, 3, 36, 32)),
+    (0, synth.MODE_BF16, rnn.FLAG_NO_WAVEFRONT, (2, 6, 9, 72, 128)),        # directions one after the other
 ]
 
 
