@@ -57,13 +57,15 @@ def test_buffer_sizes_cover_the_layouts(lib, wl):
     s = r.sizes()
     e = 2 if wl.mode == 1 else 4
     assert s["user_weights"] == wl.weight_count() * e
-    G, L, T, B, H = wl.G, wl.layers, wl.T, wl.B, wl.hidden
-    # reserve holds at least: gates (f32) + h sequence (T+1 slots) + gate gradients, per layer
-    floor = L * (T * B * G * H * 4 + (T + 1) * B * H * e + T * B * G * H * e)
+    G, L, T, B, H, D = wl.G, wl.layers, wl.T, wl.B, wl.hidden, wl.directions
+    # reserve holds at least: gates (f32) + h sequence (T+1 slots) + gate gradients, per (layer, direction)
+    floor = L * D * (T * B * G * H * 4 + (T + 1) * B * H * e + T * B * G * H * e)
     assert s["reserve"] >= floor
-    mats = sum(G * H * (wl.in_size(l) + H) for l in range(L))
-    assert s["packed_weights"] >= mats * e + L * G * H * 4   # matrices in storage type + float biases
-    assert "wavefront=%d" % (1 if L > 1 else 0) in r.describe()
+    mats = D * sum(G * H * (wl.in_size(l) + H) for l in range(L))
+    assert s["packed_weights"] >= mats * e + L * D * G * H * 4   # matrices in storage type + float biases
+    # the wavefront overlaps unidirectional layers; bidirectional ones overlap their directions instead
+    assert "wavefront=%d" % (1 if L > 1 and D == 1 else 0) in r.describe()
+    assert "directions=%d" % D in r.describe()
 
 
 def test_calls_validate_arguments_before_any_device_work(lib):
