@@ -516,6 +516,14 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
   auto hseq_of = [&](int v) -> char* { return train ? R + h->rl[v].hseq : W + h->wl[v].hseq; };
   cudaStream_t caller = s;
   const bool side = !(d.flags & RNN_FLAG_NO_WAVEFRONT);  // directions side by side
+  // variable lengths: running sequences at time t are rows 0 .. Bt[t]-1 in
+  // both directions; idle positions of y and of the h sequences read 0
+  const bool vl = h->varlen != 0;
+  auto Bt = [&](int t) { return vl ? h->Bt[t] : (t < T ? B : 0); };
+  if (vl) {
+    RNN_TRY(cu(cudaMemsetAsync(y, 0, (size_t)T * BH * 2 * e, caller)));
+    for (int v = 0; v < 2 * L; ++v) RNN_TRY(cu(cudaMemsetAsync(hseq_of(v), 0, (size_t)(T + 1) * BH * e, caller)));
+  }
   for (int l = 0; l < L; ++l) {
     if (side) RNN_TRY(fork_streams(h, caller));
     for (int dd = 0; dd < 2; ++dd) {
@@ -552,32 +560,75 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
       // the recurrence: step k at time t, after the step at time tp
       for (int k = 0; k < T; ++k) {
         const int t = dd == 0 ? k : T - 1 - k, tp = dd == 0 ? t - 1 : t + 1;
+        const int Bs = Bt(t);
+        if (Bs == 0) continue;
+        if (dd == 1 && vl && t < T - 1) {
+          // rows Bt[t+1] .. Bs-1 start their reverse sweep here: h_prev and c_prev from h0, c0
+          const int r0 = Bt(t + 1), nr = Bs - r0;
+          if (nr > 0) {
+            char* hp = hseq + hslot(dd, tp) * BH * e + (size_t)r0 * H * e;
+            if (h0)
+              RNN_TRY(cu(cudaMemcpyAsync(hp, static_cast<const char*>(h0) + (v * BH + (size_t)r0 * H) * e,
+                                         (size_t)nr * H * e, cudaMemcpyDeviceToDevice, s)));
+            else
+              RNN_TRY(cu(cudaMemsetAsync(hp, 0, (size_t)nr * H * e, s)));
+            if (lstm) {
+              float* cp = cbuf(tp) + (size_t)r0 * H;
+              if (c0)
+                RNN_TRY(cu(cudaMemcpyAsync(cp, c0 + v * BH + (size_t)r0 * H, (size_t)nr * H * 4,
+                                           cudaMemcpyDeviceToDevice, s)));
+              else
+                RNN_TRY(cu(cudaMemsetAsync(cp, 0, (size_t)nr * H * 4, s)));
+            }
+          }
+        }
         FwdStepArgs a;
-        a.B = B;
+        a.B = Bs;
         a.H = H;
         a.u = h->u;
         a.P = P + (size_t)t * BGH;
         a.write_gates = train ? 1 : 0;
         a.bias_hn = reinterpret_cast<const float*>(PW + h->pl[v].bias_hn);
-        a.c_prev = lstm ? (k == 0 ? (c0 ? c0 + v * BH : nullptr) : cbuf(tp)) : nullptr;
+        a.c_prev = lstm ? (t == (dd == 0 ? 0 : T - 1) ? (c0 ? c0 + v * BH : nullptr) : cbuf(tp)) : nullptr;
         a.c_out = lstm ? cbuf(t) : nullptr;
         a.h_prev = hseq + hslot(dd, tp) * BH * e;
         a.h_out = hseq + hslot(dd, t) * BH * e;
         a.y = nullptr;
-        a.hT = (k == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)v * BH * e : nullptr;
-        a.cT = (k == T - 1 && cT && lstm) ? cT + (size_t)v * BH : nullptr;
+        // final states: after t = T-1 forward (or each sequence's own last
+        // time, copied below), after t = 0 in reverse (every sequence runs it)
+        const bool fin = dd == 0 ? (!vl && t == T - 1) : t == 0;
+        a.hT = (fin && hT) ? static_cast<char*>(hT) + (size_t)v * BH * e : nullptr;
+        a.cT = (fin && cT && lstm) ? cT + (size_t)v * BH : nullptr;
         a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[v].hn) + (size_t)t * BH : nullptr;
         a.mcast = h->fwd_mcast;
-        Operand A{a.h_prev, H, 0, B, H};
+        Operand A{a.h_prev, H, 0, Bs, H};
         Operand Bw{PW + h->pl[v].wh, H, 0, GH, H, 1};
         Launch Lk = mk(h, s, ws, "fwd_step");
         if (h->tstep) RNN_TRY(fwd_step_t(Lk, d.cell, Bw, A, a));
         else RNN_TRY(fwd_step(Lk, mode, d.cell, A, Bw, a));
+        if (dd == 0 && vl) {
+          // sequences ending at time t (rows Bt[t+1] .. Bs-1): final states
+          const int r0 = Bt(t + 1), nr = Bs - r0;
+          if (nr > 0 && hT)
+            RNN_TRY(cu(cudaMemcpyAsync(static_cast<char*>(hT) + ((size_t)v * BH + (size_t)r0 * H) * e,
+                                       static_cast<const char*>(a.h_out) + (size_t)r0 * H * e, (size_t)nr * H * e,
+                                       cudaMemcpyDeviceToDevice, s)));
+          if (nr > 0 && cT && lstm)
+            RNN_TRY(cu(cudaMemcpyAsync(cT + (size_t)v * BH + (size_t)r0 * H, a.c_out + (size_t)r0 * H,
+                                       (size_t)nr * H * 4, cudaMemcpyDeviceToDevice, s)));
+        }
       }
       // the top layer's output y[T][B][2H] = [h_forward(t), h_reverse(t)]
-      if (l == L - 1)
+      if (l == L - 1) {
         RNN_TRY(cu(cudaMemcpy2DAsync(static_cast<char*>(y) + (size_t)dd * H * e, 2 * H * e, hseq + hslot(dd, 0) * BH * e,
                                      H * e, H * e, (size_t)T * B, cudaMemcpyDeviceToDevice, s)));
+        // the reverse h sequence holds h0 rows where sequences start: y is 0 at idle positions
+        if (dd == 1 && vl)
+          for (int t = 0; t < T; ++t)
+            if (Bt(t) < B)
+              RNN_TRY(cu(cudaMemset2DAsync(static_cast<char*>(y) + ((size_t)t * B + Bt(t)) * 2 * H * e + H * e,
+                                           2 * H * e, 0, H * e, (size_t)(B - Bt(t)), s)));
+      }
     }
     if (side) RNN_TRY(join_streams(h, caller));
   }
@@ -593,6 +644,16 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
   const Remap none{0, 1, 1, 1};
   for (int v = 0; v < 2 * L; ++v)
     RNN_TRY(cu(cudaMemsetAsync(W + h->wl[v].ctr, 0, (size_t)h->ctr_count * 4, s)));
+  // variable lengths: rows 0 .. Bt[t]-1 run at time t; the gate gradients of
+  // idle positions are never written, so they start at zero for the products
+  // that read every row (dx, dW)
+  const bool vl = h->varlen != 0;
+  auto Bt = [&](int t) { return vl ? h->Bt[t] : (t < T ? B : 0); };
+  if (vl)
+    for (int v = 0; v < 2 * L; ++v) {
+      RNN_TRY(cu(cudaMemsetAsync(R + h->rl[v].dgx, 0, (size_t)T * BGH * e, s)));
+      if (h->rl[v].dgh != h->rl[v].dgx) RNN_TRY(cu(cudaMemsetAsync(R + h->rl[v].dgh, 0, (size_t)T * BGH * e, s)));
+    }
   // the two halves of dy, each [T][B][H]
   for (int dd = 0; dd < 2; ++dd)
     RNN_TRY(cu(cudaMemcpy2DAsync(W + h->ws_dtop + (size_t)dd * T * BH * e, H * e,
@@ -639,9 +700,22 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
         a.cluster_splitk = 1;
         return a;
       };
-      auto point_args = [&](const BwdStepArgs& x, int k) {
+      // the arguments of args_for moved down by r0 batch rows
+      auto offset_rows = [&](BwdStepArgs x, int r0) {
+        x.gates += (size_t)r0 * GH;
+        if (x.c_s) x.c_s += (size_t)r0 * H;
+        if (x.c_sm1) x.c_sm1 += (size_t)r0 * H;
+        if (x.hn_s) x.hn_s += (size_t)r0 * H;
+        if (x.h_sm1) x.h_sm1 = static_cast<const char*>(x.h_sm1) + (size_t)r0 * H * e;
+        x.dy = static_cast<const char*>(x.dy) + (size_t)r0 * H * dy_es;
+        x.carry += (size_t)r0 * H;
+        x.dGx = static_cast<char*>(x.dGx) + (size_t)r0 * GH * e;
+        x.dGh = static_cast<char*>(x.dGh) + (size_t)r0 * GH * e;
+        return x;
+      };
+      auto point_args = [&](const BwdStepArgs& x, int k, int r0, int rows) {
         PointVArgs pv{};
-        pv.B = B;
+        pv.B = rows;
         pv.H = H;
         pv.dy = x.dy;
         pv.dy_f32 = x.dy_f32;
@@ -649,25 +723,36 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
         pv.c_s = x.c_s;
         pv.c_sm1 = x.c_sm1;
         pv.carry = x.carry;
-        pv.dc0 = (k == 0 && dc0 && lstm) ? dc0 + v * BH : nullptr;
+        pv.dc0 = (k == 0 && dc0 && lstm) ? dc0 + v * BH + (size_t)r0 * H : nullptr;
         pv.dGx = x.dGx;
         return pv;
       };
       Operand Bw{PW + h->pl[v].wh, H, 1, H, GH, 1};
-      // the forward steps in reverse order; the product of step k reads the
-      // gate gradients of step k + 1
+      const char* dhTv = dhT ? static_cast<const char*>(dhT) + v * BH * e : nullptr;
+      // the forward steps in reverse order.  Rows 0 .. Bn-1 take the product
+      // of the gate gradients of the forward step after this one (time tn);
+      // rows Bn .. Bs-1 start from dhT (forward: sequences ending at t)
       for (int k = T - 1; k >= 0; --k) {
-        BwdStepArgs a = args_for(k);
-        if (k < T - 1) {
-          Operand A{R + h->rl[v].dgh + (size_t)time_at(k + 1) * BGH * e, GH, 0, B, GH};
+        const int t = time_at(k), tn = dd == 0 ? t + 1 : t - 1;
+        const int Bs = Bt(t);
+        if (Bs == 0) continue;
+        const int Bn = k == T - 1 ? 0 : (dd == 0 ? Bt(t + 1) : Bs);
+        if (Bn > 0) {
+          BwdStepArgs a = args_for(k);
+          a.B = Bn;
+          Operand A{R + h->rl[v].dgh + (size_t)tn * BGH * e, GH, 0, Bn, GH};
           Launch Lk = mk(h, s, ws, "bwd_step");
           if (h->tstep) {
-            PointVArgs pv = point_args(a, k);
+            PointVArgs pv = point_args(a, k, 0, Bn);
+            const int bnn = Bn > 128 ? 256 : Bn > 64 ? 128 : 64;
+            int sp = h->bwd_splits;
+            while (sp > 1 && bnn % (16 * sp)) sp /= 2;
+            const bool fuse = h->bwd_fuse && bnn == 256 && sp == 4;
             float* dhb = reinterpret_cast<float*>(W + h->wl[v].dh);
-            RNN_TRY(bwd_dh_t(Lk, Bw, A, B, H, h->G, h->bwd_bn, h->bwd_splits, dhb, nullptr, 0,
+            RNN_TRY(bwd_dh_t(Lk, Bw, A, Bn, H, h->G, bnn, sp, dhb, nullptr, 0,
                              reinterpret_cast<float*>(W + h->wl[v].part), a.gates, a.c_s, a.c_sm1,
-                             h->bwd_fuse ? &pv : nullptr));
-            if (!h->bwd_fuse) {
+                             fuse ? &pv : nullptr));
+            if (!fuse) {
               pv.dh = dhb;
               Launch Lp = mk(h, s, ws, "bwd_point");
               RNN_TRY(bwd_point_v(Lp, d.cell, pv));
@@ -675,20 +760,49 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
           } else {
             RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
           }
-        } else {
-          // the direction's last step: dh starts from dhT
-          const char* dh_init = dhT ? static_cast<const char*>(dhT) + v * BH * e : nullptr;
+        }
+        if (Bs > Bn) {
+          BwdStepArgs ar = offset_rows(args_for(k), Bn);
+          ar.B = Bs - Bn;
+          const char* dh_init = dhTv ? dhTv + (size_t)Bn * H * e : nullptr;
           Launch Lp = mk(h, s, ws, "bwd_point");
           if (h->tstep) {
-            PointVArgs pv = point_args(a, k);
+            PointVArgs pv = point_args(ar, k, Bn, Bs - Bn);
             pv.dh_init = dh_init;
             RNN_TRY(bwd_point_v(Lp, d.cell, pv));
           } else {
-            RNN_TRY(bwd_point(Lp, mode, d.cell, a, dh_init));
+            RNN_TRY(bwd_point(Lp, mode, d.cell, ar, dh_init));
           }
         }
+        // reverse direction with variable lengths: rows Bt[t+1] .. Bs-1 began
+        // their sweep at t, so their dh0 and dc0 are due now
+        if (dd == 1 && vl) {
+          const int r0 = Bt(t + 1), nr = Bs - r0;
+          if (nr > 0 && dh0) {
+            BwdStepArgs a = offset_rows(args_for(k), r0);
+            a.B = nr;
+            a.final_ = 1;
+            a.dh0 = static_cast<char*>(dh0) + ((size_t)v * BH + (size_t)r0 * H) * e;
+            a.dc0 = nullptr;
+            Operand A{R + h->rl[v].dgh + ((size_t)t * BGH + (size_t)r0 * GH) * e, GH, 0, nr, GH};
+            Launch Lk = mk(h, s, ws, "bwd_step");
+            if (h->tstep) {
+              const int bnn = nr > 128 ? 256 : nr > 64 ? 128 : 64;
+              int sp = h->bwd_splits;
+              while (sp > 1 && bnn % (16 * sp)) sp /= 2;
+              RNN_TRY(bwd_dh_t(Lk, Bw, A, nr, H, h->G, bnn, sp, nullptr, a.dh0, 1,
+                               reinterpret_cast<float*>(W + h->wl[v].part)));
+            } else {
+              RNN_TRY(bwd_step(Lk, mode, d.cell, A, Bw, h->bwd_bn, h->bwd_splits, a));
+            }
+          }
+          // the carry out of the sequence's first step is its dc0
+          if (nr > 0 && dc0 && lstm)
+            RNN_TRY(cu(cudaMemcpyAsync(dc0 + v * BH + (size_t)r0 * H, carry + (size_t)r0 * H, (size_t)nr * H * 4,
+                                       cudaMemcpyDeviceToDevice, s)));
+        }
       }
-      if (dh0 || (dc0 && lstm)) {
+      if (!(dd == 1 && vl) && (dh0 || (dc0 && lstm))) {
         BwdStepArgs a = args_for(0);
         a.final_ = 1;
         a.dh0 = dh0 ? static_cast<char*>(dh0) + v * BH * e : nullptr;
@@ -870,8 +984,6 @@ int rnn_set_lengths(rnn_handle_t h, const int* lens) {
     for (int b = 0; b < B; ++b)
       if (lens[b] < 1 || lens[b] > T || (b > 0 && lens[b] > lens[b - 1])) return RNN_ERR_INVALID_ARG;
   }
-  // bidirectional stacks run every sequence over all T (lengths not supported)
-  if (h->D == 2 && lens && lens[B - 1] < T) return RNN_ERR_UNSUPPORTED;
   clear_graphs(h);
   h->varlen = (lens && lens[B - 1] < T) ? 1 : 0;
   h->Bt.assign(T + 1, 0);

@@ -435,3 +435,35 @@ def test_bidirectional_inference_matches_training_forward():
     b = run_gpu(wl, hi, train=True)
     for k in ("y", "hT", "cT"):
         assert np.array_equal(a[k], b[k]), k
+
+
+BIDIR_VARLEN = [
+    # cell, mode, flags, (L, T, B, I, H)
+    (0, synth.MODE_BF16, 0, (2, 7, 9, 72, 128)),
+    (0, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED, (2, 7, 9, 72, 256)),
+    (0, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED, (2, 6, 200, 64, 256)),
+    (1, synth.MODE_BF16, 0, (2, 7, 9, 72, 128)),
+    (2, synth.MODE_BF16, 0, (2, 7, 9, 72, 128)),
+    (3, synth.MODE_BF16, rnn.FLAG_FORCE_TRANSPOSED, (2, 7, 9, 72, 256)),
+    (0, synth.MODE_FP32, 0, (2, 7, 5, 40, 64)),
+    (1, synth.MODE_FP32, 0, (2, 7, 5, 40, 64)),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", BIDIR_VARLEN, ids=lambda c: "c%d_m%d_f%x_L%d_T%d_B%d_I%d_H%d" % (c[0], c[1], c[2], *c[3]))
+def test_bidirectional_variable_lengths(case):
+    """Bidirectional stacks with sequences of different lengths: the reverse
+    sweep of each sequence starts at its own last step from its h0; y is zero
+    past each end in both halves; every gradient against the oracle; twice
+    through the same handle."""
+    cell, mode, flags, (L, T, B, I, H) = case
+    wl = synth.Workload(name="bivar", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
+                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0, directions=2)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    lens = _lengths(T, B, seed=3 * B + T + cell)
+    g = run_gpu(wl, hi, flags=flags, lens=lens, repeat=2)
+    compare(wl, g, run_oracle(hi, lens=lens))
+    for b, n in enumerate(lens):
+        assert not np.any(g["y"][n:, b]), b
+        assert not np.any(g["dx"][n:, b]), b

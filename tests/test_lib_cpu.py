@@ -176,7 +176,7 @@ def test_set_lengths_validation_and_plan(lib):
 def test_bidirectional_plan_and_sizes(lib):
     """Bidirectional stacks: two weight sets per layer (the next layer's input
     is 2H wide), states per (layer, direction), no wavefront, no persistent
-    recurrence, no variable lengths."""
+    recurrence; lengths are accepted."""
     import oracle
     for cell, mode in ((0, 1), (1, 1), (2, 0), (3, 1)):
         L, T, B, I, H = 3, 10, 4, 64, 128
@@ -189,9 +189,8 @@ def test_bidirectional_plan_and_sizes(lib):
         assert "directions=1" in uni.describe()
         assert r.sizes()["reserve"] > uni.sizes()["reserve"]
     r = rnn.RNN(0, 1, 10, 4, 64, 1024, 1, flags=rnn.FLAG_BIDIRECTIONAL)
-    with pytest.raises(rnn.RnnError) as e:
-        r.set_lengths([10, 7, 7, 2])
-    assert e.value.code == -2
-    r.set_lengths([10, 10, 10, 10])
+    r.set_lengths([10, 7, 7, 2])
+    assert "recurrence=streaming" in r.describe()
+    r.set_lengths(None)
     with pytest.raises(rnn.RnnError):
         rnn.RNN(0, 1, 10, 4, 64, 1024, 1, flags=rnn.FLAG_BIDIRECTIONAL | rnn.FLAG_FORCE_PERSISTENT)
