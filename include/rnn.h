@@ -48,7 +48,7 @@
  *     the state arrays are [layers*D][B][hidden] indexed by v, and hT of the
  *     reverse direction is its state after t = 0.  With rnn_set_lengths()
  *     the reverse direction of each sequence starts at its own last step
- *     from its h0.  Bidirectional stacks do not use the persistent recurrence.
+ *     from its h0.  Small batches run each direction as one persistent launch.
  *   - Pointers must be 16-byte aligned.  Shapes: in RNN_MODE_BF16 hidden must
  *     be a multiple of 64 and input of 8; in RNN_MODE_FP32 hidden a multiple
  *     of 32 and input of 4 (RNN_ERR_UNSUPPORTED otherwise).

@@ -211,8 +211,8 @@ int plan_and_layout(rnn_s* h) {
 
   // persistent recurrence for small batches (weights on-chip, one launch per
   // layer); it runs layer after layer, so it replaces the wavefront.
-  // (not for bidirectional stacks: its hand-off runs time forwards only)
-  if (d.mode == RNN_MODE_BF16 && !(d.flags & RNN_FLAG_FORCE_STREAMING) && h->D == 1) {
+  // (bidirectional stacks: one launch per direction, the reverse one walking time backwards)
+  if (d.mode == RNN_MODE_BF16 && !(d.flags & RNN_FLAG_FORCE_STREAMING)) {
     int ctas = 0;
     int cl = 4;  // without a device: the size that co-resides on GB300 for 128 CTAs
     const bool fits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &ctas, &cl) == RNN_OK
@@ -515,7 +515,9 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
   const Remap none{0, 1, 1, 1};
   auto hseq_of = [&](int v) -> char* { return train ? R + h->rl[v].hseq : W + h->wl[v].hseq; };
   cudaStream_t caller = s;
-  const bool side = !(d.flags & RNN_FLAG_NO_WAVEFRONT);  // directions side by side
+  // directions side by side (not the persistent recurrence: two grids that
+  // each need most of the SMs at once must not be launched together)
+  const bool side = !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !h->persist;
   // variable lengths: running sequences at time t are rows 0 .. Bt[t]-1 in
   // both directions; idle positions of y and of the h sequences read 0
   const bool vl = h->varlen != 0;
@@ -557,8 +559,39 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
         return train ? reinterpret_cast<float*>(R + h->rl[v].c) + (size_t)tt * BH
                      : reinterpret_cast<float*>(W + h->wl[v].c2) + (size_t)(tt & 1) * BH;
       };
+      if (h->persist) {
+        // all T steps of this direction in one launch
+        unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
+        if (h->persist_cl) RNN_TRY(cu(cudaMemsetAsync(W + h->ws_hx, 0, (size_t)8 * B * H, s)));
+        else RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
+        PersistArgs pa{};
+        pa.arrive = arrive;
+        pa.cluster = h->persist_cl;
+        pa.hx = reinterpret_cast<uint64_t*>(W + h->ws_hx);
+        pa.T = T;
+        pa.B = B;
+        pa.H = H;
+        pa.u_pack = h->u;
+        pa.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[v].wh);
+        pa.P = P;
+        pa.gates_out = train ? P : nullptr;
+        pa.bias_hn = reinterpret_cast<const float*>(PW + h->pl[v].bias_hn);
+        pa.c0 = (lstm && c0) ? c0 + v * BH : nullptr;
+        pa.c_out = (train && lstm) ? reinterpret_cast<float*>(R + h->rl[v].c) : nullptr;
+        pa.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[v].hn) : nullptr;
+        pa.hseq = reinterpret_cast<__nv_bfloat16*>(hseq);
+        pa.y = nullptr;
+        pa.hT = hT ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(hT) + (size_t)v * BH * e) : nullptr;
+        pa.cT = (cT && lstm) ? cT + (size_t)v * BH : nullptr;
+        pa.err = reinterpret_cast<int*>(W + h->ws_err);
+        pa.limit_ns = h->limit_ns;
+        pa.test_skip_publish = (d.flags & RNN_FLAG_TEST_SKIP_PUBLISH) ? 1 : 0;
+        pa.reverse = dd;
+        Launch Lk = mk(h, s, ws, "persist_fwd");
+        RNN_TRY(persist_fwd(Lk, d.cell, pa));
+      }
       // the recurrence: step k at time t, after the step at time tp
-      for (int k = 0; k < T; ++k) {
+      for (int k = 0; k < T && !h->persist; ++k) {
         const int t = dd == 0 ? k : T - 1 - k, tp = dd == 0 ? t - 1 : t + 1;
         const int Bs = Bt(t);
         if (Bs == 0) continue;

@@ -163,6 +163,8 @@ struct PersistArgs {
   int* err;
   uint64_t limit_ns;
   int test_skip_publish;    // test hook: CTA 0 never publishes h_0
+  int reverse;              // 1: time runs T-1 .. 0 (P, gates, c, y indexed by time; h(time) at hseq
+                            // slot time, the initial state at slot T)
 };
 // RNN_OK if the persistent recurrence supports (cell, H, B) and all its CTAs
 // fit on the device at once; *ctas receives the grid size and *cluster (if

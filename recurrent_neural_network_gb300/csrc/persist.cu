@@ -100,6 +100,10 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
   const int uc = ROWS / G;
   const int H = a.H, B = a.B, GH = G * H;
   const int jbase = blockIdx.x * uc;
+  // time order: step t runs time t (forward) or T-1-t (reverse); the h
+  // sequence keeps h(time) at slot time+1 forward, at slot time in reverse,
+  // and the initial state at slot 0 or T
+  const int slot_h0 = a.reverse ? a.T : 0;
   if (threadIdx.x == 0) abort_flag = 0;
 
   // ---- this CTA's rows of W_h as A fragments (row r = g*uc + local unit)
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
   for (int g = 0; g < G; ++g) pcol[g] = packed_row(g, j, G, a.u_pack);
   if (pair) {
     if (CELL == LSTM && a.c0) c_state = a.c0[(size_t)bq * H + j];
-    if (CELL == GRU) h_prev = __bfloat162float(a.hseq[(size_t)bq * H + j]);
+    if (CELL == GRU) h_prev = __bfloat162float(a.hseq[((size_t)slot_h0 * B + bq) * H + j]);
   }
   const float bhn = (CELL == GRU && pair) ? a.bias_hn[j] : 0.f;
   const int HP2 = H / 2 + 4;            // words per padded h row
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       const int bq = q0 / uc, jj = c * uc + (q0 - bq * uc);
       offw[i] = (uint32_t)(bq * HP2 * 4 + jj * 2);
     }
-    const uint32_t* h0w = reinterpret_cast<const uint32_t*>(a.hseq);
+    const uint32_t* h0w = reinterpret_cast<const uint32_t*>(a.hseq + (size_t)slot_h0 * B * H);
     uint32_t* hw = reinterpret_cast<uint32_t*>(hbuf);
     for (int i = threadIdx.x; i < NW; i += 256) {
       const int b = i / (H / 2);
@@ -175,10 +179,13 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
   const int nb = lane >> 2;  // batch column of this lane's B fragment
   const int kw = warp * KT * 16 + (lane & 3) * 2;
   for (int t = 0; t < a.T; ++t) {
+    const int tm = a.reverse ? a.T - 1 - t : t;            // time of this step
+    const int s_in = a.reverse ? a.T - t : t;              // slot of h before it
+    const int s_out = a.reverse ? a.T - 1 - t : t + 1;     // slot of h after it
     // input projection of this step for the pair (independent of the recurrence)
     float pv[G];
     if (pair) {
-      const float* prow = a.P + ((size_t)t * B + bq) * GH;
+      const float* prow = a.P + ((size_t)tm * B + bq) * GH;
 #pragma unroll
       for (int g = 0; g < G; ++g) pv[g] = prow[pcol[g]];
     }
@@ -251,7 +258,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
         bf[kt][1] = hs[kt * 8 + 4];
       }
     } else if (nb < B) {
-      const uint32_t* hs = reinterpret_cast<const uint32_t*>(a.hseq + ((size_t)t * B + nb) * H + kw);
+      const uint32_t* hs = reinterpret_cast<const uint32_t*>(a.hseq + ((size_t)s_in * B + nb) * H + kw);
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
         bf[kt][0] = __ldcg(hs + ((kt * 16) >> 1));
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
         hnew = (1.f - z) * n + z * h_prev;
         h_prev = hnew;
         gv[0] = r; gv[1] = z; gv[G - 1] = n;
-        if (a.hn_out) a.hn_out[((size_t)t * B + bq) * H + j] = hn;
+        if (a.hn_out) a.hn_out[((size_t)tm * B + bq) * H + j] = hn;
       } else {
         hnew = simple_act<CELL, __nv_bfloat16>(av[0] + pv[0]);
         gv[0] = hnew;
@@ -315,17 +322,17 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       const unsigned short hb = bf16_bits(hnew);
       hv = hb;
       if (a.gates_out) {
-        float* grow = a.gates_out + ((size_t)t * B + bq) * GH;
+        float* grow = a.gates_out + ((size_t)tm * B + bq) * GH;
 #pragma unroll
         for (int g = 0; g < G; ++g) grow[pcol[g]] = gv[g];
       }
-      if (CELL == LSTM && a.c_out) a.c_out[(size_t)t * B * H + bj] = c_state;
-      if (a.y) reinterpret_cast<unsigned short*>(a.y)[(size_t)t * B * H + bj] = hb;
+      if (CELL == LSTM && a.c_out) a.c_out[(size_t)tm * B * H + bj] = c_state;
+      if (a.y) reinterpret_cast<unsigned short*>(a.y)[(size_t)tm * B * H + bj] = hb;
       if (t == a.T - 1) {
         if (a.hT) reinterpret_cast<unsigned short*>(a.hT)[bj] = hb;
         if (CELL == LSTM && a.cT) a.cT[bj] = c_state;
       }
-      reinterpret_cast<unsigned short*>(a.hseq)[(size_t)(t + 1) * B * H + bj] = hb;
+      reinterpret_cast<unsigned short*>(a.hseq)[(size_t)s_out * B * H + bj] = hb;
     }
     // ---- publish
     if constexpr (XCL) {

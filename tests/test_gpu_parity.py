@@ -467,3 +467,29 @@ def test_bidirectional_variable_lengths(case):
     for b, n in enumerate(lens):
         assert not np.any(g["y"][n:, b]), b
         assert not np.any(g["dx"][n:, b]), b
+
+
+PERSIST_BIDIR = [
+    # cell, layers, T, B, I, H
+    (0, 2, 6, 4, 64, 256),
+    (0, 1, 40, 4, 64, 1024),
+    (1, 2, 5, 8, 64, 128),
+    (2, 1, 7, 3, 64, 512),
+    (3, 2, 6, 4, 64, 256),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("handoff", HANDOFF, ids=["cluster", "counter"])
+@pytest.mark.parametrize("case", PERSIST_BIDIR, ids=lambda c: "c%d_L%d_T%d_B%d_I%d_H%d" % c)
+def test_bidirectional_persistent_recurrence(case, handoff):
+    """Small-batch bidirectional stacks on the persistent recurrence (one launch
+    per direction, the reverse one walking time backwards), training against
+    the oracle with both hand-offs."""
+    cell, L, T, B, I, H = case
+    wl = synth.Workload("pbidir", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3,
+                        kink_margin=0.75 if cell == 3 else 0.0, directions=2)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    fl = rnn.FLAG_FORCE_PERSISTENT | handoff
+    assert "recurrence=persistent" in runner.Runner(wl, flags=fl).r.describe()
+    compare(wl, run_gpu(wl, hi, flags=fl, repeat=2), run_oracle(hi))

@@ -175,22 +175,26 @@ def test_set_lengths_validation_and_plan(lib):
 
 def test_bidirectional_plan_and_sizes(lib):
     """Bidirectional stacks: two weight sets per layer (the next layer's input
-    is 2H wide), states per (layer, direction), no wavefront, no persistent
-    recurrence; lengths are accepted."""
+    is 2H wide), states per (layer, direction), no wavefront; small bf16
+    batches take the persistent recurrence (one launch per direction) unless
+    lengths differ."""
     import oracle
     for cell, mode in ((0, 1), (1, 1), (2, 0), (3, 1)):
         L, T, B, I, H = 3, 10, 4, 64, 128
         r = rnn.RNN(cell, L, T, B, I, H, mode, flags=rnn.FLAG_BIDIRECTIONAL)
         d = r.describe()
-        assert "directions=2" in d and "wavefront=0" in d and "recurrence=streaming" in d
+        assert "directions=2" in d and "wavefront=0" in d
+        assert ("recurrence=persistent" if mode == 1 else "recurrence=streaming") in d
         e = 2 if mode == 1 else 4
         assert r.sizes()["user_weights"] == oracle.weight_count(cell, L, I, H, D=2) * e
         uni = rnn.RNN(cell, L, T, B, I, H, mode)
         assert "directions=1" in uni.describe()
         assert r.sizes()["reserve"] > uni.sizes()["reserve"]
     r = rnn.RNN(0, 1, 10, 4, 64, 1024, 1, flags=rnn.FLAG_BIDIRECTIONAL)
+    assert "recurrence=persistent" in r.describe()
     r.set_lengths([10, 7, 7, 2])
     assert "recurrence=streaming" in r.describe()
     r.set_lengths(None)
-    with pytest.raises(rnn.RnnError):
-        rnn.RNN(0, 1, 10, 4, 64, 1024, 1, flags=rnn.FLAG_BIDIRECTIONAL | rnn.FLAG_FORCE_PERSISTENT)
+    assert "recurrence=persistent" in r.describe()
+    rb = rnn.RNN(0, 1, 10, 64, 64, 1024, 1, flags=rnn.FLAG_BIDIRECTIONAL)
+    assert "recurrence=streaming" in rb.describe()
