@@ -339,7 +339,9 @@ def test_rejects_bad_arguments():
 
 # ---------------------------------------------------------------- stored fixtures
 
-@pytest.mark.parametrize("name", ["lstm_L2_T3_B2_I3_H4", "gru_L2_T3_B2_I3_H4", "tanh_L2_T3_B2_I3_H4"])
+@pytest.mark.parametrize("name", ["lstm_L2_T3_B2_I3_H4", "gru_L2_T3_B2_I3_H4", "tanh_L2_T3_B2_I3_H4",
+                                  "relu_L2_T3_B2_I3_H4", "lstm_bidir_L2_T3_B2_I3_H4",
+                                  "gru_bidir_len_L2_T4_B3_I3_H4"])
 def test_oracle_matches_stored_fixture(name):
     """Regression pin: the fixtures were written by tests/golden/make_golden.py from the oracle."""
     import json
@@ -350,7 +352,7 @@ def test_oracle_matches_stored_fixture(name):
     import make_golden
     rec = json.load(open(os.path.join(here, name + ".json")))
     sh = rec["shape"]
-    now = make_golden.compute(sh["cell"], sh["L"], sh["T"], sh["B"], sh["I"], sh["H"])
+    now = make_golden.compute(sh["cell"], sh["L"], sh["T"], sh["B"], sh["I"], sh["H"], sh.get("D", 1), sh.get("lens"))
     for k, v in rec["values"].items():
         np.testing.assert_allclose(now[k], v, rtol=1e-12, atol=1e-14, err_msg=k)
 
