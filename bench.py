@@ -161,13 +161,11 @@ NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.36e6,
                ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.64e6}
 
 
-def time_oracle_sample(wl, budget_s=20.0):
-    """The double-precision oracle on a bounded sample of the workload (batch
-    columns and a prefix of timesteps), as TFLOP/s of that sample."""
+def oracle_sample(wl, B1, T1):
+    """The double-precision oracle on batch columns 0..B1-1 and timesteps
+    0..T1-1 of the workload (all layers); returns (cpu_baseline dict, seconds)."""
     import oracle
     from recurrent_neural_network_gb300 import runner
-    B1 = min(wl.B, 2)
-    T1 = min(wl.T, 4 if wl.hidden >= 2048 else 16)
     sw = wl.replace(B=B1, T=T1)
     hi = runner.HostInputs(sw)
     t0 = time.perf_counter()
@@ -184,16 +182,37 @@ def time_oracle_sample(wl, budget_s=20.0):
                        f"({'fwd+BPTT+dW' if wl.training else 'fwd'}), {dt:.2f} s"), dt
 
 
+def oracle_sample_shape(wl, budget_s):
+    """(B1, T1) for an oracle run of about budget_s seconds: timed on a small
+    sample first, then grown along the timesteps and then the batch."""
+    B0 = min(wl.B, 2)
+    T0 = min(wl.T, 4 if wl.hidden >= 2048 else 16)
+    _, dt0 = oracle_sample(wl, B0, T0)
+    f = budget_s / max(dt0, 1e-3)
+    T1 = min(wl.T, max(T0, int(T0 * f)))
+    B1 = min(wl.B, max(B0, int(B0 * f * T0 / T1)))
+    return B1, T1
+
+
+def time_oracle_sample(wl, budget_s=12.0):
+    """cpu_baseline: the oracle as it stands on about budget_s seconds of the workload."""
+    B1, T1 = oracle_sample_shape(wl, budget_s)
+    return oracle_sample(wl, B1, T1)
+
+
 def run_reference(args, wl, rank):
-    """--impl reference: the oracle timed on host cores, per step one bounded sample."""
+    """--impl reference: the oracle timed on host cores, per step one bounded
+    sample sized so that warm-up and timed steps together take a few minutes."""
     if rank != 0:
         return
     import oracle
     oracle.build()
+    per_step = min(20.0, max(1.5, 150.0 / max(1, args.warmup + args.steps)))
+    B1, T1 = oracle_sample_shape(wl, per_step)
     times = []
     res = None
     for i in range(args.warmup + args.steps):
-        res, dt = time_oracle_sample(wl)
+        res, dt = oracle_sample(wl, B1, T1)
         if i >= args.warmup:
             times.append(dt)
     ms = 1e3 * statistics.mean(times)
