@@ -160,8 +160,12 @@ RNN_API int rnn_pack_weights(rnn_handle_t h, const void* w_user, void* w_packed,
  * gradients in the weight-gradient product).  At each step only the
  * sequences still running are computed.  A handle that had planned the
  * persistent recurrence switches to per-step launches; cached launch graphs
- * are dropped.  Returns RNN_ERR_INVALID_ARG for unsorted or out-of-range
- * lengths (nothing changes then). */
+ * are dropped (after a device-wide synchronize, so call it between steps,
+ * not while this handle's work is being captured).  Bidirectional stacks:
+ * the reverse direction of sequence b starts at step lens[b]-1 from its h0.
+ * Returns RNN_ERR_INVALID_ARG for unsorted or out-of-range lengths (nothing
+ * changes then).  A handle is not safe to use from several host threads at
+ * once. */
 RNN_API int rnn_set_lengths(rnn_handle_t h, const int* lens);
 
 /* Forward pass over all layers and timesteps.  Per layer l and step t:
