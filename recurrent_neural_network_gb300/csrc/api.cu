@@ -216,7 +216,7 @@ int plan_and_layout(rnn_s* h) {
     int ctas = 0;
     int cl = 4;  // without a device: the size that co-resides on GB300 for 128 CTAs
     const bool fits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &ctas, &cl) == RNN_OK
-                                     : (B <= 8 && H % 128 == 0 && H <= (d.cell == RNN_GRU ? 512 : d.cell == RNN_LSTM ? 1024 : 2048));
+                                     : (B <= 8 && H % 128 == 0 && H <= (d.cell == RNN_TANH || d.cell == RNN_RELU ? 2048 : 1024));
     if (fits) {
       h->persist = 1;
       h->persist_plan = 1;

@@ -446,7 +446,7 @@ int dispatch(const Launch& L, int cell, const PersistArgs& a, bool query_only, i
 #define RNN_P(C, MT_, KT_) \
   if (cell == C && KT == KT_) return launch_one<C, MT_, KT_>(L, b, ctas, query_only, num_sms, cl_out);
   RNN_P(LSTM, 2, 1) RNN_P(LSTM, 2, 2) RNN_P(LSTM, 2, 4) RNN_P(LSTM, 2, 8)
-  RNN_P(GRU, 3, 1) RNN_P(GRU, 3, 2) RNN_P(GRU, 3, 4)
+  RNN_P(GRU, 3, 1) RNN_P(GRU, 3, 2) RNN_P(GRU, 3, 4) RNN_P(GRU, 3, 8)
   RNN_P(TANH, 1, 1) RNN_P(TANH, 1, 2) RNN_P(TANH, 1, 4) RNN_P(TANH, 1, 8) RNN_P(TANH, 1, 16)
   RNN_P(RELU, 1, 1) RNN_P(RELU, 1, 2) RNN_P(RELU, 1, 4) RNN_P(RELU, 1, 8) RNN_P(RELU, 1, 16)
 #undef RNN_P

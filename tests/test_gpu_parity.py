@@ -155,6 +155,7 @@ PERSIST_CASES = [
     (0, 1, 5, 8, 128, 256),
     (1, 2, 6, 4, 64, 256),
     (1, 1, 5, 8, 64, 128),
+    (1, 1, 6, 4, 64, 1024),
     (2, 2, 6, 5, 64, 2048),
     (3, 2, 6, 4, 64, 512),
 ]
