@@ -4,8 +4,9 @@
 //
 // "Optimizing Performance of Recurrent Neural Networks on GPUs" (review page,
 // section "제안 방법"): grouped gate matrices make each step one larger
-// product; "Persistent RNNs" (citing snippet "pointwise OPs are very cheap")
-// motivates keeping the pointwise work inside the product's epilogue.
+// product; "Persistent RNNs: Stashing Recurrent Weights On-Chip" (citing
+// snippets on its page) counts the pointwise work as cheap next to the
+// products, which is why it runs inside the product's epilogue.
 #include <cstring>
 
 #include "epilogues.cuh"
