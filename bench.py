@@ -22,6 +22,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -51,7 +52,8 @@ class Clocks:
     def __init__(self, index):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # raw samples go to a scratch file; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"clocks_bench_{os.getpid()}.csv")
 
     def start(self):
         try:
