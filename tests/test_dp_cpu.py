@@ -26,10 +26,11 @@ def _free_port():
     return p
 
 
-def _inputs(cell):
+def _inputs(cell, directions=1):
     from recurrent_neural_network_gb300 import runner, synth
     wl = synth.Workload(name="dp", cell=cell, layers=2, T=4, B=6, input=5, hidden=4, mode=synth.MODE_FP32,
-                        forget_bias=1.0, state_std=0.3)
+                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0,
+                        directions=directions)
     return wl, runner.HostInputs(wl, with_state_grads=True)
 
 
@@ -37,14 +38,14 @@ def _bwd(hi):
     import oracle
     w = hi.wl
     return oracle.bwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, hi.dy, h0=hi.h0, c0=hi.c0,
-                      dhT=hi.dhT, dcT=hi.dcT)
+                      dhT=hi.dhT, dcT=hi.dcT, D=w.directions)
 
 
-def _rank(rank, world, port, cell, out):
+def _rank(rank, world, port, cell, directions, out):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     dist.init_process_group("gloo", rank=rank, world_size=world)
-    wl, hi = _inputs(cell)
+    wl, hi = _inputs(cell, directions)
     cols = list(range(rank * wl.B // world, (rank + 1) * wl.B // world))
     dx, dh0, dc0, dw = _bwd(hi.columns(cols))
     t = torch.from_numpy(np.ascontiguousarray(dw))
@@ -53,8 +54,9 @@ def _rank(rank, world, port, cell, out):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("cell", [0, 1, 2], ids=["lstm", "gru", "tanh"])
-def test_batch_shards_plus_allreduce_equal_full_batch(cell):
+@pytest.mark.parametrize("cell,directions", [(0, 1), (1, 1), (2, 1), (3, 1), (0, 2)],
+                         ids=["lstm", "gru", "tanh", "relu", "lstm_bidir"])
+def test_batch_shards_plus_allreduce_equal_full_batch(cell, directions):
     sys.path.insert(0, ROOT)
     import oracle
     oracle.build()
@@ -62,9 +64,9 @@ def test_batch_shards_plus_allreduce_equal_full_batch(cell):
     port = _free_port()
     with mp.Manager() as m:
         out = m.dict()
-        mp.spawn(_rank, args=(world, port, cell, out), nprocs=world, join=True)
+        mp.spawn(_rank, args=(world, port, cell, directions, out), nprocs=world, join=True)
         res = dict(out)
-    wl, hi = _inputs(cell)
+    wl, hi = _inputs(cell, directions)
     dx, dh0, dc0, dw = _bwd(hi)
     for r in range(world):
         cols, rdx, rdh0, rdc0, rdw = res[r]
