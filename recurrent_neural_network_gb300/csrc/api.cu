@@ -13,6 +13,12 @@
 //     top layer first in reverse time.
 //   * small-batch recurrences run all their timesteps in one persistent
 //     launch with the recurrent weights held on-chip (see persist.cu).
+//   * variable lengths (rnn_set_lengths): with the batch sorted longest
+//     first, the sequences running at time t are a prefix of the batch, so
+//     every step launch simply gets fewer rows.
+//   * bidirectional stacks (fwd_bidir, bwd_bidir, wgrad_bidir): every layer
+//     has a second direction that walks time backwards; the two directions
+//     of a layer run side by side, layers one after another.
 #include <algorithm>
 #include <atomic>
 #include <cstdio>

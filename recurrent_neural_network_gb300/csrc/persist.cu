@@ -8,7 +8,8 @@
 // Per timestep it reads h_{t-1} (all B x H values) from global memory, forms
 // its G*uc x B slice of h_{t-1} W_h^T on the tensor cores (split over K
 // across 8 warps, reduced through shared memory), applies the cell update to
-// its units and publishes its part of h_t.
+// its units and publishes its part of h_t.  Time may also run backwards
+// (the reverse direction of a bidirectional layer).
 //
 // Step hand-off, two variants.
 //
