@@ -52,3 +52,22 @@ def test_single_process_aggregate():
     import bench
     ms, tflops, w = bench.replica_aggregate(20.0, 4.0e12)
     assert (ms, w) == (20.0, 1) and tflops == pytest.approx(200.0)
+
+
+def test_reference_arm_prints_one_contract_line():
+    """bench.py --impl reference times the oracle on the host and prints the
+    benchmark's JSON line with impl, e2e and cpu_baseline (no GPU involved)."""
+    import json
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--config", "0",
+                          "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["steps"] == 1 and d["warmup"] == 1 and d["higher_is_better"] is True
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert "columns" in d["cpu_baseline"]["sample"]
