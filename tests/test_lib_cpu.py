@@ -208,3 +208,23 @@ def test_bidirectional_plan_and_sizes(lib):
     assert "recurrence=persistent" in r.describe()
     rb = rnn.RNN(0, 1, 10, 64, 64, 1024, 1, flags=rnn.FLAG_BIDIRECTIONAL)
     assert "recurrence=streaming" in rb.describe()
+
+
+@pytest.mark.parametrize("wl", [synth.WORKLOADS[1], synth.WORKLOADS[5], synth.WORKLOADS[6],
+                                synth.Workload("g", 1, 2, 3, 4, 8, 16, 0, state_std=0.3, directions=2)],
+                         ids=lambda w: w.name)
+def test_device_generator_matches_host_generator(wl):
+    """The inputs the benchmark draws on the device (here on the CPU) are the
+    host arrays the parity tests use: the same counters per tensor, per layer
+    and per direction (normals may differ in the last float32 ulp)."""
+    import numpy as np
+    import torch
+    small = wl.replace(T=min(wl.T, 3), B=min(wl.B, 4), hidden=min(wl.hidden, 64), input=min(wl.input, 64))
+    w_dev = synth.device_tensor(small, "w", "cpu", torch.float32).numpy().astype(np.float64)
+    w_host = synth.flat_weights(small).astype(np.float32).astype(np.float64)
+    assert w_dev.shape == w_host.shape == (small.weight_count(),)
+    np.testing.assert_array_equal(w_dev, w_host)
+    for what, host in (("x", synth.make_x(small)), ("dy", synth.make_dy(small)), ("h0", synth.make_state(small, "h0"))):
+        dev = synth.device_tensor(small, what, "cpu", torch.float32).numpy().astype(np.float64)
+        assert dev.shape == host.shape, what
+        np.testing.assert_allclose(dev, host.astype(np.float32), rtol=1e-6, atol=1e-6, err_msg=what)
