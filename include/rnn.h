@@ -90,7 +90,6 @@ enum {
 #define RNN_FLAG_FORCE_STREAMING 0x2u   /* never use the persistent recurrence */
 #define RNN_FLAG_FORCE_PERSISTENT 0x4u  /* use the persistent recurrence or fail */
 #define RNN_FLAG_PROFILE 0x8u           /* record per-kernel CUDA-event timings */
-#define RNN_FLAG_NO_MULTICAST 0x10u     /* forward steps load h_{t-1} per CTA (no cluster multicast) */
 #define RNN_FLAG_NO_PAIR 0x20u          /* keep every product on single-CTA 128-row tiles */
 #define RNN_FLAG_NO_GRAPH 0x40u         /* enqueue kernels directly; by default a call whose pointers were
                                            seen before replays a cached CUDA graph of its launches */
@@ -245,7 +244,8 @@ RNN_API int rnn_gemm_bf16(int M, int N, int K, const void* A, long long lda, int
  * start-up (it synchronizes the device and can fail under memory pressure),
  * so there is no room for the workspace rnn_bwd_weights takes.
  *
- * Computes db_x and db_h of every layer from the gate gradients that
+ * Computes db_x and db_h of every layer (and, in bidirectional stacks, of
+ * both directions of every layer) from the gate gradients that
  * rnn_bwd_data left in `reserve`, and writes them into `dw` (user layout,
  * float) at the same places rnn_bwd_weights does; dW_x and dW_h in `dw` are
  * not touched.  accumulate != 0 adds instead of overwriting.

@@ -135,7 +135,6 @@ struct rnn_s {
   int persist = 0, persist_ctas = 0;  // forward recurrence kind: 1 = persistent (one launch per layer)
   int persist_plan = 0;               // the kind the plan chose (variable lengths turn it off)
   int persist_cl = 0;                 // persistent hand-off: cluster size of the tagged-word exchange, 0 = counters
-  int fwd_mcast = 4;  // forward-step clusters along N sharing h_{t-1} by TMA multicast
   int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
   int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
   // variable lengths (rnn_set_lengths): Bt[t] = number of sequences still
@@ -231,7 +230,6 @@ int plan_and_layout(rnn_s* h) {
     }
   }
   if ((d.flags & RNN_FLAG_FORCE_PERSISTENT) && !h->persist) return RNN_ERR_UNSUPPORTED;
-  h->fwd_mcast = (d.flags & RNN_FLAG_NO_MULTICAST) ? 1 : 4;
   // wavefront chunking
   // (a bidirectional layer needs all of the layer below: no wavefront)
   h->wavefront = (L > 1) && !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !h->persist && h->D == 1;
@@ -639,7 +637,6 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
         a.hT = (fin && hT) ? static_cast<char*>(hT) + (size_t)v * BH * e : nullptr;
         a.cT = (fin && cT && lstm) ? cT + (size_t)v * BH : nullptr;
         a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[v].hn) + (size_t)t * BH : nullptr;
-        a.mcast = h->fwd_mcast;
         Operand A{a.h_prev, H, 0, Bs, H};
         Operand Bw{PW + h->pl[v].wh, H, 0, GH, H, 1};
         Launch Lk = mk(h, s, ws, "fwd_step");
@@ -1052,11 +1049,11 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : h->d.cell == RNN_RELU ? "relu" : "tanh";
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
-           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d fwd_mcast=%d sms=%d transposed=%d fused_point=%d "
+           "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d transposed=%d fused_point=%d "
            "persist_cluster=%d directions=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
            h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch,
-           h->bwd_bn, h->bwd_splits, h->fwd_mcast, h->num_sms, h->tstep, h->bwd_fuse, h->persist ? h->persist_cl : 0, h->D);
+           h->bwd_bn, h->bwd_splits, h->num_sms, h->tstep, h->bwd_fuse, h->persist ? h->persist_cl : 0, h->D);
   return RNN_OK;
 }
 
@@ -1197,8 +1194,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
             a.hT = (!h->varlen && t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
             a.cT = (!h->varlen && t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
             a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
-            a.mcast = h->fwd_mcast;
-            Operand A{hseq + (size_t)t * BH * e, H, 0, Bs, H};
+                Operand A{hseq + (size_t)t * BH * e, H, 0, Bs, H};
             Operand Bw{PW + h->pl[l].wh, H, 0, GH, H, 1};
             Launch Lk = mk(h, s, ws, "fwd_step");
             if (h->tstep) RNN_TRY(fwd_step_t(Lk, d.cell, Bw, A, a));
@@ -1553,11 +1549,12 @@ extern "C" int rnn_bias_grad_static(rnn_handle_t h, const void* reserve, float* 
   int slices = (int)std::min<long long>(64, (TB + 255) / 256);
   slices = std::max(1, std::min(slices, RNN_BIAS_STATIC_FLOATS / GH));
   const char* R = static_cast<const char*>(reserve);
-  for (int l = 0; l < d.layers; ++l) {
+  // one bias block pair per (layer, direction) v = l * D + d, as rnn_bwd_weights writes them
+  for (int v = 0; v < h->V(); ++v) {
     Launch Lb = mk(h, stream, nullptr, "bias_grad_static");
     Lb.prof = nullptr;
-    RNN_TRY(bias_grad(Lb, d.mode, d.cell, d.hidden, h->u, TB, R + h->rl[l].dgx, R + h->rl[l].dgh,
-                      dw + h->ul[l].bx, dw + h->ul[l].bh, accumulate, part, slices));
+    RNN_TRY(bias_grad(Lb, d.mode, d.cell, d.hidden, h->u, TB, R + h->rl[v].dgx, R + h->rl[v].dgh,
+                      dw + h->ul[v].bx, dw + h->ul[v].bh, accumulate, part, slices));
   }
   return RNN_OK;
 }

@@ -9,7 +9,8 @@
 //    the next tile's MMAs proceed.  Operands may be K-major or MN-major (the
 //    transposed products of the backward pass need the latter).  Tiles are
 //    128 x BN, K step 64; the grid is persistent over tiles and split-K ranges.
-//  * simt_gemm_kernel: fp32 FFMA (no TF32) for the fp32 storage mode.
+//  * simt_gemm_kernel: fp32 FFMA (no TF32) for the fp32 storage mode, with
+//    compensated (error-free transformation) accumulation.
 //
 // Epilogue functors implement
 //   template <class Acc> __device__ void operator()(const TileCoord&, int row, const Acc&) const
@@ -36,8 +37,7 @@ struct GemmGeom {
   uint64_t limit_ns;           // bound on every pipeline wait
   int* err;                    // device error word
   int cluster;                 // > 1: the split-K CTAs of a tile form one thread-block cluster
-  int mcast;                   // > 1: clusters of `mcast` CTAs along N share (multicast) their A tile
-  int nfast;                   // tile order: n-tiles fastest (needed by multicast clusters)
+  int nfast;                   // tile order: n-tiles fastest
   int pdl;                     // launched as a programmatic dependent: wait before touching produced data
   int static_op;               // operand no earlier kernel writes (0 none, 1 A, 2 B): its first STAGES
                                // blocks of the first tile are loaded before that wait
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, g.mcast);  // every CTA of a multicast cluster frees the stage
+      tc::mbar_init(empty + s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tfull + a, 1);
@@ -198,26 +198,20 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (g.cluster > 1 || g.mcast > 1) tc::cluster_sync_all();  // peers' barriers exist before any remote traffic
+  if (g.cluster > 1) tc::cluster_sync_all();  // peers' barriers exist before any remote traffic
   const uint32_t tmem_base = *tmem_slot;
   tc::pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const int crank = g.mcast > 1 ? (int)tc::cluster_ctarank() : 0;
-      const uint16_t mc_mask = (uint16_t)((1u << g.mcast) - 1u);
       uint32_t stage = 0, phase = 0;
       int last_par[STAGES];  // parity of the last load issued into each stage (-1: none)
       for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
       bool ok = true;
       auto load_a = [&](uint8_t* sa, uint64_t* bar, int m0, int kb) {
         const int k0 = kb * BK;
-        if (g.mcast > 1) {
-          // this CTA's 1/mcast of the A rows, into every peer's stage
-          const int rows = BM / g.mcast;
-          tc::tma_load_2d_mc(sa + crank * rows * 128, &mapA, bar, k0, m0 + crank * rows, mc_mask);
-        } else if (g.a_mn) {
+        if (g.a_mn) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j) tc::tma_load_2d(sa + j * 8192, &mapA, bar, m0 + 64 * j, k0);
         } else {
@@ -238,7 +232,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       // on finish
       int pre = 0;
       if (g.pdl) {
-        if (g.static_op && g.mcast == 1 && (int)blockIdx.x < g.num_tiles) {
+        if (g.static_op && (int)blockIdx.x < g.num_tiles) {
           int mt, nt, split;
           decode_tile(g, blockIdx.x, mt, nt, split);
           const int kb0 = split * g.kb_per_split;
@@ -331,8 +325,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
                                        : tc::sdesc_sw128(sb + kk * 32, 16, 1024);
             tc::mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           }
-          if (g.mcast > 1) tc::mma_commit_mc(empty + stage, (uint16_t)((1u << g.mcast) - 1u));
-          else tc::mma_commit(empty + stage);
+          tc::mma_commit(empty + stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -424,7 +417,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem_base, TMEM_COLS);
   }
-  if (g.cluster > 1 || g.mcast > 1) tc::cluster_sync_all();  // no peer touches this CTA's shared memory after it exits
+  if (g.cluster > 1) tc::cluster_sync_all();  // no peer touches this CTA's shared memory after it exits
 }
 
 // ---------------------------------------------------------------------------
@@ -700,7 +693,37 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
 
 // ---------------------------------------------------------------------------
 // fp32 SIMT engine (FFMA): 32 x BN tiles, 128 threads, K step 16.
+//
+// Every dot product is accumulated with compensation: the "Dot2" scheme of
+// Ogita, Rump and Oishi ("Accurate sum and dot product", SIAM J. Sci. Comput.
+// 26(6), 2005).  Each product a*b is split exactly into p + pe with one FMA
+// (pe = fma(a, b, -p)), p is added to the running sum by Knuth's TwoSum, which
+// also yields the exact rounding error of that addition, and both errors are
+// collected in a second float.  The result is as accurate as a sum taken in
+// twice the working precision and rounded once, whatever K is; a plain
+// sequential fp32 sum instead carries an error that grows with K and, where
+// an output is a small difference of O(1) terms, exceeds the fp32 mode's
+// 1e-4 relative bound.  All operations are fp32 (no TF32, no fp64); the
+// explicit _rn intrinsics keep the compiler from contracting or reordering
+// them.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void dot2_add(float a, float b, float& hi, float& lo) {
+  const float p = __fmul_rn(a, b);
+  const float pe = __fmaf_rn(a, b, -p);  // a*b - p, exactly
+  const float s = __fadd_rn(hi, p);
+  const float bv = __fsub_rn(s, hi);
+  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bv)), __fsub_rn(p, bv));  // hi + p - s, exactly
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(e, pe));
+}
+// Compensated sum of floats (the same TwoSum step without the product).
+__device__ __forceinline__ void sum2_add(float v, float& hi, float& lo) {
+  const float s = __fadd_rn(hi, v);
+  const float bv = __fsub_rn(s, hi);
+  lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bv)), __fsub_rn(v, bv)));
+  hi = s;
+}
+
 namespace se {
 constexpr int BM = 32;
 constexpr int BK = 16;
@@ -724,11 +747,11 @@ __global__ void __launch_bounds__(128)
   int mt, nt, split;
   decode_tile(g, blockIdx.x, mt, nt, split);
   const int m0 = mt * BM, n0 = nt * BN;
-  float acc[8][NC];
+  float acc[8][NC], err[8][NC];  // compensated sums: value and collected rounding errors
 #pragma unroll
   for (int r = 0; r < 8; ++r)
 #pragma unroll
-    for (int c = 0; c < NC; ++c) acc[r][c] = 0.f;
+    for (int c = 0; c < NC; ++c) acc[r][c] = err[r][c] = 0.f;
 
   for (int k0 = 0; k0 < g.K; k0 += BK) {
     for (int e = tid; e < BM * BK; e += 128) {
@@ -756,14 +779,14 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
       for (int r = 0; r < 8; ++r)
 #pragma unroll
-        for (int c = 0; c < NC; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
+        for (int c = 0; c < NC; ++c) dot2_add(a[r], b[c], acc[r][c], err[r][c]);
     }
     __syncthreads();
   }
 #pragma unroll
   for (int r = 0; r < 8; ++r)
 #pragma unroll
-    for (int c = 0; c < NC; ++c) Cs[(ty * 8 + r) * (BN + 1) + tx + 32 * c] = acc[r][c];
+    for (int c = 0; c < NC; ++c) Cs[(ty * 8 + r) * (BN + 1) + tx + 32 * c] = __fadd_rn(acc[r][c], err[r][c]);
   __syncthreads();
   if (tid < BM) {
     TileCoord t;

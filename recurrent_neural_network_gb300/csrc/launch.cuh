@@ -101,18 +101,13 @@ inline unsigned launch_attrs(cudaLaunchAttribute* at, int cluster, int pdl) {
 // cluster_splitk: with more than one K split, the splits of each output tile
 // run as one thread-block cluster and reduce through distributed shared
 // memory (the epilogue must support it); one tile per CTA.
-// mcast > 1: CTAs that share an m-tile run as clusters of `mcast` along N and
-// multicast their A tile (each loads BM/mcast rows); used when the shape
-// allows it (K-major A, no split, n-tiles a multiple of mcast), else ignored.
 template <int BN, int STAGES, class Epi>
 int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, int splits, int max_ctas,
-              const Epi& epi, bool cluster_splitk = false, int mcast = 1) {
+              const Epi& epi, bool cluster_splitk = false) {
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
   if (B.mn_major && BN % 64) return RNN_ERR_UNSUPPORTED;
-  const int n_tiles = (N + BN - 1) / BN;
-  if (!(mcast == 2 || mcast == 4 || mcast == 8) || A.mn_major || splits > 1 || n_tiles % mcast) mcast = 1;
   CUtensorMap ma, mb;
-  int rc = encode_operand(&ma, A, tce::BM / mcast);
+  int rc = encode_operand(&ma, A, tce::BM);
   if (rc) return rc;
   rc = encode_operand(&mb, B, BN);
   if (rc) return rc;
@@ -136,11 +131,10 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   // multiple of 16*splits and at most 8 CTAs per cluster.  Otherwise the
   // partials go through global memory.
   g.cluster = (cluster_splitk && g.splits > 1 && g.splits <= 8 && BN % (16 * g.splits) == 0) ? g.splits : 1;
-  g.mcast = g.cluster > 1 ? 1 : mcast;
   // tile order: run along the dimension with fewer tiles first, so that the
   // CTAs in flight at any time share operand slabs of the other dimension
   // (for the deep-K products this keeps the slabs they stream in L2)
-  g.nfast = (g.mcast > 1 || g.n_tiles < g.m_tiles) ? 1 : 0;
+  g.nfast = g.n_tiles < g.m_tiles ? 1 : 0;
   constexpr int smem = tce::smem_bytes<BN, STAGES>();
   auto kern = tc_gemm_kernel<BN, STAGES, Epi>;
   static bool attr = false;
@@ -150,9 +144,7 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
     attr = true;
   }
   int cap = max_ctas > 0 ? max_ctas : L.num_sms;
-  int grid = std::min(g.num_tiles, cap);
-  if (g.mcast > 1) grid = std::max(g.mcast, grid / g.mcast * g.mcast);
-  const int cl = g.cluster > 1 ? g.cluster : g.mcast;
+  const int grid = std::min(g.num_tiles, cap);
   g.pdl = L.pdl;
   g.static_op = A.is_static ? 1 : B.is_static ? 2 : 0;
   cudaLaunchConfig_t cfg = {};
@@ -162,7 +154,7 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   cfg.stream = L.stream;
   cudaLaunchAttribute at[2];
   cfg.attrs = at;
-  cfg.numAttrs = launch_attrs(at, cl, L.pdl);
+  cfg.numAttrs = launch_attrs(at, g.cluster, L.pdl);
   launch_begin(L);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, g, epi);
   launch_end(L);
@@ -200,7 +192,6 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   g.limit_ns = L.limit_ns;
   g.err = L.err;
   g.cluster = g.splits;
-  g.mcast = 1;
   g.nfast = g.n_tiles < g.m_tiles ? 1 : 0;  // as in launch_tc
   constexpr int smem = tce2::smem_bytes<BN, STAGES>();
   auto kern = tc_gemm2_kernel<BN, STAGES, Epi>;
@@ -243,7 +234,6 @@ int launch_simt(const Launch& L, const Operand& A, const Operand& B, int M, int 
   g.kb_per_split = g.kb_total;
   g.num_tiles = g.m_tiles * g.n_tiles;
   g.cluster = 1;
-  g.mcast = 1;
   g.nfast = 0;
   g.pdl = 0;
   g.static_op = 0;

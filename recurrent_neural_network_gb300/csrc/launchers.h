@@ -79,7 +79,6 @@ struct FwdStepArgs {
   void* hT;
   float* cT;
   float* hn_out;
-  int mcast;  // cluster size along N for the multicast of h_{t-1} (1 = off)
 };
 // one forward timestep of one layer: A = h_{t-1} [B][H], B = packed W_h [G*H][H]
 int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, const FwdStepArgs& a);

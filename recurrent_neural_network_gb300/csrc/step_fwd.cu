@@ -42,8 +42,6 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
   if (mode == 1) {
     using S = __nv_bfloat16;
     // the tile width is one packed block of G*u gate rows
-    // the batch rows h_{t-1} are shared by every n-tile: multicast them within clusters along N
-    const int mc = a.mcast;
     // more than 128 batch rows: 256-row tiles on CTA pairs
     if (M > 128 && L.pair) {
       if (cell == LSTM && a.u == 64) return launch_tc2<256, 6>(L, A, Bw, M, N, K, 0, make_epi<LSTM, S>(a));
@@ -55,7 +53,7 @@ int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operan
       if (cell == RELU && a.u == 128) return launch_tc2<128, 8>(L, A, Bw, M, N, K, 0, make_epi<RELU, S>(a));
     }
 #define RNN_STEP(C, U, BN_, ST)     \
-  if (cell == C && a.u == U) return launch_tc<BN_, ST>(L, A, Bw, M, N, K, 1, 0, make_epi<C, S>(a), false, mc);
+  if (cell == C && a.u == U) return launch_tc<BN_, ST>(L, A, Bw, M, N, K, 1, 0, make_epi<C, S>(a));
     RNN_STEP(LSTM, 64, 256, 4) RNN_STEP(LSTM, 32, 128, 6) RNN_STEP(LSTM, 16, 64, 8)
     RNN_STEP(GRU, 64, 192, 5) RNN_STEP(GRU, 32, 96, 7) RNN_STEP(GRU, 16, 48, 8)
     RNN_STEP(TANH, 128, 128, 6) RNN_STEP(TANH, 64, 64, 8) RNN_STEP(TANH, 32, 32, 8)

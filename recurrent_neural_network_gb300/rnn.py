@@ -22,7 +22,6 @@ FLAG_NO_WAVEFRONT = 0x1
 FLAG_FORCE_STREAMING = 0x2
 FLAG_FORCE_PERSISTENT = 0x4
 FLAG_PROFILE = 0x8
-FLAG_NO_MULTICAST = 0x10
 FLAG_NO_PAIR = 0x20
 FLAG_NO_GRAPH = 0x40
 FLAG_NO_PDL = 0x80

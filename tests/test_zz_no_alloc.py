@@ -38,27 +38,44 @@ def test_rejects_shapes_beyond_the_fixed_scratch(lib):
     assert lib.rnn_bias_grad_static(r.h, None, fake, 0, None) == -1
 
 
+# (cell, mode, hidden, directions, flags): unidirectional stacks in both
+# storage modes, bidirectional stacks (one bias block pair per layer and
+# direction), and the transposed-step packing (packing unit 1, hidden >= 256)
+CASES = [
+    (0, synth.MODE_BF16, 128, 1, 0),
+    (1, synth.MODE_BF16, 128, 1, 0),
+    (2, synth.MODE_FP32, 64, 1, 0),
+    (0, synth.MODE_BF16, 128, 2, 0),
+    (1, synth.MODE_BF16, 128, 2, 0),
+    (0, synth.MODE_BF16, 256, 1, rnn.FLAG_FORCE_TRANSPOSED),
+]
+IDS = ["lstm-bf16", "gru-bf16", "tanh-fp32", "lstm-bf16-bidir", "gru-bf16-bidir", "lstm-bf16-transposed-H256"]
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("cell,mode", [(0, synth.MODE_BF16), (1, synth.MODE_BF16), (2, synth.MODE_FP32)],
-                         ids=["lstm-bf16", "gru-bf16", "tanh-fp32"])
-def test_matches_bwd_weights_on_two_calls(lib, cell, mode):
-    H = 128 if mode == synth.MODE_BF16 else 64
-    wl = synth.Workload("noalloc", cell, 2, 9, 37, 72, H, mode, forget_bias=1.0, state_std=0.3)
+@pytest.mark.parametrize("cell,mode,H,D,flags", CASES, ids=IDS)
+def test_matches_bwd_weights_on_two_calls(lib, cell, mode, H, D, flags):
+    wl = synth.Workload("noalloc", cell, 2, 9, 37, 72, H, mode, forget_bias=1.0, state_std=0.3, directions=D)
     hi = runner.HostInputs(wl, with_state_grads=True)
-    R = runner.Runner(wl)
+    R = runner.Runner(wl, flags=flags)
+    if flags & rnn.FLAG_FORCE_TRANSPOSED:
+        assert "transposed=1" in R.r.describe() and " u=1 " in R.r.describe()
     R.upload(hi)
     R.forward(True)
     R.backward()
     R.weights()
     assert R.status() == 0
     ref = R.dw.double().cpu().numpy()
+    blocks_ref = weight_blocks(wl, ref)
+    assert len(blocks_ref) == 4 * wl.layers * D
     for call in range(2):
         out = torch.full_like(R.dw, float("nan"))
         R.r.bias_grad_static(R.reserve, out)
         torch.cuda.synchronize()
         got = out.double().cpu().numpy()
-        for (nm, g), (_, o) in zip(weight_blocks(wl, got), weight_blocks(wl, ref)):
+        for (nm, g), (_, o) in zip(weight_blocks(wl, got), blocks_ref):
             if nm.endswith(("dbx", "dbh")):
+                assert np.isfinite(g).all(), (call, nm)
                 if mode == synth.MODE_FP32:
                     assert max_rel(g, o) <= FP32_MAX_REL, (call, nm)
                 else:
@@ -70,6 +87,6 @@ def test_matches_bwd_weights_on_two_calls(lib, cell, mode):
     R.r.bias_grad_static(R.reserve, out, accumulate=True)
     torch.cuda.synchronize()
     got = out.double().cpu().numpy()
-    for (nm, g), (_, o) in zip(weight_blocks(wl, got), weight_blocks(wl, ref)):
+    for (nm, g), (_, o) in zip(weight_blocks(wl, got), blocks_ref):
         if nm.endswith(("dbx", "dbh")):
             assert rel_l2(g, 2 * o) <= BF16_REL_L2, nm
