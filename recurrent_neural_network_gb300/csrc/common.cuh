@@ -98,9 +98,21 @@ __device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* p, const f
 }
 
 // ---------------------------------------------------------------- activations
-// Logistic sigmoid and tanh through CUDA's own expf / tanhf (fp32 storage mode).
-__device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + expf(-a)); }
-__device__ __forceinline__ float tanh_(float a) { return tanhf(a); }
+// Precision of the pointwise cell arithmetic per storage type.  fp32 storage
+// mode: every value the path stores is fp32 and the products run on FFMA, but
+// the pointwise work between them (activations, cell update, the gate
+// derivatives of the backward step) is evaluated in double from the stored
+// fp32 inputs and rounded to fp32 once where it is stored, so each stored
+// value carries a single fp32 rounding (CUDA's fp32 expf / tanhf and chains
+// of fp32 operations carry several).  bf16 storage mode: fp32.
+template <class S>
+struct Prec {
+  using T = double;
+};
+template <>
+struct Prec<__nv_bfloat16> {
+  using T = float;
+};
 // bf16 storage mode: the hardware tanh approximation (tanh.approx.f32, one
 // special-function op, relative error about 2^-11) and the identity
 // sigmoid(a) = (1 + tanh(a/2)) / 2.  The cell outputs are stored in bf16
@@ -111,11 +123,12 @@ __device__ __forceinline__ float tanh_hw(float a) {
   return y;
 }
 __device__ __forceinline__ float sigm_hw(float a) { return fmaf(0.5f, tanh_hw(0.5f * a), 0.5f); }
-// activation pair for storage type S
+// activation pair for storage type S, in Prec<S>::T (fp32 storage: CUDA's
+// double exp / tanh)
 template <class S>
 struct Act {
-  __device__ __forceinline__ static float sig(float a) { return sigm(a); }
-  __device__ __forceinline__ static float th(float a) { return tanh_(a); }
+  __device__ __forceinline__ static double sig(double a) { return 1.0 / (1.0 + exp(-a)); }
+  __device__ __forceinline__ static double th(double a) { return tanh(a); }
 };
 template <>
 struct Act<__nv_bfloat16> {
@@ -126,15 +139,15 @@ struct Act<__nv_bfloat16> {
 // Simple-RNN cells (one gate block): activation h = act(a) and its slope
 // written in terms of h (tanh: 1 - h^2; ReLU: 1 where h > 0, taken as 0 at
 // the kink).
-template <int CELL, class S>
-__device__ __forceinline__ float simple_act(float a) {
-  if constexpr (CELL == RELU) return fmaxf(a, 0.f);
+template <int CELL, class S, class T>
+__device__ __forceinline__ T simple_act(T a) {
+  if constexpr (CELL == RELU) return a > T(0) ? a : T(0);
   else return Act<S>::th(a);
 }
-template <int CELL>
-__device__ __forceinline__ float simple_slope(float h) {
-  if constexpr (CELL == RELU) return h > 0.f ? 1.f : 0.f;
-  else return 1.f - h * h;
+template <int CELL, class T>
+__device__ __forceinline__ T simple_slope(T h) {
+  if constexpr (CELL == RELU) return h > T(0) ? T(1) : T(0);
+  else return T(1) - h * h;
 }
 
 // ---------------------------------------------------------------- time and errors

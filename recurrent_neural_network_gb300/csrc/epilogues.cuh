@@ -112,6 +112,7 @@ struct EpiFwdStep {
   template <class Acc>
   __device__ __forceinline__ void operator()(const TileCoord& t, int row, const Acc& acc, int /*bn*/) const {
     constexpr int G = CellInfo<CELL>::G;
+    using T = typename Prec<S>::T;  // pointwise precision
     const int b = t.m0 + row;
     const int GH = G * H;
     const int jblk = (t.n0 / (G * u)) * u;
@@ -130,19 +131,21 @@ struct EpiFwdStep {
 #pragma unroll
           for (int i = 0; i < 16; ++i) cp[i] = 0.f;
         float p[16], cn[16];
+        T av[4][16];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           load16(prow + g * u, p);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) a[g][i] += p[i];
+          for (int i = 0; i < 16; ++i) av[g][i] = T(a[g][i]) + T(p[i]);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float ig = Act<S>::sig(a[0][i]), fg = Act<S>::sig(a[1][i]), gg = Act<S>::th(a[2][i]), og = Act<S>::sig(a[3][i]);
-          const float cc = fg * cp[i] + ig * gg;
-          cn[i] = cc;
-          hnew[i] = og * Act<S>::th(cc);
-          a[0][i] = ig; a[1][i] = fg; a[2][i] = gg; a[3][i] = og;
+          const T ig = Act<S>::sig(av[0][i]), fg = Act<S>::sig(av[1][i]), gg = Act<S>::th(av[2][i]),
+                  og = Act<S>::sig(av[3][i]);
+          const T cc = fg * T(cp[i]) + ig * gg;
+          cn[i] = float(cc);
+          hnew[i] = float(og * Act<S>::th(cc));
+          a[0][i] = float(ig); a[1][i] = float(fg); a[2][i] = float(gg); a[3][i] = float(og);
         }
         store16(c_out + (size_t)b * H + j0, cn);
         if (cT) store16(cT + (size_t)b * H + j0, cn);
@@ -162,11 +165,12 @@ struct EpiFwdStep {
         load16(prow + 2 * u, p);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float r = Act<S>::sig(a[0][i]), z = Act<S>::sig(a[1][i]);
-          hn[i] = a[2][i] + bn[i];
-          const float n = Act<S>::th(p[i] + r * hn[i]);
-          hnew[i] = (1.f - z) * n + z * hp[i];
-          a[0][i] = r; a[1][i] = z; a[2][i] = n;
+          const T r = Act<S>::sig(T(a[0][i])), z = Act<S>::sig(T(a[1][i]));
+          const T hnv = T(a[2][i]) + T(bn[i]);
+          hn[i] = float(hnv);
+          const T n = Act<S>::th(T(p[i]) + r * hnv);
+          hnew[i] = float((T(1) - z) * n + z * T(hp[i]));
+          a[0][i] = float(r); a[1][i] = float(z); a[2][i] = float(n);
         }
         if (hn_out) store16(hn_out + (size_t)b * H + j0, hn);
       } else {
@@ -174,7 +178,7 @@ struct EpiFwdStep {
         load16(prow, p);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          hnew[i] = simple_act<CELL, S>(a[0][i] + p[i]);
+          hnew[i] = float(simple_act<CELL, S>(T(a[0][i]) + T(p[i])));
           a[0][i] = hnew[i];
         }
       }
@@ -207,16 +211,20 @@ struct BwdPoint {
   S* dGx;               // [B][G*H]
   S* dGh;               // [B][G*H] (GRU; LSTM/RNN write only dGx)
 
-  __device__ __forceinline__ void run(int b, int j0, float* dh) const {
+  __device__ __forceinline__ void run(int b, int j0, float* dh32) const {
     constexpr int G = CellInfo<CELL>::G;
+    using T = typename Prec<S>::T;  // pointwise precision
     const int GH = G * H;
     const size_t bj = (size_t)b * H + j0;
+    T dh[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) dh[i] = T(dh32[i]);
     float t16[16];
     if (dy) {
       if (dy_f32) load16(reinterpret_cast<const float*>(dy) + bj, t16);
       else load16(reinterpret_cast<const S*>(dy) + bj, t16);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) dh[i] += t16[i];
+      for (int i = 0; i < 16; ++i) dh[i] += T(t16[i]);
     }
     const int p0 = (j0 / u) * (G * u) + (j0 % u);  // packed column of gate 0
     const float* grow = gates + (size_t)b * GH + p0;
@@ -236,14 +244,15 @@ struct BwdPoint {
       float d0[16], d1[16], d2[16], d3[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float tau = Act<S>::th(cs[i]);
-        const float dov = dh[i] * tau;
-        const float dcv = dc[i] + dh[i] * og[i] * (1.f - tau * tau);
-        d0[i] = dcv * gg[i] * ig[i] * (1.f - ig[i]);
-        d1[i] = dcv * cp[i] * fg[i] * (1.f - fg[i]);
-        d2[i] = dcv * ig[i] * (1.f - gg[i] * gg[i]);
-        d3[i] = dov * og[i] * (1.f - og[i]);
-        dc[i] = dcv * fg[i];
+        const T igv = ig[i], fgv = fg[i], ggv = gg[i], ogv = og[i];
+        const T tau = Act<S>::th(T(cs[i]));
+        const T dov = dh[i] * tau;
+        const T dcv = T(dc[i]) + dh[i] * ogv * (T(1) - tau * tau);
+        d0[i] = float(dcv * ggv * igv * (T(1) - igv));
+        d1[i] = float(dcv * T(cp[i]) * fgv * (T(1) - fgv));
+        d2[i] = float(dcv * igv * (T(1) - ggv * ggv));
+        d3[i] = float(dov * ogv * (T(1) - ogv));
+        dc[i] = float(dcv * fgv);
       }
       store16(gx, d0);
       store16(gx + u, d1);
@@ -264,15 +273,17 @@ struct BwdPoint {
       float dar[16], daz[16], dan[16], dhn[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float d = dh[i] + cz[i];
-        const float dn = d * (1.f - z[i]);
-        const float dz = d * (hp[i] - n[i]);
-        dan[i] = dn * (1.f - n[i] * n[i]);
-        const float dr = dan[i] * hn[i];
-        dhn[i] = dan[i] * r[i];
-        dar[i] = dr * r[i] * (1.f - r[i]);
-        daz[i] = dz * z[i] * (1.f - z[i]);
-        cz[i] = d * z[i];
+        const T rv = r[i], zv = z[i], nv = n[i];
+        const T d = dh[i] + T(cz[i]);
+        const T dn = d * (T(1) - zv);
+        const T dz = d * (T(hp[i]) - nv);
+        const T danv = dn * (T(1) - nv * nv);
+        const T dr = danv * T(hn[i]);
+        dan[i] = float(danv);
+        dhn[i] = float(danv * rv);
+        dar[i] = float(dr * rv * (T(1) - rv));
+        daz[i] = float(dz * zv * (T(1) - zv));
+        cz[i] = float(d * zv);
       }
       S* gh = dGh + (size_t)b * GH + p0;
       store16(gx, dar);
@@ -286,7 +297,7 @@ struct BwdPoint {
       float hv[16], da[16];
       load16(grow, hv);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) da[i] = dh[i] * simple_slope<CELL>(hv[i]);
+      for (int i = 0; i < 16; ++i) da[i] = float(dh[i] * simple_slope<CELL>(T(hv[i])));
       store16(gx, da);
     }
   }

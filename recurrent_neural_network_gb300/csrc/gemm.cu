@@ -124,7 +124,9 @@ int cast_bf16(const Launch& L, const float* src, void* dst, size_t n) {
 // owns 256 packed columns (32 lanes x 8 columns, 16-byte loads) and one slice
 // of rows, its 8 warps stride the slice and reduce through shared memory into
 // a per-slice partial.  Pass 2 sums the slices in a fixed order, so the result
-// is deterministic.
+// is deterministic.  In the fp32 storage mode both passes sum with
+// compensation (TwoSum, as in the fp32 GEMM engine), so that the bias
+// gradients carry about one rounding error whatever the number of rows.
 template <class S>
 __global__ void bias_part_kernel(const S* __restrict__ dg, float* __restrict__ part, long long rows, int GH,
                                  long long rows_per_slice) {
@@ -133,9 +135,10 @@ __global__ void bias_part_kernel(const S* __restrict__ dg, float* __restrict__ p
   const int c0 = blockIdx.x * 256 + lane * 8;
   const long long r0 = (long long)blockIdx.y * rows_per_slice;
   const long long r1 = min(rows, r0 + rows_per_slice);
-  float acc[8];
+  constexpr bool comp = sizeof(S) == 4;
+  float acc[8], err[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 8; ++i) acc[i] = err[i] = 0.f;
   if (c0 < GH) {
     for (long long r = r0 + warp; r < r1; r += 8) {
       const S* p = dg + r * GH + c0;
@@ -149,19 +152,30 @@ __global__ void bias_part_kernel(const S* __restrict__ dg, float* __restrict__ p
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += to_f32(p[i]);
+        for (int i = 0; i < 8; ++i) sum2_add(to_f32(p[i]), acc[i], err[i]);
       }
     }
   }
+  __shared__ float rerr[comp ? 8 : 1][comp ? 256 : 1];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = acc[i];
+  for (int i = 0; i < 8; ++i) {
+    red[warp][lane * 8 + i] = acc[i];
+    if constexpr (comp) rerr[warp][lane * 8 + i] = err[i];
+  }
   __syncthreads();
   const int c = threadIdx.x;  // 256 threads: one column each
-  float t = 0.f;
+  float t = 0.f, te = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) t += red[w][c];
+  for (int w = 0; w < 8; ++w) {
+    if constexpr (comp) {
+      sum2_add(red[w][c], t, te);
+      te = __fadd_rn(te, rerr[w][c]);
+    } else {
+      t += red[w][c];
+    }
+  }
   const int col = blockIdx.x * 256 + c;
-  if (col < GH) part[(size_t)blockIdx.y * GH + col] = t;
+  if (col < GH) part[(size_t)blockIdx.y * GH + col] = comp ? __fadd_rn(t, te) : t;
 }
 
 __global__ void bias_final_kernel(const float* __restrict__ part, int slices, int G, int H, int u,
@@ -169,8 +183,9 @@ __global__ void bias_final_kernel(const float* __restrict__ part, int slices, in
   const int p = blockIdx.x * blockDim.x + threadIdx.x;
   const int GH = G * H;
   if (p >= GH) return;
-  float t = 0.f;
-  for (int s = 0; s < slices; ++s) t += part[(size_t)s * GH + p];
+  float t = 0.f, te = 0.f;  // compensated: costs nothing next to the loads
+  for (int s = 0; s < slices; ++s) sum2_add(part[(size_t)s * GH + p], t, te);
+  t = __fadd_rn(t, te);
   const int blk = p / (G * u), r = p % (G * u);
   const int ur = (r / u) * H + blk * u + (r % u);
   db[ur] = accumulate ? db[ur] + t : t;

@@ -4,11 +4,10 @@ tolerances.
 
 Tolerances (fixed by the benchmark definition of this path):
   fp32 storage mode: max relative error <= 1e-4 on every output, with the
-    relative error of element i taken as |g_i - o_i| / max(|o_i|, 1e-2 max_j |o_j|).
-    The floor is needed where outputs pass through zero: an element that is the
-    small difference of O(max) terms carries an absolute fp32 rounding error of
-    ~1e-7 max however it is summed (a float32 numpy emulation of the same cells
-    reaches 5e-5 with a 1e-3 floor and 9e-6 with this one);
+    relative error of element i taken as |g_i - o_i| / max(|o_i|, 1e-3 max_j |o_j|)
+    per output tensor (the benchmark definition states no floor; one is needed
+    where outputs pass through zero, and 1e-3 of the tensor's largest magnitude
+    is the reading taken);
   bf16 storage mode: max absolute error <= 3e-2 on y, hT and cT, and relative
     L2 error ||g - o|| / ||o|| <= 2e-2 on dx, dh0, dc0 and each weight /
     bias gradient block.
@@ -19,6 +18,7 @@ import oracle
 from recurrent_neural_network_gb300 import runner, synth
 
 FP32_MAX_REL = 1e-4
+FP32_FLOOR = 1e-3
 BF16_MAX_ABS = 3e-2
 BF16_REL_L2 = 2e-2
 
@@ -56,7 +56,7 @@ def run_gpu(wl, hi, flags=0, chunk=0, train=None, timeout_ns=0, repeat=1, lens=N
 def max_rel(g, o):
     g = np.asarray(g, np.float64).ravel()
     o = np.asarray(o, np.float64).ravel()
-    floor = 1e-2 * max(np.abs(o).max(), 1e-30)
+    floor = FP32_FLOOR * max(np.abs(o).max(), 1e-30)
     return float((np.abs(g - o) / np.maximum(np.abs(o), floor)).max())
 
 
