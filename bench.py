@@ -11,8 +11,15 @@ H=4096 B=256 T=50 bf16 LSTM training step.
 
 Prints one JSON line (rank 0).  Metric: algorithmic GEMM TFLOP/s of the step
 (2*M*N*K over the input, recurrent, data-gradient and weight-gradient
-products), with timesteps/s beside it.  With N > 1 (torchrun) every rank runs
-an independent replica of the workload (no collective on the data path).
+products), with timesteps/s beside it.  With N > 1 (torchrun, one rank per
+GPU) the step is data-parallel: the global batch holds N shards of the
+workload's batch, every rank runs its shard and the weight gradients are
+summed over the ranks with one NCCL all-reduce per step inside the timed
+region (weak scaling: per-GPU work is fixed).  Inference workloads have no
+exchange step and run one shard per rank.
+
+Besides the headline workload the line carries measured sub-results of the
+other benchmark workloads ("workloads"), each with its roofline fraction.
 """
 from __future__ import annotations
 
@@ -227,76 +234,144 @@ def run_reference(args, wl, rank):
     print(json.dumps(line), flush=True)
 
 
-def e2e_run(R, wl, steps, sdt, stream, barrier):
-    """The same step through the public API with the inputs in pinned host
-    memory: host->device copies of x (and dy) and a device->host read of hT
-    inside the timed region."""
-    hx = torch.empty(R.x.shape, dtype=sdt, pin_memory=True)
-    hx.copy_(R.x)
-    hdy = None
-    if wl.training:
-        hdy = torch.empty(R.dy.shape, dtype=sdt, pin_memory=True)
-        hdy.copy_(R.dy)
-    hout = torch.empty(R.hT.shape, dtype=R.hT.dtype, pin_memory=True)
-    h2d = hx.numel() * hx.element_size() + (hdy.numel() * hdy.element_size() if hdy is not None else 0)
-    d2h = hout.numel() * hout.element_size()
+def e2e_run(R, wl, steps, stream, barrier, reduce_fn=None):
+    """The same step through the public API with host buffers: every step
+    copies its inputs (x, dy) from pinned host memory to the device and its
+    results (the weight gradients dw and the data gradient dx of a training
+    step, y of an inference step) back to pinned host memory, all inside the
+    timed region.  The copies of step i+1's inputs and of step i's results run
+    on a copy stream while step i+1 computes (inputs and results are double
+    buffered on the device), ordered by events."""
+    train = wl.training
+    ins = ["x"] + (["dy"] if train else [])
+    outs = ["dw", "dx"] if train else ["y"]
+    dev_in = {k: [getattr(R, k), torch.empty_like(getattr(R, k))] for k in ins}
+    for k in ins:
+        dev_in[k][1].copy_(dev_in[k][0])
+    dev_out = {k: [getattr(R, k), torch.empty_like(getattr(R, k))] for k in outs}
+    host_in = {k: [torch.empty(dev_in[k][0].shape, dtype=dev_in[k][0].dtype, pin_memory=True) for _ in range(2)]
+               for k in ins}
+    for k in ins:
+        for j in range(2):
+            host_in[k][j].copy_(dev_in[k][0])
+    host_out = {k: [torch.empty(dev_out[k][0].shape, dtype=dev_out[k][0].dtype, pin_memory=True) for _ in range(2)]
+                for k in outs}
+    h2d = sum(v[0].numel() * v[0].element_size() for v in dev_in.values())
+    d2h = sum(v[0].numel() * v[0].element_size() for v in dev_out.values())
+    cs = torch.cuda.Stream(device=stream.device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of buffer j landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # step on buffer j finished (inputs free, results ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # results of buffer j copied out
+
+    def bind(j):
+        for k in ins:
+            setattr(R, k, dev_in[k][j])
+        for k in outs:
+            setattr(R, k, dev_out[k][j])
+
+    def upload(j):
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev_done[j])  # the previous step on buffer j has read its inputs
+            for k in ins:
+                dev_in[k][j].copy_(host_in[k][j], non_blocking=True)
+            ev_in[j].record(cs)
+
+    def download(j):
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev_done[j])
+            for k in outs:
+                host_out[k][j].copy_(dev_out[k][j], non_blocking=True)
+            ev_out[j].record(cs)
+
+    def run(n):
+        for j in range(2):
+            ev_done[j].record(stream)
+            ev_out[j].record(stream)
+        upload(0)
+        for i in range(n):
+            j = i & 1
+            if i + 1 < n:
+                upload(1 - j)
+            stream.wait_event(ev_in[j])
+            stream.wait_event(ev_out[j])  # results of the step before last on buffer j are out
+            bind(j)
+            R.step()
+            if reduce_fn is not None:
+                reduce_fn(R)
+            ev_done[j].record(stream)
+            download(j)
+        for j in range(2):
+            stream.wait_event(ev_out[j])
+
+    run(6)  # warm-up: both buffer sets through the graph cache
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        R.x.copy_(hx, non_blocking=True)
-        if hdy is not None:
-            R.dy.copy_(hdy, non_blocking=True)
-        R.step()
-        hout.copy_(R.hT, non_blocking=True)
+    run(steps)
     e1.record(stream)
     barrier()
+    bind(0)
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
+def weight_bytes_per_launch(wl):
+    """Algorithmic bytes of one recurrent-step launch: the W_h it must read
+    (G*H*H in the storage type).  The state it reads and writes (gates, c,
+    h, carry, P) is reported beside it, not counted in the roofline."""
+    return wl.G * wl.hidden * wl.hidden * (2 if wl.mode == 1 else 4)
+
+
+def class_roofline(name, n, tot, wl, steps, pk, transposed, fused_point):
+    """Roofline of one kernel class from its serialised CUDA-event timings:
+    algorithmic flops (2*M*N*K) per launch against the burst bf16 tensor peak
+    (each launch is timed on its own), and for the recurrent steps the W_h
+    bytes per launch against the measured copy bandwidth; the slower bound
+    binds."""
+    cf = class_flops(wl)
+    sec = tot * 1e-3 / n
+    flops = cf.get(name, 0.0) * steps / n
+    nbytes = weight_bytes_per_launch(wl) if name in ("fwd_step", "bwd_step") else 0.0
+    t_tensor = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    out = {"kernel": name, "launches_per_step": n // steps, "flops_per_launch": flops,
+           "bytes_per_launch": nbytes, "ms_per_launch": 1e3 * sec,
+           "tensor_frac": flops / sec / 1e12 / pk["bf16_tflops"]}
+    if name in ("fwd_step", "bwd_step"):
+        cb = class_bytes(wl, transposed, fused_point)
+        out["state_bytes_per_launch"] = cb[name] * steps / n - nbytes if name in cb else None
+    if nbytes and t_hbm > t_tensor:
+        ach = nbytes / sec / 1e9
+        out.update(bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s", frac=ach / pk["hbm_gbs"],
+                   peak_source=pk["source"] + " copy bandwidth")
+    else:
+        ach = flops / sec / 1e12
+        out.update(bound="tensor", achieved=ach, peak=pk["bf16_tflops"], unit="TFLOP/s", frac=ach / pk["bf16_tflops"],
+                   peak_source=pk["source"] + " bf16 burst (kernel timed alone)")
+    return out
+
+
 def roofline(prof, wl, steps, pk, transposed, fused_point=False):
-    """Roofline of the dominant kernel class (largest device time): its
-    algorithmic flops and bytes per launch over its average CUDA-event launch
-    duration, against the tensor or the HBM peak, whichever its arithmetic
-    intensity makes binding."""
-    cf, cb = class_flops(wl), class_bytes(wl, transposed, fused_point)
+    """The dominant kernel class (largest device time) and its roofline; the
+    DRAM traffic per launch from the committed ncu capture of the same build."""
+    cf = class_flops(wl)
     cand = [(k, v) for k, v in prof.items() if k in cf and v[0] > 0]
     if not cand:
         return None
     name, (n, tot) = max(cand, key=lambda kv: kv[1][1])
-    sec = tot * 1e-3 / n
-    flops = cf[name] * steps / n
-    t_tensor = flops / (pk["bf16_tflops_sustained"] * 1e12)
-    nbytes = cb[name] * steps / n if name in cb else 0.0
-    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9) if nbytes else 0.0
-    common = {"kernel": name, "launches_per_step": n // steps, "flops_per_launch": flops, "bytes_per_launch": nbytes,
-              "ms_per_launch": 1e3 * sec, "measured_in": "serialised profiling pass (see kernels_note)",
-              "traffic": NCU_TRAFFIC.get((wl.name, name))}
-    if t_hbm > t_tensor:
-        ach = nbytes / sec / 1e9
-        return dict(common, bound="hbm", achieved=ach, peak=pk["hbm_gbs"], unit="GB/s", frac=ach / pk["hbm_gbs"],
-                    tensor_frac=flops / sec / 1e12 / pk["bf16_tflops_sustained"],
-                    peak_source=pk["source"] + " (copy bandwidth)")
-    ach = flops / sec / 1e12
-    return dict(common, bound="tensor", achieved=ach, peak=pk["bf16_tflops_sustained"], unit="TFLOP/s",
-                frac=ach / pk["bf16_tflops_sustained"],
-                peak_source=pk["source"] + " (sustained bf16, kernel timed inside the step)")
+    r = class_roofline(name, n, tot, wl, steps, pk, transposed, fused_point)
+    r["measured_in"] = "serialised profiling pass (see kernels_note)"
+    r["traffic"] = NCU_TRAFFIC.get((wl.name, name))
+    return r
 
 
-def kernel_profile(wl, dev, args, sdt):
+def kernel_profile(wl, dev, args):
     """Per-kernel CUDA-event timings of the same workload in a separate pass:
     launches serialised on the caller's stream (no wavefront overlap, no graph)
     and queued behind a GPU sleep so that the host is ahead of the device and
     consecutive event pairs bracket back-to-back kernels."""
-    from recurrent_neural_network_gb300 import rnn, runner
+    from recurrent_neural_network_gb300 import rnn
     flags = rnn.FLAG_PROFILE | rnn.FLAG_NO_WAVEFRONT | rnn.FLAG_NO_GRAPH
-    R = runner.Runner(wl, device=dev, flags=flags)
-    R.x = synth_tensor(wl, "x", dev, sdt)
-    R.w_user = synth_tensor(wl, "w", dev, sdt)
-    R.h0 = synth_tensor(wl, "h0", dev, sdt)
-    R.c0 = synth_tensor(wl, "c0", dev, torch.float32) if wl.cell == 0 else None
-    R.dy = synth_tensor(wl, "dy", dev, sdt) if wl.training else None
-    R.pack()
+    R = make_runner(wl, dev, flags=flags)
     R.step()
     torch.cuda.synchronize()
     R.r.profile(reset=True)
@@ -310,43 +385,92 @@ def kernel_profile(wl, dev, args, sdt):
     return prof, steps
 
 
-def persistent_probe(dev, steps=10, warmup=3):
-    """Second target of the path: the persistent small-batch recurrence
-    (1-layer LSTM, B=4, H=1024, T=1000 inference).  Per step it reads the
-    8 MiB W_h from on-chip storage; its roofline is that read at the
-    aggregate shared-memory bandwidth of the GPU, derived from the unit
-    counts (152 SMs x 128 B/clk x max SM clock)."""
-    from recurrent_neural_network_gb300 import rnn, runner, synth
-    wl = synth.WORKLOADS[2]
-    R = runner.Runner(wl, device=dev, flags=rnn.FLAG_FORCE_PERSISTENT)
-    R.x = synth_tensor(wl, "x", dev, R.dt)
-    R.w_user = synth_tensor(wl, "w", dev, R.dt)
-    R.h0 = synth_tensor(wl, "h0", dev, R.dt)
-    R.c0 = synth_tensor(wl, "c0", dev, torch.float32)
+def smem_peak_gbs(mhz):
+    """Aggregate shared-memory read bandwidth derived from the unit counts:
+    152 SMs x 128 B/clk x SM clock."""
+    return 152 * 128 * mhz * 1e6 / 1e9
+
+
+def fp32_peak_tflops(mhz):
+    """FFMA peak derived from the unit counts: 152 SMs x 128 fp32 lanes x 2 flop x SM clock."""
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def workload_roofline(wl, ms, pk, persistent):
+    """Roofline of a whole step: the slower of (a) its GEMM flops at the
+    tensor peak (sustained: the step is a long run of kernels; the FFMA peak
+    for the fp32 mode) and (b) the recurrent weights it must read, once per
+    recurrent step of every layer and direction (forward, and again in the
+    backward pass of a training step), from HBM when streamed or from shared
+    memory when the persistent recurrence keeps them on chip."""
+    mhz = pk.get("sm_max_mhz", 2070.0)
+    fl = step_flops(wl)
+    if wl.mode == 1:
+        tpk, tsrc = pk["bf16_tflops_sustained"], pk["source"] + " bf16 sustained"
+    else:
+        tpk, tsrc = fp32_peak_tflops(mhz), "derived FFMA: 152 SMs x 128 lanes x 2 x %.0f MHz" % mhz
+    passes = wl.T * wl.layers * wl.directions * (2 if wl.training else 1)
+    wbytes = passes * weight_bytes_per_launch(wl)
+    bw, bsrc = ((smem_peak_gbs(mhz), "derived: 152 SMs x 128 B/clk x %.0f MHz" % mhz) if persistent
+                else (pk["hbm_gbs"], pk["source"] + " copy bandwidth"))
+    t_t = fl / (tpk * 1e12)
+    t_w = wbytes / (bw * 1e9)
+    sec = ms * 1e-3
+    if t_w > t_t:
+        return {"bound": "smem" if persistent else "hbm", "achieved": wbytes / sec / 1e9, "peak": bw, "unit": "GB/s",
+                "frac": t_w / sec, "weight_bytes_per_step": wbytes, "peak_source": bsrc,
+                "tensor_frac": fl / sec / 1e12 / tpk}
+    return {"bound": "tensor" if wl.mode == 1 else "alu", "achieved": fl / sec / 1e12, "peak": tpk,
+            "unit": "TFLOP/s", "frac": t_t / sec, "weight_bytes_per_step": wbytes, "peak_source": tsrc,
+            "weight_frac": t_w / sec}
+
+
+def make_runner(wl, dev, flags=0, chunk=0, rank=0, world=1):
+    """A Runner of wl on dev with its synthetic inputs drawn on the device;
+    with world > 1, this rank's shard of a global batch of world * wl.B
+    sequences (same weights on every rank)."""
+    from recurrent_neural_network_gb300 import dp, runner, synth
+    R = runner.Runner(wl, device=dev, flags=flags, chunk=chunk)
+    gw = dp.global_batch(wl, world)
+
+    def t(what, dtype):
+        v = synth.device_tensor(gw, what, dev, dtype)
+        return v if (world == 1 or what == "w") else dp.shard(v, rank, world, dim=1)
+    R.x = t("x", R.dt)
+    R.w_user = t("w", R.dt)
+    R.h0 = t("h0", R.dt)
+    R.c0 = t("c0", torch.float32) if wl.cell == synth.CELL_LSTM else None
+    R.dy = t("dy", R.dt) if wl.training else None
     R.pack()
+    return R
+
+
+def workload_probe(idx, dev, pk, steps=10, warmup=3):
+    """One of the other benchmark workloads, timed with CUDA events over
+    `steps` whole steps after `warmup` (same step as the headline: forward,
+    BPTT, weight gradients, or the forward of an inference workload)."""
+    from recurrent_neural_network_gb300 import synth
+    wl = synth.WORKLOADS[idx]
+    R = make_runner(wl, dev)
     for _ in range(warmup):
-        R.forward(False)
+        R.step()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(steps):
-        R.forward(False)
+        R.step()
     e1.record()
     torch.cuda.synchronize()
     assert R.status() == 0
     ms = e0.elapsed_time(e1) / steps
-    pk = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
-        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
-    mhz = pk.get("sm_max_mhz", 2070.0)
-    smem_gbs = 152 * 128 * mhz * 1e6 / 1e9
-    wh_bytes = 4 * wl.hidden * wl.hidden * 2
-    us_step = 1e3 * ms / wl.T
-    roof_us = wh_bytes / (smem_gbs * 1e9) * 1e6
-    return {"workload": wl.name, "ms_per_call": ms, "us_per_timestep": us_step, "timesteps_per_s": wl.T / (ms * 1e-3),
-            "tflops": step_flops(wl) / (ms * 1e-3) / 1e12, "plan": R.r.describe(),
-            "roofline": {"bound": "smem", "bytes_per_timestep": wh_bytes, "peak": smem_gbs, "unit": "GB/s",
-                         "peak_source": "derived: 152 SMs x 128 B/clk x %.0f MHz" % mhz,
-                         "roofline_us_per_timestep": roof_us, "achieved": wh_bytes / (us_step * 1e-6) / 1e9,
-                         "frac": roof_us / us_step}}
+    plan = R.r.describe()
+    persistent = "recurrence=persistent" in plan
+    out = {"ms_per_step": ms, "tflops": step_flops(wl) / (ms * 1e-3) / 1e12,
+           "timesteps_per_s": wl.T / (ms * 1e-3), "us_per_timestep": 1e3 * ms / wl.T,
+           "training": wl.training, "dtype": "bf16" if wl.mode == 1 else "f32", "plan": plan,
+           "roofline": workload_roofline(wl, ms, pk, persistent)}
+    del R
+    torch.cuda.empty_cache()
+    return wl.name, out
 
 
 def sweep(dev, steps=5, warmup=2):
@@ -430,7 +554,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-persistent", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the sub-results of the other workloads")
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--sweep", action="store_true",
@@ -463,22 +587,19 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    from recurrent_neural_network_gb300 import build, rnn, runner
+    from recurrent_neural_network_gb300 import build, dp, rnn
     build.build()
     dev = torch.device("cuda", local)
-    R = runner.Runner(wl, device=dev, flags=args.flags, chunk=args.chunk)
-    sdt = R.dt
-    R.x = synth.device_tensor(wl, "x", dev, sdt)
-    R.w_user = synth.device_tensor(wl, "w", dev, sdt)
-    R.h0 = synth.device_tensor(wl, "h0", dev, sdt)
-    R.c0 = synth.device_tensor(wl, "c0", dev, torch.float32) if wl.cell == synth.CELL_LSTM else None
-    R.dy = synth.device_tensor(wl, "dy", dev, sdt) if wl.training else None
-    R.pack()
+    R = make_runner(wl, dev, flags=args.flags, chunk=args.chunk, rank=rank, world=world)
     torch.cuda.synchronize()
+    # data-parallel exchange: dW summed over the ranks once per training step
+    reduce_fn = (lambda r: dp.allreduce_grads_(r.dw)) if (world > 1 and wl.training) else None
 
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         R.step()
+        if reduce_fn is not None:
+            reduce_fn(R)
     assert R.status() == 0
 
     def barrier():
@@ -491,9 +612,9 @@ def main():
     clocks.start()
     time.sleep(0.25)
     n_launch0 = rnn.launch_count()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     for i in range(args.steps):
-        # phase boundaries on the caller's stream: forward | BPTT | weight gradients
+        # phase boundaries on the caller's stream: forward | BPTT | weight gradients | dW all-reduce
         ev[i][0].record(stream)
         R.forward()
         ev[i][1].record(stream)
@@ -503,11 +624,14 @@ def main():
         if wl.training:
             R.weights()
         ev[i][3].record(stream)
+        if reduce_fn is not None:
+            reduce_fn(R)
+        ev[i][4].record(stream)
     barrier()
     launches = rnn.launch_count() - n_launch0
-    ms = ev[0][0].elapsed_time(ev[-1][3]) / args.steps
+    ms = ev[0][0].elapsed_time(ev[-1][4]) / args.steps
     phases = {nm: statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev)
-              for k, nm in enumerate(["fwd", "bwd_data", "bwd_weights"])}
+              for k, nm in enumerate(["fwd", "bwd_data", "bwd_weights", "dw_allreduce"])}
     clk = clocks.stop()
     st = R.status()
     assert st == 0, f"device status {st}"
@@ -517,13 +641,19 @@ def main():
     if args.no_e2e:
         ms_e2e, h2d, d2h = float("nan"), 0, 0
     else:
-        ms_e2e, h2d, d2h = e2e_run(R, wl, args.steps, sdt, stream, barrier)
+        ms_e2e, h2d, d2h = e2e_run(R, wl, args.steps, stream, barrier, reduce_fn)
+        ms_e2e, _, _ = replica_aggregate(ms_e2e, fl, dist, dev)
     plan = R.r.describe()
     del R
     torch.cuda.empty_cache()
-    prof, psteps = kernel_profile(wl, dev, args, sdt)
+    prof, psteps = kernel_profile(wl, dev, args)
     roof = roofline(prof, wl, psteps, pk, "transposed=1" in plan, "fused_point=1" in plan)
-    persistent = persistent_probe(dev) if (world == 1 and args.config != 2 and not args.no_persistent) else None
+    subs = {}
+    if world == 1 and not args.no_workloads:
+        for idx in range(5):
+            if idx != args.config:
+                name, res = workload_probe(idx, dev, pk)
+                subs[name] = res
 
     if rank != 0:
         if dist is not None:
@@ -537,21 +667,28 @@ def main():
         "tensor_peak_frac": {"of_measured_burst": tflops / world / pk["bf16_tflops"],
                              "of_measured_sustained": tflops / world / pk["bf16_tflops_sustained"]},
         "config": {"workload": wl.name, "cell": synth.CELL_NAMES[wl.cell], "layers": wl.layers, "T": wl.T,
-                   "B": wl.B, "input": wl.input, "hidden": wl.hidden, "training": wl.training,
-                   "flops_per_step": fl, "plan": plan,
+                   "B": wl.B, "global_batch": wl.B * world, "input": wl.input, "hidden": wl.hidden,
+                   "training": wl.training, "flops_per_step": fl, "plan": plan,
+                   "parallelism": f"dp{world}" if world > 1 else "single",
+                   "dp_exchange": "NCCL all-reduce (sum) of dW every step" if reduce_fn is not None else None,
                    "l2": "inputs larger than L2 (weights, reserve and activations exceed 129 MB)"},
         "gpu_launches": launches,
         "roofline": roof,
+        "step_roofline": workload_roofline(wl, ms, pk, "recurrence=persistent" in plan),
         "clocks": clk,
         "e2e": {"value": world * fl / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "copies": ("x, dy in; dw, dx out" if wl.training else "x in; y out") +
+                          ", pinned host buffers, overlapped with the neighbouring steps on a copy stream"},
         "phases_ms": phases,
-        "persistent_recurrence": persistent,
-        "kernels": {k: {"launches": v[0] // psteps, "ms_per_step": v[1] / psteps, "us_per_launch": 1e3 * v[1] / v[0]}
-                    for k, v in prof.items() if v[0]},
+        "workloads": subs,
+        "kernels": {k: class_roofline(k, v[0], v[1], wl, psteps, pk, "transposed=1" in plan, "fused_point=1" in plan)
+                    for k, v in prof.items() if v[0] and k in class_flops(wl)},
         "kernels_note": "per-kernel CUDA-event times from a separate pass of the same workload with launches "
                         "serialised (no wavefront, no graph); the timed run overlaps layers and replays graphs",
     }
+    # the persistent small-batch recurrence (second target of the path) under its own key as well
+    line["persistent_recurrence"] = subs.get(synth.WORKLOADS[2].name)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"], _ = time_oracle_sample(wl)
     print(json.dumps(line), flush=True)

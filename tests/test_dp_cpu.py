@@ -1,10 +1,12 @@
-"""Data-parallel training over batch shards, simulated with world-size-2
-gloo ranks on CPU: each rank runs the double-precision oracle on its half
-of the batch, the weight gradients are summed with one all-reduce, and the
-result must equal the full-batch weight gradient (sequences are independent,
-so dW is a sum over batch entries), while each rank's dx, dh0, dc0 are the
-full-batch values of its own columns.  This is the one exchange step a
-data-parallel training step adds to the path; no GPU is involved."""
+"""Data-parallel training over batch shards with world-size-2 gloo ranks on
+CPU, through the same helpers the benchmark's data-parallel step uses
+(recurrent_neural_network_gb300.dp): each rank takes its shard of the global
+batch with dp.shard, runs the double-precision oracle on it, and sums its
+weight gradients with dp.allreduce_grads_.  The result must equal the
+full-batch weight gradient (sequences are independent, so dW is a sum over
+batch entries), while each rank's dx, dh0, dc0 are the full-batch values of
+its own columns.  This is the one exchange step a data-parallel training step
+adds to the path; no GPU is involved."""
 import os
 import socket
 import sys
@@ -43,14 +45,23 @@ def _bwd(hi):
 
 def _rank(rank, world, port, cell, directions, out):
     sys.path.insert(0, ROOT)
+    from recurrent_neural_network_gb300 import dp
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     wl, hi = _inputs(cell, directions)
-    cols = list(range(rank * wl.B // world, (rank + 1) * wl.B // world))
-    dx, dh0, dc0, dw = _bwd(hi.columns(cols))
+    # this rank's shard of every batch-indexed input, as torch tensors (the benchmark's form)
+    sh = object.__new__(type(hi))
+    sh.wl = wl.replace(B=wl.B // world)
+    sh.w = hi.w
+    for k in ("x", "h0", "c0", "dy", "dhT", "dcT"):
+        a = getattr(hi, k)
+        t = None if a is None else dp.shard(torch.from_numpy(a), rank, world, dim=1)
+        setattr(sh, k, None if t is None else t.numpy())
+    dx, dh0, dc0, dw = _bwd(sh)
     t = torch.from_numpy(np.ascontiguousarray(dw))
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    out[rank] = (cols, dx, dh0, dc0, t.numpy().copy())
+    assert dp.allreduce_grads_(t) is t
+    k = wl.B // world
+    out[rank] = (list(range(rank * k, (rank + 1) * k)), dx, dh0, dc0, t.numpy().copy())
     dist.destroy_process_group()
 
 
@@ -75,3 +86,22 @@ def test_batch_shards_plus_allreduce_equal_full_batch(cell, directions):
         np.testing.assert_allclose(rdh0, dh0[:, cols], rtol=1e-12, atol=1e-15)
         if dc0 is not None:
             np.testing.assert_allclose(rdc0, dc0[:, cols], rtol=1e-12, atol=1e-15)
+
+
+def test_shard_and_global_batch_helpers():
+    sys.path.insert(0, ROOT)
+    from recurrent_neural_network_gb300 import dp, synth
+    wl = synth.WORKLOADS[3]
+    g = dp.global_batch(wl, 4)
+    assert g.B == 4 * wl.B and g.T == wl.T and g.hidden == wl.hidden
+    assert dp.global_batch(wl, 1) == wl
+    a = np.arange(2 * 8 * 3).reshape(2, 8, 3)
+    parts = [dp.shard(a, r, 4) for r in range(4)]
+    np.testing.assert_array_equal(np.concatenate(parts, axis=1), a)
+    t = torch.from_numpy(a)
+    assert torch.equal(dp.shard(t, 1, 4), t[:, 2:4])
+    assert dp.shard(None, 0, 2) is None
+    with pytest.raises(ValueError):
+        dp.shard(a, 0, 3)
+    x = torch.ones(3)
+    assert dp.allreduce_grads_(x) is x and torch.equal(x, torch.ones(3))  # no process group: no-op
