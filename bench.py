@@ -473,6 +473,45 @@ def workload_probe(idx, dev, pk, steps=10, warmup=3):
     return wl.name, out
 
 
+def fp8_stash_probe(dev, pk, steps=5, warmup=2):
+    """The fp8 stash of W_h (RNN_FLAG_FP8_STASH): a 1-layer LSTM, H=2048, B=4,
+    T=1000 inference, whose bf16 W_h (32 MiB) is too large for the
+    register-resident recurrence, timed with the persistent recurrence on the
+    e4m3 stash (16 MiB in shared memory across the CTAs) and with streaming
+    bf16 steps.  Roofline of the stash: its bytes read from shared memory once
+    per timestep at the aggregate shared-memory bandwidth."""
+    from recurrent_neural_network_gb300 import rnn, synth
+    wl = synth.Workload("lstm_bf16_L1_T1000_B4_H2048_infer", synth.CELL_LSTM, 1, 1000, 4, 2048, 2048,
+                        synth.MODE_BF16, forget_bias=1.0, training=False)
+    out = {"workload": wl.name}
+    for name, fl in (("fp8_stash_persistent", rnn.FLAG_FP8_STASH), ("bf16_streaming", 0)):
+        R = make_runner(wl, dev, flags=fl)
+        for _ in range(warmup):
+            R.forward(False)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            R.forward(False)
+        e1.record()
+        torch.cuda.synchronize()
+        assert R.status() == 0
+        ms = e0.elapsed_time(e1) / steps
+        out[name] = {"ms_per_call": ms, "us_per_timestep": 1e3 * ms / wl.T, "timesteps_per_s": wl.T / (ms * 1e-3),
+                     "plan": R.r.describe()}
+        del R
+        torch.cuda.empty_cache()
+    mhz = pk.get("sm_max_mhz", 2070.0)
+    stash = wl.G * wl.hidden * wl.hidden  # e4m3 bytes
+    roof_us = stash / (smem_peak_gbs(mhz) * 1e9) * 1e6
+    us = out["fp8_stash_persistent"]["us_per_timestep"]
+    out["fp8_stash_persistent"]["roofline"] = {
+        "bound": "smem", "bytes_per_timestep": stash, "peak": smem_peak_gbs(mhz), "unit": "GB/s",
+        "achieved": stash / (us * 1e-6) / 1e9, "frac": roof_us / us,
+        "peak_source": "derived: 152 SMs x 128 B/clk x %.0f MHz" % mhz}
+    out["speedup_vs_streaming"] = out["bf16_streaming"]["ms_per_call"] / out["fp8_stash_persistent"]["ms_per_call"]
+    return out
+
+
 def sweep(dev, steps=5, warmup=2):
     """Selector sweep: one-layer bf16 LSTM and tanh-RNN training steps (T=16)
     over a grid of batch sizes and widths, timed with the library's own plan
@@ -689,6 +728,8 @@ def main():
     }
     # the persistent small-batch recurrence (second target of the path) under its own key as well
     line["persistent_recurrence"] = subs.get(synth.WORKLOADS[2].name)
+    if world == 1 and not args.no_workloads:
+        line["fp8_stash"] = fp8_stash_probe(dev, pk)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"], _ = time_oracle_sample(wl)
     print(json.dumps(line), flush=True)

@@ -109,6 +109,13 @@ enum {
                                                gathered per thread-block cluster */
 #define RNN_FLAG_BIDIRECTIONAL 0x2000u /* every layer gets a second direction that runs time backwards
                                           with its own weights (see the layouts below) */
+#define RNN_FLAG_FP8_STASH 0x4000u /* bf16 inference: the persistent recurrence keeps W_h on chip as e4m3
+                                      (fp8) with one float scale per gate row (half the bf16 footprint), which
+                                      lets LSTM and GRU layers up to hidden 2048 and simple RNNs up to 4096
+                                      with B <= 8 keep their recurrent weights on chip.  A deliberate
+                                      approximation (3 mantissa bits per weight): the forward then computes
+                                      with W_h' = e4m3(W_h / s) * s.  Training calls (with a reserve) keep the
+                                      bf16 path.  rnn_get_sizes includes the stash in the packed size. */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */
@@ -235,6 +242,14 @@ RNN_API int rnn_profile_query(rnn_handle_t h, int k, char* name, int* n_classes,
 RNN_API int rnn_gemm_bf16(int M, int N, int K, const void* A, long long lda, int a_mn_major,
                   const void* B, long long ldb, int b_mn_major, float* D, long long ldd,
                   const float* bias, int accumulate, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Building block exposed for tests: the per-row e4m3 quantisation of the
+ * fp8 stash (RNN_FLAG_FP8_STASH).  w: bf16 [rows][cols] on the device;
+ * scale[r] = max_k |w[r][k]| / 448 (1 for an all-zero row) and
+ * q[r][k] = e4m3(w[r][k] / scale[r]), round to nearest even.
+ * ---------------------------------------------------------------------- */
+RNN_API int rnn_quantize_e4m3_rows(int rows, int cols, const void* w, void* q, float* scale, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
  * Bias gradients with no workspace and no allocation.  The paper has no

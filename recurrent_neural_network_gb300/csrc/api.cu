@@ -135,6 +135,7 @@ struct rnn_s {
   int persist = 0, persist_ctas = 0;  // forward recurrence kind: 1 = persistent (one launch per layer)
   int persist_plan = 0;               // the kind the plan chose (variable lengths turn it off)
   int persist_cl = 0;                 // persistent hand-off: cluster size of the tagged-word exchange, 0 = counters
+  int persist8 = 0, persist8_cl = 0;  // fp8 stash (RNN_FLAG_FP8_STASH): persistent inference on e4m3 W_h
   int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
   int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
   // variable lengths (rnn_set_lengths): Bt[t] = number of sequences still
@@ -145,7 +146,7 @@ struct rnn_s {
   uint64_t limit_ns = 2000000000ull;
   // sizes (bytes)
   size_t user_w_bytes = 0, packed_bytes = 0, reserve_bytes = 0, ws_bytes = 0;
-  struct PL { size_t wx, wh, bias, bias_hn; };
+  struct PL { size_t wx, wh, bias, bias_hn, wh8, wsc; };
   struct RL { size_t gates, c, hn, hseq, dgx, dgh; };
   struct WL { size_t P, hseq, c2, dyab, carry, part, ctr, dh; };
   size_t ws_bias = 0;  // bias-gradient slices (shared by the layers, used one layer at a time)
@@ -230,6 +231,23 @@ int plan_and_layout(rnn_s* h) {
     }
   }
   if ((d.flags & RNN_FLAG_FORCE_PERSISTENT) && !h->persist) return RNN_ERR_UNSUPPORTED;
+  // fp8 stash of W_h for the persistent inference recurrence (wider layers on chip)
+  if (d.flags & RNN_FLAG_FP8_STASH) {
+    if (d.mode != RNN_MODE_BF16 || (d.flags & RNN_FLAG_FORCE_STREAMING)) return RNN_ERR_UNSUPPORTED;
+    int ctas = 0, cl = 0;
+    const bool simple = d.cell == RNN_TANH || d.cell == RNN_RELU;
+    bool fits;
+    if (h->have_device) {
+      fits = persist_check(d.cell, H, B, h->num_sms, &ctas, &cl, true) == RNN_OK;
+    } else {  // host-side planning: the sizes the device check accepts on GB300
+      fits = B <= 8 && H % 128 == 0 && H <= (simple ? 4096 : 2048);
+      for (int c = 2; c <= 8 && fits; c *= 2)
+        if ((H / 2) * B / c <= 1024) { cl = c; break; }
+    }
+    if (!fits) return RNN_ERR_UNSUPPORTED;
+    h->persist8 = 1;
+    h->persist8_cl = (d.flags & RNN_FLAG_NO_PERSIST_CLUSTER) ? 0 : cl;
+  }
   // wavefront chunking
   // (a bidirectional layer needs all of the layer below: no wavefront)
   h->wavefront = (L > 1) && !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !h->persist && h->D == 1;
@@ -310,6 +328,8 @@ int plan_and_layout(rnn_s* h) {
     h->pl[l].wh = take(cur, (size_t)GH * H * e);
     h->pl[l].bias = take(cur, (size_t)GH * 4);
     h->pl[l].bias_hn = take(cur, (size_t)H * 4);
+    h->pl[l].wh8 = (d.flags & RNN_FLAG_FP8_STASH) ? take(cur, (size_t)GH * H) : 0;
+    h->pl[l].wsc = (d.flags & RNN_FLAG_FP8_STASH) ? take(cur, (size_t)GH * 4) : 0;
   }
   h->packed_bytes = (cur + 255) & ~size_t(255);
   // reserve
@@ -329,7 +349,7 @@ int plan_and_layout(rnn_s* h) {
   cur = 0;
   h->ws_err = take(cur, 256);
   h->ws_arrive = take(cur, (size_t)T * 4);
-  h->ws_hx = h->persist_plan ? take(cur, (size_t)8 * B * H) : 0;
+  h->ws_hx = (h->persist_plan || h->persist8) ? take(cur, (size_t)8 * B * H) : 0;
   h->bias_slices = std::max(1, std::min(64, (T * B + 255) / 256));
   h->ws_bias = take(cur, (size_t)h->bias_slices * GH * 4);
   h->ws_dtop = Dn == 2 ? take(cur, (size_t)2 * T * BH * e) : 0;
@@ -506,6 +526,9 @@ int cu(cudaError_t e) { return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA; }
 // directions of a layer run side by side on two streams, forked from and
 // joined back into the caller's stream around each layer.
 
+// hand-off cluster size of the persistent recurrence (0: counters), bf16 or fp8-stash plan
+int pa_cluster(const rnn_s* h, bool p8) { return p8 ? h->persist8_cl : h->persist_cl; }
+
 // slot of h at time t in direction d (t = -1 forward, t = T reverse: the initial state)
 size_t hslot(int d, int t) { return (size_t)(t + 1 - d); }
 
@@ -521,7 +544,9 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
   cudaStream_t caller = s;
   // directions side by side (not the persistent recurrence: two grids that
   // each need most of the SMs at once must not be launched together)
-  const bool side = !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !h->persist;
+  const bool p8 = !train && h->persist8 && h->varlen == 0;  // fp8 stash (inference)
+  const bool pers = p8 || h->persist;
+  const bool side = !(d.flags & RNN_FLAG_NO_WAVEFRONT) && !pers;
   // variable lengths: running sequences at time t are rows 0 .. Bt[t]-1 in
   // both directions; idle positions of y and of the h sequences read 0
   const bool vl = h->varlen != 0;
@@ -563,14 +588,16 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
         return train ? reinterpret_cast<float*>(R + h->rl[v].c) + (size_t)tt * BH
                      : reinterpret_cast<float*>(W + h->wl[v].c2) + (size_t)(tt & 1) * BH;
       };
-      if (h->persist) {
+      if (pers) {
         // all T steps of this direction in one launch
         unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
-        if (h->persist_cl) RNN_TRY(cu(cudaMemsetAsync(W + h->ws_hx, 0, (size_t)8 * B * H, s)));
+        if (pa_cluster(h, p8)) RNN_TRY(cu(cudaMemsetAsync(W + h->ws_hx, 0, (size_t)8 * B * H, s)));
         else RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
         PersistArgs pa{};
         pa.arrive = arrive;
-        pa.cluster = h->persist_cl;
+        pa.cluster = pa_cluster(h, p8);
+        pa.Wh8 = p8 ? reinterpret_cast<const uint8_t*>(PW + h->pl[v].wh8) : nullptr;
+        pa.wscale = p8 ? reinterpret_cast<const float*>(PW + h->pl[v].wsc) : nullptr;
         pa.hx = reinterpret_cast<uint64_t*>(W + h->ws_hx);
         pa.T = T;
         pa.B = B;
@@ -595,7 +622,7 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
         RNN_TRY(persist_fwd(Lk, d.cell, pa));
       }
       // the recurrence: step k at time t, after the step at time tp
-      for (int k = 0; k < T && !h->persist; ++k) {
+      for (int k = 0; k < T && !pers; ++k) {
         const int t = dd == 0 ? k : T - 1 - k, tp = dd == 0 ? t - 1 : t + 1;
         const int Bs = Bt(t);
         if (Bs == 0) continue;
@@ -1050,10 +1077,10 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
            "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d transposed=%d fused_point=%d "
-           "persist_cluster=%d directions=%d",
+           "persist_cluster=%d directions=%d fp8_stash=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
            h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch,
-           h->bwd_bn, h->bwd_splits, h->num_sms, h->tstep, h->bwd_fuse, h->persist ? h->persist_cl : 0, h->D);
+           h->bwd_bn, h->bwd_splits, h->num_sms, h->tstep, h->bwd_fuse, h->persist ? h->persist_cl : 0, h->D, h->persist8);
   return RNN_OK;
 }
 
@@ -1072,6 +1099,12 @@ int rnn_pack_weights(rnn_handle_t h, const void* w_user, void* w_packed, cudaStr
                        U + h->ul[l].wh * e, U + h->ul[l].bx * e, U + h->ul[l].bh * e, P + h->pl[l].wx,
                        P + h->pl[l].wh, reinterpret_cast<float*>(P + h->pl[l].bias),
                        reinterpret_cast<float*>(P + h->pl[l].bias_hn)));
+    if (h->d.flags & RNN_FLAG_FP8_STASH) {
+      // the e4m3 stash of the packed W_h rows with one scale per row
+      Launch Lq = mk(h, stream, nullptr, "pack");
+      RNN_TRY(quant_rows_e4m3(Lq, P + h->pl[l].wh, h->GH, h->d.hidden, reinterpret_cast<uint8_t*>(P + h->pl[l].wh8),
+                              reinterpret_cast<float*>(P + h->pl[l].wsc)));
+    }
   }
   return RNN_OK;
 }
@@ -1095,6 +1128,13 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
     const char* PW = static_cast<const char*>(w_packed);
     (void)G;
     if (h->D == 2) return fwd_bidir(h, x, h0, c0, PW, y, hT, cT, R, W, ws, stream);
+    // inference with the fp8 stash: the persistent recurrence on e4m3 W_h,
+    // layer after layer (no wavefront)
+    const bool p8 = !train && h->persist8 && !h->varlen;
+    const bool pers = p8 || h->persist;
+    const int wf = p8 ? 0 : wf;
+    const int nch = p8 ? 1 : nch;
+    const int chunk = p8 ? T : chunk;
 
     if (h->varlen) {
       // rows past a sequence's end are never written by the steps: y reads 0
@@ -1105,14 +1145,14 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
         RNN_TRY(cu(cudaMemsetAsync(train ? R + h->rl[l].hseq : W + h->wl[l].hseq, 0, (size_t)(T + 1) * BH * e,
                                    stream)));
     }
-    if (h->wavefront) RNN_TRY(fork_streams(h, stream));
-    const int nd = h->wavefront ? (L + h->nch - 1) : 1;
+    if (wf) RNN_TRY(fork_streams(h, stream));
+    const int nd = wf ? (L + nch - 1) : 1;
     for (int dg = 0; dg < nd; ++dg) {
       for (int l = 0; l < L; ++l) {
-        for (int c = 0; c < h->nch; ++c) {
-          if (h->wavefront && l + c != dg) continue;
-          cudaStream_t s = h->wavefront ? h->streams[l] : stream;
-          const int t0 = c * h->chunk, t1 = std::min(T, t0 + h->chunk);
+        for (int c = 0; c < nch; ++c) {
+          if (wf && l + c != dg) continue;
+          cudaStream_t s = wf ? h->streams[l] : stream;
+          const int t0 = c * chunk, t1 = std::min(T, t0 + chunk);
           char* hseq = train ? R + h->rl[l].hseq : W + h->wl[l].hseq;
           float* P = reinterpret_cast<float*>(train ? R + h->rl[l].gates : W + h->wl[l].P);
           if (c == 0) {
@@ -1120,7 +1160,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
                                                cudaMemcpyDeviceToDevice, s)));
             else RNN_TRY(cu(cudaMemsetAsync(hseq, 0, BH * e, s)));
           }
-          if (h->wavefront && l > 0) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l - 1) * h->nch + c], 0)));
+          if (wf && l > 0) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l - 1) * nch + c], 0)));
           // input projection (layer 0: all T at once)
           if (l > 0 || c == 0) {
             const int r0 = l == 0 ? 0 : t0, r1 = l == 0 ? T : t1;
@@ -1140,13 +1180,15 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
                              reinterpret_cast<const float*>(PW + h->pl[l].bias), 0, none, 0));
           }
           // persistent recurrence: all T steps of the layer in one launch
-          if (h->persist) {
+          if (pers) {
             unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
-            if (h->persist_cl) RNN_TRY(cu(cudaMemsetAsync(W + h->ws_hx, 0, (size_t)8 * B * H, s)));
+            if (pa_cluster(h, p8)) RNN_TRY(cu(cudaMemsetAsync(W + h->ws_hx, 0, (size_t)8 * B * H, s)));
             else RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
             PersistArgs pa{};
             pa.arrive = arrive;
-            pa.cluster = h->persist_cl;
+            pa.cluster = p8 ? h->persist8_cl : h->persist_cl;
+            pa.Wh8 = p8 ? reinterpret_cast<const uint8_t*>(PW + h->pl[l].wh8) : nullptr;
+            pa.wscale = p8 ? reinterpret_cast<const float*>(PW + h->pl[l].wsc) : nullptr;
             pa.hx = reinterpret_cast<uint64_t*>(W + h->ws_hx);
             pa.T = T;
             pa.B = B;
@@ -1211,11 +1253,11 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
                                            (size_t)nr * H * 4, cudaMemcpyDeviceToDevice, s)));
             }
           }
-          if (h->wavefront) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * h->nch + c], s)));
+          if (wf) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * nch + c], s)));
         }
       }
     }
-    if (h->wavefront) RNN_TRY(join_streams(h, stream));
+    if (wf) RNN_TRY(join_streams(h, stream));
     return RNN_OK;
   };
   return run_graphed(h, stream, key, issue);
@@ -1505,6 +1547,18 @@ int rnn_gemm_bf16(int M, int N, int K, const void* A, long long lda, int a_mn_ma
   L.name = "gemm";
   Remap none{0, 1, 1, 1};
   return gemm_f32(L, RNN_MODE_BF16, a, b, M, N, K, D, ldd, bias, accumulate, none, 0);
+}
+
+int rnn_quantize_e4m3_rows(int rows, int cols, const void* w, void* q, float* scale, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0 || !w || !q || !scale) return RNN_ERR_INVALID_ARG;
+  Launch L;
+  L.stream = stream;
+  L.err = nullptr;
+  L.limit_ns = 2000000000ull;
+  L.num_sms = 0;
+  L.prof = nullptr;
+  L.name = "quant";
+  return quant_rows_e4m3(L, w, rows, cols, static_cast<uint8_t*>(q), scale);
 }
 
 }  // extern "C"

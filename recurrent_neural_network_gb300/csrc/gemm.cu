@@ -8,6 +8,8 @@
 // is a single large product over all timesteps with a cheap bias update.
 #include <algorithm>
 
+#include <cuda_fp8.h>
+
 #include "epilogues.cuh"
 #include "launch.cuh"
 
@@ -114,6 +116,38 @@ int cast_bf16(const Launch& L, const float* src, void* dst, size_t n) {
   const int blocks = (int)std::min<size_t>((n4 + 255) / 256, (size_t)L.num_sms * 8);
   launch_begin(L);
   cast_bf16_kernel<<<blocks, 256, 0, L.stream>>>(reinterpret_cast<const float4*>(src), static_cast<uint2*>(dst), n4);
+  cudaError_t e = cudaGetLastError();
+  launch_end(L);
+  return cuda_status(e);
+}
+
+// ---------------------------------------------------------------- fp8 stash of W_h
+// One block per row: the row's largest magnitude, the scale that maps it to
+// the largest finite e4m3 value (448), and every element divided by the scale
+// and rounded to the nearest e4m3 value (ties to even; CUDA's conversion).
+__global__ void quant_rows_kernel(const __nv_bfloat16* __restrict__ w, int cols, uint8_t* __restrict__ q,
+                                  float* __restrict__ scale) {
+  __shared__ float red[32];
+  const __nv_bfloat16* row = w + (size_t)blockIdx.x * cols;
+  float m = 0.f;
+  for (int k = threadIdx.x; k < cols; k += blockDim.x) m = fmaxf(m, fabsf(__bfloat162float(row[k])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+  const float s = m > 0.f ? m / 448.f : 1.f;
+  if (threadIdx.x == 0) scale[blockIdx.x] = s;
+  uint8_t* qr = q + (size_t)blockIdx.x * cols;
+  for (int k = threadIdx.x; k < cols; k += blockDim.x)
+    qr[k] = (uint8_t)__nv_cvt_float_to_fp8(__bfloat162float(row[k]) / s, __NV_SATFINITE, __NV_E4M3);
+}
+
+int quant_rows_e4m3(const Launch& L, const void* w, int rows, int cols, uint8_t* q, float* scale) {
+  if (rows <= 0 || cols <= 0 || !w || !q || !scale) return RNN_ERR_INVALID_ARG;
+  launch_begin(L);
+  quant_rows_kernel<<<rows, 256, 0, L.stream>>>(static_cast<const __nv_bfloat16*>(w), cols, q, scale);
   cudaError_t e = cudaGetLastError();
   launch_end(L);
   return cuda_status(e);

@@ -64,6 +64,10 @@ int bias_grad(const Launch& L, int mode, int cell, int H, int u, long long rows,
               float* dbx, float* dbh, int accumulate, float* part, int slices);
 // dst[i] = src[i] rounded to bf16 (n a multiple of 4; both 16-byte aligned)
 int cast_bf16(const Launch& L, const float* src, void* dst, size_t n);
+// Per-row e4m3 quantisation of a bf16 matrix w[rows][cols]: scale[r] =
+// max_k |w[r][k]| / 448 (1 for an all-zero row) and q[r][k] = e4m3(w / scale)
+// rounded to nearest even (|w / scale| <= 448 by construction).
+int quant_rows_e4m3(const Launch& L, const void* w, int rows, int cols, uint8_t* q, float* scale);
 
 // ---------------------------------------------------------------- step_fwd.cu
 struct FwdStepArgs {
@@ -146,6 +150,8 @@ int bwd_point_v(const Launch& L, int cell, const PointVArgs& a);
 struct PersistArgs {
   int T, B, H, u_pack, uc;
   const __nv_bfloat16* Wh;  // packed [G*H][H]
+  const uint8_t* Wh8;       // fp8 stash: packed [G*H][H] e4m3 bytes (null: bf16 fragments from Wh)
+  const float* wscale;      // fp8 stash: scale of each packed row
   const float* P;           // [T][B][G*H] input projection incl. bias
   float* gates_out;         // training: activated gates [T][B][G*H] (may alias P), else null
   const float* bias_hn;     // GRU [H]
@@ -168,8 +174,9 @@ struct PersistArgs {
 // RNN_OK if the persistent recurrence supports (cell, H, B) and all its CTAs
 // fit on the device at once; *ctas receives the grid size and *cluster (if
 // not null) the largest cluster size (8, 4 or 2) whose clusters all fit at
-// once for the cluster-exchange hand-off, 0 if none.
-int persist_check(int cell, int H, int B, int num_sms, int* ctas, int* cluster = nullptr);
+// once for the cluster-exchange hand-off, 0 if none.  fp8: with the e4m3
+// stash of W_h.
+int persist_check(int cell, int H, int B, int num_sms, int* ctas, int* cluster = nullptr, bool fp8 = false);
 // all T timesteps of one layer in one cooperative launch (bf16 storage only)
 int persist_fwd(const Launch& L, int cell, const PersistArgs& a);
 

@@ -28,11 +28,21 @@
 // one thread per CTA polls the counter of the previous step until every CTA
 // has arrived, then the CTA reads h_{t-1} once through L2.
 //
+// fp8 stash (PersistArgs::Wh8 set): W_h is held as e4m3 bytes with one fp32
+// scale per packed row, in shared memory (in fragment order, read once per
+// step), so that LSTM and GRU layers twice as wide as the register-resident
+// bf16 variant keep their recurrent weights on chip ("Persistent RNNs" page,
+// citing snippets: on-chip storage is small and inflexible in precision).
+// Each step widens the bytes to f16 with an exact bit rearrangement, runs the
+// product as f16 MMAs against h (bf16 converted to f16) and applies the row
+// scales to the fp32 sums.
+//
 // Every wait is bounded (globaltimer); on timeout the CTA records
 // DEV_TIMEOUT_STEP in the error word and leaves (in the cluster variant the
 // whole cluster leaves together, after the step's cluster barrier).
 // Co-residency of all CTAs is guaranteed by a cooperative launch.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "../../include/rnn.h"
 #include "common.cuh"
@@ -49,6 +59,30 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, cons
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Two e4m3 bytes of x (bytes 0,1 with sel 0x1404, bytes 2,3 with sel 0x3424)
+// as an f16 pair worth 2^-8 times their value.  Each byte s.eeee.mmm lands in
+// the high byte of a half (sign at bit 15), and the seven bits below the sign
+// move down one place, giving exponent field 0eeee and mantissa mmm0000000:
+// 2^(e-15) (1 + m/8) for normal bytes and 2^-14 (m/8) for subnormal ones,
+// i.e. the e4m3 value (bias 7) times 2^-8, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_lo8(uint32_t x, uint32_t sel) {
+  const uint32_t p = __byte_perm(x, 0u, sel);
+  return ((p >> 1) & 0x3F803F80u) | (p & 0x80008000u);
+}
+// bf16 pair -> f16 pair (round to nearest)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
@@ -83,20 +117,27 @@ __device__ __forceinline__ unsigned short bf16_bits(float v) {
 }
 
 // most tagged words one thread polls per step (the cluster size is chosen so
-// that B*H/2 words over the cluster's CTAs of 256 threads stay within it)
+// that B*H/2 words over the cluster's CTAs' threads stay within it)
 constexpr int kMaxWords = 4;
 
-template <int CELL, int MT, int KT, bool XCL>
-__global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a) {
+// NT threads (8 or 16 warps, each taking KT 16-deep k-tiles of W_h's K range)
+template <int CELL, int MT, int KT, bool XCL, bool W8, int NT>
+__global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a) {
   constexpr int G = CellInfo<CELL>::G;
   constexpr int ROWS = MT * 16;  // = G * uc
-  __shared__ float part[8][ROWS][8];
+  constexpr int NWARP = NT / 32;
+  __shared__ float part[NWARP][ROWS][8];
   __shared__ float sums[ROWS][8];
+  __shared__ float rscale[W8 ? ROWS : 1];  // fp8 stash: row scale x 2^8
   __shared__ int abort_flag;
   __shared__ int abort_x[2];  // cluster exchange: set in every CTA of the cluster by one that gave up
-  // cluster exchange: h_{t-1} ping-pong [2][B][H + 8] bf16 (rows padded so
-  // that the eight batch rows of a fragment load fall in distinct banks)
-  extern __shared__ __align__(16) unsigned char hbuf[];
+  // dynamic shared memory: fp8 stash of this CTA's W_h rows (ROWS x H bytes
+  // in fragment order), then for the cluster exchange the h_{t-1} ping-pong
+  // [2][B][H + 8] bf16 (rows padded so that the eight batch rows of a
+  // fragment load fall in distinct banks)
+  extern __shared__ __align__(16) unsigned char dsm[];
+  uint32_t* w8s = reinterpret_cast<uint32_t*>(dsm);
+  unsigned char* hbuf = dsm + (W8 ? ROWS * a.H : 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int uc = ROWS / G;
   const int H = a.H, B = a.B, GH = G * H;
@@ -107,8 +148,11 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
   const int slot_h0 = a.reverse ? a.T : 0;
   if (threadIdx.x == 0) abort_flag = 0;
 
-  // ---- this CTA's rows of W_h as A fragments (row r = g*uc + local unit)
-  uint32_t wf[MT][KT][4];
+  // ---- this CTA's rows of W_h as A fragments (row r = g*uc + local unit),
+  // in registers; fp8 stash: in shared memory, per row of a fragment the four
+  // bytes at k, k+1, k+8, k+9, word i of (mt, kt) of this thread at
+  // w8s[((warp * MT + mt) * KT + kt) * 64 + lane * 2 + i]
+  uint32_t wf[W8 ? 1 : MT][W8 ? 1 : KT][4];
   {
     const int kw = warp * KT * 16;
 #pragma unroll
@@ -116,17 +160,32 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       const int r0 = mt * 16 + (lane >> 2), r1 = r0 + 8;
       const int p0 = packed_row(r0 / uc, jbase + r0 % uc, G, a.u_pack);
       const int p1 = packed_row(r1 / uc, jbase + r1 % uc, G, a.u_pack);
-      const uint32_t* w0 = reinterpret_cast<const uint32_t*>(a.Wh + (size_t)p0 * H);
-      const uint32_t* w1 = reinterpret_cast<const uint32_t*>(a.Wh + (size_t)p1 * H);
+      if constexpr (W8) {
+        const uint16_t* w0 = reinterpret_cast<const uint16_t*>(a.Wh8 + (size_t)p0 * H);
+        const uint16_t* w1 = reinterpret_cast<const uint16_t*>(a.Wh8 + (size_t)p1 * H);
+        for (int kt = 0; kt < KT; ++kt) {
+          const int k = kw + kt * 16 + (lane & 3) * 2;
+          uint32_t* d = w8s + ((warp * MT + mt) * KT + kt) * 64 + lane * 2;
+          d[0] = (uint32_t)w0[k >> 1] | ((uint32_t)w0[(k + 8) >> 1] << 16);
+          d[1] = (uint32_t)w1[k >> 1] | ((uint32_t)w1[(k + 8) >> 1] << 16);
+        }
+      } else {
+        const uint32_t* w0 = reinterpret_cast<const uint32_t*>(a.Wh + (size_t)p0 * H);
+        const uint32_t* w1 = reinterpret_cast<const uint32_t*>(a.Wh + (size_t)p1 * H);
 #pragma unroll
-      for (int kt = 0; kt < KT; ++kt) {
-        const int k = kw + kt * 16 + (lane & 3) * 2;
-        wf[mt][kt][0] = w0[k >> 1];
-        wf[mt][kt][1] = w1[k >> 1];
-        wf[mt][kt][2] = w0[(k + 8) >> 1];
-        wf[mt][kt][3] = w1[(k + 8) >> 1];
+        for (int kt = 0; kt < KT; ++kt) {
+          const int k = kw + kt * 16 + (lane & 3) * 2;
+          wf[mt][kt][0] = w0[k >> 1];
+          wf[mt][kt][1] = w1[k >> 1];
+          wf[mt][kt][2] = w0[(k + 8) >> 1];
+          wf[mt][kt][3] = w1[(k + 8) >> 1];
+        }
       }
     }
+  }
+  if constexpr (W8) {
+    for (int r = threadIdx.x; r < ROWS; r += NT)
+      rscale[r] = a.wscale[packed_row(r / uc, jbase + r % uc, G, a.u_pack)] * 256.f;
   }
 
   // ---- cell-update threads: one (unit, batch row) pair each
@@ -147,7 +206,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
   const int NW = (H / 2) * B;           // tagged words of h per step
   const int WS = (uc * B) / 2;          // of which this CTA produces
   uint32_t crank = 0, csize = 1;
-  // this thread's share of the tagged words of a step: w0 + 256 i, i < nmine,
+  // this thread's share of the tagged words of a step: w0 + NT i, i < nmine,
   // and where word i lands in an h buffer (word w of CTA c holds units jj,
   // jj+1 of batch row bq)
   int w0 = 0, nmine = 0;
@@ -157,17 +216,17 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
     csize = (uint32_t)a.cluster;
     const int per = NW / (int)csize;
     w0 = (int)crank * per + threadIdx.x;
-    nmine = per > (int)threadIdx.x ? min(kMaxWords, (per - (int)threadIdx.x + 255) / 256) : 0;
+    nmine = per > (int)threadIdx.x ? min(kMaxWords, (per - (int)threadIdx.x + NT - 1) / NT) : 0;
 #pragma unroll
     for (int i = 0; i < kMaxWords; ++i) {
-      const int w = w0 + i * 256;
+      const int w = w0 + i * NT;
       const int c = w / WS, q0 = 2 * (w - c * WS);
       const int bq = q0 / uc, jj = c * uc + (q0 - bq * uc);
       offw[i] = (uint32_t)(bq * HP2 * 4 + jj * 2);
     }
     const uint32_t* h0w = reinterpret_cast<const uint32_t*>(a.hseq + (size_t)slot_h0 * B * H);
     uint32_t* hw = reinterpret_cast<uint32_t*>(hbuf);
-    for (int i = threadIdx.x; i < NW; i += 256) {
+    for (int i = threadIdx.x; i < NW; i += NT) {
       const int b = i / (H / 2);
       hw[b * HP2 + (i - b * (H / 2))] = h0w[i];
     }
@@ -207,7 +266,7 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
         uint64_t v[kMaxWords];
 #pragma unroll
         for (int i = 0; i < kMaxWords; ++i)
-          if ((pending >> i) & 1u) v[i] = ld_relaxed_u64(src + w0 + i * 256);
+          if ((pending >> i) & 1u) v[i] = ld_relaxed_u64(src + w0 + i * NT);
 #pragma unroll
         for (int i = 0; i < kMaxWords; ++i) {
           if (((pending >> i) & 1u) && (uint32_t)(v[i] >> 32) == want) {
@@ -250,34 +309,47 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       __syncthreads();
       if (abort_flag) break;
     }
-    uint32_t bf[KT][2];
-    if (XCL && nb < B) {
-      const uint32_t* hs = reinterpret_cast<const uint32_t*>(hbuf) + ((t & 1) * B + nb) * HP2 + (kw >> 1);
-#pragma unroll
-      for (int kt = 0; kt < KT; ++kt) {
-        bf[kt][0] = hs[kt * 8];
-        bf[kt][1] = hs[kt * 8 + 4];
-      }
-    } else if (nb < B) {
-      const uint32_t* hs = reinterpret_cast<const uint32_t*>(a.hseq + ((size_t)s_in * B + nb) * H + kw);
-#pragma unroll
-      for (int kt = 0; kt < KT; ++kt) {
-        bf[kt][0] = __ldcg(hs + ((kt * 16) >> 1));
-        bf[kt][1] = __ldcg(hs + ((kt * 16 + 8) >> 1));
-      }
-    } else {
-#pragma unroll
-      for (int kt = 0; kt < KT; ++kt) bf[kt][0] = bf[kt][1] = 0u;
-    }
-    // ---- partial products over this warp's K range
+    // ---- partial products over this warp's K range (B fragments of h_{t-1}
+    // from the cluster's shared-memory copy or through L2)
     float acc[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    const uint32_t* hsx = reinterpret_cast<const uint32_t*>(hbuf) + ((t & 1) * B + nb) * HP2 + (kw >> 1);
+    const uint32_t* hsg = reinterpret_cast<const uint32_t*>(a.hseq + ((size_t)s_in * B + min(nb, B - 1)) * H + kw);
+    auto load_b = [&](int kt, uint32_t* b2) {
+      if (nb >= B) {
+        b2[0] = b2[1] = 0u;
+      } else if (XCL) {
+        b2[0] = hsx[kt * 8];
+        b2[1] = hsx[kt * 8 + 4];
+      } else {
+        b2[0] = __ldcg(hsg + kt * 8);
+        b2[1] = __ldcg(hsg + kt * 8 + 4);
+      }
+    };
+    if constexpr (W8) {
+#pragma unroll 4
+      for (int kt = 0; kt < KT; ++kt) {
+        uint32_t b2[2];
+        load_b(kt, b2);
+        const uint32_t hb[2] = {bf16x2_to_f16x2(b2[0]), bf16x2_to_f16x2(b2[1])};
 #pragma unroll
-    for (int kt = 0; kt < KT; ++kt)
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint2 q = *reinterpret_cast<const uint2*>(w8s + ((warp * MT + mt) * KT + kt) * 64 + lane * 2);
+          const uint32_t af[4] = {e4m3x2_to_f16x2_lo8(q.x, 0x1404u), e4m3x2_to_f16x2_lo8(q.y, 0x1404u),
+                                  e4m3x2_to_f16x2_lo8(q.x, 0x3424u), e4m3x2_to_f16x2_lo8(q.y, 0x3424u)};
+          mma_f16_16816(acc[mt], af, hb);
+        }
+      }
+    } else {
+      uint32_t bf[KT][2];
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[mt], wf[mt][kt], bf[kt]);
+      for (int kt = 0; kt < KT; ++kt) load_b(kt, bf[kt]);
 #pragma unroll
+      for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) mma_bf16_16816(acc[mt], reinterpret_cast<const uint32_t*>(wf[mt][kt]), bf[kt]);
+    }
     for (int mt = 0; mt < MT; ++mt) {
       const int r = mt * 16 + (lane >> 2), c = (lane & 3) * 2;
       part[warp][r][c] = acc[mt][0];
@@ -286,11 +358,12 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
       part[warp][r + 8][c + 1] = acc[mt][3];
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < ROWS * 8; idx += 256) {
+    for (int idx = threadIdx.x; idx < ROWS * 8; idx += NT) {
       const int r = idx >> 3, c = idx & 7;
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < 8; ++w) s += part[w][r][c];
+      for (int w = 0; w < NWARP; ++w) s += part[w][r][c];
+      if constexpr (W8) s *= rscale[r];
       sums[r][c] = s;
     }
     __syncthreads();
@@ -363,14 +436,19 @@ __global__ void __launch_bounds__(256, 1) persist_fwd_kernel(const PersistArgs a
   }
 }
 
-template <int CELL, int MT, int KT>
+template <int CELL, int MT, int KT, bool W8, int NT>
 int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only, int num_sms, int* cl_out) {
-  auto kc = persist_fwd_kernel<CELL, MT, KT, false>;
-  auto kx = persist_fwd_kernel<CELL, MT, KT, true>;
-  const size_t dyn = (size_t)2 * a.B * (a.H + 8) * 2;  // h_{t-1} ping-pong of the cluster variant
+  auto kc = persist_fwd_kernel<CELL, MT, KT, false, W8, NT>;
+  auto kx = persist_fwd_kernel<CELL, MT, KT, true, W8, NT>;
+  const size_t dyn_w = W8 ? (size_t)MT * 16 * a.H : 0;               // fp8 stash of the CTA's rows
+  const size_t dyn = dyn_w + (size_t)2 * a.B * (a.H + 8) * 2;  // + h_{t-1} ping-pong of the cluster variant
+  if (dyn_w && cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_w) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return RNN_ERR_UNSUPPORTED;
+  }
   if (query_only) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, 256, 0) != cudaSuccess) return RNN_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kc, NT, dyn_w) != cudaSuccess) return RNN_ERR_CUDA;
     if (per_sm * num_sms < ctas) return RNN_ERR_LAUNCH;
     if (cl_out) {
       // the largest cluster size whose clusters all co-reside (0: none)
@@ -380,10 +458,10 @@ int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only,
         return RNN_OK;
       }
       for (int c = 8; c >= 2; c /= 2) {
-        if (ctas % c || (a.H / 2) * a.B / c > 256 * kMaxWords) continue;
+        if (ctas % c || (a.H / 2) * a.B / c > NT * kMaxWords) continue;
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(ctas);
-        cfg.blockDim = dim3(256);
+        cfg.blockDim = dim3(NT);
         cfg.dynamicSmemBytes = dyn;
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeClusterDimension;
@@ -410,7 +488,7 @@ int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only,
     if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg{};
       cfg.gridDim = dim3(ctas);
-      cfg.blockDim = dim3(256);
+      cfg.blockDim = dim3(NT);
       cfg.dynamicSmemBytes = dyn;
       cfg.stream = L.stream;
       cudaLaunchAttribute at[2];
@@ -426,7 +504,7 @@ int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only,
     }
   } else {
     void* params[] = {&args};
-    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kc), dim3(ctas), dim3(256), params, 0, L.stream);
+    e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kc), dim3(ctas), dim3(NT), params, dyn_w, L.stream);
   }
   launch_end(L);
   if (e == cudaErrorCooperativeLaunchTooLarge) return RNN_ERR_LAUNCH;
@@ -434,33 +512,57 @@ int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only,
 }
 
 // (cell, H) -> kernel instance; MT*16 = G*uc rows per CTA, KT*16*8 = H.
+// bf16 fragments in registers: LSTM up to H = 1024 (8 units per CTA), GRU up
+// to 1024 and the simple RNNs up to 2048 (16 units).  fp8 stash in shared
+// memory: LSTM up to 2048 (16 units per CTA from H = 2048, 128 KB of weights),
+// GRU up to 2048 (96 KB) and the simple RNNs up to 2048; about 128 CTAs.
 int dispatch(const Launch& L, int cell, const PersistArgs& a, bool query_only, int num_sms, int* ctas_out,
              int* cl_out) {
   const int H = a.H;
+  const bool w8 = a.Wh8 != nullptr;
   if (H % 128 || a.B < 1 || a.B > 8) return RNN_ERR_UNSUPPORTED;
-  const int KT = H / 128;
   int uc = cell == LSTM ? 8 : 16;
+  if (w8 && cell == LSTM && H >= 2048) uc = 16;
+  const int NT = 256;
+  const int KT = H / (16 * (NT / 32));
   const int ctas = H / uc;
   if (ctas_out) *ctas_out = ctas;
   PersistArgs b = a;
   b.uc = uc;
 #define RNN_P(C, MT_, KT_) \
-  if (cell == C && KT == KT_) return launch_one<C, MT_, KT_>(L, b, ctas, query_only, num_sms, cl_out);
-  RNN_P(LSTM, 2, 1) RNN_P(LSTM, 2, 2) RNN_P(LSTM, 2, 4) RNN_P(LSTM, 2, 8)
-  RNN_P(GRU, 3, 1) RNN_P(GRU, 3, 2) RNN_P(GRU, 3, 4) RNN_P(GRU, 3, 8)
-  RNN_P(TANH, 1, 1) RNN_P(TANH, 1, 2) RNN_P(TANH, 1, 4) RNN_P(TANH, 1, 8) RNN_P(TANH, 1, 16)
-  RNN_P(RELU, 1, 1) RNN_P(RELU, 1, 2) RNN_P(RELU, 1, 4) RNN_P(RELU, 1, 8) RNN_P(RELU, 1, 16)
+  if (cell == C && KT == KT_ && NT == 256) return launch_one<C, MT_, KT_, false, 256>(L, b, ctas, query_only, num_sms, cl_out);
+#define RNN_P8(C, MT_, KT_, NT_) \
+  if (cell == C && KT == KT_ && NT == NT_ && MT_ * 16 == CellInfo<C>::G * uc) \
+    return launch_one<C, MT_, KT_, true, NT_>(L, b, ctas, query_only, num_sms, cl_out);
+  if (!w8) {
+    RNN_P(LSTM, 2, 1) RNN_P(LSTM, 2, 2) RNN_P(LSTM, 2, 4) RNN_P(LSTM, 2, 8)
+    RNN_P(GRU, 3, 1) RNN_P(GRU, 3, 2) RNN_P(GRU, 3, 4) RNN_P(GRU, 3, 8)
+    RNN_P(TANH, 1, 1) RNN_P(TANH, 1, 2) RNN_P(TANH, 1, 4) RNN_P(TANH, 1, 8) RNN_P(TANH, 1, 16)
+    RNN_P(RELU, 1, 1) RNN_P(RELU, 1, 2) RNN_P(RELU, 1, 4) RNN_P(RELU, 1, 8) RNN_P(RELU, 1, 16)
+  } else {
+    RNN_P8(LSTM, 2, 1, 256) RNN_P8(LSTM, 2, 2, 256) RNN_P8(LSTM, 2, 4, 256) RNN_P8(LSTM, 2, 8, 256)
+    RNN_P8(LSTM, 4, 16, 256)
+    RNN_P8(GRU, 3, 1, 256) RNN_P8(GRU, 3, 2, 256) RNN_P8(GRU, 3, 4, 256) RNN_P8(GRU, 3, 8, 256)
+    RNN_P8(GRU, 3, 16, 256)
+    RNN_P8(TANH, 1, 1, 256) RNN_P8(TANH, 1, 2, 256) RNN_P8(TANH, 1, 4, 256) RNN_P8(TANH, 1, 8, 256)
+    RNN_P8(TANH, 1, 16, 256)
+    RNN_P8(RELU, 1, 1, 256) RNN_P8(RELU, 1, 2, 256) RNN_P8(RELU, 1, 4, 256) RNN_P8(RELU, 1, 8, 256)
+    RNN_P8(RELU, 1, 16, 256)
+  }
 #undef RNN_P
+#undef RNN_P8
   return RNN_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
-int persist_check(int cell, int H, int B, int num_sms, int* ctas, int* cluster) {
+int persist_check(int cell, int H, int B, int num_sms, int* ctas, int* cluster, bool fp8) {
   Launch L{};
   PersistArgs a{};
   a.H = H;
   a.B = B;
+  static const uint8_t dummy = 0;
+  a.Wh8 = fp8 ? &dummy : nullptr;
   return dispatch(L, cell, a, true, num_sms, ctas, cluster);
 }
 

@@ -31,11 +31,13 @@ FLAG_FORCE_TRANSPOSED = 0x400
 FLAG_NO_FUSED_POINT = 0x800
 FLAG_NO_PERSIST_CLUSTER = 0x1000
 FLAG_BIDIRECTIONAL = 0x2000
+FLAG_FP8_STASH = 0x4000
 
 # every symbol include/rnn.h declares
 SYMBOLS = ["rnn_create", "rnn_destroy", "rnn_get_sizes", "rnn_pack_weights", "rnn_fwd", "rnn_bwd_data",
            "rnn_bwd_weights", "rnn_sync_status", "rnn_strerror", "rnn_describe", "rnn_launch_count",
-           "rnn_profile_query", "rnn_gemm_bf16", "rnn_bias_grad_static", "rnn_set_lengths"]
+           "rnn_profile_query", "rnn_gemm_bf16", "rnn_bias_grad_static", "rnn_set_lengths",
+           "rnn_quantize_e4m3_rows"]
 BIAS_STATIC_FLOATS = 1 << 20
 
 
@@ -83,6 +85,7 @@ def load(path: str = LIB_PATH):
                                   ctypes.c_longlong, vp, ci, vp]
     lib.rnn_bias_grad_static.argtypes = [H, vp, vp, ci, vp]
     lib.rnn_set_lengths.argtypes = [H, ctypes.POINTER(ci)]
+    lib.rnn_quantize_e4m3_rows.argtypes = [ci, ci, vp, vp, vp, vp]
     for name in SYMBOLS:
         if name != "rnn_strerror" and name != "rnn_launch_count":
             getattr(lib, name).restype = ci
@@ -118,6 +121,13 @@ def gemm_bf16(A, B, D, M, N, K, lda, ldb, ldd, a_mn=False, b_mn=False, bias=None
     """D[m][n] = sum_k A(m,k) B(n,k) (+bias) (+D) on the tcgen05 engine (test hook)."""
     check(load().rnn_gemm_bf16(M, N, K, _ptr(A), lda, int(a_mn), _ptr(B), ldb, int(b_mn), _ptr(D), ldd, _ptr(bias),
                                int(accumulate), _stream(stream)), "rnn_gemm_bf16")
+
+
+def quantize_e4m3_rows(w, q, scale, stream=None):
+    """Per-row e4m3 quantisation of a bf16 [rows][cols] device tensor (test hook of the fp8 stash)."""
+    rows, cols = w.shape
+    check(load().rnn_quantize_e4m3_rows(rows, cols, _ptr(w), _ptr(q), _ptr(scale), _stream(stream)),
+          "rnn_quantize_e4m3_rows")
 
 
 class RNN:

@@ -228,3 +228,24 @@ def test_device_generator_matches_host_generator(wl):
         dev = synth.device_tensor(small, what, "cpu", torch.float32).numpy().astype(np.float64)
         assert dev.shape == host.shape, what
         np.testing.assert_allclose(dev, host.astype(np.float32), rtol=1e-6, atol=1e-6, err_msg=what)
+
+
+def test_fp8_stash_plan_and_sizes(lib):
+    """RNN_FLAG_FP8_STASH: bf16 persistent inference with e4m3 W_h up to H=2048
+    (LSTM, GRU); the packed buffer gains G*H*H bytes and G*H scales per layer;
+    refused where no persistent plan exists or in the fp32 mode."""
+    for cell, H, B in [(0, 2048, 4), (1, 2048, 8), (0, 256, 3), (2, 1024, 5)]:
+        a = rnn.RNN(cell, 2, 8, B, 64, H, 1, flags=rnn.FLAG_FP8_STASH)
+        b = rnn.RNN(cell, 2, 8, B, 64, H, 1)
+        assert "fp8_stash=1" in a.describe() and "fp8_stash=0" in b.describe()
+        G = synth.GATES[cell]
+        extra = a.sizes()["packed_weights"] - b.sizes()["packed_weights"]
+        assert extra >= 2 * (G * H * H + G * H * 4) and extra <= 2 * (G * H * H + G * H * 4) + 4 * 256
+        assert a.sizes()["workspace"] >= b.sizes()["workspace"]
+    for bad in [dict(mode=0, hidden=256), dict(B=16, hidden=256), dict(hidden=4096), dict(flags_extra=rnn.FLAG_FORCE_STREAMING)]:
+        kw = dict(cell=0, layers=1, T=4, B=4, input=64, hidden=512, mode=1)
+        extra = bad.pop("flags_extra", 0)
+        kw.update(bad)
+        with pytest.raises(rnn.RnnError) as e:
+            rnn.RNN(**kw, flags=rnn.FLAG_FP8_STASH | extra)
+        assert e.value.code == -2
