@@ -59,6 +59,11 @@ def _load():
         lib.rnn_ref_fwd_dir.restype = ci
         lib.rnn_ref_bwd_dir.argtypes = [ci] * 7 + [ip] + [dp] * 11
         lib.rnn_ref_bwd_dir.restype = ci
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.rnn_ref_fwd_kp.argtypes = [ci] * 7 + [ip, ci, u8p, dp] + [dp] * 7
+        lib.rnn_ref_fwd_kp.restype = ci
+        lib.rnn_ref_bwd_kp.argtypes = [ci] * 7 + [ip, ci, u8p] + [dp] * 11
+        lib.rnn_ref_bwd_kp.restype = ci
         lib.rnn_ref_threads.restype = ci
         _lib = lib
     return _lib
@@ -101,11 +106,49 @@ def _ip(a):
     return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
 
 
-def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None, lens=None, D=1):
+def _on(on, cell, L, T, B, H, D, decide):
+    """uint8 decisions array [L*D][T][B][H]: given (decide = 3) or to be filled."""
+    if cell != 3:
+        return None
+    if decide == 3:
+        if on is None:
+            raise ValueError("decide=3 needs the decisions `on`")
+        a = np.ascontiguousarray(on, dtype=np.uint8)
+        assert a.shape == (L * D, T, B, H)
+        return a
+    return np.zeros((L * D, T, B, H), np.uint8)
+
+
+def _u8(a):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+
+
+def relu_decisions(L, T, B, I, H, x, w, h0=None, lens=None, D=1, decide=1):
+    """ReLU cell: (decisions uint8 [L*D][T][B][H], pre-activations [L*D][T][B][H])
+    of the forward pass that takes the decisions in precision `decide`."""
+    lens = _lens(lens, T, B)
+    x = _c(x, (T, B, I))
+    w = _c(w, (weight_count(3, L, I, H, D),))
+    h0 = _c(h0, (L * D, B, H))
+    on = np.zeros((L * D, T, B, H), np.uint8)
+    pre = np.zeros((L * D, T, B, H))
+    y = np.zeros((T, B, D * H))
+    hT = np.zeros((L * D, B, H))
+    rc = _load().rnn_ref_fwd_kp(3, L, D, T, B, I, H, _ip(lens), int(decide), _u8(on), _p(pre), _p(x), _p(h0), None,
+                                _p(w), _p(y), _p(hT), None)
+    if rc != 0:
+        raise ValueError(f"rnn_ref_fwd_kp rejected its arguments ({rc})")
+    return on, pre
+
+
+def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None, lens=None, D=1, decide=0, on=None):
     """Forward pass. Returns (y[T][B][D*H], hT[L*D][B][H], cT[L*D][B][H] or None).
     lens[B] (optional): per-sequence lengths; later outputs are 0 and hT / cT
     are each sequence's state after its own last step.  D = 2: bidirectional
-    layers (direction 1 runs time backwards; states indexed layer * 2 + direction)."""
+    layers (direction 1 runs time backwards; states indexed layer * 2 + direction).
+    decide (ReLU cell): 0 decides on/off in double, 1 / 2 as a device storing
+    h in bf16 / fp32 would, 3 takes the decisions `on` [L*D][T][B][H]
+    (values stay double, see rnn_ref.h)."""
     lens = _lens(lens, T, B)
     x = _c(x, (T, B, I))
     w = _c(w, (weight_count(cell, L, I, H, D),))
@@ -114,15 +157,17 @@ def fwd(cell, L, T, B, I, H, x, w, h0=None, c0=None, lens=None, D=1):
     y = np.zeros((T, B, D * H))
     hT = np.zeros((L * D, B, H))
     cT = np.zeros((L * D, B, H)) if cell == 0 else None
-    rc = _load().rnn_ref_fwd_dir(cell, L, D, T, B, I, H, _ip(lens), _p(x), _p(h0), _p(c0), _p(w), _p(y), _p(hT),
-                                 _p(cT))
+    onb = _on(on, cell, L, T, B, H, D, decide)
+    rc = _load().rnn_ref_fwd_kp(cell, L, D, T, B, I, H, _ip(lens), int(decide), _u8(onb), None, _p(x), _p(h0),
+                                _p(c0), _p(w), _p(y), _p(hT), _p(cT))
     if rc != 0:
         raise ValueError(f"rnn_ref_fwd rejected its arguments ({rc})")
     return y, hT, cT
 
 
-def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None, lens=None, D=1):
-    """Backward pass. Returns (dx[T][B][I], dh0[L*D][B][H], dc0 or None, dw like w)."""
+def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None, lens=None, D=1, decide=0, on=None):
+    """Backward pass. Returns (dx[T][B][I], dh0[L*D][B][H], dc0 or None, dw like w).
+    decide: as for fwd."""
     lens = _lens(lens, T, B)
     x = _c(x, (T, B, I))
     w = _c(w, (weight_count(cell, L, I, H, D),))
@@ -135,8 +180,9 @@ def bwd(cell, L, T, B, I, H, x, w, dy, h0=None, c0=None, dhT=None, dcT=None, len
     dh0 = np.zeros((L * D, B, H))
     dc0 = np.zeros((L * D, B, H)) if cell == 0 else None
     dw = np.zeros_like(w)
-    rc = _load().rnn_ref_bwd_dir(cell, L, D, T, B, I, H, _ip(lens), _p(x), _p(h0), _p(c0), _p(w), _p(dy), _p(dhT),
-                                 _p(dcT), _p(dx), _p(dh0), _p(dc0), _p(dw))
+    onb = _on(on, cell, L, T, B, H, D, decide)
+    rc = _load().rnn_ref_bwd_kp(cell, L, D, T, B, I, H, _ip(lens), int(decide), _u8(onb), _p(x), _p(h0), _p(c0),
+                                _p(w), _p(dy), _p(dhT), _p(dcT), _p(dx), _p(dh0), _p(dc0), _p(dw))
     if rc != 0:
         raise ValueError(f"rnn_ref_bwd rejected its arguments ({rc})")
     return dx, dh0, dc0, dw

@@ -28,10 +28,20 @@
 //   L = sum(y*dy) + sum(hT*dhT) + sum(cT*dcT)
 // taken in reverse time, top layer first, one step and one layer at a time
 // (no reordering beyond the definition).
+// ReLU decisions in a given precision (the *_kp entry points): the on/off
+// decision a > 0 of the ReLU cell is a comparison of a floating-point value,
+// and a device that stores h in bf16 or fp32 can take it differently from
+// double arithmetic where a is close to 0.  With decide = 1 (bf16) or 2 (fp32)
+// the decisions come from a first forward pass whose h is rounded to that
+// type after every step (round to nearest even, as the device stores it);
+// with decide = 3 they are given by the caller.  Every value, forward and
+// backward, is then computed in double with those decisions imposed (h = a
+// where on, 0 where off; slope 1 where on).
 #include "rnn_ref.h"
 
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <vector>
 #ifdef _OPENMP
@@ -83,11 +93,27 @@ struct Record {
   std::vector<double> cs;     // (T+1) x B x H (LSTM)
   std::vector<double> gates;  // T x B x G*H   activated gate values
   std::vector<double> hn;     // T x B x H     GRU: W_hn h_prev + b_hn
+  std::vector<unsigned char> on;  // T x B x H ReLU: the on/off decision of each unit
   double* h(int t1, int b) { return &hs[((size_t)t1 * B + b) * H]; }
   double* c(int t1, int b) { return &cs[((size_t)t1 * B + b) * H]; }
   double* g(int t, int b) { return &gates[((size_t)t * B + b) * G * H]; }
   double* n(int t, int b) { return &hn[((size_t)t * B + b) * H]; }
+  unsigned char* o(int t, int b) { return &on[((size_t)t * B + b) * H]; }
 };
+
+// v rounded as the device stores it: 1 = bf16 (via float, then to nearest
+// even on the upper 16 bits of the float), 2 = float; 0 = unchanged.
+double store_round(double v, int prec) {
+  if (prec == 0) return v;
+  float f = (float)v;
+  if (prec == 1) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) != 0x7F800000u) u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+    std::memcpy(&f, &u, 4);
+  }
+  return (double)f;
+}
 
 bool bad_args(int cell, int L, int D, int T, int B, int I, int H, const double* x, const double* w) {
   return cell < 0 || cell > 3 || L < 1 || D < 1 || D > 2 || T < 0 || B < 0 || I < 1 || H < 1 ||
@@ -98,9 +124,15 @@ bool bad_args(int cell, int L, int D, int T, int B, int I, int H, const double* 
 // layer outputs out[l] = [T][B][D*H] (zero where a sequence has ended).
 // lens (nullable = all T): sequence b runs times 0 .. lens[b]-1; at its other
 // steps its state is carried unchanged (so slot T holds its final state).
+// round_h: h stored rounded (store_round) after every step; relu_in (nullable):
+// ReLU decisions to impose, one vector per (layer, direction), T x B x H.
+// preact (nullable): ReLU pre-activations [L*D][T][B][H] by step.
 void forward(int cell, int L, int D, int T, int B, int I, int H, const double* x, const double* h0,
              const double* c0, const std::vector<LayerW>& W, std::vector<Record>& rec,
-             std::vector<std::vector<double>>& out, const int* lens) {
+             std::vector<std::vector<double>>& out, const int* lens, int round_h = 0,
+             const std::vector<std::vector<unsigned char>>* relu_in = nullptr,
+             std::vector<double>* preact = nullptr) {
+  if (preact) preact->assign((size_t)L * D * T * B * H, 0.0);
   const int G = gates_of(cell);
   const int GH = G * H, DH = D * H;
   rec.assign((size_t)L * D, Record());
@@ -115,6 +147,7 @@ void forward(int cell, int L, int D, int T, int B, int I, int H, const double* x
       R.gates.assign((size_t)T * B * GH, 0.0);
       if (cell == RNN_REF_LSTM) R.cs.assign((size_t)(T + 1) * B * H, 0.0);
       if (cell == RNN_REF_GRU) R.hn.assign((size_t)T * B * H, 0.0);
+      if (cell == RNN_REF_RELU) R.on.assign((size_t)T * B * H, 0);
       if (h0) std::memcpy(R.h(0, 0), h0 + (size_t)v * B * H, sizeof(double) * B * H);
       if (c0 && cell == RNN_REF_LSTM) std::memcpy(R.c(0, 0), c0 + (size_t)v * B * H, sizeof(double) * B * H);
       const LayerW& lw = W[v];
@@ -169,12 +202,17 @@ void forward(int cell, int L, int D, int T, int B, int I, int H, const double* x
               R.n(st, b)[j] = hn;
               gt[j] = r; gt[H + j] = z; gt[2 * H + j] = n;
             } else if (cell == RNN_REF_RELU) {
-              hnew = std::max(0.0, sx[j] + sh[j]);
+              const double a = sx[j] + sh[j];
+              const bool on = relu_in ? (*relu_in)[v][((size_t)st * B + b) * H + j] != 0 : a > 0.0;
+              if (preact) (*preact)[(((size_t)v * T + st) * B + b) * H + j] = a;
+              R.o(st, b)[j] = on ? 1 : 0;
+              hnew = on ? a : 0.0;
               gt[j] = hnew;
             } else {
               hnew = std::tanh(sx[j] + sh[j]);
               gt[j] = hnew;
             }
+            hnew = store_round(hnew, round_h);
             R.h(st + 1, b)[j] = hnew;
             out[l][((size_t)t * B + b) * DH + (size_t)d * H + j] = hnew;
           }
@@ -182,6 +220,45 @@ void forward(int cell, int L, int D, int T, int B, int I, int H, const double* x
       }
     }
   }
+}
+
+// The forward pass with ReLU decisions taken in precision `decide` (see the
+// header comment): a first pass with h rounded after every step records the
+// decisions, a second exact pass imposes them.  Other cells, or decide = 0:
+// one exact pass.
+// on (nullable, [L*D][T][B][H] by time): the decisions given (decide = 3) or
+// taken; preact (nullable, same layout): the ReLU pre-activations of the pass
+// that took them.
+void forward_kp(int cell, int L, int D, int T, int B, int I, int H, const double* x, const double* h0,
+                const double* c0, const std::vector<LayerW>& W, std::vector<Record>& rec,
+                std::vector<std::vector<double>>& out, const int* lens, int decide, unsigned char* on_io,
+                double* preact) {
+  const size_t per = (size_t)T * B * H;
+  auto by_time = [&](int v, int st) { return (size_t)v * per + (size_t)time_of(v % D, T, st) * B * H; };
+  if (cell != RNN_REF_RELU) {
+    forward(cell, L, D, T, B, I, H, x, h0, c0, W, rec, out, lens);
+    return;
+  }
+  std::vector<std::vector<unsigned char>> on(rec.size());
+  if (decide == 3) {
+    on.assign((size_t)L * D, std::vector<unsigned char>(per));
+    for (int v = 0; v < L * D; ++v)
+      for (int st = 0; st < T; ++st)
+        std::memcpy(&on[v][(size_t)st * B * H], on_io + by_time(v, st), (size_t)B * H);
+  } else {
+    std::vector<double> pre;
+    forward(cell, L, D, T, B, I, H, x, h0, c0, W, rec, out, lens, decide, nullptr, preact ? &pre : nullptr);
+    on.resize(rec.size());
+    for (size_t v = 0; v < rec.size(); ++v) on[v] = rec[v].on;
+    for (int v = 0; v < L * D; ++v)
+      for (int st = 0; st < T; ++st) {
+        if (on_io) std::memcpy(on_io + by_time(v, st), &on[v][(size_t)st * B * H], (size_t)B * H);
+        if (preact) std::memcpy(preact + by_time(v, st), &pre[(size_t)v * per + (size_t)st * B * H],
+                                sizeof(double) * B * H);
+      }
+    if (decide == 0) return;  // the decisions are the double ones: this pass is the result
+  }
+  forward(cell, L, D, T, B, I, H, x, h0, c0, W, rec, out, lens, 0, &on);
 }
 
 bool bad_lens(int T, int B, const int* lens) {
@@ -201,15 +278,17 @@ extern "C" int rnn_ref_threads(void) {
 #endif
 }
 
-extern "C" int rnn_ref_fwd_dir(int cell, int L, int D, int T, int B, int I, int H, const int* lens,
-                               const double* x, const double* h0, const double* c0, const double* w, double* y,
-                               double* hT, double* cT) {
-  if (bad_args(cell, L, D, T, B, I, H, x, w) || bad_lens(T, B, lens)) return -1;
+extern "C" int rnn_ref_fwd_kp(int cell, int L, int D, int T, int B, int I, int H, const int* lens, int decide,
+                              unsigned char* on, double* preact, const double* x, const double* h0,
+                              const double* c0, const double* w, double* y, double* hT, double* cT) {
+  if (bad_args(cell, L, D, T, B, I, H, x, w) || bad_lens(T, B, lens) || decide < 0 || decide > 3 ||
+      (decide == 3 && !on))
+    return -1;
   const int G = gates_of(cell);
   std::vector<LayerW> W = split_weights(w, G, L, D, I, H);
   std::vector<Record> rec;
   std::vector<std::vector<double>> out;
-  forward(cell, L, D, T, B, I, H, x, h0, c0, W, rec, out, lens);
+  forward_kp(cell, L, D, T, B, I, H, x, h0, c0, W, rec, out, lens, decide, on, preact);
   if (y && T > 0) std::memcpy(y, out[L - 1].data(), sizeof(double) * (size_t)T * B * D * H);
   for (int v = 0; v < L * D; ++v) {
     if (hT) std::memcpy(hT + (size_t)v * B * H, rec[v].h(T, 0), sizeof(double) * B * H);
@@ -217,6 +296,12 @@ extern "C" int rnn_ref_fwd_dir(int cell, int L, int D, int T, int B, int I, int 
       std::memcpy(cT + (size_t)v * B * H, rec[v].c(T, 0), sizeof(double) * B * H);
   }
   return 0;
+}
+
+extern "C" int rnn_ref_fwd_dir(int cell, int L, int D, int T, int B, int I, int H, const int* lens,
+                               const double* x, const double* h0, const double* c0, const double* w, double* y,
+                               double* hT, double* cT) {
+  return rnn_ref_fwd_kp(cell, L, D, T, B, I, H, lens, 0, nullptr, nullptr, x, h0, c0, w, y, hT, cT);
 }
 
 extern "C" int rnn_ref_fwd_len(int cell, int L, int T, int B, int I, int H, const int* lens, const double* x,
@@ -231,17 +316,19 @@ extern "C" int rnn_ref_fwd(int cell, int L, int T, int B, int I, int H, const do
   return rnn_ref_fwd_dir(cell, L, 1, T, B, I, H, nullptr, x, h0, c0, w, y, hT, cT);
 }
 
-extern "C" int rnn_ref_bwd_dir(int cell, int L, int D, int T, int B, int I, int H, const int* lens,
-                               const double* x, const double* h0, const double* c0, const double* w,
-                               const double* dy, const double* dhT, const double* dcT, double* dx,
-                               double* dh0, double* dc0, double* dw) {
-  if (bad_args(cell, L, D, T, B, I, H, x, w) || (!dy && T * B > 0) || bad_lens(T, B, lens)) return -1;
+extern "C" int rnn_ref_bwd_kp(int cell, int L, int D, int T, int B, int I, int H, const int* lens, int decide,
+                              unsigned char* on, const double* x, const double* h0, const double* c0,
+                              const double* w, const double* dy, const double* dhT, const double* dcT, double* dx,
+                              double* dh0, double* dc0, double* dw) {
+  if (bad_args(cell, L, D, T, B, I, H, x, w) || (!dy && T * B > 0) || bad_lens(T, B, lens) || decide < 0 ||
+      decide > 3 || (decide == 3 && !on))
+    return -1;
   const int G = gates_of(cell);
   const int GH = G * H, DH = D * H;
   std::vector<LayerW> W = split_weights(w, G, L, D, I, H);
   std::vector<Record> rec;
   std::vector<std::vector<double>> out;
-  forward(cell, L, D, T, B, I, H, x, h0, c0, W, rec, out, lens);
+  forward_kp(cell, L, D, T, B, I, H, x, h0, c0, W, rec, out, lens, decide, on, nullptr);
 
   // gradient arriving at each layer's outputs [T][B][D*H] from above (dy for the top layer)
   std::vector<double> dabove(dy, dy + (size_t)T * B * DH);
@@ -321,8 +408,8 @@ extern "C" int rnn_ref_bwd_dir(int cell, int L, int D, int T, int B, int I, int 
               gh[2 * H + j] = dhn;
               dh_new[(size_t)b * H + j] = dh * z;  // direct path h' = ... + z h
             } else if (cell == RNN_REF_RELU) {
-              // d max(0, a)/da = 1 where a > 0 (h > 0), else 0
-              gx[j] = gt[j] > 0.0 ? dh : 0.0;
+              // d max(0, a)/da = 1 where the unit is on (a > 0), else 0
+              gx[j] = R.o(st, b)[j] ? dh : 0.0;
               gh[j] = gx[j];
               dh_new[(size_t)b * H + j] = 0.0;
             } else {
@@ -379,6 +466,13 @@ extern "C" int rnn_ref_bwd_dir(int cell, int L, int D, int T, int B, int I, int 
     }
   }
   return 0;
+}
+
+extern "C" int rnn_ref_bwd_dir(int cell, int L, int D, int T, int B, int I, int H, const int* lens,
+                               const double* x, const double* h0, const double* c0, const double* w,
+                               const double* dy, const double* dhT, const double* dcT, double* dx,
+                               double* dh0, double* dc0, double* dw) {
+  return rnn_ref_bwd_kp(cell, L, D, T, B, I, H, lens, 0, nullptr, x, h0, c0, w, dy, dhT, dcT, dx, dh0, dc0, dw);
 }
 
 extern "C" int rnn_ref_bwd_len(int cell, int L, int T, int B, int I, int H, const int* lens, const double* x,

@@ -67,6 +67,27 @@ int rnn_ref_bwd_dir(int cell, int L, int D, int T, int B, int I, int H, const in
                     const double* dy, const double* dhT, const double* dcT,
                     double* dx, double* dh0, double* dc0, double* dw);
 
+/* The same, with the on/off decisions of the ReLU cell taken in the precision
+ * the device stores h in: decide = 0 (double, as above), 1 (bf16) or 2
+ * (fp32): a first forward pass rounds h to that type after every step and
+ * records each unit's decision a > 0; or decide = 3: the decisions are given
+ * in `on`.  All values are then computed in double with those decisions
+ * imposed (h = a where on, 0 where off, slope 1 where on).
+ *   on:     [L*D][T][B][H] (by time), nullable unless decide = 3; receives the
+ *           decisions taken when decide < 3
+ *   preact: [L*D][T][B][H], nullable (forward only); receives the ReLU
+ *           pre-activations of the pass that took the decisions
+ * Other cells ignore decide, on and preact. */
+int rnn_ref_fwd_kp(int cell, int L, int D, int T, int B, int I, int H, const int* lens, int decide,
+                   unsigned char* on, double* preact,
+                   const double* x, const double* h0, const double* c0, const double* w,
+                   double* y, double* hT, double* cT);
+int rnn_ref_bwd_kp(int cell, int L, int D, int T, int B, int I, int H, const int* lens, int decide,
+                   unsigned char* on,
+                   const double* x, const double* h0, const double* c0, const double* w,
+                   const double* dy, const double* dhT, const double* dcT,
+                   double* dx, double* dh0, double* dc0, double* dw);
+
 #ifdef __cplusplus
 }
 #endif

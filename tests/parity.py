@@ -23,14 +23,24 @@ BF16_MAX_ABS = 3e-2
 BF16_REL_L2 = 2e-2
 
 
-def run_oracle(hi: runner.HostInputs, train=True, lens=None):
+def kernel_decisions(wl):
+    """Precision in which the ReLU cell's on/off decisions are taken on the
+    oracle side: the one the device stores h in (bf16 or fp32).  Where a
+    floating-point value decides a discrete choice, both sides take it in the
+    kernel's precision; every value stays double."""
+    return (1 if wl.mode == synth.MODE_BF16 else 2) if wl.cell == synth.CELL_RELU else 0
+
+
+def run_oracle(hi: runner.HostInputs, train=True, lens=None, decide=None, on=None):
     w = hi.wl
+    decide = kernel_decisions(w) if decide is None else decide
     y, hT, cT = oracle.fwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, h0=hi.h0, c0=hi.c0, lens=lens,
-                           D=w.directions)
+                           D=w.directions, decide=decide, on=on)
     out = dict(y=y, hT=hT, cT=cT)
     if train:
         dx, dh0, dc0, dw = oracle.bwd(w.cell, w.layers, w.T, w.B, w.input, w.hidden, hi.x, hi.w, hi.dy, h0=hi.h0,
-                                      c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT, lens=lens, D=w.directions)
+                                      c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT, lens=lens, D=w.directions, decide=decide,
+                                      on=on)
         out.update(dx=dx, dh0=dh0, dc0=dc0, dw=dw)
     return out
 
@@ -100,3 +110,52 @@ def compare(wl, g, o, keys=None, report=None):
     bad = {k: v for k, v in errs.items() if not (v[1] <= v[2])}
     assert not bad, f"parity failed: {bad}"
     return errs
+
+
+def sub_inputs(hi, layers):
+    """The host inputs of the first `layers` layers of a stack (weights are
+    stored layer by layer, so the first layers' weights are a prefix)."""
+    wl = hi.wl.replace(layers=layers)
+    out = object.__new__(type(hi))
+    out.__dict__.update(hi.__dict__)
+    out.wl = wl
+    out.w = hi.w[:wl.weight_count()]
+    out.h0 = hi.h0[:wl.states]
+    out.c0 = None if hi.c0 is None else hi.c0[:wl.states]
+    out.dhT = None if hi.dhT is None else hi.dhT[:wl.states]
+    out.dcT = None if hi.dcT is None else hi.dcT[:wl.states]
+    return out
+
+
+def device_relu_decisions(wl, hi, g, flags=0, chunk=0, lens=None, cols=None):
+    """The on/off decision of every ReLU unit as the device took it, [L*D][T][B][H]:
+    on where its output h > 0.  Layer l's outputs come from an (l+1)-layer run
+    of the same inputs, which computes the first l+1 layers exactly as the full
+    stack does (same kernels and plan per layer); the top layer's from g.
+    cols: restrict to these batch columns."""
+    L, D, H = wl.layers, wl.directions, wl.hidden
+    on = []
+    for l in range(L):
+        y = g["y"] if l == L - 1 else run_gpu(wl.replace(layers=l + 1), sub_inputs(hi, l + 1), flags=flags,
+                                               chunk=chunk, lens=lens)["y"]
+        if cols is not None:
+            y = y[:, cols]
+        for d in range(D):
+            on.append((y[:, :, d * H:(d + 1) * H] > 0).astype(np.uint8))
+    return np.stack(on)
+
+
+def relu_check(wl, hi, g, on_dev, lens=None):
+    """Parity of a ReLU run with the decisions the device took.  Each decision
+    that differs from the oracle's (taken in the device's storage precision)
+    must sit at a pre-activation within the forward bar of 0 (there the device's
+    own pre-activation may lie on the other side of 0 within the stated
+    tolerance); the outputs and gradients must then match the oracle computed
+    with the device's decisions.  Returns the number of differing decisions."""
+    on_ref, pre = oracle.relu_decisions(wl.layers, wl.T, wl.B, wl.input, wl.hidden, hi.x, hi.w, h0=hi.h0,
+                                        lens=lens, D=wl.directions, decide=kernel_decisions(wl))
+    diff = on_dev != on_ref
+    far = np.abs(pre[diff]) > (BF16_MAX_ABS if wl.mode == synth.MODE_BF16 else 1e-4)
+    assert not far.any(), f"{int(far.sum())} decisions differ away from the kink: |a| up to {np.abs(pre[diff]).max()}"
+    compare(wl, g, run_oracle(hi, lens=lens, decide=3, on=on_dev))
+    return int(diff.sum())

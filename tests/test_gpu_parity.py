@@ -8,7 +8,7 @@ import pytest
 
 from recurrent_neural_network_gb300 import rnn, runner, synth
 
-from parity import compare, run_gpu, run_oracle
+from parity import compare, device_relu_decisions, relu_check, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -22,7 +22,7 @@ TINY = {
 def tiny(cell, mode, **kw):
     L, T, B, I, H = TINY[mode]
     base = dict(name="tiny", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
-                forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0)
+                forget_bias=1.0, state_std=0.3)
     base.update(kw)
     return synth.Workload(**base)
 
@@ -139,7 +139,25 @@ def test_workload_gru_8layer_sampled_columns():
 
 
 def test_workload_relu_4layer_sampled_columns():
-    masked_columns_check(synth.WORKLOADS[5], [3, 250])
+    """4-layer ReLU RNN, H=2048, B=256, T=100, ordinary weights.  Over 100 steps
+    and 4 layers a few on/off decisions are taken at pre-activations within
+    rounding of 0, and each one reroutes gradient paths through time, so the
+    gradients are checked with the decisions the device took (every one that
+    differs from the oracle's bf16-precision decision must lie within the
+    forward bar of 0)."""
+    wl = synth.WORKLOADS[5]
+    cols = [3, 250]
+    hi = runner.HostInputs(wl)
+    mask = np.zeros(wl.B, bool)
+    mask[cols] = True
+    hi.dy[:, ~mask] = 0
+    g = run_gpu(wl, hi)
+    sub = hi.columns(cols)
+    gs = dict(y=g["y"][:, cols], hT=g["hT"][:, cols], cT=None, dx=g["dx"][:, cols], dh0=g["dh0"][:, cols], dc0=None,
+              dw=g["dw"])
+    on = device_relu_decisions(wl, hi, g, cols=cols)
+    relu_check(sub.wl, sub, gs, on)
+    assert not np.any(g["dx"][:, ~mask])
 
 
 def test_workload_bidirectional_lstm_sampled_columns():
@@ -173,8 +191,7 @@ def persist_cluster_of(r):
 @pytest.mark.parametrize("case", PERSIST_CASES, ids=lambda c: "c%d_L%d_T%d_B%d_I%d_H%d" % c)
 def test_persistent_recurrence_training(case, handoff):
     cell, L, T, B, I, H = case
-    wl = synth.Workload("persist", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3,
-                        kink_margin=0.75 if cell == 3 else 0.0)
+    wl = synth.Workload("persist", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3)
     hi = runner.HostInputs(wl, with_state_grads=True)
     fl = rnn.FLAG_FORCE_PERSISTENT | handoff
     r = runner.Runner(wl, flags=fl)
@@ -187,8 +204,7 @@ def test_persistent_recurrence_training(case, handoff):
 @pytest.mark.parametrize("cell,H,B", [(0, 1024, 4), (1, 512, 8), (2, 2048, 3), (3, 256, 1)])
 def test_persistent_handoff_variants_bit_identical(cell, H, B):
     """Both hand-offs feed the same bf16 h_{t-1} to the same arithmetic."""
-    wl = synth.Workload("hand", cell, 1, 40, B, 64, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3,
-                        kink_margin=0.75 if cell == 3 else 0.0)
+    wl = synth.Workload("hand", cell, 1, 40, B, 64, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3)
     hi = runner.HostInputs(wl, with_state_grads=True)
     assert persist_cluster_of(runner.Runner(wl, flags=rnn.FLAG_FORCE_PERSISTENT)) in (2, 4, 8)
     a = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_PERSISTENT)
@@ -290,7 +306,7 @@ def test_transposed_steps(case):
     columns) against the oracle, every output and gradient."""
     cell, L, T, B, I, H = case
     wl = synth.Workload(name="transposed", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=synth.MODE_BF16,
-                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0)
+                        forget_bias=1.0, state_std=0.3)
     hi = runner.HostInputs(wl, with_state_grads=True)
     g = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING, chunk=2)
     compare(wl, g, run_oracle(hi))
@@ -337,19 +353,25 @@ def test_fused_pointwise_equals_separate_kernel(B):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("flags", [rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_TRANSPOSED, rnn.FLAG_FORCE_TRANSPOSED],
-                         ids=["row_major", "transposed"])
-def test_relu_forward_with_unshaped_weights(flags):
-    """ReLU RNN with the ordinary weight distribution (pre-activations
-    crossing 0 everywhere): the forward outputs still agree within the bf16
-    bound; gradients are compared only on margin-shaped inputs, where the
-    on/off decision cannot flip between precisions."""
-    wl = synth.Workload(name="relu", cell=3, layers=2, T=6, B=33, input=72, hidden=256, mode=synth.MODE_BF16,
+@pytest.mark.parametrize("flags,B", [(rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_TRANSPOSED, 33),
+                                     (rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING, 33),
+                                     (rnn.FLAG_FORCE_PERSISTENT, 4),
+                                     (rnn.FLAG_FORCE_PERSISTENT | rnn.FLAG_NO_PERSIST_CLUSTER, 4)],
+                         ids=["row_major", "transposed", "persistent", "persistent_counter"])
+def test_relu_training_with_ordinary_weights(flags, B):
+    """ReLU RNN with the ordinary weight distribution (pre-activations cross 0
+    everywhere): every output and gradient against the oracle, which takes each
+    unit's on/off decision as a device storing h in bf16 does (the values stay
+    double), and against the oracle run with the decisions the device took."""
+    wl = synth.Workload(name="relu", cell=3, layers=2, T=6, B=B, input=72, hidden=256, mode=synth.MODE_BF16,
                         state_std=0.3)
-    hi = runner.HostInputs(wl)
-    g = run_gpu(wl, hi, flags=flags, train=False)
-    compare(wl, g, run_oracle(hi, train=False))
-
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    g = run_gpu(wl, hi, flags=flags)
+    # with the oracle deciding in bf16 precision the gradients agree as they are
+    compare(wl, g, run_oracle(hi))
+    # and exactly so with the device's own decisions, which differ from the
+    # oracle's only at pre-activations within the forward bar of 0
+    relu_check(wl, hi, g, device_relu_decisions(wl, hi, g, flags=flags))
 
 
 # ---------------------------------------------------------------- variable lengths
@@ -384,7 +406,7 @@ def test_variable_lengths(case):
     same handle (direct call, then the captured graph)."""
     cell, mode, flags, (L, T, B, I, H) = case
     wl = synth.Workload(name="varlen", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
-                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0)
+                        forget_bias=1.0, state_std=0.3)
     hi = runner.HostInputs(wl, with_state_grads=True)
     lens = _lengths(T, B, seed=B + T + cell)
     g = run_gpu(wl, hi, flags=flags, chunk=2, lens=lens, repeat=2)
@@ -421,7 +443,7 @@ def test_bidirectional(case):
     captured graph)."""
     cell, mode, flags, (L, T, B, I, H) = case
     wl = synth.Workload(name="bidir", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
-                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0, directions=2)
+                        forget_bias=1.0, state_std=0.3, directions=2)
     hi = runner.HostInputs(wl, with_state_grads=True)
     g = run_gpu(wl, hi, flags=flags, repeat=2)
     compare(wl, g, run_oracle(hi))
@@ -460,7 +482,7 @@ def test_bidirectional_variable_lengths(case):
     through the same handle."""
     cell, mode, flags, (L, T, B, I, H) = case
     wl = synth.Workload(name="bivar", cell=cell, layers=L, T=T, B=B, input=I, hidden=H, mode=mode,
-                        forget_bias=1.0, state_std=0.3, kink_margin=0.75 if cell == 3 else 0.0, directions=2)
+                        forget_bias=1.0, state_std=0.3, directions=2)
     hi = runner.HostInputs(wl, with_state_grads=True)
     lens = _lengths(T, B, seed=3 * B + T + cell)
     g = run_gpu(wl, hi, flags=flags, lens=lens, repeat=2)
@@ -489,7 +511,7 @@ def test_bidirectional_persistent_recurrence(case, handoff):
     the oracle with both hand-offs."""
     cell, L, T, B, I, H = case
     wl = synth.Workload("pbidir", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3,
-                        kink_margin=0.75 if cell == 3 else 0.0, directions=2)
+                        directions=2)
     hi = runner.HostInputs(wl, with_state_grads=True)
     fl = rnn.FLAG_FORCE_PERSISTENT | handoff
     assert "recurrence=persistent" in runner.Runner(wl, flags=fl).r.describe()

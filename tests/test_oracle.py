@@ -583,3 +583,91 @@ def test_bidirectional_central_finite_differences(cell):
         scale = max(np.abs(num).max(), 1e-3)
         err = np.abs(num - grad.reshape(-1)).max() / scale
         assert err < 1e-7, (name, err)
+
+
+# ---------------------------------------------------------------- ReLU decisions in the device's precision
+
+def test_relu_decisions_in_storage_precision_by_hand():
+    """One unit, two steps, x chosen so that h_1 = 1 + 2^-10 and the second
+    pre-activation a_2 = h_1 - (1 + 2^-11) = +2^-11 is on in double, while a
+    device storing h_1 in bf16 (spacing 2^-7 at 1, so h_1 -> 1) sees
+    a_2 = -2^-11 and switches the unit off.  fp32 holds 1 + 2^-10 exactly.
+    Values stay double: h_1 is 1 + 2^-10 in every mode."""
+    w = np.array([1.0, 1.0, 0.0, 0.0])  # W_x, W_h, b_x, b_h of a 1x1 ReLU cell
+    x = np.array([1.0 + 2.0 ** -10, -(1.0 + 2.0 ** -11)]).reshape(2, 1, 1)
+    dy = np.array([0.5, 2.0]).reshape(2, 1, 1)
+    for decide, h2 in ((0, 2.0 ** -11), (2, 2.0 ** -11), (1, 0.0)):
+        y, hT, _ = oracle.fwd(3, 1, 2, 1, 1, 1, x, w, decide=decide)
+        assert y[0, 0, 0] == 1.0 + 2.0 ** -10 and y[1, 0, 0] == h2, (decide, y.ravel())
+        dx, dh0, _, dw = oracle.bwd(3, 1, 2, 1, 1, 1, x, w, dy, decide=decide)
+        on2 = h2 > 0
+        # dL/da_2 = dy_2 if on; dL/da_1 = dy_1 + W_h dL/da_2 (unit 1 is on)
+        da2 = 2.0 if on2 else 0.0
+        da1 = 0.5 + da2
+        np.testing.assert_allclose(dx.ravel(), [da1, da2], rtol=0, atol=0)
+        np.testing.assert_allclose(dw, [da1 * x[0, 0, 0] + da2 * x[1, 0, 0], da2 * y[0, 0, 0], da1 + da2, da1 + da2],
+                                   rtol=1e-15)
+
+
+@pytest.mark.parametrize("cell", CELLS)
+def test_decisions_in_storage_precision_leave_clear_cases_unchanged(cell):
+    """Away from the kink (margin-shaped ReLU inputs) and for the other cells the
+    kernel-precision decisions are the double ones, so every output and
+    gradient is bit-identical to the plain definition."""
+    wl = synth.Workload("dec", cell, 2, 5, 3, 6, 8, synth.MODE_BF16, forget_bias=1.0, state_std=0.3,
+                        kink_margin=0.75 if cell == 3 else 0.0)
+    from recurrent_neural_network_gb300 import runner
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    ref = oracle.bwd(cell, 2, 5, 3, 6, 8, hi.x, hi.w, hi.dy, h0=hi.h0, c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT)
+    for decide in (1, 2):
+        got = oracle.bwd(cell, 2, 5, 3, 6, 8, hi.x, hi.w, hi.dy, h0=hi.h0, c0=hi.c0, dhT=hi.dhT, dcT=hi.dcT,
+                         decide=decide)
+        for a, b in zip(got, ref):
+            if a is not None:
+                np.testing.assert_array_equal(a, b)
+    with pytest.raises(ValueError):
+        oracle.fwd(cell, 1, 2, 1, 1, 1, np.zeros((2, 1, 1)), np.zeros(oracle.weight_count(cell, 1, 1, 1)), decide=4)
+
+
+def test_relu_decisions_in_storage_precision_with_ordinary_weights():
+    """With ordinary weights a few bf16 decisions differ from the double ones
+    (units whose pre-activation lies within bf16 rounding of 0): the forward
+    outputs stay close (the function is continuous) and only a small share of
+    the decisions changes."""
+    wl = synth.Workload("dec", 3, 1, 20, 6, 16, 64, synth.MODE_BF16, state_std=0.3)
+    from recurrent_neural_network_gb300 import runner
+    hi = runner.HostInputs(wl)
+    y0, _, _ = oracle.fwd(3, 1, 20, 6, 16, 64, hi.x, hi.w, h0=hi.h0)
+    y1, _, _ = oracle.fwd(3, 1, 20, 6, 16, 64, hi.x, hi.w, h0=hi.h0, decide=1)
+    assert np.abs(y0 - y1).max() < 1e-2
+    on0, on1 = y0 > 0, (y1 > 0) | (y1 < 0)  # imposed "on" may carry a pre-activation just below 0
+    changed = int((on0 != on1).sum())
+    assert 0 < changed < on0.size // 100, changed
+
+
+def test_relu_given_decisions_reproduce_the_taken_ones():
+    """Decisions taken in bf16 precision and handed back (decide = 3) give the
+    same outputs and gradients bit for bit; the pre-activations returned are
+    consistent with them (on exactly where the bf16-pass pre-activation > 0,
+    and h = max(0, a) when decided in double)."""
+    wl = synth.Workload("dec", 3, 2, 7, 4, 16, 32, synth.MODE_BF16, state_std=0.3)
+    from recurrent_neural_network_gb300 import runner
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    args = (3, 2, 7, 4, 16, 32, hi.x, hi.w)
+    on, pre = oracle.relu_decisions(2, 7, 4, 16, 32, hi.x, hi.w, h0=hi.h0, decide=1)
+    np.testing.assert_array_equal(on, (pre > 0).astype(np.uint8))
+    a = oracle.bwd(*args, hi.dy, h0=hi.h0, dhT=hi.dhT, decide=1)
+    b = oracle.bwd(*args, hi.dy, h0=hi.h0, dhT=hi.dhT, decide=3, on=on)
+    for u, v in zip(a, b):
+        if u is not None:
+            np.testing.assert_array_equal(u, v)
+    on0, pre0 = oracle.relu_decisions(2, 7, 4, 16, 32, hi.x, hi.w, h0=hi.h0, decide=0)
+    y0, _, _ = oracle.fwd(*args, h0=hi.h0)
+    np.testing.assert_array_equal(y0, np.maximum(pre0[1], 0.0))   # top layer output from its pre-activations
+    # a decision flipped by hand changes exactly that unit's output at that step
+    on2 = on0.copy()
+    t, bq, j = np.argwhere(on0[1] == 1)[0]
+    on2[1, t, bq, j] = 0
+    y2, _, _ = oracle.fwd(*args, h0=hi.h0, decide=3, on=on2)
+    assert y2[t, bq, j] == 0.0 and y0[t, bq, j] > 0
+    np.testing.assert_array_equal(y2[:t], y0[:t])
