@@ -165,9 +165,9 @@ def class_bytes(wl, transposed, fused_point=False):
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one
 # ncu capture of the same kernel build on `bench.py --ncu-steps` (one layer,
 # T=2, the same per-step shape; transposed steps, BPTT pointwise fused into the
-# product); summarised in profiles/ncu_step_kernels_lstm_B256_H4096.md.
-NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.36e6,
-               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.64e6}
+# product): the first launch of each class.
+NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.13e6,
+               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.46e6}
 
 
 def oracle_sample(wl, B1, T1):
@@ -563,19 +563,20 @@ def synth_tensor(wl, what, dev, dtype):
 
 
 def ncu_steps(args):
-    """A short program for ncu: two timesteps of one layer of the configured
-    workload (forward, BPTT, weight gradients), run twice, no timing."""
+    """A short program for ncu: --ncu-T timesteps (default 2) of one layer of
+    the configured workload (forward, BPTT, weight gradients; the forward of an
+    inference workload), run twice, no timing."""
     from recurrent_neural_network_gb300 import build, runner, synth
     build.build()
     dev = torch.device("cuda", 0)
-    wl = synth.WORKLOADS[args.config].replace(layers=1, T=2)
+    wl = synth.WORKLOADS[args.config].replace(layers=1, T=args.ncu_T)
     R = runner.Runner(wl, device=dev, flags=args.flags, chunk=args.chunk)
     R.x = synth_tensor(wl, "x", dev, R.dt)
     R.w_user = synth_tensor(wl, "w", dev, R.dt)
     R.h0 = synth_tensor(wl, "h0", dev, R.dt)
     if wl.cell == synth.CELL_LSTM:
         R.c0 = synth_tensor(wl, "c0", dev, torch.float32)
-    R.dy = synth_tensor(wl, "dy", dev, R.dt)
+    R.dy = synth_tensor(wl, "dy", dev, R.dt) if wl.training else None
     R.pack()
     for _ in range(2):
         R.step()
@@ -598,6 +599,7 @@ def main():
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--sweep", action="store_true",
                     help="selector sweep over batch sizes and widths instead of the benchmark line")
+    ap.add_argument("--ncu-T", type=int, default=2, help="timesteps of the --ncu-steps program")
     ap.add_argument("--ncu-steps", action="store_true",
                     help="one training pass (forward, BPTT, weight gradients) of a one-layer T=2 copy of the "
                          "workload, for profiler captures: every recurrent-step launch has the full per-step shape")
