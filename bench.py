@@ -454,19 +454,27 @@ def workload_probe(idx, dev, pk, steps=10, warmup=3):
     R = make_runner(wl, dev)
     for _ in range(warmup):
         R.step()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        R.step()
-    e1.record()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record()
+        R.forward()
+        ev[i][1].record()
+        if wl.training:
+            R.backward()
+        ev[i][2].record()
+        if wl.training:
+            R.weights()
+        ev[i][3].record()
     torch.cuda.synchronize()
     assert R.status() == 0
-    ms = e0.elapsed_time(e1) / steps
+    ms = ev[0][0].elapsed_time(ev[-1][3]) / steps
+    phases = {nm: statistics.mean(e[k].elapsed_time(e[k + 1]) for e in ev)
+              for k, nm in enumerate(["fwd", "bwd_data", "bwd_weights"])}
     plan = R.r.describe()
     persistent = "recurrence=persistent" in plan
     out = {"ms_per_step": ms, "tflops": step_flops(wl) / (ms * 1e-3) / 1e12,
            "timesteps_per_s": wl.T / (ms * 1e-3), "us_per_timestep": 1e3 * ms / wl.T,
-           "training": wl.training, "dtype": "bf16" if wl.mode == 1 else "f32", "plan": plan,
+           "training": wl.training, "dtype": "bf16" if wl.mode == 1 else "f32", "plan": plan, "phases_ms": phases,
            "roofline": workload_roofline(wl, ms, pk, persistent)}
     del R
     torch.cuda.empty_cache()
@@ -512,49 +520,50 @@ def fp8_stash_probe(dev, pk, steps=5, warmup=2):
     return out
 
 
-def sweep(dev, steps=5, warmup=2):
-    """Selector sweep: one-layer bf16 LSTM and tanh-RNN training steps (T=16)
-    over a grid of batch sizes and widths, timed with the library's own plan
-    and with each recurrent-step orientation forced, one JSON line per shape.
-    Used to place the planner's switch between the two orientations."""
-    from recurrent_neural_network_gb300 import rnn, runner, synth
-    variants = [("default", 0), ("transposed", rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING),
+def sweep(dev, steps=5, warmup=2, cells=(0, 1), batches=(1, 2, 4, 8, 16, 32, 64, 128, 256, 512),
+          widths=(256, 512, 1024, 2048, 4096, 8192)):
+    """Selector sweep: one-layer bf16 training steps (T=16) over batch sizes
+    and widths, timed with the library's own plan and with each recurrence
+    variant forced (persistent, streaming transposed, streaming row-major),
+    one JSON line per shape.  Places the planner's switches (persistent vs
+    streaming, step orientation) and shows how throughput moves with the
+    batch at each width."""
+    from recurrent_neural_network_gb300 import rnn, synth
+    variants = [("default", 0), ("persistent", rnn.FLAG_FORCE_PERSISTENT),
+                ("transposed", rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING),
                 ("row_major", rnn.FLAG_NO_TRANSPOSED | rnn.FLAG_FORCE_STREAMING)]
-    for cell, H, B in [(c, h, b) for c in (0, 2) for h in (512, 1024, 2048, 4096) for b in (16, 32, 64, 128, 256)]:
-        if True:
-            wl = synth.Workload(name=f"sweep_c{cell}_B{B}_H{H}", cell=cell, layers=1, T=16, B=B, input=H, hidden=H,
-                                mode=synth.MODE_BF16, forget_bias=1.0, state_std=0.1)
-            res, plan = {}, None
-            for name, fl in variants:
-                try:
-                    R = runner.Runner(wl, device=dev, flags=fl)
-                except rnn.RnnError:
-                    continue
-                if name == "default":
-                    plan = R.r.describe()
-                R.x = synth_tensor(wl, "x", dev, R.dt)
-                R.w_user = synth_tensor(wl, "w", dev, R.dt)
-                R.h0 = synth_tensor(wl, "h0", dev, R.dt)
-                R.c0 = synth_tensor(wl, "c0", dev, torch.float32) if cell == 0 else None
-                R.dy = synth_tensor(wl, "dy", dev, R.dt)
-                R.pack()
-                for _ in range(warmup):
-                    R.step()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                for _ in range(steps):
-                    R.step()
-                e1.record()
-                torch.cuda.synchronize()
-                assert R.status() == 0
-                res[name] = e0.elapsed_time(e1) / steps
-                del R
-                torch.cuda.empty_cache()
-            fl = step_flops(wl)
-            print(json.dumps({"sweep": {"cell": ["lstm", "gru", "tanh"][cell], "L": 1, "T": 16, "B": B, "H": H},
-                              "ms": {k: round(v, 4) for k, v in res.items()},
-                              "tflops": {k: round(fl / (v * 1e-3) / 1e12, 1) for k, v in res.items()},
-                              "plan": plan}), flush=True)
+    for cell in cells:
+        for H in widths:
+            for B in batches:
+                wl = synth.Workload(name=f"sweep_c{cell}_B{B}_H{H}", cell=cell, layers=1, T=16, B=B, input=H,
+                                    hidden=H, mode=synth.MODE_BF16, forget_bias=1.0, state_std=0.1)
+                res, plan = {}, None
+                for name, fl in variants:
+                    try:
+                        R = make_runner(wl, dev, flags=fl)
+                    except rnn.RnnError:
+                        continue
+                    if name == "default":
+                        plan = R.r.describe()
+                    for _ in range(warmup):
+                        R.step()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for _ in range(steps):
+                        R.step()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    assert R.status() == 0
+                    res[name] = e0.elapsed_time(e1) / steps
+                    del R
+                    torch.cuda.empty_cache()
+                fl = step_flops(wl)
+                forced = {k: v for k, v in res.items() if k != "default"}
+                best = min(forced, key=forced.get) if forced else None
+                print(json.dumps({"sweep": {"cell": synth.CELL_NAMES[cell], "L": 1, "T": 16, "B": B, "H": H},
+                                  "ms": {k: round(v, 4) for k, v in res.items()},
+                                  "tflops": {k: round(fl / (v * 1e-3) / 1e12, 2) for k, v in res.items()},
+                                  "best_forced": best, "plan": plan}), flush=True)
 
 
 def synth_tensor(wl, what, dev, dtype):

@@ -101,7 +101,7 @@ enum {
 #define RNN_FLAG_FORCE_TRANSPOSED 0x400u /* take the recurrent steps as W_h h^T (bf16 LSTM / simple RNN,
                                             B <= 256, H % 32 == 0) or fail; by default chosen where it
                                             measured faster (LSTM: H >= 2048, or H >= 1024 and B >= 64,
-                                            or H >= 512 and 64 <= B <= 128; simple RNN: H >= 2048) */
+                                            or H >= 256 and 64 <= B <= 128; simple RNN: H >= 2048) */
 #define RNN_FLAG_NO_FUSED_POINT 0x800u  /* transposed LSTM steps: run the pointwise BPTT step as its own
                                            kernel after each product instead of inside its epilogue */
 #define RNN_FLAG_NO_PERSIST_CLUSTER 0x1000u /* persistent recurrence: hand h_t over through per-step
@@ -211,8 +211,10 @@ RNN_API int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const
                     int accumulate, void* ws, cudaStream_t stream);
 
 /* Synchronizes `stream`, then reads and clears the device error word in the
- * workspace: RNN_OK, or RNN_ERR_TIMEOUT if a bounded device wait gave up in
- * any call since the last check. */
+ * workspace: RNN_OK, RNN_ERR_TIMEOUT if a bounded device wait gave up in any
+ * call since the last check, or RNN_ERR_LAUNCH if the persistent recurrence
+ * found itself launched in clusters of another size than planned (it then
+ * computes nothing). */
 RNN_API int rnn_sync_status(rnn_handle_t h, void* ws, cudaStream_t stream);
 
 RNN_API const char* rnn_strerror(int code);

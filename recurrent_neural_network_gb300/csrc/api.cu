@@ -258,13 +258,14 @@ int plan_and_layout(rnn_s* h) {
 
   // Transposed recurrent steps: with at most 256 batch entries, W_h h^T puts
   // the batch on the tile columns and keeps the epilogue's accesses
-  // contiguous.  Where it wins was measured over batch and width (one-layer
-  // training steps): LSTM from H = 2048 at every batch size, from H = 1024 at
-  // B >= 64 and at H = 512 for 64 <= B <= 128; tanh RNN from H = 2048.
+  // contiguous.  Where it wins was measured over batch (1..512) and width
+  // (256..8192) on one-layer training steps: LSTM from H = 2048 at every batch
+  // size, from H = 1024 at B >= 64 and from H = 256 for 64 <= B <= 128; tanh
+  // RNN from H = 2048.
   if (d.mode == RNN_MODE_BF16 && !h->persist && d.cell != RNN_GRU && B <= 256 &&
       H % 32 == 0 && !(d.flags & RNN_FLAG_NO_TRANSPOSED)) {
     const bool lstm_wins = d.cell == RNN_LSTM && (H >= 2048 || (H >= 1024 && B >= 64) ||
-                                                   (H >= 512 && B >= 64 && B <= 128));
+                                                   (H >= 256 && B >= 64 && B <= 128));
     const bool tanh_wins = (d.cell == RNN_TANH || d.cell == RNN_RELU) && H >= 2048;
     if (lstm_wins || tanh_wins || (d.flags & RNN_FLAG_FORCE_TRANSPOSED)) h->tstep = 1;
   }
@@ -1498,7 +1499,7 @@ int rnn_sync_status(rnn_handle_t h, void* ws, cudaStream_t stream) {
   if (cudaMemcpy(&word, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return RNN_ERR_CUDA;
   if (word != 0) {
     if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return RNN_ERR_CUDA;
-    return RNN_ERR_TIMEOUT;
+    return word == 3 /* DEV_BAD_CLUSTER (common.cuh) */ ? RNN_ERR_LAUNCH : RNN_ERR_TIMEOUT;
   }
   return RNN_OK;
 }

@@ -22,7 +22,7 @@ template <>
 struct CellInfo<RELU> { static constexpr int G = 1; };
 
 // Device error word codes (written into the first word of the workspace).
-enum DevErr { DEV_OK = 0, DEV_TIMEOUT_PIPE = 1, DEV_TIMEOUT_STEP = 2 };
+enum DevErr { DEV_OK = 0, DEV_TIMEOUT_PIPE = 1, DEV_TIMEOUT_STEP = 2, DEV_BAD_CLUSTER = 3 };
 
 // ---------------------------------------------------------------- storage types
 __device__ __forceinline__ float to_f32(float v) { return v; }

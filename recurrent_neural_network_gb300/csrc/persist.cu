@@ -37,6 +37,10 @@
 // product as f16 MMAs against h (bf16 converted to f16) and applies the row
 // scales to the fp32 sums.
 //
+// The cluster variant first checks that its launch has the cluster size the
+// arguments name (it addresses every peer's shared memory); otherwise every
+// CTA records DEV_BAD_CLUSTER and returns.
+//
 // Every wait is bounded (globaltimer); on timeout the CTA records
 // DEV_TIMEOUT_STEP in the error word and leaves (in the cluster variant the
 // whole cluster leaves together, after the step's cluster barrier).
@@ -212,6 +216,15 @@ __global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a)
   int w0 = 0, nmine = 0;
   uint32_t offw[kMaxWords];
   if constexpr (XCL) {
+    // the exchange addresses the shared memory of every CTA of the cluster:
+    // a launch whose cluster is not the size the arguments promise leaves at
+    // once (every CTA alike, before any peer access or cluster barrier)
+    uint32_t ncta;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
+    if ((int)ncta != a.cluster || a.cluster < 2) {
+      if (threadIdx.x == 0) raise_error(a.err, DEV_BAD_CLUSTER);
+      return;
+    }
     crank = tc::cluster_ctarank();
     csize = (uint32_t)a.cluster;
     const int per = NW / (int)csize;

@@ -141,6 +141,8 @@ def test_transposed_step_plan(lib):
     assert "transposed=0" in rnn.RNN(1, 4, 50, 256, 4096, 4096, 1).describe()   # GRU keeps h W_h^T
     assert "transposed=1" in rnn.RNN(0, 2, 10, 64, 512, 512, 1).describe()      # measured faster there
     assert "transposed=0" in rnn.RNN(0, 2, 10, 256, 512, 512, 1).describe()     # ... but not at B=256
+    assert "transposed=1" in rnn.RNN(0, 2, 10, 128, 256, 256, 1).describe()     # from H=256 at 64 <= B <= 128
+    assert "transposed=0" in rnn.RNN(0, 2, 10, 32, 256, 256, 1).describe()
     assert "transposed=0" in rnn.RNN(0, 2, 10, 32, 1024, 1024, 1).describe()    # nor at H=1024, B<64
     assert "transposed=1" in rnn.RNN(0, 2, 10, 32, 2048, 2048, 1).describe()
     assert "transposed=1" in rnn.RNN(2, 2, 10, 16, 2048, 2048, 1).describe()    # tanh from H=2048
