@@ -107,6 +107,11 @@ enum {
 #define RNN_FLAG_NO_PERSIST_CLUSTER 0x1000u /* persistent recurrence: hand h_t over through per-step
                                                arrival counters and L2 reads instead of tagged words
                                                gathered per thread-block cluster */
+#define RNN_FLAG_PERSIST_CLUSTER_SYNC 0x8000u /* persistent recurrence, cluster hand-off: end each step with a
+                                                barrier across the cluster after the gathered h_{t-1} is scattered
+                                                to every CTA; by default the scatter uses asynchronous stores whose
+                                                bytes each CTA counts on its own mbarrier, with no cluster-wide
+                                                barrier per step */
 #define RNN_FLAG_BIDIRECTIONAL 0x2000u /* every layer gets a second direction that runs time backwards
                                           with its own weights (see the layouts below) */
 #define RNN_FLAG_FP8_STASH 0x4000u /* bf16 inference: the persistent recurrence keeps W_h on chip as e4m3

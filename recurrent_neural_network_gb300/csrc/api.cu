@@ -597,6 +597,7 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
         PersistArgs pa{};
         pa.arrive = arrive;
         pa.cluster = pa_cluster(h, p8);
+        pa.cluster_sync = (d.flags & RNN_FLAG_PERSIST_CLUSTER_SYNC) ? 1 : 0;
         pa.Wh8 = p8 ? reinterpret_cast<const uint8_t*>(PW + h->pl[v].wh8) : nullptr;
         pa.wscale = p8 ? reinterpret_cast<const float*>(PW + h->pl[v].wsc) : nullptr;
         pa.hx = reinterpret_cast<uint64_t*>(W + h->ws_hx);
@@ -1188,6 +1189,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
             PersistArgs pa{};
             pa.arrive = arrive;
             pa.cluster = p8 ? h->persist8_cl : h->persist_cl;
+            pa.cluster_sync = (d.flags & RNN_FLAG_PERSIST_CLUSTER_SYNC) ? 1 : 0;
             pa.Wh8 = p8 ? reinterpret_cast<const uint8_t*>(PW + h->pl[l].wh8) : nullptr;
             pa.wscale = p8 ? reinterpret_cast<const float*>(PW + h->pl[l].wsc) : nullptr;
             pa.hx = reinterpret_cast<uint64_t*>(W + h->ws_hx);

@@ -161,6 +161,8 @@ struct PersistArgs {
   __nv_bfloat16* hseq;      // [T+1][B][H]; slot 0 = h0
   unsigned int* arrive;     // [T] arrival counters, zero before the launch
   int cluster;              // > 0: cluster-exchange hand-off with clusters of this size
+  int cluster_sync;         // cluster exchange ended by a barrier across the cluster each step
+                            // (0: each CTA waits on its own mbarrier for asynchronous stores)
   uint64_t* hx;             // cluster exchange: [2][B*H/2] tagged words, zero before the launch
   __nv_bfloat16* y;         // [T][B][H] or null
   __nv_bfloat16* hT;        // [B][H] or null

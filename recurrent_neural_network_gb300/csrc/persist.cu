@@ -111,6 +111,13 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
 __device__ __forceinline__ void st_dsmem_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
+// Asynchronous 4-byte store into the shared memory of a CTA of the cluster
+// whose completion is counted (4 transaction bytes) on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(cluster_addr),
+               "r"(v), "r"(cluster_bar)
+               : "memory");
+}
 // every thread of every CTA of the cluster (threads may arrive diverged)
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
@@ -124,9 +131,14 @@ __device__ __forceinline__ unsigned short bf16_bits(float v) {
 // that B*H/2 words over the cluster's CTAs' threads stay within it)
 constexpr int kMaxWords = 4;
 
-// NT threads (8 or 16 warps, each taking KT 16-deep k-tiles of W_h's K range)
-template <int CELL, int MT, int KT, bool XCL, bool W8, int NT>
+// NT threads (8 or 16 warps, each taking KT 16-deep k-tiles of W_h's K range).
+// HO: hand-off of h_t.  0 counters; 1 tagged words gathered per cluster, then a
+// cluster barrier; 2 tagged words gathered per cluster with asynchronous
+// stores into every peer, each CTA waiting on its own mbarrier for the bytes
+// of its copy of h_{t-1} (no barrier across the cluster per step).
+template <int CELL, int MT, int KT, int HO, bool W8, int NT>
 __global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a) {
+  constexpr bool XCL = HO > 0;
   constexpr int G = CellInfo<CELL>::G;
   constexpr int ROWS = MT * 16;  // = G * uc
   constexpr int NWARP = NT / 32;
@@ -135,6 +147,7 @@ __global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a)
   __shared__ float rscale[W8 ? ROWS : 1];  // fp8 stash: row scale x 2^8
   __shared__ int abort_flag;
   __shared__ int abort_x[2];  // cluster exchange: set in every CTA of the cluster by one that gave up
+  __shared__ __align__(8) uint64_t hbar[2];  // HO = 2: bytes of h_{t-1} landed in buffer t & 1
   // dynamic shared memory: fp8 stash of this CTA's W_h rows (ROWS x H bytes
   // in fragment order), then for the cluster exchange the h_{t-1} ping-pong
   // [2][B][H + 8] bf16 (rows padded so that the eight batch rows of a
@@ -244,7 +257,12 @@ __global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a)
       hw[b * HP2 + (i - b * (H / 2))] = h0w[i];
     }
     if (threadIdx.x < 2) abort_x[threadIdx.x] = 0;
-    // peers write into this CTA's buffers and flags only after this point
+    if (HO == 2 && threadIdx.x == 0) {
+      tc::mbar_init(&hbar[0], 1);
+      tc::mbar_init(&hbar[1], 1);
+      tc::fence_mbar_init();
+    }
+    // peers write into this CTA's buffers, barriers and flags only after this point
     cluster_barrier();
   }
   __syncthreads();
@@ -270,6 +288,10 @@ __global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a)
       const uint64_t* src = a.hx + (size_t)((t - 1) & 1) * NW;
       const uint32_t want = (uint32_t)t;
       const uint32_t hbase = tc::smem_addr(hbuf) + (uint32_t)((t & 1) * B * HP2 * 4);
+      const uint32_t bar_local = tc::smem_addr(&hbar[t & 1]);
+      // HO = 2: this CTA's buffer receives one 4-byte store per word from the
+      // cluster's pollers (remote completions may come before this arrival)
+      if (HO == 2 && threadIdx.x == 0) tc::mbar_arrive_expect_tx(&hbar[t & 1], (uint32_t)NW * 4u);
       // every round loads all of this thread's missing words at once, so a
       // word that is already there costs no extra round trip
       uint32_t pending = (1u << nmine) - 1u;
@@ -285,7 +307,12 @@ __global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a)
           if (((pending >> i) & 1u) && (uint32_t)(v[i] >> 32) == want) {
             pending &= ~(1u << i);
             const uint32_t off = hbase + offw[i];
-            for (uint32_t r = 0; r < csize; ++r) st_dsmem_u32(tc::mapa(off, r), (uint32_t)v[i]);
+            if constexpr (HO == 2) {
+              for (uint32_t r = 0; r < csize; ++r)
+                st_async_u32(tc::mapa(off, r), (uint32_t)v[i], tc::mapa(bar_local, r));
+            } else {
+              for (uint32_t r = 0; r < csize; ++r) st_dsmem_u32(tc::mapa(off, r), (uint32_t)v[i]);
+            }
           }
         }
         if (!pending) break;
@@ -301,8 +328,32 @@ __global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a)
         const uint32_t fo = tc::smem_addr(&abort_x[t & 1]);
         for (uint32_t r = 0; r < csize; ++r) st_dsmem_u32(tc::mapa(fo, r), 1u);
       }
-      cluster_barrier();
-      if (*reinterpret_cast<volatile int*>(&abort_x[t & 1])) break;
+      if constexpr (HO == 2) {
+        // this CTA's copy of h_{t-1} is complete once all its bytes landed
+        // (bounded; a peer that gave up marks abort_x here, and this CTA leaves)
+        const uint32_t par = (uint32_t)((t - 1) >> 1) & 1u;
+        bool ok = tc::mbar_try_wait_cluster(&hbar[t & 1], par);
+        if (!ok) {
+          const uint64_t w0t = globaltimer_ns();
+          while (!(ok = tc::mbar_try_wait_cluster(&hbar[t & 1], par))) {
+            if (*reinterpret_cast<volatile int*>(&abort_x[t & 1])) break;
+            if (globaltimer_ns() - w0t > a.limit_ns) {
+              raise_error(a.err, DEV_TIMEOUT_STEP);
+              break;
+            }
+          }
+        }
+        if (!ok || bad) {
+          // stop every CTA of the cluster at its next wait
+          const uint32_t fo = tc::smem_addr(&abort_x[t & 1]);
+          for (uint32_t r = 0; r < csize; ++r) st_dsmem_u32(tc::mapa(fo, r), 1u);
+        }
+        __syncthreads();
+        if (*reinterpret_cast<volatile int*>(&abort_x[t & 1])) break;
+      } else {
+        cluster_barrier();
+        if (*reinterpret_cast<volatile int*>(&abort_x[t & 1])) break;
+      }
     }
     if (!XCL && t > 0) {
       if (threadIdx.x == 0) {
@@ -447,12 +498,15 @@ __global__ void __launch_bounds__(NT, 1) persist_fwd_kernel(const PersistArgs a)
       if (threadIdx.x == 0 && !(a.test_skip_publish && blockIdx.x == 0 && t == 0)) red_release_add(a.arrive + t, 1u);
     }
   }
+  // HO = 2: no CTA leaves while a peer may still store into its shared memory
+  // (after an abort the peers leave their loops at different steps)
+  if constexpr (HO == 2) cluster_barrier();
 }
 
 template <int CELL, int MT, int KT, bool W8, int NT>
 int launch_one(const Launch& L, const PersistArgs& a, int ctas, bool query_only, int num_sms, int* cl_out) {
-  auto kc = persist_fwd_kernel<CELL, MT, KT, false, W8, NT>;
-  auto kx = persist_fwd_kernel<CELL, MT, KT, true, W8, NT>;
+  auto kc = persist_fwd_kernel<CELL, MT, KT, 0, W8, NT>;
+  auto kx = a.cluster_sync ? persist_fwd_kernel<CELL, MT, KT, 1, W8, NT> : persist_fwd_kernel<CELL, MT, KT, 2, W8, NT>;
   const size_t dyn_w = W8 ? (size_t)MT * 16 * a.H : 0;               // fp8 stash of the CTA's rows
   const size_t dyn = dyn_w + (size_t)2 * a.B * (a.H + 8) * 2;  // + h_{t-1} ping-pong of the cluster variant
   if (dyn_w && cudaFuncSetAttribute(kc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_w) != cudaSuccess) {

@@ -180,14 +180,15 @@ PERSIST_CASES = [
 
 
 # hand-off variants: tagged words gathered per cluster (default), arrival counters
-HANDOFF = [0, rnn.FLAG_NO_PERSIST_CLUSTER]
+HANDOFF = [0, rnn.FLAG_PERSIST_CLUSTER_SYNC, rnn.FLAG_NO_PERSIST_CLUSTER]
+HANDOFF_IDS = ["cluster_async", "cluster_sync", "counter"]
 
 
 def persist_cluster_of(r):
     return int(r.r.describe().split("persist_cluster=")[1].split()[0])
 
 
-@pytest.mark.parametrize("handoff", HANDOFF, ids=["cluster", "counter"])
+@pytest.mark.parametrize("handoff", HANDOFF, ids=HANDOFF_IDS)
 @pytest.mark.parametrize("case", PERSIST_CASES, ids=lambda c: "c%d_L%d_T%d_B%d_I%d_H%d" % c)
 def test_persistent_recurrence_training(case, handoff):
     cell, L, T, B, I, H = case
@@ -197,21 +198,22 @@ def test_persistent_recurrence_training(case, handoff):
     r = runner.Runner(wl, flags=fl)
     assert "recurrence=persistent" in r.r.describe()
     # the cluster hand-off is taken where its words fit the pollers (else counters)
-    assert (persist_cluster_of(r) in (0, 2, 4, 8)) if handoff == 0 else persist_cluster_of(r) == 0
+    assert (persist_cluster_of(r) == 0) if handoff == rnn.FLAG_NO_PERSIST_CLUSTER else persist_cluster_of(r) in (0, 2, 4, 8)
     compare(wl, run_gpu(wl, hi, flags=fl), run_oracle(hi))
 
 
 @pytest.mark.parametrize("cell,H,B", [(0, 1024, 4), (1, 512, 8), (2, 2048, 3), (3, 256, 1)])
 def test_persistent_handoff_variants_bit_identical(cell, H, B):
-    """Both hand-offs feed the same bf16 h_{t-1} to the same arithmetic."""
+    """Every hand-off feeds the same bf16 h_{t-1} to the same arithmetic."""
     wl = synth.Workload("hand", cell, 1, 40, B, 64, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3)
     hi = runner.HostInputs(wl, with_state_grads=True)
     assert persist_cluster_of(runner.Runner(wl, flags=rnn.FLAG_FORCE_PERSISTENT)) in (2, 4, 8)
     a = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_PERSISTENT)
-    b = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_PERSISTENT | rnn.FLAG_NO_PERSIST_CLUSTER)
-    for k in a:
-        if a[k] is not None:
-            assert np.array_equal(a[k], b[k]), k
+    for other in (rnn.FLAG_PERSIST_CLUSTER_SYNC, rnn.FLAG_NO_PERSIST_CLUSTER):
+        b = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_PERSISTENT | other)
+        for k in a:
+            if a[k] is not None:
+                assert np.array_equal(a[k], b[k]), (other, k)
 
 
 def test_persistent_equals_streaming_within_tolerance():
@@ -223,7 +225,7 @@ def test_persistent_equals_streaming_within_tolerance():
         assert float(np.abs(p[k] - s[k]).max()) <= 3e-2, k
 
 
-@pytest.mark.parametrize("handoff", HANDOFF, ids=["cluster", "counter"])
+@pytest.mark.parametrize("handoff", HANDOFF, ids=HANDOFF_IDS)
 def test_persistent_bounded_wait_reports_timeout(handoff):
     """One CTA never publishes its first step: the others' waits give up after
     the handle's bound and the error word says so; the context stays usable."""
@@ -503,7 +505,7 @@ PERSIST_BIDIR = [
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("handoff", HANDOFF, ids=["cluster", "counter"])
+@pytest.mark.parametrize("handoff", HANDOFF, ids=HANDOFF_IDS)
 @pytest.mark.parametrize("case", PERSIST_BIDIR, ids=lambda c: "c%d_L%d_T%d_B%d_I%d_H%d" % c)
 def test_bidirectional_persistent_recurrence(case, handoff):
     """Small-batch bidirectional stacks on the persistent recurrence (one launch
