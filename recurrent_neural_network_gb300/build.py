@@ -19,7 +19,9 @@ OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "librnn.so")
 UNITS = ["api.cu", "gemm.cu", "step_fwd.cu", "step_bwd.cu", "persist.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
+# a variable read before it is set (diagnostic 549) fails the build instead of warning
+FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+         "--diag-error", "549"]
 
 
 def nvcc() -> str:

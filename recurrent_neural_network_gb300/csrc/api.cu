@@ -1134,9 +1134,9 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
     // layer after layer (no wavefront)
     const bool p8 = !train && h->persist8 && !h->varlen;
     const bool pers = p8 || h->persist;
-    const int wf = p8 ? 0 : wf;
-    const int nch = p8 ? 1 : nch;
-    const int chunk = p8 ? T : chunk;
+    const int wf = p8 ? 0 : h->wavefront;
+    const int nch = p8 ? 1 : h->nch;
+    const int chunk = p8 ? T : h->chunk;
 
     if (h->varlen) {
       // rows past a sequence's end are never written by the steps: y reads 0

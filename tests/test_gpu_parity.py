@@ -111,6 +111,19 @@ def test_workload_lstm_b4_inference():
     compare(wl, run_gpu(wl, hi), run_oracle(hi, train=False))
 
 
+@pytest.mark.parametrize("flags", [rnn.FLAG_FORCE_STREAMING | rnn.FLAG_FORCE_TRANSPOSED,
+                                   rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_TRANSPOSED],
+                         ids=["transposed", "row_major"])
+def test_workload_lstm_b4_inference_streaming(flags):
+    """The same 1000-step inference on streaming step launches (graph replay on
+    the third call), against the oracle."""
+    wl = synth.WORKLOADS[2]
+    hi = runner.HostInputs(wl)
+    o = run_oracle(hi, train=False)
+    for repeat in (1, 3):
+        compare(wl, run_gpu(wl, hi, flags=flags, repeat=repeat), o)
+
+
 def masked_columns_check(wl, cols):
     """Full-size run with dy zero outside `cols`; forward outputs, data
     gradients and weight gradients of those columns against the oracle run on
