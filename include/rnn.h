@@ -121,7 +121,14 @@ enum {
                                       approximation (3 mantissa bits per weight): the forward then computes
                                       with W_h' = e4m3(W_h / s) * s.  Training calls (with a reserve) keep the
                                       bf16 path.  rnn_get_sizes includes the stash in the packed size. */
-#define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrence one CTA never
+#define RNN_FLAG_NO_STACK 0x10000u /* bf16, one direction, 9..64 sequences: run the forward recurrence as
+                                      step launches (with the layer wavefront) instead of the persistent
+                                      stacked recurrence (up to 4 layers per launch, each layer's
+                                      [W_x | W_h] rows resident in shared memory, layer l+1 starting step t
+                                      as soon as layer l has finished it) */
+#define RNN_FLAG_FORCE_STACK 0x20000u /* use the persistent stacked forward recurrence (also for B <= 8, in
+                                         place of the single-layer persistent recurrence) or fail */
+#define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrences one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */
 

@@ -137,6 +137,11 @@ struct rnn_s {
   int persist_cl = 0;                 // persistent hand-off: cluster size of the tagged-word exchange, 0 = counters
   int persist8 = 0, persist8_cl = 0;  // fp8 stash (RNN_FLAG_FP8_STASH): persistent inference on e4m3 W_h
   int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
+  // persistent stacked forward (9..64 sequences): groups of up to
+  // kStackMaxLayers layers, each group one launch; stack_plan is the plan's
+  // choice, stack what the current lengths allow (variable lengths: off)
+  int stack = 0, stack_plan = 0;
+  std::vector<std::pair<int, int>> stack_groups;  // (first layer, layers)
   int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
   // variable lengths (rnn_set_lengths): Bt[t] = number of sequences still
   // running at step t (the batch is sorted by non-increasing length, so the
@@ -218,7 +223,7 @@ int plan_and_layout(rnn_s* h) {
   // persistent recurrence for small batches (weights on-chip, one launch per
   // layer); it runs layer after layer, so it replaces the wavefront.
   // (bidirectional stacks: one launch per direction, the reverse one walking time backwards)
-  if (d.mode == RNN_MODE_BF16 && !(d.flags & RNN_FLAG_FORCE_STREAMING)) {
+  if (d.mode == RNN_MODE_BF16 && !(d.flags & (RNN_FLAG_FORCE_STREAMING | RNN_FLAG_FORCE_STACK))) {
     int ctas = 0;
     int cl = 4;  // without a device: the size that co-resides on GB300 for 128 CTAs
     const bool fits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &ctas, &cl) == RNN_OK
@@ -307,6 +312,32 @@ int plan_and_layout(rnn_s* h) {
     h->ctr_count = 1;
   }
 
+  // persistent stacked forward for moderate batches: the layers in groups of
+  // up to kStackMaxLayers that fit on the device together
+  if (d.mode == RNN_MODE_BF16 && h->D == 1 && !h->persist && B <= 64 &&
+      !(d.flags & (RNN_FLAG_NO_STACK | RNN_FLAG_FORCE_STREAMING)) &&
+      (B > 8 || (d.flags & RNN_FLAG_FORCE_STACK))) {
+    const int sms = h->have_device ? h->num_sms : 0;
+    auto fits = [&](int l0, int nl) {
+      int ctas = 0;
+      return stack_check(d.cell, H, B, nl, l0 == 0 ? 1 : 0, h->u, sms, &ctas) == RNN_OK;
+    };
+    std::vector<std::pair<int, int>> groups;
+    bool ok = true;
+    for (int l0 = 0; l0 < L && ok;) {
+      int nl = 0;
+      while (l0 + nl < L && nl < kStackMaxLayers && fits(l0, nl + 1)) ++nl;
+      if (nl == 0) ok = false;
+      else groups.emplace_back(l0, nl);
+      l0 += nl;
+    }
+    if (ok) {
+      h->stack = h->stack_plan = 1;
+      h->stack_groups = groups;
+    }
+  }
+  if ((d.flags & RNN_FLAG_FORCE_STACK) && !h->stack) return RNN_ERR_UNSUPPORTED;
+
   const size_t e = h->elem;
   const size_t BH = (size_t)B * H, BGH = (size_t)B * GH;
   // per (layer, direction) v = l * D + d; In of layer l = v / D
@@ -349,7 +380,7 @@ int plan_and_layout(rnn_s* h) {
   h->wl.resize(V);
   cur = 0;
   h->ws_err = take(cur, 256);
-  h->ws_arrive = take(cur, (size_t)T * 4);
+  h->ws_arrive = take(cur, (size_t)kStackMaxLayers * T * 4);  // per-timestep counters (stack: per layer)
   h->ws_hx = (h->persist_plan || h->persist8) ? take(cur, (size_t)8 * B * H) : 0;
   h->bias_slices = std::max(1, std::min(64, (T * B + 255) / 256));
   h->ws_bias = take(cur, (size_t)h->bias_slices * GH * 4);
@@ -529,6 +560,69 @@ int cu(cudaError_t e) { return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA; }
 
 // hand-off cluster size of the persistent recurrence (0: counters), bf16 or fp8-stash plan
 int pa_cluster(const rnn_s* h, bool p8) { return p8 ? h->persist8_cl : h->persist_cl; }
+
+// Forward pass with the persistent stacked recurrence: layer 0's input
+// projection for all timesteps as one GEMM, then one launch per layer group.
+int fwd_stack(rnn_s* h, const void* x, const void* h0, const float* c0, const char* PW, void* y, void* hT, float* cT,
+              char* R, char* W, void* ws, cudaStream_t stream) {
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = h->d.hidden, GH = h->GH;
+  const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
+  const bool train = R != nullptr;
+  const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+  auto hseq_of = [&](int l) { return train ? R + h->rl[l].hseq : W + h->wl[l].hseq; };
+  float* P0 = reinterpret_cast<float*>(train ? R + h->rl[0].gates : W + h->wl[0].P);
+  {
+    Operand A{x, d.input, 0, T * B, d.input};
+    Operand Bw{PW + h->pl[0].wx, d.input, 0, GH, d.input, 1};
+    Remap none{0, 1, 1, 1};
+    Launch Lk = mk(h, stream, ws, "input_proj_gemm");
+    RNN_TRY(gemm_f32(Lk, d.mode, A, Bw, T * B, GH, d.input, P0, GH, reinterpret_cast<const float*>(PW + h->pl[0].bias),
+                     0, none, 0));
+  }
+  unsigned int* cnt = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
+  for (const auto& grp : h->stack_groups) {
+    const int l0 = grp.first, nl = grp.second;
+    StackArgs sa{};
+    sa.T = T;
+    sa.B = B;
+    sa.H = H;
+    sa.u_pack = h->u;
+    sa.nl = nl;
+    for (int i = 0; i < nl; ++i) {
+      const int l = l0 + i;
+      char* hs = hseq_of(l);
+      if (h0) RNN_TRY(cu(cudaMemcpyAsync(hs, static_cast<const char*>(h0) + l * BH * e, BH * e,
+                                         cudaMemcpyDeviceToDevice, stream)));
+      else RNN_TRY(cu(cudaMemsetAsync(hs, 0, BH * e, stream)));
+      StackLayer& ly = sa.lay[i];
+      ly.Wx = l > 0 ? reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wx) : nullptr;
+      ly.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
+      ly.P = l == 0 ? P0 : nullptr;
+      ly.bias = reinterpret_cast<const float*>(PW + h->pl[l].bias);
+      ly.bias_hn = reinterpret_cast<const float*>(PW + h->pl[l].bias_hn);
+      ly.c0 = (lstm && c0) ? c0 + l * BH : nullptr;
+      ly.gates_out = train ? reinterpret_cast<float*>(R + h->rl[l].gates) : nullptr;
+      ly.c_out = (train && lstm) ? reinterpret_cast<float*>(R + h->rl[l].c) : nullptr;
+      ly.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) : nullptr;
+      ly.hseq = reinterpret_cast<__nv_bfloat16*>(hs);
+      ly.in = l > 0 ? reinterpret_cast<const __nv_bfloat16*>(hseq_of(l - 1)) : nullptr;
+      ly.y = l == L - 1 ? static_cast<__nv_bfloat16*>(y) : nullptr;
+      ly.hT = hT ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(hT) + (size_t)l * BH * e) : nullptr;
+      ly.cT = (cT && lstm) ? cT + (size_t)l * BH : nullptr;
+      ly.In = l > 0 ? H : d.input;
+      ly.wait_in = i > 0 ? 1 : 0;
+    }
+    RNN_TRY(cu(cudaMemsetAsync(cnt, 0, (size_t)nl * T * 4, stream)));
+    sa.cnt = cnt;
+    sa.err = reinterpret_cast<int*>(W + h->ws_err);
+    sa.limit_ns = h->limit_ns;
+    sa.test_skip_publish = (d.flags & RNN_FLAG_TEST_SKIP_PUBLISH) ? 1 : 0;
+    Launch Lk = mk(h, stream, ws, "stack_fwd");
+    RNN_TRY(stack_fwd(Lk, d.cell, sa));
+  }
+  return RNN_OK;
+}
 
 // slot of h at time t in direction d (t = -1 forward, t = T reverse: the initial state)
 size_t hslot(int d, int t) { return (size_t)(t + 1 - d); }
@@ -1060,6 +1154,7 @@ int rnn_set_lengths(rnn_handle_t h, const int* lens) {
   // the persistent recurrence runs all T steps of every sequence: step
   // launches take over (the packing unit it was planned with serves them)
   h->persist = h->varlen ? 0 : h->persist_plan;
+  h->stack = h->varlen ? 0 : h->stack_plan;
   return RNN_OK;
 }
 
@@ -1076,13 +1171,22 @@ int rnn_get_sizes(rnn_handle_t h, size_t* user_weight_bytes, size_t* packed_weig
 int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   if (!h || !buf || len == 0) return RNN_ERR_INVALID_ARG;
   const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : h->d.cell == RNN_RELU ? "relu" : "tanh";
+  // layer groups of the stacked forward, "first+count" each
+  char groups[128] = "-";
+  if (h->stack) {
+    size_t n = 0;
+    for (size_t i = 0; i < h->stack_groups.size() && n + 16 < sizeof(groups); ++i)
+      n += (size_t)snprintf(groups + n, sizeof(groups) - n, "%s%d+%d", i ? "," : "", h->stack_groups[i].first,
+                            h->stack_groups[i].second);
+  }
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
            "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d transposed=%d fused_point=%d "
-           "persist_cluster=%d directions=%d fp8_stash=%d",
+           "persist_cluster=%d directions=%d fp8_stash=%d stack_groups=%s",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
-           h->persist ? "persistent" : "streaming", h->d.mode ? "tcgen05" : "ffma", h->wavefront, h->chunk, h->nch,
-           h->bwd_bn, h->bwd_splits, h->num_sms, h->tstep, h->bwd_fuse, h->persist ? h->persist_cl : 0, h->D, h->persist8);
+           h->persist ? "persistent" : h->stack ? "stacked" : "streaming", h->d.mode ? "tcgen05" : "ffma",
+           h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->num_sms, h->tstep, h->bwd_fuse,
+           h->persist ? h->persist_cl : 0, h->D, h->persist8, groups);
   return RNN_OK;
 }
 
@@ -1133,6 +1237,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
     // inference with the fp8 stash: the persistent recurrence on e4m3 W_h,
     // layer after layer (no wavefront)
     const bool p8 = !train && h->persist8 && !h->varlen;
+    if (!p8 && h->stack && !h->varlen) return fwd_stack(h, x, h0, c0, PW, y, hT, cT, R, W, ws, stream);
     const bool pers = p8 || h->persist;
     const int wf = p8 ? 0 : h->wavefront;
     const int nch = p8 ? 1 : h->nch;

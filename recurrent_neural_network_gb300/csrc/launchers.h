@@ -182,4 +182,51 @@ int persist_check(int cell, int H, int B, int num_sms, int* ctas, int* cluster =
 // all T timesteps of one layer in one cooperative launch (bf16 storage only)
 int persist_fwd(const Launch& L, int cell, const PersistArgs& a);
 
+// ---------------------------------------------------------------- stack.cu
+// Persistent forward recurrence of up to kStackMaxLayers stacked layers in one
+// launch (bf16, one direction, 1..64 sequences): each layer's CTAs hold
+// blocks of its packed [W_x | W_h] rows on chip, layer l works on step t as
+// soon as layer l-1 has finished it (per-layer, per-step arrival counters).
+constexpr int kStackMaxLayers = 4;
+struct StackLayer {
+  const __nv_bfloat16* Wx;  // packed [G*H][In] (layers without P)
+  const __nv_bfloat16* Wh;  // packed [G*H][H]
+  const float* P;           // [T][B][G*H] input projection incl. bias (the stack's first layer), else null
+  const float* bias;        // packed folded bias [G*H] (layers without P)
+  const float* bias_hn;     // GRU [H]
+  const float* c0;          // LSTM [B][H] or null
+  float* gates_out;         // training: activated gates [T][B][G*H] (may alias P), else null
+  float* c_out;             // training LSTM [T][B][H], else null
+  float* hn_out;            // training GRU [T][B][H], else null
+  __nv_bfloat16* hseq;      // [T+1][B][H]; slot 0 = h0, written before the launch
+  const __nv_bfloat16* in;  // layers without P: the layer below's h sequence [T+1][B][In] (its output at t in slot t+1)
+  __nv_bfloat16* y;         // [T][B][H] or null
+  __nv_bfloat16* hT;        // [B][H] or null
+  float* cT;                // LSTM [B][H] or null
+  int In;                   // input width of a layer without P (must equal H)
+  int wait_in;              // 1: the input is produced by the previous layer of this launch
+};
+struct StackSmem {
+  int a, ring, rbuf, smg, smhn, bars;
+};
+struct StackArgs {
+  int T, B, H, u_pack;
+  int nl;                   // layers in this launch
+  StackLayer lay[kStackMaxLayers];
+  unsigned int* cnt;        // [nl][T] arrival counters, zero before the launch
+  int* err;
+  uint64_t limit_ns;
+  int test_skip_publish;    // test hook: CTA 0 never publishes step 0
+  // geometry (filled by stack_fwd)
+  int kc, cluster;
+  int ks[kStackMaxLayers], kcx[kStackMaxLayers], cta0[kStackMaxLayers + 1], ctas[kStackMaxLayers];
+  StackSmem sm;
+};
+// RNN_OK if nl stacked layers of (cell, H, B) run as one stack launch on the
+// device (first_p: the first of them reads a precomputed input projection;
+// u_pack: the packing unit); *ctas receives the grid size.  num_sms <= 0:
+// host-side planning for GB300 without a device query.
+int stack_check(int cell, int H, int B, int nl, int first_p, int u_pack, int num_sms, int* ctas);
+int stack_fwd(const Launch& L, int cell, const StackArgs& a);
+
 }  // namespace rnn

@@ -33,6 +33,8 @@ FLAG_NO_PERSIST_CLUSTER = 0x1000
 FLAG_BIDIRECTIONAL = 0x2000
 FLAG_FP8_STASH = 0x4000
 FLAG_PERSIST_CLUSTER_SYNC = 0x8000
+FLAG_NO_STACK = 0x10000
+FLAG_FORCE_STACK = 0x20000
 
 # every symbol include/rnn.h declares
 SYMBOLS = ["rnn_create", "rnn_destroy", "rnn_get_sizes", "rnn_pack_weights", "rnn_fwd", "rnn_bwd_data",

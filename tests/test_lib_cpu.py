@@ -85,7 +85,7 @@ def test_persistent_plan_selection(lib):
     # small batch, supported width: persistent, no wavefront
     assert "recurrence=persistent" in rnn.RNN(0, 2, 10, 4, 64, 1024, 1).describe()
     assert "recurrence=streaming" in rnn.RNN(0, 2, 10, 4, 64, 1024, 1, flags=rnn.FLAG_FORCE_STREAMING).describe()
-    assert "recurrence=streaming" in rnn.RNN(0, 2, 10, 64, 64, 1024, 1).describe()
+    assert "recurrence=persistent" not in rnn.RNN(0, 2, 10, 64, 64, 1024, 1).describe()
     with pytest.raises(rnn.RnnError) as e:
         rnn.RNN(0, 1, 10, 64, 64, 1024, 1, flags=rnn.FLAG_FORCE_PERSISTENT)
     assert e.value.code == -2
@@ -95,12 +95,49 @@ def test_persistent_plan_selection(lib):
     for cell, hmax in ((0, 1024), (1, 1024), (2, 2048), (3, 2048)):
         assert "recurrence=persistent" in rnn.RNN(cell, 1, 10, 8, 64, hmax, 1).describe()
         assert "recurrence=streaming" in rnn.RNN(cell, 1, 10, 8, 64, 2 * hmax, 1).describe()
-        assert "recurrence=streaming" in rnn.RNN(cell, 1, 10, 9, 64, hmax, 1).describe()
+        assert "recurrence=persistent" not in rnn.RNN(cell, 1, 10, 9, 64, hmax, 1).describe()
     # the hand-off variant the plan reports: clusters unless turned off
     d = rnn.RNN(0, 1, 10, 4, 64, 1024, 1).describe()
     assert "persist_cluster=0" not in d
     d = rnn.RNN(0, 1, 10, 4, 64, 1024, 1, flags=rnn.FLAG_NO_PERSIST_CLUSTER).describe()
     assert "persist_cluster=0" in d
+
+
+def test_stacked_plan_groups(lib):
+    """Persistent stacked forward (bf16, one direction, 9..64 sequences): the
+    layers run in groups of up to 4 per launch, as many as fit on the SMs
+    (layer 0: 32 units x K chunks of 512 per CTA over its recurrent part;
+    higher layers also over their input part)."""
+    import re
+
+    def plan(*a, **k):
+        d = rnn.RNN(*a, **k).describe()
+        return re.search(r"recurrence=(\w+)", d).group(1), re.search(r"stack_groups=(\S+)", d).group(1)
+    # 4-layer LSTM H=512 B=64: 16 + 3 x 32 CTAs, one launch
+    assert plan(0, 4, 100, 64, 512, 512, 1) == ("stacked", "0+4")
+    # 8-layer GRU H=1024 B=32: layer 0 64 CTAs, the others 128: one layer per launch
+    assert plan(1, 8, 200, 32, 1024, 1024, 1) == ("stacked", "0+1,1+1,2+1,3+1,4+1,5+1,6+1,7+1")
+    # tanh H=1024 B=32: 8 + 16 + 16 + 16 + 16 CTAs -> 4 + 1
+    assert plan(2, 5, 20, 32, 64, 1024, 1) == ("stacked", "0+4,4+1")
+    # B <= 8 keeps the single-layer persistent recurrence unless forced
+    assert plan(0, 2, 10, 4, 64, 1024, 1)[0] == "persistent"
+    assert plan(0, 2, 10, 4, 64, 1024, 1, flags=rnn.FLAG_FORCE_STACK)[0] == "stacked"
+    # off: flag, streaming forced, wider batches, fp32, bidirectional, H not a multiple of 256
+    assert plan(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK)[0] == "streaming"
+    assert plan(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_FORCE_STREAMING)[0] == "streaming"
+    assert plan(0, 4, 100, 65, 512, 512, 1)[0] == "streaming"
+    assert plan(0, 4, 100, 32, 512, 512, 0)[0] == "streaming"
+    assert plan(0, 2, 10, 32, 512, 512, 1, flags=rnn.FLAG_BIDIRECTIONAL)[0] == "streaming"
+    assert plan(0, 2, 10, 32, 64, 320, 1)[0] == "streaming"
+    with pytest.raises(rnn.RnnError):
+        rnn.RNN(0, 2, 10, 32, 64, 320, 1, flags=rnn.FLAG_FORCE_STACK)
+    # variable lengths switch the forward to step launches
+    r = rnn.RNN(0, 2, 10, 16, 64, 512, 1)
+    assert "recurrence=stacked" in r.describe()
+    r.set_lengths([10] * 8 + [5] * 8)
+    assert "recurrence=streaming" in r.describe()
+    r.set_lengths([10] * 16)
+    assert "recurrence=stacked" in r.describe()
 
 
 def test_wavefront_chunking_plan(lib):
