@@ -124,7 +124,7 @@ enum {
 #define RNN_FLAG_NO_STACK 0x10000u /* bf16, one direction, 9..64 sequences: run the forward recurrence as
                                       step launches (with the layer wavefront) instead of the persistent
                                       stacked recurrence (up to 4 layers per launch, each layer's
-                                      [W_x | W_h] rows resident in shared memory, layer l+1 starting step t
+                                      [W_x | W_h] rows resident in tensor memory, layer l+1 starting step t
                                       as soon as layer l has finished it) */
 #define RNN_FLAG_FORCE_STACK 0x20000u /* use the persistent stacked forward recurrence (also for B <= 8, in
                                          place of the single-layer persistent recurrence) or fail */

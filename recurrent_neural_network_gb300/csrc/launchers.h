@@ -207,7 +207,7 @@ struct StackLayer {
   int wait_in;              // 1: the input is produced by the previous layer of this launch
 };
 struct StackSmem {
-  int a, ring, rbuf, smg, smhn, bars;
+  int stages, ring, rbuf, smg, smhn, bars;
 };
 struct StackArgs {
   int T, B, H, u_pack;

@@ -11,8 +11,10 @@
 //  * Every layer of the group owns its CTAs.  A CTA holds one block of 128
 //    packed gate rows (all gates of 32 hidden units; 128 units for the
 //    simple RNNs) times one 512-wide (or 256-wide) chunk of the layer's K =
-//    [input | recurrent] in shared memory for the whole launch, in the
-//    tensor core's 128-byte-swizzled K-major layout.  The first layer of the
+//    [input | recurrent] in tensor memory for the whole launch (row i in
+//    TMEM lane i, the A operand of every MMA): read from shared memory, the
+//    128 KB block cost the tensor core ~270 ns per 64-deep K block whatever
+//    the batch width, from TMEM it costs nothing extra.  The first layer of the
 //    whole stack takes its input projection P = x W_x^T + b from one GEMM
 //    over all timesteps and its K is the recurrent part only; every other
 //    layer computes its input projection step by step from the layer
@@ -22,9 +24,9 @@
 //    reads (the layer below's step t for an input chunk, its own layer's
 //    step t-1 for a recurrent chunk), then one thread streams the batch rows
 //    of that chunk (N = batch rounded up to 16, x 64 k per block) from L2
-//    into a ring of shared-memory stages with TMA, and one thread issues
-//    tcgen05.mma (M = 128 rows, N, K = 16) into a double-buffered TMEM
-//    accumulator.
+//    into a ring of shared-memory stages with TMA (two timesteps deep where
+//    it fits), and one thread issues tcgen05.mma (A from TMEM, M = 128 rows,
+//    N, K = 16) into a double-buffered TMEM accumulator.
 //  * The K chunks of one row block form a thread-block cluster.  Their
 //    partial sums are reduce-scattered over the batch: each CTA sends the
 //    other chunks' batch slices with asynchronous stores into their shared
@@ -69,16 +71,16 @@ namespace {
     if (rc_ != RNN_OK) return rc_; \
   } while (0)
 
-// TMA maps of one launch: packed W_x and W_h rows of each layer (box 64 k x
-// 128 rows) and the h sequences (box 64 k x N batch rows): h[0] the input
-// of the first layer (when it has no P), h[1 + l] layer l's own.
+// TMA maps of one launch over the h sequences, 3-D: (64 k of a block, batch
+// row, k block) with box (64, N, kc / 64), so that one load brings a CTA's
+// whole K chunk of a timestep (a TMA load costs ~150 ns to issue whatever
+// its size, and 8 loads of 4-8 KB each per timestep were the bound): h[0]
+// the input of the first layer (when it has no P), h[1 + l] layer l's own.
 struct StackMaps {
-  CUtensorMap wx[kStackMaxLayers];
-  CUtensorMap wh[kStackMaxLayers];
   CUtensorMap h[kStackMaxLayers + 1];
 };
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;  // input buffers, one timestep's K chunk each
 constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue (one per TMEM lane quadrant)
 
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
@@ -100,15 +102,19 @@ __device__ __forceinline__ void st_dsmem_s32(uint32_t cluster_addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
-// Shared-memory layout of a CTA (offsets from the 1024-aligned base).
+// Shared-memory layout of a CTA (offsets from the 1024-aligned base): the
+// ring of input buffers (kc / 64 blocks of N x 64 bf16 each), the receive
+// buffers of the cross-chunk reduction, the gate tile, barriers.  The
+// weights are in TMEM.
 struct Smem {
-  int a, ring, rbuf, smg, smhn, bars, total;
+  int a, ring, rbuf, smg, smhn, bars, total, stages;
 };
-__host__ __device__ inline Smem smem_layout(int cell, int N, int kc, int ksmin, int ksmax) {
+__host__ __device__ inline Smem smem_layout(int cell, int N, int kc, int ksmin, int ksmax, int stages) {
   Smem s;
   s.a = 0;
-  s.ring = s.a + (kc / 64) * 16384;
-  s.rbuf = s.ring + kStages * N * 128;
+  s.stages = stages;
+  s.ring = 0;
+  s.rbuf = s.ring + stages * (kc / 64) * N * 128;
   // [2][ksmax-1][N/ks/4][128] float4 for the largest ks of the launch (the
   // footprint (ks-1)/ks * N is largest for the largest ks)
   const int rb = ksmax > 1 ? 2 * (ksmax - 1) * (N / ksmax) * 128 * 4 : 0;
@@ -117,7 +123,7 @@ __host__ __device__ inline Smem smem_layout(int cell, int N, int kc, int ksmin, 
   // widest batch slice of the launch (smallest ks)
   s.smhn = s.smg + (N / ksmin) * 128 * 4;
   s.bars = s.smhn + (cell == GRU ? (N / ksmin) * 32 * 4 : 0);
-  s.total = s.bars + 256;
+  s.total = s.bars + 512;
   return s;
 }
 
@@ -128,6 +134,22 @@ struct Ctx {
   volatile int* abort_flag;
   int* ep_fail;
   int li, rb, me, ks, kcx, crank;
+};
+
+// What the loops of one CTA read, copied once out of the launch arguments
+// into registers: the arguments live in parameter space, and a field read
+// there inside a loop that also stores to global memory is read again on
+// every iteration (measured: ~150-270 ns per producer, MMA or epilogue
+// iteration before this copy).
+struct Run {
+  int T, B, H, u_pack, kc, cluster, test_skip_publish;
+  int* err;
+  uint64_t limit_ns;
+  unsigned int* cnt;        // [layers][T] counters of the launch
+  unsigned int want_h;      // CTAs of this CTA's layer
+  unsigned int want_x;      // CTAs of the layer below (when it runs in this launch)
+  StackSmem sm;
+  StackLayer ly;            // this CTA's layer
 };
 
 // Raise the abort flag in every CTA of the cluster (this one included).
@@ -141,7 +163,7 @@ __device__ __forceinline__ void abort_cluster(const Ctx& c, int cluster) {
 
 // Wait until *cnt >= want (bounded; gives up at once when the CTA aborts).
 __device__ __forceinline__ bool wait_count(const unsigned int* cnt, unsigned int want, const Ctx& c,
-                                           const StackArgs& a) {
+                                           const Run& a) {
   if (ld_acquire_u32(cnt) >= want) return true;
   const uint64_t t0 = globaltimer_ns();
   while (ld_acquire_u32(cnt) < want) {
@@ -160,14 +182,14 @@ __device__ __forceinline__ bool wait_count(const unsigned int* cnt, unsigned int
 // CTA's block; KS chunks per row block, this CTA's batch slice is
 // [me*NS, me*NS + NS)
 template <int CELL, int N, int KS>
-__device__ void epilogue(const StackArgs& a, const Ctx& c, int row, int e) {
+__device__ void epilogue(const Run& a, const Ctx& c, int row, int e, uint32_t acc_base) {
   constexpr int G = CellInfo<CELL>::G;
   constexpr bool SIMPLE = G == 1;
   constexpr int UC = SIMPLE ? 128 : 32;
   constexpr int ROWS = G * UC;
   constexpr int NS = N / KS;
   constexpr int PP = SIMPLE ? 1 : (UC * NS + 127) / 128;  // (unit, batch) pairs per thread
-  const StackLayer& ly = a.lay[c.li];
+  const StackLayer& ly = a.ly;
   const int T = a.T, B = a.B, H = a.H, GH = G * H, u = a.u_pack;
   const int me = c.me, kcx = c.kcx;
   const int j0 = c.rb * UC, r0 = j0 * G;
@@ -179,10 +201,19 @@ __device__ void epilogue(const StackArgs& a, const Ctx& c, int row, int e) {
   const int rj = (row / (G * u)) * u + row % u;
   const float bias = (live_row && !ly.P) ? ly.bias[r0 + row] : 0.f;
   const float bias_hn = (CELL == GRU && live_row && rg == 2) ? ly.bias_hn[j0 + rj] : 0.f;
+  // gate activation of this row as ga * tanh(ga * x) + gc: sigmoid (input,
+  // forget, output, reset, update) or tanh (LSTM cell candidate)
+  const bool is_tanh = CELL == LSTM && rg == 2;
+  const float ga = is_tanh ? 1.f : 0.5f, gc = is_tanh ? 0.f : 0.5f;
+  float* const gout = ly.gates_out;
+  // rows of the G gates of unit j0 + lane in the gate tile (cell update)
+  const int o0 = packed_row(0, lane, G, u), o1 = packed_row(G > 1 ? 1 : 0, lane, G, u);
+  const int o2 = packed_row(G > 2 ? 2 : 0, lane, G, u), o3 = packed_row(G > 3 ? 3 : 0, lane, G, u);
   float* smg = reinterpret_cast<float*>(c.smem + a.sm.smg);
   float* smhn = reinterpret_cast<float*>(c.smem + a.sm.smhn);
   float4* rbuf = reinterpret_cast<float4*>(c.smem + a.sm.rbuf);
   constexpr int NC4 = NS / 4;  // float4 chunks of a slice
+  constexpr bool SPLIT = CELL == GRU;  // input and recurrent sums apart (GRU candidate gate)
   constexpr int ACC = N < 32 ? 32 : N;  // TMEM columns between the two accumulators
   // receive buffer of parity p from the peer in slot s: [p][s][chunk][row]
   auto rb_at = [&](int p, int s, int ch) -> float4* { return rbuf + ((p * (KS - 1) + s) * NC4 + ch) * 128; };
@@ -208,7 +239,6 @@ __device__ void epilogue(const StackArgs& a, const Ctx& c, int row, int e) {
     // sx: input part (the first layer's input projection P, loaded before the
     // accumulator is ready, or the folded bias plus the input chunks); sh:
     // recurrent part (GRU only: the other cells add everything into sx)
-    constexpr bool SPLIT = CELL == GRU;
     float sx[NS], sh[SPLIT ? NS : 1];
 #pragma unroll
     for (int cc = 0; cc < NS; ++cc) {
@@ -231,7 +261,7 @@ __device__ void epilogue(const StackArgs& a, const Ctx& c, int row, int e) {
 #pragma unroll
       for (int i = 0; i < N / 16; ++i) {
         float w[16];
-        tc::tmem_load16(c.tmem + lane_q + (uint32_t)(acc * ACC + 16 * i), w);
+        tc::tmem_load16(c.tmem + lane_q + acc_base + (uint32_t)(acc * ACC + 16 * i), w);
 #pragma unroll
         for (int g4 = 0; g4 < 4; ++g4) {
           const int col = 16 * i + 4 * g4, p = col / NS, cc = col % NS;
@@ -298,75 +328,140 @@ __device__ void epilogue(const StackArgs& a, const Ctx& c, int row, int e) {
       }
     }
 
-    // ---- gates of this row for the batch slice
+    // ---- gates of this row for the batch slice.  One epilogue warp per
+    // scheduler leaves nothing to hide latency behind but the independent
+    // columns of a loop, so the loops are branch-free: sigmoid(x) = 1/2 +
+    // tanh(x/2)/2 makes every gate ga * tanh(ga * x) + gc; column bounds only
+    // guard the global stores (nval: columns of this slice inside the batch).
     const size_t tb = (size_t)t * B;
+    const int nval = live_row ? min(NS, B - me * NS) : 0;
+    if constexpr (!SIMPLE) {
+      float gv[NS];
 #pragma unroll
-    for (int cc = 0; cc < NS; ++cc) {
-      const int b = me * NS + cc;
-      if (!live_row || b >= B) continue;
-      if constexpr (CELL == LSTM) {
-        const float pre = sx[cc];
-        const float gv = rg == 2 ? tanh_hw(pre) : sigm_hw(pre);
-        if (ly.gates_out) ly.gates_out[(tb + b) * GH + r0 + row] = gv;
-        smg[cc * 128 + row] = gv;
-      } else if constexpr (CELL == GRU) {
-        if (rg < 2) {
-          const float gv = sigm_hw(sx[cc] + sh[cc]);
-          if (ly.gates_out) ly.gates_out[(tb + b) * GH + r0 + row] = gv;
-          smg[cc * 128 + row] = gv;
-        } else {
-          smg[cc * 128 + row] = sx[cc];           // x_n + b_xn
-          smhn[cc * 32 + rj] = sh[cc] + bias_hn;  // W_hn h_{t-1} + b_hn
+      for (int cc = 0; cc < NS; ++cc) {
+        const float x = SPLIT ? sx[cc] + sh[SPLIT ? cc : 0] : sx[cc];
+        gv[cc] = fmaf(ga, tanh_hw(ga * x), gc);
+        if constexpr (SPLIT) gv[cc] = rg == 2 ? sx[cc] : gv[cc];  // GRU candidate row: x_n + b_xn
+      }
+#pragma unroll
+      for (int cc = 0; cc < NS; ++cc) smg[cc * 128 + row] = gv[cc];
+      if constexpr (SPLIT) {
+        if (live_row && rg == 2) {
+#pragma unroll
+          for (int cc = 0; cc < NS; ++cc) smhn[cc * 32 + rj] = sh[cc] + bias_hn;  // W_hn h_{t-1} + b_hn
         }
-      } else {
-        const float hv = simple_act<CELL, __nv_bfloat16>(sx[cc]);
-        const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-        const size_t bj = (size_t)b * H + j0 + row;
-        if (ly.gates_out) ly.gates_out[(tb + b) * GH + r0 + row] = hv;
-        ly.hseq[(size_t)(t + 1) * B * H + bj] = hb;
-        if (ly.y) ly.y[tb * H + bj] = hb;
-        if (t == T - 1 && ly.hT) ly.hT[bj] = hb;
+      }
+      if (gout && (!SPLIT || rg < 2)) {
+        float* const go = gout + (tb + me * NS) * GH + r0 + row;
+        if (nval == NS) {
+#pragma unroll
+          for (int cc = 0; cc < NS; ++cc) go[(size_t)cc * GH] = gv[cc];
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < NS; ++cc)
+            if (cc < nval) go[(size_t)cc * GH] = gv[cc];
+        }
+      }
+    } else {
+      // simple RNN: the row is the unit, h = act(x) directly
+      float hv[NS];
+#pragma unroll
+      for (int cc = 0; cc < NS; ++cc) hv[cc] = simple_act<CELL, __nv_bfloat16>(sx[cc]);
+      const size_t b0 = (size_t)me * NS;
+      __nv_bfloat16* const hs = ly.hseq + ((size_t)(t + 1) * B + b0) * H + j0 + row;
+      __nv_bfloat16* const ys = ly.y ? ly.y + (tb + b0) * H + j0 + row : nullptr;
+      __nv_bfloat16* const hTs = (t == T - 1 && ly.hT) ? ly.hT + b0 * H + j0 + row : nullptr;
+      float* const go = gout ? gout + (tb + b0) * GH + r0 + row : nullptr;
+#pragma unroll
+      for (int cc = 0; cc < NS; ++cc) {
+        if (cc >= nval) break;
+        const __nv_bfloat16 hb = __float2bfloat16_rn(hv[cc]);
+        hs[(size_t)cc * H] = hb;
+        if (ys) ys[(size_t)cc * H] = hb;
+        if (hTs) hTs[(size_t)cc * H] = hb;
+        if (go) go[(size_t)cc * GH] = hv[cc];
       }
     }
     if constexpr (!SIMPLE) {
       tc::named_bar(1, 128);
-      // ---- cell update of this thread's (unit, batch entry) pairs
+      // ---- cell update of this thread's (unit, batch entry) pairs: unit
+      // j0 + lane, batch column cc = 4 i + warp of the epilogue; arithmetic
+      // first, then the stores, so that the pairs' latencies overlap
+      const int w4 = e >> 5;
+      float hv[PP], nv[SPLIT ? PP : 1], hnv[SPLIT ? PP : 1];
+      if constexpr (CELL == LSTM) {
+        if (u == 1) {
 #pragma unroll
-      for (int i = 0; i < PP; ++i) {
-        const int q = i * 128 + e, jl = q % UC, cc = q / UC, b = me * NS + cc;
-        if (cc >= NS || b >= B) continue;
-        const int j = j0 + jl;
-        const size_t bj = (size_t)b * H + j;
-        const float* gr = smg + cc * 128;
-        float hv;
-        if constexpr (CELL == LSTM) {
-          float ig, fg, gg, og;
-          if (u == 1) {
-            const float4 g4 = *reinterpret_cast<const float4*>(gr + 4 * jl);
-            ig = g4.x; fg = g4.y; gg = g4.z; og = g4.w;
-          } else {
-            ig = gr[packed_row(0, jl, 4, u)];
-            fg = gr[packed_row(1, jl, 4, u)];
-            gg = gr[packed_row(2, jl, 4, u)];
-            og = gr[packed_row(3, jl, 4, u)];
+          for (int i = 0; i < PP; ++i) {
+            const float4 g4 = *reinterpret_cast<const float4*>(smg + (4 * i + w4) * 128 + 4 * lane);
+            st[i] = fmaf(g4.y, st[i], g4.x * g4.z);
+            hv[i] = g4.w * tanh_hw(st[i]);
           }
-          st[i] = fg * st[i] + ig * gg;
-          hv = og * tanh_hw(st[i]);
-          if (ly.c_out) ly.c_out[tb * H + bj] = st[i];
-          if (t == T - 1 && ly.cT) ly.cT[bj] = st[i];
         } else {
-          const float r = gr[packed_row(0, jl, 3, u)], z = gr[packed_row(1, jl, 3, u)];
-          const float xn = gr[packed_row(2, jl, 3, u)], hn = smhn[cc * 32 + jl];
-          const float n = tanh_hw(xn + r * hn);
-          hv = (1.f - z) * n + z * st[i];
-          st[i] = hv;
-          if (ly.gates_out) ly.gates_out[(tb + b) * GH + r0 + packed_row(2, jl, 3, u)] = n;
-          if (ly.hn_out) ly.hn_out[tb * H + bj] = hn;
+#pragma unroll
+          for (int i = 0; i < PP; ++i) {
+            const float* gr = smg + (4 * i + w4) * 128;
+            st[i] = fmaf(gr[o1], st[i], gr[o0] * gr[o2]);
+            hv[i] = gr[o3] * tanh_hw(st[i]);
+          }
         }
-        const __nv_bfloat16 hb = __float2bfloat16_rn(hv);
-        ly.hseq[(size_t)(t + 1) * B * H + bj] = hb;
-        if (ly.y) ly.y[tb * H + bj] = hb;
-        if (t == T - 1 && ly.hT) ly.hT[bj] = hb;
+      } else {
+#pragma unroll
+        for (int i = 0; i < PP; ++i) {
+          const float* gr = smg + (4 * i + w4) * 128;
+          const float r = gr[o0], z = gr[o1], xn = gr[o2];
+          const float hn = smhn[(4 * i + w4) * 32 + lane];
+          const float n = tanh_hw(fmaf(r, hn, xn));
+          hv[i] = fmaf(z, st[i] - n, n);  // (1 - z) n + z h_{t-1}
+          st[i] = hv[i];
+          nv[i] = n;
+          hnv[i] = hn;
+        }
+      }
+      // stores: column cc of the slice is batch entry me * NS + cc
+      const int bb = me * NS + w4;  // batch entry of pair 0
+      const bool full = me * NS + NS <= B;
+      const size_t off = (size_t)bb * H + j0 + lane;
+      __nv_bfloat16* const hs = ly.hseq + (size_t)(t + 1) * B * H + off;
+#pragma unroll
+      for (int i = 0; i < PP; ++i)
+        if (full || bb + 4 * i < B) hs[(size_t)(4 * i) * H] = __float2bfloat16_rn(hv[i]);
+      if (ly.y) {
+        __nv_bfloat16* const ys = ly.y + tb * H + off;
+#pragma unroll
+        for (int i = 0; i < PP; ++i)
+          if (full || bb + 4 * i < B) ys[(size_t)(4 * i) * H] = __float2bfloat16_rn(hv[i]);
+      }
+      if (t == T - 1 && ly.hT) {
+#pragma unroll
+        for (int i = 0; i < PP; ++i)
+          if (full || bb + 4 * i < B) ly.hT[off + (size_t)(4 * i) * H] = __float2bfloat16_rn(hv[i]);
+      }
+      if constexpr (CELL == LSTM) {
+        if (ly.c_out) {
+          float* const cs = ly.c_out + tb * H + off;
+#pragma unroll
+          for (int i = 0; i < PP; ++i)
+            if (full || bb + 4 * i < B) cs[(size_t)(4 * i) * H] = st[i];
+        }
+        if (t == T - 1 && ly.cT) {
+#pragma unroll
+          for (int i = 0; i < PP; ++i)
+            if (full || bb + 4 * i < B) ly.cT[off + (size_t)(4 * i) * H] = st[i];
+        }
+      } else {
+        if (gout) {
+          float* const gs = gout + (tb + bb) * GH + r0 + o2;
+#pragma unroll
+          for (int i = 0; i < PP; ++i)
+            if (full || bb + 4 * i < B) gs[(size_t)(4 * i) * GH] = nv[i];
+        }
+        if (ly.hn_out) {
+          float* const hns = ly.hn_out + tb * H + off;
+#pragma unroll
+          for (int i = 0; i < PP; ++i)
+            if (full || bb + 4 * i < B) hns[(size_t)(4 * i) * H] = hnv[i];
+        }
       }
     }
     // ---- publish h_t of this CTA's units and batch slice: the readers load
@@ -380,30 +475,47 @@ __device__ void epilogue(const StackArgs& a, const Ctx& c, int row, int e) {
 
 template <int CELL, int N>
 __global__ void __launch_bounds__(kThreads, 1)
-    stack_fwd_kernel(const __grid_constant__ StackMaps maps, const StackArgs a) {
+    stack_fwd_kernel(const __grid_constant__ StackMaps maps, const __grid_constant__ StackArgs p) {
   constexpr int G = CellInfo<CELL>::G;
   constexpr int UC = G == 1 ? 128 : 32;
   constexpr int RING = N * 128;
-  constexpr int ACC = N < 32 ? 32 : N;  // TMEM columns between the two accumulators
-  constexpr uint32_t TMEM_COLS = 2 * ACC <= 64 ? 64 : 128;
+  constexpr uint32_t TMEM_COLS = 512;  // weights (kc / 2 columns) + two accumulators
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (a.cluster > 1) {
+  if (p.cluster > 1) {
     uint32_t ncta;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
-    if ((int)ncta != a.cluster) {
-      if (threadIdx.x == 0) raise_error(a.err, DEV_BAD_CLUSTER);
+    if ((int)ncta != p.cluster) {
+      if (threadIdx.x == 0) raise_error(p.err, DEV_BAD_CLUSTER);
       return;
     }
   }
+  int li = 0;
+  while (li + 1 < p.nl && (int)blockIdx.x >= p.cta0[li + 1]) ++li;
+  Run a;
+  a.T = p.T;
+  a.B = p.B;
+  a.H = p.H;
+  a.u_pack = p.u_pack;
+  a.kc = p.kc;
+  a.cluster = p.cluster;
+  a.test_skip_publish = p.test_skip_publish;
+  a.err = p.err;
+  a.limit_ns = p.limit_ns;
+  a.cnt = p.cnt;
+  a.want_h = (unsigned)p.ctas[li];
+  a.want_x = li > 0 ? (unsigned)p.ctas[li - 1] : 0u;
+  a.sm = p.sm;
+  a.ly = p.lay[li];
+  const int NST = a.sm.stages;
   Ctx c;
   c.smem = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.sm.bars);
   c.full = bars;
-  c.empty = c.full + kStages;
-  c.tfull = c.empty + kStages;
+  c.empty = c.full + kMaxStages;
+  c.tfull = c.empty + kMaxStages;
   c.tempty = c.tfull + 2;
   c.rbar = c.tempty + 2;
   c.abar = c.rbar + 2;
@@ -411,22 +523,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.dbar + 1);
   c.abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   c.ep_fail = reinterpret_cast<int*>(tmem_slot + 2);
-  c.li = 0;
-  while (c.li + 1 < a.nl && (int)blockIdx.x >= a.cta0[c.li + 1]) ++c.li;
-  c.ks = a.ks[c.li];
-  c.kcx = a.kcx[c.li];
-  const int local = (int)blockIdx.x - a.cta0[c.li];
+  c.li = li;
+  c.ks = p.ks[li];
+  c.kcx = p.kcx[li];
+  const int local = (int)blockIdx.x - p.cta0[li];
   c.rb = local / c.ks;
   c.me = local % c.ks;
   c.crank = a.cluster > 1 ? (int)tc::cluster_ctarank() : 0;
-  const StackLayer& ly = a.lay[c.li];
+  const StackLayer& ly = a.ly;
   const bool xpart = c.me < c.kcx;
   const int k0 = (xpart ? c.me : c.me - c.kcx) * a.kc;
   const int nkb = a.kc / 64;
   const int r0 = c.rb * UC * G;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       tc::mbar_init(c.full + s, 1);
       tc::mbar_init(c.empty + s, 1);
     }
@@ -435,12 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(c.tempty + i, 4);
       tc::mbar_init(c.rbar + i, 1);
     }
-    tc::mbar_init(c.abar, 1);
+    tc::mbar_init(c.abar, 4);  // the four epilogue warps, once their rows of the weights are in TMEM
     tc::mbar_init(c.dbar, 1);
     *c.abort_flag = 0;
     *c.ep_fail = 0;
     tc::fence_mbar_init();
-    tc::tma_prefetch_desc(xpart ? &maps.wx[c.li] : &maps.wh[c.li]);
     tc::tma_prefetch_desc(xpart ? &maps.h[c.li] : &maps.h[c.li + 1]);
   }
   if (warp == 1) {
@@ -452,44 +562,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   if (a.cluster > 1) tc::cluster_sync_all();  // every peer's barriers and flags exist before remote traffic
   c.tmem = *tmem_slot;
+  // TMEM columns: [0, kc/2) this CTA's block of weight rows (row i in lane i,
+  // two consecutive k per column), then the two accumulators
+  const uint32_t acc_base = (uint32_t)(a.kc / 2);
 
-  int last_par[kStages];  // producer: parity of the last load issued into each stage (-1: none)
-  for (int s = 0; s < kStages; ++s) last_par[s] = -1;
+  int last_par[kMaxStages];  // producer: parity of the last load issued into each buffer (-1: none)
+  for (int s = 0; s < kMaxStages; ++s) last_par[s] = -1;
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      // this CTA's block of weight rows, resident for the whole launch
-      tc::mbar_arrive_expect_tx(c.abar, (uint32_t)nkb * 16384u);
-      for (int kb = 0; kb < nkb; ++kb)
-        tc::tma_load_2d(smem + a.sm.a + kb * 16384, xpart ? &maps.wx[c.li] : &maps.wh[c.li], c.abar, k0 + kb * 64,
-                        r0);
       uint32_t stage = 0, phase = 0;
       const CUtensorMap* src = xpart ? &maps.h[c.li] : &maps.h[c.li + 1];
       for (int t = 0; t < a.T; ++t) {
         bool ok = true;
         if (xpart) {
-          if (ly.wait_in) ok = wait_count(a.cnt + (size_t)(c.li - 1) * a.T + t, (unsigned)a.ctas[c.li - 1], c, a);
+          if (ly.wait_in) ok = wait_count(a.cnt + (size_t)(c.li - 1) * a.T + t, a.want_x, c, a);
         } else if (t > 0) {
-          ok = wait_count(a.cnt + (size_t)c.li * a.T + t - 1, (unsigned)a.ctas[c.li], c, a);
+          ok = wait_count(a.cnt + (size_t)c.li * a.T + t - 1, a.want_h, c, a);
         }
         if (!ok) break;
         // h written by other CTAs' generic stores, read here through the async proxy
         tc::fence_proxy_async_global();
         const int slot = xpart ? t + 1 : t;
-        for (int kb = 0; kb < nkb && ok; ++kb) {
-          if (!tc::mbar_wait(c.empty + stage, phase ^ 1, c.abort_flag, a.err, a.limit_ns)) {
-            ok = false;
-            break;
-          }
-          tc::mbar_arrive_expect_tx(c.full + stage, RING);
-          last_par[stage] = (int)phase;
-          tc::tma_load_2d(smem + a.sm.ring + stage * RING, src, c.full + stage, k0 + kb * 64, slot * a.B);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+        // the whole K chunk of this timestep in one load: nkb blocks of N
+        // batch rows x 64 k, laid out one block after the other
+        if (!tc::mbar_wait(c.empty + stage, phase ^ 1, c.abort_flag, a.err, a.limit_ns)) break;
+        tc::mbar_arrive_expect_tx(c.full + stage, (uint32_t)(nkb * RING));
+        last_par[stage] = (int)phase;
+        tc::tma_load_3d(smem + a.sm.ring + stage * nkb * RING, src, c.full + stage, 0, slot * a.B, k0 / 64);
+        if (++stage == (uint32_t)NST) {
+          stage = 0;
+          phase ^= 1;
         }
-        if (!ok) break;
       }
       if (*c.abort_flag) abort_cluster(c, a.cluster);
     }
@@ -500,30 +604,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = tc::mbar_wait(c.abar, 0, c.abort_flag, a.err, a.limit_ns);
       tc::fence_after_sync();
       uint32_t stage = 0, phase = 0;
-      const uint32_t sa = tc::smem_addr(smem + a.sm.a);
       for (int t = 0; t < a.T && ok; ++t) {
         const int acc = t & 1;
         if (!tc::mbar_wait(c.tempty + acc, ((uint32_t)(t >> 1) & 1u) ^ 1u, c.abort_flag, a.err, a.limit_ns)) break;
         tc::fence_after_sync();
-        const uint32_t d = c.tmem + (uint32_t)(acc * ACC);
+        const uint32_t d = c.tmem + acc_base + (uint32_t)(acc * (N < 32 ? 32 : N));
+        if (!tc::mbar_wait(c.full + stage, phase, c.abort_flag, a.err, a.limit_ns)) break;
+        tc::fence_after_sync();
+        const uint32_t sb0 = tc::smem_addr(smem + a.sm.ring + stage * nkb * RING);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!tc::mbar_wait(c.full + stage, phase, c.abort_flag, a.err, a.limit_ns)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const uint32_t sb = tc::smem_addr(smem + a.sm.ring + stage * RING);
+          const uint32_t sb = sb0 + (uint32_t)(kb * RING);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16(d, tc::sdesc_sw128(sa + kb * 16384 + kk * 32, 16, 1024),
-                         tc::sdesc_sw128(sb + kk * 32, 16, 1024), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(c.empty + stage);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+            tc::mma_bf16_ta(d, c.tmem + (uint32_t)(kb * 32 + kk * 8), tc::sdesc_sw128(sb + kk * 32, 16, 1024), idesc,
+                            (kb > 0 || kk > 0) ? 1u : 0u);
         }
-        if (!ok) break;
+        tc::mma_commit(c.empty + stage);
+        if (++stage == (uint32_t)NST) {
+          stage = 0;
+          phase ^= 1;
+        }
         tc::mma_commit(c.tfull + acc);
       }
       // every MMA issued has completed before the tensor memory is freed
@@ -537,9 +637,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int row = (warp & 3) * 32 + lane;
     const int e = threadIdx.x - 64;
-    if (c.ks == 1) epilogue<CELL, N, 1>(a, c, row, e);
-    else if (c.ks == 2) epilogue<CELL, N, 2>(a, c, row, e);
-    else epilogue<CELL, N, 4>(a, c, row, e);
+    {
+      // this row of the CTA's weight block into TMEM (rows past the block's
+      // gate rows, GRU's last 32, hold zeros)
+      const int G_H = G * a.H;
+      const bool live = row < G * UC && r0 + row < G_H;
+      const __nv_bfloat16* wrow = (xpart ? ly.Wx : ly.Wh) + (size_t)(r0 + row) * a.H + k0;
+      const uint32_t lane_q = static_cast<uint32_t>(row & ~31) << 16;
+      for (int c16 = 0; c16 < a.kc / 32; ++c16) {
+        float v[16];
+        if (live) {
+          const uint4* q = reinterpret_cast<const uint4*>(wrow + c16 * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 u = q[i];
+            v[4 * i] = __uint_as_float(u.x);
+            v[4 * i + 1] = __uint_as_float(u.y);
+            v[4 * i + 2] = __uint_as_float(u.z);
+            v[4 * i + 3] = __uint_as_float(u.w);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        }
+        tc::tmem_store16(c.tmem + lane_q + (uint32_t)(c16 * 16), v);
+      }
+      tc::tmem_store_wait();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(c.abar);
+    }
+    if (c.ks == 1) epilogue<CELL, N, 1>(a, c, row, e, acc_base);
+    else if (c.ks == 2) epilogue<CELL, N, 2>(a, c, row, e, acc_base);
+    else epilogue<CELL, N, 4>(a, c, row, e, acc_base);
   }
 
   tc::fence_before_sync();
@@ -547,14 +677,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0 && *c.abort_flag) {
     // copies already issued land before the CTA's shared memory goes away
     // (after an abort some were never consumed)
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       if (last_par[s] < 0) continue;
       const uint64_t t0 = globaltimer_ns();
       while (!tc::mbar_try_wait(c.full + s, (uint32_t)last_par[s]) && globaltimer_ns() - t0 < 1000000ull) {
       }
-    }
-    const uint64_t t0 = globaltimer_ns();
-    while (!tc::mbar_try_wait(c.abar, 0) && globaltimer_ns() - t0 < 1000000ull) {
     }
   }
   if (warp == 1) {
@@ -562,6 +689,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_dealloc(c.tmem, TMEM_COLS);
   }
   if (a.cluster > 1) tc::cluster_sync_all();  // no peer stores into this CTA's shared memory after it exits
+}
+
+// 3-D map over an h sequence [rows][H] bf16 seen as (64 k, row, k block):
+// box (64, N, nkb) with 128-byte swizzle; its shared-memory image is nkb
+// consecutive N x 128-byte blocks, each one K-major tensor-core operand.
+int encode_h3(CUtensorMap* map, const void* ptr, long long rows, int H, int N, int nkb) {
+  auto enc = tmap_encoder();
+  if (!enc) return RNN_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || H % 64) return RNN_ERR_INVALID_ARG;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(H / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)H * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)N, (cuuint32_t)nkb}, es[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RNN_OK : RNN_ERR_INVALID_ARG;
 }
 
 // Geometry of a launch over layers [0, nl) of a group: K chunk, chunks per
@@ -600,8 +743,17 @@ int geometry(int cell, int H, int B, int nl, int first_p, Geom* g) {
   g->cluster = ksmax;
   for (int l = 0; l < nl; ++l)
     if (g->lctas[l] % ksmax) return RNN_ERR_UNSUPPORTED;
-  g->sm = smem_layout(cell, g->N, g->kc, ksmin, ksmax);
-  if (g->sm.total + 1024 > 227 * 1024) return RNN_ERR_UNSUPPORTED;
+  // input buffers: two where they fit (a chunk whose input is ready early
+  // loads the next step while this one computes)
+  bool fit = false;
+  for (int st : {2, 1}) {
+    g->sm = smem_layout(cell, g->N, g->kc, ksmin, ksmax, st);
+    if (g->sm.total + 1024 <= 227 * 1024) {
+      fit = true;
+      break;
+    }
+  }
+  if (!fit) return RNN_ERR_UNSUPPORTED;
   return RNN_OK;
 }
 
@@ -699,31 +851,27 @@ int stack_fwd(const Launch& L, int cell, const StackArgs& in) {
     a.ctas[l] = g.lctas[l];
   }
   a.cta0[in.nl] = g.cta0[in.nl];
-  a.sm.a = g.sm.a;
+  a.sm.stages = g.sm.stages;
   a.sm.ring = g.sm.ring;
   a.sm.rbuf = g.sm.rbuf;
   a.sm.smg = g.sm.smg;
   a.sm.smhn = g.sm.smhn;
   a.sm.bars = g.sm.bars;
-  const int G = cell == LSTM ? 4 : cell == GRU ? 3 : 1;
-  const int GH = G * in.H;
   StackMaps maps;
   memset(&maps, 0, sizeof(maps));
   for (int l = 0; l < in.nl; ++l) {
     const StackLayer& ly = in.lay[l];
     if (!ly.hseq || !ly.Wh) return RNN_ERR_INVALID_ARG;
-    // weight rows: box of 64 k x 128 rows (rows past the end read zero)
-    RNN_TRY_LOCAL(encode_operand(&maps.wh[l], Operand{ly.Wh, in.H, 0, GH, in.H}, 128));
+    if (reinterpret_cast<uintptr_t>(ly.Wh) & 15) return RNN_ERR_INVALID_ARG;
     if (g.kcx[l]) {
-      if (!ly.Wx || !ly.in || ly.In != in.H) return RNN_ERR_INVALID_ARG;
-      RNN_TRY_LOCAL(encode_operand(&maps.wx[l], Operand{ly.Wx, in.H, 0, GH, in.H}, 128));
+      if (!ly.Wx || !ly.in || ly.In != in.H || (reinterpret_cast<uintptr_t>(ly.Wx) & 15)) return RNN_ERR_INVALID_ARG;
     } else if (!ly.P) {
       return RNN_ERR_INVALID_ARG;
     }
-    // h sequence [T+1][B][H] as (T+1)*B rows: box of 64 k x N batch rows
-    RNN_TRY_LOCAL(encode_operand(&maps.h[l + 1], Operand{ly.hseq, in.H, 0, (in.T + 1) * in.B, in.H}, g.N));
+    // h sequence [T+1][B][H] as (T+1)*B rows
+    RNN_TRY_LOCAL(encode_h3(&maps.h[l + 1], ly.hseq, (long long)(in.T + 1) * in.B, in.H, g.N, g.kc / 64));
   }
-  if (g.kcx[0]) RNN_TRY_LOCAL(encode_operand(&maps.h[0], Operand{in.lay[0].in, in.H, 0, (in.T + 1) * in.B, in.H}, g.N));
+  if (g.kcx[0]) RNN_TRY_LOCAL(encode_h3(&maps.h[0], in.lay[0].in, (long long)(in.T + 1) * in.B, in.H, g.N, g.kc / 64));
   return dispatch(L, cell, maps, a, g, false, L.num_sms);
 }
 
