@@ -218,7 +218,8 @@ struct StackArgs {
   uint64_t limit_ns;
   int test_skip_publish;    // test hook: CTA 0 never publishes step 0
   // geometry (filled by stack_fwd)
-  int kc, cluster;
+  int cluster;
+  int kcl[kStackMaxLayers];  // K chunk width of each layer's CTAs
   int ks[kStackMaxLayers], kcx[kStackMaxLayers], cta0[kStackMaxLayers + 1], ctas[kStackMaxLayers];
   StackSmem sm;
 };

@@ -74,10 +74,10 @@ namespace {
 // TMA maps of one launch over the h sequences, 3-D: (64 k of a block, batch
 // row, k block) with box (64, N, kc / 64), so that one load brings a CTA's
 // whole K chunk of a timestep (a TMA load costs ~150 ns to issue whatever
-// its size, and 8 loads of 4-8 KB each per timestep were the bound): h[0]
-// the input of the first layer (when it has no P), h[1 + l] layer l's own.
+// its size, and 8 loads of 4-8 KB each per timestep were the bound).
 struct StackMaps {
-  CUtensorMap h[kStackMaxLayers + 1];
+  CUtensorMap hx[kStackMaxLayers];  // layer l's input (the layer below's h sequence), box depth of layer l
+  CUtensorMap hh[kStackMaxLayers];  // layer l's own h sequence, box depth of layer l
 };
 
 constexpr int kMaxStages = 4;  // input buffers, one timestep's K chunk each
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   a.B = p.B;
   a.H = p.H;
   a.u_pack = p.u_pack;
-  a.kc = p.kc;
+  a.kc = p.kcl[li];
   a.cluster = p.cluster;
   a.test_skip_publish = p.test_skip_publish;
   a.err = p.err;
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *c.abort_flag = 0;
     *c.ep_fail = 0;
     tc::fence_mbar_init();
-    tc::tma_prefetch_desc(xpart ? &maps.h[c.li] : &maps.h[c.li + 1]);
+    tc::tma_prefetch_desc(xpart ? &maps.hx[c.li] : &maps.hh[c.li]);
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, TMEM_COLS);
@@ -572,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
-      const CUtensorMap* src = xpart ? &maps.h[c.li] : &maps.h[c.li + 1];
+      const CUtensorMap* src = xpart ? &maps.hx[c.li] : &maps.hh[c.li];
       for (int t = 0; t < a.T; ++t) {
         bool ok = true;
         if (xpart) {
@@ -707,33 +707,61 @@ int encode_h3(CUtensorMap* map, const void* ptr, long long rows, int H, int N, i
   return r == CUDA_SUCCESS ? RNN_OK : RNN_ERR_INVALID_ARG;
 }
 
-// Geometry of a launch over layers [0, nl) of a group: K chunk, chunks per
-// layer, CTAs.  first_p: the group's first layer reads P (it is the stack's
-// layer 0).
+// Geometry of a launch over layers [0, nl) of a group: K chunk width and
+// chunks per layer, CTAs.  first_p: the group's first layer reads P (it is
+// the stack's layer 0, K = H; the others have K = 2H).  A CTA's epilogue
+// works on N / ks batch columns, and the wavefront moves at the pace of its
+// slowest layer, so chunks are narrowed (512 -> 256) on the layers with the
+// fewest chunks while the CTAs stay within `budget`.
 struct Geom {
-  int kc, N, cluster, ctas;
-  int ks[kStackMaxLayers], kcx[kStackMaxLayers], cta0[kStackMaxLayers + 1], lctas[kStackMaxLayers];
+  int N, cluster, ctas;
+  int kc[kStackMaxLayers], ks[kStackMaxLayers], kcx[kStackMaxLayers], cta0[kStackMaxLayers + 1],
+      lctas[kStackMaxLayers];
   Smem sm;
 };
 
-int geometry(int cell, int H, int B, int nl, int first_p, Geom* g) {
+int geometry(int cell, int H, int B, int nl, int first_p, int budget, Geom* g) {
   if (nl < 1 || nl > kStackMaxLayers || B < 1 || B > 64) return RNN_ERR_UNSUPPORTED;
   const int G = cell == LSTM ? 4 : cell == GRU ? 3 : 1;
   const int uc = G == 1 ? 128 : 32;
-  if (H % uc) return RNN_ERR_UNSUPPORTED;
-  g->kc = H % 512 == 0 ? 512 : H % 256 == 0 ? 256 : 0;
-  if (!g->kc) return RNN_ERR_UNSUPPORTED;
+  if (H % uc || H % 256) return RNN_ERR_UNSUPPORTED;
   g->N = B <= 16 ? 16 : B <= 32 ? 32 : 64;
   const int rbs = H / uc;
-  int cta = 0, ksmax = 1, ksmin = 4;
-  for (int l = 0; l < nl; ++l) {
+  auto set = [&](int l, int kc) {
     const bool p = l == 0 && first_p;
-    g->kcx[l] = p ? 0 : H / g->kc;  // layers above the first: input width H
-    g->ks[l] = g->kcx[l] + H / g->kc;
+    g->kc[l] = kc;
+    g->kcx[l] = p ? 0 : H / kc;  // layers above the first: input width H
+    g->ks[l] = g->kcx[l] + H / kc;
+  };
+  int cta = 0;
+  for (int l = 0; l < nl; ++l) {
+    set(l, H % 512 == 0 ? 512 : 256);
     if (g->ks[l] != 1 && g->ks[l] != 2 && g->ks[l] != 4) return RNN_ERR_UNSUPPORTED;
     if (g->N / g->ks[l] < 4) return RNN_ERR_UNSUPPORTED;
+    cta += rbs * g->ks[l];
+  }
+  // narrow the chunks of every layer that has the fewest, while they fit
+  for (;;) {
+    int kmin = 8;
+    for (int l = 0; l < nl; ++l) kmin = std::min(kmin, g->ks[l]);
+    int extra = 0;
+    bool can = true;
+    for (int l = 0; l < nl; ++l) {
+      if (g->ks[l] != kmin) continue;
+      if (g->kc[l] != 512 || 2 * g->ks[l] > 4 || g->N / (2 * g->ks[l]) < 8) can = false;
+      extra += rbs * g->ks[l];
+    }
+    if (!can || cta + extra > budget) break;
+    for (int l = 0; l < nl; ++l)
+      if (g->ks[l] == kmin) set(l, 256);
+    cta += extra;
+  }
+  int ksmax = 1, ksmin = 4, kcmax = 0;
+  cta = 0;
+  for (int l = 0; l < nl; ++l) {
     ksmax = std::max(ksmax, g->ks[l]);
     ksmin = std::min(ksmin, g->ks[l]);
+    kcmax = std::max(kcmax, g->kc[l]);
     g->cta0[l] = cta;
     g->lctas[l] = rbs * g->ks[l];
     cta += g->lctas[l];
@@ -747,7 +775,7 @@ int geometry(int cell, int H, int B, int nl, int first_p, Geom* g) {
   // loads the next step while this one computes)
   bool fit = false;
   for (int st : {2, 1}) {
-    g->sm = smem_layout(cell, g->N, g->kc, ksmin, ksmax, st);
+    g->sm = smem_layout(cell, g->N, kcmax, ksmin, ksmax, st);
     if (g->sm.total + 1024 <= 227 * 1024) {
       fit = true;
       break;
@@ -826,7 +854,7 @@ int dispatch(const Launch& L, int cell, const StackMaps& maps, const StackArgs& 
 
 int stack_check(int cell, int H, int B, int nl, int first_p, int u_pack, int num_sms, int* ctas) {
   Geom g;
-  RNN_TRY_LOCAL(geometry(cell, H, B, nl, first_p, &g));
+  RNN_TRY_LOCAL(geometry(cell, H, B, nl, first_p, num_sms > 0 ? num_sms : 152, &g));
   const int uc = cell == LSTM || cell == GRU ? 32 : 128;
   if (u_pack < 1 || uc % u_pack) return RNN_ERR_UNSUPPORTED;
   if (ctas) *ctas = g.ctas;
@@ -839,12 +867,12 @@ int stack_check(int cell, int H, int B, int nl, int first_p, int u_pack, int num
 
 int stack_fwd(const Launch& L, int cell, const StackArgs& in) {
   Geom g;
-  const int rc = geometry(cell, in.H, in.B, in.nl, in.lay[0].P != nullptr, &g);
+  const int rc = geometry(cell, in.H, in.B, in.nl, in.lay[0].P != nullptr, L.num_sms > 0 ? L.num_sms : 152, &g);
   if (rc != RNN_OK) return rc;
   StackArgs a = in;
-  a.kc = g.kc;
   a.cluster = g.cluster;
   for (int l = 0; l < in.nl; ++l) {
+    a.kcl[l] = g.kc[l];
     a.ks[l] = g.ks[l];
     a.kcx[l] = g.kcx[l];
     a.cta0[l] = g.cta0[l];
@@ -868,10 +896,14 @@ int stack_fwd(const Launch& L, int cell, const StackArgs& in) {
     } else if (!ly.P) {
       return RNN_ERR_INVALID_ARG;
     }
-    // h sequence [T+1][B][H] as (T+1)*B rows
-    RNN_TRY_LOCAL(encode_h3(&maps.h[l + 1], ly.hseq, (long long)(in.T + 1) * in.B, in.H, g.N, g.kc / 64));
+    // h sequences [T+1][B][H] as (T+1)*B rows, boxes of this layer's chunk depth
+    const long long rows = (long long)(in.T + 1) * in.B;
+    RNN_TRY_LOCAL(encode_h3(&maps.hh[l], ly.hseq, rows, in.H, g.N, g.kc[l] / 64));
+    if (g.kcx[l]) {
+      const __nv_bfloat16* src = l == 0 ? ly.in : in.lay[l - 1].hseq;
+      RNN_TRY_LOCAL(encode_h3(&maps.hx[l], src, rows, in.H, g.N, g.kc[l] / 64));
+    }
   }
-  if (g.kcx[0]) RNN_TRY_LOCAL(encode_h3(&maps.h[0], in.lay[0].in, (long long)(in.T + 1) * in.B, in.H, g.N, g.kc / 64));
   return dispatch(L, cell, maps, a, g, false, L.num_sms);
 }
 
