@@ -126,6 +126,9 @@ enum {
                                       stacked recurrence (up to 4 layers per launch, each layer's
                                       [W_x | W_h] rows resident in tensor memory, layer l+1 starting step t
                                       as soon as layer l has finished it) */
+#define RNN_FLAG_NO_STACK_BWD 0x40000u /* run the backward recurrence as step launches even where the persistent
+                                          stacked backward (the transposed products of up to 4 layers per
+                                          launch, 9..64 sequences) fits; RNN_FLAG_NO_STACK turns off both */
 #define RNN_FLAG_FORCE_STACK 0x20000u /* use the persistent stacked forward recurrence (also for B <= 8, in
                                          place of the single-layer persistent recurrence) or fail */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrences one CTA never

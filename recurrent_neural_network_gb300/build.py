@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "librnn.so")
-UNITS = ["api.cu", "gemm.cu", "step_fwd.cu", "step_bwd.cu", "persist.cu", "stack.cu"]
+UNITS = ["api.cu", "gemm.cu", "step_fwd.cu", "step_bwd.cu", "persist.cu", "stack.cu", "stack_bwd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # a variable read before it is set (diagnostic 549) fails the build instead of warning
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

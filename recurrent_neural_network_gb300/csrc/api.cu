@@ -142,6 +142,10 @@ struct rnn_s {
   // choice, stack what the current lengths allow (variable lengths: off)
   int stack = 0, stack_plan = 0;
   std::vector<std::pair<int, int>> stack_groups;  // (first layer, layers)
+  // persistent stacked backward: groups from the top of the stack down
+  int stackb = 0, stackb_plan = 0;
+  std::vector<std::pair<int, int>> stackb_groups;  // (lowest layer, layers), highest group first
+  std::vector<int> stackb_budget;                  // CTA budget of each group's geometry
   int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
   // variable lengths (rnn_set_lengths): Bt[t] = number of sequences still
   // running at step t (the batch is sorted by non-increasing length, so the
@@ -337,6 +341,36 @@ int plan_and_layout(rnn_s* h) {
     }
   }
   if ((d.flags & RNN_FLAG_FORCE_STACK) && !h->stack) return RNN_ERR_UNSUPPORTED;
+  // persistent stacked backward, same batch range: groups of up to
+  // kStackMaxLayers layers from the top of the stack down
+  if (d.mode == RNN_MODE_BF16 && h->D == 1 && !h->persist && B <= 64 &&
+      !(d.flags & (RNN_FLAG_NO_STACK | RNN_FLAG_NO_STACK_BWD | RNN_FLAG_FORCE_STREAMING)) &&
+      (B > 8 || (d.flags & RNN_FLAG_FORCE_STACK))) {
+    const int sms = h->have_device ? h->num_sms : 0;
+    std::vector<std::pair<int, int>> groups;
+    std::vector<int> budgets;
+    bool ok = true;
+    for (int top = L - 1; top >= 0 && ok;) {
+      int nl = 0, budget = 0;
+      while (top - nl >= 0 && nl < kStackMaxLayers) {
+        int ctas = 0, b = 0;
+        if (stack_bwd_check(d.cell, H, B, nl + 1, top == L - 1 ? 1 : 0, h->u, sms, &ctas, &b) != RNN_OK) break;
+        ++nl;
+        budget = b;
+      }
+      if (nl == 0) ok = false;
+      else {
+        groups.emplace_back(top - nl + 1, nl);
+        budgets.push_back(budget);
+      }
+      top -= nl;
+    }
+    if (ok) {
+      h->stackb = h->stackb_plan = 1;
+      h->stackb_groups = groups;
+      h->stackb_budget = budgets;
+    }
+  }
 
   const size_t e = h->elem;
   const size_t BH = (size_t)B * H, BGH = (size_t)B * GH;
@@ -560,6 +594,65 @@ int cu(cudaError_t e) { return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA; }
 
 // hand-off cluster size of the persistent recurrence (0: counters), bf16 or fp8-stash plan
 int pa_cluster(const rnn_s* h, bool p8) { return p8 ? h->persist8_cl : h->persist_cl; }
+
+// Backward data pass with the persistent stacked recurrence: one launch per
+// layer group from the top of the stack down (each computes its layers' gate
+// gradients, dh0 and dc0), then the gradient of the stack's input dGx^0 W_x^0
+// as one GEMM over all timesteps.
+int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const char* PW, const float* c0, void* dx,
+              void* dh0, float* dc0, char* R, char* W, void* ws, cudaStream_t stream) {
+  const rnn_desc_t& d = h->d;
+  const int L = d.layers, T = d.T, B = d.B, H = d.hidden, GH = h->GH;
+  const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
+  const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+  unsigned int* cnt = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
+  for (size_t gi = 0; gi < h->stackb_groups.size(); ++gi) {
+    const int l0 = h->stackb_groups[gi].first, nl = h->stackb_groups[gi].second;
+    StackBwdArgs sa{};
+    sa.budget = h->stackb_budget[gi];
+    sa.T = T;
+    sa.B = B;
+    sa.H = H;
+    sa.u_pack = h->u;
+    sa.nl = nl;
+    for (int i = 0; i < nl; ++i) {
+      const int l = l0 + i;
+      const bool top = l == L - 1;
+      StackBwdLayer& ly = sa.lay[i];
+      ly.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
+      ly.Wx_above = top ? nullptr : reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l + 1].wx);
+      ly.dgx = reinterpret_cast<__nv_bfloat16*>(R + h->rl[l].dgx);
+      ly.dgh = reinterpret_cast<__nv_bfloat16*>(R + h->rl[l].dgh);
+      ly.dgx_above = top ? nullptr : reinterpret_cast<const __nv_bfloat16*>(R + h->rl[l + 1].dgx);
+      ly.gates = reinterpret_cast<const float*>(R + h->rl[l].gates);
+      ly.c = lstm ? reinterpret_cast<const float*>(R + h->rl[l].c) : nullptr;
+      ly.c0 = (lstm && c0) ? c0 + l * BH : nullptr;
+      ly.hn = gru ? reinterpret_cast<const float*>(R + h->rl[l].hn) : nullptr;
+      ly.hseq = reinterpret_cast<const __nv_bfloat16*>(R + h->rl[l].hseq);
+      ly.dy = top ? static_cast<const __nv_bfloat16*>(dy) : nullptr;
+      ly.dhT = dhT ? reinterpret_cast<const __nv_bfloat16*>(static_cast<const char*>(dhT) + l * BH * e) : nullptr;
+      ly.dcT = (lstm && dcT) ? dcT + l * BH : nullptr;
+      ly.dh0 = dh0 ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(dh0) + l * BH * e) : nullptr;
+      ly.dc0 = (lstm && dc0) ? dc0 + l * BH : nullptr;
+      ly.wait_above = i + 1 < nl ? 1 : 0;
+    }
+    RNN_TRY(cu(cudaMemsetAsync(cnt, 0, (size_t)nl * T * 4, stream)));
+    sa.cnt = cnt;
+    sa.err = reinterpret_cast<int*>(W + h->ws_err);
+    sa.limit_ns = h->limit_ns;
+    sa.test_skip_publish = (d.flags & RNN_FLAG_TEST_SKIP_PUBLISH) ? 1 : 0;
+    Launch Lk = mk(h, stream, ws, "stack_bwd");
+    RNN_TRY(stack_bwd(Lk, d.cell, sa));
+  }
+  if (dx) {
+    Operand A{R + h->rl[0].dgx, GH, 0, T * B, GH};
+    Operand Bx{PW + h->pl[0].wx, d.input, 1, d.input, GH, 1};
+    Launch Lk = mk(h, stream, ws, "dx_gemm");
+    RNN_TRY(gemm_store(Lk, d.mode, A, Bx, T * B, d.input, GH, dx, d.input, 0));
+  }
+  (void)BGH;
+  return RNN_OK;
+}
 
 // Forward pass with the persistent stacked recurrence: layer 0's input
 // projection for all timesteps as one GEMM, then one launch per layer group.
@@ -1155,6 +1248,7 @@ int rnn_set_lengths(rnn_handle_t h, const int* lens) {
   // launches take over (the packing unit it was planned with serves them)
   h->persist = h->varlen ? 0 : h->persist_plan;
   h->stack = h->varlen ? 0 : h->stack_plan;
+  h->stackb = h->varlen ? 0 : h->stackb_plan;
   return RNN_OK;
 }
 
@@ -1172,21 +1266,22 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   if (!h || !buf || len == 0) return RNN_ERR_INVALID_ARG;
   const char* cell = h->d.cell == RNN_LSTM ? "lstm" : h->d.cell == RNN_GRU ? "gru" : h->d.cell == RNN_RELU ? "relu" : "tanh";
   // layer groups of the stacked forward, "first+count" each
-  char groups[128] = "-";
-  if (h->stack) {
+  char groups[128] = "-", bgroups[128] = "-";
+  auto list = [](char* out, size_t len, const std::vector<std::pair<int, int>>& gs) {
     size_t n = 0;
-    for (size_t i = 0; i < h->stack_groups.size() && n + 16 < sizeof(groups); ++i)
-      n += (size_t)snprintf(groups + n, sizeof(groups) - n, "%s%d+%d", i ? "," : "", h->stack_groups[i].first,
-                            h->stack_groups[i].second);
-  }
+    for (size_t i = 0; i < gs.size() && n + 16 < len; ++i)
+      n += (size_t)snprintf(out + n, len - n, "%s%d+%d", i ? "," : "", gs[i].first, gs[i].second);
+  };
+  if (h->stack) list(groups, sizeof(groups), h->stack_groups);
+  if (h->stackb) list(bgroups, sizeof(bgroups), h->stackb_groups);
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
            "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d transposed=%d fused_point=%d "
-           "persist_cluster=%d directions=%d fp8_stash=%d stack_groups=%s",
+           "persist_cluster=%d directions=%d fp8_stash=%d stack_groups=%s stack_bwd_groups=%s",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
            h->persist ? "persistent" : h->stack ? "stacked" : "streaming", h->d.mode ? "tcgen05" : "ffma",
            h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->num_sms, h->tstep, h->bwd_fuse,
-           h->persist ? h->persist_cl : 0, h->D, h->persist8, groups);
+           h->persist ? h->persist_cl : 0, h->D, h->persist8, groups, bgroups);
   return RNN_OK;
 }
 
@@ -1390,6 +1485,7 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
     char* W = static_cast<char*>(ws);
     const char* PW = static_cast<const char*>(w_packed);
     if (h->D == 2) return bwd_bidir(h, dy, dhT, dcT, PW, c0, dx, dh0, dc0, R, W, ws, stream);
+    if (h->stackb && !h->varlen) return bwd_stack(h, dy, dhT, dcT, PW, c0, dx, dh0, dc0, R, W, ws, stream);
 
     for (int l = 0; l < L; ++l)
       RNN_TRY(cu(cudaMemsetAsync(W + h->wl[l].ctr, 0, (size_t)h->ctr_count * 4, stream)));

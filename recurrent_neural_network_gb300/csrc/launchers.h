@@ -230,4 +230,49 @@ struct StackArgs {
 int stack_check(int cell, int H, int B, int nl, int first_p, int u_pack, int num_sms, int* ctas);
 int stack_fwd(const Launch& L, int cell, const StackArgs& a);
 
+// Persistent backward-through-time of up to kStackMaxLayers stacked layers in
+// one launch (bf16, one direction, no variable lengths): each CTA owns 128
+// hidden units and holds their columns of [W_h^l ; W_x^{l+1}] (one K chunk)
+// in tensor memory; layer l works on reverse step s once it has its own
+// dGh_{s+1} and the layer above's dGx_s.  lay[0] is the lowest layer.
+struct StackBwdLayer {
+  const __nv_bfloat16* Wh;        // packed [G*H][H] of this layer
+  const __nv_bfloat16* Wx_above;  // packed W_x [G*H][H] of the layer above, null at the top of the stack
+  __nv_bfloat16* dgx;             // [T][B][G*H] gate gradients (written)
+  __nv_bfloat16* dgh;             // [T][B][G*H] recurrent-side gate gradients (GRU; others: = dgx)
+  const __nv_bfloat16* dgx_above; // the layer above's dgx, null at the top of the stack
+  const float* gates;             // [T][B][G*H] activated gates
+  const float* c;                 // LSTM [T][B][H]
+  const float* c0;                // LSTM [B][H] or null
+  const float* hn;                // GRU [T][B][H]
+  const __nv_bfloat16* hseq;      // GRU: [T+1][B][H] (h_{s-1} in slot s)
+  const __nv_bfloat16* dy;        // top of the stack: [T][B][H], else null
+  const __nv_bfloat16* dhT;       // [B][H] or null
+  const float* dcT;               // LSTM [B][H] or null
+  __nv_bfloat16* dh0;             // [B][H] or null
+  float* dc0;                     // LSTM [B][H] or null
+  int wait_above;                 // 1: the layer above runs in this launch
+};
+struct StackBwdArgs {
+  int T, B, H, u_pack;
+  int nl;
+  StackBwdLayer lay[kStackMaxLayers];
+  unsigned int* cnt;  // [nl][T] arrival counters, zero before the launch
+  int* err;
+  uint64_t limit_ns;
+  int test_skip_publish;
+  int budget;  // most CTAs of the launch (from stack_bwd_check)
+  // geometry (filled by stack_bwd)
+  int cluster;
+  int kcl[kStackMaxLayers], ks[kStackMaxLayers], kr[kStackMaxLayers], cta0[kStackMaxLayers + 1],
+      ctas[kStackMaxLayers];
+  StackSmem sm;
+};
+// RNN_OK if nl stacked layers of (cell, H, B) run their BPTT as one launch
+// (has_top: the group's highest layer is the top of the stack, with no layer
+// above it); *ctas receives the grid size and *budget the CTA budget to pass
+// in StackBwdArgs::budget (the geometry the device can hold).
+int stack_bwd_check(int cell, int H, int B, int nl, int has_top, int u_pack, int num_sms, int* ctas, int* budget);
+int stack_bwd(const Launch& L, int cell, const StackBwdArgs& a);
+
 }  // namespace rnn

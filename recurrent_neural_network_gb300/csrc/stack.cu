@@ -59,17 +59,14 @@
 #include "common.cuh"
 #include "launch.cuh"
 #include "launchers.h"
+#include "stack.cuh"
 #include "tc.cuh"
 
 namespace rnn {
 
 namespace {
 
-#define RNN_TRY_LOCAL(x)          \
-  do {                            \
-    const int rc_ = (x);          \
-    if (rc_ != RNN_OK) return rc_; \
-  } while (0)
+using namespace stk;
 
 // TMA maps of one launch over the h sequences, 3-D: (64 k of a block, batch
 // row, k block) with box (64, N, kc / 64), so that one load brings a CTA's
@@ -82,25 +79,6 @@ struct StackMaps {
 
 constexpr int kMaxStages = 4;  // input buffers, one timestep's K chunk each
 constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue (one per TMEM lane quadrant)
-
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add_u32(unsigned int* p, unsigned int v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, const float* v, uint32_t cluster_bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                   cluster_addr),
-               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-               "r"(__float_as_uint(v[3])), "r"(cluster_bar)
-               : "memory");
-}
-__device__ __forceinline__ void st_dsmem_s32(uint32_t cluster_addr, int v) {
-  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
 
 // Shared-memory layout of a CTA (offsets from the 1024-aligned base): the
 // ring of input buffers (kc / 64 blocks of N x 64 bf16 each), the receive
@@ -152,29 +130,9 @@ struct Run {
   StackLayer ly;            // this CTA's layer
 };
 
-// Raise the abort flag in every CTA of the cluster (this one included).
-__device__ __forceinline__ void abort_cluster(const Ctx& c, int cluster) {
-  *c.abort_flag = 1;
-  if (cluster > 1) {
-    const uint32_t fa = tc::smem_addr(const_cast<int*>(c.abort_flag));
-    for (int r = 0; r < cluster; ++r) st_dsmem_s32(tc::mapa(fa, (uint32_t)r), 1);
-  }
-}
-
-// Wait until *cnt >= want (bounded; gives up at once when the CTA aborts).
-__device__ __forceinline__ bool wait_count(const unsigned int* cnt, unsigned int want, const Ctx& c,
-                                           const Run& a) {
-  if (ld_acquire_u32(cnt) >= want) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (ld_acquire_u32(cnt) < want) {
-    if (*c.abort_flag) return false;
-    if (globaltimer_ns() - t0 > a.limit_ns) {
-      raise_error(a.err, DEV_TIMEOUT_STEP);
-      abort_cluster(c, a.cluster);
-      return false;
-    }
-  }
-  return true;
+__device__ __forceinline__ void abort_cluster(const Ctx& c, int cluster) { stk::abort_cluster(c.abort_flag, cluster); }
+__device__ __forceinline__ bool wait_count(const unsigned int* cnt, unsigned int want, const Ctx& c, const Run& a) {
+  return stk::wait_count(cnt, want, c.abort_flag, a.cluster, a.err, a.limit_ns);
 }
 
 // ---------------------------------------------------------------------------
@@ -691,22 +649,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (a.cluster > 1) tc::cluster_sync_all();  // no peer stores into this CTA's shared memory after it exits
 }
 
-// 3-D map over an h sequence [rows][H] bf16 seen as (64 k, row, k block):
-// box (64, N, nkb) with 128-byte swizzle; its shared-memory image is nkb
-// consecutive N x 128-byte blocks, each one K-major tensor-core operand.
-int encode_h3(CUtensorMap* map, const void* ptr, long long rows, int H, int N, int nkb) {
-  auto enc = tmap_encoder();
-  if (!enc) return RNN_ERR_CUDA;
-  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || H % 64) return RNN_ERR_INVALID_ARG;
-  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(H / 64)};
-  cuuint64_t strides[2] = {(cuuint64_t)H * 2, 128};
-  cuuint32_t box[3] = {64, (cuuint32_t)N, (cuuint32_t)nkb}, es[3] = {1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? RNN_OK : RNN_ERR_INVALID_ARG;
-}
-
 // Geometry of a launch over layers [0, nl) of a group: K chunk width and
 // chunks per layer, CTAs.  first_p: the group's first layer reads P (it is
 // the stack's layer 0, K = H; the others have K = 2H).  A CTA's epilogue
@@ -898,10 +840,10 @@ int stack_fwd(const Launch& L, int cell, const StackArgs& in) {
     }
     // h sequences [T+1][B][H] as (T+1)*B rows, boxes of this layer's chunk depth
     const long long rows = (long long)(in.T + 1) * in.B;
-    RNN_TRY_LOCAL(encode_h3(&maps.hh[l], ly.hseq, rows, in.H, g.N, g.kc[l] / 64));
+    RNN_TRY_LOCAL(encode_seq3(&maps.hh[l], ly.hseq, rows, in.H, g.N, g.kc[l] / 64));
     if (g.kcx[l]) {
       const __nv_bfloat16* src = l == 0 ? ly.in : in.lay[l - 1].hseq;
-      RNN_TRY_LOCAL(encode_h3(&maps.hx[l], src, rows, in.H, g.N, g.kc[l] / 64));
+      RNN_TRY_LOCAL(encode_seq3(&maps.hx[l], src, rows, in.H, g.N, g.kc[l] / 64));
     }
   }
   return dispatch(L, cell, maps, a, g, false, L.num_sms);

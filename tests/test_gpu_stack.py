@@ -15,7 +15,7 @@ import pytest
 
 from recurrent_neural_network_gb300 import rnn, runner, synth
 
-from parity import compare, device_relu_decisions, relu_check, run_gpu, run_oracle
+from parity import compare, device_relu_decisions, rel_l2, relu_check, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -26,28 +26,51 @@ def plan_of(r):
         int(re.search(r" u=(\d+)", d).group(1))
 
 
+def bwd_groups(r):
+    return re.search(r"stack_bwd_groups=(\S+)", r.r.describe()).group(1)
+
+
 STACK_CASES = [
-    # cell, layers, T, B, I, H, expected groups
-    (0, 3, 12, 24, 64, 512, "0+3"),          # LSTM, packing unit 16, N=32
-    (0, 4, 9, 64, 512, 512, "0+4"),          # LSTM, the 4-layer H=512 B=64 shape, unit 1, N=64
-    (0, 2, 7, 9, 40, 256, "0+2"),            # ragged batch (N=16), 256-wide K chunks
-    (1, 2, 10, 32, 72, 256, "0+2"),          # GRU, input and recurrent sums apart
-    (1, 3, 6, 20, 64, 1024, "0+1,1+1,2+1"),  # GRU one layer per launch: a group's input from the previous one
-    (2, 5, 8, 33, 96, 1024, "0+4,4+1"),      # tanh: 128 units per CTA, two groups
-    (0, 1, 11, 48, 32, 1024, "0+1"),         # one layer, K split in two
+    # cell, layers, T, B, I, H, forward groups, backward groups (highest first; "-": step launches)
+    (0, 3, 12, 24, 64, 512, "0+3", "0+3"),            # LSTM, packing unit 16, N=32
+    (0, 4, 9, 64, 512, 512, "0+4", "0+4"),            # LSTM, the 4-layer H=512 B=64 shape, unit 1, N=64
+    (0, 2, 7, 9, 40, 256, "0+2", "0+2"),              # ragged batch (N=16), 256-wide K chunks
+    (1, 2, 10, 32, 72, 256, "0+2", "0+2"),            # GRU, input and recurrent sums apart; 384-wide bwd chunks
+    (1, 3, 6, 20, 64, 1024, "0+1,1+1,2+1", "-"),      # GRU one layer per launch: a group's input from the previous one
+    (2, 5, 8, 33, 96, 1024, "0+4,4+1", "1+4,0+1"),    # tanh: 128 units per CTA, two groups each way
+    (0, 1, 11, 48, 32, 1024, "0+1", "0+1"),           # one layer, K split in two
 ]
 
 
 @pytest.mark.parametrize("train", [True, False], ids=["train", "infer"])
 @pytest.mark.parametrize("case", STACK_CASES, ids=lambda c: "c%d_L%d_T%d_B%d_I%d_H%d" % c[:6])
 def test_stacked_forward(case, train):
-    cell, L, T, B, I, H, groups = case
+    cell, L, T, B, I, H, groups, bgroups = case
     wl = synth.Workload("stack", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3,
                         training=train)
     hi = runner.HostInputs(wl, with_state_grads=True)
     r = runner.Runner(wl)
     assert plan_of(r)[:2] == ("stacked", groups)
+    # the backward groups depend on how many clusters of up to 8 CTAs the
+    # device holds at once: stacked where planned, in as many groups as fit
+    assert (bwd_groups(r) == "-") == (bgroups == "-"), bwd_groups(r)
     compare(wl, run_gpu(wl, hi), run_oracle(hi, train=train))
+
+
+@pytest.mark.parametrize("case", [c for c in STACK_CASES if c[7] != "-"], ids=lambda c: "c%d_L%d_T%d_B%d_I%d_H%d" % c[:6])
+def test_stacked_backward_equals_step_launches_within_tolerance(case):
+    """The stacked backward (the transposed products of all layers in one
+    launch, dh0 and dc0 from its last step) against the step-launch backward
+    on the same forward: both at the bf16 gradient bar of each other."""
+    cell, L, T, B, I, H = case[:6]
+    wl = synth.Workload("sbw", cell, L, T, B, I, H, synth.MODE_BF16, forget_bias=1.0, state_std=0.3)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    a = run_gpu(wl, hi)
+    b = run_gpu(wl, hi, flags=rnn.FLAG_NO_STACK_BWD)
+    assert bwd_groups(runner.Runner(wl, flags=rnn.FLAG_NO_STACK_BWD)) == "-"
+    for k in ("dx", "dh0", "dc0"):
+        if a.get(k) is not None:
+            assert rel_l2(a[k], b[k]) <= 2e-2, k
 
 
 def test_forced_below_nine_sequences():
@@ -103,6 +126,22 @@ def test_bounded_wait_reports_timeout():
     compare(wl, run_gpu(wl, hi), run_oracle(hi, train=False))
 
 
+def test_bounded_wait_reports_timeout_in_training():
+    """The same hook in a training call: the stacked forward and then the
+    stacked backward each lose CTA 0's first step, their waits give up, and the
+    next call on a clean handle is right."""
+    wl = synth.Workload("sskipt", 0, 2, 4, 16, 64, 256, synth.MODE_BF16)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    r = runner.Runner(wl, flags=rnn.FLAG_TEST_SKIP_PUBLISH, timeout_ns=20_000_000)
+    assert plan_of(r)[0] == "stacked" and bwd_groups(r) != "-"
+    r.upload(hi)
+    r.forward(True)
+    assert r.status() == -5
+    r.backward()
+    assert r.status() == -5
+    compare(wl, run_gpu(wl, hi), run_oracle(hi))
+
+
 def test_relu_with_ordinary_weights():
     """ReLU stack on ordinary weights, gradients checked with the decisions the
     device took (each differing one within the forward bar of 0)."""
@@ -114,10 +153,11 @@ def test_relu_with_ordinary_weights():
 
 
 def test_workload_lstm_4layer_b64_is_stacked():
-    """The 4-layer LSTM H=512 B=64 T=100 training workload runs its forward as
-    one stacked launch; full-size parity is in test_workload_lstm_h512_training."""
+    """The 4-layer LSTM H=512 B=64 T=100 training workload runs its forward and
+    its backward as one stacked launch each; full-size parity is in
+    test_workload_lstm_h512_training."""
     r = runner.Runner(synth.WORKLOADS[1])
-    assert plan_of(r)[:2] == ("stacked", "0+4")
+    assert plan_of(r)[:2] == ("stacked", "0+4") and bwd_groups(r) != "-"
 
 
 def test_workload_gru_8layer_is_stacked():

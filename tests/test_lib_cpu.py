@@ -131,6 +131,14 @@ def test_stacked_plan_groups(lib):
     assert plan(0, 2, 10, 32, 64, 320, 1)[0] == "streaming"
     with pytest.raises(rnn.RnnError):
         rnn.RNN(0, 2, 10, 32, 64, 320, 1, flags=rnn.FLAG_FORCE_STACK)
+    # the backward, highest group first (host planning for GB300: clusters
+    # of up to 8 CTAs, at most 152 CTAs per launch)
+    bw = lambda *a, **k: re.search(r"stack_bwd_groups=(\S+)", rnn.RNN(*a, **k).describe()).group(1)
+    assert bw(0, 4, 100, 64, 512, 512, 1) == "0+4"
+    assert bw(2, 5, 8, 33, 96, 1024, 1) == "1+4,0+1"
+    assert bw(1, 8, 200, 32, 1024, 1024, 1) == "-"        # GRU H=1024: K = 6144 per layer does not fit
+    assert bw(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK_BWD) == "-"
+    assert bw(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK) == "-"
     # variable lengths switch the forward to step launches
     r = rnn.RNN(0, 2, 10, 16, 64, 512, 1)
     assert "recurrence=stacked" in r.describe()
