@@ -134,30 +134,34 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
     const int acc = ti & 1, par = ti & 1;
     const uint32_t ph = (uint32_t)(ti >> 1) & 1u;
     if (KS > 1 && threadIdx.x == 64) tc::mbar_arrive_expect_tx(&c.rbar[par], (uint32_t)((KS - 1) * 128 * NS * 4));
-    // ---- inputs of the pointwise step, independent of the recurrence
-    float gv[G][NS], cs[NS], cp[NS], hp[NS], hnv[NS], dyv[NS];
+    // ---- inputs of the pointwise step, independent of the recurrence: only
+    // loads here, every conversion after the accumulator wait, so that all
+    // columns' loads are in flight together (a conversion per column made
+    // each column's load complete before the next one was issued).
+    // Addresses are clamped into range instead of predicating the loads (a
+    // value selected against 0 right after its load is consumed there):
+    // columns past the batch are never stored, step -1 runs no pointwise
+    // step, and c_{-1} without c0 is zeroed where it is used.
+    float gv[G][NS], cs[NS], cp[NS], hnv[NS];
+    unsigned short hpr[NS], dyr[NS];
+    const int sl = s < 0 ? 0 : s;
+    const bool cp_zero = CELL == LSTM && sl == 0 && !ly.c0;
 #pragma unroll
     for (int cc = 0; cc < NS; ++cc) {
-      const bool v = s >= 0 && cc < nval;
-      const size_t bs = (size_t)s * B + b0 + cc;
+      const int b = min(b0 + cc, B - 1);
+      const size_t bs = (size_t)sl * B + b;
 #pragma unroll
-      for (int g = 0; g < G; ++g) gv[g][cc] = v ? ly.gates[bs * GH + prow[g]] : 0.f;
-      cs[cc] = cp[cc] = hp[cc] = hnv[cc] = 0.f;
+      for (int g = 0; g < G; ++g) gv[g][cc] = ly.gates[bs * GH + prow[g]];
       if constexpr (CELL == LSTM) {
-        if (v) {
-          cs[cc] = ly.c[bs * H + j];
-          cp[cc] = s > 0 ? ly.c[(bs - B) * H + j] : (ly.c0 ? ly.c0[(size_t)(b0 + cc) * H + j] : 0.f);
-        }
+        cs[cc] = ly.c[bs * H + j];
+        const float* cpp = sl > 0 ? ly.c + (bs - B) * H + j : (ly.c0 ? ly.c0 + (size_t)b * H + j : ly.c + bs * H + j);
+        cp[cc] = *cpp;
       } else if constexpr (CELL == GRU) {
-        if (v) {
-          hnv[cc] = ly.hn[bs * H + j];
-          hp[cc] = __bfloat162float(ly.hseq[bs * H + j]);  // slot s holds h_{s-1}
-        }
+        hnv[cc] = ly.hn[bs * H + j];
+        hpr[cc] = reinterpret_cast<const unsigned short*>(ly.hseq)[bs * H + j];  // slot s holds h_{s-1}
       }
-      float d = 0.f;
-      if (v && ly.dy) d = __bfloat162float(ly.dy[bs * H + j]);
-      if (v && s == T - 1 && ly.dhT) d += __bfloat162float(ly.dhT[(size_t)(b0 + cc) * H + j]);
-      dyv[cc] = d;
+      if (ly.dy) dyr[cc] = reinterpret_cast<const unsigned short*>(ly.dy)[bs * H + j];
+      else dyr[cc] = 0;
     }
     // ---- accumulator of this step: own batch slice summed, the others sent
     float sum[NS];
@@ -229,7 +233,14 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
       break;
     }
     // ---- pointwise step s: the gate gradients of this unit and batch slice
-    float dgx[G][NS], dgh[G][NS];
+    float dgx[G][NS], dgh[G][NS], dyv[NS], hp[NS];
+#pragma unroll
+    for (int cc = 0; cc < NS; ++cc) {
+      dyv[cc] = __uint_as_float((uint32_t)dyr[cc] << 16);
+      // the gradient reaching the final state, at the first reverse step only
+      if (s == T - 1 && ly.dhT && cc < nval) dyv[cc] += __bfloat162float(ly.dhT[(size_t)(b0 + cc) * H + j]);
+      hp[cc] = __uint_as_float((uint32_t)hpr[cc] << 16);
+    }
 #pragma unroll
     for (int cc = 0; cc < NS; ++cc) {
       if constexpr (CELL == LSTM) {
@@ -238,7 +249,7 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
         const float tau = tanh_hw(cs[cc]);
         const float dcv = carry[cc] + d * og * (1.f - tau * tau);
         dgx[0][cc] = dcv * gg * ig * (1.f - ig);
-        dgx[1][cc] = dcv * cp[cc] * fg * (1.f - fg);
+        dgx[1][cc] = dcv * (cp_zero ? 0.f : cp[cc]) * fg * (1.f - fg);
         dgx[2][cc] = dcv * ig * (1.f - gg * gg);
         dgx[3][cc] = d * tau * og * (1.f - og);
         carry[cc] = dcv * fg;
