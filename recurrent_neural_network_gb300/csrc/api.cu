@@ -1671,9 +1671,15 @@ int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* r
     const char* R = static_cast<const char*>(reserve);
     const int TB = T * B;
     if (h->D == 2) return wgrad_bidir(h, x, R, dw, accumulate, ws, stream);
-    // Each weight-gradient product has (G*H / 128) x (I_l / 256) tiles over
-    // K = T*B and fills the GPU by itself: the products run back to back on the
-    // caller's stream.
+    // A weight-gradient product has about (G*H / 256) x (I_l / 256) tiles of
+    // 256 x 256 on CTA pairs over K = T*B.  Where one fills the GPU, the
+    // products run back to back on the caller's stream; where one would leave
+    // most SMs idle (moderate widths), each layer's two products run on its
+    // own stream, side by side with the other layers' (the outputs are
+    // disjoint).  The bias reductions share one scratch buffer and run after.
+    const int tiles = ((GH + 255) / 256) * ((std::max(d.input, H) + 255) / 256);
+    const bool side = L > 1 && 2 * tiles * 4 <= h->num_sms && !(d.flags & RNN_FLAG_PROFILE);
+    if (side) RNN_TRY(fork_streams(h, stream));
     for (int l = 0; l < L; ++l) {
       const int In = h->In(l);
       Remap rm{1, G, h->u, H};
@@ -1681,9 +1687,12 @@ int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* r
       Operand dgh{R + h->rl[l].dgh, GH, 1, GH, TB};
       Operand X = l == 0 ? Operand{x, In, 1, In, TB} : Operand{R + h->rl[l - 1].hseq + BH * e, H, 1, H, TB};
       Operand Hp{R + h->rl[l].hseq, H, 1, H, TB};
-      Launch Lk = mk(h, stream, ws, "dw_gemm");
+      Launch Lk = mk(h, side ? h->streams[l] : stream, ws, "dw_gemm");
       RNN_TRY(gemm_f32(Lk, mode, dgx, X, GH, In, TB, dw + h->ul[l].wx, In, nullptr, accumulate, rm, 0));
       RNN_TRY(gemm_f32(Lk, mode, dgh, Hp, GH, H, TB, dw + h->ul[l].wh, H, nullptr, accumulate, rm, 0));
+    }
+    if (side) RNN_TRY(join_streams(h, stream));
+    for (int l = 0; l < L; ++l) {
       Launch Lb = mk(h, stream, ws, "bias_grad");
       RNN_TRY(bias_grad(Lb, mode, d.cell, H, h->u, TB, R + h->rl[l].dgx, R + h->rl[l].dgh, dw + h->ul[l].bx,
                         dw + h->ul[l].bh, accumulate, reinterpret_cast<float*>(static_cast<char*>(ws) + h->ws_bias),
