@@ -158,7 +158,7 @@ struct rnn_s {
   struct PL { size_t wx, wh, bias, bias_hn, wh8, wsc; };
   struct RL { size_t gates, c, hn, hseq, dgx, dgh; };
   struct WL { size_t P, hseq, c2, dyab, carry, part, ctr, dh; };
-  size_t ws_bias = 0;  // bias-gradient slices (shared by the layers, used one layer at a time)
+  size_t ws_bias = 0;  // bias-gradient partial sums, one scratch slice per (layer, direction)
   int bias_slices = 1;
   struct UL { size_t wx, wh, bx, bh; };  // element offsets in the user weight vector
   std::vector<PL> pl;
@@ -417,7 +417,7 @@ int plan_and_layout(rnn_s* h) {
   h->ws_arrive = take(cur, (size_t)kStackMaxLayers * T * 4);  // per-timestep counters (stack: per layer)
   h->ws_hx = (h->persist_plan || h->persist8) ? take(cur, (size_t)8 * B * H) : 0;
   h->bias_slices = std::max(1, std::min(64, (T * B + 255) / 256));
-  h->ws_bias = take(cur, (size_t)h->bias_slices * GH * 4);
+  h->ws_bias = take(cur, (size_t)V * h->bias_slices * GH * 4);  // one scratch slice per (layer, direction)
   h->ws_dtop = Dn == 2 ? take(cur, (size_t)2 * T * BH * e) : 0;
   h->ws_dxacc = (Dn == 2 && d.mode == RNN_MODE_BF16) ? take(cur, (size_t)T * B * d.input * 4) : 0;
   for (int l = 0; l < V; ++l) {
@@ -1676,7 +1676,7 @@ int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* r
     // products run back to back on the caller's stream; where one would leave
     // most SMs idle (moderate widths), each layer's two products run on its
     // own stream, side by side with the other layers' (the outputs are
-    // disjoint).  The bias reductions share one scratch buffer and run after.
+    // disjoint), each followed by its bias reduction (own scratch slice).
     const int tiles = ((GH + 255) / 256) * ((std::max(d.input, H) + 255) / 256);
     const bool side = L > 1 && 2 * tiles * 4 <= h->num_sms && !(d.flags & RNN_FLAG_PROFILE);
     if (side) RNN_TRY(fork_streams(h, stream));
@@ -1691,13 +1691,13 @@ int rnn_bwd_weights(rnn_handle_t h, const void* x, const void* h0, const void* r
       RNN_TRY(gemm_f32(Lk, mode, dgx, X, GH, In, TB, dw + h->ul[l].wx, In, nullptr, accumulate, rm, 0));
       RNN_TRY(gemm_f32(Lk, mode, dgh, Hp, GH, H, TB, dw + h->ul[l].wh, H, nullptr, accumulate, rm, 0));
     }
-    if (side) RNN_TRY(join_streams(h, stream));
     for (int l = 0; l < L; ++l) {
-      Launch Lb = mk(h, stream, ws, "bias_grad");
+      Launch Lb = mk(h, side ? h->streams[l] : stream, ws, "bias_grad");
+      float* scratch = reinterpret_cast<float*>(static_cast<char*>(ws) + h->ws_bias) + (size_t)l * h->bias_slices * GH;
       RNN_TRY(bias_grad(Lb, mode, d.cell, H, h->u, TB, R + h->rl[l].dgx, R + h->rl[l].dgh, dw + h->ul[l].bx,
-                        dw + h->ul[l].bh, accumulate, reinterpret_cast<float*>(static_cast<char*>(ws) + h->ws_bias),
-                        h->bias_slices));
+                        dw + h->ul[l].bh, accumulate, scratch, h->bias_slices));
     }
+    if (side) RNN_TRY(join_streams(h, stream));
     return RNN_OK;
   };
   return run_graphed(h, stream, key, issue);

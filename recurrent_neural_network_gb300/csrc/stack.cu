@@ -78,7 +78,7 @@ struct StackMaps {
 };
 
 constexpr int kMaxStages = 4;  // input buffers, one timestep's K chunk each
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue (one per TMEM lane quadrant)
+constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quadrant)
 
 // Shared-memory layout of a CTA (offsets from the 1024-aligned base): the
 // ring of input buffers (kc / 64 blocks of N x 64 bf16 each), the receive
@@ -136,22 +136,34 @@ __device__ __forceinline__ bool wait_count(const unsigned int* cnt, unsigned int
 }
 
 // ---------------------------------------------------------------------------
-// epilogue: 128 threads, thread e owns TMEM lane / packed row `row` of the
-// CTA's block; KS chunks per row block, this CTA's batch slice is
-// [me*NS, me*NS + NS)
+// epilogue: 256 threads, two halves of four warps (one warp per TMEM lane
+// quadrant in each).  Thread (row, hf) owns packed row `row` of the CTA's
+// block for the columns [hf*NH, hf*NH + NH) of this CTA's batch slice
+// [me*NS, me*NS + NS) (NH = NS/2; with NS < 8 the first half takes all NS);
+// in the cell update thread e takes unit j0 + lane and slice columns
+// 8 i + e / 32.  Two warps per scheduler halve every loop of the epilogue
+// and leave a second warp to issue while one waits.
 template <int CELL, int N, int KS>
-__device__ void epilogue(const Run& a, const Ctx& c, int row, int e, uint32_t acc_base) {
+__device__ void epilogue(const Run& a, const Ctx& c, int row, int hf, int e, uint32_t acc_base) {
   constexpr int G = CellInfo<CELL>::G;
   constexpr bool SIMPLE = G == 1;
   constexpr int UC = SIMPLE ? 128 : 32;
   constexpr int ROWS = G * UC;
   constexpr int NS = N / KS;
-  constexpr int PP = SIMPLE ? 1 : (UC * NS + 127) / 128;  // (unit, batch) pairs per thread
+  constexpr bool TWO = NS >= 8;               // both halves take columns
+  constexpr int NH = TWO ? NS / 2 : NS;       // columns of a half
+  constexpr int PP = SIMPLE ? 1 : (NS + 7) / 8;  // (unit, batch column) pairs per thread
+  constexpr int NC4 = NS / 4;                 // float4 chunks of a slice
+  constexpr bool SPLIT = CELL == GRU;         // input and recurrent sums apart (GRU candidate gate)
+  constexpr int ACC = N < 32 ? 32 : N;        // TMEM columns between the two accumulators
   const StackLayer& ly = a.ly;
   const int T = a.T, B = a.B, H = a.H, GH = G * H, u = a.u_pack;
   const int me = c.me, kcx = c.kcx;
   const int j0 = c.rb * UC, r0 = j0 * G;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, w8 = e >> 5;
+  const bool act = TWO || hf == 0;            // this half takes columns
+  const int c0h = hf * NH;                    // first slice column of this half
+  const int cb = me * NS + c0h;               // its first batch entry
   const uint32_t lane_q = static_cast<uint32_t>(row & ~31) << 16;
   const bool live_row = row < ROWS;
   // gate and unit of this thread's row
@@ -170,9 +182,6 @@ __device__ void epilogue(const Run& a, const Ctx& c, int row, int e, uint32_t ac
   float* smg = reinterpret_cast<float*>(c.smem + a.sm.smg);
   float* smhn = reinterpret_cast<float*>(c.smem + a.sm.smhn);
   float4* rbuf = reinterpret_cast<float4*>(c.smem + a.sm.rbuf);
-  constexpr int NC4 = NS / 4;  // float4 chunks of a slice
-  constexpr bool SPLIT = CELL == GRU;  // input and recurrent sums apart (GRU candidate gate)
-  constexpr int ACC = N < 32 ? 32 : N;  // TMEM columns between the two accumulators
   // receive buffer of parity p from the peer in slot s: [p][s][chunk][row]
   auto rb_at = [&](int p, int s, int ch) -> float4* { return rbuf + ((p * (KS - 1) + s) * NC4 + ch) * 128; };
 
@@ -182,10 +191,10 @@ __device__ void epilogue(const Run& a, const Ctx& c, int row, int e, uint32_t ac
   for (int i = 0; i < PP; ++i) {
     st[i] = 0.f;
     if constexpr (!SIMPLE) {
-      const int q = i * 128 + e, jl = q % UC, cc = q / UC, b = me * NS + cc;
+      const int cc = 8 * i + w8, b = me * NS + cc;
       if (cc < NS && b < B) {
-        if (CELL == LSTM && ly.c0) st[i] = ly.c0[(size_t)b * H + j0 + jl];
-        if (CELL == GRU) st[i] = __bfloat162float(ly.hseq[(size_t)b * H + j0 + jl]);
+        if (CELL == LSTM && ly.c0) st[i] = ly.c0[(size_t)b * H + j0 + lane];
+        if (CELL == GRU) st[i] = __bfloat162float(ly.hseq[(size_t)b * H + j0 + lane]);
       }
     }
   }
@@ -196,16 +205,25 @@ __device__ void epilogue(const Run& a, const Ctx& c, int row, int e, uint32_t ac
     if (KS > 1 && e == 0) tc::mbar_arrive_expect_tx(&c.rbar[par], (uint32_t)((KS - 1) * 128 * NS * 4));
     // sx: input part (the first layer's input projection P, loaded before the
     // accumulator is ready, or the folded bias plus the input chunks); sh:
-    // recurrent part (GRU only: the other cells add everything into sx)
-    float sx[NS], sh[SPLIT ? NS : 1];
+    // recurrent part (GRU only: the other cells add everything into sx).  P
+    // is loaded unconditionally from clamped addresses (a loaded value
+    // selected against 0 is consumed at the select, which made each column's
+    // load wait for the previous one); columns past the batch and rows past
+    // the block are never stored.
+    float sx[NH], sh[SPLIT ? NH : 1];
+    if (ly.P) {
+      const float* prow = ly.P + (size_t)t * B * GH + min(r0 + row, GH - 1);
 #pragma unroll
-    for (int cc = 0; cc < NS; ++cc) {
-      const int b = me * NS + cc;
-      sx[cc] = ly.P ? ((live_row && b < B) ? ly.P[((size_t)t * B + b) * GH + r0 + row] : 0.f) : bias;
-      if constexpr (SPLIT) sh[cc] = 0.f;
+      for (int cc = 0; cc < NH; ++cc) sx[cc] = prow[(size_t)min(cb + cc, B - 1) * GH];
+    } else {
+#pragma unroll
+      for (int cc = 0; cc < NH; ++cc) sx[cc] = bias;
     }
-    // ---- accumulator of this step
-    bool ok = true;
+#pragma unroll
+    for (int cc = 0; cc < (SPLIT ? NH : 0); ++cc) sh[cc] = 0.f;
+    // ---- accumulator of this step: this half's columns of every chunk's
+    // slice, its own added to the sums, the others sent to their owners
+    bool ok;
     {
       int w = 1;
       if (lane == 0) w = tc::mbar_wait(&c.tfull[acc], ph, c.abort_flag, a.err, a.limit_ns) ? 1 : 0;
@@ -213,27 +231,29 @@ __device__ void epilogue(const Run& a, const Ctx& c, int row, int e, uint32_t ac
     }
     if (ok) {
       tc::fence_after_sync();
-      // the accumulator 16 columns at a time: each group of 4 columns is either
-      // this CTA's batch slice (added to its sums) or another chunk's (sent
-      // into that CTA's receive buffer)
+      if (act) {
+        constexpr int NL = NH < 16 ? NH : 16;  // columns per TMEM load
 #pragma unroll
-      for (int i = 0; i < N / 16; ++i) {
-        float w[16];
-        tc::tmem_load16(c.tmem + lane_q + acc_base + (uint32_t)(acc * ACC + 16 * i), w);
+        for (int p = 0; p < KS; ++p) {
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          const int col = 16 * i + 4 * g4, p = col / NS, cc = col % NS;
-          if (p == me) {
+          for (int l0 = 0; l0 < NH; l0 += NL) {
+            float w[NL];
+            tc::tmem_load_cols<NL>(c.tmem + lane_q + acc_base + (uint32_t)(acc * ACC + p * NS + c0h + l0), w);
+            if (p == me) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (SPLIT && me >= kcx) sh[cc + q] += w[4 * g4 + q];
-              else sx[cc + q] += w[4 * g4 + q];
+              for (int q = 0; q < NL; ++q) {
+                if (SPLIT && me >= kcx) sh[SPLIT ? l0 + q : 0] += w[q];
+                else sx[l0 + q] += w[q];
+              }
+            } else if constexpr (KS > 1) {
+              const int slot = me < p ? me : me - 1;
+              const uint32_t prank = (uint32_t)(c.crank - me + p);
+              const uint32_t bar = tc::mapa(tc::smem_addr(&c.rbar[par]), prank);
+#pragma unroll
+              for (int q = 0; q < NL / 4; ++q)
+                st_async_v4(tc::mapa(tc::smem_addr(rb_at(par, slot, (c0h + l0) / 4 + q) + row), prank), w + 4 * q,
+                            bar);
             }
-          } else if constexpr (KS > 1) {
-            const int slot = me < p ? me : me - 1;
-            const uint32_t prank = (uint32_t)(c.crank - me + p);
-            st_async_v4(tc::mapa(tc::smem_addr(rb_at(par, slot, cc / 4) + row), prank), w + 4 * g4,
-                        tc::mapa(tc::smem_addr(&c.rbar[par]), prank));
           }
         }
       }
@@ -242,21 +262,7 @@ __device__ void epilogue(const Run& a, const Ctx& c, int row, int e, uint32_t ac
       if (lane == 0) tc::mbar_arrive(&c.tempty[acc]);
       if constexpr (KS > 1) {
         int w = 1;
-        if (lane == 0) {
-          w = 0;
-          const uint64_t t0 = globaltimer_ns();
-          while (true) {
-            if (tc::mbar_try_wait_cluster(&c.rbar[par], ph)) {
-              w = 1;
-              break;
-            }
-            if (*c.abort_flag) break;
-            if (globaltimer_ns() - t0 > a.limit_ns) {
-              raise_error(a.err, DEV_TIMEOUT_STEP);
-              break;
-            }
-          }
-        }
+        if (lane == 0) w = wait_cluster_bytes(&c.rbar[par], ph, c.abort_flag, a.err, a.limit_ns) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
       }
     }
@@ -264,168 +270,159 @@ __device__ void epilogue(const Run& a, const Ctx& c, int row, int e, uint32_t ac
       *c.ep_fail = 1;
       abort_cluster(c, a.cluster);
     }
-    tc::named_bar(1, 128);
+    tc::named_bar(1, 256);
     if (*reinterpret_cast<volatile int*>(c.ep_fail)) break;
 
-    // ---- the other chunks' partial sums of this CTA's slice, in chunk order
-    // (input and recurrent parts apart for GRU)
+    // ---- the other chunks' partial sums of this half's columns, in chunk
+    // order (input and recurrent parts apart for GRU)
+    if (act) {
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      if (k == me) continue;
-      const bool xk = !SPLIT || k < kcx;
-      const int slot = k < me ? k : k - 1;
+      for (int k = 0; k < KS; ++k) {
+        if (k == me) continue;
+        const bool xk = !SPLIT || k < kcx;
+        const int slot = k < me ? k : k - 1;
 #pragma unroll
-      for (int ch = 0; ch < NC4; ++ch) {
-        const float4 q = rb_at(par, slot, ch)[row];
-        const float qq[4] = {q.x, q.y, q.z, q.w};
+        for (int q = 0; q < NH / 4; ++q) {
+          const float4 v = rb_at(par, slot, c0h / 4 + q)[row];
+          const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (SPLIT && !xk) sh[4 * ch + i] += qq[i];
-          else sx[4 * ch + i] += qq[i];
+          for (int i = 0; i < 4; ++i) {
+            if (SPLIT && !xk) sh[SPLIT ? 4 * q + i : 0] += vv[i];
+            else sx[4 * q + i] += vv[i];
+          }
         }
       }
     }
 
-    // ---- gates of this row for the batch slice.  One epilogue warp per
-    // scheduler leaves nothing to hide latency behind but the independent
-    // columns of a loop, so the loops are branch-free: sigmoid(x) = 1/2 +
-    // tanh(x/2)/2 makes every gate ga * tanh(ga * x) + gc; column bounds only
-    // guard the global stores (nval: columns of this slice inside the batch).
+    // ---- gates of this row for this half's columns (branch-free: sigmoid
+    // is ga * tanh(ga x) + gc; column bounds only guard the global stores)
     const size_t tb = (size_t)t * B;
-    const int nval = live_row ? min(NS, B - me * NS) : 0;
+    const int nval = (live_row && act) ? min(NH, B - cb) : 0;
     if constexpr (!SIMPLE) {
-      float gv[NS];
+      if (act) {
+        float gv[NH];
 #pragma unroll
-      for (int cc = 0; cc < NS; ++cc) {
-        const float x = SPLIT ? sx[cc] + sh[SPLIT ? cc : 0] : sx[cc];
-        gv[cc] = fmaf(ga, tanh_hw(ga * x), gc);
-        if constexpr (SPLIT) gv[cc] = rg == 2 ? sx[cc] : gv[cc];  // GRU candidate row: x_n + b_xn
-      }
-#pragma unroll
-      for (int cc = 0; cc < NS; ++cc) smg[cc * 128 + row] = gv[cc];
-      if constexpr (SPLIT) {
-        if (live_row && rg == 2) {
-#pragma unroll
-          for (int cc = 0; cc < NS; ++cc) smhn[cc * 32 + rj] = sh[cc] + bias_hn;  // W_hn h_{t-1} + b_hn
+        for (int cc = 0; cc < NH; ++cc) {
+          const float x = SPLIT ? sx[cc] + sh[SPLIT ? cc : 0] : sx[cc];
+          gv[cc] = fmaf(ga, tanh_hw(ga * x), gc);
+          if constexpr (SPLIT) gv[cc] = rg == 2 ? sx[cc] : gv[cc];  // GRU candidate row: x_n + b_xn
         }
-      }
-      if (gout && (!SPLIT || rg < 2)) {
-        float* const go = gout + (tb + me * NS) * GH + r0 + row;
-        if (nval == NS) {
 #pragma unroll
-          for (int cc = 0; cc < NS; ++cc) go[(size_t)cc * GH] = gv[cc];
-        } else {
+        for (int cc = 0; cc < NH; ++cc) smg[(c0h + cc) * 128 + row] = gv[cc];
+        if constexpr (SPLIT) {
+          if (live_row && rg == 2) {
 #pragma unroll
-          for (int cc = 0; cc < NS; ++cc)
+            for (int cc = 0; cc < NH; ++cc) smhn[(c0h + cc) * 32 + rj] = sh[SPLIT ? cc : 0] + bias_hn;
+          }
+        }
+        if (gout && (!SPLIT || rg < 2)) {
+          float* const go = gout + (tb + cb) * GH + r0 + row;
+#pragma unroll
+          for (int cc = 0; cc < NH; ++cc)
             if (cc < nval) go[(size_t)cc * GH] = gv[cc];
         }
       }
     } else {
       // simple RNN: the row is the unit, h = act(x) directly
-      float hv[NS];
+      if (act) {
+        float hv[NH];
 #pragma unroll
-      for (int cc = 0; cc < NS; ++cc) hv[cc] = simple_act<CELL, __nv_bfloat16>(sx[cc]);
-      const size_t b0 = (size_t)me * NS;
-      __nv_bfloat16* const hs = ly.hseq + ((size_t)(t + 1) * B + b0) * H + j0 + row;
-      __nv_bfloat16* const ys = ly.y ? ly.y + (tb + b0) * H + j0 + row : nullptr;
-      __nv_bfloat16* const hTs = (t == T - 1 && ly.hT) ? ly.hT + b0 * H + j0 + row : nullptr;
-      float* const go = gout ? gout + (tb + b0) * GH + r0 + row : nullptr;
+        for (int cc = 0; cc < NH; ++cc) hv[cc] = simple_act<CELL, __nv_bfloat16>(sx[cc]);
+        __nv_bfloat16* const hs = ly.hseq + ((size_t)(t + 1) * B + cb) * H + j0 + row;
+        __nv_bfloat16* const ys = ly.y ? ly.y + (tb + cb) * H + j0 + row : nullptr;
+        __nv_bfloat16* const hTs = (t == T - 1 && ly.hT) ? ly.hT + (size_t)cb * H + j0 + row : nullptr;
+        float* const go = gout ? gout + (tb + cb) * GH + r0 + row : nullptr;
 #pragma unroll
-      for (int cc = 0; cc < NS; ++cc) {
-        if (cc >= nval) break;
-        const __nv_bfloat16 hb = __float2bfloat16_rn(hv[cc]);
-        hs[(size_t)cc * H] = hb;
-        if (ys) ys[(size_t)cc * H] = hb;
-        if (hTs) hTs[(size_t)cc * H] = hb;
-        if (go) go[(size_t)cc * GH] = hv[cc];
+        for (int cc = 0; cc < NH; ++cc) {
+          if (cc >= nval) break;
+          const __nv_bfloat16 hb = __float2bfloat16_rn(hv[cc]);
+          hs[(size_t)cc * H] = hb;
+          if (ys) ys[(size_t)cc * H] = hb;
+          if (hTs) hTs[(size_t)cc * H] = hb;
+          if (go) go[(size_t)cc * GH] = hv[cc];
+        }
       }
     }
     if constexpr (!SIMPLE) {
-      tc::named_bar(1, 128);
-      // ---- cell update of this thread's (unit, batch entry) pairs: unit
-      // j0 + lane, batch column cc = 4 i + warp of the epilogue; arithmetic
-      // first, then the stores, so that the pairs' latencies overlap
-      const int w4 = e >> 5;
+      tc::named_bar(1, 256);
+      // ---- cell update of this thread's (unit, batch column) pairs: unit
+      // j0 + lane, slice column cc = 8 i + w8; arithmetic first, then the
+      // stores, so that the pairs' latencies overlap
       float hv[PP], nv[SPLIT ? PP : 1], hnv[SPLIT ? PP : 1];
-      if constexpr (CELL == LSTM) {
-        if (u == 1) {
 #pragma unroll
-          for (int i = 0; i < PP; ++i) {
-            const float4 g4 = *reinterpret_cast<const float4*>(smg + (4 * i + w4) * 128 + 4 * lane);
-            st[i] = fmaf(g4.y, st[i], g4.x * g4.z);
-            hv[i] = g4.w * tanh_hw(st[i]);
+      for (int i = 0; i < PP; ++i) {
+        const int cc = min(8 * i + w8, NS - 1);  // pairs past the slice compute on column NS-1 and store nothing
+        const float* gr = smg + cc * 128;
+        if constexpr (CELL == LSTM) {
+          float ig, fg, gg, og;
+          if (u == 1) {
+            const float4 g4 = *reinterpret_cast<const float4*>(gr + 4 * lane);
+            ig = g4.x; fg = g4.y; gg = g4.z; og = g4.w;
+          } else {
+            ig = gr[o0]; fg = gr[o1]; gg = gr[o2]; og = gr[o3];
           }
+          st[i] = fmaf(fg, st[i], ig * gg);
+          hv[i] = og * tanh_hw(st[i]);
         } else {
-#pragma unroll
-          for (int i = 0; i < PP; ++i) {
-            const float* gr = smg + (4 * i + w4) * 128;
-            st[i] = fmaf(gr[o1], st[i], gr[o0] * gr[o2]);
-            hv[i] = gr[o3] * tanh_hw(st[i]);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < PP; ++i) {
-          const float* gr = smg + (4 * i + w4) * 128;
           const float r = gr[o0], z = gr[o1], xn = gr[o2];
-          const float hn = smhn[(4 * i + w4) * 32 + lane];
+          const float hn = smhn[cc * 32 + lane];
           const float n = tanh_hw(fmaf(r, hn, xn));
           hv[i] = fmaf(z, st[i] - n, n);  // (1 - z) n + z h_{t-1}
           st[i] = hv[i];
-          nv[i] = n;
-          hnv[i] = hn;
+          nv[SPLIT ? i : 0] = n;
+          hnv[SPLIT ? i : 0] = hn;
         }
       }
-      // stores: column cc of the slice is batch entry me * NS + cc
-      const int bb = me * NS + w4;  // batch entry of pair 0
-      const bool full = me * NS + NS <= B;
+      // stores: slice column cc is batch entry me * NS + cc
+      const int bb = me * NS + w8;  // batch entry of pair 0
+      auto okp = [&](int i) { return 8 * i + w8 < NS && bb + 8 * i < B; };
       const size_t off = (size_t)bb * H + j0 + lane;
       __nv_bfloat16* const hs = ly.hseq + (size_t)(t + 1) * B * H + off;
 #pragma unroll
       for (int i = 0; i < PP; ++i)
-        if (full || bb + 4 * i < B) hs[(size_t)(4 * i) * H] = __float2bfloat16_rn(hv[i]);
+        if (okp(i)) hs[(size_t)(8 * i) * H] = __float2bfloat16_rn(hv[i]);
       if (ly.y) {
         __nv_bfloat16* const ys = ly.y + tb * H + off;
 #pragma unroll
         for (int i = 0; i < PP; ++i)
-          if (full || bb + 4 * i < B) ys[(size_t)(4 * i) * H] = __float2bfloat16_rn(hv[i]);
+          if (okp(i)) ys[(size_t)(8 * i) * H] = __float2bfloat16_rn(hv[i]);
       }
       if (t == T - 1 && ly.hT) {
 #pragma unroll
         for (int i = 0; i < PP; ++i)
-          if (full || bb + 4 * i < B) ly.hT[off + (size_t)(4 * i) * H] = __float2bfloat16_rn(hv[i]);
+          if (okp(i)) ly.hT[off + (size_t)(8 * i) * H] = __float2bfloat16_rn(hv[i]);
       }
       if constexpr (CELL == LSTM) {
         if (ly.c_out) {
           float* const cs = ly.c_out + tb * H + off;
 #pragma unroll
           for (int i = 0; i < PP; ++i)
-            if (full || bb + 4 * i < B) cs[(size_t)(4 * i) * H] = st[i];
+            if (okp(i)) cs[(size_t)(8 * i) * H] = st[i];
         }
         if (t == T - 1 && ly.cT) {
 #pragma unroll
           for (int i = 0; i < PP; ++i)
-            if (full || bb + 4 * i < B) ly.cT[off + (size_t)(4 * i) * H] = st[i];
+            if (okp(i)) ly.cT[off + (size_t)(8 * i) * H] = st[i];
         }
       } else {
         if (gout) {
           float* const gs = gout + (tb + bb) * GH + r0 + o2;
 #pragma unroll
           for (int i = 0; i < PP; ++i)
-            if (full || bb + 4 * i < B) gs[(size_t)(4 * i) * GH] = nv[i];
+            if (okp(i)) gs[(size_t)(8 * i) * GH] = nv[SPLIT ? i : 0];
         }
         if (ly.hn_out) {
           float* const hns = ly.hn_out + tb * H + off;
 #pragma unroll
           for (int i = 0; i < PP; ++i)
-            if (full || bb + 4 * i < B) hns[(size_t)(4 * i) * H] = hnv[i];
+            if (okp(i)) hns[(size_t)(8 * i) * H] = hnv[SPLIT ? i : 0];
         }
       }
     }
     // ---- publish h_t of this CTA's units and batch slice: the readers load
     // it with TMA (async proxy) after acquiring the counter
     tc::fence_proxy_async_global();
-    tc::named_bar(1, 128);
+    tc::named_bar(1, 256);
     if (e == 0 && !(a.test_skip_publish && blockIdx.x == 0 && t == 0))
       red_release_add_u32(a.cnt + (size_t)c.li * T + t, 1u);
   }
@@ -501,10 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(c.tfull + i, 1);
-      tc::mbar_init(c.tempty + i, 4);
+      tc::mbar_init(c.tempty + i, 8);
       tc::mbar_init(c.rbar + i, 1);
     }
-    tc::mbar_init(c.abar, 4);  // the four epilogue warps, once their rows of the weights are in TMEM
+    tc::mbar_init(c.abar, 8);  // the eight epilogue warps, once their share of the weights is in TMEM
     tc::mbar_init(c.dbar, 1);
     *c.abort_flag = 0;
     *c.ep_fail = 0;
@@ -570,12 +567,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tc::mbar_wait(c.full + stage, phase, c.abort_flag, a.err, a.limit_ns)) break;
         tc::fence_after_sync();
         const uint32_t sb0 = tc::smem_addr(smem + a.sm.ring + stage * nkb * RING);
-        for (int kb = 0; kb < nkb; ++kb) {
-          const uint32_t sb = sb0 + (uint32_t)(kb * RING);
+        // descriptors stepped in their 16-byte address field (one 64-k block
+        // of the buffer is RING bytes, one 16-k step 32 bytes; the field
+        // does not carry out for shared-memory addresses), the first MMA
+        // overwriting the accumulator
+        const uint64_t bd0 = tc::sdesc_sw128(sb0, 16, 1024);
+        tc::mma_bf16_ta(d, c.tmem, bd0, idesc, 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16_ta(d, c.tmem + (uint32_t)(kb * 32 + kk * 8), tc::sdesc_sw128(sb + kk * 32, 16, 1024), idesc,
-                            (kb > 0 || kk > 0) ? 1u : 0u);
+        for (int i = 1; i < 4 * 8; ++i) {
+          if (i >= 4 * nkb) break;
+          const int kb = i >> 2, kk = i & 3;
+          tc::mma_bf16_ta(d, c.tmem + (uint32_t)(8 * i), bd0 + (uint64_t)((kb * RING + kk * 32) >> 4), idesc, 1u);
         }
         tc::mma_commit(c.empty + stage);
         if (++stage == (uint32_t)NST) {
@@ -594,15 +596,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int row = (warp & 3) * 32 + lane;
+    const int hf = (warp - 2) >> 2;  // half of the epilogue (two warps per TMEM lane quadrant)
     const int e = threadIdx.x - 64;
     {
-      // this row of the CTA's weight block into TMEM (rows past the block's
-      // gate rows, GRU's last 32, hold zeros)
+      // this row of the CTA's weight block into TMEM, the two halves taking
+      // alternate 32-wide k blocks (rows past the block's gate rows, GRU's
+      // last 32, hold zeros)
       const int G_H = G * a.H;
       const bool live = row < G * UC && r0 + row < G_H;
       const __nv_bfloat16* wrow = (xpart ? ly.Wx : ly.Wh) + (size_t)(r0 + row) * a.H + k0;
       const uint32_t lane_q = static_cast<uint32_t>(row & ~31) << 16;
-      for (int c16 = 0; c16 < a.kc / 32; ++c16) {
+      for (int c16 = hf; c16 < a.kc / 32; c16 += 2) {
         float v[16];
         if (live) {
           const uint4* q = reinterpret_cast<const uint4*>(wrow + c16 * 32);
@@ -625,9 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(c.abar);
     }
-    if (c.ks == 1) epilogue<CELL, N, 1>(a, c, row, e, acc_base);
-    else if (c.ks == 2) epilogue<CELL, N, 2>(a, c, row, e, acc_base);
-    else epilogue<CELL, N, 4>(a, c, row, e, acc_base);
+    if (c.ks == 1) epilogue<CELL, N, 1>(a, c, row, hf, e, acc_base);
+    else if (c.ks == 2) epilogue<CELL, N, 2>(a, c, row, hf, e, acc_base);
+    else epilogue<CELL, N, 4>(a, c, row, hf, e, acc_base);
   }
 
   tc::fence_before_sync();

@@ -62,7 +62,7 @@ struct BwdMaps {
 };
 
 constexpr int kBufs = 2;        // input buffers, one timestep's K chunk each
-constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quadrant)
 constexpr int kUnits = 128;     // hidden units per CTA (TMEM lanes)
 
 // shared memory: input buffers, receive buffers of the reduction, barriers
@@ -102,14 +102,19 @@ struct BRun {
 };
 
 // ---------------------------------------------------------------------------
-// epilogue: thread `row` owns hidden unit j = 128 ub + row (TMEM lane row);
-// this CTA's batch slice is [me*NS, me*NS + NS)
+// epilogue: 256 threads in two halves of four warps; thread (row, hf) owns
+// hidden unit j = 128 ub + row (TMEM lane row) for the columns [hf*NH,
+// hf*NH + NH) of this CTA's batch slice [me*NS, me*NS + NS) (NH = NS/2;
+// with NS < 8 the first half takes all of them)
 template <int CELL, int N, int KS>
-__device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc_base) {
+__device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, int hf, uint32_t acc_base) {
   constexpr int G = CellInfo<CELL>::G;
   constexpr int NS = N / KS;
   constexpr int NC4 = NS / 4;
   constexpr int ACC = N < 32 ? 32 : N;
+  constexpr bool TWO = NS >= 8;          // both halves take columns
+  constexpr int NH = TWO ? NS / 2 : NS;  // columns of a half
+  constexpr int NL = NH < 16 ? NH : 16;  // columns per TMEM load
   const StackBwdLayer& ly = a.ly;
   const int T = a.T, B = a.B, H = a.H, GH = G * H, u = a.u_pack;
   const int me = c.me;
@@ -121,12 +126,14 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
   for (int g = 0; g < G; ++g) prow[g] = packed_row(g, j, G, u);
   float4* rbuf = reinterpret_cast<float4*>(c.smem + a.sm.rbuf);
   auto rb_at = [&](int p, int s, int ch) -> float4* { return rbuf + ((p * (KS - 1) + s) * NC4 + ch) * 128; };
-  const int b0 = me * NS;
-  const int nval = min(NS, B - b0);
+  const bool act = TWO || hf == 0;  // this half takes columns
+  const int c0h = hf * NH;          // first slice column of this half
+  const int b0 = me * NS + c0h;     // its first batch entry
+  const int nval = act ? min(NH, B - b0) : 0;
   // carried state: LSTM dc flowing into step s, GRU dh_{s+1} z_{s+1}
-  float carry[NS];
+  float carry[NH];
 #pragma unroll
-  for (int cc = 0; cc < NS; ++cc)
+  for (int cc = 0; cc < NH; ++cc)
     carry[cc] = (CELL == LSTM && ly.dcT && cc < nval) ? ly.dcT[(size_t)(b0 + cc) * H + j] : 0.f;
 
   for (int ti = 0; ti <= T; ++ti) {
@@ -142,12 +149,12 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
     // value selected against 0 right after its load is consumed there):
     // columns past the batch are never stored, step -1 runs no pointwise
     // step, and c_{-1} without c0 is zeroed where it is used.
-    float gv[G][NS], cs[NS], cp[NS], hnv[NS];
-    unsigned short hpr[NS], dyr[NS];
+    float gv[G][NH], cs[NH], cp[NH], hnv[NH];
+    unsigned short hpr[NH], dyr[NH];
     const int sl = s < 0 ? 0 : s;
     const bool cp_zero = CELL == LSTM && sl == 0 && !ly.c0;
 #pragma unroll
-    for (int cc = 0; cc < NS; ++cc) {
+    for (int cc = 0; cc < NH; ++cc) {
       const int b = min(b0 + cc, B - 1);
       const size_t bs = (size_t)sl * B + b;
 #pragma unroll
@@ -163,10 +170,11 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
       if (ly.dy) dyr[cc] = reinterpret_cast<const unsigned short*>(ly.dy)[bs * H + j];
       else dyr[cc] = 0;
     }
-    // ---- accumulator of this step: own batch slice summed, the others sent
-    float sum[NS];
+    // ---- accumulator of this step: this half's columns of every chunk's
+    // slice, its own summed, the others sent to their owners
+    float sum[NH];
 #pragma unroll
-    for (int cc = 0; cc < NS; ++cc) sum[cc] = 0.f;
+    for (int cc = 0; cc < NH; ++cc) sum[cc] = 0.f;
     bool ok;
     {
       int w = 1;
@@ -175,21 +183,25 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
     }
     if (ok) {
       tc::fence_after_sync();
+      if (act) {
 #pragma unroll
-      for (int i = 0; i < N / 16; ++i) {
-        float w[16];
-        tc::tmem_load16(c.tmem + lane_q + acc_base + (uint32_t)(acc * ACC + 16 * i), w);
+        for (int p = 0; p < KS; ++p) {
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          const int col = 16 * i + 4 * g4, p = col / NS, cc = col % NS;
-          if (p == me) {
+          for (int l0 = 0; l0 < NH; l0 += NL) {
+            float w[NL];
+            tc::tmem_load_cols<NL>(c.tmem + lane_q + acc_base + (uint32_t)(acc * ACC + p * NS + c0h + l0), w);
+            if (p == me) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) sum[cc + q] += w[4 * g4 + q];
-          } else if constexpr (KS > 1) {
-            const int slot = me < p ? me : me - 1;
-            const uint32_t prank = (uint32_t)(c.crank - me + p);
-            st_async_v4(tc::mapa(tc::smem_addr(rb_at(par, slot, cc / 4) + row), prank), w + 4 * g4,
-                        tc::mapa(tc::smem_addr(&c.rbar[par]), prank));
+              for (int q = 0; q < NL; ++q) sum[l0 + q] += w[q];
+            } else if constexpr (KS > 1) {
+              const int slot = me < p ? me : me - 1;
+              const uint32_t prank = (uint32_t)(c.crank - me + p);
+              const uint32_t bar = tc::mapa(tc::smem_addr(&c.rbar[par]), prank);
+#pragma unroll
+              for (int q = 0; q < NL / 4; ++q)
+                st_async_v4(tc::mapa(tc::smem_addr(rb_at(par, slot, (c0h + l0) / 4 + q) + row), prank), w + 4 * q,
+                            bar);
+            }
           }
         }
       }
@@ -206,25 +218,27 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
       *c.ep_fail = 1;
       abort_cluster(c.abort_flag, a.cluster);
     }
-    tc::named_bar(1, 128);
+    tc::named_bar(1, 256);
     if (*reinterpret_cast<volatile int*>(c.ep_fail)) break;
+    if (act) {
 #pragma unroll
-    for (int k = 0; k < KS; ++k) {
-      if (k == me) continue;
-      const int slot = k < me ? k : k - 1;
+      for (int k = 0; k < KS; ++k) {
+        if (k == me) continue;
+        const int slot = k < me ? k : k - 1;
 #pragma unroll
-      for (int ch = 0; ch < NC4; ++ch) {
-        const float4 q = rb_at(par, slot, ch)[row];
-        sum[4 * ch] += q.x;
-        sum[4 * ch + 1] += q.y;
-        sum[4 * ch + 2] += q.z;
-        sum[4 * ch + 3] += q.w;
+        for (int q4 = 0; q4 < NH / 4; ++q4) {
+          const float4 q = rb_at(par, slot, c0h / 4 + q4)[row];
+          sum[4 * q4] += q.x;
+          sum[4 * q4 + 1] += q.y;
+          sum[4 * q4 + 2] += q.z;
+          sum[4 * q4 + 3] += q.w;
+        }
       }
     }
     if (s < 0) {
       // ---- dh0 (GRU: plus the carried dh_0 z_0) and dc0
 #pragma unroll
-      for (int cc = 0; cc < NS; ++cc) {
+      for (int cc = 0; cc < NH; ++cc) {
         if (cc >= nval) break;
         const size_t bj = (size_t)(b0 + cc) * H + j;
         if (ly.dh0) ly.dh0[bj] = __float2bfloat16_rn(sum[cc] + (CELL == GRU ? carry[cc] : 0.f));
@@ -233,16 +247,16 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
       break;
     }
     // ---- pointwise step s: the gate gradients of this unit and batch slice
-    float dgx[G][NS], dgh[G][NS], dyv[NS], hp[NS];
+    float dgx[G][NH], dgh[G][NH], dyv[NH], hp[NH];
 #pragma unroll
-    for (int cc = 0; cc < NS; ++cc) {
+    for (int cc = 0; cc < NH; ++cc) {
       dyv[cc] = __uint_as_float((uint32_t)dyr[cc] << 16);
       // the gradient reaching the final state, at the first reverse step only
       if (s == T - 1 && ly.dhT && cc < nval) dyv[cc] += __bfloat162float(ly.dhT[(size_t)(b0 + cc) * H + j]);
       hp[cc] = __uint_as_float((uint32_t)hpr[cc] << 16);
     }
 #pragma unroll
-    for (int cc = 0; cc < NS; ++cc) {
+    for (int cc = 0; cc < NH; ++cc) {
       if constexpr (CELL == LSTM) {
         const float ig = gv[0][cc], fg = gv[1][cc], gg = gv[2][cc], og = gv[3][cc];
         const float d = sum[cc] + dyv[cc];
@@ -271,7 +285,7 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
     // ---- stores, then publish step s of this layer
     const size_t base = ((size_t)s * B + b0) * GH;
 #pragma unroll
-    for (int cc = 0; cc < NS; ++cc) {
+    for (int cc = 0; cc < NH; ++cc) {
       if (cc >= nval) break;
       __nv_bfloat16* gx = ly.dgx + base + (size_t)cc * GH;
       if (CELL == LSTM && u == 1) {
@@ -290,7 +304,7 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, uint32_t acc
       }
     }
     tc::fence_proxy_async_global();
-    tc::named_bar(1, 128);
+    tc::named_bar(1, 256);
     if (threadIdx.x == 64 && !(a.test_skip_publish && blockIdx.x == 0 && ti == 0))
       red_release_add_u32(a.cnt + (size_t)c.li * T + s, 1u);
   }
@@ -362,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(c.tfull + i, 1);
-      tc::mbar_init(c.tempty + i, 4);
+      tc::mbar_init(c.tempty + i, 8);
       tc::mbar_init(c.rbar + i, 1);
     }
-    tc::mbar_init(c.abar, 4);
+    tc::mbar_init(c.abar, 8);
     tc::mbar_init(c.dbar, 1);
     *c.abort_flag = 0;
     *c.ep_fail = 0;
@@ -431,12 +445,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!tc::mbar_wait(c.full + buf, phase, c.abort_flag, a.err, a.limit_ns)) break;
         tc::fence_after_sync();
         const uint32_t sb0 = tc::smem_addr(smem + a.sm.ring + buf * nkb * RING);
-        for (int kb = 0; kb < nkb; ++kb) {
-          const uint32_t sb = sb0 + (uint32_t)(kb * RING);
+        // descriptors stepped in their 16-byte address field (one 64-k block
+        // of the buffer is RING bytes, one 16-k step 32 bytes; the field
+        // does not carry out for shared-memory addresses), the first MMA
+        // overwriting the accumulator
+        const uint64_t bd0 = tc::sdesc_sw128(sb0, 16, 1024);
+        tc::mma_bf16_ta(d, c.tmem, bd0, idesc, 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_bf16_ta(d, c.tmem + (uint32_t)(kb * 32 + kk * 8), tc::sdesc_sw128(sb + kk * 32, 16, 1024), idesc,
-                            (kb > 0 || kk > 0) ? 1u : 0u);
+        for (int i = 1; i < 4 * 8; ++i) {
+          if (i >= 4 * nkb) break;
+          const int kb = i >> 2, kk = i & 3;
+          tc::mma_bf16_ta(d, c.tmem + (uint32_t)(8 * i), bd0 + (uint64_t)((kb * RING + kk * 32) >> 4), idesc, 1u);
         }
         tc::mma_commit(c.empty + buf);
         if (++buf == (uint32_t)NB) {
@@ -454,14 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int row = (warp & 3) * 32 + lane;
+    const int hf = (warp - 2) >> 2;  // half of the epilogue (two warps per TMEM lane quadrant)
     {
       // this unit's column of the chunk's weights into TMEM: A[j][k] =
-      // W[k0 + k][j], two consecutive k per 32-bit column
+      // W[k0 + k][j], two consecutive k per 32-bit column; the two halves
+      // take alternate 32-wide k blocks
       const int j = c.ub * kUnits + row;
       const unsigned short* wcol =
           reinterpret_cast<const unsigned short*>(rec ? ly.Wh : ly.Wx_above) + (size_t)k0 * a.H + j;
       const uint32_t lane_q = static_cast<uint32_t>(row & ~31) << 16;
-      for (int c16 = 0; c16 < a.kc / 32; ++c16) {
+      for (int c16 = hf; c16 < a.kc / 32; c16 += 2) {
         float v[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -478,11 +499,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the geometry keeps 4..16 batch columns per CTA: only those variants exist
     if constexpr (N / 2 <= 16) {
-      if (c.ks == 2) bwd_epilogue<CELL, N, 2>(a, c, row, acc_base);
+      if (c.ks == 2) bwd_epilogue<CELL, N, 2>(a, c, row, hf, acc_base);
     }
-    if (c.ks == 4) bwd_epilogue<CELL, N, 4>(a, c, row, acc_base);
+    if (c.ks == 4) bwd_epilogue<CELL, N, 4>(a, c, row, hf, acc_base);
     if constexpr (N / 8 >= 4) {
-      if (c.ks == 8) bwd_epilogue<CELL, N, 8>(a, c, row, acc_base);
+      if (c.ks == 8) bwd_epilogue<CELL, N, 8>(a, c, row, hf, acc_base);
     }
   }
 

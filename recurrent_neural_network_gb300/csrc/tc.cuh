@@ -308,6 +308,43 @@ __device__ __forceinline__ void tmem_load32x2(uint32_t ta, uint32_t tb, float* v
     vb[i] = __uint_as_float(r[32 + i]);
   }
 }
+// 4 or 8 consecutive 32-bit columns of this warp's lanes (32x32b.x4 / .x8)
+// and the wait, in one asm statement.
+__device__ __forceinline__ void tmem_load4(uint32_t taddr, float* v) {
+  uint32_t r[4];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_load8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+// NC (4, 8 or a multiple of 16) consecutive columns
+template <int NC>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float* v) {
+  if constexpr (NC == 4) {
+    tmem_load4(taddr, v);
+  } else if constexpr (NC == 8) {
+    tmem_load8(taddr, v);
+  } else {
+    static_assert(NC % 16 == 0, "4, 8 or a multiple of 16 columns");
+#pragma unroll
+    for (int i = 0; i < NC / 16; ++i) tmem_load16(taddr + 16 * i, v + 16 * i);
+  }
+}
 // Stores 16 consecutive 32-bit columns of this thread's TMEM lane (32x32b
 // shape, one lane per thread of the warp); tmem_store_wait makes them visible
 // to this thread's later tcgen05.ld.
