@@ -144,6 +144,7 @@ struct rnn_s {
   std::vector<std::pair<int, int>> stack_groups;  // (first layer, layers)
   // persistent stacked backward: groups from the top of the stack down
   int stackb = 0, stackb_plan = 0;
+  int stackb_rec = 0;  // recurrent-only groups: one layer per launch, the layer above's share as a GEMM before it
   std::vector<std::pair<int, int>> stackb_groups;  // (lowest layer, layers), highest group first
   std::vector<int> stackb_budget;                  // CTA budget of each group's geometry
   int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
@@ -364,6 +365,21 @@ int plan_and_layout(rnn_s* h) {
         budgets.push_back(budget);
       }
       top -= nl;
+    }
+    if (!ok) {
+      // the layer above's share does not fit beside the recurrent one (K =
+      // 2 G H): each layer alone with only its recurrent product in the
+      // kernel, the gradient from above computed before it as one GEMM
+      groups.clear();
+      budgets.clear();
+      ok = true;
+      for (int l = L - 1; l >= 0 && ok; --l) {
+        int ctas = 0, b = 0;
+        ok = stack_bwd_check(d.cell, H, B, 1, 1, h->u, sms, &ctas, &b) == RNN_OK;
+        groups.emplace_back(l, 1);
+        budgets.push_back(b);
+      }
+      h->stackb_rec = ok ? 1 : 0;
     }
     if (ok) {
       h->stackb = h->stackb_plan = 1;
@@ -608,6 +624,17 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
   unsigned int* cnt = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
   for (size_t gi = 0; gi < h->stackb_groups.size(); ++gi) {
     const int l0 = h->stackb_groups[gi].first, nl = h->stackb_groups[gi].second;
+    // recurrent-only groups: the gradient reaching this layer's outputs from
+    // the layer above, dGx^{l+1} W_x^{l+1}, as one product over all steps
+    float* dyab = nullptr;
+    if (h->stackb_rec && l0 < L - 1) {
+      dyab = reinterpret_cast<float*>(W + h->wl[l0].dyab);
+      Operand A{R + h->rl[l0 + 1].dgx, GH, 0, T * B, GH};
+      Operand Bx{PW + h->pl[l0 + 1].wx, H, 1, H, GH, 1};
+      Remap none{0, 1, 1, 1};
+      Launch Lg = mk(h, stream, ws, "dx_gemm");
+      RNN_TRY(gemm_f32(Lg, d.mode, A, Bx, T * B, H, GH, dyab, H, nullptr, 0, none, 0));
+    }
     StackBwdArgs sa{};
     sa.budget = h->stackb_budget[gi];
     sa.T = T;
@@ -617,7 +644,7 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
     sa.nl = nl;
     for (int i = 0; i < nl; ++i) {
       const int l = l0 + i;
-      const bool top = l == L - 1;
+      const bool top = l == L - 1 || h->stackb_rec;  // no layer above inside the kernel
       StackBwdLayer& ly = sa.lay[i];
       ly.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
       ly.Wx_above = top ? nullptr : reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l + 1].wx);
@@ -629,7 +656,8 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
       ly.c0 = (lstm && c0) ? c0 + l * BH : nullptr;
       ly.hn = gru ? reinterpret_cast<const float*>(R + h->rl[l].hn) : nullptr;
       ly.hseq = reinterpret_cast<const __nv_bfloat16*>(R + h->rl[l].hseq);
-      ly.dy = top ? static_cast<const __nv_bfloat16*>(dy) : nullptr;
+      ly.dy = l == L - 1 ? dy : dyab;
+      ly.dy_f32 = l == L - 1 ? 0 : 1;
       ly.dhT = dhT ? reinterpret_cast<const __nv_bfloat16*>(static_cast<const char*>(dhT) + l * BH * e) : nullptr;
       ly.dcT = (lstm && dcT) ? dcT + l * BH : nullptr;
       ly.dh0 = dh0 ? reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(dh0) + l * BH * e) : nullptr;
@@ -1274,6 +1302,7 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   };
   if (h->stack) list(groups, sizeof(groups), h->stack_groups);
   if (h->stackb) list(bgroups, sizeof(bgroups), h->stackb_groups);
+  if (h->stackb && h->stackb_rec) strncat(bgroups, "r", sizeof(bgroups) - strlen(bgroups) - 1);
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
            "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d transposed=%d fused_point=%d "

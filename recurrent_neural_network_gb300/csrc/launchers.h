@@ -246,7 +246,9 @@ struct StackBwdLayer {
   const float* c0;                // LSTM [B][H] or null
   const float* hn;                // GRU [T][B][H]
   const __nv_bfloat16* hseq;      // GRU: [T+1][B][H] (h_{s-1} in slot s)
-  const __nv_bfloat16* dy;        // top of the stack: [T][B][H], else null
+  const void* dy;                 // gradient from above [T][B][H]: the user's dy (bf16) at the top of the
+                                  // stack, or (dy_f32) a float gradient computed before the launch, or null
+  int dy_f32;
   const __nv_bfloat16* dhT;       // [B][H] or null
   const float* dcT;               // LSTM [B][H] or null
   __nv_bfloat16* dh0;             // [B][H] or null

@@ -150,7 +150,8 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, int hf, uint
     // columns past the batch are never stored, step -1 runs no pointwise
     // step, and c_{-1} without c0 is zeroed where it is used.
     float gv[G][NH], cs[NH], cp[NH], hnv[NH];
-    unsigned short hpr[NH], dyr[NH];
+    unsigned short hpr[NH];
+    uint32_t dyr[NH];  // the gradient from above as stored: bf16 bits, or float bits with dy_f32
     const int sl = s < 0 ? 0 : s;
     const bool cp_zero = CELL == LSTM && sl == 0 && !ly.c0;
 #pragma unroll
@@ -167,8 +168,19 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, int hf, uint
         hnv[cc] = ly.hn[bs * H + j];
         hpr[cc] = reinterpret_cast<const unsigned short*>(ly.hseq)[bs * H + j];  // slot s holds h_{s-1}
       }
-      if (ly.dy) dyr[cc] = reinterpret_cast<const unsigned short*>(ly.dy)[bs * H + j];
-      else dyr[cc] = 0;
+    }
+    // (one loop per storage type: the branch stays outside the loads)
+    if (!ly.dy) {
+#pragma unroll
+      for (int cc = 0; cc < NH; ++cc) dyr[cc] = 0u;
+    } else if (ly.dy_f32) {
+      const uint32_t* dp = reinterpret_cast<const uint32_t*>(ly.dy) + (size_t)sl * B * H + j;
+#pragma unroll
+      for (int cc = 0; cc < NH; ++cc) dyr[cc] = dp[(size_t)min(b0 + cc, B - 1) * H];
+    } else {
+      const unsigned short* dp = reinterpret_cast<const unsigned short*>(ly.dy) + (size_t)sl * B * H + j;
+#pragma unroll
+      for (int cc = 0; cc < NH; ++cc) dyr[cc] = dp[(size_t)min(b0 + cc, B - 1) * H];
     }
     // ---- accumulator of this step: this half's columns of every chunk's
     // slice, its own summed, the others sent to their owners
@@ -250,7 +262,7 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, int hf, uint
     float dgx[G][NH], dgh[G][NH], dyv[NH], hp[NH];
 #pragma unroll
     for (int cc = 0; cc < NH; ++cc) {
-      dyv[cc] = __uint_as_float((uint32_t)dyr[cc] << 16);
+      dyv[cc] = __uint_as_float(ly.dy_f32 ? dyr[cc] : dyr[cc] << 16);
       // the gradient reaching the final state, at the first reverse step only
       if (s == T - 1 && ly.dhT && cc < nval) dyv[cc] += __bfloat162float(ly.dhT[(size_t)(b0 + cc) * H + j]);
       hp[cc] = __uint_as_float((uint32_t)hpr[cc] << 16);

@@ -36,7 +36,8 @@ STACK_CASES = [
     (0, 4, 9, 64, 512, 512, "0+4", "0+4"),            # LSTM, the 4-layer H=512 B=64 shape, unit 1, N=64
     (0, 2, 7, 9, 40, 256, "0+2", "0+2"),              # ragged batch (N=16), 256-wide K chunks
     (1, 2, 10, 32, 72, 256, "0+2", "0+2"),            # GRU, input and recurrent sums apart; 384-wide bwd chunks
-    (1, 3, 6, 20, 64, 1024, "0+1,1+1,2+1", "-"),      # GRU one layer per launch: a group's input from the previous one
+    (1, 3, 6, 20, 64, 1024, "0+1,1+1,2+1", "2+1,1+1,0+1r"),  # GRU one layer per launch each way; backward
+                                                              # recurrent-only, the layer above's share as a GEMM
     (2, 5, 8, 33, 96, 1024, "0+4,4+1", "1+4,0+1"),    # tanh: 128 units per CTA, two groups each way
     (0, 1, 11, 48, 32, 1024, "0+1", "0+1"),           # one layer, K split in two
 ]

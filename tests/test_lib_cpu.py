@@ -136,7 +136,9 @@ def test_stacked_plan_groups(lib):
     bw = lambda *a, **k: re.search(r"stack_bwd_groups=(\S+)", rnn.RNN(*a, **k).describe()).group(1)
     assert bw(0, 4, 100, 64, 512, 512, 1) == "0+4"
     assert bw(2, 5, 8, 33, 96, 1024, 1) == "1+4,0+1"
-    assert bw(1, 8, 200, 32, 1024, 1024, 1) == "-"        # GRU H=1024: K = 6144 per layer does not fit
+    # GRU H=1024: K = 2 G H = 6144 per layer does not fit beside the layer
+    # above's share: one layer per launch, its recurrent product only ("r")
+    assert bw(1, 8, 200, 32, 1024, 1024, 1) == "7+1,6+1,5+1,4+1,3+1,2+1,1+1,0+1r"
     assert bw(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK_BWD) == "-"
     assert bw(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK) == "-"
     # variable lengths switch the forward to step launches
