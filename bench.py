@@ -20,6 +20,9 @@ exchange step and run one shard per rank.
 
 Besides the headline workload the line carries measured sub-results of the
 other benchmark workloads ("workloads"), each with its roofline fraction.
+Moderate batches (9..64 sequences: the 4-layer H=512 B=64 LSTM and the
+8-layer H=1024 B=32 GRU) run the persistent stacked recurrences, whose plan
+string the sub-result carries.
 """
 from __future__ import annotations
 
@@ -396,13 +399,16 @@ def fp32_peak_tflops(mhz):
     return 152 * 128 * 2 * mhz * 1e6 / 1e12
 
 
-def workload_roofline(wl, ms, pk, persistent):
+def workload_roofline(wl, ms, pk, persistent, stacked=False):
     """Roofline of a whole step: the slower of (a) its GEMM flops at the
     tensor peak (sustained: the step is a long run of kernels; the FFMA peak
     for the fp32 mode) and (b) the recurrent weights it must read, once per
     recurrent step of every layer and direction (forward, and again in the
     backward pass of a training step), from HBM when streamed or from shared
-    memory when the persistent recurrence keeps them on chip."""
+    memory when the persistent recurrence keeps them on chip.  The stacked
+    recurrences keep the weights in tensor memory, the tensor core's own
+    operand store, with no bandwidth bound of their own: their step is held
+    to the tensor peak (the weight bytes are reported as read on chip)."""
     mhz = pk.get("sm_max_mhz", 2070.0)
     fl = step_flops(wl)
     if wl.mode == 1:
@@ -416,6 +422,9 @@ def workload_roofline(wl, ms, pk, persistent):
     t_t = fl / (tpk * 1e12)
     t_w = wbytes / (bw * 1e9)
     sec = ms * 1e-3
+    if stacked:
+        return {"bound": "tensor", "achieved": fl / sec / 1e12, "peak": tpk, "unit": "TFLOP/s", "frac": t_t / sec,
+                "weight_bytes_per_step": wbytes, "weights": "tensor memory (read on chip)", "peak_source": tsrc}
     if t_w > t_t:
         return {"bound": "smem" if persistent else "hbm", "achieved": wbytes / sec / 1e9, "peak": bw, "unit": "GB/s",
                 "frac": t_w / sec, "weight_bytes_per_step": wbytes, "peak_source": bsrc,
@@ -472,10 +481,11 @@ def workload_probe(idx, dev, pk, steps=10, warmup=3):
               for k, nm in enumerate(["fwd", "bwd_data", "bwd_weights"])}
     plan = R.r.describe()
     persistent = "recurrence=persistent" in plan
+    stacked = "recurrence=stacked" in plan
     out = {"ms_per_step": ms, "tflops": step_flops(wl) / (ms * 1e-3) / 1e12,
            "timesteps_per_s": wl.T / (ms * 1e-3), "us_per_timestep": 1e3 * ms / wl.T,
            "training": wl.training, "dtype": "bf16" if wl.mode == 1 else "f32", "plan": plan, "phases_ms": phases,
-           "roofline": workload_roofline(wl, ms, pk, persistent)}
+           "roofline": workload_roofline(wl, ms, pk, persistent, stacked)}
     del R
     torch.cuda.empty_cache()
     return wl.name, out

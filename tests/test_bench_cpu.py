@@ -69,6 +69,15 @@ def test_workload_roofline_streaming_and_persistent():
     assert r.get("tensor_frac", 0) >= 0
 
 
+def test_workload_roofline_stacked_is_tensor_bound():
+    """A stacked recurrence keeps its weights in tensor memory: the step is
+    held to the sustained tensor peak."""
+    wl = synth.WORKLOADS[1]  # 4-layer LSTM H=512 B=64 T=100 training
+    r = bench.workload_roofline(wl, 1.4, PK, persistent=False, stacked=True)
+    assert r["bound"] == "tensor" and r["peak"] == PK["bf16_tflops_sustained"]
+    assert r["frac"] == pytest.approx(bench.step_flops(wl) / (PK["bf16_tflops_sustained"] * 1e12) / 1.4e-3)
+
+
 def test_dp_aggregate_counts_every_rank():
     ms, tflops, w = bench.replica_aggregate(34.0, bench.step_flops(synth.WORKLOADS[3]))
     assert w == 1 and tflops == pytest.approx(41.23168604e12 / 34e-3 / 1e12, rel=1e-6)
