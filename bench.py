@@ -531,21 +531,21 @@ def fp8_stash_probe(dev, pk, steps=5, warmup=2):
 
 
 def sweep(dev, steps=5, warmup=2, cells=(0, 1), batches=(1, 2, 4, 8, 16, 32, 64, 128, 256, 512),
-          widths=(256, 512, 1024, 2048, 4096, 8192)):
-    """Selector sweep: one-layer bf16 training steps (T=16) over batch sizes
-    and widths, timed with the library's own plan and with each recurrence
-    variant forced (persistent, streaming transposed, streaming row-major),
-    one JSON line per shape.  Places the planner's switches (persistent vs
-    streaming, step orientation) and shows how throughput moves with the
-    batch at each width."""
+          widths=(256, 512, 1024, 2048, 4096, 8192), layers=1, T=16):
+    """Selector sweep: bf16 training steps (`layers` layers, T timesteps) over
+    batch sizes and widths, timed with the library's own plan and with each
+    recurrence variant forced (persistent, stacked, streaming transposed,
+    streaming row-major), one JSON line per shape.  Places the planner's
+    switches (persistent / stacked / streaming, step orientation) and shows
+    how throughput moves with the batch at each width."""
     from recurrent_neural_network_gb300 import rnn, synth
-    variants = [("default", 0), ("persistent", rnn.FLAG_FORCE_PERSISTENT),
+    variants = [("default", 0), ("persistent", rnn.FLAG_FORCE_PERSISTENT), ("stacked", rnn.FLAG_FORCE_STACK),
                 ("transposed", rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING),
                 ("row_major", rnn.FLAG_NO_TRANSPOSED | rnn.FLAG_FORCE_STREAMING)]
     for cell in cells:
         for H in widths:
             for B in batches:
-                wl = synth.Workload(name=f"sweep_c{cell}_B{B}_H{H}", cell=cell, layers=1, T=16, B=B, input=H,
+                wl = synth.Workload(name=f"sweep_c{cell}_B{B}_H{H}", cell=cell, layers=layers, T=T, B=B, input=H,
                                     hidden=H, mode=synth.MODE_BF16, forget_bias=1.0, state_std=0.1)
                 res, plan = {}, None
                 for name, fl in variants:
@@ -570,7 +570,7 @@ def sweep(dev, steps=5, warmup=2, cells=(0, 1), batches=(1, 2, 4, 8, 16, 32, 64,
                 fl = step_flops(wl)
                 forced = {k: v for k, v in res.items() if k != "default"}
                 best = min(forced, key=forced.get) if forced else None
-                print(json.dumps({"sweep": {"cell": synth.CELL_NAMES[cell], "L": 1, "T": 16, "B": B, "H": H},
+                print(json.dumps({"sweep": {"cell": synth.CELL_NAMES[cell], "L": layers, "T": T, "B": B, "H": H},
                                   "ms": {k: round(v, 4) for k, v in res.items()},
                                   "tflops": {k: round(fl / (v * 1e-3) / 1e12, 2) for k, v in res.items()},
                                   "best_forced": best, "plan": plan}), flush=True)
@@ -618,6 +618,10 @@ def main():
     ap.add_argument("--chunk", type=int, default=0)
     ap.add_argument("--sweep", action="store_true",
                     help="selector sweep over batch sizes and widths instead of the benchmark line")
+    ap.add_argument("--sweep-shape", default="1,16",
+                    help="layers,timesteps of the sweep's training steps (e.g. 4,100 for the stacked range)")
+    ap.add_argument("--sweep-batches", default="1,2,4,8,16,32,64,128,256,512")
+    ap.add_argument("--sweep-widths", default="256,512,1024,2048,4096,8192")
     ap.add_argument("--ncu-T", type=int, default=2, help="timesteps of the --ncu-steps program")
     ap.add_argument("--ncu-steps", action="store_true",
                     help="one training pass (forward, BPTT, weight gradients) of a one-layer T=2 copy of the "
@@ -626,7 +630,10 @@ def main():
     if args.sweep:
         from recurrent_neural_network_gb300 import build
         build.build()
-        sweep(torch.device("cuda", 0))
+        layers, T = (int(v) for v in args.sweep_shape.split(","))
+        sweep(torch.device("cuda", 0), layers=layers, T=T,
+              batches=tuple(int(v) for v in args.sweep_batches.split(",")),
+              widths=tuple(int(v) for v in args.sweep_widths.split(",")))
         return
     if args.ncu_steps:
         ncu_steps(args)

@@ -226,21 +226,25 @@ int plan_and_layout(rnn_s* h) {
   h->limit_ns = d.timeout_ns > 0 ? (uint64_t)d.timeout_ns : 2000000000ull;
 
   // persistent recurrence for small batches (weights on-chip, one launch per
-  // layer); it runs layer after layer, so it replaces the wavefront.
+  // layer): whether it fits is found here, whether it is taken after the
+  // stacked plans below (it runs layer after layer and replaces the
+  // wavefront; for several layers the stacked recurrences, which overlap the
+  // layers, measured faster).
   // (bidirectional stacks: one launch per direction, the reverse one walking time backwards)
+  bool pfits = false;
+  int p_ctas = 0, p_cl = 0;
   if (d.mode == RNN_MODE_BF16 && !(d.flags & (RNN_FLAG_FORCE_STREAMING | RNN_FLAG_FORCE_STACK))) {
-    int ctas = 0;
-    int cl = 4;  // without a device: the size that co-resides on GB300 for 128 CTAs
-    const bool fits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &ctas, &cl) == RNN_OK
-                                     : (B <= 8 && H % 128 == 0 && H <= (d.cell == RNN_TANH || d.cell == RNN_RELU ? 2048 : 1024));
-    if (fits) {
-      h->persist = 1;
-      h->persist_plan = 1;
-      h->persist_ctas = ctas;
-      h->persist_cl = (d.flags & RNN_FLAG_NO_PERSIST_CLUSTER) ? 0 : cl;
-    }
+    p_cl = 4;  // without a device: the size that co-resides on GB300 for 128 CTAs
+    pfits = h->have_device ? persist_check(d.cell, H, B, h->num_sms, &p_ctas, &p_cl) == RNN_OK
+                           : (B <= 8 && H % 128 == 0 && H <= (d.cell == RNN_TANH || d.cell == RNN_RELU ? 2048 : 1024));
   }
-  if ((d.flags & RNN_FLAG_FORCE_PERSISTENT) && !h->persist) return RNN_ERR_UNSUPPORTED;
+  if ((d.flags & RNN_FLAG_FORCE_PERSISTENT) && !pfits) return RNN_ERR_UNSUPPORTED;
+  const bool persist_first = pfits && ((d.flags & RNN_FLAG_FORCE_PERSISTENT) || L == 1 || h->D == 2);
+  if (persist_first) {
+    h->persist = h->persist_plan = 1;
+    h->persist_ctas = p_ctas;
+    h->persist_cl = (d.flags & RNN_FLAG_NO_PERSIST_CLUSTER) ? 0 : p_cl;
+  }
   // fp8 stash of W_h for the persistent inference recurrence (wider layers on chip)
   if (d.flags & RNN_FLAG_FP8_STASH) {
     if (d.mode != RNN_MODE_BF16 || (d.flags & RNN_FLAG_FORCE_STREAMING)) return RNN_ERR_UNSUPPORTED;
@@ -320,33 +324,46 @@ int plan_and_layout(rnn_s* h) {
   // persistent stacked forward for moderate batches: the layers in groups of
   // up to kStackMaxLayers that fit on the device together
   if (d.mode == RNN_MODE_BF16 && h->D == 1 && !h->persist && B <= 64 &&
-      !(d.flags & (RNN_FLAG_NO_STACK | RNN_FLAG_FORCE_STREAMING)) &&
-      (B > 8 || (d.flags & RNN_FLAG_FORCE_STACK))) {
+      !(d.flags & (RNN_FLAG_NO_STACK | RNN_FLAG_FORCE_STREAMING))) {
     const int sms = h->have_device ? h->num_sms : 0;
     auto fits = [&](int l0, int nl) {
       int ctas = 0;
       return stack_check(d.cell, H, B, nl, l0 == 0 ? 1 : 0, h->u, sms, &ctas) == RNN_OK;
     };
     std::vector<std::pair<int, int>> groups;
-    bool ok = true;
+    bool ok = true, overlap = false;
     for (int l0 = 0; l0 < L && ok;) {
       int nl = 0;
       while (l0 + nl < L && nl < kStackMaxLayers && fits(l0, nl + 1)) ++nl;
       if (nl == 0) ok = false;
       else groups.emplace_back(l0, nl);
+      overlap = overlap || nl > 1;
       l0 += nl;
     }
+    // up to 8 sequences the single-layer persistent recurrence (or the step
+    // launches) keep the forward unless the stacked groups overlap layers
+    // (measured: one-layer groups of LSTM H=1024 at B <= 8 lost to both)
+    if (B <= 8 && !overlap && !(d.flags & RNN_FLAG_FORCE_STACK)) ok = false;
     if (ok) {
       h->stack = h->stack_plan = 1;
       h->stack_groups = groups;
     }
   }
   if ((d.flags & RNN_FLAG_FORCE_STACK) && !h->stack) return RNN_ERR_UNSUPPORTED;
+  if (!h->persist && !h->stack && pfits) {
+    // no stacked plan fits: the single-layer persistent recurrence after all
+    // (layer after layer, no wavefront)
+    h->persist = h->persist_plan = 1;
+    h->persist_ctas = p_ctas;
+    h->persist_cl = (d.flags & RNN_FLAG_NO_PERSIST_CLUSTER) ? 0 : p_cl;
+    h->wavefront = 0;
+    h->chunk = T;
+    h->nch = 1;
+  }
   // persistent stacked backward, same batch range: groups of up to
   // kStackMaxLayers layers from the top of the stack down
-  if (d.mode == RNN_MODE_BF16 && h->D == 1 && !h->persist && B <= 64 &&
-      !(d.flags & (RNN_FLAG_NO_STACK | RNN_FLAG_NO_STACK_BWD | RNN_FLAG_FORCE_STREAMING)) &&
-      (B > 8 || (d.flags & RNN_FLAG_FORCE_STACK))) {
+  if (d.mode == RNN_MODE_BF16 && h->D == 1 && B <= 64 &&
+      !(d.flags & (RNN_FLAG_NO_STACK | RNN_FLAG_NO_STACK_BWD | RNN_FLAG_FORCE_STREAMING | RNN_FLAG_FORCE_PERSISTENT))) {
     const int sms = h->have_device ? h->num_sms : 0;
     std::vector<std::pair<int, int>> groups;
     std::vector<int> budgets;

@@ -553,7 +553,9 @@ int bwd_geometry(int cell, int H, int B, int nl, int has_top, int budget, BGeom*
   if (nl < 1 || nl > kStackMaxLayers || B < 1 || B > 64 || H % kUnits) return RNN_ERR_UNSUPPORTED;
   const int G = cell == LSTM ? 4 : cell == GRU ? 3 : 1;
   const int GH = G * H;
-  g->N = B <= 16 ? 16 : B <= 32 ? 32 : 64;
+  // at least 32 batch columns: eight K chunks then still leave each CTA 4
+  // columns of the reduction (the columns past the batch compute on zeros)
+  g->N = B <= 32 ? 32 : 64;
   const int acc_cols = 2 * (g->N < 32 ? 32 : g->N);
   auto valid = [&](int l, int kc) {
     if (kc % 64 || GH % kc || kc / 2 + acc_cols > 512 || kc > 512) return false;
