@@ -131,6 +131,11 @@ enum {
                                           launch, 9..64 sequences) fits; RNN_FLAG_NO_STACK turns off both */
 #define RNN_FLAG_FORCE_STACK 0x20000u /* use the persistent stacked forward recurrence (also for B <= 8, in
                                          place of the single-layer persistent recurrence) or fail */
+#define RNN_FLAG_SLIM_STEP 0x80000u /* bf16 LSTM, transposed steps, more than 128 sequences: run the forward
+                                       steps on a kernel with three pipeline stages and one tensor-memory
+                                       accumulator (97.5 KB of shared memory, 256 TMEM columns), so that a
+                                       CTA of another layer's step can share each SM and stream its weights
+                                       while this one runs its epilogue */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrences one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */

@@ -137,6 +137,7 @@ struct rnn_s {
   int persist_cl = 0;                 // persistent hand-off: cluster size of the tagged-word exchange, 0 = counters
   int persist8 = 0, persist8_cl = 0;  // fp8 stash (RNN_FLAG_FP8_STASH): persistent inference on e4m3 W_h
   int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
+  int slim_step = 0;  // 1: transposed LSTM forward steps on the shared-SM kernel (three stages, one accumulator)
   // persistent stacked forward (9..64 sequences): groups of up to
   // kStackMaxLayers layers, each group one launch; stack_plan is the plan's
   // choice, stack what the current lengths allow (variable lengths: off)
@@ -286,6 +287,7 @@ int plan_and_layout(rnn_s* h) {
   if ((d.flags & RNN_FLAG_FORCE_TRANSPOSED) && !h->tstep) return RNN_ERR_UNSUPPORTED;
   if (h->tstep) {
     h->u = 1;
+    h->slim_step = (d.cell == RNN_LSTM && B > 128 && (d.flags & RNN_FLAG_SLIM_STEP)) ? 1 : 0;
     // backward: 128-unit x bn-batch tiles, K split in clusters of a power of
     // two that the K blocks fill exactly, until the step covers the SMs
     h->bwd_bn = B > 128 ? 256 : B > 64 ? 128 : 64;
@@ -898,6 +900,7 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
         a.hT = (fin && hT) ? static_cast<char*>(hT) + (size_t)v * BH * e : nullptr;
         a.cT = (fin && cT && lstm) ? cT + (size_t)v * BH : nullptr;
         a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[v].hn) + (size_t)t * BH : nullptr;
+        a.slim = h->slim_step;
         Operand A{a.h_prev, H, 0, Bs, H};
         Operand Bw{PW + h->pl[v].wh, H, 0, GH, H, 1};
         Launch Lk = mk(h, s, ws, "fwd_step");
@@ -1323,11 +1326,11 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
            "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d transposed=%d fused_point=%d "
-           "persist_cluster=%d directions=%d fp8_stash=%d stack_groups=%s stack_bwd_groups=%s",
+           "persist_cluster=%d directions=%d fp8_stash=%d stack_groups=%s stack_bwd_groups=%s slim_step=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
            h->persist ? "persistent" : h->stack ? "stacked" : "streaming", h->d.mode ? "tcgen05" : "ffma",
            h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->num_sms, h->tstep, h->bwd_fuse,
-           h->persist ? h->persist_cl : 0, h->D, h->persist8, groups, bgroups);
+           h->persist ? h->persist_cl : 0, h->D, h->persist8, groups, bgroups, h->slim_step);
   return RNN_OK;
 }
 
@@ -1485,6 +1488,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
             a.hT = (!h->varlen && t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
             a.cT = (!h->varlen && t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
             a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
+            a.slim = h->slim_step;
                 Operand A{hseq + (size_t)t * BH * e, H, 0, Bs, H};
             Operand Bw{PW + h->pl[l].wh, H, 0, GH, H, 1};
             Launch Lk = mk(h, s, ws, "fwd_step");

@@ -443,15 +443,22 @@ template <int BN, int STAGES>
 __host__ __device__ constexpr int smem_bytes() { return STAGES * stage_bytes<BN>() + 1024 + 512; }
 }  // namespace tce2
 
-template <int BN, int STAGES, class Epi>
-__global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
+// ACCS = 2: two TMEM accumulators (the next tile's MMAs overlap this tile's
+// epilogue; a CTA with a single tile stages its epilogue's inputs in the
+// second).  ACCS = 1: one accumulator of BN columns and occupancy 2, for
+// kernels small enough in shared memory that a second CTA (of another launch)
+// shares the SM and streams its operands while this one runs its epilogue;
+// two such CTAs fill the SM's 512 TMEM columns exactly.
+template <int BN, int STAGES, class Epi, int ACCS = 2>
+__global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 : 1)
     tc_gemm2_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                     const GemmGeom g, const __grid_constant__ Epi epi) {
   using namespace tce2;
   constexpr int STAGE = stage_bytes<BN>();
-  constexpr uint32_t TMEM_COLS = tce::tmem_cols<BN>();
+  constexpr uint32_t TMEM_COLS = ACCS == 1 ? tce::tmem_cols<BN / 2>() : tce::tmem_cols<BN>();
   constexpr int HB = BN / 2;  // B rows per CTA
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=256");
+  static_assert(ACCS == 1 || ACCS == 2, "one or two accumulators");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -623,7 +630,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
         }
         if (!ok) break;
         tc::mma_commit_pair(tfull + acc, pair_mask);
-        acc ^= 1;
+        if (ACCS == 2) acc ^= 1;
         if (acc == 0) aphase ^= 1;
       }
     }
@@ -659,7 +666,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       t.red_done = red_done;
       t.aux = aux;
       epi.prefetch(t, row, BN);
-      if constexpr (EpiStaged<Epi>::value) {
+      if constexpr (EpiStaged<Epi>::value && ACCS == 2) {
         if (solo) epi.stage(t, row, tmem_base + BN + lane_q, BN, stash);
       }
       int ok = 1;
@@ -668,7 +675,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       if (!ok) break;
       tc::fence_after_sync();
       TmemAcc a{tmem_base + acc * BN + lane_q};
-      if constexpr (EpiStaged<Epi>::value) {
+      if constexpr (EpiStaged<Epi>::value && ACCS == 2) {
         if (solo) epi.run_staged(t, row, a, TmemAcc{tmem_base + BN + lane_q}, BN, stash);
         else epi(t, row, a, BN);
       } else {
@@ -677,7 +684,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_remote(te_base + acc * 8);
-      acc ^= 1;
+      if (ACCS == 2) acc ^= 1;
       if (acc == 0) aphase ^= 1;
     }
   }

@@ -754,6 +754,111 @@ struct EpiFwdStepT {
   }
 };
 
+// Forward LSTM step for CTAs that share their SM (one TMEM accumulator, three
+// pipeline stages: a CTA of another launch fits beside it and streams its
+// operands while this one runs its epilogue).  Tile = 128 packed gate rows x
+// bn batch entries.  With no room to stage P in TMEM or whole output tiles
+// in shared memory, each half of the epilogue warps walks its batch columns
+// in slices of 16 through four slots of the freed pipeline buffers: a bulk
+// tensor load brings the slice's P [16][128] into a slot three slices ahead
+// of its use, the gates are activated in place, the cell update writes c and
+// h beside them, and bulk tensor stores send the slot out while the next
+// slices are computed.  The maps are those of the base with 16-row boxes.
+template <int CELL>
+struct EpiFwdStepTR : EpiFwdStepT<CELL> {
+  static_assert(CELL == LSTM, "the shared-SM step is built for the LSTM cell");
+  using Base = EpiFwdStepT<CELL>;
+  using S = typename Base::S;
+  static constexpr int kWarps = 8;
+  static constexpr int kRows = 16;   // batch entries per slice
+  static constexpr int kSlots = 4;   // per half of the epilogue warps
+  static constexpr int kU = Base::kUnits;
+  static constexpr int kSlotG = kRows * 128 * 4, kSlotC = kRows * kU * 4, kSlotH = kRows * kU * 2;
+  static constexpr int kSlotBytes = kSlotG + kSlotC + kSlotH;
+  static constexpr int kPartBytes = kSlots * kSlotBytes + 128;  // slots, then the slots' barriers
+  int* err;
+  uint64_t limit_ns;
+
+  template <class Acc>
+  __device__ __forceinline__ void operator()(const TileCoord& t, int row, const Acc& acc, int bn) const {
+    const int H = this->H;
+    const int p = t.m0 + row;
+    const bool live = p < 4 * H;
+    const int cw = bn / t.parts, cb = t.part * cw;
+    const int nmax = min(cb + cw, this->B - t.n0);
+    const int nsl = nmax > cb ? (nmax - cb + kRows - 1) / kRows : 0;
+    uint8_t* ring = reinterpret_cast<uint8_t*>(t.red) + (size_t)t.part * kPartBytes;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(ring + kSlots * kSlotBytes);
+    const bool leader = threadIdx.x == 64 + 128 * t.part;
+    const int cx = t.m0 / 4;
+    auto slot_g = [&](int k) { return reinterpret_cast<float*>(ring + (k & (kSlots - 1)) * kSlotBytes); };
+    auto slot_c = [&](int k) { return reinterpret_cast<float*>(ring + (k & (kSlots - 1)) * kSlotBytes + kSlotG); };
+    auto slot_h = [&](int k) { return reinterpret_cast<S*>(ring + (k & (kSlots - 1)) * kSlotBytes + kSlotG + kSlotC); };
+    auto load_p = [&](int k) {
+      tc::mbar_arrive_expect_tx(bar + (k & (kSlots - 1)), kSlotG);
+      tc::tma_load_2d(slot_g(k), &this->map_p, bar + (k & (kSlots - 1)), t.m0, t.n0 + cb + kRows * k);
+    };
+    if (leader) {
+      for (int i = 0; i < kSlots; ++i) tc::mbar_init(bar + i, 1);
+      tc::fence_mbar_init();
+      for (int k = 0; k < kSlots - 1 && k < nsl; ++k) load_p(k);
+    }
+    // c_{t-1} of the next kAhead chunks, in the lane mapping of the cell update
+    constexpr int kAhead = Base::kAhead;
+    float q[kAhead][4];
+#pragma unroll
+    for (int a = 0; a < kAhead; ++a) this->load_cp(t.n0, p, live, cb + kRows * a, nmax, q[a], true);
+    tc::named_bar(2 + t.part, 128);  // the slots' barriers are initialised
+    bool dead = false;
+#pragma unroll 1
+    for (int k = 0; k < nsl; ++k) {
+      const int c = cb + kRows * k;
+      float v[16], cp[4];
+      acc.load16(c, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cp[j] = q[0][j];
+#pragma unroll
+      for (int a = 0; a + 1 < kAhead; ++a)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) q[a][j] = q[a + 1][j];
+      this->load_cp(t.n0, p, live, c + kRows * kAhead, nmax, q[kAhead - 1], true);
+      if (!dead) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!tc::mbar_try_wait(bar + (k & (kSlots - 1)), (uint32_t)((k / kSlots) & 1))) {
+          if (globaltimer_ns() - t0 > limit_ns) {
+            raise_error(err, DEV_TIMEOUT_PIPE);
+            dead = true;
+            break;
+          }
+        }
+      }
+      float* sg = slot_g(k);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] += sg[i * 128 + row];
+      this->finish(t.n0, p, live, 0, min(16, nmax - c), v, cp, row, sg, slot_c(k), slot_h(k));
+      tc::fence_proxy_async_smem();
+      tc::named_bar(2 + t.part, 128);
+      if (leader) {
+        const int y0 = t.n0 + c;
+        if (this->write_gates) tc::tma_store_2d(&this->map_p, sg, t.m0, y0);
+        tc::tma_store_2d(&this->map_c, slot_c(k), cx, y0);
+        if (this->cT) tc::tma_store_2d(&this->map_cT, slot_c(k), cx, y0);
+        tc::tma_store_2d(&this->map_h, slot_h(k), cx, y0);
+        if (this->y) tc::tma_store_2d(&this->map_y, slot_h(k), cx, y0);
+        if (this->hT) tc::tma_store_2d(&this->map_hT, slot_h(k), cx, y0);
+        tc::bulk_commit();
+        // slice k + 3 goes into the slot slice k - 1 was stored from
+        if (k + kSlots - 1 < nsl) {
+          tc::bulk_wait_read<1>();
+          load_p(k + kSlots - 1);
+        }
+      }
+    }
+    // the slots must outlive the stores' reads
+    if (leader) tc::bulk_wait_read_all();
+  }
+};
+
 // Backward step product, tile = 128 hidden units x bn batch entries:
 // acc[j][b] = (W_h^T dG_{s+1}^T)[j][b] = dh_s[b][j] before the gradient from
 // above is added.  The epilogue only stores dh (fp32 [B][H]; bf16 dh0 for

@@ -165,7 +165,7 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
 // the K splits of a tile run as one cluster of 2*splits CTAs (pairs at ranks
 // 2i, 2i+1) and reduce through distributed shared memory (the epilogue must
 // support it); RNN_ERR_UNSUPPORTED when the split cannot be laid out so.
-template <int BN, int STAGES, class Epi>
+template <int BN, int STAGES, class Epi, int ACCS = 2>
 int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, int max_ctas,
                const Epi& epi, int splits = 1) {
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
@@ -194,7 +194,7 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   g.cluster = g.splits;
   g.nfast = g.n_tiles < g.m_tiles ? 1 : 0;  // as in launch_tc
   constexpr int smem = tce2::smem_bytes<BN, STAGES>();
-  auto kern = tc_gemm2_kernel<BN, STAGES, Epi>;
+  auto kern = tc_gemm2_kernel<BN, STAGES, Epi, ACCS>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -83,6 +83,7 @@ struct FwdStepArgs {
   void* hT;
   float* cT;
   float* hn_out;
+  int slim = 0;  // transposed LSTM steps over more than 128 sequences: the shared-SM kernel
 };
 // one forward timestep of one layer: A = h_{t-1} [B][H], B = packed W_h [G*H][H]
 int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, const FwdStepArgs& a);

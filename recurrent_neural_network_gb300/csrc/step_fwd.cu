@@ -98,6 +98,22 @@ EpiFwdStepT<CELL> make_epi_t(const FwdStepArgs& a, int bn) {
   e.tma_out = rc == RNN_OK ? 1 : 0;
   return e;
 }
+
+// the shared-SM variant: the same fields, every map with 16-row boxes
+int make_epi_tr(const Launch& L, const FwdStepArgs& a, EpiFwdStepTR<LSTM>* e) {
+  std::memset(e, 0, sizeof(*e));
+  static_cast<EpiFwdStepT<LSTM>&>(*e) = make_epi_t<LSTM>(a, 256);
+  constexpr int rows = EpiFwdStepTR<LSTM>::kRows, ku = EpiFwdStepTR<LSTM>::kU;
+  int rc = encode_plain(&e->map_p, a.P, 4, a.B, 4LL * a.H, 4LL * a.H, 128, rows);
+  if (!rc) rc = encode_plain(&e->map_c, a.c_out, 4, a.B, a.H, a.H, ku, rows);
+  if (!rc && a.cT) rc = encode_plain(&e->map_cT, a.cT, 4, a.B, a.H, a.H, ku, rows);
+  if (!rc) rc = encode_plain(&e->map_h, a.h_out, 2, a.B, a.H, a.H, ku, rows);
+  if (!rc && a.y) rc = encode_plain(&e->map_y, a.y, 2, a.B, a.H, a.H, ku, rows);
+  if (!rc && a.hT) rc = encode_plain(&e->map_hT, a.hT, 2, a.B, a.H, a.H, ku, rows);
+  e->err = L.err;
+  e->limit_ns = L.limit_ns;
+  return rc;
+}
 }  // namespace
 
 int fwd_step_t(const Launch& L, int cell, const Operand& Wh, const Operand& Hp, const FwdStepArgs& a) {
@@ -109,6 +125,17 @@ int fwd_step_t(const Launch& L, int cell, const Operand& Wh, const Operand& Hp, 
   if (cell == LSTM) return launch_tc2<BN_, ST>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, BN_));      \
   if (cell == RELU) return launch_tc2<BN_, ST>(L, Wh, Hp, M, N, K, 0, make_epi_t<RELU>(a, BN_));      \
   return launch_tc2<BN_, ST>(L, Wh, Hp, M, N, K, 0, make_epi_t<TANH>(a, BN_));
+  if (N > 128 && cell == LSTM && a.slim) {
+    // three stages and one accumulator: 97.5 KB of shared memory and 256 TMEM
+    // columns, so that a CTA of another launch (the next layer's step) fits
+    // beside each of these
+    static_assert(tce2::smem_bytes<256, 3>() + 1024 <= (227 * 1024) / 2, "two CTAs per SM");
+    static_assert(2 * EpiFwdStepTR<LSTM>::kPartBytes <= 3 * tce2::stage_bytes<256>(), "slots in the stages");
+    EpiFwdStepTR<LSTM> e;
+    const int rc = make_epi_tr(L, a, &e);
+    if (rc) return rc;
+    return launch_tc2<256, 3, EpiFwdStepTR<LSTM>, 1>(L, Wh, Hp, M, N, K, 0, e);
+  }
   if (N > 128) {
     RNN_STEP_T(256, 6)
   }

@@ -367,6 +367,31 @@ def test_fused_pointwise_equals_separate_kernel(B):
     compare(wl, a, run_oracle(hi))
 
 
+SLIM = [dict(layers=2, T=5, B=256, hidden=256), dict(layers=2, T=4, B=200, hidden=384),
+        dict(layers=1, T=3, B=129, hidden=128), dict(layers=2, T=4, B=256, hidden=256, training=False)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kw", SLIM, ids=["B256_H256", "B200_H384", "B129_H128", "B256_H256_infer"])
+def test_slim_forward_step_equals_standard(kw):
+    """RNN_FLAG_SLIM_STEP: the transposed LSTM forward step on the shared-SM
+    kernel (three stages, one TMEM accumulator; P brought in and gates, c and
+    h sent out by 16-row bulk copies through a ring of slots) does the same
+    arithmetic in the same order as the standard step: bit-identical outputs
+    and gradients (ragged last slices included), and the oracle's."""
+    wl = tiny(0, synth.MODE_BF16, **kw)
+    train = kw.get("training", True)
+    hi = runner.HostInputs(wl, with_state_grads=train)
+    fl = rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING
+    assert "slim_step=1" in runner.Runner(wl, flags=fl | rnn.FLAG_SLIM_STEP).r.describe()
+    a = run_gpu(wl, hi, flags=fl | rnn.FLAG_SLIM_STEP)
+    b = run_gpu(wl, hi, flags=fl)
+    for k in b:
+        if b[k] is not None:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    compare(wl, a, run_oracle(hi, train=train))
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("flags,B", [(rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_TRANSPOSED, 33),
                                      (rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING, 33),
