@@ -604,6 +604,20 @@ def ncu_steps(args):
     print(json.dumps({"ncu_steps": wl.name, "plan": R.r.describe()}))
 
 
+def one_step(args):
+    """One direct training step (forward, BPTT, weight gradients) of workload
+    --config with its default plan, after packing the weights: the launch
+    list of a profiler run over it is one step's kernels.  Prints the device
+    status word (0, or the error code a kernel recorded) and the plan."""
+    from recurrent_neural_network_gb300 import build, rnn, synth
+    build.build()
+    wl = synth.WORKLOADS[args.config]
+    R = make_runner(wl, torch.device("cuda", 0), flags=args.flags | rnn.FLAG_NO_GRAPH, chunk=args.chunk)
+    R.step()
+    torch.cuda.synchronize()
+    print(json.dumps({"one_step": wl.name, "status": R.status(), "plan": R.r.describe()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -622,6 +636,8 @@ def main():
                     help="layers,timesteps of the sweep's training steps (e.g. 4,100 for the stacked range)")
     ap.add_argument("--sweep-batches", default="1,2,4,8,16,32,64,128,256,512")
     ap.add_argument("--sweep-widths", default="256,512,1024,2048,4096,8192")
+    ap.add_argument("--one-step", action="store_true",
+                    help="one direct training step of the --config workload (packing included), for launch lists")
     ap.add_argument("--ncu-T", type=int, default=2, help="timesteps of the --ncu-steps program")
     ap.add_argument("--ncu-steps", action="store_true",
                     help="one training pass (forward, BPTT, weight gradients) of a one-layer T=2 copy of the "
@@ -637,6 +653,9 @@ def main():
         return
     if args.ncu_steps:
         ncu_steps(args)
+        return
+    if args.one_step:
+        one_step(args)
         return
 
     from recurrent_neural_network_gb300 import synth

@@ -94,9 +94,11 @@ enum {
 #define RNN_FLAG_NO_GRAPH 0x40u         /* enqueue kernels directly; by default a call whose pointers were
                                            seen before replays a cached CUDA graph of its launches */
 #define RNN_FLAG_NO_PDL 0x80u          /* launch every kernel after the previous one on its stream has
-                                           finished; by default the tensor-core kernels of a call start
-                                           while their predecessor drains (programmatic dependent launch)
-                                           and load the packed weights before they wait on it */
+                                           finished; by default, where one stream carries the call's
+                                           launches (one layer, or RNN_FLAG_NO_WAVEFRONT), the tensor-core
+                                           kernels start while their predecessor drains (programmatic
+                                           dependent launch) and load the packed weights before they wait
+                                           on it; the layer wavefront's streams launch without it */
 #define RNN_FLAG_NO_TRANSPOSED 0x200u   /* keep the recurrent steps in the h W_h^T orientation */
 #define RNN_FLAG_FORCE_TRANSPOSED 0x400u /* take the recurrent steps as W_h h^T (bf16 LSTM / simple RNN,
                                             B <= 256, H % 32 == 0) or fail; by default chosen where it

@@ -513,8 +513,14 @@ Launch mk(rnn_s* h, cudaStream_t s, void* ws, const char* name) {
   L.prof = (h->d.flags & RNN_FLAG_PROFILE) ? h->prof : nullptr;
   L.name = name;
   L.pair = (h->d.flags & RNN_FLAG_NO_PAIR) ? 0 : 1;
-  // per-kernel event timing needs each kernel to start after the previous one
-  L.pdl = (h->d.flags & (RNN_FLAG_NO_PDL | RNN_FLAG_PROFILE)) ? 0 : 1;
+  // per-kernel event timing needs each kernel to start after the previous one.
+  // A programmatic dependent launch lets the next kernel on a stream take
+  // SMs while the previous one drains; in the layer wavefront of the step
+  // launches another layer's kernel can use them instead, which measured
+  // faster (4-layer LSTM H=4096 B=256 training step: 33.6 ms without, 34.1
+  // ms with, three alternating runs each), so only a single stream of
+  // launches (one layer, or the wavefront off) is launched dependently.
+  L.pdl = ((h->d.flags & (RNN_FLAG_NO_PDL | RNN_FLAG_PROFILE)) || (h->wavefront && !h->stack)) ? 0 : 1;
   return L;
 }
 

@@ -284,13 +284,15 @@ def test_graph_capture_and_replay_match_direct_calls(flags, kw):
 @pytest.mark.parametrize("kw", [dict(layers=3, T=7, B=9, hidden=256), dict(layers=2, T=5, B=200, hidden=256)],
                          ids=["one_cta", "pairs"])
 def test_dependent_launch_matches_serialised_launches(cell, kw):
-    """Programmatic dependent launch (the default) lets each tensor-core kernel
-    start and load its weights while the previous one drains; the results are
+    """Programmatic dependent launch (the default on a single stream of
+    launches: here the wavefront is off) lets each tensor-core kernel start
+    and load its weights while the previous one drains; the results are
     bit-identical to launches that each wait for their predecessor."""
     wl = tiny(cell, synth.MODE_BF16, **kw)
     hi = runner.HostInputs(wl, with_state_grads=True)
-    a = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_STREAMING)
-    b = run_gpu(wl, hi, flags=rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_PDL)
+    fl = rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_WAVEFRONT
+    a = run_gpu(wl, hi, flags=fl)
+    b = run_gpu(wl, hi, flags=fl | rnn.FLAG_NO_PDL)
     for k in b:
         if b[k] is not None:
             np.testing.assert_array_equal(a[k], b[k], err_msg=k)
