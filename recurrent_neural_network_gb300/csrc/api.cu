@@ -328,9 +328,10 @@ int plan_and_layout(rnn_s* h) {
   if (d.mode == RNN_MODE_BF16 && h->D == 1 && !h->persist && B <= 64 &&
       !(d.flags & (RNN_FLAG_NO_STACK | RNN_FLAG_FORCE_STREAMING))) {
     const int sms = h->have_device ? h->num_sms : 0;
+    int wide = 0;  // the last group checked needs chunks wider than TMEM holds
     auto fits = [&](int l0, int nl) {
       int ctas = 0;
-      return stack_check(d.cell, H, B, nl, l0 == 0 ? 1 : 0, h->u, sms, &ctas) == RNN_OK;
+      return stack_check(d.cell, H, B, nl, l0 == 0 ? 1 : 0, h->u, sms, &ctas, &wide) == RNN_OK;
     };
     std::vector<std::pair<int, int>> groups;
     bool ok = true, overlap = false;
@@ -339,12 +340,17 @@ int plan_and_layout(rnn_s* h) {
       while (l0 + nl < L && nl < kStackMaxLayers && fits(l0, nl + 1)) ++nl;
       if (nl == 0) ok = false;
       else groups.emplace_back(l0, nl);
-      overlap = overlap || nl > 1;
+      if (nl > 1) {
+        fits(l0, nl);
+        overlap = overlap || !wide;
+      }
       l0 += nl;
     }
     // up to 8 sequences the single-layer persistent recurrence (or the step
-    // launches) keep the forward unless the stacked groups overlap layers
-    // (measured: one-layer groups of LSTM H=1024 at B <= 8 lost to both)
+    // launches) keep the forward unless a stacked group overlaps layers on
+    // chunks that fit TMEM (measured at B <= 8, LSTM and GRU H=1024, 4
+    // layers: one-layer groups and two-layer groups on widened chunks both
+    // lost to the persistent forward; H <= 512 four-layer groups won 5-6x)
     if (B <= 8 && !overlap && !(d.flags & RNN_FLAG_FORCE_STACK)) ok = false;
     if (ok) {
       h->stack = h->stack_plan = 1;

@@ -208,7 +208,7 @@ struct StackLayer {
   int wait_in;              // 1: the input is produced by the previous layer of this launch
 };
 struct StackSmem {
-  int stages, ring, rbuf, smg, smhn, bars;
+  int stages, a, ring, rbuf, smg, smhn, bars;
 };
 struct StackArgs {
   int T, B, H, u_pack;
@@ -221,6 +221,7 @@ struct StackArgs {
   // geometry (filled by stack_fwd)
   int cluster;
   int kcl[kStackMaxLayers];  // K chunk width of each layer's CTAs
+  int kctl[kStackMaxLayers]; // the first kctl of it in tensor memory, the rest (if any) in shared memory
   int ks[kStackMaxLayers], kcx[kStackMaxLayers], cta0[kStackMaxLayers + 1], ctas[kStackMaxLayers];
   StackSmem sm;
 };
@@ -228,7 +229,9 @@ struct StackArgs {
 // device (first_p: the first of them reads a precomputed input projection;
 // u_pack: the packing unit); *ctas receives the grid size.  num_sms <= 0:
 // host-side planning for GB300 without a device query.
-int stack_check(int cell, int H, int B, int nl, int first_p, int u_pack, int num_sms, int* ctas);
+// *wide (optional) is set to 1 when some layer needs K chunks wider than
+// TMEM holds beside the accumulators (part of its weights in shared memory).
+int stack_check(int cell, int H, int B, int nl, int first_p, int u_pack, int num_sms, int* ctas, int* wide = nullptr);
 int stack_fwd(const Launch& L, int cell, const StackArgs& a);
 
 // Persistent backward-through-time of up to kStackMaxLayers stacked layers in

@@ -81,17 +81,18 @@ constexpr int kMaxStages = 4;  // input buffers, one timestep's K chunk each
 constexpr int kThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quadrant)
 
 // Shared-memory layout of a CTA (offsets from the 1024-aligned base): the
+// weights beyond what TMEM holds (kcs k of the 128 rows, 128-byte-swizzled
+// K-major blocks of 128 x 64, the A operand of the MMAs that read it), the
 // ring of input buffers (kc / 64 blocks of N x 64 bf16 each), the receive
-// buffers of the cross-chunk reduction, the gate tile, barriers.  The
-// weights are in TMEM.
+// buffers of the cross-chunk reduction, the gate tile, barriers.
 struct Smem {
   int a, ring, rbuf, smg, smhn, bars, total, stages;
 };
-__host__ __device__ inline Smem smem_layout(int cell, int N, int kc, int ksmin, int ksmax, int stages) {
+__host__ __device__ inline Smem smem_layout(int cell, int N, int kc, int ksmin, int ksmax, int stages, int kcs = 0) {
   Smem s;
   s.a = 0;
   s.stages = stages;
-  s.ring = 0;
+  s.ring = 128 * kcs * 2;
   s.rbuf = s.ring + stages * (kc / 64) * N * 128;
   // [2][ksmax-1][N/ks/4][128] float4 for the largest ks of the launch (the
   // footprint (ks-1)/ks * N is largest for the largest ks)
@@ -120,7 +121,7 @@ struct Ctx {
 // every iteration (measured: ~150-270 ns per producer, MMA or epilogue
 // iteration before this copy).
 struct Run {
-  int T, B, H, u_pack, kc, cluster, test_skip_publish;
+  int T, B, H, u_pack, kc, kct, cluster, test_skip_publish;
   int* err;
   uint64_t limit_ns;
   unsigned int* cnt;        // [layers][T] counters of the launch
@@ -434,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int G = CellInfo<CELL>::G;
   constexpr int UC = G == 1 ? 128 : 32;
   constexpr int RING = N * 128;
-  constexpr uint32_t TMEM_COLS = 512;  // weights (kc / 2 columns) + two accumulators
+  constexpr uint32_t TMEM_COLS = 512;  // weights (kct / 2 columns) + two accumulators
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -455,6 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   a.H = p.H;
   a.u_pack = p.u_pack;
   a.kc = p.kcl[li];
+  a.kct = p.kctl[li];
   a.cluster = p.cluster;
   a.test_skip_publish = p.test_skip_publish;
   a.err = p.err;
@@ -517,9 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   if (a.cluster > 1) tc::cluster_sync_all();  // every peer's barriers and flags exist before remote traffic
   c.tmem = *tmem_slot;
-  // TMEM columns: [0, kc/2) this CTA's block of weight rows (row i in lane i,
-  // two consecutive k per column), then the two accumulators
-  const uint32_t acc_base = (uint32_t)(a.kc / 2);
+  // TMEM columns: [0, kct/2) this CTA's block of weight rows (row i in lane
+  // i, two consecutive k per column), then the two accumulators; k from kct
+  // to kc (if any) in shared memory
+  const uint32_t acc_base = (uint32_t)(a.kct / 2);
 
   int last_par[kMaxStages];  // producer: parity of the last load issued into each buffer (-1: none)
   for (int s = 0; s < kMaxStages; ++s) last_par[s] = -1;
@@ -556,6 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16(128, N, 0, 0);
+      const int nkt = a.kct / 64;
+      const uint64_t ad0 = tc::sdesc_sw128(tc::smem_addr(smem + a.sm.a), 16, 1024);
       bool ok = tc::mbar_wait(c.abar, 0, c.abort_flag, a.err, a.limit_ns);
       tc::fence_after_sync();
       uint32_t stage = 0, phase = 0;
@@ -574,10 +579,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd0 = tc::sdesc_sw128(sb0, 16, 1024);
         tc::mma_bf16_ta(d, c.tmem, bd0, idesc, 0u);
 #pragma unroll
-        for (int i = 1; i < 4 * 8; ++i) {
-          if (i >= 4 * nkb) break;
+        for (int i = 1; i < 4 * 14; ++i) {
+          if (i >= 4 * nkt) break;
           const int kb = i >> 2, kk = i & 3;
           tc::mma_bf16_ta(d, c.tmem + (uint32_t)(8 * i), bd0 + (uint64_t)((kb * RING + kk * 32) >> 4), idesc, 1u);
+        }
+        // the k blocks past kct: A from the swizzled blocks in shared memory
+        for (int i = 0; i < 4 * (nkb - nkt); ++i) {
+          const int kb = nkt + (i >> 2), kk = i & 3;
+          tc::mma_bf16(d, ad0 + (uint64_t)(((i >> 2) * 16384 + kk * 32) >> 4),
+                       bd0 + (uint64_t)((kb * RING + kk * 32) >> 4), idesc, 1u);
         }
         tc::mma_commit(c.empty + stage);
         if (++stage == (uint32_t)NST) {
@@ -606,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = row < G * UC && r0 + row < G_H;
       const __nv_bfloat16* wrow = (xpart ? ly.Wx : ly.Wh) + (size_t)(r0 + row) * a.H + k0;
       const uint32_t lane_q = static_cast<uint32_t>(row & ~31) << 16;
-      for (int c16 = hf; c16 < a.kc / 32; c16 += 2) {
+      for (int c16 = hf; c16 < a.kct / 32; c16 += 2) {
         float v[16];
         if (live) {
           const uint4* q = reinterpret_cast<const uint4*>(wrow + c16 * 32);
@@ -624,6 +635,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tmem_store16(c.tmem + lane_q + (uint32_t)(c16 * 16), v);
       }
+      // k past kct into shared memory as K-major 128 x 64 blocks with the
+      // 128-byte swizzle (16-byte piece q of row r at piece q ^ (r % 8)),
+      // the layout a TMA load with that swizzle would write
+      for (int q8 = hf; q8 < (a.kc - a.kct) / 8; q8 += 2) {
+        const uint4 u = live ? *reinterpret_cast<const uint4*>(wrow + a.kct + q8 * 8) : make_uint4(0, 0, 0, 0);
+        const int blk = q8 >> 3, q = q8 & 7;
+        *reinterpret_cast<uint4*>(smem + a.sm.a + blk * 16384 + row * 128 + ((q ^ (row & 7)) << 4)) = u;
+      }
+      tc::fence_proxy_async_smem();  // generic stores read by the tensor core (async proxy)
       tc::tmem_store_wait();
       tc::fence_before_sync();
       __syncwarp();
@@ -658,11 +678,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the stack's layer 0, K = H; the others have K = 2H).  A CTA's epilogue
 // works on N / ks batch columns, and the wavefront moves at the pace of its
 // slowest layer, so chunks are narrowed (512 -> 256) on the layers with the
-// fewest chunks while the CTAs stay within `budget`.
+// fewest chunks while the CTAs stay within `budget`.  Where the group does
+// not fit the budget with 512-wide chunks, the layers with the most chunks
+// are widened to 1024 (H a multiple of 1024): such a chunk keeps what fits
+// beside the accumulators in TMEM (kct) and the rest in shared memory.
 struct Geom {
   int N, cluster, ctas;
-  int kc[kStackMaxLayers], ks[kStackMaxLayers], kcx[kStackMaxLayers], cta0[kStackMaxLayers + 1],
-      lctas[kStackMaxLayers];
+  int kc[kStackMaxLayers], kct[kStackMaxLayers], ks[kStackMaxLayers], kcx[kStackMaxLayers],
+      cta0[kStackMaxLayers + 1], lctas[kStackMaxLayers];
   Smem sm;
 };
 
@@ -673,9 +696,12 @@ int geometry(int cell, int H, int B, int nl, int first_p, int budget, Geom* g) {
   if (H % uc || H % 256) return RNN_ERR_UNSUPPORTED;
   g->N = B <= 16 ? 16 : B <= 32 ? 32 : 64;
   const int rbs = H / uc;
+  // TMEM columns beside two accumulators of N (at least 32) columns: two k per column
+  const int kt_max = 2 * (512 - 2 * (g->N < 32 ? 32 : g->N));
   auto set = [&](int l, int kc) {
     const bool p = l == 0 && first_p;
     g->kc[l] = kc;
+    g->kct[l] = std::min(kc, kt_max / 64 * 64);
     g->kcx[l] = p ? 0 : H / kc;  // layers above the first: input width H
     g->ks[l] = g->kcx[l] + H / kc;
   };
@@ -686,6 +712,17 @@ int geometry(int cell, int H, int B, int nl, int first_p, int budget, Geom* g) {
     if (g->N / g->ks[l] < 4) return RNN_ERR_UNSUPPORTED;
     cta += rbs * g->ks[l];
   }
+  // widen the layers with the most chunks while the group exceeds the budget
+  while (cta > budget && H % 1024 == 0) {
+    int kmax = 0, lw = -1;
+    for (int l = 0; l < nl; ++l)
+      if (g->kc[l] == 512 && g->ks[l] > kmax) kmax = g->ks[l], lw = l;
+    if (lw < 0) break;
+    cta -= rbs * g->ks[lw];
+    set(lw, 1024);
+    cta += rbs * g->ks[lw];
+  }
+  if (cta > budget) return RNN_ERR_LAUNCH;
   // narrow the chunks of every layer that has the fewest, while they fit
   for (;;) {
     int kmin = 8;
@@ -702,12 +739,13 @@ int geometry(int cell, int H, int B, int nl, int first_p, int budget, Geom* g) {
       if (g->ks[l] == kmin) set(l, 256);
     cta += extra;
   }
-  int ksmax = 1, ksmin = 4, kcmax = 0;
+  int ksmax = 1, ksmin = 4, kcmax = 0, kcsmax = 0;
   cta = 0;
   for (int l = 0; l < nl; ++l) {
     ksmax = std::max(ksmax, g->ks[l]);
     ksmin = std::min(ksmin, g->ks[l]);
     kcmax = std::max(kcmax, g->kc[l]);
+    kcsmax = std::max(kcsmax, g->kc[l] - g->kct[l]);
     g->cta0[l] = cta;
     g->lctas[l] = rbs * g->ks[l];
     cta += g->lctas[l];
@@ -721,7 +759,7 @@ int geometry(int cell, int H, int B, int nl, int first_p, int budget, Geom* g) {
   // loads the next step while this one computes)
   bool fit = false;
   for (int st : {2, 1}) {
-    g->sm = smem_layout(cell, g->N, kcmax, ksmin, ksmax, st);
+    g->sm = smem_layout(cell, g->N, kcmax, ksmin, ksmax, st, kcsmax);
     if (g->sm.total + 1024 <= 227 * 1024) {
       fit = true;
       break;
@@ -798,9 +836,12 @@ int dispatch(const Launch& L, int cell, const StackMaps& maps, const StackArgs& 
 
 }  // namespace
 
-int stack_check(int cell, int H, int B, int nl, int first_p, int u_pack, int num_sms, int* ctas) {
+int stack_check(int cell, int H, int B, int nl, int first_p, int u_pack, int num_sms, int* ctas, int* wide) {
   Geom g;
+  if (wide) *wide = 0;
   RNN_TRY_LOCAL(geometry(cell, H, B, nl, first_p, num_sms > 0 ? num_sms : 152, &g));
+  if (wide)
+    for (int l = 0; l < nl; ++l) *wide |= g.kc[l] > g.kct[l] ? 1 : 0;
   const int uc = cell == LSTM || cell == GRU ? 32 : 128;
   if (u_pack < 1 || uc % u_pack) return RNN_ERR_UNSUPPORTED;
   if (ctas) *ctas = g.ctas;
@@ -819,6 +860,7 @@ int stack_fwd(const Launch& L, int cell, const StackArgs& in) {
   a.cluster = g.cluster;
   for (int l = 0; l < in.nl; ++l) {
     a.kcl[l] = g.kc[l];
+    a.kctl[l] = g.kct[l];
     a.ks[l] = g.ks[l];
     a.kcx[l] = g.kcx[l];
     a.cta0[l] = g.cta0[l];
@@ -826,6 +868,7 @@ int stack_fwd(const Launch& L, int cell, const StackArgs& in) {
   }
   a.cta0[in.nl] = g.cta0[in.nl];
   a.sm.stages = g.sm.stages;
+  a.sm.a = g.sm.a;
   a.sm.ring = g.sm.ring;
   a.sm.rbuf = g.sm.rbuf;
   a.sm.smg = g.sm.smg;

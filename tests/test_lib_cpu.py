@@ -82,8 +82,8 @@ def test_calls_validate_arguments_before_any_device_work(lib):
 
 
 def test_persistent_plan_selection(lib):
-    # small batch, supported width: persistent, no wavefront
-    assert "recurrence=persistent" in rnn.RNN(0, 2, 10, 4, 64, 1024, 1).describe()
+    # small batch, supported width, one layer: persistent, no wavefront
+    assert "recurrence=persistent" in rnn.RNN(0, 1, 10, 4, 64, 1024, 1).describe()
     assert "recurrence=streaming" in rnn.RNN(0, 2, 10, 4, 64, 1024, 1, flags=rnn.FLAG_FORCE_STREAMING).describe()
     assert "recurrence=persistent" not in rnn.RNN(0, 2, 10, 64, 64, 1024, 1).describe()
     with pytest.raises(rnn.RnnError) as e:
@@ -115,13 +115,21 @@ def test_stacked_plan_groups(lib):
         return re.search(r"recurrence=(\w+)", d).group(1), re.search(r"stack_groups=(\S+)", d).group(1)
     # 4-layer LSTM H=512 B=64: 16 + 3 x 32 CTAs, one launch
     assert plan(0, 4, 100, 64, 512, 512, 1) == ("stacked", "0+4")
-    # 8-layer GRU H=1024 B=32: layer 0 64 CTAs, the others 128: one layer per launch
-    assert plan(1, 8, 200, 32, 1024, 1024, 1) == ("stacked", "0+1,1+1,2+1,3+1,4+1,5+1,6+1,7+1")
+    # 8-layer GRU H=1024 B=32: on 512-wide chunks layer 0 takes 64 CTAs and the
+    # others 128 each; the higher layers of a pair widen to 1024-wide chunks
+    # (64 CTAs; 896 k in TMEM, 128 in shared memory): two layers per launch
+    assert plan(1, 8, 200, 32, 1024, 1024, 1) == ("stacked", "0+2,2+2,4+2,6+2")
+    # B = 33..64 at H = 1024: the widened chunks do not fit shared memory, one layer per launch
+    assert plan(1, 4, 100, 48, 1024, 1024, 1) == ("stacked", "0+1,1+1,2+1,3+1")
     # tanh H=1024 B=32: 8 + 16 + 16 + 16 + 16 CTAs -> 4 + 1
     assert plan(2, 5, 20, 32, 64, 1024, 1) == ("stacked", "0+4,4+1")
-    # B <= 8 keeps the single-layer persistent recurrence unless forced
-    assert plan(0, 2, 10, 4, 64, 1024, 1)[0] == "persistent"
-    assert plan(0, 2, 10, 4, 64, 1024, 1, flags=rnn.FLAG_FORCE_STACK)[0] == "stacked"
+    # B <= 8: the single-layer persistent recurrence keeps the forward unless
+    # forced or a stacked group holds several layers on chunks that fit TMEM
+    assert plan(0, 1, 10, 4, 64, 1024, 1)[0] == "persistent"
+    assert plan(0, 1, 10, 4, 64, 1024, 1, flags=rnn.FLAG_FORCE_STACK)[0] == "stacked"
+    assert plan(0, 2, 10, 4, 64, 1024, 1)[0] == "persistent"  # two layers only on widened chunks
+    assert plan(0, 2, 10, 4, 64, 1024, 1, flags=rnn.FLAG_FORCE_STACK) == ("stacked", "0+2")
+    assert plan(0, 4, 100, 8, 512, 512, 1) == ("stacked", "0+4")
     # off: flag, streaming forced, wider batches, fp32, bidirectional, H not a multiple of 256
     assert plan(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK)[0] == "streaming"
     assert plan(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_FORCE_STREAMING)[0] == "streaming"
