@@ -145,7 +145,7 @@ struct rnn_s {
   std::vector<std::pair<int, int>> stack_groups;  // (first layer, layers)
   // persistent stacked backward: groups from the top of the stack down
   int stackb = 0, stackb_plan = 0;
-  int stackb_rec = 0;  // recurrent-only groups: one layer per launch, the layer above's share as a GEMM before it
+  int stackb_rec = 0;  // recurrent-only tops: each group's top layer without the share from above, which a GEMM computes before the group
   std::vector<std::pair<int, int>> stackb_groups;  // (lowest layer, layers), highest group first
   std::vector<int> stackb_budget;                  // CTA budget of each group's geometry
   int bwd_fuse = 0;   // transposed LSTM: the pointwise BPTT step runs inside the product's epilogue
@@ -391,20 +391,36 @@ int plan_and_layout(rnn_s* h) {
       }
       top -= nl;
     }
-    if (!ok) {
-      // the layer above's share does not fit beside the recurrent one (K =
-      // 2 G H): each layer alone with only its recurrent product in the
-      // kernel, the gradient from above computed before it as one GEMM
-      groups.clear();
-      budgets.clear();
-      ok = true;
-      for (int l = L - 1; l >= 0 && ok; --l) {
+    // Recurrent-only tops: each group's top layer runs only its recurrent
+    // product in the kernel, the gradient from the layer above (computed by
+    // the group before) entering as one GEMM over all steps; the layers below
+    // it in the group take the share from above in the kernel as usual.  It
+    // needs fewer CTAs where the share from above does not fit beside the
+    // recurrent one (K = 2 G H); taken when the full groups do not fit or
+    // it makes fewer groups.
+    std::vector<std::pair<int, int>> rgroups;
+    std::vector<int> rbudgets;
+    bool rok = true;
+    for (int top = L - 1; top >= 0 && rok;) {
+      int nl = 0, budget = 0;
+      while (top - nl >= 0 && nl < kStackMaxLayers) {
         int ctas = 0, b = 0;
-        ok = stack_bwd_check(d.cell, H, B, 1, 1, h->u, sms, &ctas, &b) == RNN_OK;
-        groups.emplace_back(l, 1);
-        budgets.push_back(b);
+        if (stack_bwd_check(d.cell, H, B, nl + 1, 1, h->u, sms, &ctas, &b) != RNN_OK) break;
+        ++nl;
+        budget = b;
       }
-      h->stackb_rec = ok ? 1 : 0;
+      if (nl == 0) rok = false;
+      else {
+        rgroups.emplace_back(top - nl + 1, nl);
+        rbudgets.push_back(budget);
+      }
+      top -= nl;
+    }
+    if (rok && (!ok || rgroups.size() < groups.size())) {
+      groups = rgroups;
+      budgets = rbudgets;
+      ok = true;
+      h->stackb_rec = 1;
     }
     if (ok) {
       h->stackb = h->stackb_plan = 1;
@@ -657,11 +673,12 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
     const int l0 = h->stackb_groups[gi].first, nl = h->stackb_groups[gi].second;
     // recurrent-only groups: the gradient reaching this layer's outputs from
     // the layer above, dGx^{l+1} W_x^{l+1}, as one product over all steps
+    const int lt = l0 + nl - 1;  // the group's top layer
     float* dyab = nullptr;
-    if (h->stackb_rec && l0 < L - 1) {
-      dyab = reinterpret_cast<float*>(W + h->wl[l0].dyab);
-      Operand A{R + h->rl[l0 + 1].dgx, GH, 0, T * B, GH};
-      Operand Bx{PW + h->pl[l0 + 1].wx, H, 1, H, GH, 1};
+    if (h->stackb_rec && lt < L - 1) {
+      dyab = reinterpret_cast<float*>(W + h->wl[lt].dyab);
+      Operand A{R + h->rl[lt + 1].dgx, GH, 0, T * B, GH};
+      Operand Bx{PW + h->pl[lt + 1].wx, H, 1, H, GH, 1};
       Remap none{0, 1, 1, 1};
       Launch Lg = mk(h, stream, ws, "dx_gemm");
       RNN_TRY(gemm_f32(Lg, d.mode, A, Bx, T * B, H, GH, dyab, H, nullptr, 0, none, 0));
@@ -675,7 +692,7 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
     sa.nl = nl;
     for (int i = 0; i < nl; ++i) {
       const int l = l0 + i;
-      const bool top = l == L - 1 || h->stackb_rec;  // no layer above inside the kernel
+      const bool top = l == L - 1 || (h->stackb_rec && l == lt);  // no layer above inside the kernel
       StackBwdLayer& ly = sa.lay[i];
       ly.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
       ly.Wx_above = top ? nullptr : reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l + 1].wx);
@@ -687,7 +704,7 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
       ly.c0 = (lstm && c0) ? c0 + l * BH : nullptr;
       ly.hn = gru ? reinterpret_cast<const float*>(R + h->rl[l].hn) : nullptr;
       ly.hseq = reinterpret_cast<const __nv_bfloat16*>(R + h->rl[l].hseq);
-      ly.dy = l == L - 1 ? dy : dyab;
+      ly.dy = l == L - 1 ? dy : l == lt ? dyab : nullptr;
       ly.dy_f32 = l == L - 1 ? 0 : 1;
       ly.dhT = dhT ? reinterpret_cast<const __nv_bfloat16*>(static_cast<const char*>(dhT) + l * BH * e) : nullptr;
       ly.dcT = (lstm && dcT) ? dcT + l * BH : nullptr;

@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bd0 = tc::sdesc_sw128(sb0, 16, 1024);
         tc::mma_bf16_ta(d, c.tmem, bd0, idesc, 0u);
 #pragma unroll
-        for (int i = 1; i < 4 * 8; ++i) {
+        for (int i = 1; i < 4 * 14; ++i) {
           if (i >= 4 * nkb) break;
           const int kb = i >> 2, kk = i & 3;
           tc::mma_bf16_ta(d, c.tmem + (uint32_t)(8 * i), bd0 + (uint64_t)((kb * RING + kk * 32) >> 4), idesc, 1u);
@@ -557,8 +557,9 @@ int bwd_geometry(int cell, int H, int B, int nl, int has_top, int budget, BGeom*
   // columns of the reduction (the columns past the batch compute on zeros)
   g->N = B <= 32 ? 32 : 64;
   const int acc_cols = 2 * (g->N < 32 ? 32 : g->N);
+  const int kt_max = 2 * (512 - acc_cols);  // k that fit TMEM beside the two accumulators
   auto valid = [&](int l, int kc) {
-    if (kc % 64 || GH % kc || kc / 2 + acc_cols > 512 || kc > 512) return false;
+    if (kc % 64 || GH % kc || kc > kt_max) return false;
     const int parts = (has_top && l == nl - 1) ? 1 : 2;
     const int ks = parts * (GH / kc);
     return (ks == 2 || ks == 4 || ks == 8) && g->N / ks >= 4 && g->N / ks <= 16;
@@ -571,12 +572,26 @@ int bwd_geometry(int cell, int H, int B, int nl, int has_top, int budget, BGeom*
   const int rbs = H / kUnits;
   int cta = 0;
   for (int l = 0; l < nl; ++l) {
+    // the widest chunk of at most 512, else the narrowest wider one
     int kc = 0;
     for (int c = 512; c >= 64 && !kc; c -= 64)
+      if (valid(l, c)) kc = c;
+    for (int c = 576; c <= kt_max && !kc; c += 64)
       if (valid(l, c)) kc = c;
     if (!kc) return RNN_ERR_UNSUPPORTED;
     set(l, kc);
     cta += rbs * g->ks[l];
+  }
+  // over the budget: widen (kc -> 2 kc, halving ks) the layer with the most
+  // chunks that can be widened, while any can
+  while (cta > budget) {
+    int lw = -1;
+    for (int l = 0; l < nl; ++l)
+      if (valid(l, 2 * g->kc[l]) && (lw < 0 || g->ks[l] > g->ks[lw])) lw = l;
+    if (lw < 0) break;
+    cta -= rbs * g->ks[lw];
+    set(lw, 2 * g->kc[lw]);
+    cta += rbs * g->ks[lw];
   }
   // narrow the layers with the fewest chunks (kc -> kc / 2, doubling ks)
   for (;;) {
@@ -701,6 +716,8 @@ int stack_bwd_check(int cell, int H, int B, int nl, int has_top, int u_pack, int
       StackBwdArgs a{};
       Launch L{};
       rc = dispatch(L, cell, maps, a, g, true, num_sms);
+    } else if (g.cluster == 8 && g.ctas > 14 * 8) {
+      rc = RNN_ERR_LAUNCH;  // host-side planning: GB300 held 14 clusters of 8 of this kernel at once, not 16
     }
     if (rc == RNN_OK) {
       if (ctas) *ctas = g.ctas;

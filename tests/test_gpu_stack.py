@@ -36,10 +36,11 @@ STACK_CASES = [
     (0, 4, 9, 64, 512, 512, "0+4", "0+4"),            # LSTM, the 4-layer H=512 B=64 shape, unit 1, N=64
     (0, 2, 7, 9, 40, 256, "0+2", "0+2"),              # ragged batch (N=16), 256-wide K chunks
     (1, 2, 10, 32, 72, 256, "0+2", "0+2"),            # GRU, input and recurrent sums apart; 384-wide bwd chunks
-    (1, 3, 6, 20, 64, 1024, "0+2,2+1", "2+1,1+1,0+1r"),  # GRU: two layers in the first forward launch, layer 1
-                                                          # on 1024-wide chunks (896 k in TMEM, 128 in shared
-                                                          # memory); backward recurrent-only, one layer per
-                                                          # launch, the layer above's share as a GEMM
+    (1, 3, 6, 20, 64, 1024, "0+2,2+1", "1+2,0+1"),  # GRU: two layers in the first forward launch, layer 1
+                                                     # on 1024-wide chunks (896 k in TMEM, 128 in shared
+                                                     # memory); backward on 768-wide chunks
+    (1, 5, 6, 24, 64, 1024, "0+2,2+2,4+1", "3+2,1+2,0+1r"),  # GRU backward with recurrent-only group tops:
+                                                              # the share from above of layers 4 and 2 by GEMM
     (0, 4, 5, 32, 48, 1024, "0+2,2+2", "3+1,2+1,1+1,0+1r"),  # LSTM: 1024-wide chunks split between TMEM and
                                                               # shared memory in both forward launches
     (1, 2, 7, 12, 64, 1024, "0+2", "1+1,0+1r"),       # GRU, N=16, ragged batch on the split chunks

@@ -140,13 +140,17 @@ def test_stacked_plan_groups(lib):
     with pytest.raises(rnn.RnnError):
         rnn.RNN(0, 2, 10, 32, 64, 320, 1, flags=rnn.FLAG_FORCE_STACK)
     # the backward, highest group first (host planning for GB300: clusters
-    # of up to 8 CTAs, at most 152 CTAs per launch)
+    # of up to 8 CTAs, at most 152 CTAs per launch and 14 clusters of 8)
     bw = lambda *a, **k: re.search(r"stack_bwd_groups=(\S+)", rnn.RNN(*a, **k).describe()).group(1)
     assert bw(0, 4, 100, 64, 512, 512, 1) == "0+4"
     assert bw(2, 5, 8, 33, 96, 1024, 1) == "1+4,0+1"
-    # GRU H=1024: K = 2 G H = 6144 per layer does not fit beside the layer
-    # above's share: one layer per launch, its recurrent product only ("r")
-    assert bw(1, 8, 200, 32, 1024, 1024, 1) == "7+1,6+1,5+1,4+1,3+1,2+1,1+1,0+1r"
+    # GRU H=1024: a layer with the share from above (K = 2 G H = 6144, 768-wide
+    # chunks) takes 64 CTAs, two of them 16 clusters of 8, which do not fit;
+    # with each group's top layer on its recurrent product only ("r": 32
+    # CTAs, the share from above computed by a GEMM) two layers per launch
+    assert bw(1, 8, 200, 32, 1024, 1024, 1) == "6+2,4+2,2+2,0+2r"
+    # LSTM H=1024: the lower layer's K = 8192 needs chunks wider than TMEM holds
+    assert bw(0, 4, 100, 32, 1024, 1024, 1) == "3+1,2+1,1+1,0+1r"
     assert bw(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK_BWD) == "-"
     assert bw(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK) == "-"
     # variable lengths switch the forward to step launches
