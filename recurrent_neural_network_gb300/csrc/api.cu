@@ -644,6 +644,17 @@ int run_graphed(rnn_s* h, cudaStream_t user, const std::vector<uintptr_t>& key, 
 
 int cu(cudaError_t e) { return e == cudaSuccess ? RNN_OK : RNN_ERR_CUDA; }
 
+// Copies and zero fills inside a call run as kernels on the call's stream
+// (dev_copy, dev_zero): never as copy-engine operations, which would wait
+// behind a large transfer the caller keeps on a copy engine.
+int zero_async(rnn_s* h, void* p, size_t n, cudaStream_t s) { return dev_zero(mk(h, s, nullptr, "fill"), p, n); }
+int copy_async(rnn_s* h, void* d, const void* src, size_t n, cudaStream_t s) {
+  return dev_copy(mk(h, s, nullptr, "copy"), d, src, n);
+}
+int copy2d_async(rnn_s* h, void* d, size_t dp, const void* src, size_t sp, size_t w, size_t rows, cudaStream_t s) {
+  return dev_copy2d(mk(h, s, nullptr, "copy"), d, dp, src, sp, w, rows);
+}
+
 // ---------------------------------------------------------------- bidirectional stacks
 // Every layer has a forward (d = 0) and a reverse (d = 1) direction with their
 // own weights, v = 2 l + d.  Both keep their h sequence in time order: the
@@ -712,7 +723,7 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
       ly.dc0 = (lstm && dc0) ? dc0 + l * BH : nullptr;
       ly.wait_above = i + 1 < nl ? 1 : 0;
     }
-    RNN_TRY(cu(cudaMemsetAsync(cnt, 0, (size_t)nl * T * 4, stream)));
+    RNN_TRY(zero_async(h, cnt, (size_t)nl * T * 4, stream));
     sa.cnt = cnt;
     sa.err = reinterpret_cast<int*>(W + h->ws_err);
     sa.limit_ns = h->limit_ns;
@@ -761,9 +772,8 @@ int fwd_stack(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
     for (int i = 0; i < nl; ++i) {
       const int l = l0 + i;
       char* hs = hseq_of(l);
-      if (h0) RNN_TRY(cu(cudaMemcpyAsync(hs, static_cast<const char*>(h0) + l * BH * e, BH * e,
-                                         cudaMemcpyDeviceToDevice, stream)));
-      else RNN_TRY(cu(cudaMemsetAsync(hs, 0, BH * e, stream)));
+      if (h0) RNN_TRY(copy_async(h, hs, static_cast<const char*>(h0) + l * BH * e, BH * e, stream));
+      else RNN_TRY(zero_async(h, hs, BH * e, stream));
       StackLayer& ly = sa.lay[i];
       ly.Wx = l > 0 ? reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wx) : nullptr;
       ly.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
@@ -782,7 +792,7 @@ int fwd_stack(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
       ly.In = l > 0 ? H : d.input;
       ly.wait_in = i > 0 ? 1 : 0;
     }
-    RNN_TRY(cu(cudaMemsetAsync(cnt, 0, (size_t)nl * T * 4, stream)));
+    RNN_TRY(zero_async(h, cnt, (size_t)nl * T * 4, stream));
     sa.cnt = cnt;
     sa.err = reinterpret_cast<int*>(W + h->ws_err);
     sa.limit_ns = h->limit_ns;
@@ -816,8 +826,8 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
   const bool vl = h->varlen != 0;
   auto Bt = [&](int t) { return vl ? h->Bt[t] : (t < T ? B : 0); };
   if (vl) {
-    RNN_TRY(cu(cudaMemsetAsync(y, 0, (size_t)T * BH * 2 * e, caller)));
-    for (int v = 0; v < 2 * L; ++v) RNN_TRY(cu(cudaMemsetAsync(hseq_of(v), 0, (size_t)(T + 1) * BH * e, caller)));
+    RNN_TRY(zero_async(h, y, (size_t)T * BH * 2 * e, caller));
+    for (int v = 0; v < 2 * L; ++v) RNN_TRY(zero_async(h, hseq_of(v), (size_t)(T + 1) * BH * e, caller));
   }
   for (int l = 0; l < L; ++l) {
     if (side) RNN_TRY(fork_streams(h, caller));
@@ -828,10 +838,9 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
       float* P = reinterpret_cast<float*>(train ? R + h->rl[v].gates : W + h->wl[v].P);
       char* hinit = hseq + hslot(dd, dd == 0 ? -1 : T) * BH * e;
       if (h0)
-        RNN_TRY(cu(cudaMemcpyAsync(hinit, static_cast<const char*>(h0) + v * BH * e, BH * e, cudaMemcpyDeviceToDevice,
-                                   s)));
+        RNN_TRY(copy_async(h, hinit, static_cast<const char*>(h0) + v * BH * e, BH * e, s));
       else
-        RNN_TRY(cu(cudaMemsetAsync(hinit, 0, BH * e, s)));
+        RNN_TRY(zero_async(h, hinit, BH * e, s));
       // input projection over all T (layer >= 1: one product per half of the input)
       const float* bias = reinterpret_cast<const float*>(PW + h->pl[v].bias);
       if (l == 0) {
@@ -855,8 +864,8 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
       if (pers) {
         // all T steps of this direction in one launch
         unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
-        if (pa_cluster(h, p8)) RNN_TRY(cu(cudaMemsetAsync(W + h->ws_hx, 0, (size_t)8 * B * H, s)));
-        else RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
+        if (pa_cluster(h, p8)) RNN_TRY(zero_async(h, W + h->ws_hx, (size_t)8 * B * H, s));
+        else RNN_TRY(zero_async(h, arrive, (size_t)T * 4, s));
         PersistArgs pa{};
         pa.arrive = arrive;
         pa.cluster = pa_cluster(h, p8);
@@ -897,17 +906,15 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
           if (nr > 0) {
             char* hp = hseq + hslot(dd, tp) * BH * e + (size_t)r0 * H * e;
             if (h0)
-              RNN_TRY(cu(cudaMemcpyAsync(hp, static_cast<const char*>(h0) + (v * BH + (size_t)r0 * H) * e,
-                                         (size_t)nr * H * e, cudaMemcpyDeviceToDevice, s)));
+              RNN_TRY(copy_async(h, hp, static_cast<const char*>(h0) + (v * BH + (size_t)r0 * H) * e, (size_t)nr * H * e, s));
             else
-              RNN_TRY(cu(cudaMemsetAsync(hp, 0, (size_t)nr * H * e, s)));
+              RNN_TRY(zero_async(h, hp, (size_t)nr * H * e, s));
             if (lstm) {
               float* cp = cbuf(tp) + (size_t)r0 * H;
               if (c0)
-                RNN_TRY(cu(cudaMemcpyAsync(cp, c0 + v * BH + (size_t)r0 * H, (size_t)nr * H * 4,
-                                           cudaMemcpyDeviceToDevice, s)));
+                RNN_TRY(copy_async(h, cp, c0 + v * BH + (size_t)r0 * H, (size_t)nr * H * 4, s));
               else
-                RNN_TRY(cu(cudaMemsetAsync(cp, 0, (size_t)nr * H * 4, s)));
+                RNN_TRY(zero_async(h, cp, (size_t)nr * H * 4, s));
             }
           }
         }
@@ -939,18 +946,14 @@ int fwd_bidir(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
           // sequences ending at time t (rows Bt[t+1] .. Bs-1): final states
           const int r0 = Bt(t + 1), nr = Bs - r0;
           if (nr > 0 && hT)
-            RNN_TRY(cu(cudaMemcpyAsync(static_cast<char*>(hT) + ((size_t)v * BH + (size_t)r0 * H) * e,
-                                       static_cast<const char*>(a.h_out) + (size_t)r0 * H * e, (size_t)nr * H * e,
-                                       cudaMemcpyDeviceToDevice, s)));
+            RNN_TRY(copy_async(h, static_cast<char*>(hT) + ((size_t)v * BH + (size_t)r0 * H) * e, static_cast<const char*>(a.h_out) + (size_t)r0 * H * e, (size_t)nr * H * e, s));
           if (nr > 0 && cT && lstm)
-            RNN_TRY(cu(cudaMemcpyAsync(cT + (size_t)v * BH + (size_t)r0 * H, a.c_out + (size_t)r0 * H,
-                                       (size_t)nr * H * 4, cudaMemcpyDeviceToDevice, s)));
+            RNN_TRY(copy_async(h, cT + (size_t)v * BH + (size_t)r0 * H, a.c_out + (size_t)r0 * H, (size_t)nr * H * 4, s));
         }
       }
       // the top layer's output y[T][B][2H] = [h_forward(t), h_reverse(t)]
       if (l == L - 1) {
-        RNN_TRY(cu(cudaMemcpy2DAsync(static_cast<char*>(y) + (size_t)dd * H * e, 2 * H * e, hseq + hslot(dd, 0) * BH * e,
-                                     H * e, H * e, (size_t)T * B, cudaMemcpyDeviceToDevice, s)));
+        RNN_TRY(copy2d_async(h, static_cast<char*>(y) + (size_t)dd * H * e, 2 * H * e, hseq + hslot(dd, 0) * BH * e, H * e, H * e, (size_t)T * B, s));
         // the reverse h sequence holds h0 rows where sequences start: y is 0 at idle positions
         if (dd == 1 && vl)
           for (int t = 0; t < T; ++t)
@@ -972,7 +975,7 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
   const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
   const Remap none{0, 1, 1, 1};
   for (int v = 0; v < 2 * L; ++v)
-    RNN_TRY(cu(cudaMemsetAsync(W + h->wl[v].ctr, 0, (size_t)h->ctr_count * 4, s)));
+    RNN_TRY(zero_async(h, W + h->wl[v].ctr, (size_t)h->ctr_count * 4, s));
   // variable lengths: rows 0 .. Bt[t]-1 run at time t; the gate gradients of
   // idle positions are never written, so they start at zero for the products
   // that read every row (dx, dW)
@@ -980,14 +983,12 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
   auto Bt = [&](int t) { return vl ? h->Bt[t] : (t < T ? B : 0); };
   if (vl)
     for (int v = 0; v < 2 * L; ++v) {
-      RNN_TRY(cu(cudaMemsetAsync(R + h->rl[v].dgx, 0, (size_t)T * BGH * e, s)));
-      if (h->rl[v].dgh != h->rl[v].dgx) RNN_TRY(cu(cudaMemsetAsync(R + h->rl[v].dgh, 0, (size_t)T * BGH * e, s)));
+      RNN_TRY(zero_async(h, R + h->rl[v].dgx, (size_t)T * BGH * e, s));
+      if (h->rl[v].dgh != h->rl[v].dgx) RNN_TRY(zero_async(h, R + h->rl[v].dgh, (size_t)T * BGH * e, s));
     }
   // the two halves of dy, each [T][B][H]
   for (int dd = 0; dd < 2; ++dd)
-    RNN_TRY(cu(cudaMemcpy2DAsync(W + h->ws_dtop + (size_t)dd * T * BH * e, H * e,
-                                 static_cast<const char*>(dy) + (size_t)dd * H * e, 2 * H * e, H * e, (size_t)T * B,
-                                 cudaMemcpyDeviceToDevice, s)));
+    RNN_TRY(copy2d_async(h, W + h->ws_dtop + (size_t)dd * T * BH * e, H * e, static_cast<const char*>(dy) + (size_t)dd * H * e, 2 * H * e, H * e, (size_t)T * B, s));
   cudaStream_t caller = s;
   const bool side = !(d.flags & RNN_FLAG_NO_WAVEFRONT);  // directions side by side
   for (int l = L - 1; l >= 0; --l) {
@@ -1002,8 +1003,8 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
       char* hseq = R + h->rl[v].hseq;
       const float* c0v = c0 ? c0 + v * BH : nullptr;
       if (lstm || gru) {
-        if (lstm && dcT) RNN_TRY(cu(cudaMemcpyAsync(carry, dcT + v * BH, BH * 4, cudaMemcpyDeviceToDevice, s)));
-        else RNN_TRY(cu(cudaMemsetAsync(carry, 0, BH * 4, s)));
+        if (lstm && dcT) RNN_TRY(copy_async(h, carry, dcT + v * BH, BH * 4, s));
+        else RNN_TRY(zero_async(h, carry, BH * 4, s));
       }
       // time of the k-th step of this direction's forward pass
       auto time_at = [&](int k) { return dd == 0 ? k : T - 1 - k; };
@@ -1127,8 +1128,7 @@ int bwd_bidir(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
           }
           // the carry out of the sequence's first step is its dc0
           if (nr > 0 && dc0 && lstm)
-            RNN_TRY(cu(cudaMemcpyAsync(dc0 + v * BH + (size_t)r0 * H, carry + (size_t)r0 * H, (size_t)nr * H * 4,
-                                       cudaMemcpyDeviceToDevice, s)));
+            RNN_TRY(copy_async(h, dc0 + v * BH + (size_t)r0 * H, carry + (size_t)r0 * H, (size_t)nr * H * 4, s));
         }
       }
       if (!(dd == 1 && vl) && (dh0 || (dc0 && lstm))) {
@@ -1420,10 +1420,9 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
       // rows past a sequence's end are never written by the steps: y reads 0
       // there, and the h sequences the weight gradients and the next layer
       // read hold zeros instead of stale memory
-      RNN_TRY(cu(cudaMemsetAsync(y, 0, (size_t)T * BH * e, stream)));
+      RNN_TRY(zero_async(h, y, (size_t)T * BH * e, stream));
       for (int l = 0; l < L; ++l)
-        RNN_TRY(cu(cudaMemsetAsync(train ? R + h->rl[l].hseq : W + h->wl[l].hseq, 0, (size_t)(T + 1) * BH * e,
-                                   stream)));
+        RNN_TRY(zero_async(h, train ? R + h->rl[l].hseq : W + h->wl[l].hseq, (size_t)(T + 1) * BH * e, stream));
     }
     if (wf) RNN_TRY(fork_streams(h, stream));
     const int nd = wf ? (L + nch - 1) : 1;
@@ -1436,9 +1435,8 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
           char* hseq = train ? R + h->rl[l].hseq : W + h->wl[l].hseq;
           float* P = reinterpret_cast<float*>(train ? R + h->rl[l].gates : W + h->wl[l].P);
           if (c == 0) {
-            if (h0) RNN_TRY(cu(cudaMemcpyAsync(hseq, static_cast<const char*>(h0) + l * BH * e, BH * e,
-                                               cudaMemcpyDeviceToDevice, s)));
-            else RNN_TRY(cu(cudaMemsetAsync(hseq, 0, BH * e, s)));
+            if (h0) RNN_TRY(copy_async(h, hseq, static_cast<const char*>(h0) + l * BH * e, BH * e, s));
+            else RNN_TRY(zero_async(h, hseq, BH * e, s));
           }
           if (wf && l > 0) RNN_TRY(cu(cudaStreamWaitEvent(s, h->ev[(size_t)(l - 1) * nch + c], 0)));
           // input projection (layer 0: all T at once)
@@ -1462,8 +1460,8 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
           // persistent recurrence: all T steps of the layer in one launch
           if (pers) {
             unsigned int* arrive = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
-            if (pa_cluster(h, p8)) RNN_TRY(cu(cudaMemsetAsync(W + h->ws_hx, 0, (size_t)8 * B * H, s)));
-            else RNN_TRY(cu(cudaMemsetAsync(arrive, 0, (size_t)T * 4, s)));
+            if (pa_cluster(h, p8)) RNN_TRY(zero_async(h, W + h->ws_hx, (size_t)8 * B * H, s));
+            else RNN_TRY(zero_async(h, arrive, (size_t)T * 4, s));
             PersistArgs pa{};
             pa.arrive = arrive;
             pa.cluster = p8 ? h->persist8_cl : h->persist_cl;
@@ -1527,12 +1525,9 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
               // sequences ending at step t (rows Bt[t+1] .. Bt[t]-1): final states
               const int r0 = h->Bt[t + 1], nr = Bs - r0;
               if (nr > 0 && hT)
-                RNN_TRY(cu(cudaMemcpyAsync(static_cast<char*>(hT) + ((size_t)l * BH + (size_t)r0 * H) * e,
-                                           static_cast<const char*>(a.h_out) + (size_t)r0 * H * e, (size_t)nr * H * e,
-                                           cudaMemcpyDeviceToDevice, s)));
+                RNN_TRY(copy_async(h, static_cast<char*>(hT) + ((size_t)l * BH + (size_t)r0 * H) * e, static_cast<const char*>(a.h_out) + (size_t)r0 * H * e, (size_t)nr * H * e, s));
               if (nr > 0 && cT && lstm)
-                RNN_TRY(cu(cudaMemcpyAsync(cT + (size_t)l * BH + (size_t)r0 * H, a.c_out + (size_t)r0 * H,
-                                           (size_t)nr * H * 4, cudaMemcpyDeviceToDevice, s)));
+                RNN_TRY(copy_async(h, cT + (size_t)l * BH + (size_t)r0 * H, a.c_out + (size_t)r0 * H, (size_t)nr * H * 4, s));
             }
           }
           if (wf) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * nch + c], s)));
@@ -1567,14 +1562,14 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
     if (h->stackb && !h->varlen) return bwd_stack(h, dy, dhT, dcT, PW, c0, dx, dh0, dc0, R, W, ws, stream);
 
     for (int l = 0; l < L; ++l)
-      RNN_TRY(cu(cudaMemsetAsync(W + h->wl[l].ctr, 0, (size_t)h->ctr_count * 4, stream)));
+      RNN_TRY(zero_async(h, W + h->wl[l].ctr, (size_t)h->ctr_count * 4, stream));
     if (h->varlen) {
       // gate gradients of finished sequences are never written: zero, so that
       // the products that read every row (dx, dW, the next step) see zeros
       for (int l = 0; l < L; ++l) {
-        RNN_TRY(cu(cudaMemsetAsync(R + h->rl[l].dgx, 0, (size_t)T * BGH * e, stream)));
+        RNN_TRY(zero_async(h, R + h->rl[l].dgx, (size_t)T * BGH * e, stream));
         if (h->rl[l].dgh != h->rl[l].dgx)
-          RNN_TRY(cu(cudaMemsetAsync(R + h->rl[l].dgh, 0, (size_t)T * BGH * e, stream)));
+          RNN_TRY(zero_async(h, R + h->rl[l].dgh, (size_t)T * BGH * e, stream));
       }
     }
     if (h->wavefront) RNN_TRY(fork_streams(h, stream));
@@ -1594,8 +1589,8 @@ int rnn_bwd_data(rnn_handle_t h, const void* dy, const void* dhT, const float* d
           char* hseq = R + h->rl[l].hseq;
           const float* c0l = c0 ? c0 + l * BH : nullptr;
           if (rc == 0 && (lstm || gru)) {
-            if (lstm && dcT) RNN_TRY(cu(cudaMemcpyAsync(carry, dcT + l * BH, BH * 4, cudaMemcpyDeviceToDevice, s)));
-            else RNN_TRY(cu(cudaMemsetAsync(carry, 0, BH * 4, s)));
+            if (lstm && dcT) RNN_TRY(copy_async(h, carry, dcT + l * BH, BH * 4, s));
+            else RNN_TRY(zero_async(h, carry, BH * 4, s));
           }
           auto args_for = [&](int st) {
             BwdStepArgs a;

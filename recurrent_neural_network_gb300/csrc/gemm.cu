@@ -99,6 +99,68 @@ int pack_layer(const Launch& L, int mode, int cell, int H, int In, int u, const 
   return cuda_status(e);
 }
 
+// ---------------------------------------------------------------- device copies and zero fills
+// The copies and fills inside a call run as kernels on the SMs.  As
+// copy-engine operations they would queue behind any large transfer the
+// caller keeps running on a copy engine, e.g. the read-back of the previous
+// step's weight gradients to the host, and hold the whole step up until it
+// has finished.
+namespace {
+template <class V>
+__global__ void copy2d_kernel(const uint8_t* __restrict__ src, size_t spitch, uint8_t* __restrict__ dst,
+                              size_t dpitch, size_t w, size_t rows) {
+  const size_t n = w * rows;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = rows == 1 ? 0 : i / w, c = rows == 1 ? i : i - r * w;
+    reinterpret_cast<V*>(dst + r * dpitch)[c] = reinterpret_cast<const V*>(src + r * spitch)[c];
+  }
+}
+template <class V>
+__global__ void zero_kernel(V* __restrict__ dst, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = V{};
+}
+inline size_t align_of(uintptr_t v) { return v & 15 ? (v & 3 ? 1 : 4) : 16; }
+int grid_for(const Launch& L, size_t n) { return (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, (size_t)L.num_sms * 8)); }
+}  // namespace
+
+int dev_copy2d(const Launch& L, void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, size_t rows) {
+  if (!width || !rows) return RNN_OK;
+  if (!dst || !src) return RNN_ERR_INVALID_ARG;
+  const size_t a = std::min({align_of(reinterpret_cast<uintptr_t>(dst)), align_of(reinterpret_cast<uintptr_t>(src)),
+                             align_of(rows > 1 ? dpitch : 16), align_of(rows > 1 ? spitch : 16), align_of(width)});
+  const uint8_t* s = static_cast<const uint8_t*>(src);
+  uint8_t* d = static_cast<uint8_t*>(dst);
+  launch_begin(L);
+  if (a == 16) {
+    copy2d_kernel<uint4><<<grid_for(L, width / 16 * rows), 256, 0, L.stream>>>(s, spitch, d, dpitch, width / 16, rows);
+  } else if (a == 4) {
+    copy2d_kernel<uint32_t><<<grid_for(L, width / 4 * rows), 256, 0, L.stream>>>(s, spitch, d, dpitch, width / 4, rows);
+  } else {
+    copy2d_kernel<uint8_t><<<grid_for(L, width * rows), 256, 0, L.stream>>>(s, spitch, d, dpitch, width, rows);
+  }
+  const cudaError_t e = cudaGetLastError();
+  launch_end(L);
+  return cuda_status(e);
+}
+
+int dev_copy(const Launch& L, void* dst, const void* src, size_t bytes) {
+  return dev_copy2d(L, dst, bytes, src, bytes, bytes, 1);
+}
+
+int dev_zero(const Launch& L, void* dst, size_t bytes) {
+  if (!bytes) return RNN_OK;
+  if (!dst) return RNN_ERR_INVALID_ARG;
+  const size_t a = std::min(align_of(reinterpret_cast<uintptr_t>(dst)), align_of(bytes));
+  launch_begin(L);
+  if (a == 16) zero_kernel<uint4><<<grid_for(L, bytes / 16), 256, 0, L.stream>>>(static_cast<uint4*>(dst), bytes / 16);
+  else if (a == 4) zero_kernel<uint32_t><<<grid_for(L, bytes / 4), 256, 0, L.stream>>>(static_cast<uint32_t*>(dst), bytes / 4);
+  else zero_kernel<uint8_t><<<grid_for(L, bytes), 256, 0, L.stream>>>(static_cast<uint8_t*>(dst), bytes);
+  const cudaError_t e = cudaGetLastError();
+  launch_end(L);
+  return cuda_status(e);
+}
+
 // ---------------------------------------------------------------- f32 -> bf16 copy
 __global__ void cast_bf16_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {

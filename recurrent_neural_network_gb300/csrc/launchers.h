@@ -45,6 +45,12 @@ struct Remap {
 };
 
 // ---------------------------------------------------------------- gemm.cu
+// Device-to-device copies (1-D, and rows of `width` bytes between pitched
+// buffers) and zero fills as kernels on the stream (any alignment; 16-byte
+// vectors where every address, pitch and size allows).
+int dev_copy(const Launch& L, void* dst, const void* src, size_t bytes);
+int dev_copy2d(const Launch& L, void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, size_t rows);
+int dev_zero(const Launch& L, void* dst, size_t bytes);
 // D[m][n] = sum_k A(m,k) B(n,k) (+ bias[n]) (+ D) with float output.
 // mode 1: bf16 operands on tcgen05; mode 0: fp32 operands on FFMA.
 int gemm_f32(const Launch& L, int mode, const Operand& A, const Operand& B, int M, int N, int K, float* D,
