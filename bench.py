@@ -314,6 +314,14 @@ def e2e_run(R, wl, steps, stream, barrier, reduce_fn=None):
     e1.record(stream)
     barrier()
     bind(0)
+    # the host link of this machine: one read-back of the same results with nothing else running
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for k in outs:
+        host_out[k][0].copy_(dev_out[k][0], non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_run.d2h_gbs = d2h / (f0.elapsed_time(f1) * 1e-3) / 1e9
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
@@ -764,8 +772,10 @@ def main():
         "clocks": clk,
         "e2e": {"value": world * fl / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+                "d2h_gbs_alone": None if args.no_e2e else round(getattr(e2e_run, "d2h_gbs", float("nan")), 1),
                 "copies": ("x, dy in; dw, dx out" if wl.training else "x in; y out") +
-                          ", pinned host buffers, overlapped with the neighbouring steps on a copy stream"},
+                          ", pinned host buffers, overlapped with the neighbouring steps on a copy stream; "
+                          "d2h_gbs_alone: one read-back of the same results with nothing else running"},
         "phases_ms": phases,
         "workloads": subs,
         "kernels": {k: class_roofline(k, v[0], v[1], wl, psteps, pk, "transposed=1" in plan, "fused_point=1" in plan)
