@@ -471,7 +471,7 @@ int plan_and_layout(rnn_s* h) {
   h->wl.resize(V);
   cur = 0;
   h->ws_err = take(cur, 256);
-  h->ws_arrive = take(cur, (size_t)kStackMaxLayers * T * 4);  // per-timestep counters (stack: per layer)
+  h->ws_arrive = take(cur, (size_t)std::max(kStackMaxLayers, L) * T * 4);  // per-timestep counters (stack: a row per layer)
   h->ws_hx = (h->persist_plan || h->persist8) ? take(cur, (size_t)8 * B * H) : 0;
   h->bias_slices = std::max(1, std::min(64, (T * B + 255) / 256));
   h->ws_bias = take(cur, (size_t)V * h->bias_slices * GH * 4);  // one scratch slice per (layer, direction)
@@ -679,7 +679,9 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
   const int L = d.layers, T = d.T, B = d.B, H = d.hidden, GH = h->GH;
   const size_t e = h->elem, BH = (size_t)B * H, BGH = (size_t)B * GH;
   const bool lstm = d.cell == RNN_LSTM, gru = d.cell == RNN_GRU;
+  // one counter row per layer, zeroed once for all groups
   unsigned int* cnt = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
+  RNN_TRY(zero_async(h, cnt, (size_t)L * T * 4, stream));
   for (size_t gi = 0; gi < h->stackb_groups.size(); ++gi) {
     const int l0 = h->stackb_groups[gi].first, nl = h->stackb_groups[gi].second;
     // recurrent-only groups: the gradient reaching this layer's outputs from
@@ -723,8 +725,7 @@ int bwd_stack(rnn_s* h, const void* dy, const void* dhT, const float* dcT, const
       ly.dc0 = (lstm && dc0) ? dc0 + l * BH : nullptr;
       ly.wait_above = i + 1 < nl ? 1 : 0;
     }
-    RNN_TRY(zero_async(h, cnt, (size_t)nl * T * 4, stream));
-    sa.cnt = cnt;
+    sa.cnt = cnt + (size_t)l0 * T;
     sa.err = reinterpret_cast<int*>(W + h->ws_err);
     sa.limit_ns = h->limit_ns;
     sa.test_skip_publish = (d.flags & RNN_FLAG_TEST_SKIP_PUBLISH) ? 1 : 0;
@@ -760,7 +761,15 @@ int fwd_stack(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
     RNN_TRY(gemm_f32(Lk, d.mode, A, Bw, T * B, GH, d.input, P0, GH, reinterpret_cast<const float*>(PW + h->pl[0].bias),
                      0, none, 0));
   }
+  // every layer's h_{-1} and every layer's counter row (one per layer, so
+  // that the groups need no zeroing between them) in one launch
   unsigned int* cnt = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
+  {
+    std::vector<DevOp> ops;
+    for (int l = 0; l < L; ++l) ops.push_back({hseq_of(l), h0 ? static_cast<const char*>(h0) + l * BH * e : nullptr, BH * e});
+    ops.push_back({cnt, nullptr, (size_t)L * T * 4});
+    RNN_TRY(dev_batch(mk(h, stream, nullptr, "copy"), ops.data(), (int)ops.size()));
+  }
   for (const auto& grp : h->stack_groups) {
     const int l0 = grp.first, nl = grp.second;
     StackArgs sa{};
@@ -772,8 +781,6 @@ int fwd_stack(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
     for (int i = 0; i < nl; ++i) {
       const int l = l0 + i;
       char* hs = hseq_of(l);
-      if (h0) RNN_TRY(copy_async(h, hs, static_cast<const char*>(h0) + l * BH * e, BH * e, stream));
-      else RNN_TRY(zero_async(h, hs, BH * e, stream));
       StackLayer& ly = sa.lay[i];
       ly.Wx = l > 0 ? reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wx) : nullptr;
       ly.Wh = reinterpret_cast<const __nv_bfloat16*>(PW + h->pl[l].wh);
@@ -792,8 +799,7 @@ int fwd_stack(rnn_s* h, const void* x, const void* h0, const float* c0, const ch
       ly.In = l > 0 ? H : d.input;
       ly.wait_in = i > 0 ? 1 : 0;
     }
-    RNN_TRY(zero_async(h, cnt, (size_t)nl * T * 4, stream));
-    sa.cnt = cnt;
+    sa.cnt = cnt + (size_t)l0 * T;
     sa.err = reinterpret_cast<int*>(W + h->ws_err);
     sa.limit_ns = h->limit_ns;
     sa.test_skip_publish = (d.flags & RNN_FLAG_TEST_SKIP_PUBLISH) ? 1 : 0;

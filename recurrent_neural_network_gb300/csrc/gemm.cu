@@ -144,6 +144,47 @@ int dev_copy2d(const Launch& L, void* dst, size_t dpitch, const void* src, size_
   return cuda_status(e);
 }
 
+struct DevOps {
+  DevOp op[kMaxDevOps];
+};
+namespace {
+__global__ void batch_kernel(const __grid_constant__ DevOps ops) {
+  const DevOp o = ops.op[blockIdx.y];
+  const size_t stride = (size_t)gridDim.x * blockDim.x, i0 = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  const bool vec = !(reinterpret_cast<uintptr_t>(o.dst) & 15) && !(reinterpret_cast<uintptr_t>(o.src) & 15) &&
+                   !(o.bytes & 15);
+  if (vec) {
+    uint4* d = static_cast<uint4*>(o.dst);
+    const uint4* s = static_cast<const uint4*>(o.src);
+    for (size_t i = i0; i < o.bytes / 16; i += stride) d[i] = s ? s[i] : make_uint4(0, 0, 0, 0);
+  } else {
+    uint8_t* d = static_cast<uint8_t*>(o.dst);
+    const uint8_t* s = static_cast<const uint8_t*>(o.src);
+    for (size_t i = i0; i < o.bytes; i += stride) d[i] = s ? s[i] : 0;
+  }
+}
+}  // namespace
+
+int dev_batch(const Launch& L, const DevOp* ops, int n) {
+  for (int b = 0; b < n; b += kMaxDevOps) {
+    DevOps p{};
+    const int m = std::min(kMaxDevOps, n - b);
+    size_t most = 0;
+    for (int i = 0; i < m; ++i) {
+      if (!ops[b + i].dst && ops[b + i].bytes) return RNN_ERR_INVALID_ARG;
+      p.op[i] = ops[b + i];
+      most = std::max(most, ops[b + i].bytes / 16 + (ops[b + i].bytes & 15));
+    }
+    if (!most) continue;
+    launch_begin(L);
+    batch_kernel<<<dim3(grid_for(L, most), m), 256, 0, L.stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    launch_end(L);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return RNN_OK;
+}
+
 int dev_copy(const Launch& L, void* dst, const void* src, size_t bytes) {
   return dev_copy2d(L, dst, bytes, src, bytes, bytes, 1);
 }

@@ -51,6 +51,14 @@ struct Remap {
 int dev_copy(const Launch& L, void* dst, const void* src, size_t bytes);
 int dev_copy2d(const Launch& L, void* dst, size_t dpitch, const void* src, size_t spitch, size_t width, size_t rows);
 int dev_zero(const Launch& L, void* dst, size_t bytes);
+// Up to kMaxDevOps copies (src non-null) and zero fills (src null) in one launch.
+struct DevOp {
+  void* dst;
+  const void* src;
+  size_t bytes;
+};
+constexpr int kMaxDevOps = 16;
+int dev_batch(const Launch& L, const DevOp* ops, int n);
 // D[m][n] = sum_k A(m,k) B(n,k) (+ bias[n]) (+ D) with float output.
 // mode 1: bf16 operands on tcgen05; mode 0: fp32 operands on FFMA.
 int gemm_f32(const Launch& L, int mode, const Operand& A, const Operand& B, int M, int N, int K, float* D,
@@ -278,6 +286,7 @@ struct StackBwdArgs {
   int cluster;
   int kcl[kStackMaxLayers], ks[kStackMaxLayers], kr[kStackMaxLayers], cta0[kStackMaxLayers + 1],
       ctas[kStackMaxLayers];
+  int kctl[kStackMaxLayers];  // the first kctl of each chunk in TMEM, the rest (if any) in shared memory
   StackSmem sm;
 };
 // RNN_OK if nl stacked layers of (cell, H, B) run their BPTT as one launch

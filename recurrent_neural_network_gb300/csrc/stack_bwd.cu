@@ -65,14 +65,17 @@ constexpr int kBufs = 2;        // input buffers, one timestep's K chunk each
 constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quadrant)
 constexpr int kUnits = 128;     // hidden units per CTA (TMEM lanes)
 
-// shared memory: input buffers, receive buffers of the reduction, barriers
+// shared memory: the weights past what TMEM holds (kcs k of the 128 rows,
+// 128-byte-swizzled K-major 128 x 64 blocks), input buffers, receive buffers
+// of the reduction, barriers
 struct BSmem {
-  int ring, rbuf, bars, total, bufs;
+  int a, ring, rbuf, bars, total, bufs;
 };
-inline BSmem bwd_layout(int N, int kcmax, int ksmax, int bufs) {
+inline BSmem bwd_layout(int N, int kcmax, int ksmax, int bufs, int kcs = 0) {
   BSmem s;
   s.bufs = bufs;
-  s.ring = 0;
+  s.a = 0;
+  s.ring = 128 * kcs * 2;
   s.rbuf = s.ring + bufs * (kcmax / 64) * N * 128;
   const int rb = ksmax > 1 ? 2 * (ksmax - 1) * (N / ksmax) * 128 * 4 : 0;
   s.bars = s.rbuf + rb;
@@ -92,7 +95,7 @@ struct BCtx {
 // loop-invariant arguments of one CTA, in registers (see stack.cu: a field
 // of the launch arguments read inside a loop is read again every iteration)
 struct BRun {
-  int T, B, H, u_pack, kc, cluster, test_skip_publish;
+  int T, B, H, u_pack, kc, kct, cluster, test_skip_publish;
   int* err;
   uint64_t limit_ns;
   unsigned int* cnt;
@@ -322,7 +325,9 @@ __device__ void bwd_epilogue(const BRun& a, const BCtx& c, int row, int hf, uint
   }
 }
 
-template <int CELL, int N>
+// SA: some chunk keeps weights in shared memory (a separate variant: the
+// extra MMA loop slowed the issue of the TMEM-only products by ~5% measured)
+template <int CELL, int N, bool SA>
 __global__ void __launch_bounds__(kThreads, 1)
     stack_bwd_kernel(const __grid_constant__ BwdMaps maps, const __grid_constant__ StackBwdArgs p) {
   constexpr int RING = N * 128;
@@ -346,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   a.H = p.H;
   a.u_pack = p.u_pack;
   a.kc = p.kcl[li];
+  a.kct = p.kctl[li];
   a.cluster = p.cluster;
   a.test_skip_publish = p.test_skip_publish;
   a.err = p.err;
@@ -407,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   if (a.cluster > 1) tc::cluster_sync_all();
   c.tmem = *tmem_slot;
-  const uint32_t acc_base = (uint32_t)(a.kc / 2);
+  // TMEM columns [0, kct/2): the chunk's weights (k past kct in shared memory); then the accumulators
+  const uint32_t acc_base = (uint32_t)(a.kct / 2);
 
   int last_par[kBufs];
   for (int i = 0; i < kBufs; ++i) last_par[i] = -1;
@@ -446,6 +453,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16(128, N, 0, 0);
+      const int nkt = a.kct / 64;
+      const uint64_t ad0 = tc::sdesc_sw128(tc::smem_addr(smem + a.sm.a), 16, 1024);
       bool ok = tc::mbar_wait(c.abar, 0, c.abort_flag, a.err, a.limit_ns);
       tc::fence_after_sync();
       uint32_t buf = 0, phase = 0;
@@ -465,9 +474,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_bf16_ta(d, c.tmem, bd0, idesc, 0u);
 #pragma unroll
         for (int i = 1; i < 4 * 14; ++i) {
-          if (i >= 4 * nkb) break;
+          if (i >= 4 * nkt) break;
           const int kb = i >> 2, kk = i & 3;
           tc::mma_bf16_ta(d, c.tmem + (uint32_t)(8 * i), bd0 + (uint64_t)((kb * RING + kk * 32) >> 4), idesc, 1u);
+        }
+        if constexpr (SA) {
+          // the k blocks past kct: A from the swizzled blocks in shared memory
+          for (int i = 0; i < 4 * (nkb - nkt); ++i) {
+            const int kb = nkt + (i >> 2), kk = i & 3;
+            tc::mma_bf16(d, ad0 + (uint64_t)(((i >> 2) * 16384 + kk * 32) >> 4),
+                         bd0 + (uint64_t)((kb * RING + kk * 32) >> 4), idesc, 1u);
+          }
+        } else {
+          (void)ad0;
         }
         tc::mma_commit(c.empty + buf);
         if (++buf == (uint32_t)NB) {
@@ -494,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned short* wcol =
           reinterpret_cast<const unsigned short*>(rec ? ly.Wh : ly.Wx_above) + (size_t)k0 * a.H + j;
       const uint32_t lane_q = static_cast<uint32_t>(row & ~31) << 16;
-      for (int c16 = hf; c16 < a.kc / 32; c16 += 2) {
+      for (int c16 = hf; c16 < a.kct / 32; c16 += 2) {
         float v[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -503,6 +522,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[q] = __uint_as_float(lo | (hi << 16));
         }
         tc::tmem_store16(c.tmem + lane_q + (uint32_t)(c16 * 16), v);
+      }
+      // k past kct into shared memory as K-major 128 x 64 blocks with the
+      // 128-byte swizzle (16-byte piece q of row r at piece q ^ (r % 8))
+      if constexpr (SA) {
+        for (int q8 = hf; q8 < (a.kc - a.kct) / 8; q8 += 2) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const size_t k = (size_t)(a.kct + 8 * q8 + 2 * i);
+            w[i] = (uint32_t)wcol[k * a.H] | ((uint32_t)wcol[(k + 1) * a.H] << 16);
+          }
+          const int blk = q8 >> 3, q = q8 & 7;
+          *reinterpret_cast<uint4*>(smem + a.sm.a + blk * 16384 + row * 128 + ((q ^ (row & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        tc::fence_proxy_async_smem();  // generic stores read by the tensor core (async proxy)
       }
       tc::tmem_store_wait();
       tc::fence_before_sync();
@@ -543,9 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // reduces N / ks batch columns (4..16); chunks are narrowed on the layers
 // with the fewest while the CTAs stay within `budget`, as in the forward.
 struct BGeom {
-  int N, cluster, ctas;
-  int kc[kStackMaxLayers], kr[kStackMaxLayers], ks[kStackMaxLayers], cta0[kStackMaxLayers + 1],
-      lctas[kStackMaxLayers];
+  int N, cluster, ctas, sa;  // sa: some chunk keeps weights in shared memory
+  int kc[kStackMaxLayers], kct[kStackMaxLayers], kr[kStackMaxLayers], ks[kStackMaxLayers],
+      cta0[kStackMaxLayers + 1], lctas[kStackMaxLayers];
   BSmem sm;
 };
 
@@ -558,14 +593,16 @@ int bwd_geometry(int cell, int H, int B, int nl, int has_top, int budget, BGeom*
   g->N = B <= 32 ? 32 : 64;
   const int acc_cols = 2 * (g->N < 32 ? 32 : g->N);
   const int kt_max = 2 * (512 - acc_cols);  // k that fit TMEM beside the two accumulators
+  constexpr int kKs = 256;                  // at most this many k of a chunk in shared memory
   auto valid = [&](int l, int kc) {
-    if (kc % 64 || GH % kc || kc > kt_max) return false;
+    if (kc % 64 || GH % kc || kc > kt_max + kKs) return false;
     const int parts = (has_top && l == nl - 1) ? 1 : 2;
     const int ks = parts * (GH / kc);
     return (ks == 2 || ks == 4 || ks == 8) && g->N / ks >= 4 && g->N / ks <= 16;
   };
   auto set = [&](int l, int kc) {
     g->kc[l] = kc;
+    g->kct[l] = std::min(kc, kt_max / 64 * 64);
     g->kr[l] = GH / kc;
     g->ks[l] = ((has_top && l == nl - 1) ? 1 : 2) * g->kr[l];
   };
@@ -576,7 +613,7 @@ int bwd_geometry(int cell, int H, int B, int nl, int has_top, int budget, BGeom*
     int kc = 0;
     for (int c = 512; c >= 64 && !kc; c -= 64)
       if (valid(l, c)) kc = c;
-    for (int c = 576; c <= kt_max && !kc; c += 64)
+    for (int c = 576; c <= kt_max + kKs && !kc; c += 64)
       if (valid(l, c)) kc = c;
     if (!kc) return RNN_ERR_UNSUPPORTED;
     set(l, kc);
@@ -609,11 +646,13 @@ int bwd_geometry(int cell, int H, int B, int nl, int has_top, int budget, BGeom*
       if (g->ks[l] == kmin) set(l, g->kc[l] / 2);
     cta += extra;
   }
-  int ksmax = 1, kcmax = 0;
+  int ksmax = 1, kcmax = 0, kcsmax = 0;
   cta = 0;
   for (int l = 0; l < nl; ++l) {
     ksmax = std::max(ksmax, g->ks[l]);
     kcmax = std::max(kcmax, g->kc[l]);
+    kcsmax = std::max(kcsmax, g->kc[l] - g->kct[l]);
+    g->sa = kcsmax > 0 ? 1 : 0;
     g->cta0[l] = cta;
     g->lctas[l] = rbs * g->ks[l];
     cta += g->lctas[l];
@@ -626,7 +665,7 @@ int bwd_geometry(int cell, int H, int B, int nl, int has_top, int budget, BGeom*
     if (g->lctas[l] % ksmax) return RNN_ERR_UNSUPPORTED;
   bool fit = false;
   for (int bufs : {2, 1}) {
-    g->sm = bwd_layout(g->N, kcmax, ksmax, bufs);
+    g->sm = bwd_layout(g->N, kcmax, ksmax, bufs, kcsmax);
     if (g->sm.total + 1024 <= 227 * 1024) {
       fit = true;
       break;
@@ -635,10 +674,10 @@ int bwd_geometry(int cell, int H, int B, int nl, int has_top, int budget, BGeom*
   return fit ? RNN_OK : RNN_ERR_UNSUPPORTED;
 }
 
-template <int CELL, int N>
+template <int CELL, int N, bool SA>
 int launch_t(const Launch& L, const BwdMaps& maps, const StackBwdArgs& a, const BGeom& g, bool query_only,
              int num_sms) {
-  auto k = stack_bwd_kernel<CELL, N>;
+  auto k = stack_bwd_kernel<CELL, N, SA>;
   const int dyn = g.sm.total + 1024;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -689,11 +728,15 @@ int launch_t(const Launch& L, const BwdMaps& maps, const StackBwdArgs& a, const 
 
 int dispatch(const Launch& L, int cell, const BwdMaps& maps, const StackBwdArgs& a, const BGeom& g, bool query_only,
              int num_sms) {
-#define RNN_S(C)                                                               \
-  if (cell == C) {                                                             \
-    if (g.N == 16) return launch_t<C, 16>(L, maps, a, g, query_only, num_sms); \
-    if (g.N == 32) return launch_t<C, 32>(L, maps, a, g, query_only, num_sms); \
-    return launch_t<C, 64>(L, maps, a, g, query_only, num_sms);                \
+  const bool sa = g.sa != 0;
+  if (sa && g.N > 32) return RNN_ERR_UNSUPPORTED;  // the shared-memory chunks only fit up to 32 columns
+#define RNN_S(C)                                                                                  \
+  if (cell == C) {                                                                                \
+    if (g.N == 16) return sa ? launch_t<C, 16, true>(L, maps, a, g, query_only, num_sms)          \
+                             : launch_t<C, 16, false>(L, maps, a, g, query_only, num_sms);        \
+    if (g.N == 32) return sa ? launch_t<C, 32, true>(L, maps, a, g, query_only, num_sms)          \
+                             : launch_t<C, 32, false>(L, maps, a, g, query_only, num_sms);        \
+    return launch_t<C, 64, false>(L, maps, a, g, query_only, num_sms);                            \
   }
   RNN_S(LSTM) RNN_S(GRU) RNN_S(TANH) RNN_S(RELU)
 #undef RNN_S
@@ -739,6 +782,7 @@ int stack_bwd(const Launch& L, int cell, const StackBwdArgs& in) {
   a.cluster = g.cluster;
   for (int l = 0; l < in.nl; ++l) {
     a.kcl[l] = g.kc[l];
+    a.kctl[l] = g.kct[l];
     a.kr[l] = g.kr[l];
     a.ks[l] = g.ks[l];
     a.cta0[l] = g.cta0[l];
@@ -746,6 +790,7 @@ int stack_bwd(const Launch& L, int cell, const StackBwdArgs& in) {
   }
   a.cta0[in.nl] = g.cta0[in.nl];
   a.sm.stages = g.sm.bufs;
+  a.sm.a = g.sm.a;
   a.sm.ring = g.sm.ring;
   a.sm.rbuf = g.sm.rbuf;
   a.sm.smg = 0;

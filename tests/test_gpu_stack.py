@@ -41,8 +41,8 @@ STACK_CASES = [
                                                      # memory); backward on 768-wide chunks
     (1, 5, 6, 24, 64, 1024, "0+2,2+2,4+1", "3+2,1+2,0+1r"),  # GRU backward with recurrent-only group tops:
                                                               # the share from above of layers 4 and 2 by GEMM
-    (0, 4, 5, 32, 48, 1024, "0+2,2+2", "3+1,2+1,1+1,0+1r"),  # LSTM: 1024-wide chunks split between TMEM and
-                                                              # shared memory in both forward launches
+    (0, 4, 5, 32, 48, 1024, "0+2,2+2", "2+2,0+2r"),  # LSTM: 1024-wide chunks split between TMEM and shared
+                                                      # memory in both forward and both backward launches
     (1, 2, 7, 12, 64, 1024, "0+2", "1+1,0+1r"),       # GRU, N=16, ragged batch on the split chunks
     (2, 5, 8, 33, 96, 1024, "0+4,4+1", "1+4,0+1"),    # tanh: 128 units per CTA, two groups each way
     (0, 1, 11, 48, 32, 1024, "0+1", "0+1"),           # one layer, K split in two

@@ -149,8 +149,11 @@ def test_stacked_plan_groups(lib):
     # with each group's top layer on its recurrent product only ("r": 32
     # CTAs, the share from above computed by a GEMM) two layers per launch
     assert bw(1, 8, 200, 32, 1024, 1024, 1) == "6+2,4+2,2+2,0+2r"
-    # LSTM H=1024: the lower layer's K = 8192 needs chunks wider than TMEM holds
-    assert bw(0, 4, 100, 32, 1024, 1024, 1) == "3+1,2+1,1+1,0+1r"
+    # LSTM H=1024: a lower layer's K = 8192 on 1024-wide chunks (896 k in TMEM,
+    # 128 in shared memory: 64 CTAs) and a recurrent-only top (32 CTAs)
+    assert bw(0, 4, 100, 32, 1024, 1024, 1) == "2+2,0+2r"
+    # B = 33..64: two accumulators of 64 columns leave 768 k of TMEM; one layer per launch
+    assert bw(0, 4, 100, 48, 1024, 1024, 1) == "3+1,2+1,1+1,0+1r"
     assert bw(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK_BWD) == "-"
     assert bw(0, 4, 100, 64, 512, 512, 1, flags=rnn.FLAG_NO_STACK) == "-"
     # variable lengths switch the forward to step launches
