@@ -782,6 +782,10 @@ def main():
                     for k, v in prof.items() if v[0] and k in class_flops(wl)},
         "kernels_note": "per-kernel CUDA-event times from a separate pass of the same workload with launches "
                         "serialised (no wavefront, no graph); the timed run overlaps layers and replays graphs",
+        # every kernel class of that pass (the stacked and persistent recurrences included, which ncu
+        # cannot time: it launches them without their cluster shape): launches and ms per step
+        "kernel_classes": {k: {"launches": v[0] // psteps, "ms": round(v[1] / psteps, 4)}
+                           for k, v in sorted(prof.items()) if v[0]},
     }
     # the persistent small-batch recurrence (second target of the path) under its own key as well
     line["persistent_recurrence"] = subs.get(synth.WORKLOADS[2].name)
