@@ -346,12 +346,14 @@ int plan_and_layout(rnn_s* h) {
       }
       l0 += nl;
     }
-    // up to 8 sequences the single-layer persistent recurrence (or the step
-    // launches) keep the forward unless a stacked group overlaps layers on
+    // up to 8 sequences the single-layer persistent recurrence, where it
+    // fits, keeps the forward unless a stacked group overlaps layers on
     // chunks that fit TMEM (measured at B <= 8, LSTM and GRU H=1024, 4
     // layers: one-layer groups and two-layer groups on widened chunks both
-    // lost to the persistent forward; H <= 512 four-layer groups won 5-6x)
-    if (B <= 8 && !overlap && !(d.flags & RNN_FLAG_FORCE_STACK)) ok = false;
+    // lost to the persistent forward; H <= 512 four-layer groups won 5-6x).
+    // Where it does not fit (LSTM and GRU H=2048) the stacked forward beat
+    // the step launches (one layer, T=16: 0.58 against 0.69 ms).
+    if (B <= 8 && !overlap && pfits && !(d.flags & RNN_FLAG_FORCE_STACK)) ok = false;
     if (ok) {
       h->stack = h->stack_plan = 1;
       h->stack_groups = groups;

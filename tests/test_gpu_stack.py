@@ -46,6 +46,8 @@ STACK_CASES = [
     (1, 2, 7, 12, 64, 1024, "0+2", "1+1,0+1r"),       # GRU, N=16, ragged batch on the split chunks
     (2, 5, 8, 33, 96, 1024, "0+4,4+1", "1+4,0+1"),    # tanh: 128 units per CTA, two groups each way
     (0, 1, 11, 48, 32, 1024, "0+1", "0+1"),           # one layer, K split in two
+    (0, 1, 6, 4, 64, 2048, "0+1", "-"),               # B <= 8 beyond the persistent widths: one layer on
+    (1, 1, 5, 8, 32, 2048, "0+1", "-"),               # 1024-wide split chunks (N=16), step-launch backward
 ]
 
 
