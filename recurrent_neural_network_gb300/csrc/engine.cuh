@@ -34,6 +34,7 @@ struct GemmGeom {
   int kb_total, kb_per_split;  // K blocks of 64 (tcgen05) or 16 (SIMT)
   int num_tiles;               // m_tiles * n_tiles * splits
   int a_mn, b_mn;              // operand majorness (1 = MN-major)
+  int a3, b3;                  // MN-major operand with a 3-D map: all 64-wide blocks of a tile in one load
   uint64_t limit_ns;           // bound on every pipeline wait
   int* err;                    // device error word
   int cluster;                 // > 1: the split-K CTAs of a tile form one thread-block cluster
@@ -211,7 +212,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       bool ok = true;
       auto load_a = [&](uint8_t* sa, uint64_t* bar, int m0, int kb) {
         const int k0 = kb * BK;
-        if (g.a_mn) {
+        if (g.a3) {
+          tc::tma_load_3d(sa, &mapA, bar, 0, k0, m0 / 64);
+        } else if (g.a_mn) {
 #pragma unroll
           for (int j = 0; j < BM / 64; ++j) tc::tma_load_2d(sa + j * 8192, &mapA, bar, m0 + 64 * j, k0);
         } else {
@@ -220,7 +223,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       };
       auto load_b = [&](uint8_t* sb, uint64_t* bar, int n0, int kb) {
         const int k0 = kb * BK;
-        if (g.b_mn) {
+        if (g.b3) {
+          tc::tma_load_3d(sb, &mapB, bar, 0, k0, n0 / 64);
+        } else if (g.b_mn) {
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j) tc::tma_load_2d(sb + j * 8192, &mapB, bar, n0 + 64 * j, k0);
         } else {
@@ -521,7 +526,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
       bool ok = true;
       auto load_a = [&](uint8_t* sa, uint32_t fb, int m0, int kb) {
         const int k0 = kb * BK;
-        if (g.a_mn) {
+        if (g.a3) {
+          tc::tma_load_3d_pair(sa, &mapA, fb, 0, k0, m0 / 64);
+        } else if (g.a_mn) {
 #pragma unroll
           for (int j = 0; j < 2; ++j) tc::tma_load_2d_pair(sa + j * 8192, &mapA, fb, m0 + 64 * j, k0);
         } else {
@@ -530,7 +537,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
       };
       auto load_b = [&](uint8_t* sb, uint32_t fb, int n0, int kb) {
         const int k0 = kb * BK;
-        if (g.b_mn) {
+        if (g.b3) {
+          tc::tma_load_3d_pair(sb, &mapB, fb, 0, k0, n0 / 64);
+        } else if (g.b_mn) {
 #pragma unroll
           for (int j = 0; j < HB / 64; ++j) tc::tma_load_2d_pair(sb + j * 8192, &mapB, fb, n0 + 64 * j, k0);
         } else {

@@ -30,10 +30,28 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 
 // 2-D bf16 tensor map over an operand with 128-byte swizzle.  K-major operands
 // use a box of 64 (k) x box_rows (mn); MN-major operands a box of 64 (mn) x 64 (k).
-inline int encode_operand(CUtensorMap* map, const Operand& op, int box_rows) {
+// An MN-major operand whose MN extent is a multiple of 64 gets a 3-D map
+// (64 MN, K, MN / 64) with box (64, 64, box_rows / 64), *three_d = 1: one
+// load brings all 64-wide blocks of a tile, in the same shared-memory image
+// (block j at j x 8 KB, 128-byte swizzle) the per-block 2-D loads write (a
+// TMA load costs about the same to issue whatever its size).
+inline int encode_operand(CUtensorMap* map, const Operand& op, int box_rows, int* three_d = nullptr) {
   auto enc = tmap_encoder();
   if (!enc) return RNN_ERR_CUDA;
   if ((reinterpret_cast<uintptr_t>(op.ptr) & 15) || ((op.ld * 2) & 15)) return RNN_ERR_INVALID_ARG;
+  if (three_d) *three_d = 0;
+  if (three_d && op.mn_major && box_rows > 64 && box_rows % 64 == 0 && op.mn_ext % 64 == 0) {
+    cuuint64_t dims3[3] = {64, (cuuint64_t)op.k_ext, (cuuint64_t)(op.mn_ext / 64)};
+    cuuint64_t strides3[2] = {(cuuint64_t)op.ld * 2, 128};
+    cuuint32_t box3[3] = {64, 64, (cuuint32_t)(box_rows / 64)}, es3[3] = {1, 1, 1};
+    const CUresult r3 = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(op.ptr), dims3, strides3, box3,
+                            es3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r3 == CUDA_SUCCESS) {
+      *three_d = 1;
+      return RNN_OK;
+    }
+  }
   cuuint64_t dims[2], strides[1];
   cuuint32_t box[2], es[2] = {1, 1};
   if (op.mn_major) {
@@ -107,9 +125,10 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
   if (B.mn_major && BN % 64) return RNN_ERR_UNSUPPORTED;
   CUtensorMap ma, mb;
-  int rc = encode_operand(&ma, A, tce::BM);
+  int a3 = 0, b3 = 0;
+  int rc = encode_operand(&ma, A, tce::BM, &a3);
   if (rc) return rc;
-  rc = encode_operand(&mb, B, BN);
+  rc = encode_operand(&mb, B, BN, &b3);
   if (rc) return rc;
   GemmGeom g;
   g.M = M;
@@ -124,6 +143,8 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   g.num_tiles = g.m_tiles * g.n_tiles * g.splits;
   g.a_mn = A.mn_major;
   g.b_mn = B.mn_major;
+  g.a3 = a3;
+  g.b3 = b3;
   g.limit_ns = L.limit_ns;
   g.err = L.err;
   // The cluster reduction gives each CTA BN/splits columns, read as 16-byte
@@ -171,9 +192,10 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
   if (B.mn_major && (BN / 2) % 64) return RNN_ERR_UNSUPPORTED;
   CUtensorMap ma, mb;
-  int rc = encode_operand(&ma, A, 128);
+  int a3 = 0, b3 = 0;
+  int rc = encode_operand(&ma, A, 128, &a3);
   if (rc) return rc;
-  rc = encode_operand(&mb, B, BN / 2);
+  rc = encode_operand(&mb, B, BN / 2, &b3);
   if (rc) return rc;
   GemmGeom g;
   g.M = M;
@@ -189,6 +211,8 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   g.num_tiles = g.m_tiles * g.n_tiles * g.splits;
   g.a_mn = A.mn_major;
   g.b_mn = B.mn_major;
+  g.a3 = a3;
+  g.b3 = b3;
   g.limit_ns = L.limit_ns;
   g.err = L.err;
   g.cluster = g.splits;
@@ -239,6 +263,8 @@ int launch_simt(const Launch& L, const Operand& A, const Operand& B, int M, int 
   g.static_op = 0;
   g.a_mn = A.mn_major;
   g.b_mn = B.mn_major;
+  g.a3 = 0;
+  g.b3 = 0;
   g.limit_ns = L.limit_ns;
   g.err = L.err;
   constexpr int smem = se::smem_bytes<BN>();
