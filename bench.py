@@ -84,7 +84,7 @@ class Clocks:
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
@@ -95,13 +95,17 @@ class Clocks:
                 mx.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[3]))
+            except ValueError:
+                pass
             for nm, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "power_w": statistics.median(pw) if pw else None, "reasons": sorted(reasons)}
 
 
 def replica_aggregate(ms_local, flops_per_step, dist=None, device="cpu"):
@@ -169,8 +173,8 @@ def class_bytes(wl, transposed, fused_point=False):
 # ncu capture of the same kernel build on `bench.py --ncu-steps` (one layer,
 # T=2, the same per-step shape; transposed steps, BPTT pointwise fused into the
 # product): the first launch of each class.
-NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.13e6,
-               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.46e6}
+NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.23e6,
+               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.48e6}
 
 
 def oracle_sample(wl, B1, T1):
@@ -732,10 +736,14 @@ def main():
     fl = step_flops(wl)
     ms, tflops, world = replica_aggregate(ms, fl, dist, dev)
     pk = peaks()
+    e2e_clk = None
     if args.no_e2e:
         ms_e2e, h2d, d2h = float("nan"), 0, 0
     else:
+        clocks_e2e = Clocks(local)
+        clocks_e2e.start()
         ms_e2e, h2d, d2h = e2e_run(R, wl, args.steps, stream, barrier, reduce_fn)
+        e2e_clk = clocks_e2e.stop()
         ms_e2e, _, _ = replica_aggregate(ms_e2e, fl, dist, dev)
     plan = R.r.describe()
     del R
@@ -773,6 +781,7 @@ def main():
         "e2e": {"value": world * fl / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                 "d2h_gbs_alone": None if args.no_e2e else round(getattr(e2e_run, "d2h_gbs", float("nan")), 1),
+                "clocks": e2e_clk,
                 "copies": ("x, dy in; dw, dx out" if wl.training else "x in; y out") +
                           ", pinned host buffers, overlapped with the neighbouring steps on a copy stream; "
                           "d2h_gbs_alone: one read-back of the same results with nothing else running"},
