@@ -43,7 +43,9 @@ STACK_CASES = [
                                                               # the share from above of layers 4 and 2 by GEMM
     (0, 4, 5, 32, 48, 1024, "0+2,2+2", "2+2,0+2r"),  # LSTM: 1024-wide chunks split between TMEM and shared
                                                       # memory in both forward and both backward launches
-    (1, 2, 7, 12, 64, 1024, "0+2", "1+1,0+1r"),       # GRU, N=16, ragged batch on the split chunks
+    (1, 2, 7, 12, 64, 1024, "0+2", "0+2"),            # GRU, N=16, ragged batch on the split chunks
+    (0, 2, 5, 12, 64, 1024, "0+2", "0+2"),            # LSTM, N=16: backward chunks split between TMEM and
+                                                      # shared memory too (the shared-memory kernel variant)
     (2, 5, 8, 33, 96, 1024, "0+4,4+1", "1+4,0+1"),    # tanh: 128 units per CTA, two groups each way
     (0, 1, 11, 48, 32, 1024, "0+1", "0+1"),           # one layer, K split in two
     (0, 1, 6, 4, 64, 2048, "0+1", "-"),               # B <= 8 beyond the persistent widths: one layer on
