@@ -648,6 +648,7 @@ def main():
                     help="layers,timesteps of the sweep's training steps (e.g. 4,100 for the stacked range)")
     ap.add_argument("--sweep-batches", default="1,2,4,8,16,32,64,128,256,512")
     ap.add_argument("--sweep-widths", default="256,512,1024,2048,4096,8192")
+    ap.add_argument("--sweep-cells", default="0,1", help="cells of the sweep (0 LSTM, 1 GRU, 2 tanh, 3 ReLU)")
     ap.add_argument("--one-step", action="store_true",
                     help="one direct training step of the --config workload (packing included), for launch lists")
     ap.add_argument("--ncu-T", type=int, default=2, help="timesteps of the --ncu-steps program")
@@ -659,7 +660,7 @@ def main():
         from recurrent_neural_network_gb300 import build
         build.build()
         layers, T = (int(v) for v in args.sweep_shape.split(","))
-        sweep(torch.device("cuda", 0), layers=layers, T=T,
+        sweep(torch.device("cuda", 0), layers=layers, T=T, cells=tuple(int(v) for v in args.sweep_cells.split(",")),
               batches=tuple(int(v) for v in args.sweep_batches.split(",")),
               widths=tuple(int(v) for v in args.sweep_widths.split(",")))
         return
