@@ -48,6 +48,9 @@ STACK_CASES = [
                                                       # shared memory too (the shared-memory kernel variant)
     (2, 5, 8, 33, 96, 1024, "0+4,4+1", "1+4,0+1"),    # tanh: 128 units per CTA, two groups each way
     (0, 1, 11, 48, 32, 1024, "0+1", "0+1"),           # one layer, K split in two
+    (0, 17, 4, 12, 64, 256, "0+4,4+4,8+4,12+4,16+1", "13+4,9+4,5+4,1+4,0+1"),  # 17 layers: five launches each
+                                                      # way, a counter row per layer, the h_{-1} copies and counter
+                                                      # zeroing of the forward in two batched launches (18 > 16 ops)
     (0, 1, 6, 4, 64, 2048, "0+1", "-"),               # B <= 8 beyond the persistent widths: one layer on
     (1, 1, 5, 8, 32, 2048, "0+1", "-"),               # 1024-wide split chunks (N=16), step-launch backward
 ]
