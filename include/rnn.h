@@ -123,16 +123,16 @@ enum {
                                       approximation (3 mantissa bits per weight): the forward then computes
                                       with W_h' = e4m3(W_h / s) * s.  Training calls (with a reserve) keep the
                                       bf16 path.  rnn_get_sizes includes the stash in the packed size. */
-#define RNN_FLAG_NO_STACK 0x10000u /* bf16, one direction, 9..64 sequences: run the forward recurrence as
+#define RNN_FLAG_NO_STACK 0x10000u /* bf16, one direction, up to 64 sequences: run the forward recurrence as
                                       step launches (with the layer wavefront) instead of the persistent
                                       stacked recurrence (up to 4 layers per launch, each layer's
                                       [W_x | W_h] rows resident in tensor memory, layer l+1 starting step t
                                       as soon as layer l has finished it) */
 #define RNN_FLAG_NO_STACK_BWD 0x40000u /* run the backward recurrence as step launches even where the persistent
                                           stacked backward (the transposed products of up to 4 layers per
-                                          launch, 9..64 sequences) fits; RNN_FLAG_NO_STACK turns off both */
-#define RNN_FLAG_FORCE_STACK 0x20000u /* use the persistent stacked forward recurrence (also for B <= 8, in
-                                         place of the single-layer persistent recurrence) or fail */
+                                          launch, up to 64 sequences) fits; RNN_FLAG_NO_STACK turns off both */
+#define RNN_FLAG_FORCE_STACK 0x20000u /* use the persistent stacked forward recurrence (also for B <= 8 where
+                                         the planner would take the single-layer persistent one) or fail */
 #define RNN_FLAG_SLIM_STEP 0x80000u /* bf16 LSTM, transposed steps, more than 128 sequences: run the forward
                                        steps on a kernel with three pipeline stages and one tensor-memory
                                        accumulator (97.5 KB of shared memory, 256 TMEM columns), so that a

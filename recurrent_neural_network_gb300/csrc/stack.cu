@@ -1,5 +1,5 @@
 // stack.cu -- persistent forward recurrence of a group of stacked layers for
-// moderate batches (9 to 64 sequences), all timesteps in one launch.
+// batches of up to 64 sequences, all timesteps in one launch.
 //
 // "Persistent RNNs: Stashing Recurrent Weights On-Chip" (citing snippets on
 // its page): keep the recurrent weights on chip across timesteps and run the

@@ -1,5 +1,5 @@
 // stack_bwd.cu -- persistent backward-through-time of a group of stacked
-// layers for moderate batches (9 to 64 sequences), all reverse timesteps of
+// layers for batches of up to 64 sequences, all reverse timesteps of
 // every layer of the group in one launch.
 //
 // "Persistent RNNs: Stashing Recurrent Weights On-Chip" (citing snippets on
