@@ -1,6 +1,7 @@
-"""The persistent stacked forward recurrence (bf16, one direction, 9..64
-sequences; RNN_FLAG_FORCE_STACK also below): groups of up to four layers in one
-launch, each layer's [W_x | W_h] rows resident in tensor memory, layer l+1
+"""The persistent stacked recurrences (bf16, one direction, up to 64
+sequences): groups of up to four layers in one launch each way, each layer's
+[W_x | W_h] rows (forward) or transposed columns (backward) resident in tensor
+memory, the part of a chunk wider than it holds in shared memory, layer l+1
 starting step t once layer l has finished it.
 
 "Persistent RNNs: Stashing Recurrent Weights On-Chip" (citing snippets on its
