@@ -138,6 +138,12 @@ enum {
                                        accumulator (97.5 KB of shared memory, 256 TMEM columns), so that a
                                        CTA of another layer's step can share each SM and stream its weights
                                        while this one runs its epilogue */
+#define RNN_FLAG_STEP_CHUNKS 0x100000u /* bf16 LSTM training forward, transposed steps, one direction, fixed
+                                        lengths, batch a multiple of 32: run the steps of each chunk after the
+                                        first step as one cooperative launch in which each CTA pair loads
+                                        h_{t-1} once every pair has stored it (bounded waits; a timeout
+                                        reported as RNN_ERR_TIMEOUT); ignored where a step's tiles
+                                        outnumber the SM pairs */
 #define RNN_FLAG_TEST_SKIP_PUBLISH 0x100u /* test hook: in the persistent recurrences one CTA never
                                              publishes its first step, so the others' bounded waits
                                              give up and rnn_sync_status reports RNN_ERR_TIMEOUT */

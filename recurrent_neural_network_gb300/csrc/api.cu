@@ -138,6 +138,7 @@ struct rnn_s {
   int persist8 = 0, persist8_cl = 0;  // fp8 stash (RNN_FLAG_FP8_STASH): persistent inference on e4m3 W_h
   int tstep = 0;      // 1: transposed recurrent steps (W_h as the row operand, packing unit 1)
   int slim_step = 0;  // 1: transposed LSTM forward steps on the shared-SM kernel (three stages, one accumulator)
+  int step_chunks = 0;  // 1: transposed LSTM training steps of a chunk (after t = 0) in one cooperative launch
   // persistent stacked forward (9..64 sequences): groups of up to
   // kStackMaxLayers layers, each group one launch; stack_plan is the plan's
   // choice, stack what the current lengths allow (variable lengths: off)
@@ -288,6 +289,11 @@ int plan_and_layout(rnn_s* h) {
   if (h->tstep) {
     h->u = 1;
     h->slim_step = (d.cell == RNN_LSTM && B > 128 && (d.flags & RNN_FLAG_SLIM_STEP)) ? 1 : 0;
+    // several steps per launch: one tile of 256 gate rows x the batch per SM pair and step
+    const int sbn = B > 128 ? 256 : B > 64 ? 128 : 64;
+    h->step_chunks = (d.cell == RNN_LSTM && !h->slim_step && h->D == 1 && B % 32 == 0 &&
+                      ((GH + 255) / 256) * ((B + sbn - 1) / sbn) <= h->num_sms / 2 &&
+                      (d.flags & RNN_FLAG_STEP_CHUNKS)) ? 1 : 0;
     // backward: 128-unit x bn-batch tiles, K split in clusters of a power of
     // two that the K blocks fill exactly, until the step covers the SMs
     h->bwd_bn = B > 128 ? 256 : B > 64 ? 128 : 64;
@@ -1363,11 +1369,13 @@ int rnn_describe(rnn_handle_t h, char* buf, size_t len) {
   snprintf(buf, len,
            "cell=%s mode=%s L=%d T=%d B=%d I=%d H=%d G=%d u=%d recurrence=%s engine=%s wavefront=%d "
            "chunk=%d nchunks=%d bwd_bn=%d bwd_splits=%d sms=%d transposed=%d fused_point=%d "
-           "persist_cluster=%d directions=%d fp8_stash=%d stack_groups=%s stack_bwd_groups=%s slim_step=%d",
+           "persist_cluster=%d directions=%d fp8_stash=%d stack_groups=%s stack_bwd_groups=%s slim_step=%d "
+           "step_chunks=%d",
            cell, h->d.mode ? "bf16" : "fp32", h->d.layers, h->d.T, h->d.B, h->d.input, h->d.hidden, h->G, h->u,
            h->persist ? "persistent" : h->stack ? "stacked" : "streaming", h->d.mode ? "tcgen05" : "ffma",
            h->wavefront, h->chunk, h->nch, h->bwd_bn, h->bwd_splits, h->num_sms, h->tstep, h->bwd_fuse,
-           h->persist ? h->persist_cl : 0, h->D, h->persist8, groups, bgroups, h->slim_step);
+           h->persist ? h->persist_cl : 0, h->D, h->persist8, groups, bgroups, h->slim_step,
+           h->step_chunks);
   return RNN_OK;
 }
 
@@ -1432,6 +1440,10 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
       for (int l = 0; l < L; ++l)
         RNN_TRY(zero_async(h, train ? R + h->rl[l].hseq : W + h->wl[l].hseq, (size_t)(T + 1) * BH * e, stream));
     }
+    // several steps per launch: arrival counters per (layer, step), zeroed once per call
+    const bool chunks = h->step_chunks && train && !pers && !h->varlen;
+    unsigned int* step_cnt = reinterpret_cast<unsigned int*>(W + h->ws_arrive);
+    if (chunks) RNN_TRY(zero_async(h, step_cnt, (size_t)L * T * 4, stream));
     if (wf) RNN_TRY(fork_streams(h, stream));
     const int nd = wf ? (L + nch - 1) : 1;
     for (int dg = 0; dg < nd; ++dg) {
@@ -1504,6 +1516,9 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
           for (int t = t0; t < t1; ++t) {
             const int Bs = h->varlen ? h->Bt[t] : B;
             if (Bs == 0) continue;
+            // the chunk's steps from t on in one launch (t = 0 reads c0 and runs alone)
+            const int ns = (chunks && t > 0) ? t1 - t : 1;
+            const int tl = t + ns - 1;
             FwdStepArgs a;
             a.B = Bs;
             a.H = H;
@@ -1520,11 +1535,14 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
             a.h_prev = hseq + (size_t)t * BH * e;
             a.h_out = hseq + (size_t)(t + 1) * BH * e;
             a.y = l == L - 1 ? static_cast<char*>(y) + (size_t)t * BH * e : nullptr;
-            a.hT = (!h->varlen && t == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
-            a.cT = (!h->varlen && t == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
+            a.hT = (!h->varlen && tl == T - 1 && hT) ? static_cast<char*>(hT) + (size_t)l * BH * e : nullptr;
+            a.cT = (!h->varlen && tl == T - 1 && cT && lstm) ? cT + (size_t)l * BH : nullptr;
             a.hn_out = (train && gru) ? reinterpret_cast<float*>(R + h->rl[l].hn) + (size_t)t * BH : nullptr;
             a.slim = h->slim_step;
-                Operand A{hseq + (size_t)t * BH * e, H, 0, Bs, H};
+            a.steps = ns;
+            a.hT_step = T - 1 - t;
+            a.step_cnt = ns > 1 ? step_cnt + (size_t)l * T + t : nullptr;
+            Operand A{hseq + (size_t)t * BH * e, H, 0, Bs, H};
             Operand Bw{PW + h->pl[l].wh, H, 0, GH, H, 1};
             Launch Lk = mk(h, s, ws, "fwd_step");
             if (h->tstep) RNN_TRY(fwd_step_t(Lk, d.cell, Bw, A, a));
@@ -1537,6 +1555,7 @@ int rnn_fwd(rnn_handle_t h, const void* x, const void* h0, const float* c0, cons
               if (nr > 0 && cT && lstm)
                 RNN_TRY(copy_async(h, cT + (size_t)l * BH + (size_t)r0 * H, a.c_out + (size_t)r0 * H, (size_t)nr * H * 4, s));
             }
+            t = tl;
           }
           if (wf) RNN_TRY(cu(cudaEventRecord(h->ev[(size_t)l * nch + c], s)));
         }

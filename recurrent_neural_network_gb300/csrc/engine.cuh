@@ -42,11 +42,19 @@ struct GemmGeom {
   int pdl;                     // launched as a programmatic dependent: wait before touching produced data
   int static_op;               // operand no earlier kernel writes (0 none, 1 A, 2 B): its first STAGES
                                // blocks of the first tile are loaded before that wait
+  // Several dependent steps in one launch (CTA pairs, one tile per pair and step; steps > 1): tile
+  // index = step * tiles_per_step + tile of the step, the B rows of step s start b_step_rows * s
+  // further, and a pair loads the B operand of step s > 0 only once step_cnt[s - 1] has reached
+  // step_want (the epilogue arrives on step_cnt[s] when its stores of step s are complete).
+  int steps, tiles_per_step, b_step_rows;
+  unsigned int* step_cnt;
+  unsigned int step_want;
 };
 
 struct TileCoord {
   int m0, n0;       // first row / column of the tile
   int mt, nt;       // tile indices
+  int step;         // step of a launch over several dependent steps (GemmGeom::steps), else 0
   int split, splits;
   int part, parts;  // this thread's share of the tile's columns (epilogues with 8 warps: 2 parts)
   int* scratch;     // 8 ints of shared memory for the epilogue warps (tcgen05 only)
@@ -120,6 +128,35 @@ struct SmemAcc {
     for (int i = 0; i < 16; ++i) v[i] = row[col + i];
   }
 };
+
+// Launches over several dependent steps: the step of a tile index, the tile
+// index within its step left in `tile`.
+__device__ __forceinline__ int step_of(const GemmGeom& g, int& tile) {
+  if (g.steps <= 1) return 0;
+  const int s = tile / g.tiles_per_step;
+  tile -= s * g.tiles_per_step;
+  return s;
+}
+
+// Bounded wait until *cnt >= want (acquire); gives up when the CTA aborts, and
+// on timeout records DEV_TIMEOUT_STEP and marks the CTA aborted.
+__device__ __forceinline__ bool wait_step(const unsigned int* cnt, unsigned int want, volatile int* abort_flag,
+                                          int* err, uint64_t limit_ns) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+  if (v >= want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v >= want) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      raise_error(err, DEV_TIMEOUT_STEP);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
 
 __device__ __forceinline__ void decode_tile(const GemmGeom& g, int tile, int& mt, int& nt, int& split) {
   split = tile % g.splits;
@@ -385,6 +422,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       if (!ok) break;
       tc::fence_after_sync();
       TileCoord t;
+      t.step = 0;
       t.m0 = mt * BM;
       t.n0 = nt * BN;
       t.mt = mt;
@@ -566,12 +604,37 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
         tc::pdl_wait();
       }
       for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
-        int mt, nt, split;
-        decode_tile(g, tile, mt, nt, split);
+        int mt, nt, split, tl = tile;
+        const int st_ = step_of(g, tl);
+        decode_tile(g, tl, mt, nt, split);
         const int kb0 = split * g.kb_per_split;
         const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
-        const int m0 = mt * BM + pr * 128, n0 = nt * BN + pr * HB;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        const int m0 = mt * BM + pr * 128, n0 = nt * BN + pr * HB + st_ * g.b_step_rows;
+        int kb = kb0;
+        if (st_ > 0) {
+          // a later step: the stages hold this CTA's output tiles until its
+          // epilogue of the step before is done, and B (h of that step) is
+          // complete once every pair has stored it: one counter covers both.
+          // Meanwhile the step's first weight blocks stream into L2.
+          const int npf = min(2 * STAGES, kb1 - kb0);
+          for (int i = 0; i < npf; ++i) {
+            const int k0 = (kb0 + i) * BK;
+            if (g.a3) {
+              tc::tma_prefetch_3d(&mapA, 0, k0, m0 / 64);
+            } else if (g.a_mn) {
+              tc::tma_prefetch_2d(&mapA, m0, k0);
+              tc::tma_prefetch_2d(&mapA, m0 + 64, k0);
+            } else {
+              tc::tma_prefetch_2d(&mapA, k0, m0);
+            }
+          }
+          if (!wait_step(g.step_cnt + st_ - 1, g.step_want, abort_flag, g.err, g.limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc::fence_proxy_async_global();  // h written by other CTAs' bulk stores, read by TMA here
+        }
+        for (; kb < kb1; ++kb) {
           const bool prefilled = tile == pair && kb - kb0 < pre;  // static operand in flight, stage armed
           if (!prefilled && !tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, g.err, g.limit_ns)) {
             ok = false;
@@ -608,8 +671,9 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
       uint32_t stage = 0, phase = 0, acc = 0, aphase = 0;
       bool ok = true;
       for (int tile = pair; tile < g.num_tiles && ok; tile += npairs) {
-        int mt, nt, split;
-        decode_tile(g, tile, mt, nt, split);
+        int mt, nt, split, tl = tile;
+        step_of(g, tl);
+        decode_tile(g, tl, mt, nt, split);
         const int kb0 = split * g.kb_per_split;
         const int kb1 = min(g.kb_total, kb0 + g.kb_per_split);
         if (!tc::mbar_wait(tempty + acc, aphase ^ 1, abort_flag, g.err, g.limit_ns)) break;
@@ -653,11 +717,18 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
     uint32_t acc = 0, aphase = 0;
     const uint32_t lane_q = static_cast<uint32_t>(q * 32) << 16;
     for (int tile = pair; tile < g.num_tiles; tile += npairs) {
-      int mt, nt, split;
-      decode_tile(g, tile, mt, nt, split);
-      const bool solo = tile == pair && tile + npairs >= g.num_tiles;
+      int mt, nt, split, tl = tile;
+      const int st_ = step_of(g, tl);
+      decode_tile(g, tl, mt, nt, split);
+      // a CTA with one tile stages its epilogue inputs in the idle second
+      // accumulator; over several dependent steps, in the accumulator of the
+      // step before (its epilogue is done, and the next step's products wait
+      // for this step's stores in every CTA)
+      const bool solo = (tile == pair && tile + npairs >= g.num_tiles) || g.steps > 1;
+      const uint32_t st_col = (acc ^ 1u) * BN;
       typename EpiStaged<Epi>::Stash stash;
       TileCoord t;
+      t.step = st_;
       t.m0 = mt * BM + pr * 128;
       t.n0 = nt * BN;
       t.mt = mt * 2 + pr;
@@ -676,7 +747,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
       t.aux = aux;
       epi.prefetch(t, row, BN);
       if constexpr (EpiStaged<Epi>::value && ACCS == 2) {
-        if (solo) epi.stage(t, row, tmem_base + BN + lane_q, BN, stash);
+        if (solo) epi.stage(t, row, tmem_base + st_col + lane_q, BN, stash);
       }
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
@@ -685,7 +756,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
       tc::fence_after_sync();
       TmemAcc a{tmem_base + acc * BN + lane_q};
       if constexpr (EpiStaged<Epi>::value && ACCS == 2) {
-        if (solo) epi.run_staged(t, row, a, TmemAcc{tmem_base + BN + lane_q}, BN, stash);
+        if (solo) epi.run_staged(t, row, a, TmemAcc{tmem_base + st_col + lane_q}, BN, stash);
         else epi(t, row, a, BN);
       } else {
         epi(t, row, a, BN);
@@ -806,6 +877,7 @@ __global__ void __launch_bounds__(128)
   __syncthreads();
   if (tid < BM) {
     TileCoord t;
+    t.step = 0;
     t.m0 = m0;
     t.n0 = n0;
     t.mt = mt;

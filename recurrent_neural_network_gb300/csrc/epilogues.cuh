@@ -510,6 +510,13 @@ struct EpiFwdStepT {
   S* y;                 // [B][H] or null
   S* hT;                // [B][H] or null
   float* cT;            // [B][H] or null
+  // launches over several dependent steps (TileCoord::step): P, c, h and y
+  // are the chunk's sequences, step s at rows step_rows * s further (c_prev
+  // the row block before c_out's: step s reads step s-1's c); hT / cT are
+  // written by step hT_step only; after its stores of step s are complete
+  // each storing thread arrives on step_cnt[s]
+  int step_rows, hT_step;
+  unsigned int* step_cnt;
 
   __device__ __forceinline__ void prefetch(const TileCoord& t, int row, int bn) const {
     constexpr int G = CellInfo<CELL>::G;
@@ -517,7 +524,7 @@ struct EpiFwdStepT {
     if (t.m0 >= GH) return;
     const int rows = min(128, GH - t.m0);
     for (int i = row; i < bn; i += 128) {
-      const int b = t.n0 + i;
+      const int b = t.n0 + i + t.step * step_rows;
       if (b >= B) break;
       tc::prefetch_l2(P + (size_t)b * GH + t.m0, rows * 4);
       if (CELL == LSTM && c_prev) tc::prefetch_l2(c_prev + (size_t)b * H + t.m0 / 4, rows);
@@ -653,14 +660,15 @@ struct EpiFwdStepT {
     for (int c = cb; c < nmax; c += 16) {
       float v[16], pv[16], cp[4];
       const int nb = min(16, nmax - c);
-      const float* pc = P + (size_t)(t.n0 + c) * GH + p;
+      const int rn = t.n0 + t.step * step_rows;
+      const float* pc = P + (size_t)(rn + c) * GH + p;
 #pragma unroll
       for (int i = 0; i < 16; ++i) pv[i] = (live && i < nb) ? pc[(size_t)i * GH] : 0.f;
-      if (CELL == LSTM) load_cp(t.n0, p, live, c, nmax, cp);
+      if (CELL == LSTM) load_cp(rn, p, live, c, nmax, cp);
       acc.load16(c, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] += pv[i];
-      finish(t.n0, p, live, c, nb, v, cp);
+      finish(rn, p, live, c, nb, v, cp);
     }
   }
 
@@ -673,13 +681,14 @@ struct EpiFwdStepT {
     const int nmax = min(cb + cw, B - t.n0);
     if constexpr (CELL == LSTM) {
 #pragma unroll
-      for (int a = 0; a < kAhead; ++a) load_cp(t.n0, p, live, cb + 16 * a, nmax, st.cp[a], tma_out);
+      for (int a = 0; a < kAhead; ++a)
+        load_cp(t.n0 + t.step * step_rows, p, live, cb + 16 * a, nmax, st.cp[a], tma_out);
     }
     // P, two chunks (32 loads per lane) in flight at a time
 #pragma unroll 1
     for (int c = cb; c < nmax; c += 32) {
       float v0[16], v1[16];
-      const float* pc = P + (size_t)(t.n0 + c) * GH + p;
+      const float* pc = P + (size_t)(t.n0 + t.step * step_rows + c) * GH + p;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         v0[i] = (live && c + i < nmax) ? pc[(size_t)i * GH] : 0.f;
@@ -723,12 +732,12 @@ struct EpiFwdStepT {
           for (int a = 0; a + 1 < kAhead; ++a)
 #pragma unroll
             for (int k = 0; k < 4; ++k) st.cp[a][k] = st.cp[a + 1][k];
-          load_cp(t.n0, p, live, c + 16 * kAhead, nmax, st.cp[kAhead - 1], tma_out);
+          load_cp(t.n0 + t.step * step_rows, p, live, c + 16 * kAhead, nmax, st.cp[kAhead - 1], tma_out);
         }
         if (tma_out)
           finish(t.n0, p, live, c, min(16, nmax - c), v2 + 16 * h, cp, row, sm_g, sm_c, sm_h);
         else
-          finish(t.n0, p, live, c, min(16, nmax - c), v2 + 16 * h, cp);
+          finish(t.n0 + t.step * step_rows, p, live, c, min(16, nmax - c), v2 + 16 * h, cp);
       }
       if (tma_out) {
         // this part's 32 batch rows are complete: its first thread stores
@@ -736,21 +745,34 @@ struct EpiFwdStepT {
         tc::fence_proxy_async_smem();
         tc::named_bar(2 + t.part, 128);
         if (threadIdx.x == 64 + 128 * t.part) {
-          const int cx = CELL == LSTM ? t.m0 / 4 : t.m0, y0 = t.n0 + c2;
+          const int cx = CELL == LSTM ? t.m0 / 4 : t.m0, yb = t.n0 + c2, y0 = yb + t.step * step_rows;
+          const bool fin = t.step == hT_step;
           if (write_gates) tc::tma_store_2d(&map_p, sm_g + (size_t)c2 * 128, t.m0, y0);
           if (CELL == LSTM) {
             tc::tma_store_2d(&map_c, sm_c + (size_t)c2 * kUnits, cx, y0);
-            if (cT) tc::tma_store_2d(&map_cT, sm_c + (size_t)c2 * kUnits, cx, y0);
+            if (cT && fin) tc::tma_store_2d(&map_cT, sm_c + (size_t)c2 * kUnits, cx, yb);
           }
           tc::tma_store_2d(&map_h, sm_h + (size_t)c2 * kUnits, cx, y0);
           if (y) tc::tma_store_2d(&map_y, sm_h + (size_t)c2 * kUnits, cx, y0);
-          if (hT) tc::tma_store_2d(&map_hT, sm_h + (size_t)c2 * kUnits, cx, y0);
+          if (hT && fin) tc::tma_store_2d(&map_hT, sm_h + (size_t)c2 * kUnits, cx, yb);
           tc::bulk_commit();
         }
       }
     }
     // the shared-memory tiles must outlive the stores' reads
-    if (tma_out && threadIdx.x == 64 + 128 * t.part) tc::bulk_wait_read_all();
+    if (tma_out && threadIdx.x == 64 + 128 * t.part) {
+      if (step_cnt) {
+        // this part's stores of the step are complete and visible: the
+        // pairs waiting to load h of this step may go on
+        tc::bulk_wait_all();
+        tc::fence_proxy_async_global();
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(step_cnt + t.step) : "memory");
+      } else {
+        tc::bulk_wait_read_all();
+      }
+    }
+    // the part's next step reads this step's c (stored by its first thread)
+    if (tma_out && step_cnt) tc::named_bar(2 + t.part, 128);
   }
 };
 

@@ -147,6 +147,11 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
   g.b3 = b3;
   g.limit_ns = L.limit_ns;
   g.err = L.err;
+  g.steps = 1;
+  g.tiles_per_step = 0;
+  g.b_step_rows = 0;
+  g.step_cnt = nullptr;
+  g.step_want = 0;
   // The cluster reduction gives each CTA BN/splits columns, read as 16-byte
   // vectors and processed 16 hidden units at a time: it needs BN to be a
   // multiple of 16*splits and at most 8 CTAs per cluster.  Otherwise the
@@ -186,9 +191,14 @@ int launch_tc(const Launch& L, const Operand& A, const Operand& B, int M, int N,
 // the K splits of a tile run as one cluster of 2*splits CTAs (pairs at ranks
 // 2i, 2i+1) and reduce through distributed shared memory (the epilogue must
 // support it); RNN_ERR_UNSUPPORTED when the split cannot be laid out so.
+// steps > 1: the products of `steps` dependent steps in one cooperative
+// launch, one tile per pair and step (see GemmGeom::steps); B's rows of step
+// s at b_step_rows * s; the epilogue of each tile arrives tile_arrivals times
+// on step_cnt[s]; RNN_ERR_UNSUPPORTED where a step's tiles outnumber the pairs.
 template <int BN, int STAGES, class Epi, int ACCS = 2>
 int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N, int K, int max_ctas,
-               const Epi& epi, int splits = 1) {
+               const Epi& epi, int splits = 1, int steps = 1, int b_step_rows = 0, unsigned int* step_cnt = nullptr,
+               unsigned int tile_arrivals = 0) {
   if (M <= 0 || N <= 0 || K <= 0) return RNN_ERR_INVALID_ARG;
   if (B.mn_major && (BN / 2) % 64) return RNN_ERR_UNSUPPORTED;
   CUtensorMap ma, mb;
@@ -215,6 +225,11 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   g.b3 = b3;
   g.limit_ns = L.limit_ns;
   g.err = L.err;
+  g.steps = 1;
+  g.tiles_per_step = 0;
+  g.b_step_rows = 0;
+  g.step_cnt = nullptr;
+  g.step_want = 0;
   g.cluster = g.splits;
   g.nfast = g.n_tiles < g.m_tiles ? 1 : 0;  // as in launch_tc
   constexpr int smem = tce2::smem_bytes<BN, STAGES>();
@@ -227,17 +242,35 @@ int launch_tc2(const Launch& L, const Operand& A, const Operand& B, int M, int N
   }
   const int cap = (max_ctas > 0 ? max_ctas : L.num_sms) / 2;
   // split-K: one tile per pair so that the cluster reduction can reuse the stages
-  const int pairs = g.cluster > 1 ? g.num_tiles : std::max(1, std::min(g.num_tiles, cap));
-  g.pdl = L.pdl;
+  int pairs = g.cluster > 1 ? g.num_tiles : std::max(1, std::min(g.num_tiles, cap));
+  if (steps > 1) {
+    if (g.cluster > 1 || g.num_tiles > cap || !step_cnt) return RNN_ERR_UNSUPPORTED;
+    g.steps = steps;
+    g.tiles_per_step = g.num_tiles;
+    g.b_step_rows = b_step_rows;
+    g.step_cnt = step_cnt;
+    g.step_want = tile_arrivals * static_cast<unsigned int>(g.num_tiles);
+    pairs = g.num_tiles;
+    g.num_tiles *= steps;
+  }
+  // (a cooperative launch is never a programmatic dependent)
+  const int pdl = steps > 1 ? 0 : L.pdl;
+  g.pdl = pdl;
   g.static_op = A.is_static ? 1 : B.is_static ? 2 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(64 + 32 * EpiWarps<Epi>::value);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
-  cudaLaunchAttribute at[2];
+  cudaLaunchAttribute at[3];
   cfg.attrs = at;
-  cfg.numAttrs = launch_attrs(at, 2 * g.cluster, L.pdl);
+  cfg.numAttrs = launch_attrs(at, 2 * g.cluster, pdl);
+  if (steps > 1) {
+    // the pairs wait on one another's stores: all of them resident at once
+    at[cfg.numAttrs].id = cudaLaunchAttributeCooperative;
+    at[cfg.numAttrs].val.cooperative = 1;
+    ++cfg.numAttrs;
+  }
   launch_begin(L);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, g, epi);
   launch_end(L);
@@ -267,6 +300,11 @@ int launch_simt(const Launch& L, const Operand& A, const Operand& B, int M, int 
   g.b3 = 0;
   g.limit_ns = L.limit_ns;
   g.err = L.err;
+  g.steps = 1;
+  g.tiles_per_step = 0;
+  g.b_step_rows = 0;
+  g.step_cnt = nullptr;
+  g.step_want = 0;
   constexpr int smem = se::smem_bytes<BN>();
   auto kern = simt_gemm_kernel<BN, Epi>;
   static bool attr = false;

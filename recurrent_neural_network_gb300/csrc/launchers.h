@@ -98,6 +98,12 @@ struct FwdStepArgs {
   float* cT;
   float* hn_out;
   int slim = 0;  // transposed LSTM steps over more than 128 sequences: the shared-SM kernel
+  // transposed LSTM steps, several in one launch: `steps` consecutive steps
+  // whose P, c, h_prev / h_out and y follow one another B rows apart (c_prev
+  // of step s is c_out of step s-1); hT / cT written by step hT_step (none
+  // when out of range); step_cnt: `steps` zeroed arrival counters
+  int steps = 1, hT_step = -1;
+  unsigned int* step_cnt = nullptr;
 };
 // one forward timestep of one layer: A = h_{t-1} [B][H], B = packed W_h [G*H][H]
 int fwd_step(const Launch& L, int mode, int cell, const Operand& A, const Operand& Bw, const FwdStepArgs& a);

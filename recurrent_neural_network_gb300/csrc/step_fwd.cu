@@ -85,15 +85,20 @@ EpiFwdStepT<CELL> make_epi_t(const FwdStepArgs& a, int bn) {
   e.y = static_cast<S*>(a.y);
   e.hT = static_cast<S*>(a.hT);
   e.cT = a.cT;
+  // several steps in one launch: the sequences' rows of all of them
+  const int steps = a.steps > 1 ? a.steps : 1, rs = a.B * steps;
+  e.step_rows = a.B;
+  e.hT_step = steps > 1 ? a.hT_step : 0;
+  e.step_cnt = steps > 1 ? a.step_cnt : nullptr;
   // bulk-store maps for the single-tile path; any failure keeps plain stores
   const int G = CellInfo<CELL>::G, ku = EpiFwdStepT<CELL>::kUnits;
   constexpr int rows = 32;  // batch rows per bulk store
   (void)bn;
-  int rc = encode_plain(&e.map_p, a.P, 4, a.B, (long long)G * a.H, (long long)G * a.H, 128, rows);
-  if (!rc && CELL == LSTM) rc = encode_plain(&e.map_c, a.c_out, 4, a.B, a.H, a.H, ku, rows);
+  int rc = encode_plain(&e.map_p, a.P, 4, rs, (long long)G * a.H, (long long)G * a.H, 128, rows);
+  if (!rc && CELL == LSTM) rc = encode_plain(&e.map_c, a.c_out, 4, rs, a.H, a.H, ku, rows);
   if (!rc && CELL == LSTM && a.cT) rc = encode_plain(&e.map_cT, a.cT, 4, a.B, a.H, a.H, ku, rows);
-  if (!rc) rc = encode_plain(&e.map_h, a.h_out, 2, a.B, a.H, a.H, ku, rows);
-  if (!rc && a.y) rc = encode_plain(&e.map_y, a.y, 2, a.B, a.H, a.H, ku, rows);
+  if (!rc) rc = encode_plain(&e.map_h, a.h_out, 2, rs, a.H, a.H, ku, rows);
+  if (!rc && a.y) rc = encode_plain(&e.map_y, a.y, 2, rs, a.H, a.H, ku, rows);
   if (!rc && a.hT) rc = encode_plain(&e.map_hT, a.hT, 2, a.B, a.H, a.H, ku, rows);
   e.tma_out = rc == RNN_OK ? 1 : 0;
   return e;
@@ -120,6 +125,21 @@ int fwd_step_t(const Launch& L, int cell, const Operand& Wh, const Operand& Hp, 
   const int G = cell == LSTM ? 4 : (cell == TANH || cell == RELU) ? 1 : 0;
   if (!G || a.u != 1) return RNN_ERR_UNSUPPORTED;
   const int M = G * a.H, N = a.B, K = a.H;
+  if (a.steps > 1) {
+    // the LSTM steps of a chunk in one cooperative launch: a pair loads h of
+    // step s-1 once all pairs have stored it (each pair's two CTAs arrive
+    // once per half of their epilogue warps); the bulk stores of 32 batch rows
+    // must not reach into the next step's rows
+    if (cell != LSTM || a.slim || !a.step_cnt || N % 32) return RNN_ERR_UNSUPPORTED;
+    Operand Hs = Hp;
+    Hs.mn_ext = N * a.steps;
+    const int bn = N > 128 ? 256 : N > 64 ? 128 : 64;
+    const EpiFwdStepT<LSTM> e = make_epi_t<LSTM>(a, bn);
+    if (!e.tma_out) return RNN_ERR_UNSUPPORTED;
+    if (bn == 256) return launch_tc2<256, 6>(L, Wh, Hs, M, N, K, 0, e, 1, a.steps, N, a.step_cnt, 4);
+    if (bn == 128) return launch_tc2<128, 8>(L, Wh, Hs, M, N, K, 0, e, 1, a.steps, N, a.step_cnt, 4);
+    return launch_tc2<64, 10>(L, Wh, Hs, M, N, K, 0, e, 1, a.steps, N, a.step_cnt, 4);
+  }
   // one n-tile holds the whole batch (up to 256 entries): W_h streams once per step
 #define RNN_STEP_T(BN_, ST)                                                                          \
   if (cell == LSTM) return launch_tc2<BN_, ST>(L, Wh, Hp, M, N, K, 0, make_epi_t<LSTM>(a, BN_));      \

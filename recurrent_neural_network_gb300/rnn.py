@@ -37,6 +37,7 @@ FLAG_NO_STACK = 0x10000
 FLAG_FORCE_STACK = 0x20000
 FLAG_NO_STACK_BWD = 0x40000
 FLAG_SLIM_STEP = 0x80000
+FLAG_STEP_CHUNKS = 0x100000
 
 # every symbol include/rnn.h declares
 SYMBOLS = ["rnn_create", "rnn_destroy", "rnn_get_sizes", "rnn_pack_weights", "rnn_fwd", "rnn_bwd_data",

@@ -394,6 +394,32 @@ def test_slim_forward_step_equals_standard(kw):
     compare(wl, a, run_oracle(hi, train=train))
 
 
+CHUNKS = [(dict(layers=2, T=9, B=256, hidden=256), 4), (dict(layers=3, T=8, B=96, hidden=384), 8),
+          (dict(layers=1, T=6, B=64, hidden=128), 0), (dict(layers=2, T=7, B=160, hidden=1024), 0)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kw,chunk", CHUNKS, ids=["B256_H256_c4", "B96_H384_c8", "B64_H128_L1", "B160_H1024"])
+def test_step_chunks_equal_step_launches(kw, chunk):
+    """RNN_FLAG_STEP_CHUNKS: the transposed LSTM training steps of a chunk
+    after t = 0 in one cooperative launch (each CTA pair loads h_{t-1} once
+    every pair has stored it, and c_{t-1} comes from its own stores) do the
+    same arithmetic in the same order as one launch per step: bit-identical
+    outputs, final states and gradients (single-step chunks, the last step
+    inside a multi-step launch, tiles wider than the batch), and the
+    oracle's."""
+    wl = tiny(0, synth.MODE_BF16, **kw)
+    hi = runner.HostInputs(wl, with_state_grads=True)
+    fl = rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING
+    assert "step_chunks=1" in runner.Runner(wl, flags=fl | rnn.FLAG_STEP_CHUNKS, chunk=chunk).r.describe()
+    a = run_gpu(wl, hi, flags=fl | rnn.FLAG_STEP_CHUNKS, chunk=chunk, repeat=2)
+    b = run_gpu(wl, hi, flags=fl, chunk=chunk)
+    for k in b:
+        if b[k] is not None:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    compare(wl, a, run_oracle(hi))
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("flags,B", [(rnn.FLAG_FORCE_STREAMING | rnn.FLAG_NO_TRANSPOSED, 33),
                                      (rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING, 33),

@@ -198,6 +198,14 @@ def test_transposed_step_plan(lib):
     assert "transposed=1" in d and " u=1 " in d and "bwd_bn=256 bwd_splits=4" in d and "fused_point=1" in d
     assert "fused_point=0" in rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, flags=rnn.FLAG_NO_FUSED_POINT).describe()
     assert "fused_point=0" in rnn.RNN(2, 1, 10, 256, 4096, 16384, 1).describe()  # tanh: separate kernel
+    # several steps per launch: opt-in, LSTM, batch a multiple of 32, a step's tiles within the SM pairs
+    assert "step_chunks=0" in d
+    ch = lambda *a: rnn.RNN(*a, flags=rnn.FLAG_STEP_CHUNKS).describe()
+    assert "step_chunks=1" in ch(0, 4, 50, 256, 4096, 4096, 1)
+    assert "step_chunks=1" in ch(0, 2, 10, 96, 384, 384, 1)
+    assert "step_chunks=0" in ch(0, 2, 10, 200, 2048, 2048, 1)   # 200 % 32
+    assert "step_chunks=0" in ch(0, 2, 10, 256, 8192, 8192, 1)   # 128 tiles of 256 gate rows > 76 pairs
+    assert "step_chunks=0" in ch(2, 2, 10, 256, 4096, 4096, 1)   # tanh
     d = rnn.RNN(0, 4, 50, 256, 4096, 4096, 1, flags=rnn.FLAG_NO_TRANSPOSED).describe()
     assert "transposed=0" in d and " u=64 " in d
     assert "transposed=0" in rnn.RNN(0, 4, 50, 257, 4096, 4096, 1).describe()   # batch wider than one tile
