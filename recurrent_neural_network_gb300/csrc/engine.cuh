@@ -614,20 +614,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
         if (st_ > 0) {
           // a later step: the stages hold this CTA's output tiles until its
           // epilogue of the step before is done, and B (h of that step) is
-          // complete once every pair has stored it: one counter covers both.
-          // Meanwhile the step's first weight blocks stream into L2.
-          const int npf = min(2 * STAGES, kb1 - kb0);
-          for (int i = 0; i < npf; ++i) {
-            const int k0 = (kb0 + i) * BK;
-            if (g.a3) {
-              tc::tma_prefetch_3d(&mapA, 0, k0, m0 / 64);
-            } else if (g.a_mn) {
-              tc::tma_prefetch_2d(&mapA, m0, k0);
-              tc::tma_prefetch_2d(&mapA, m0 + 64, k0);
-            } else {
-              tc::tma_prefetch_2d(&mapA, k0, m0);
-            }
-          }
+          // complete once every pair has stored it: one counter covers both
           if (!wait_step(g.step_cnt + st_ - 1, g.step_want, abort_flag, g.err, g.limit_ns)) {
             ok = false;
             break;
