@@ -395,11 +395,11 @@ def test_slim_forward_step_equals_standard(kw):
 
 
 CHUNKS = [(dict(layers=2, T=9, B=256, hidden=256), 4), (dict(layers=3, T=8, B=96, hidden=384), 8),
-          (dict(layers=1, T=6, B=64, hidden=128), 0), (dict(layers=2, T=7, B=160, hidden=1024), 0)]
+          (dict(layers=1, T=6, B=64, hidden=128), 0), (dict(layers=2, T=7, B=160, hidden=1024), 4)]
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("kw,chunk", CHUNKS, ids=["B256_H256_c4", "B96_H384_c8", "B64_H128_L1", "B160_H1024"])
+@pytest.mark.parametrize("kw,chunk", CHUNKS, ids=["B256_H256_c4", "B96_H384_c8", "B64_H128_L1", "B160_H1024_c4"])
 def test_step_chunks_equal_step_launches(kw, chunk):
     """RNN_FLAG_STEP_CHUNKS: the transposed LSTM training steps of a chunk
     after t = 0 in one cooperative launch (each CTA pair loads h_{t-1} once
@@ -412,6 +412,17 @@ def test_step_chunks_equal_step_launches(kw, chunk):
     hi = runner.HostInputs(wl, with_state_grads=True)
     fl = rnn.FLAG_FORCE_TRANSPOSED | rnn.FLAG_FORCE_STREAMING
     assert "step_chunks=1" in runner.Runner(wl, flags=fl | rnn.FLAG_STEP_CHUNKS, chunk=chunk).r.describe()
+
+    def fwd_launches(flags):
+        r = runner.Runner(wl, flags=flags | rnn.FLAG_NO_GRAPH, chunk=chunk)
+        r.upload(hi)
+        n0 = rnn.launch_count()
+        r.forward(True)
+        assert r.status() == 0
+        return rnn.launch_count() - n0
+
+    # the steps of a chunk after t = 0 really run as one launch
+    assert fwd_launches(fl | rnn.FLAG_STEP_CHUNKS) < fwd_launches(fl)
     a = run_gpu(wl, hi, flags=fl | rnn.FLAG_STEP_CHUNKS, chunk=chunk, repeat=2)
     b = run_gpu(wl, hi, flags=fl, chunk=chunk)
     for k in b:
