@@ -83,6 +83,18 @@ __device__ __forceinline__ void store16<float>(float* p, const float* v) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
+// One share of a 16-element store: elements e, e + es, ... (es a power of
+// two; es = 1 is the whole vector store).
+template <class S>
+__device__ __forceinline__ void store16_share(S* p, const float* v, int e, int es) {
+  if (es == 1) {
+    store16(p, v);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if ((i & (es - 1)) == e) p[i] = from_f32<S>(v[i]);
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

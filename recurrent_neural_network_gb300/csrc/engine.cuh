@@ -97,6 +97,16 @@ template <class E>
 struct EpiWarps<E, std::void_t<decltype(E::kWarps)>> {
   static constexpr int value = E::kWarps;
 };
+// FFMA engine: threads per tile row in the epilogue (1 unless the epilogue
+// declares kSimtShares and shares out a row's elements by TileCoord::part)
+template <class E, class = void>
+struct EpiSimtShares {
+  static constexpr int value = 1;
+};
+template <class E>
+struct EpiSimtShares<E, std::void_t<decltype(E::kSimtShares)>> {
+  static constexpr int value = E::kSimtShares;
+};
 
 // Epilogues with a tail_prefetch(const TileCoord&, int bn) member get it
 // called by the TMA producer thread of the single-CTA engine once it has
@@ -862,9 +872,15 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int c = 0; c < NC; ++c) Cs[(ty * 8 + r) * (BN + 1) + tx + 32 * c] = __fadd_rn(acc[r][c], err[r][c]);
   __syncthreads();
-  if (tid < BM) {
+  // one thread per tile row, or EpiSimtShares of them sharing out its elements
+  constexpr int ES = EpiSimtShares<Epi>::value;
+  static_assert(ES * BM <= 128, "shares of a tile row");
+  if (tid < ES * BM) {
+    const int row = tid % BM;
     TileCoord t;
     t.step = 0;
+    t.part = tid / BM;
+    t.parts = ES;
     t.m0 = m0;
     t.n0 = n0;
     t.mt = mt;
@@ -877,8 +893,8 @@ __global__ void __launch_bounds__(128)
     t.peer_stride = 1;
     t.red = nullptr;
     t.red_full = t.red_done = nullptr;
-    SmemAcc a{Cs + tid * (BN + 1)};
-    epi(t, tid, a, BN);
+    SmemAcc a{Cs + row * (BN + 1)};
+    epi(t, row, a, BN);
   }
 }
 

@@ -86,6 +86,10 @@ struct EpiStore {
 // tile's block of u hidden units.
 template <int CELL, class S>
 struct EpiFwdStep {
+  // fp32 storage (the FFMA engine): the pointwise work, in double precision,
+  // is shared out over four threads per tile row, each taking every fourth
+  // element of a 16-unit chunk (TileCoord::part of TileCoord::parts)
+  static constexpr int kSimtShares = std::is_same<S, float>::value ? 4 : 1;
   int B, H, u;
   float* P;              // [B][G*H] this step: input projection incl. bias; activated gates written back if write_gates
   int write_gates;
@@ -116,6 +120,7 @@ struct EpiFwdStep {
     const int b = t.m0 + row;
     const int GH = G * H;
     const int jblk = (t.n0 / (G * u)) * u;
+    const int es = kSimtShares == 1 ? 1 : t.parts, e = kSimtShares == 1 ? 0 : t.part;
     for (int c = 0; c < u; c += 16) {
       float a[G][16];
 #pragma unroll
@@ -123,14 +128,14 @@ struct EpiFwdStep {
       if (b >= B) continue;
       const int j0 = jblk + c;
       float* prow = P + (size_t)b * GH + t.n0 + c;
-      float hnew[16];
+      float hnew[16] = {};
       if constexpr (CELL == LSTM) {
         float cp[16];
         if (c_prev) load16(c_prev + (size_t)b * H + j0, cp);
         else
 #pragma unroll
           for (int i = 0; i < 16; ++i) cp[i] = 0.f;
-        float p[16], cn[16];
+        float p[16], cn[16] = {};
         T av[4][16];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -140,6 +145,7 @@ struct EpiFwdStep {
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+          if ((i & (es - 1)) != e) continue;
           const T ig = Act<S>::sig(av[0][i]), fg = Act<S>::sig(av[1][i]), gg = Act<S>::th(av[2][i]),
                   og = Act<S>::sig(av[3][i]);
           const T cc = fg * T(cp[i]) + ig * gg;
@@ -147,10 +153,10 @@ struct EpiFwdStep {
           hnew[i] = float(og * Act<S>::th(cc));
           a[0][i] = float(ig); a[1][i] = float(fg); a[2][i] = float(gg); a[3][i] = float(og);
         }
-        store16(c_out + (size_t)b * H + j0, cn);
-        if (cT) store16(cT + (size_t)b * H + j0, cn);
+        store16_share(c_out + (size_t)b * H + j0, cn, e, es);
+        if (cT) store16_share(cT + (size_t)b * H + j0, cn, e, es);
       } else if constexpr (CELL == GRU) {
-        float hp[16], p[16], bn[16], hn[16];
+        float hp[16], p[16], bn[16], hn[16] = {};
         if (h_prev) load16(h_prev + (size_t)b * H + j0, hp);
         else
 #pragma unroll
@@ -165,6 +171,7 @@ struct EpiFwdStep {
         load16(prow + 2 * u, p);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+          if ((i & (es - 1)) != e) continue;
           const T r = Act<S>::sig(T(a[0][i])), z = Act<S>::sig(T(a[1][i]));
           const T hnv = T(a[2][i]) + T(bn[i]);
           hn[i] = float(hnv);
@@ -172,23 +179,24 @@ struct EpiFwdStep {
           hnew[i] = float((T(1) - z) * n + z * T(hp[i]));
           a[0][i] = float(r); a[1][i] = float(z); a[2][i] = float(n);
         }
-        if (hn_out) store16(hn_out + (size_t)b * H + j0, hn);
+        if (hn_out) store16_share(hn_out + (size_t)b * H + j0, hn, e, es);
       } else {
         float p[16];
         load16(prow, p);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+          if ((i & (es - 1)) != e) continue;
           hnew[i] = float(simple_act<CELL, S>(T(a[0][i]) + T(p[i])));
           a[0][i] = hnew[i];
         }
       }
       if (write_gates) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) store16(prow + g * u, a[g]);
+        for (int g = 0; g < G; ++g) store16_share(prow + g * u, a[g], e, es);
       }
-      store16(h_out + (size_t)b * H + j0, hnew);
-      if (y) store16(y + (size_t)b * H + j0, hnew);
-      if (hT) store16(hT + (size_t)b * H + j0, hnew);
+      store16_share(h_out + (size_t)b * H + j0, hnew, e, es);
+      if (y) store16_share(y + (size_t)b * H + j0, hnew, e, es);
+      if (hT) store16_share(hT + (size_t)b * H + j0, hnew, e, es);
     }
   }
 };
