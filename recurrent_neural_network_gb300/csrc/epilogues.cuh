@@ -219,7 +219,9 @@ struct BwdPoint {
   S* dGx;               // [B][G*H]
   S* dGh;               // [B][G*H] (GRU; LSTM/RNN write only dGx)
 
-  __device__ __forceinline__ void run(int b, int j0, float* dh32) const {
+  // e, es: this thread's share of the 16 elements (every es-th from e; es a
+  // power of two), as the forward step's FFMA epilogue shares them out
+  __device__ __forceinline__ void run(int b, int j0, float* dh32, int e = 0, int es = 1) const {
     constexpr int G = CellInfo<CELL>::G;
     using T = typename Prec<S>::T;  // pointwise precision
     const int GH = G * H;
@@ -249,9 +251,10 @@ struct BwdPoint {
 #pragma unroll
         for (int i = 0; i < 16; ++i) cp[i] = 0.f;
       load16(carry + bj, dc);
-      float d0[16], d1[16], d2[16], d3[16];
+      float d0[16] = {}, d1[16] = {}, d2[16] = {}, d3[16] = {};
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
+        if ((i & (es - 1)) != e) continue;
         const T igv = ig[i], fgv = fg[i], ggv = gg[i], ogv = og[i];
         const T tau = Act<S>::th(T(cs[i]));
         const T dov = dh[i] * tau;
@@ -262,11 +265,11 @@ struct BwdPoint {
         d3[i] = float(dov * ogv * (T(1) - ogv));
         dc[i] = float(dcv * fgv);
       }
-      store16(gx, d0);
-      store16(gx + u, d1);
-      store16(gx + 2 * u, d2);
-      store16(gx + 3 * u, d3);
-      store16(carry + bj, dc);
+      store16_share(gx, d0, e, es);
+      store16_share(gx + u, d1, e, es);
+      store16_share(gx + 2 * u, d2, e, es);
+      store16_share(gx + 3 * u, d3, e, es);
+      store16_share(carry + bj, dc, e, es);
     } else if constexpr (CELL == GRU) {
       float r[16], z[16], n[16], hn[16], hp[16], cz[16];
       load16(grow, r);
@@ -278,9 +281,10 @@ struct BwdPoint {
 #pragma unroll
         for (int i = 0; i < 16; ++i) hp[i] = 0.f;
       load16(carry + bj, cz);
-      float dar[16], daz[16], dan[16], dhn[16];
+      float dar[16] = {}, daz[16] = {}, dan[16] = {}, dhn[16] = {};
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
+        if ((i & (es - 1)) != e) continue;
         const T rv = r[i], zv = z[i], nv = n[i];
         const T d = dh[i] + T(cz[i]);
         const T dn = d * (T(1) - zv);
@@ -294,19 +298,20 @@ struct BwdPoint {
         cz[i] = float(d * zv);
       }
       S* gh = dGh + (size_t)b * GH + p0;
-      store16(gx, dar);
-      store16(gx + u, daz);
-      store16(gx + 2 * u, dan);
-      store16(gh, dar);
-      store16(gh + u, daz);
-      store16(gh + 2 * u, dhn);
-      store16(carry + bj, cz);
+      store16_share(gx, dar, e, es);
+      store16_share(gx + u, daz, e, es);
+      store16_share(gx + 2 * u, dan, e, es);
+      store16_share(gh, dar, e, es);
+      store16_share(gh + u, daz, e, es);
+      store16_share(gh + 2 * u, dhn, e, es);
+      store16_share(carry + bj, cz, e, es);
     } else {
-      float hv[16], da[16];
+      float hv[16], da[16] = {};
       load16(grow, hv);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) da[i] = float(dh[i] * simple_slope<CELL>(T(hv[i])));
-      store16(gx, da);
+      for (int i = 0; i < 16; ++i)
+        if ((i & (es - 1)) == e) da[i] = float(dh[i] * simple_slope<CELL>(T(hv[i])));
+      store16_share(gx, da, e, es);
     }
   }
 };
@@ -317,6 +322,9 @@ struct BwdPoint {
 // running a pointwise step.
 template <int CELL, class S>
 struct EpiBwdStep {
+  // fp32 storage (the FFMA engine): four threads per tile row share out the
+  // double-precision pointwise work, every fourth element each
+  static constexpr int kSimtShares = std::is_same<S, float>::value ? 4 : 1;
   BwdPoint<CELL, S> pt;
   int final_;
   S* dh0;        // [B][H] (final)
@@ -326,10 +334,10 @@ struct EpiBwdStep {
   int* err;      // device error word (cluster reduction waits)
   uint64_t limit_ns;
 
-  __device__ __forceinline__ void finish(int b, int j0, float* dh) const {
+  __device__ __forceinline__ void finish(int b, int j0, float* dh, int e = 0, int es = 1) const {
     const int H = pt.H;
     if (!final_) {
-      pt.run(b, j0, dh);
+      pt.run(b, j0, dh, e, es);
       return;
     }
     const size_t bj = (size_t)b * H + j0;
@@ -339,11 +347,11 @@ struct EpiBwdStep {
 #pragma unroll
       for (int i = 0; i < 16; ++i) dh[i] += cz[i];
     }
-    if (dh0) store16(dh0 + bj, dh);
+    if (dh0) store16_share(dh0 + bj, dh, e, es);
     if (CELL == LSTM && dc0) {
       float dc[16];
       load16(pt.carry + bj, dc);
-      store16(dc0 + bj, dc);
+      store16_share(dc0 + bj, dc, e, es);
     }
   }
 
@@ -463,11 +471,13 @@ struct EpiBwdStep {
       }
       return;
     }
+    // (the FFMA engine's shares of a row; one share in the tensor-core engines)
+    const int es = kSimtShares == 1 ? 1 : t.parts, e = kSimtShares == 1 ? 0 : t.part;
     for (int c = 0; c < bn; c += 16) {
       float v[16];
       acc.load16(c, v);
       const int j0 = t.n0 + c;
-      if (b < B && j0 < H) finish(b, j0, v);
+      if (b < B && j0 < H) finish(b, j0, v, e, es);
     }
   }
 };
