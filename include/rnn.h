@@ -77,7 +77,7 @@ typedef enum { RNN_MODE_FP32 = 0, RNN_MODE_BF16 = 1 } rnn_mode_t;
 enum {
   RNN_OK = 0,
   RNN_ERR_INVALID_ARG = -1, /* null handle/pointer, bad size, misaligned buffer */
-  RNN_ERR_UNSUPPORTED = -2, /* shape or mode this build does not handle */
+  RNN_ERR_UNSUPPORTED = -2, /* shape or mode the library does not handle */
   RNN_ERR_LAUNCH = -3,      /* kernel could not be launched (e.g. co-residency) */
   RNN_ERR_CUDA = -4,        /* a CUDA runtime call failed */
   RNN_ERR_TIMEOUT = -5,     /* a bounded device-side wait gave up */
