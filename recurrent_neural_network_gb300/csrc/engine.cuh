@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       {
         // let the epilogue's own global inputs travel to L2 (or on-chip) while the MMAs run
         TileCoord tp;
+        tp.step = 0;
         tp.m0 = mt * BM;
         tp.n0 = nt * BN;
         tp.mt = mt;
@@ -429,6 +430,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, 1)
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      // every epilogue warp takes the same decision: a warp that gave up just
+      // before the accumulator completed must not leave the others waiting at
+      // the epilogue's named barriers
+      ok = tc::bar_and(1, 32 * EpiWarps<Epi>::value, ok);
       if (!ok) break;
       tc::fence_after_sync();
       TileCoord t;
@@ -749,6 +754,10 @@ __global__ void __launch_bounds__(64 + 32 * EpiWarps<Epi>::value, ACCS == 1 ? 2 
       int ok = 1;
       if (lane == 0) ok = tc::mbar_wait(tfull + acc, aphase, abort_flag, g.err, g.limit_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      // every epilogue warp takes the same decision: a warp that gave up just
+      // before the accumulator completed must not leave the others waiting at
+      // the epilogue's named barriers
+      ok = tc::bar_and(1, 32 * EpiWarps<Epi>::value, ok);
       if (!ok) break;
       tc::fence_after_sync();
       TmemAcc a{tmem_base + acc * BN + lane_q};

@@ -187,6 +187,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.p
 // the same for global memory
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 // named barrier over `threads` threads of the CTA
+// Named barrier that also ANDs a flag over the participating threads.
+__device__ __forceinline__ int bar_and(int id, int threads, int v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(v), "r"(id), "r"(threads)
+      : "memory");
+  return r;
+}
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
