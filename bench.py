@@ -173,8 +173,8 @@ def class_bytes(wl, transposed, fused_point=False):
 # ncu capture of the same kernel build on `bench.py --ncu-steps` (one layer,
 # T=2, the same per-step shape; transposed steps, BPTT pointwise fused into the
 # product): the first launch of each class.
-NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.12e6,
-               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.51e6}
+NCU_TRAFFIC = {("lstm_bf16_L4_T50_B256_H4096", "bwd_step"): 177.24e6,
+               ("lstm_bf16_L4_T50_B256_H4096", "fwd_step"): 162.46e6}
 
 
 def oracle_sample(wl, B1, T1):
