@@ -881,15 +881,21 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int c = 0; c < NC; ++c) Cs[(ty * 8 + r) * (BN + 1) + tx + 32 * c] = __fadd_rn(acc[r][c], err[r][c]);
   __syncthreads();
-  // one thread per tile row, or EpiSimtShares of them sharing out its elements
+  // one thread per tile row, or EpiSimtShares of them sharing out its
+  // elements; with few rows in the tile (a small batch) the shares double
+  // while the block has threads for them, up to 32 per row
   constexpr int ES = EpiSimtShares<Epi>::value;
   static_assert(ES * BM <= 128, "shares of a tile row");
-  if (tid < ES * BM) {
-    const int row = tid % BM;
+  const int nrow = ES > 1 ? max(1, min(BM, g.M - m0)) : BM;
+  int es = ES;
+  if (ES > 1)
+    while (es < 32 && 2 * es * nrow <= 128) es *= 2;
+  if (tid < es * nrow) {
+    const int row = tid % nrow;
     TileCoord t;
     t.step = 0;
-    t.part = tid / BM;
-    t.parts = ES;
+    t.part = tid / nrow;
+    t.parts = es;
     t.m0 = m0;
     t.n0 = n0;
     t.mt = mt;

@@ -87,8 +87,9 @@ struct EpiStore {
 template <int CELL, class S>
 struct EpiFwdStep {
   // fp32 storage (the FFMA engine): the pointwise work, in double precision,
-  // is shared out over four threads per tile row, each taking every fourth
-  // element of a 16-unit chunk (TileCoord::part of TileCoord::parts)
+  // is shared out over at least four threads per tile row, each taking every
+  // fourth element of a 16-unit chunk (TileCoord::part of TileCoord::parts;
+  // more shares where the tile has few rows)
   static constexpr int kSimtShares = std::is_same<S, float>::value ? 4 : 1;
   int B, H, u;
   float* P;              // [B][G*H] this step: input projection incl. bias; activated gates written back if write_gates
@@ -120,8 +121,11 @@ struct EpiFwdStep {
     const int b = t.m0 + row;
     const int GH = G * H;
     const int jblk = (t.n0 / (G * u)) * u;
-    const int es = kSimtShares == 1 ? 1 : t.parts, e = kSimtShares == 1 ? 0 : t.part;
-    for (int c = 0; c < u; c += 16) {
+    // this thread's share: every es-th element of a chunk from e; beyond 16
+    // shares the chunks are shared out too (cs threads per element)
+    const int sh = kSimtShares == 1 ? 1 : t.parts, s = kSimtShares == 1 ? 0 : t.part;
+    const int es = sh > 16 ? 16 : sh, e = s & (es - 1), cs = sh / es, c0 = (s / es) * 16;
+    for (int c = c0; c < u; c += 16 * cs) {
       float a[G][16];
 #pragma unroll
       for (int g = 0; g < G; ++g) acc.load16(g * u + c, a[g]);
@@ -322,8 +326,8 @@ struct BwdPoint {
 // running a pointwise step.
 template <int CELL, class S>
 struct EpiBwdStep {
-  // fp32 storage (the FFMA engine): four threads per tile row share out the
-  // double-precision pointwise work, every fourth element each
+  // fp32 storage (the FFMA engine): at least four threads per tile row share
+  // out the double-precision pointwise work (more where the tile has few rows)
   static constexpr int kSimtShares = std::is_same<S, float>::value ? 4 : 1;
   BwdPoint<CELL, S> pt;
   int final_;
@@ -472,8 +476,9 @@ struct EpiBwdStep {
       return;
     }
     // (the FFMA engine's shares of a row; one share in the tensor-core engines)
-    const int es = kSimtShares == 1 ? 1 : t.parts, e = kSimtShares == 1 ? 0 : t.part;
-    for (int c = 0; c < bn; c += 16) {
+    const int sh = kSimtShares == 1 ? 1 : t.parts, s = kSimtShares == 1 ? 0 : t.part;
+    const int es = sh > 16 ? 16 : sh, e = s & (es - 1), cs = sh / es, c0 = (s / es) * 16;
+    for (int c = c0; c < bn; c += 16 * cs) {
       float v[16];
       acc.load16(c, v);
       const int j0 = t.n0 + c;
